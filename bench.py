@@ -1,0 +1,421 @@
+"""Benchmark: conv GFLOP/s and fraction of the GB300 roofline, one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME] [--no-extra]
+
+A step is one forward convolution over the whole batch of the headline
+workload (Conv3d, x [16,3,64,64,64], kernel (3,5,7), 64 output channels,
+bias), through the C ABI (conv_fwd_nd), with inputs already resident in HBM.
+L2 is flushed (a 2x-L2 buffer is written) before every step, outside the
+per-step CUDA events.  The line also carries:
+  e2e          the same metric with the step's inputs copied host->device from
+               pinned memory and the output copied back, inside the timing;
+  roofline     the dominant kernel's achieved rate against the measured peak;
+  cpu_baseline the fp64 oracle timed on a bounded sample on the host cores;
+  per_config   the other workloads (fused conv3d+min+softmax, long Conv1d,
+               the two sweep shapes, the tiny Conv1d), each timed the same way.
+With --impl reference the oracle itself is the measured implementation.
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the problem shards by batch with no exchange); value sums all ranks' work
+over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+HEADLINE = "conv3d_asym"
+EXTRA = ["conv3d_min_softmax", "conv1d_long", "conv3d_sweep_a", "conv3d_sweep_b", "conv1d_tiny"]
+METRIC = "conv GFLOP/s and % of GB300 roofline (fp32/TF32 or HBM) per config, 1 GPU"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+SM_COUNT_NOMINAL, FP32_LANES_PER_SM, SM_MAX_MHZ_NOMINAL = 152, 128, 2070.0
+BF16_TO_TF32 = 1.1 / 2.25  # nominal dense tensor-core ratio TF32 : BF16
+CPU_BASELINE_MACS = 8e9     # ~10-20 s of the oracle on the host cores
+REFERENCE_STEP_MACS = 1e9   # one reference-arm step: a ~1-2 s slab of the workload
+
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+                "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
+
+
+def problem_counts(wl, out_dims):
+    """Algorithmic FLOPs (2 per MAC, padded taps included) and compulsory bytes."""
+    out_sp = int(np.prod(out_dims))
+    k_sp = int(np.prod(wl.k_dims))
+    flops = 2.0 * wl.N * wl.C_out * out_sp * wl.C_in * k_sp
+    x_b = 4.0 * wl.N * wl.C_in * int(np.prod(wl.in_dims))
+    w_b = 4.0 * wl.C_out * wl.C_in * k_sp
+    b_b = 4.0 * wl.C_out if wl.bias else 0.0
+    if wl.kind == "fused":
+        y_b = 4.0 * wl.N * wl.C_out * out_dims[1] * out_dims[2]
+    else:
+        y_b = 4.0 * wl.N * wl.C_out * out_sp
+    return flops, x_b + w_b + b_b + y_b, x_b + w_b + b_b, y_b
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle sampling in the background during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"convfwd_clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, r in rows:
+            for nm, v in zip(names, r[1:5]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        mhz = [r[0] for r in rows]
+        loaded = [m for m in mhz if m > 0.5 * max(mhz)] or mhz
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# --------------------------------------------------------------- our arm
+
+class OurRunner:
+    def __init__(self, wl, device):
+        import torch
+        import implicit_gemm_convolution_fwd_gb300 as cf
+        self.torch, self.cf, self.wl, self.dev = torch, cf, wl, device
+        x, w, b = wl.make_inputs(seed=0)
+        self.host = {"x": x, "w": w, "b": b}
+        self.x = torch.from_numpy(x).to(device)
+        self.w = torch.from_numpy(w).to(device)
+        self.b = None if b is None else torch.from_numpy(b).to(device)
+        if wl.kind == "fused":
+            self.out_dims = (x.shape[2] - w.shape[2] + 1, x.shape[3] - w.shape[3] + 1, x.shape[4] - w.shape[4] + 1)
+            self.y = torch.empty((wl.N, wl.C_out, self.out_dims[1], self.out_dims[2]), device=device)
+            self.algo = "fused_ffma"
+        else:
+            self.out_dims = cf.out_dims(wl.in_dims, wl.k_dims, wl.stride, wl.pad, wl.dilation)
+            self.y = torch.empty((wl.N, wl.C_out) + tuple(self.out_dims), device=device)
+            self.algo = cf.ALGO_NAMES[cf.select_algo(wl.N, wl.C_in, wl.C_out, wl.in_dims, wl.k_dims, wl.stride,
+                                                     wl.pad, wl.dilation)]
+        self.stream = torch.cuda.current_stream(device)
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.flush_buf = torch.empty(int(2 * l2 // 4) + 1024, dtype=torch.float32, device=device)
+
+    def launches_per_step(self):
+        return 1
+
+    def step(self):
+        if self.wl.kind == "fused":
+            self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.wl.min_dim, out=self.y, stream=self.stream)
+        else:
+            self.cf.conv_fwd_nd(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation, out=self.y,
+                                stream=self.stream)
+
+    def flush(self):
+        self.flush_buf.fill_(1.0)
+
+    def timed(self, steps, warmup, flush=True):
+        """Per-step device times (ms) with CUDA events on the launching stream."""
+        torch = self.torch
+        for _ in range(warmup):
+            if flush:
+                self.flush()
+            self.step()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for s, e in evs:
+            if flush:
+                self.flush()
+            s.record(self.stream)
+            self.step()
+            e.record(self.stream)
+        torch.cuda.synchronize()
+        return [s.elapsed_time(e) for s, e in evs]
+
+    def timed_e2e(self, steps, warmup):
+        """Same call with H2D of the step's inputs (pinned) and D2H of its output inside the timing."""
+        torch = self.torch
+        hx = torch.from_numpy(self.host["x"]).pin_memory()
+        hw = torch.from_numpy(self.host["w"]).pin_memory()
+        hb = None if self.host["b"] is None else torch.from_numpy(self.host["b"]).pin_memory()
+        hy = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
+
+        def one():
+            self.x.copy_(hx, non_blocking=True)
+            self.w.copy_(hw, non_blocking=True)
+            if hb is not None:
+                self.b.copy_(hb, non_blocking=True)
+            self.step()
+            hy.copy_(self.y, non_blocking=True)
+
+        for _ in range(warmup):
+            one()
+        torch.cuda.synchronize()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(self.stream)
+        for _ in range(steps):
+            one()
+        e.record(self.stream)
+        torch.cuda.synchronize()
+        h2d = hx.numel() * 4 + hw.numel() * 4 + (0 if hb is None else hb.numel() * 4)
+        return s.elapsed_time(e) / steps, h2d, hy.numel() * 4
+
+
+def roofline_for(runner, peaks, ms, sustained=False):
+    """Roofline entry for the one kernel a step launches."""
+    wl = runner.wl
+    flops, bytes_alg, _, _ = problem_counts(wl, runner.out_dims)
+    t = ms * 1e-3
+    hbm_peak = peaks["hbm_gbs"]
+    if runner.algo == "igemm_3xtf32":
+        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        peak = bf16 * BF16_TO_TF32 / 3.0  # three TF32 products per fp32 MAC
+        compute = {"bound": "tensor", "peak": peak, "peak_note": "TF32 = measured bf16 x 1.1/2.25, /3 for 3xTF32"}
+    else:
+        peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12
+        compute = {"bound": "alu", "peak": peak, "peak_note": "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"}
+    t_compute = flops / (compute["peak"] * 1e12)
+    t_mem = bytes_alg / (hbm_peak * 1e9)
+    if t_mem > t_compute:
+        return {"bound": "hbm", "achieved": bytes_alg / t / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "frac": (bytes_alg / t / 1e9) / hbm_peak, "traffic": None,
+                "compute_frac": (flops / t / 1e12) / compute["peak"]}
+    ach = flops / t / 1e12
+    return {"bound": compute["bound"], "achieved": ach, "peak": compute["peak"], "unit": "TFLOP/s",
+            "frac": ach / compute["peak"], "traffic": None, "peak_note": compute["peak_note"],
+            "hbm_frac": (bytes_alg / t / 1e9) / hbm_peak}
+
+
+# ----------------------------------------------------------- oracle legs
+
+def oracle_sample(wl, target_macs):
+    """A bounded sample of workload `wl` for the oracle: the leading batch items
+    and, for long inputs, a leading slab of the outermost spatial dim of x,
+    sized to about `target_macs` multiply-adds."""
+    k_sp = int(np.prod(wl.k_dims))
+    if wl.kind == "fused":
+        od = [wl.in_dims[i] - wl.k_dims[i] + 1 for i in range(3)]
+    else:
+        import oracle
+        od = list(oracle.out_dims(wl.in_dims, wl.k_dims, wl.stride, wl.pad, wl.dilation))
+    per_item = wl.C_out * int(np.prod(od)) * wl.C_in * k_sp
+    n = int(min(wl.N, max(1, target_macs // per_item)))
+    x, w, b = wl.with_batch(n).make_inputs(seed=0)
+    if n == 1 and per_item > 2 * target_macs:
+        # keep enough of the outermost spatial dim for ~target_macs
+        frac = target_macs / per_item
+        keep_out = max(1, int(od[0] * frac))
+        s0, d0, k0 = wl.stride[0], wl.dilation[0], wl.k_dims[0]
+        keep_in = min(wl.in_dims[0], (keep_out - 1) * s0 + (k0 - 1) * d0 + 1)
+        x = np.ascontiguousarray(x[:, :, :keep_in])
+    return x, w, b
+
+
+def time_oracle(wl, target_macs):
+    import oracle
+    x, w, b = oracle_sample(wl, target_macs)
+    threads = oracle.threads()
+    t0 = time.perf_counter()
+    if wl.kind == "fused":
+        y = oracle.conv3d_min_softmax(x, w, b, nthreads=threads)
+        od = (x.shape[2] - w.shape[2] + 1,) + tuple(y.shape[2:])
+    else:
+        y = oracle.conv_nd(x, w, b, wl.stride, wl.pad, wl.dilation, nthreads=threads)
+        od = y.shape[2:]
+    dt = time.perf_counter() - t0
+    macs = float(x.shape[0]) * wl.C_out * int(np.prod(od)) * wl.C_in * int(np.prod(wl.k_dims))
+    sample = (f"{wl.name}: first {x.shape[0]} of {wl.N} batch items, x spatial {list(x.shape[2:])} "
+              f"({macs:.3g} MACs, fp64 accumulation, {threads} threads)")
+    return 2.0 * macs / dt / 1e9, dt, threads, sample
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank, world, local = env_rank()
+    wl = synth.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return main_reference(args, wl, rank, world)
+
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    peaks, peaks_src = load_peaks()
+
+    runner = OurRunner(wl, dev)
+    flops, bytes_alg, in_b, out_b = problem_counts(wl, runner.out_dims)
+    # warm-up, then EXACTLY K timed steps bracketed by barrier + synchronize
+    runner.timed(0, args.warmup)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        per_step = runner.timed(args.steps, 0)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        dist.barrier()
+    ms = sum(per_step) / len(per_step)
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * flops / (ms * 1e-3) / 1e9
+
+    e2e_ms, h2d, d2h = runner.timed_e2e(max(3, args.steps // 4), 2)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    roof = roofline_for(runner, peaks, ms)
+    roof["peak_source"] = peaks_src
+    roof["kernel"] = runner.algo
+    clocks = clk.summary()
+
+    per_config = {}
+    if not args.no_extra and rank == 0:
+        del runner.flush_buf
+        for name in EXTRA:
+            if name == wl.name:
+                continue
+            r = OurRunner(synth.WORKLOADS[name], dev)
+            times = r.timed(max(5, args.steps // 2), 3)
+            m = statistics.median(times)
+            f, bts, _, _ = problem_counts(r.wl, r.out_dims)
+            rf = roofline_for(r, peaks, m)
+            per_config[name] = {"algo": r.algo, "ms": m, "ms_min": min(times), "gflops": f / (m * 1e-3) / 1e9,
+                                "gbs": bts / (m * 1e-3) / 1e9, "roofline_bound": rf["bound"],
+                                "roofline_frac": rf["frac"], "roofline_peak": rf["peak"], "unit": rf["unit"]}
+            del r
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        v, dt, threads, sample = time_oracle(wl, CPU_BASELINE_MACS)
+        cpu = {"value": v, "unit": "GFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
+               "seconds": dt}
+
+    if world > 1:
+        dist.barrier()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
+            "config": {"workload": wl.name, "description": wl.description, "global_batch": wl.N * world,
+                       "in_dims": list(wl.in_dims), "k_dims": list(wl.k_dims), "C_in": wl.C_in, "C_out": wl.C_out,
+                       "stride": list(wl.stride), "pad": list(wl.pad), "dilation": list(wl.dilation),
+                       "bias": wl.bias, "parallelism": f"replicas{world}",
+                       "l2": "flushed before every step (2x L2 write, outside the per-step events)",
+                       "kernel": runner.algo, "gflop_per_step": flops / 1e9, "bytes_per_step": bytes_alg,
+                       "gbs": bytes_alg / (ms * 1e-3) / 1e9, "ms_min": min(per_step),
+                       "ms_median": statistics.median(per_step), "wall_s": wall},
+            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": e2e_ms,
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "gpu_launches": runner.launches_per_step() * args.steps,
+            "roofline": roof, "clocks": clocks, "cpu_baseline": cpu, "per_config": per_config,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def main_reference(args, wl, rank, world):
+    """The oracle as the measured implementation, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        time_oracle(wl, REFERENCE_STEP_MACS)
+    t0 = time.perf_counter()
+    runs = [time_oracle(wl, REFERENCE_STEP_MACS) for _ in range(args.steps)]
+    wall = time.perf_counter() - t0
+    mean_dt = sum(r[1] for r in runs) / len(runs)
+    v = statistics.mean(r[0] for r in runs)
+    threads, sample = runs[0][2], runs[0][3]
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "GFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": wl.name, "description": wl.description, "global_batch": wl.N,
+                   "parallelism": "host cores", "wall_s": wall, "step": sample},
+        "cpu_baseline": {"value": v, "unit": "GFLOP/s", "cores": threads, "kind": "oracle", "sample": sample},
+        "e2e": {"value": v, "unit": "GFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,182 @@
+"""Thin Python binding over the C ABI in ``include/convfwd.h``.
+
+Argument marshalling only: every step of the convolution runs in the CUDA
+library ``libconvfwd.so`` (built in-tree by ``build_lib.py``).  PyTorch is
+used for device memory and streams.  There is no CPU fallback: if the library
+is missing or a call fails, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libconvfwd.so")
+
+CONV_OK, CONV_ERR_NULL, CONV_ERR_ARG, CONV_ERR_SHAPE, CONV_ERR_UNSUPPORTED, CONV_ERR_CUDA = range(6)
+CONV_ALGO_AUTO, CONV_ALGO_DIRECT_FFMA, CONV_ALGO_IGEMM_3XTF32 = 0, 1, 2
+ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV_ALGO_IGEMM_3XTF32: "igemm_3xtf32"}
+
+# every symbol include/convfwd.h declares
+EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
+            "conv3d_min_softmax",
+            "conv_status_string", "conv_last_error", "conv_device_status")
+
+
+class ConvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{message} (status {status})")
+        self.status = status
+
+
+class Tensor5(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dims", ctypes.c_int64 * 5)]
+
+
+class Tensor4(ctypes.Structure):
+    _fields_ = [("data", ctypes.c_void_p), ("dims", ctypes.c_int64 * 4)]
+
+
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load (once) and return the ctypes handle of libconvfwd.so; raises if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing (run build_lib.build())")
+    lib = ctypes.CDLL(path)
+    vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    arr = ctypes.POINTER(ctypes.c_int64)
+    lib.conv_out_dims.argtypes = [i32, arr, arr, arr, arr, arr, arr]
+    lib.conv_fwd_nd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, arr, arr, arr, arr, arr, vp]
+    lib.conv_fwd_nd_ex.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, arr, arr, arr, arr, arr, i32, vp]
+    lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
+    lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
+    lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
+                                       ctypes.POINTER(Tensor4), i32, vp]
+    lib.conv_status_string.argtypes = [i32]
+    lib.conv_status_string.restype = ctypes.c_char_p
+    lib.conv_last_error.argtypes = []
+    lib.conv_last_error.restype = ctypes.c_char_p
+    lib.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    for f in ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
+              "conv3d_min_softmax",
+              "conv_device_status"):
+        getattr(lib, f).restype = i32
+    _lib = lib
+    return lib
+
+
+def _arr(vals):
+    vals = [int(v) for v in vals]
+    return (ctypes.c_int64 * max(1, len(vals)))(*vals)
+
+
+def _check(status: int):
+    if status != CONV_OK:
+        lib = load()
+        raise ConvError(status, lib.conv_last_error().decode() or lib.conv_status_string(status).decode())
+
+
+def _tuple(v, nd):
+    if isinstance(v, int):
+        return (v,) * nd
+    v = tuple(int(a) for a in v)
+    if len(v) != nd:
+        raise ValueError(f"expected {nd} values, got {v}")
+    return v
+
+
+def out_dims(in_dims, k_dims, stride, pad, dilation):
+    """Output spatial dims via the library's conv_out_dims (raises ConvError on invalid input)."""
+    nd = len(in_dims)
+    out = (ctypes.c_int64 * nd)()
+    _check(load().conv_out_dims(nd, _arr(in_dims), _arr(k_dims), _arr(_tuple(stride, nd)),
+                                _arr(_tuple(pad, nd)), _arr(_tuple(dilation, nd)), out))
+    return tuple(out)
+
+
+def select_algo(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1) -> int:
+    nd = len(in_dims)
+    a = ctypes.c_int(-1)
+    _check(load().conv_select_algo(nd, N, C_in, C_out, _arr(in_dims), _arr(k_dims), _arr(_tuple(stride, nd)),
+                                   _arr(_tuple(pad, nd)), _arr(_tuple(dilation, nd)), ctypes.byref(a)))
+    return a.value
+
+
+def algo_supported(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1, algo=CONV_ALGO_AUTO) -> bool:
+    """Host-only query: can kernel family `algo` run this problem?  Raises ConvError if it is invalid."""
+    nd = len(in_dims)
+    st = load().conv_algo_supported(nd, N, C_in, C_out, _arr(in_dims), _arr(k_dims), _arr(_tuple(stride, nd)),
+                                    _arr(_tuple(pad, nd)), _arr(_tuple(dilation, nd)), int(algo))
+    if st == CONV_ERR_UNSUPPORTED:
+        return False
+    _check(st)
+    return True
+
+
+def _stream_handle(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CONV_ALGO_AUTO, stream=None):
+    """y = conv(x, w) + bias for contiguous fp32 CUDA tensors x [N,C_in,*in], w [C_out,C_in,*k]."""
+    import torch
+    nd = x.dim() - 2
+    if nd not in (1, 2, 3) or w.dim() != x.dim():
+        raise ValueError("x and w must be 3-D, 4-D or 5-D tensors of the same rank")
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous float32 CUDA tensors")
+    s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[0]
+    if w.shape[1] != C_in:
+        raise ValueError("w.shape[1] must equal x.shape[1] (groups = 1)")
+    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    if out is None:
+        out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
+    elif tuple(out.shape) != (N, C_out) + od or not out.is_contiguous():
+        raise ValueError("out has the wrong shape or is not contiguous")
+    lib = load()
+    st = lib.conv_fwd_nd_ex(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
+                            nd, N, C_in, C_out, _arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d),
+                            int(algo), _stream_handle(stream))
+    _check(st)
+    return out
+
+
+def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None):
+    """softmax_o(min_d(conv3d(x, w) + bias)) for contiguous fp32 CUDA tensors (stride 1, no padding)."""
+    import torch
+    if x.dim() != 5 or w.dim() != 5:
+        raise ValueError("x and w must be 5-D")
+    N, C_out = x.shape[0], w.shape[0]
+    od = [x.shape[2 + i] - w.shape[2 + i] + 1 for i in range(3)]
+    if min_dim in (2, 3, 4):
+        keep = [od[i] for i in range(3) if i != min_dim - 2]
+    else:
+        keep = od[1:]
+    if out is None:
+        out = torch.empty((N, C_out, max(keep[0], 1), max(keep[1], 1)), device=x.device, dtype=torch.float32)
+    xd = Tensor5(x.data_ptr(), (ctypes.c_int64 * 5)(*x.shape))
+    wd = Tensor5(w.data_ptr(), (ctypes.c_int64 * 5)(*w.shape))
+    yd = Tensor4(out.data_ptr(), (ctypes.c_int64 * 4)(*out.shape))
+    st = load().conv3d_min_softmax(ctypes.byref(xd), ctypes.byref(wd), None if bias is None else bias.data_ptr(),
+                                   ctypes.byref(yd), int(min_dim), _stream_handle(stream))
+    _check(st)
+    return out
+
+
+def device_status() -> int:
+    """Synchronise and read/clear the device-side watchdog word (0 = no kernel gave up a wait)."""
+    v = ctypes.c_uint(0)
+    _check(load().conv_device_status(ctypes.byref(v)))
+    return v.value

@@ -1,0 +1,279 @@
+// C ABI entry points: argument validation, output-size arithmetic, kernel
+// family selection and dispatch.  Nothing here touches tensor data on the host.
+#include <stdio.h>
+#include <string.h>
+
+#include <cuda_runtime.h>
+
+#include "../../include/convfwd.h"
+#include "conv_internal.cuh"
+
+using convfwd::Geom;
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+int fail(int status, const char *fmt, const char *detail = nullptr, long long a = 0, long long b = 0) {
+  snprintf(g_last_error, sizeof(g_last_error), fmt, detail ? detail : "", a, b);
+  return status;
+}
+
+int fail_cuda(cudaError_t e, const char *where) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
+  return CONV_ERR_CUDA;
+}
+
+constexpr int64_t kMaxDim = 0x7fffffff;  // every size must fit a signed 32-bit int
+constexpr int64_t kMaxHyper = 1 << 20;   // kernel size, stride, pad, dilation cap
+
+// floor(a / b) for b > 0.
+int64_t floor_div(int64_t a, int64_t b) {
+  int64_t q = a / b;
+  if ((a % b != 0) && (a < 0)) q -= 1;
+  return q;
+}
+
+// a * b with overflow detection against `limit`.
+bool mul_ok(int64_t a, int64_t b, int64_t limit, int64_t *out) {
+  if (a < 0 || b < 0) return false;
+  if (a != 0 && b > limit / a) return false;
+  *out = a * b;
+  return true;
+}
+
+bool ranges_overlap(const void *a, int64_t abytes, const void *b, int64_t bbytes) {
+  if (!a || !b) return false;
+  uintptr_t a0 = (uintptr_t)a, a1 = a0 + (uintptr_t)abytes;
+  uintptr_t b0 = (uintptr_t)b, b1 = b0 + (uintptr_t)bbytes;
+  return a0 < b1 && b0 < a1;
+}
+
+// Hyper-parameter checks and output sizes (shared by every entry point).
+int compute_out_dims(int ndim, const int64_t *in, const int64_t *k, const int64_t *s, const int64_t *p,
+                     const int64_t *d, int64_t *out) {
+  if (!in || !k || !s || !p || !d || !out) return fail(CONV_ERR_NULL, "conv: NULL dimension array%s");
+  if (ndim < 1 || ndim > 3) return fail(CONV_ERR_ARG, "conv: ndim must be 1, 2 or 3%s");
+  bool nonpos = false;
+  for (int i = 0; i < ndim; ++i) {
+    if (in[i] < 1 || in[i] > kMaxDim) return fail(CONV_ERR_ARG, "conv: in_dims[%s%lld] out of range", "", i);
+    if (k[i] < 1 || k[i] > kMaxHyper) return fail(CONV_ERR_ARG, "conv: k_dims[%s%lld] out of range", "", i);
+    if (s[i] < 1 || s[i] > kMaxHyper) return fail(CONV_ERR_ARG, "conv: stride[%s%lld] out of range", "", i);
+    if (d[i] < 1 || d[i] > kMaxHyper) return fail(CONV_ERR_ARG, "conv: dilation[%s%lld] out of range", "", i);
+    if (p[i] < 0 || p[i] > kMaxHyper) return fail(CONV_ERR_ARG, "conv: pad[%s%lld] out of range", "", i);
+    // all terms are bounded well inside int64 by the caps above
+    out[i] = floor_div(in[i] + 2 * p[i] - d[i] * (k[i] - 1) - 1, s[i]) + 1;
+    if (out[i] < 1) nonpos = true;
+  }
+  if (nonpos) return fail(CONV_ERR_SHAPE, "conv: an output size is <= 0 (kernel extent exceeds padded input)%s");
+  return CONV_OK;
+}
+
+// Shape validation of a conv problem; fills the 3-D geometry and the element
+// counts of x, w and y.
+int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k,
+              const int64_t *s, const int64_t *p, const int64_t *d, Geom *g, int64_t *xe, int64_t *we,
+              int64_t *ye) {
+  int64_t out[3];
+  int st = compute_out_dims(ndim, in, k, s, p, d, out);
+  if (st != CONV_OK) return st;
+  if (N < 0 || N > kMaxDim || C_in < 1 || C_in > kMaxDim || C_out < 1 || C_out > kMaxDim)
+    return fail(CONV_ERR_ARG, "conv: N must be in [0, 2^31), C_in and C_out in [1, 2^31)%s");
+  const int64_t lim = INT64_MAX / 8;
+  int64_t in_sp = 1, out_sp = 1, k_sp = 1, t;
+  for (int i = 0; i < ndim; ++i) {
+    if (!mul_ok(in_sp, in[i], lim, &in_sp) || !mul_ok(out_sp, out[i], lim, &out_sp) ||
+        !mul_ok(k_sp, k[i], lim, &k_sp))
+      return fail(CONV_ERR_ARG, "conv: tensor size overflows int64%s");
+  }
+  if (!mul_ok(N, C_in, lim, &t) || !mul_ok(t, in_sp, lim, xe) || !mul_ok(C_out, C_in, lim, &t) ||
+      !mul_ok(t, k_sp, lim, we) || !mul_ok(N, C_out, lim, &t) || !mul_ok(t, out_sp, lim, ye))
+    return fail(CONV_ERR_ARG, "conv: tensor size overflows int64%s");
+  if (k_sp > kMaxDim || C_in * k_sp > kMaxDim)
+    return fail(CONV_ERR_ARG, "conv: reduction length C_in*prod(k) must fit in int32%s");
+  // Embed into 3-D with leading singleton dims.
+  const int off = 3 - ndim;
+  int gi[3] = {1, 1, 1}, go[3] = {1, 1, 1}, gk[3] = {1, 1, 1}, gs[3] = {1, 1, 1}, gp[3] = {0, 0, 0},
+      gd[3] = {1, 1, 1};
+  for (int i = 0; i < ndim; ++i) {
+    gi[off + i] = (int)in[i];
+    go[off + i] = (int)out[i];
+    gk[off + i] = (int)k[i];
+    gs[off + i] = (int)s[i];
+    gp[off + i] = (int)p[i];
+    gd[off + i] = (int)d[i];
+  }
+  g->N = N;
+  g->C = C_in;
+  g->K = C_out;
+  g->D = gi[0], g->H = gi[1], g->W = gi[2];
+  g->OD = go[0], g->OH = go[1], g->OW = go[2];
+  g->KD = gk[0], g->KH = gk[1], g->KW = gk[2];
+  g->SD = gs[0], g->SH = gs[1], g->SW = gs[2];
+  g->PD = gp[0], g->PH = gp[1], g->PW = gp[2];
+  g->DD = gd[0], g->DH = gd[1], g->DW = gd[2];
+  return CONV_OK;
+}
+
+// Full validation of a conv_fwd_nd call: shapes, then pointers.
+int validate_conv(const float *x, const float *w, const float *bias, const float *y, int ndim, int64_t N,
+                  int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s,
+                  const int64_t *p, const int64_t *d, Geom *g) {
+  int64_t xe, we, ye;
+  int st = make_geom(ndim, N, C_in, C_out, in, k, s, p, d, g, &xe, &we, &ye);
+  if (st != CONV_OK) return st;
+  // an empty batch has empty x and y, which may be NULL
+  if (!w || (N > 0 && (!x || !y))) return fail(CONV_ERR_NULL, "conv: x, w and y must be non-NULL%s");
+  if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)y | (uintptr_t)bias) & 3u)
+    return fail(CONV_ERR_ARG, "conv: x, w, bias, y must be 4-byte aligned%s");
+  if (ranges_overlap(y, ye * 4, x, xe * 4) || ranges_overlap(y, ye * 4, w, we * 4) ||
+      ranges_overlap(y, ye * 4, bias, C_out * 4))
+    return fail(CONV_ERR_ARG, "conv: y overlaps an input buffer%s");
+  return CONV_OK;
+}
+
+// Planner: the tensor-core path where the reduction is a real dense
+// contraction (K = C_in*taps and C_out large enough to fill an MMA tile), the
+// FFMA direct path otherwise.
+int choose_algo(const Geom &g) {
+  const int64_t red = g.C * (int64_t)g.taps();
+  const char *why = nullptr;
+  if (red >= 64 && g.K >= 16 && convfwd::igemm_supported(g, &why)) return CONV_ALGO_IGEMM_3XTF32;
+  return CONV_ALGO_DIRECT_FFMA;
+}
+
+// CONV_OK when kernel family `algo` can run geometry g, else the status to return.
+int check_algo(const Geom &g, int algo) {
+  const char *why = "";
+  switch (algo) {
+    case CONV_ALGO_DIRECT_FFMA:
+      if (!convfwd::direct_supported(g, &why)) return fail(CONV_ERR_UNSUPPORTED, "conv: %s", why);
+      return CONV_OK;
+    case CONV_ALGO_IGEMM_3XTF32:
+      if (!convfwd::igemm_supported(g, &why))
+        return fail(CONV_ERR_UNSUPPORTED, "conv: tensor-core path cannot run this shape: %s", why);
+      return CONV_OK;
+    default:
+      return fail(CONV_ERR_ARG, "conv: unknown algo %s%lld", "", algo);
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *conv_status_string(int status) {
+  switch (status) {
+    case CONV_OK: return "CONV_OK";
+    case CONV_ERR_NULL: return "CONV_ERR_NULL: a required pointer is NULL";
+    case CONV_ERR_ARG: return "CONV_ERR_ARG: argument out of range or misaligned";
+    case CONV_ERR_SHAPE: return "CONV_ERR_SHAPE: non-positive output size or inconsistent shapes";
+    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED: valid request not implemented by this build";
+    case CONV_ERR_CUDA: return "CONV_ERR_CUDA: CUDA runtime error";
+    default: return "unknown conv status";
+  }
+}
+
+const char *conv_last_error(void) { return g_last_error; }
+
+int conv_out_dims(int ndim, const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                  const int64_t *pad, const int64_t *dilation, int64_t *out_dims) {
+  g_last_error[0] = 0;
+  return compute_out_dims(ndim, in_dims, k_dims, stride, pad, dilation, out_dims);
+}
+
+int conv_select_algo(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in_dims,
+                     const int64_t *k_dims, const int64_t *stride, const int64_t *pad, const int64_t *dilation,
+                     int *algo_out) {
+  g_last_error[0] = 0;
+  if (!algo_out) return fail(CONV_ERR_NULL, "conv_select_algo: algo_out is NULL%s");
+  Geom g;
+  int64_t xe, we, ye;
+  int st = make_geom(ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, &xe, &we, &ye);
+  if (st != CONV_OK) return st;
+  *algo_out = choose_algo(g);
+  return CONV_OK;
+}
+
+int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                   int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
+                   const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,
+                   conv_stream_t stream) {
+  g_last_error[0] = 0;
+  Geom g;
+  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g);
+  if (st != CONV_OK) return st;
+  if (algo == CONV_ALGO_AUTO) algo = choose_algo(g);
+  st = check_algo(g, algo);
+  if (st != CONV_OK) return st;
+  if (g.N == 0) return CONV_OK;  // empty batch: nothing to compute
+  cudaStream_t s = (cudaStream_t)stream;
+  cudaError_t e = algo == CONV_ALGO_DIRECT_FFMA ? convfwd::launch_direct_ffma(x, w, bias, y, g, s)
+                                                : convfwd::launch_igemm_3xtf32(x, w, bias, y, g, s);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd: kernel launch");
+  return CONV_OK;
+}
+
+int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in_dims,
+                        const int64_t *k_dims, const int64_t *stride, const int64_t *pad, const int64_t *dilation,
+                        int algo) {
+  g_last_error[0] = 0;
+  Geom g;
+  int64_t xe, we, ye;
+  int st = make_geom(ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, &xe, &we, &ye);
+  if (st != CONV_OK) return st;
+  if (algo == CONV_ALGO_AUTO) return CONV_OK;
+  return check_algo(g, algo);
+}
+
+int conv_fwd_nd(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
+                const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream) {
+  return conv_fwd_nd_ex(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation,
+                        CONV_ALGO_AUTO, stream);
+}
+
+int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
+                       int min_dim, conv_stream_t stream) {
+  g_last_error[0] = 0;
+  if (!x || !w || !y) return fail(CONV_ERR_NULL, "conv3d_min_softmax: descriptor pointer is NULL%s");
+  if (!w->data || (x->dims[0] != 0 && (!x->data || !y->data)))
+    return fail(CONV_ERR_NULL, "conv3d_min_softmax: tensor data is NULL%s");
+  if (min_dim == 3 || min_dim == 4)
+    return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: min_dim %s%lld not implemented (only 2)", "", min_dim);
+  if (min_dim != 2) return fail(CONV_ERR_ARG, "conv3d_min_softmax: min_dim must be 2, 3 or 4%s");
+  for (int i = 0; i < 5; ++i) {
+    if (x->dims[i] < (i == 0 ? 0 : 1) || x->dims[i] > kMaxDim)
+      return fail(CONV_ERR_ARG, "conv3d_min_softmax: bad x dim%s");
+    if (w->dims[i] < 1 || w->dims[i] > kMaxDim) return fail(CONV_ERR_ARG, "conv3d_min_softmax: bad w dim%s");
+  }
+  if (w->dims[1] != x->dims[1])
+    return fail(CONV_ERR_SHAPE, "conv3d_min_softmax: w C_in %s%lld != x C_in %lld", "", w->dims[1], x->dims[1]);
+  const int64_t ins[3] = {x->dims[2], x->dims[3], x->dims[4]};
+  const int64_t ks[3] = {w->dims[2], w->dims[3], w->dims[4]};
+  const int64_t one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
+  Geom g;
+  float *yd = y->data;
+  int st = validate_conv(x->data, w->data, bias, yd, 3, x->dims[0], x->dims[1], w->dims[0], ins, ks, one, zero,
+                         one, &g);
+  if (st != CONV_OK) return st;
+  if (y->dims[0] != g.N || y->dims[1] != g.K || y->dims[2] != g.OH || y->dims[3] != g.OW)
+    return fail(CONV_ERR_SHAPE, "conv3d_min_softmax: y dims must be [N, C_out, H_out, W_out]%s");
+  const char *why = "";
+  if (!convfwd::fused_supported(g, &why))
+    return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
+  if (g.N == 0) return CONV_OK;  // empty batch
+  cudaError_t e = convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: kernel launch");
+  return CONV_OK;
+}
+
+int conv_device_status(unsigned int *flags) {
+  g_last_error[0] = 0;
+  if (!flags) return fail(CONV_ERR_NULL, "conv_device_status: flags is NULL%s");
+  cudaError_t e = convfwd::read_and_clear_device_status(flags);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_device_status");
+  return CONV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,47 @@
+// Internal declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace convfwd {
+
+// A convolution problem in a uniform 3-D view: 1-D and 2-D problems are
+// embedded with leading singleton dims (size 1, kernel 1, stride 1, pad 0,
+// dilation 1), which leaves the sum in the l1_p60 / l1_p76 pages unchanged.
+struct Geom {
+  int64_t N, C, K;             // batch, input channels, output channels
+  int D, H, W;                 // input spatial dims
+  int OD, OH, OW;              // output spatial dims
+  int KD, KH, KW;              // kernel dims
+  int SD, SH, SW;              // stride
+  int PD, PH, PW;              // zero padding (symmetric)
+  int DD, DH, DW;              // dilation
+  int64_t in_spatial() const { return (int64_t)D * H * W; }
+  int64_t out_spatial() const { return (int64_t)OD * OH * OW; }
+  int taps() const { return KD * KH * KW; }
+};
+
+// Device-side status word written by kernels whose bounded waits gave up.
+enum : unsigned { kStatusIgemmWatchdog = 1u };
+
+// Launchers (return cudaSuccess or the launch error).  All validation happens
+// before these are called.
+bool direct_supported(const Geom &g, const char **why);
+cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias, float *y, const Geom &g,
+                               cudaStream_t stream);
+
+// Fused conv3d -> min over output depth -> channel softmax.
+cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
+                                     const Geom &g, cudaStream_t stream);
+// True when launch_fused_min_softmax supports this geometry (channel count,
+// kernel width, shared-memory footprint).
+bool fused_supported(const Geom &g, const char **why);
+
+// Tensor-core implicit GEMM (tcgen05, 3xTF32).
+bool igemm_supported(const Geom &g, const char **why);
+cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
+                                cudaStream_t stream);
+cudaError_t read_and_clear_device_status(unsigned *flags);
+
+}  // namespace convfwd

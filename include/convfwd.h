@@ -1,0 +1,161 @@
+/*
+ * convfwd.h -- C ABI of the GB300 (sm_103a) forward-convolution library.
+ *
+ * The operations follow three POPCORNBENCH reasoning-trace pages:
+ *   - "Kimi-K2.6 l1_p60": nn.Conv3d with an asymmetric (3,5,7) kernel,
+ *     turn 1 (the forward sum, the per-dimension output size, zero padding).
+ *   - "Kimi-K2.6 l1_p76": nn.Conv1d with stride 3 and dilation 4, turns 1-2
+ *     (tap positions j*stride + k*dilation, output length 174758).
+ *   - "Kimi-K2.6 l2_p24": Conv3d -> torch.min(dim=2) -> torch.softmax(dim=1),
+ *     turns 1-2 (min over output depth, then a max-subtracted channel softmax).
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are dense, contiguous, row-major fp32 (PyTorch's default NC[D][H]W).
+ *   - Pointers named x, w, bias, y are DEVICE pointers.  Dimension/hyper-
+ *     parameter arrays (in_dims, k_dims, stride, pad, dilation, out_dims) and
+ *     the descriptor structs are HOST memory, read during the call only.
+ *   - The caller owns every buffer.  The library allocates no device memory and
+ *     keeps no pointer after the call returns.  y must not overlap x, w or bias.
+ *   - All device work is enqueued on `stream` (NULL = legacy default stream);
+ *     calls return without synchronising.  Errors from kernels that already
+ *     ran surface at the caller's next synchronisation (cudaStreamSynchronize).
+ *   - Every argument is validated on the host before anything is launched; a
+ *     non-zero status means nothing was written to y.  conv_last_error()
+ *     returns a human-readable reason for the most recent failure on the
+ *     calling thread.
+ *   - Kernels never trap or assert.  Waits inside kernels are bounded; if one
+ *     gives up, the kernel records it in a device-side status word that
+ *     conv_device_status() reads.
+ */
+#ifndef CONVFWD_H
+#define CONVFWD_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define CONVFWD_API __attribute__((visibility("default")))
+#else
+#define CONVFWD_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as the CUDA runtime's cudaStream_t / the driver's CUstream. */
+struct CUstream_st;
+typedef struct CUstream_st *conv_stream_t;
+
+typedef enum {
+  CONV_OK = 0,
+  CONV_ERR_NULL = 1,        /* a required pointer is NULL */
+  CONV_ERR_ARG = 2,         /* a size/hyper-parameter is out of range, or a pointer is misaligned */
+  CONV_ERR_SHAPE = 3,       /* an output size is <= 0, or descriptor shapes disagree */
+  CONV_ERR_UNSUPPORTED = 4, /* valid request that this build does not implement */
+  CONV_ERR_CUDA = 5         /* a CUDA runtime call failed (see conv_last_error) */
+} conv_status_t;
+
+/* Kernel families.  AUTO lets the planner choose. */
+typedef enum {
+  CONV_ALGO_AUTO = 0,
+  CONV_ALGO_DIRECT_FFMA = 1,  /* FP32 FFMA direct convolution (CUDA cores) */
+  CONV_ALGO_IGEMM_3XTF32 = 2  /* implicit GEMM on tcgen05 tensor cores, 3xTF32 split, fp32 accumulation in TMEM */
+} conv_algo_t;
+
+/* Shape descriptors for the fused entry point (host structs, device data). */
+typedef struct {
+  const float *data; /* device pointer */
+  int64_t dims[5];   /* x: [N, C_in, D, H, W];  w: [C_out, C_in, KD, KH, KW] */
+} conv_tensor5_t;
+
+typedef struct {
+  float *data;     /* device pointer */
+  int64_t dims[4]; /* y: [N, C_out, H_out, W_out] */
+} conv_tensor4_t;
+
+/*
+ * Output size per spatial dimension (l1_p60 page turn 1 host code; l1_p76 page
+ * turns 1-2):   out[i] = floor((in[i] + 2*pad[i] - dilation[i]*(k[i]-1) - 1) / stride[i]) + 1
+ * ndim in {1,2,3}; in, k, stride, dilation >= 1; pad >= 0.  Writes out_dims
+ * (host, ndim entries) and returns CONV_OK, or CONV_ERR_SHAPE when some size is
+ * <= 0 (out_dims still written), CONV_ERR_ARG / CONV_ERR_NULL otherwise.
+ */
+CONVFWD_API int conv_out_dims(int ndim, const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                  const int64_t *pad, const int64_t *dilation, int64_t *out_dims);
+
+/*
+ * Forward N-D convolution, ndim in {1,2,3} (l1_p60 page turn 1; l1_p76 page turns 1-2):
+ *   y[n,o,p] = bias[o] + sum_{c<C_in} sum_{k} w[o,c,k] * x[n,c, p*stride + k*dilation - pad]
+ * with taps outside the input reading zero (symmetric zero padding, groups = 1).
+ *   x    [N, C_in, in_dims...]          device, fp32
+ *   w    [C_out, C_in, k_dims...]       device, fp32
+ *   bias [C_out] or NULL (no bias)      device, fp32
+ *   y    [N, C_out, out_dims...]        device, fp32, out_dims as conv_out_dims
+ *   in_dims, k_dims, stride, pad, dilation: host arrays of ndim int64
+ * N = 0 is a valid empty batch (nothing is launched).
+ * Accuracy: |y - exact| <= 1e-4 * (1 + |exact|) elementwise for inputs of the
+ * magnitudes used in the tests (accumulation in fp32; the tensor-core path
+ * splits each operand into two TF32 halves and sums three products).
+ * Returns CONV_OK or an error status; nothing is launched on error.
+ */
+CONVFWD_API int conv_fwd_nd(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
+                const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream);
+
+/* conv_fwd_nd with an explicit kernel family (conv_algo_t).  CONV_ALGO_AUTO is
+ * what conv_fwd_nd uses.  Returns CONV_ERR_UNSUPPORTED when the requested
+ * family cannot run this shape (e.g. the tensor-core path's weight tile does
+ * not fit in shared memory). */
+CONVFWD_API int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                   int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
+                   const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,
+                   conv_stream_t stream);
+
+/* The kernel family conv_fwd_nd would use for this problem (host only, no
+ * device access).  Writes *algo_out and returns CONV_OK, or an error status
+ * for an invalid problem. */
+CONVFWD_API int conv_select_algo(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in_dims,
+                     const int64_t *k_dims, const int64_t *stride, const int64_t *pad, const int64_t *dilation,
+                     int *algo_out);
+
+/* CONV_OK when kernel family `algo` can run this problem, CONV_ERR_UNSUPPORTED
+ * when it cannot (reason in conv_last_error), or the validation status of an
+ * invalid problem.  Host only, no device access. */
+CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in_dims,
+                                    const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                                    const int64_t *dilation, int algo);
+
+/*
+ * Fused Conv3d -> min over one spatial dim of the conv output -> softmax over
+ * channels (l2_p24 page, turns 1-2):
+ *   z[n,o,d,h,w] = bias[o] + sum_{c,kd,kh,kw} w[o,c,kd,kh,kw] * x[n,c,d+kd,h+kh,w+kw]
+ *   m[n,o,h,w]   = min_d z[n,o,d,h,w]                     (min_dim = 2, depth)
+ *   y[n,o,h,w]   = exp(m - max_o m) / sum_o exp(m - max_o m)
+ * Conv hyper-parameters are fixed to stride 1, padding 0, dilation 1, groups 1.
+ * The 5-D intermediate z is never written to memory.
+ *   x->dims = [N, C_in, D, H, W], w->dims = [C_out, C_in, KD, KH, KW],
+ *   bias: [C_out] device or NULL, y->dims must be [N, C_out, D-KD+1 ... ] with the
+ *   reduced dim removed: for min_dim = 2, [N, C_out, H-KH+1, W-KW+1].
+ * min_dim: 2 (depth) is implemented; 3 and 4 return CONV_ERR_UNSUPPORTED;
+ * anything else CONV_ERR_ARG.  C_out is limited to 96.
+ */
+CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
+                       int min_dim, conv_stream_t stream);
+
+/* Static description of a status code. */
+CONVFWD_API const char *conv_status_string(int status);
+
+/* Reason for the most recent non-OK return on the calling thread ("" if none). */
+CONVFWD_API const char *conv_last_error(void);
+
+/* Synchronises the current device, then returns and clears the device-side
+ * status word: 0 when no kernel gave up on a bounded wait since the last call,
+ * else a bit set per kernel family that did (bit 0: tensor-core path).  Writes
+ * the word to *flags and returns CONV_OK, or CONV_ERR_CUDA. */
+CONVFWD_API int conv_device_status(unsigned int *flags);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CONVFWD_H */

@@ -1,0 +1,133 @@
+"""Host-only checks of the C-ABI library: it loads, exports every symbol that
+include/convfwd.h declares, and rejects invalid requests with the documented
+status before touching a device.  No compute call runs here.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import implicit_gemm_convolution_fwd_gb300 as cf
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "convfwd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from implicit_gemm_convolution_fwd_gb300 import build_lib
+    build_lib.build()
+    return cf.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*CONVFWD_API\s+[A-Za-z_][A-Za-z0-9_ ]*?\**\s*\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_binding_surface():
+    assert declared_functions() == sorted(cf.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_out_dims_matches_oracle(lib):
+    rng = np.random.default_rng(0)
+    for _ in range(300):
+        nd = int(rng.integers(1, 4))
+        ins = rng.integers(1, 40, nd)
+        k = rng.integers(1, 6, nd)
+        s = rng.integers(1, 4, nd)
+        p = rng.integers(0, 4, nd)
+        d = rng.integers(1, 4, nd)
+        ref = oracle.out_dims(ins, k, s, p, d)
+        if min(ref) <= 0:
+            with pytest.raises(cf.ConvError) as e:
+                cf.out_dims(ins, k, s, p, d)
+            assert e.value.status == cf.CONV_ERR_SHAPE
+        else:
+            assert cf.out_dims(ins, k, s, p, d) == ref
+
+
+def test_page_worked_shapes_through_library(lib):
+    assert cf.out_dims((524280,), (3,), 3, 0, 4) == (174758,)
+    assert cf.out_dims((64, 64, 64), (3, 5, 7), 1, 0, 1) == (62, 60, 58)
+    assert cf.out_dims((24, 32, 32), (3, 3, 3), 1, 0, 1) == (22, 30, 30)
+
+
+def _call(lib, x=0x1000, w=0x2000, b=None, y=0x10000000, nd=1, N=1, C=1, K=1, ins=(8,), k=(3,), s=(1,), p=(0,),
+          d=(1,), algo=0):
+    A = cf._arr
+    return lib.conv_fwd_nd_ex(x, w, b, y, nd, N, C, K, A(ins), A(k), A(s), A(p), A(d), algo, None)
+
+
+def test_validation_statuses(lib):
+    # every one of these returns before any CUDA call
+    assert _call(lib, x=None) == cf.CONV_ERR_NULL
+    assert _call(lib, y=None) == cf.CONV_ERR_NULL
+    assert lib.conv_fwd_nd_ex(0x1000, 0x2000, None, 0x3000, 1, 1, 1, 1, None, cf._arr((3,)), cf._arr((1,)),
+                              cf._arr((0,)), cf._arr((1,)), 0, None) == cf.CONV_ERR_NULL
+    assert _call(lib, nd=0) == cf.CONV_ERR_ARG
+    assert _call(lib, nd=4, ins=(8,) * 4, k=(1,) * 4, s=(1,) * 4, p=(0,) * 4, d=(1,) * 4) == cf.CONV_ERR_ARG
+    assert _call(lib, N=-1) == cf.CONV_ERR_ARG
+    assert _call(lib, C=-1) == cf.CONV_ERR_ARG
+    assert _call(lib, s=(0,)) == cf.CONV_ERR_ARG
+    assert _call(lib, d=(0,)) == cf.CONV_ERR_ARG
+    assert _call(lib, p=(-1,)) == cf.CONV_ERR_ARG
+    assert _call(lib, ins=(2,), k=(3,)) == cf.CONV_ERR_SHAPE                    # output length <= 0
+    assert _call(lib, ins=(8,), k=(3,), d=(4,)) == cf.CONV_ERR_SHAPE            # dilated extent 9 > 8
+    assert _call(lib, x=0x1002) == cf.CONV_ERR_ARG                               # misaligned
+    assert _call(lib, y=0x1000 + 4) == cf.CONV_ERR_ARG                           # y overlaps x
+    assert _call(lib, algo=7) == cf.CONV_ERR_ARG
+    assert _call(lib, N=1 << 40) == cf.CONV_ERR_ARG
+    msg = lib.conv_last_error().decode()
+    assert "N must be" in msg
+
+
+def test_status_strings(lib):
+    for s in range(6):
+        assert lib.conv_status_string(s).decode().startswith("CONV_")
+    assert b"unknown" in lib.conv_status_string(99)
+
+
+def test_fused_validation_statuses(lib):
+    T5, T4 = cf.Tensor5, cf.Tensor4
+    x = T5(0x1000, (ctypes.c_int64 * 5)(2, 3, 24, 32, 32))
+    w = T5(0x100000, (ctypes.c_int64 * 5)(24, 3, 3, 3, 3))
+    y = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 30, 30))
+    f = lib.conv3d_min_softmax
+    assert f(None, ctypes.byref(w), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_NULL
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 3, None) == cf.CONV_ERR_UNSUPPORTED
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 4, None) == cf.CONV_ERR_UNSUPPORTED
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 1, None) == cf.CONV_ERR_ARG
+    wbad = T5(0x100000, (ctypes.c_int64 * 5)(24, 4, 3, 3, 3))
+    assert f(ctypes.byref(x), ctypes.byref(wbad), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE
+    ybad = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 30, 29))
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(ybad), 2, None) == cf.CONV_ERR_SHAPE
+    wbig = T5(0x100000, (ctypes.c_int64 * 5)(200, 3, 3, 3, 3))
+    ybig = T4(0x40000000, (ctypes.c_int64 * 4)(2, 200, 30, 30))
+    assert f(ctypes.byref(x), ctypes.byref(wbig), None, ctypes.byref(ybig), 2, None) == cf.CONV_ERR_UNSUPPORTED
+    xsmall = T5(0x1000, (ctypes.c_int64 * 5)(2, 3, 2, 32, 32))
+    assert f(ctypes.byref(xsmall), ctypes.byref(w), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE
+
+
+def test_select_algo_host_only(lib):
+    # tiny reductions always take the FFMA direct path
+    assert cf.select_algo(2, 4, 8, (1024,), (3,), 3, 0, 4) == cf.CONV_ALGO_DIRECT_FFMA
+    a = cf.select_algo(64, 64, 128, (524280,), (3,), 3, 0, 4)
+    assert a in (cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_IGEMM_3XTF32)
+
+
+def test_algo_supported_queries(lib):
+    assert cf.algo_supported(2, 4, 8, (1024,), (3,), 3, 0, 4, cf.CONV_ALGO_DIRECT_FFMA)
+    assert not cf.algo_supported(1, 1, 1, (9999,), (1025,), 1, 0, 1, cf.CONV_ALGO_DIRECT_FFMA)
+    with pytest.raises(cf.ConvError):
+        cf.algo_supported(1, 1, 1, (2,), (3,), 1, 0, 1, cf.CONV_ALGO_DIRECT_FFMA)

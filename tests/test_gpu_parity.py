@@ -1,0 +1,250 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64 oracle.
+
+Tolerance (from the pages' harness, atol = rtol = 1e-4, restated elementwise):
+    |y_gpu - y_oracle| <= 1e-4 * (1 + |y_oracle|)
+Shapes must match exactly.  Small cases are compared element by element over
+the whole output; the benchmark workloads at full size are compared on
+sampled outputs (including the first and last elements and tile edges), which
+the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+import implicit_gemm_convolution_fwd_gb300 as cf
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-4
+ALGOS = (cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_IGEMM_3XTF32)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from implicit_gemm_convolution_fwd_gb300 import build_lib
+    build_lib.build()
+    cf.load()
+    yield
+    assert cf.device_status() == 0, "a kernel gave up on a bounded wait"
+
+
+def assert_close(y, ref, what=""):
+    y = np.asarray(y, np.float64)
+    assert y.shape == ref.shape, (what, y.shape, ref.shape)
+    err = np.abs(y - ref)
+    bound = TOL * (1.0 + np.abs(ref))
+    bad = err > bound
+    if bad.any():
+        i = np.unravel_index(np.argmax(err / bound), err.shape)
+        raise AssertionError(f"{what}: {bad.sum()} of {err.size} outside tolerance; worst at {i}: "
+                             f"gpu {y[i]!r} oracle {ref[i]!r}")
+
+
+def run_conv(x, w, b, s, p, d, algo=cf.CONV_ALGO_AUTO):
+    xt = torch.from_numpy(x).cuda()
+    wt = torch.from_numpy(w).cuda()
+    bt = None if b is None else torch.from_numpy(b).cuda()
+    y = cf.conv_fwd_nd(xt, wt, bt, s, p, d, algo=algo)
+    torch.cuda.synchronize()
+    return y
+
+
+def random_case(seed, nd):
+    rng = np.random.default_rng(seed)
+    N = int(rng.integers(1, 3))
+    C_in = int(rng.integers(1, 24))
+    C_out = int(rng.integers(1, 70))
+    k = tuple(int(v) for v in rng.integers(1, 6, nd))
+    s = tuple(int(v) for v in rng.integers(1, 4, nd))
+    p = tuple(int(v) for v in rng.integers(0, 4, nd))
+    d = tuple(int(v) for v in rng.integers(1, 4, nd))
+    ext = [(k[i] - 1) * d[i] + 1 for i in range(nd)]
+    hi = {1: 300, 2: 40, 3: 14}[nd]
+    ins = tuple(int(rng.integers(max(1, ext[i] - 2 * p[i]), max(ext[i] - 2 * p[i], 1) + hi)) for i in range(nd))
+    x = rng.standard_normal((N, C_in) + ins).astype(np.float32)
+    w = (rng.random((C_out, C_in) + k).astype(np.float32) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))
+    b = rng.standard_normal(C_out).astype(np.float32) if seed % 2 else None
+    return x, w, b, s, p, d
+
+
+def supported(x, w, s, p, d, algo):
+    return cf.algo_supported(x.shape[0], x.shape[1], w.shape[0], x.shape[2:], w.shape[2:], s, p, d, algo)
+
+
+# ------------------------------------------------------------ small cases
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("nd", [1, 2, 3])
+@pytest.mark.parametrize("seed", range(6))
+def test_random_small(algo, nd, seed):
+    x, w, b, s, p, d = random_case(1000 * nd + seed, nd)
+    if not supported(x, w, s, p, d, algo):
+        pytest.skip("shape not supported by this kernel family")
+    ref = oracle.conv_nd(x, w, b, s, p, d)
+    y = run_conv(x, w, b, s, p, d, algo).cpu().numpy()
+    assert_close(y, ref, f"nd={nd} seed={seed} algo={cf.ALGO_NAMES[algo]}")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_edge_geometries(algo):
+    rng = np.random.default_rng(5)
+    cases = [
+        # (x shape, w shape, stride, pad, dilation)
+        ((1, 1, 1), (1, 1, 1), (1,), (0,), (1,)),                    # single output
+        ((2, 3, 5), (4, 3, 5), (1,), (0,), (1,)),                    # kernel == input
+        ((1, 2, 9), (3, 2, 2), (5,), (3,), (1,)),                    # pad > kernel, stride > kernel
+        ((1, 2, 17), (2, 2, 3), (7,), (0,), (3,)),                   # stride skips inputs
+        ((1, 3, 4, 5, 6), (5, 3, 1, 1, 1), (1, 1, 1), (0, 0, 0), (1, 1, 1)),  # 1x1x1 kernel
+        ((1, 2, 3, 3, 3), (2, 2, 3, 3, 3), (1, 1, 1), (2, 2, 2), (1, 1, 1)),  # pad 2 around 3^3
+        ((2, 1, 7, 1, 9), (3, 1, 2, 1, 4), (2, 1, 1), (1, 0, 2), (2, 1, 2)),  # singleton H
+        ((1, 4, 130), (67, 4, 3), (1,), (1,), (1,)),                  # C_out not a multiple of any tile
+    ]
+    for xs, ws, s, p, d in cases:
+        x = rng.standard_normal(xs).astype(np.float32)
+        w = rng.standard_normal(ws).astype(np.float32) * 0.3
+        b = rng.standard_normal(ws[0]).astype(np.float32)
+        if not supported(x, w, s, p, d, algo):
+            continue
+        ref = oracle.conv_nd(x, w, b, s, p, d)
+        y = run_conv(x, w, b, s, p, d, algo).cpu().numpy()
+        assert_close(y, ref, f"edge {xs} {ws} s={s} p={p} d={d}")
+
+
+def test_empty_batch_is_a_no_op():
+    x = torch.empty((0, 3, 10), device="cuda")
+    w = torch.randn((4, 3, 3), device="cuda")
+    y = cf.conv_fwd_nd(x, w, None, 1, 0, 1)
+    assert tuple(y.shape) == (0, 4, 8)
+
+
+def test_deterministic_and_stream_ordered():
+    x, w, b, s, p, d = random_case(77, 3)
+    xt, wt, bt = torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda(), torch.from_numpy(b).cuda()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        y1 = cf.conv_fwd_nd(xt, wt, bt, s, p, d, stream=st)
+        y2 = cf.conv_fwd_nd(xt, wt, bt, s, p, d, stream=st)
+    st.synchronize()
+    assert torch.equal(y1, y2)
+
+
+# ----------------------------------------------- workloads, reduced batch
+
+def workload_inputs(name, N=None):
+    wl = synth.WORKLOADS[name]
+    if N is not None:
+        wl = wl.with_batch(N)
+    return (wl,) + wl.make_inputs(seed=0)
+
+
+@pytest.mark.parametrize("name,N", [("conv1d_tiny", None), ("conv3d_asym", 1), ("conv3d_sweep_a", 1),
+                                    ("conv3d_sweep_b", 1), ("conv3d_sweep_b_dil", 1)])
+def test_workload_reduced_batch_full_compare(name, N):
+    wl, x, w, b = workload_inputs(name, N)
+    ref = oracle.conv_nd(x, w, b, wl.stride, wl.pad, wl.dilation)
+    y = run_conv(x, w, b, wl.stride, wl.pad, wl.dilation).cpu().numpy()
+    assert_close(y, ref, wl.name)
+
+
+def test_conv1d_long_short_length_full_compare():
+    wl = synth.WORKLOADS["conv1d_long"]
+    x = synth.uniform((2, 64, 3 * 2000 + 11), 0, 1, 0, synth.TENSOR_X)
+    w = synth.uniform(wl.w_shape(), -wl.kaiming_bound, wl.kaiming_bound, 0, synth.TENSOR_W)
+    ref = oracle.conv_nd(x, w, None, wl.stride, wl.pad, wl.dilation)
+    y = run_conv(x, w, None, wl.stride, wl.pad, wl.dilation).cpu().numpy()
+    assert_close(y, ref, "conv1d_long geometry, L=6011")
+
+
+# ------------------------------------------------- full size, sampled
+
+def sample_indices(shape, count, seed):
+    total = int(np.prod(shape))
+    rng = np.random.default_rng(seed)
+    idx = set(rng.integers(0, total, count).tolist())
+    idx.update([0, total - 1])
+    # corners and edges of every (n, o) slab for the first/last batch and channel
+    sp = shape[2:]
+    for n in (0, shape[0] - 1):
+        for o in (0, shape[1] - 1):
+            for corner in np.ndindex(*[2] * len(sp)):
+                pos = [0 if c == 0 else sp[i] - 1 for i, c in enumerate(corner)]
+                idx.add(int(np.ravel_multi_index((n, o) + tuple(pos), shape)))
+    return np.array(sorted(idx), np.int64)
+
+
+@pytest.mark.parametrize("name", ["conv3d_asym", "conv1d_long", "conv3d_sweep_a", "conv3d_sweep_b"])
+def test_workload_full_size_sampled(name):
+    wl, x, w, b = workload_inputs(name)
+    y = run_conv(x, w, b, wl.stride, wl.pad, wl.dilation)
+    idx = sample_indices(tuple(y.shape), 4000, 123)
+    got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+    del y
+    ref = oracle.conv_nd_at(x, w, b, wl.stride, wl.pad, wl.dilation, idx)
+    assert_close(got, ref, f"{name} full size, {idx.size} sampled outputs")
+
+
+def test_indexing_beyond_int32():
+    # x and y both hold more than 2^31 elements: offsets must be 64-bit.
+    L = (1 << 31) + 1000
+    x = synth.uniform((1, 1, L), 0, 1, 3, synth.TENSOR_X)
+    w = np.array([[[0.25, -0.5, 1.0]]], np.float32)
+    y = run_conv(x, w, None, (1,), (0,), (1,))
+    n_out = y.shape[-1]
+    idx = np.array([0, 1, (1 << 31) - 2, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, n_out - 1], np.int64)
+    got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
+    del y
+    ref = oracle.conv_nd_at(x, w, None, (1,), (0,), (1,), idx)
+    assert_close(got, ref, "int64 indexing")
+
+
+# ------------------------------------------------------------------ fused
+
+def run_fused(x, w, b):
+    xt = torch.from_numpy(x).cuda()
+    wt = torch.from_numpy(w).cuda()
+    bt = None if b is None else torch.from_numpy(b).cuda()
+    y = cf.conv3d_min_softmax(xt, wt, bt, 2)
+    torch.cuda.synchronize()
+    return y
+
+
+@pytest.mark.parametrize("C_out", [1, 5, 12, 13, 24, 25, 48, 49, 96])
+@pytest.mark.parametrize("k", [(3, 3, 3), (2, 3, 5)])
+def test_fused_small(C_out, k):
+    rng = np.random.default_rng(C_out * 10 + k[2])
+    x = rng.random((3, 3, 7, 11, 37)).astype(np.float32)  # W=37: scalar path, 2 column tiles
+    w = (rng.random((C_out, 3) + k).astype(np.float32) - 0.5) * 0.4
+    b = (rng.random(C_out).astype(np.float32) - 0.5) * 0.4
+    ref = oracle.conv3d_min_softmax(x, w, b)
+    y = run_fused(x, w, b).cpu().numpy()
+    assert_close(y, ref, f"fused C_out={C_out} k={k}")
+    assert np.abs(y.sum(axis=1) - 1).max() < 1e-5
+
+
+def test_fused_vector_path_and_ragged_rows():
+    rng = np.random.default_rng(3)
+    x = rng.random((3, 3, 6, 9, 40)).astype(np.float32)  # W % 4 == 0, OW = 38 -> 2 column tiles; 7 rows/img
+    w = (rng.random((24, 3, 3, 3, 3)).astype(np.float32) - 0.5) * 0.4
+    b = (rng.random(24).astype(np.float32) - 0.5) * 0.4
+    ref = oracle.conv3d_min_softmax(x, w, b)
+    assert_close(run_fused(x, w, b).cpu().numpy(), ref, "fused vector path")
+    assert_close(run_fused(x, w, None).cpu().numpy(), oracle.conv3d_min_softmax(x, w, None), "fused no bias")
+
+
+def test_fused_workload_reduced_batch_full_compare():
+    wl, x, w, b = workload_inputs("conv3d_min_softmax", 4)
+    ref = oracle.conv3d_min_softmax(x, w, b)
+    assert_close(run_fused(x, w, b).cpu().numpy(), ref, "fused workload N=4")
+
+
+def test_fused_workload_full_size_sampled():
+    wl, x, w, b = workload_inputs("conv3d_min_softmax")
+    y = run_fused(x, w, b)
+    N, C_out, OH, OW = y.shape
+    rng = np.random.default_rng(9)
+    cols = np.unique(np.concatenate([rng.integers(0, N * OH * OW, 1500), [0, OW - 1, OH * OW - 1, N * OH * OW - 1]]))
+    yc = y.permute(0, 2, 3, 1).reshape(-1, C_out)[torch.from_numpy(cols).cuda()].cpu().numpy()
+    ref = oracle.conv3d_min_softmax_at(x, w, b, cols)
+    assert_close(yc, ref, "fused full size sampled")
+    assert torch.allclose(y.sum(dim=1), torch.ones((), device="cuda"), atol=1e-5)
