@@ -116,14 +116,17 @@ int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *i
 }
 
 // Full validation of a conv_fwd_nd call: shapes, then pointers.
+// y_elems_override >= 0 replaces the conv output size in the overlap check
+// (the fused entry point writes a reduced 4-D output).
 int validate_conv(const float *x, const float *w, const float *bias, const float *y, int ndim, int64_t N,
                   int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s,
-                  const int64_t *p, const int64_t *d, Geom *g) {
+                  const int64_t *p, const int64_t *d, Geom *g, int64_t y_elems_override = -1) {
   int64_t xe, we, ye;
   int st = make_geom(ndim, N, C_in, C_out, in, k, s, p, d, g, &xe, &we, &ye);
   if (st != CONV_OK) return st;
   // an empty batch has empty x and y, which may be NULL
   if (!w || (N > 0 && (!x || !y))) return fail(CONV_ERR_NULL, "conv: x, w and y must be non-NULL%s");
+  if (y_elems_override >= 0) ye = y_elems_override;
   if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)y | (uintptr_t)bias) & 3u)
     return fail(CONV_ERR_ARG, "conv: x, w, bias, y must be 4-byte aligned%s");
   if (ranges_overlap(y, ye * 4, x, xe * 4) || ranges_overlap(y, ye * 4, w, we * 4) ||
@@ -254,8 +257,13 @@ int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const f
   const int64_t one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
   Geom g;
   float *yd = y->data;
+  int64_t y4 = 1;
+  for (int i = 0; i < 4; ++i) {
+    if (y->dims[i] < 0 || y->dims[i] > kMaxDim) return fail(CONV_ERR_SHAPE, "conv3d_min_softmax: bad y dim%s");
+    y4 *= y->dims[i];  // each factor < 2^31, product checked against x/w sizes below
+  }
   int st = validate_conv(x->data, w->data, bias, yd, 3, x->dims[0], x->dims[1], w->dims[0], ins, ks, one, zero,
-                         one, &g);
+                         one, &g, y4);
   if (st != CONV_OK) return st;
   if (y->dims[0] != g.N || y->dims[1] != g.K || y->dims[2] != g.OH || y->dims[3] != g.OW)
     return fail(CONV_ERR_SHAPE, "conv3d_min_softmax: y dims must be [N, C_out, H_out, W_out]%s");

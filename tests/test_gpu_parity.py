@@ -63,7 +63,7 @@ def random_case(seed, nd):
     hi = {1: 300, 2: 40, 3: 14}[nd]
     ins = tuple(int(rng.integers(max(1, ext[i] - 2 * p[i]), max(ext[i] - 2 * p[i], 1) + hi)) for i in range(nd))
     x = rng.standard_normal((N, C_in) + ins).astype(np.float32)
-    w = (rng.random((C_out, C_in) + k).astype(np.float32) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))).astype(np.float32)
     b = rng.standard_normal(C_out).astype(np.float32) if seed % 2 else None
     return x, w, b, s, p, d
 
@@ -185,13 +185,15 @@ def test_workload_full_size_sampled(name):
 
 
 def test_indexing_beyond_int32():
-    # x and y both hold more than 2^31 elements: offsets must be 64-bit.
-    L = (1 << 31) + 1000
-    x = synth.uniform((1, 1, L), 0, 1, 3, synth.TENSOR_X)
+    # x and y both hold more than 2^31 elements (each dim fits int32): element
+    # offsets must be 64-bit.
+    L = (1 << 30) + 1000
+    x = synth.uniform((2, 1, L), 0, 1, 3, synth.TENSOR_X)
     w = np.array([[[0.25, -0.5, 1.0]]], np.float32)
     y = run_conv(x, w, None, (1,), (0,), (1,))
-    n_out = y.shape[-1]
-    idx = np.array([0, 1, (1 << 31) - 2, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, n_out - 1], np.int64)
+    total = y.numel()
+    assert total > (1 << 31)
+    idx = np.array([0, 1, L - 3, L - 2, (1 << 31) - 1, 1 << 31, (1 << 31) + 1, total - 1], np.int64)
     got = y.reshape(-1)[torch.from_numpy(idx).cuda()].cpu().numpy()
     del y
     ref = oracle.conv_nd_at(x, w, None, (1,), (0,), (1,), idx)
