@@ -296,9 +296,13 @@ def main():
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch size (small cases for profiler captures)")
     args = ap.parse_args()
     rank, world, local = env_rank()
     wl = synth.WORKLOADS[args.workload]
+    if args.batch is not None:
+        wl = wl.with_batch(args.batch)
 
     if args.impl == "reference":
         return main_reference(args, wl, rank, world)

@@ -1,21 +1,408 @@
-// Placeholder translation unit for the tensor-core implicit GEMM; the tcgen05
-// kernel replaces it.
+// Implicit-GEMM forward convolution on the 5th-generation tensor cores
+// (tcgen05, TMEM accumulators), fp32-accurate through a 3xTF32 split.
+//
+// The GEMM view is the one the l1_p60 page (turn 1) uses to size the problem:
+// rows = output positions (N x OD x OH x OW), columns = output channels, and
+// the reduction runs over K = C_in x KD x KH x KW taps of
+//   y[n,o,p] = b[o] + sum_{c,k} w[o,c,k] * x[n,c, p*stride + k*dilation - pad]
+// (zero padding: taps outside the input contribute 0).  The im2col matrix is
+// never materialised in memory: producer warps gather it straight from x
+// into tensor memory.
+//
+// Per CTA (persistent, one per SM, 416 threads):
+//   warps 0-3   epilogue: tcgen05.ld the accumulator, add bias, store y
+//               (each warp store covers 32 consecutive output positions of
+//               one channel, i.e. 128 contiguous bytes)
+//   warps 4-7   producer group 0 \  each thread owns one output position (one
+//   warps 8-11  producer group 1 /  TMEM lane) of the 128-row tile; it gathers
+//               the position's receptive field for a chunk of K, splits every
+//               value into TF32 hi + lo (hi = top 10 mantissa bits, lo = exact
+//               remainder) and writes both to TMEM with tcgen05.st.  The two
+//               groups fill alternate chunk stages.
+//   warp 12     TMEM allocation; lane 0 issues the MMAs:
+//               D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi   (M=128, N=C_out pad 32, K=8 per MMA)
+// A (im2col tile) comes from TMEM, B (weights, split hi/lo once per CTA) from
+// shared memory in the K-major no-swizzle core-matrix layout, D double-buffered
+// in TMEM.  Hand-off between roles uses mbarriers; tcgen05.commit signals MMA
+// completion.  Every wait is bounded: on timeout the kernel raises a flag,
+// lets the other roles fall through, drains its MMAs and frees TMEM.
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 #include "conv_internal.cuh"
+#include "sm100_ptx.cuh"
 
 namespace convfwd {
 
 __device__ unsigned int g_device_status = 0;
 
-bool igemm_supported(const Geom &, const char **why) {
-  *why = "tensor-core path not built";
-  return false;
+namespace {
+
+constexpr int kTileM = 128;
+constexpr int kEpiWarps = 4;
+constexpr int kProdGroups = 2;
+constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 12
+constexpr int kThreads = (kMmaWarp + 1) * 32;          // 416
+constexpr uint32_t kTmemCols = 512;
+constexpr int kMaxNpad = 128;
+constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMinSmem = 116 * 1024;  // keeps one CTA per SM, so TMEM allocation never contends
+constexpr long long kWaitLimitCycles = 1ll << 32;  // about two seconds
+
+struct IgemmParams {
+  const float *__restrict__ x;
+  const float *__restrict__ w;
+  const float *__restrict__ bias;
+  float *__restrict__ y;
+  Geom g;
+  int64_t M_total;  // N * OD * OH * OW
+  int64_t osp;      // OD * OH * OW
+  int64_t tiles;    // ceil(M_total / 128)
+  int Kred;         // C_in * taps
+  int Kpad;         // Kred rounded up to 32
+  int Npad;         // C_out rounded up to 32
+  int KC;           // K columns per pipeline chunk (multiple of 32)
+  int nchunks;      // ceil(Kpad / KC)
+  uint32_t b_bytes; // Npad * Kpad * 4
+};
+
+struct Plan {
+  int Kred, Kpad, Npad, KC, nchunks;
+  size_t smem;
+};
+
+bool make_plan(const Geom &g, Plan *pl, const char **why) {
+  const int64_t taps = (int64_t)g.KD * g.KH * g.KW;
+  const int64_t kred = g.C * taps;
+  if (g.K > kMaxNpad) {
+    *why = "C_out above 128";
+    return false;
+  }
+  if (g.KD > 32 || g.KH > 32 || g.KW > 32) {
+    *why = "a kernel dimension above 32";
+    return false;
+  }
+  const int64_t HW = (int64_t)g.H * g.W, DHW = HW * g.D;
+  const int64_t max_off = (g.C - 1) * DHW + (int64_t)(g.KD - 1) * g.DD * HW + (int64_t)(g.KH - 1) * g.DH * g.W +
+                          (int64_t)(g.KW - 1) * g.DW;
+  if (max_off >= (int64_t)1 << 31) {
+    *why = "receptive-field offsets of one image exceed 2^31 elements";
+    return false;
+  }
+  pl->Kred = (int)kred;
+  pl->Kpad = (int)((kred + 31) / 32 * 32);
+  pl->Npad = (int)((g.K + 31) / 32 * 32);
+  int kc = (int)((kTmemCols - 2 * pl->Npad) / 4) / 32 * 32;
+  if (kc > pl->Kpad) kc = pl->Kpad;
+  pl->KC = kc;
+  pl->nchunks = (pl->Kpad + kc - 1) / kc;
+  size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 + 9 * 8 + 16;
+  if (smem > (size_t)kMaxSmem) {
+    *why = "weights (hi + lo) do not fit in shared memory";
+    return false;
+  }
+  pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
+  return true;
 }
 
-cudaError_t launch_igemm_3xtf32(const float *, const float *, const float *, float *, const Geom &,
-                                cudaStream_t) {
-  return cudaErrorNotSupported;
+// Bounded mbarrier wait.  Returns false (and raises the abort flag plus the
+// device status bit on timeout) when the phase did not complete.
+__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      *abort_flag = 1;
+      atomicOr(&g_device_status, kStatusIgemmWatchdog);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_uint(v) & 0xffffe000u; }
+
+__global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Geom &g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  uint8_t *b_hi = smem;
+  uint8_t *b_lo = smem + p.b_bytes;
+  uint2 *table = reinterpret_cast<uint2 *>(smem + 2 * (size_t)p.b_bytes);
+  float *bias_s = reinterpret_cast<float *>(table + p.Kpad);
+  uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const uint32_t bar_a_full = ptx::smem_addr(bars + 0);   // [2]
+  const uint32_t bar_a_empty = ptx::smem_addr(bars + 2);  // [2]
+  const uint32_t bar_d_full = ptx::smem_addr(bars + 4);   // [2]
+  const uint32_t bar_d_empty = ptx::smem_addr(bars + 6);  // [2]
+  const uint32_t bar_drain = ptx::smem_addr(bars + 8);
+
+  const uint32_t SBO = (uint32_t)p.Kpad * 32;  // bytes between 8-row groups of B
+  const int taps = g.KD * g.KH * g.KW;
+  const int64_t HW = (int64_t)g.H * g.W, DHW = HW * g.D;
+
+  // ---- weights -> shared memory, split into TF32 hi / lo.  Word i of the
+  // core-matrix layout holds B[n][k] with n = 8*(cm / (Kpad/4)) + row,
+  // k = 4*(cm % (Kpad/4)) + col, so consecutive threads write consecutive
+  // words (conflict-free).
+  {
+    const int kq = p.Kpad / 4;
+    const int words = p.Npad * p.Kpad;
+    for (int i = tid; i < words; i += kThreads) {
+      const int cm = i >> 5, r = (i >> 2) & 7, cw = i & 3;
+      const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
+      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kred + k) : 0.f;
+      const float hi = __uint_as_float(tf32_hi_bits(v));
+      reinterpret_cast<float *>(b_hi)[i] = hi;
+      reinterpret_cast<float *>(b_lo)[i] = v - hi;
+    }
+    // ---- reduction index -> (input offset, tap coordinates)
+    for (int kk = tid; kk < p.Kpad; kk += kThreads) {
+      uint2 e;
+      if (kk < p.Kred) {
+        const int c = kk / taps, t = kk - c * taps;
+        const int kd = t / (g.KH * g.KW), r2 = t - kd * g.KH * g.KW;
+        const int kh = r2 / g.KW, kw = r2 - kh * g.KW;
+        e.x = (uint32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
+        e.y = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
+      } else {
+        e.x = 0;
+        e.y = 0x80000000u;  // padding column: contributes zero
+      }
+      table[kk] = e;
+    }
+    for (int i = tid; i < p.Npad; i += kThreads) bias_s[i] = (p.bias && i < g.K) ? __ldg(p.bias + i) : 0.f;
+  }
+  ptx::fence_proxy_async_smem();
+  if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s) {
+      ptx::mbar_init(bar_a_full + 8 * s, 128);
+      ptx::mbar_init(bar_a_empty + 8 * s, 1);
+      ptx::mbar_init(bar_d_full + 8 * s, 1);
+      ptx::mbar_init(bar_d_empty + 8 * s, 128);
+    }
+    ptx::mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t a_col0 = 2u * p.Npad;  // A stage s: hi at a_col0 + 2*KC*s, lo at + KC
+
+  if (warp < kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    int64_t it = 0;
+    for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
+      const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
+      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const int64_t m = tile * kTileM + tid;
+      const bool valid = m < p.M_total;
+      const int64_t n = valid ? m / p.osp : 0;
+      const int64_t pp = valid ? m - n * p.osp : 0;
+      float *yp = p.y + n * g.K * p.osp + pp;
+      for (int c0 = 0; c0 < p.Npad; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
+        ptx::tmem_wait_ld();
+        if (c0 + 32 >= p.Npad) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d_empty + 8 * b);
+        }
+        if (valid) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int o = c0 + j;
+            if (o < g.K) yp[(int64_t)o * p.osp] = __uint_as_float(v[j]) + bias_s[o];
+          }
+        }
+      }
+    }
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ producers
+    const int grp = (warp - kEpiWarps) >> 2;
+    const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * grp);
+    const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
+    const uint32_t full_d = (1u << g.KD) - 1u, full_h = (1u << g.KH) - 1u, full_w = (1u << g.KW) - 1u;
+    const int64_t OHW = (int64_t)g.OH * g.OW;
+    int64_t it = 0;
+    bool aborted = false;
+    for (int64_t tile = blockIdx.x; tile < p.tiles && !aborted; tile += gridDim.x, ++it) {
+      const int64_t m = tile * kTileM + t;
+      const bool valid = m < p.M_total;
+      int64_t n = 0;
+      int od = 0, oh = 0, ow = 0;
+      if (valid) {
+        n = m / p.osp;
+        const int64_t pp = m - n * p.osp;
+        od = (int)(pp / OHW);
+        const int rem = (int)(pp - (int64_t)od * OHW);
+        oh = rem / g.OW;
+        ow = rem - oh * g.OW;
+      }
+      const int id0 = od * g.SD - g.PD, ih0 = oh * g.SH - g.PH, iw0 = ow * g.SW - g.PW;
+      uint32_t dm = 0, hm = 0, wm = 0;
+      for (int k = 0; k < g.KD; ++k) dm |= (uint32_t)((unsigned)(id0 + k * g.DD) < (unsigned)g.D) << k;
+      for (int k = 0; k < g.KH; ++k) hm |= (uint32_t)((unsigned)(ih0 + k * g.DH) < (unsigned)g.H) << k;
+      for (int k = 0; k < g.KW; ++k) wm |= (uint32_t)((unsigned)(iw0 + k * g.DW) < (unsigned)g.W) << k;
+      const bool full = valid && dm == full_d && hm == full_h && wm == full_w;
+      const bool warp_full = __all_sync(0xffffffffu, full);
+      // element offset of the receptive field's origin (may lie in the padding)
+      const int64_t xoff = n * g.C * DHW + (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;
+      const float *xo = p.x + (valid ? xoff : 0);
+
+      for (int q = 0; q < p.nchunks; ++q) {
+        const int64_t gidx = it * p.nchunks + q;
+        if ((int)(gidx & 1) != grp) continue;
+        const uint32_t r = (uint32_t)(gidx >> 1);
+        bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          aborted = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        const int k0 = q * p.KC;
+        const int ncols = min(p.KC, p.Kpad - k0);
+        for (int h = 0; h < ncols; h += 32) {
+          const uint2 *tb = table + k0 + h;
+          uint32_t vh[32], vl[32];
+          if (warp_full) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const uint2 e = tb[j];
+              const float v = (e.y >> 31) ? 0.f : __ldg(xo + (int32_t)e.x);
+              vh[j] = tf32_hi_bits(v);
+              vl[j] = __float_as_uint(v - __uint_as_float(vh[j]));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const uint2 e = tb[j];
+              const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu, kw = (e.y >> 16) & 0xffu;
+              const bool in = valid && !(e.y >> 31) && (((dm >> kd) & (hm >> kh) & (wm >> kw)) & 1u);
+              const float v = in ? __ldg(xo + (int32_t)e.x) : 0.f;
+              vh[j] = tf32_hi_bits(v);
+              vl[j] = __float_as_uint(v - __uint_as_float(vh[j]));
+            }
+          }
+          ptx::tmem_st32(tmem + lane_base + a_hi_col + (uint32_t)h, vh);
+          ptx::tmem_st32(tmem + lane_base + a_lo_col + (uint32_t)h, vl);
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_a_full + 8 * grp);
+      }
+    }
+  } else if (lane == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
+    const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
+    int64_t it = 0;
+    bool aborted = false;
+    for (int64_t tile = blockIdx.x; tile < p.tiles && !aborted; tile += gridDim.x, ++it) {
+      const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
+      if (!wait_phase(bar_d_empty + 8 * b, (rb & 1) ^ 1, abort_flag)) break;
+      ptx::tc_fence_after();
+      const uint32_t d_tmem = tmem + b * (uint32_t)p.Npad;
+      for (int q = 0; q < p.nchunks; ++q) {
+        const int64_t gidx = it * p.nchunks + q;
+        const uint32_t s = (uint32_t)(gidx & 1), r = (uint32_t)(gidx >> 1);
+        if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag)) {
+          aborted = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a_hi = tmem + a_col0 + 2u * (uint32_t)p.KC * s;
+        const uint32_t a_lo = a_hi + (uint32_t)p.KC;
+        const int k0 = q * p.KC;
+        const int ksteps = min(p.KC, p.Kpad - k0) / 8;
+        for (int ks = 0; ks < ksteps; ++ks) {
+          const uint32_t kbyte = (uint32_t)(k0 + ks * 8) * 32u;  // (k/4) core matrices of 128 B
+          const uint64_t dh = ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
+          const uint64_t dl = ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
+          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (q | ks) != 0);
+          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
+          ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
+        }
+        ptx::mma_commit(bar_a_empty + 8 * s);
+      }
+      if (aborted) break;
+      ptx::mma_commit(bar_d_full + 8 * b);
+    }
+    if (*abort_flag) {
+      // drain: every MMA issued so far completes before TMEM is released
+      ptx::mma_commit(bar_drain);
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int g_num_sms[64] = {0};
+bool g_attr_set[64] = {false};
+
+}  // namespace
+
+bool igemm_supported(const Geom &g, const char **why) {
+  Plan pl;
+  return make_plan(g, &pl, why);
+}
+
+cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
+                                cudaStream_t stream) {
+  Plan pl;
+  const char *why = "";
+  if (!make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (g_num_sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  if (!g_attr_set[dev]) {
+    e = cudaFuncSetAttribute(igemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e != cudaSuccess) return e;
+    g_attr_set[dev] = true;
+  }
+  IgemmParams p;
+  p.x = x;
+  p.w = w;
+  p.bias = bias;
+  p.y = y;
+  p.g = g;
+  p.osp = (int64_t)g.OD * g.OH * g.OW;
+  p.M_total = g.N * p.osp;
+  p.tiles = (p.M_total + kTileM - 1) / kTileM;
+  p.Kred = pl.Kred;
+  p.Kpad = pl.Kpad;
+  p.Npad = pl.Npad;
+  p.KC = pl.KC;
+  p.nchunks = pl.nchunks;
+  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
+  const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+  igemm_3xtf32_kernel<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t read_and_clear_device_status(unsigned *flags) {
