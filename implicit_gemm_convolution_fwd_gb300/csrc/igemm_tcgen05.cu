@@ -123,6 +123,102 @@ __device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_fl
 
 __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_uint(v) & 0xffffe000u; }
 
+// One producer thread's output position within a tile.
+struct PosInfo {
+  const float *xo;    // x at the receptive field's origin (may lie in the padding)
+  uint32_t dm, hm, wm;  // bit k set: tap k along D / H / W lands inside the input
+  bool valid;           // the position exists (last tile may be partial)
+  bool warp_full;       // every lane's receptive field is entirely inside the input
+};
+
+__device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t tile, int t) {
+  const Geom &g = p.g;
+  PosInfo ps;
+  const int64_t m = tile * kTileM + t;
+  ps.valid = m < p.M_total;
+  int64_t n = 0;
+  int od = 0, oh = 0, ow = 0;
+  if (ps.valid) {
+    const int64_t OHW = (int64_t)g.OH * g.OW;
+    n = m / p.osp;
+    const int64_t pp = m - n * p.osp;
+    od = (int)(pp / OHW);
+    const int rem = (int)(pp - (int64_t)od * OHW);
+    oh = rem / g.OW;
+    ow = rem - oh * g.OW;
+  }
+  const int id0 = od * g.SD - g.PD, ih0 = oh * g.SH - g.PH, iw0 = ow * g.SW - g.PW;
+  uint32_t dm = 0, hm = 0, wm = 0;
+  for (int k = 0; k < g.KD; ++k) dm |= (uint32_t)((unsigned)(id0 + k * g.DD) < (unsigned)g.D) << k;
+  for (int k = 0; k < g.KH; ++k) hm |= (uint32_t)((unsigned)(ih0 + k * g.DH) < (unsigned)g.H) << k;
+  for (int k = 0; k < g.KW; ++k) wm |= (uint32_t)((unsigned)(iw0 + k * g.DW) < (unsigned)g.W) << k;
+  ps.dm = dm;
+  ps.hm = hm;
+  ps.wm = wm;
+  const bool full = ps.valid && dm == (1u << g.KD) - 1u && hm == (1u << g.KH) - 1u && wm == (1u << g.KW) - 1u;
+  ps.warp_full = __all_sync(0xffffffffu, full);
+  const int64_t HW = (int64_t)g.H * g.W;
+  const int64_t xoff = n * g.C * HW * g.D + (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;
+  ps.xo = p.x + (ps.valid ? xoff : 0);
+  return ps;
+}
+
+// 32 consecutive reduction columns of one output position (0 for padded taps).
+__device__ __forceinline__ void gather32(const PosInfo &ps, const uint2 *tb, float (&v)[32]) {
+  if (ps.warp_full) {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint2 e = tb[j];
+      v[j] = (e.y >> 31) ? 0.f : __ldg(ps.xo + (int32_t)e.x);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const uint2 e = tb[j];
+      const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu, kw = (e.y >> 16) & 0xffu;
+      const bool in = ps.valid && !(e.y >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      v[j] = in ? __ldg(ps.xo + (int32_t)e.x) : 0.f;
+    }
+  }
+}
+
+// Prefetch into L2 the input rows that tile `tile` will read: for every output
+// row (n, od, oh) the tile touches and every (c, kd, kh), the span of input
+// columns its positions reach.  Addresses stay inside x.  Run by the 128
+// epilogue threads (t = 0..127) a couple of tiles ahead of the producers.
+__device__ void prefetch_tile_inputs(const IgemmParams &p, int64_t tile, int t) {
+  const Geom &g = p.g;
+  const int64_t m0 = tile * kTileM;
+  if (m0 >= p.M_total) return;
+  const int64_t m1 = min(m0 + kTileM - 1, p.M_total - 1);
+  const int64_t R0 = m0 / g.OW, R1 = m1 / g.OW;  // flattened output rows (n, od, oh)
+  const int per_row = (int)g.C * g.KD * g.KH;
+  const int64_t items = (R1 - R0 + 1) * per_row;
+  const int64_t HW = (int64_t)g.H * g.W;
+  const int64_t ODH = (int64_t)g.OD * g.OH;
+  for (int64_t i = t; i < items; i += kTileM) {
+    const int64_t ri = i / per_row;
+    int rest = (int)(i - ri * per_row);
+    const int c = rest / (g.KD * g.KH);
+    rest -= c * g.KD * g.KH;
+    const int kd = rest / g.KH, kh = rest - kd * g.KH;
+    const int64_t R = R0 + ri;
+    const int64_t n = R / ODH;
+    const int odoh = (int)(R - n * ODH);
+    const int od = odoh / g.OH, oh = odoh - od * g.OH;
+    const int id = od * g.SD - g.PD + kd * g.DD, ih = oh * g.SH - g.PH + kh * g.DH;
+    if ((unsigned)id >= (unsigned)g.D || (unsigned)ih >= (unsigned)g.H) continue;
+    const int owa = (R == R0) ? (int)(m0 - R0 * g.OW) : 0;
+    const int owb = (R == R1) ? (int)(m1 - R1 * g.OW) : g.OW - 1;
+    const int iwa = max(owa * g.SW - g.PW, 0);
+    const int iwb = min(owb * g.SW - g.PW + (g.KW - 1) * g.DW, g.W - 1);
+    if (iwa > iwb) continue;
+    const float *row = p.x + ((n * g.C + c) * g.D + id) * HW + (int64_t)ih * g.W;
+    for (int iw = iwa; iw <= iwb; iw += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + iw));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + iwb));
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -199,9 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    prefetch_tile_inputs(p, (int64_t)blockIdx.x + gridDim.x, tid);
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
       const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
+      prefetch_tile_inputs(p, tile + 2 * (int64_t)gridDim.x, tid);
       bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
@@ -222,86 +320,77 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int o = c0 + j;
-            if (o < g.K) yp[(int64_t)o * p.osp] = __uint_as_float(v[j]) + bias_s[o];
+            if (o < g.K) __stcs(yp + (int64_t)o * p.osp, __uint_as_float(v[j]) + bias_s[o]);
           }
         }
       }
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
+    // The group's work is a sequence of 32-column units: chunks gidx = grp,
+    // grp + 2, ... of the CTA's (tile, chunk) order, each cut into 32-column
+    // slices.  Loads for the next unit are issued before the current unit is
+    // converted and written, and before waiting for the stage to drain, so a
+    // thread always has two units of loads in flight.
     const int grp = (warp - kEpiWarps) >> 2;
     const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * grp);
     const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
-    const uint32_t full_d = (1u << g.KD) - 1u, full_h = (1u << g.KH) - 1u, full_w = (1u << g.KW) - 1u;
-    const int64_t OHW = (int64_t)g.OH * g.OW;
-    int64_t it = 0;
-    bool aborted = false;
-    for (int64_t tile = blockIdx.x; tile < p.tiles && !aborted; tile += gridDim.x, ++it) {
-      const int64_t m = tile * kTileM + t;
-      const bool valid = m < p.M_total;
-      int64_t n = 0;
-      int od = 0, oh = 0, ow = 0;
-      if (valid) {
-        n = m / p.osp;
-        const int64_t pp = m - n * p.osp;
-        od = (int)(pp / OHW);
-        const int rem = (int)(pp - (int64_t)od * OHW);
-        oh = rem / g.OW;
-        ow = rem - oh * g.OW;
-      }
-      const int id0 = od * g.SD - g.PD, ih0 = oh * g.SH - g.PH, iw0 = ow * g.SW - g.PW;
-      uint32_t dm = 0, hm = 0, wm = 0;
-      for (int k = 0; k < g.KD; ++k) dm |= (uint32_t)((unsigned)(id0 + k * g.DD) < (unsigned)g.D) << k;
-      for (int k = 0; k < g.KH; ++k) hm |= (uint32_t)((unsigned)(ih0 + k * g.DH) < (unsigned)g.H) << k;
-      for (int k = 0; k < g.KW; ++k) wm |= (uint32_t)((unsigned)(iw0 + k * g.DW) < (unsigned)g.W) << k;
-      const bool full = valid && dm == full_d && hm == full_h && wm == full_w;
-      const bool warp_full = __all_sync(0xffffffffu, full);
-      // element offset of the receptive field's origin (may lie in the padding)
-      const int64_t xoff = n * g.C * DHW + (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;
-      const float *xo = p.x + (valid ? xoff : 0);
-
-      for (int q = 0; q < p.nchunks; ++q) {
-        const int64_t gidx = it * p.nchunks + q;
-        if ((int)(gidx & 1) != grp) continue;
-        const uint32_t r = (uint32_t)(gidx >> 1);
-        bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
-          aborted = true;
-          break;
+    const int64_t my_tiles = (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const int64_t total_chunks = my_tiles * p.nchunks;
+    int64_t gidx = grp;
+    if (gidx < total_chunks) {
+      int64_t cur_it = gidx / p.nchunks;
+      PosInfo cur = decode_position(p, blockIdx.x + cur_it * gridDim.x, t);
+      int h = 0;
+      float va[32];
+      gather32(cur, table + (int)(gidx - cur_it * p.nchunks) * p.KC, va);
+      for (;;) {
+        const int q = (int)(gidx - cur_it * p.nchunks);
+        const int ncols = min(p.KC, p.Kpad - q * p.KC);
+        // next unit
+        int64_t ngidx = gidx;
+        int nh = h + 32;
+        if (nh >= ncols) {
+          ngidx = gidx + 2;
+          nh = 0;
         }
-        ptx::tc_fence_after();
-        const int k0 = q * p.KC;
-        const int ncols = min(p.KC, p.Kpad - k0);
-        for (int h = 0; h < ncols; h += 32) {
-          const uint2 *tb = table + k0 + h;
-          uint32_t vh[32], vl[32];
-          if (warp_full) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const uint2 e = tb[j];
-              const float v = (e.y >> 31) ? 0.f : __ldg(xo + (int32_t)e.x);
-              vh[j] = tf32_hi_bits(v);
-              vl[j] = __float_as_uint(v - __uint_as_float(vh[j]));
-            }
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const uint2 e = tb[j];
-              const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu, kw = (e.y >> 16) & 0xffu;
-              const bool in = valid && !(e.y >> 31) && (((dm >> kd) & (hm >> kh) & (wm >> kw)) & 1u);
-              const float v = in ? __ldg(xo + (int32_t)e.x) : 0.f;
-              vh[j] = tf32_hi_bits(v);
-              vl[j] = __float_as_uint(v - __uint_as_float(vh[j]));
-            }
-          }
-          ptx::tmem_st32(tmem + lane_base + a_hi_col + (uint32_t)h, vh);
-          ptx::tmem_st32(tmem + lane_base + a_lo_col + (uint32_t)h, vl);
+        const bool has_next = ngidx < total_chunks;
+        const int64_t n_it = ngidx / p.nchunks;
+        PosInfo nxt = cur;
+        if (has_next && n_it != cur_it) nxt = decode_position(p, blockIdx.x + n_it * gridDim.x, t);
+        float vb[32];
+        if (has_next) gather32(nxt, table + (int)(ngidx - n_it * p.nchunks) * p.KC + nh, vb);
+        if (h == 0) {
+          const uint32_t r = (uint32_t)(gidx >> 1);
+          const bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
+          if (!__all_sync(0xffffffffu, ok)) break;
+          ptx::tc_fence_after();
         }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_a_full + 8 * grp);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t tmp[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) tmp[j] = tf32_hi_bits(va[16 * half + j]);
+          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(h + 16 * half), tmp);
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            tmp[j] = __float_as_uint(va[16 * half + j] - __uint_as_float(tf32_hi_bits(va[16 * half + j])));
+          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(h + 16 * half), tmp);
+        }
+        if (h + 32 >= ncols) {
+          ptx::tmem_wait_st();
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_a_full + 8 * grp);
+        }
+        if (!has_next) break;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) va[j] = vb[j];
+        h = nh;
+        gidx = ngidx;
+        cur_it = n_it;
+        cur = nxt;
       }
     }
   } else if (lane == 0) {
