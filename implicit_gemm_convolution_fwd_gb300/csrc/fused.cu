@@ -27,6 +27,8 @@
 namespace convfwd {
 namespace {
 
+__host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+
 constexpr int kCO = 12;  // channels per thread
 constexpr int kR = 4;    // columns per thread
 constexpr int kMaxKW = 7;
@@ -179,6 +181,223 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
   }
 }
 
+// ---------------------------------------------------------------------------
+// Staged variant for the common shape (C_out <= 24, output width <= 32, KW = 3):
+// one persistent CTA per SM owns a contiguous block of (n, oh) output rows
+// (26 at a time, 2 per warp).  The input rows that block needs are streamed
+// through a ring of KD + 1 depth planes in shared memory with cp.async, one
+// plane ahead of the compute, so the FMA loop reads x from shared memory.
+// Lane mapping, register tile (12 channels x 4 columns) and the min / softmax
+// epilogue are the same as above.
+constexpr int kSWarps = 13;
+constexpr int kSThreads = kSWarps * 32;
+constexpr int kSRows = 2 * kSWarps;  // output rows per block
+constexpr int kSNcg = 2;             // 2 x 12 = 24 channel slots
+constexpr int kSMaxSrows = 128;      // shared rows per channel per plane (output rows + halos)
+
+struct StagedParams {
+  const float *__restrict__ x;
+  const float *__restrict__ w;
+  const float *__restrict__ bias;
+  float *__restrict__ y;
+  Geom g;
+  int64_t rows;          // N * OH
+  int WP;                // shared-memory row pitch (floats): W rounded up to 4, plus 4
+  int srows_max;         // shared-memory rows per channel per plane
+  int ring;              // planes in the ring (KD + 1)
+  int vec;               // 16-byte copies are legal
+  uint32_t w_floats;     // weight region size (floats, multiple of 4)
+  uint32_t slot_floats;  // one plane: C * srows_max * WP
+};
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const float *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const float *src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(const StagedParams p) {
+  constexpr int NCH = kSNcg * kCO;  // 24
+  constexpr int NOWG = 8;
+  extern __shared__ __align__(16) float sm[];
+  float *ws = sm;                 // [C*taps][2][12]
+  float *ring = sm + p.w_floats;  // [ring][C][srows_max][WP]
+  __shared__ int64_t srow_src[kSMaxSrows];  // input-row base offset of each shared row
+  __shared__ int nsrows_s;
+
+  const Geom &g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int taps = g.KD * g.KH * 3;
+  const int64_t HW = (int64_t)g.H * g.W;
+
+  for (int i = tid; i < (int)(g.C * taps) * NCH; i += kSThreads) {
+    const int o = i % NCH, ct = i / NCH;
+    ws[i] = o < g.K ? p.w[(int64_t)o * g.C * taps + ct] : 0.f;
+  }
+  // zero the ring once so the row padding never holds stale bits
+  for (uint32_t i = tid; i < (uint32_t)p.ring * p.slot_floats; i += kSThreads) ring[i] = 0.f;
+
+  const int owg = lane & 7, cg = (lane >> 3) & 1, rr = lane >> 4;
+  const int ow0 = owg * 4;
+  const int64_t r_begin = (int64_t)blockIdx.x * p.rows / gridDim.x;
+  const int64_t r_end = (int64_t)(blockIdx.x + 1) * p.rows / gridDim.x;
+  const uint32_t ring_addr = (uint32_t)__cvta_generic_to_shared(ring);
+  const int WQ = p.vec ? g.W / 4 : g.W;  // copy units per row
+
+  for (int64_t r0 = r_begin; r0 < r_end; r0 += kSRows) {
+    const int nrows = (int)min64(kSRows, r_end - r0);
+    const int64_t n0 = r0 / g.OH;
+    __syncthreads();  // the previous block's readers are done with the ring and the row table
+    if (tid == 0) {
+      // shared rows: per image in the block, its output rows plus KH-1 halo rows
+      int srow = 0;
+      for (int lr = 0; lr < nrows;) {
+        const int64_t r = r0 + lr;
+        const int64_t n = r / g.OH;
+        const int oh_lo = (int)(r - n * g.OH);
+        const int cnt = (int)min64(nrows - lr, g.OH - oh_lo);
+        for (int k = 0; k < cnt + g.KH - 1; ++k)
+          srow_src[srow + k] = n * g.C * g.D * HW + (int64_t)(oh_lo + k) * g.W;
+        srow += cnt + g.KH - 1;
+        lr += cnt;
+      }
+      nsrows_s = srow;
+    }
+    __syncthreads();
+    const int nsrows = nsrows_s;
+
+    auto issue_plane = [&](int dd) {
+      const uint32_t slot = ring_addr + 4u * (uint32_t)(dd % p.ring) * p.slot_floats;
+      const int per_c = nsrows * WQ;
+      for (int i = tid; i < (int)g.C * per_c; i += kSThreads) {
+        const int c = i / per_c, rest = i - c * per_c;
+        const int s = rest / WQ, q = rest - s * WQ;
+        const float *src = p.x + srow_src[s] + ((int64_t)c * g.D + dd) * HW;
+        const uint32_t dst = slot + 4u * (uint32_t)((c * p.srows_max + s) * p.WP);
+        if (p.vec)
+          cp_async16(dst + 16u * q, src + 4 * q);
+        else
+          cp_async4(dst + 4u * q, src + q);
+      }
+      cp_async_commit();
+    };
+    for (int dd = 0; dd < g.KD; ++dd) issue_plane(dd);
+
+    // this lane's output row and its shared-memory row
+    const int lr = 2 * warp + rr;
+    const bool row_ok = lr < nrows;
+    const int lrc = row_ok ? lr : nrows - 1;
+    const int64_t rabs = r0 + lrc;
+    const int64_t n = rabs / g.OH;
+    const int oh = (int)(rabs - n * g.OH);
+    const int my_srow = lrc + (g.KH - 1) * (int)(n - n0);
+
+    float mins[kCO][kR];
+#pragma unroll
+    for (int o = 0; o < kCO; ++o)
+#pragma unroll
+      for (int r = 0; r < kR; ++r) mins[o][r] = INFINITY;
+
+    for (int od = 0; od < g.OD; ++od) {
+      cp_async_wait_all();
+      __syncthreads();  // planes od .. od+KD-1 are in shared memory; plane od-1 is free
+      if (od + g.KD < g.D) issue_plane(od + g.KD);
+      float acc[kCO][kR];
+#pragma unroll
+      for (int o = 0; o < kCO; ++o)
+#pragma unroll
+        for (int r = 0; r < kR; ++r) acc[o][r] = 0.f;
+      for (int c = 0; c < g.C; ++c) {
+        for (int kd = 0; kd < g.KD; ++kd) {
+          const float *plane = ring + (size_t)((od + kd) % p.ring) * p.slot_floats +
+                               (size_t)(c * p.srows_max + my_srow) * p.WP + ow0;
+          const float *wrow = ws + ((c * g.KD + kd) * g.KH) * 3 * NCH + cg * kCO;
+#pragma unroll 3
+          for (int kh = 0; kh < g.KH; ++kh) {
+            const float *xr = plane + kh * p.WP;
+            const float4 a = *reinterpret_cast<const float4 *>(xr);
+            const float2 b2 = *reinterpret_cast<const float2 *>(xr + 4);
+            const float xv[6] = {a.x, a.y, a.z, a.w, b2.x, b2.y};
+            const float *wt = wrow + kh * 3 * NCH;
+#pragma unroll
+            for (int kw = 0; kw < 3; ++kw) {
+              const float4 w0 = *reinterpret_cast<const float4 *>(wt + kw * NCH);
+              const float4 w1 = *reinterpret_cast<const float4 *>(wt + kw * NCH + 4);
+              const float4 w2 = *reinterpret_cast<const float4 *>(wt + kw * NCH + 8);
+              const float wv[kCO] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w, w2.x, w2.y, w2.z, w2.w};
+#pragma unroll
+              for (int o = 0; o < kCO; ++o)
+#pragma unroll
+                for (int r = 0; r < kR; ++r) acc[o][r] = fmaf(wv[o], xv[r + kw], acc[o][r]);
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 0; o < kCO; ++o)
+#pragma unroll
+        for (int r = 0; r < kR; ++r) mins[o][r] = fminf(mins[o][r], acc[o][r]);
+    }
+
+    // channel softmax per column; the channel-group partner is lane ^ 8
+    const int64_t OHW = (int64_t)g.OH * g.OW;
+#pragma unroll
+    for (int r = 0; r < kR; ++r) {
+      float v[kCO];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int o = 0; o < kCO; ++o) {
+        const int oc = cg * kCO + o;
+        v[o] = oc < g.K ? mins[o][r] + (p.bias ? __ldg(p.bias + oc) : 0.f) : -INFINITY;
+        mx = fmaxf(mx, v[o]);
+      }
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, NOWG));
+      float ssum = 0.f;
+#pragma unroll
+      for (int o = 0; o < kCO; ++o) {
+        v[o] = expf(v[o] - mx);
+        ssum += v[o];
+      }
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, NOWG);
+      const int ow = ow0 + r;
+      if (row_ok && ow < g.OW) {
+        float *yo = p.y + n * g.K * OHW + (int64_t)oh * g.OW + ow;
+#pragma unroll
+        for (int o = 0; o < kCO; ++o) {
+          const int oc = cg * kCO + o;
+          if (oc < g.K) yo[(int64_t)oc * OHW] = v[o] / ssum;
+        }
+      }
+    }
+  }
+  cp_async_wait_all();
+}
+
+// Shared-memory plan of the staged variant; false when it does not apply.
+bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
+  if (g.K > kSNcg * kCO || g.OW > 32 || g.KW != 3) return false;
+  const int64_t seg = (kSRows - 1) / g.OH + 2;  // images a block of kSRows rows can touch
+  const int64_t srows64 = kSRows + (int64_t)(g.KH - 1) * seg;
+  if (srows64 > kSMaxSrows) return false;
+  const int srows = (int)srows64;
+  const int WP = (g.W + 3) / 4 * 4 + 4;
+  const int64_t w_floats = (int64_t)g.C * g.taps() * kSNcg * kCO;
+  const int64_t slot = (int64_t)g.C * srows * WP;
+  const int ring = g.KD + 1;
+  const int64_t bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot);
+  if (bytes > kMaxSmemBytes) return false;
+  sp->WP = WP;
+  sp->srows_max = srows;
+  sp->ring = ring;
+  sp->vec = (g.W % 4 == 0) && ((((uintptr_t)x) & 15u) == 0);
+  sp->w_floats = (uint32_t)((w_floats + 3) / 4 * 4);
+  sp->slot_floats = (uint32_t)slot;
+  return true;
+}
+
 template <int NCG, int NROW, int KWT, bool VEC>
 cudaError_t launch_t(const FusedParams &p0, cudaStream_t stream) {
   constexpr int NOWG = 32 / (NCG * NROW);
@@ -243,6 +462,27 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
   p.g = g;
   p.rows = g.N * (int64_t)g.OH;
   p.coltiles = 1;
+  StagedParams sp;
+  if (staged_plan(g, x, &sp)) {
+    sp.x = x;
+    sp.w = w;
+    sp.bias = bias;
+    sp.y = y;
+    sp.g = g;
+    sp.rows = p.rows;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const size_t smem = 4 * ((size_t)sp.w_floats + (size_t)sp.ring * sp.slot_floats);
+    e = cudaFuncSetAttribute(fused_min_softmax_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    const int64_t blocks = (p.rows + kSRows - 1) / kSRows;
+    const int grid = (int)(blocks < sms ? blocks : sms);
+    fused_min_softmax_staged_kernel<<<grid, kSThreads, smem, stream>>>(sp);
+    return cudaGetLastError();
+  }
   switch (pick_ncg(g.K)) {
     case 1: return launch_ncg<1, 4>(p, stream);
     case 2: return launch_ncg<2, 2>(p, stream);

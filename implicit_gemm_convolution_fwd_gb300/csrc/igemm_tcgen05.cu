@@ -40,13 +40,16 @@ namespace {
 
 constexpr int kTileM = 128;
 constexpr int kEpiWarps = 4;
-constexpr int kProdGroups = 2;
-constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 12
-constexpr int kThreads = (kMmaWarp + 1) * 32;          // 416
+constexpr int kProdGroups = 4;                         // one TMEM A stage per group
+constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20
+constexpr int kThreads = (kMmaWarp + 1) * 32;          // 672
+constexpr int kUnit = 16;                              // reduction columns per gather / TMEM store
+constexpr int kRowCols = 8;                            // row mode: columns per (c, kd, kh) row
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxNpad = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA per SM, so TMEM allocation never contends
+constexpr int kNumBars = 2 * kProdGroups + 5;
 constexpr long long kWaitLimitCycles = 1ll << 32;  // about two seconds
 
 struct IgemmParams {
@@ -58,22 +61,50 @@ struct IgemmParams {
   int64_t M_total;  // N * OD * OH * OW
   int64_t osp;      // OD * OH * OW
   int64_t tiles;    // ceil(M_total / 128)
-  int Kred;         // C_in * taps
-  int Kpad;         // Kred rounded up to 32
+  int Kred;         // reduction length of w: C_in * taps
+  int Kpad;         // padded reduction length in the GEMM (multiple of 32)
   int Npad;         // C_out rounded up to 32
-  int KC;           // K columns per pipeline chunk (multiple of 32)
+  int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
+  int ntab;         // table entries (Kpad, or Kpad / 8 in row mode)
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
+// Row mode: the reduction is ordered as (c, kd, kh) rows of 8 columns, the
+// last 8 - KW columns of every row carrying zero weights.  A producer then
+// reads one table entry per row and KW consecutive input elements with
+// immediate offsets.  Used when 5 <= KW <= 8 (at most 3/8 padding);
+// otherwise the table holds one entry per reduction column.
 struct Plan {
-  int Kred, Kpad, Npad, KC, nchunks;
+  bool row;
+  int Kred, Kpad, Npad, KC, nchunks, ntab;
   size_t smem;
 };
 
-bool make_plan(const Geom &g, Plan *pl, const char **why) {
+bool make_plan_mode(const Geom &g, bool row, Plan *pl, const char **why) {
   const int64_t taps = (int64_t)g.KD * g.KH * g.KW;
   const int64_t kred = g.C * taps;
+  const int64_t kgemm = row ? g.C * g.KD * g.KH * kRowCols : kred;
+  pl->row = row;
+  pl->Kred = (int)kred;
+  pl->Kpad = (int)((kgemm + 31) / 32 * 32);
+  pl->Npad = (int)((g.K + 31) / 32 * 32);
+  pl->ntab = row ? pl->Kpad / kRowCols : pl->Kpad;
+  int kc = (int)((kTmemCols - 2 * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
+  if (kc > pl->Kpad) kc = pl->Kpad;
+  pl->KC = kc;
+  pl->nchunks = (pl->Kpad + kc - 1) / kc;
+  const size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->ntab * 8 + (size_t)pl->Npad * 4 + 16 +
+                      kNumBars * 8 + 16;
+  if (smem > (size_t)kMaxSmem) {
+    *why = "weights (hi + lo) do not fit in shared memory";
+    return false;
+  }
+  pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
+  return true;
+}
+
+bool make_plan(const Geom &g, Plan *pl, const char **why) {
   if (g.K > kMaxNpad) {
     *why = "C_out above 128";
     return false;
@@ -89,20 +120,8 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
     *why = "receptive-field offsets of one image exceed 2^31 elements";
     return false;
   }
-  pl->Kred = (int)kred;
-  pl->Kpad = (int)((kred + 31) / 32 * 32);
-  pl->Npad = (int)((g.K + 31) / 32 * 32);
-  int kc = (int)((kTmemCols - 2 * pl->Npad) / 4) / 32 * 32;
-  if (kc > pl->Kpad) kc = pl->Kpad;
-  pl->KC = kc;
-  pl->nchunks = (pl->Kpad + kc - 1) / kc;
-  size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 + 9 * 8 + 16;
-  if (smem > (size_t)kMaxSmem) {
-    *why = "weights (hi + lo) do not fit in shared memory";
-    return false;
-  }
-  pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
-  return true;
+  if (g.KW >= 5 && g.KW <= kRowCols && make_plan_mode(g, true, pl, why)) return true;
+  return make_plan_mode(g, false, pl, why);
 }
 
 // Bounded mbarrier wait.  Returns false (and raises the abort flag plus the
@@ -125,7 +144,7 @@ __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_ui
 
 // One producer thread's output position within a tile.
 struct PosInfo {
-  const float *xo;    // x at the receptive field's origin (may lie in the padding)
+  const float *xo;      // x at the receptive field's origin (may lie in the padding)
   uint32_t dm, hm, wm;  // bit k set: tap k along D / H / W lands inside the input
   bool valid;           // the position exists (last tile may be partial)
   bool warp_full;       // every lane's receptive field is entirely inside the input
@@ -163,21 +182,43 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   return ps;
 }
 
-// 32 consecutive reduction columns of one output position (0 for padded taps).
-__device__ __forceinline__ void gather32(const PosInfo &ps, const uint2 *tb, float (&v)[32]) {
+// 16 consecutive reduction columns of one output position (0 for padded taps).
+// Column mode: table entry per column = {input offset, kd | kh<<8 | kw<<16 | pad<<31}.
+__device__ __forceinline__ void gather_cols(const PosInfo &ps, const uint2 *tb, float (&v)[kUnit]) {
   if (ps.warp_full) {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < kUnit; ++j) {
       const uint2 e = tb[j];
       v[j] = (e.y >> 31) ? 0.f : __ldg(ps.xo + (int32_t)e.x);
     }
   } else {
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < kUnit; ++j) {
       const uint2 e = tb[j];
       const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu, kw = (e.y >> 16) & 0xffu;
       const bool in = ps.valid && !(e.y >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
       v[j] = in ? __ldg(ps.xo + (int32_t)e.x) : 0.f;
+    }
+  }
+}
+
+// Row mode: two rows of 8 columns; table entry per row = {input offset of the
+// row's first tap, kd | kh<<8 | pad<<31}.  DW1: unit dilation along W, so the
+// KW taps of a row are consecutive elements.
+template <bool DW1>
+__device__ __forceinline__ void gather_rows(const PosInfo &ps, const uint2 *tb, int KW, int DW,
+                                            float (&v)[kUnit]) {
+#pragma unroll
+  for (int rr = 0; rr < kUnit / kRowCols; ++rr) {
+    const uint2 e = tb[rr];
+    const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu;
+    const bool row_in = ps.warp_full ? !(e.y >> 31)
+                                     : (ps.valid && !(e.y >> 31) && (((ps.dm >> kd) & (ps.hm >> kh)) & 1u));
+    const float *rp = ps.xo + (int32_t)e.x;
+#pragma unroll
+    for (int kw = 0; kw < kRowCols; ++kw) {
+      const bool in = row_in && kw < KW && (ps.warp_full || ((ps.wm >> kw) & 1u));
+      v[rr * kRowCols + kw] = in ? __ldg(rp + (DW1 ? kw : kw * DW)) : 0.f;
     }
   }
 }
@@ -219,6 +260,7 @@ __device__ void prefetch_tile_inputs(const IgemmParams &p, int64_t tile, int t) 
   }
 }
 
+template <bool ROW, bool DW1>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -227,15 +269,15 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   uint8_t *b_hi = smem;
   uint8_t *b_lo = smem + p.b_bytes;
   uint2 *table = reinterpret_cast<uint2 *>(smem + 2 * (size_t)p.b_bytes);
-  float *bias_s = reinterpret_cast<float *>(table + p.Kpad);
+  float *bias_s = reinterpret_cast<float *>(table + p.ntab);
   uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 9);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  const uint32_t bar_a_full = ptx::smem_addr(bars + 0);   // [2]
-  const uint32_t bar_a_empty = ptx::smem_addr(bars + 2);  // [2]
-  const uint32_t bar_d_full = ptx::smem_addr(bars + 4);   // [2]
-  const uint32_t bar_d_empty = ptx::smem_addr(bars + 6);  // [2]
-  const uint32_t bar_drain = ptx::smem_addr(bars + 8);
+  const uint32_t bar_a_full = ptx::smem_addr(bars + 0);                 // [kProdGroups]
+  const uint32_t bar_a_empty = ptx::smem_addr(bars + kProdGroups);      // [kProdGroups]
+  const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kProdGroups);   // [2]
+  const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kProdGroups + 2);  // [2]
+  const uint32_t bar_drain = ptx::smem_addr(bars + 2 * kProdGroups + 4);
 
   const uint32_t SBO = (uint32_t)p.Kpad * 32;  // bytes between 8-row groups of B
   const int taps = g.KD * g.KH * g.KW;
@@ -244,30 +286,41 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   // ---- weights -> shared memory, split into TF32 hi / lo.  Word i of the
   // core-matrix layout holds B[n][k] with n = 8*(cm / (Kpad/4)) + row,
   // k = 4*(cm % (Kpad/4)) + col, so consecutive threads write consecutive
-  // words (conflict-free).
+  // words (conflict-free).  In row mode GEMM column k = 8*r + kw maps to
+  // weight element r*KW + kw (zero for kw >= KW).
   {
     const int kq = p.Kpad / 4;
     const int words = p.Npad * p.Kpad;
     for (int i = tid; i < words; i += kThreads) {
       const int cm = i >> 5, r = (i >> 2) & 7, cw = i & 3;
       const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
-      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kred + k) : 0.f;
+      int kw_idx = k;
+      bool in = k < p.Kred;
+      if (ROW) {
+        const int rowk = k / kRowCols, kw = k - rowk * kRowCols;
+        kw_idx = rowk * g.KW + kw;
+        in = kw < g.KW && kw_idx < p.Kred;
+      }
+      const float v = (n < g.K && in) ? __ldg(p.w + (int64_t)n * p.Kred + kw_idx) : 0.f;
       const float hi = __uint_as_float(tf32_hi_bits(v));
       reinterpret_cast<float *>(b_hi)[i] = hi;
       reinterpret_cast<float *>(b_lo)[i] = v - hi;
     }
-    // ---- reduction index -> (input offset, tap coordinates)
-    for (int kk = tid; kk < p.Kpad; kk += kThreads) {
+    // ---- reduction column (or row) -> (input offset, tap coordinates)
+    const int nent = ROW ? (int)(g.C * g.KD * g.KH) : p.Kred;
+    for (int kk = tid; kk < p.ntab; kk += kThreads) {
       uint2 e;
-      if (kk < p.Kred) {
-        const int c = kk / taps, t = kk - c * taps;
-        const int kd = t / (g.KH * g.KW), r2 = t - kd * g.KH * g.KW;
-        const int kh = r2 / g.KW, kw = r2 - kh * g.KW;
+      if (kk < nent) {
+        const int per_c = ROW ? g.KD * g.KH : taps;
+        const int c = kk / per_c, t = kk - c * per_c;
+        const int kw = ROW ? 0 : t % g.KW;
+        const int khd = ROW ? t : t / g.KW;
+        const int kd = khd / g.KH, kh = khd - kd * g.KH;
         e.x = (uint32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
         e.y = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
       } else {
         e.x = 0;
-        e.y = 0x80000000u;  // padding column: contributes zero
+        e.y = 0x80000000u;  // padding: contributes zero
       }
       table[kk] = e;
     }
@@ -276,11 +329,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   ptx::fence_proxy_async_smem();
   if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
   if (tid == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kProdGroups; ++s) {
       ptx::mbar_init(bar_a_full + 8 * s, 128);
       ptx::mbar_init(bar_a_empty + 8 * s, 1);
-      ptx::mbar_init(bar_d_full + 8 * s, 1);
-      ptx::mbar_init(bar_d_empty + 8 * s, 128);
+    }
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar_d_full + 8 * b, 1);
+      ptx::mbar_init(bar_d_empty + 8 * b, 128);
     }
     ptx::mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -327,11 +382,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
-    // The group's work is a sequence of 32-column units: chunks gidx = grp,
-    // grp + 2, ... of the CTA's (tile, chunk) order, each cut into 32-column
-    // slices.  Loads for the next unit are issued before the current unit is
-    // converted and written, and before waiting for the stage to drain, so a
-    // thread always has two units of loads in flight.
+    // Group `grp` fills TMEM stage `grp` with chunks gidx = grp, grp + G, ...
+    // of the CTA's (tile, chunk) order, kUnit columns at a time.
     const int grp = (warp - kEpiWarps) >> 2;
     const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
@@ -339,59 +391,38 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
     const int64_t my_tiles = (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
     const int64_t total_chunks = my_tiles * p.nchunks;
-    int64_t gidx = grp;
-    if (gidx < total_chunks) {
-      int64_t cur_it = gidx / p.nchunks;
-      PosInfo cur = decode_position(p, blockIdx.x + cur_it * gridDim.x, t);
-      int h = 0;
-      float va[32];
-      gather32(cur, table + (int)(gidx - cur_it * p.nchunks) * p.KC, va);
-      for (;;) {
-        const int q = (int)(gidx - cur_it * p.nchunks);
-        const int ncols = min(p.KC, p.Kpad - q * p.KC);
-        // next unit
-        int64_t ngidx = gidx;
-        int nh = h + 32;
-        if (nh >= ncols) {
-          ngidx = gidx + 2;
-          nh = 0;
-        }
-        const bool has_next = ngidx < total_chunks;
-        const int64_t n_it = ngidx / p.nchunks;
-        PosInfo nxt = cur;
-        if (has_next && n_it != cur_it) nxt = decode_position(p, blockIdx.x + n_it * gridDim.x, t);
-        float vb[32];
-        if (has_next) gather32(nxt, table + (int)(ngidx - n_it * p.nchunks) * p.KC + nh, vb);
-        if (h == 0) {
-          const uint32_t r = (uint32_t)(gidx >> 1);
-          const bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
-          if (!__all_sync(0xffffffffu, ok)) break;
-          ptx::tc_fence_after();
-        }
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t tmp[16];
-#pragma unroll
-          for (int j = 0; j < 16; ++j) tmp[j] = tf32_hi_bits(va[16 * half + j]);
-          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(h + 16 * half), tmp);
-#pragma unroll
-          for (int j = 0; j < 16; ++j)
-            tmp[j] = __float_as_uint(va[16 * half + j] - __uint_as_float(tf32_hi_bits(va[16 * half + j])));
-          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(h + 16 * half), tmp);
-        }
-        if (h + 32 >= ncols) {
-          ptx::tmem_wait_st();
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_a_full + 8 * grp);
-        }
-        if (!has_next) break;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) va[j] = vb[j];
-        h = nh;
-        gidx = ngidx;
-        cur_it = n_it;
-        cur = nxt;
+    int64_t cur_it = -1;
+    PosInfo ps;
+    for (int64_t gidx = grp; gidx < total_chunks; gidx += kProdGroups) {
+      const int64_t it = gidx / p.nchunks;
+      const int q = (int)(gidx - it * p.nchunks);
+      if (it != cur_it) {
+        ps = decode_position(p, blockIdx.x + it * gridDim.x, t);
+        cur_it = it;
       }
+      const int k0 = q * p.KC;
+      const int ncols = min(p.KC, p.Kpad - k0);
+      const uint32_t r = (uint32_t)(gidx / kProdGroups);
+      const bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      for (int h = 0; h < ncols; h += kUnit) {
+        float v[kUnit];
+        if (ROW)
+          gather_rows<DW1>(ps, table + (k0 + h) / kRowCols, g.KW, g.DW, v);
+        else
+          gather_cols(ps, table + k0 + h, v);
+        uint32_t tmp[kUnit];
+#pragma unroll
+        for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[j]);
+        ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)h, tmp);
+#pragma unroll
+        for (int j = 0; j < kUnit; ++j) tmp[j] = __float_as_uint(v[j] - __uint_as_float(tf32_hi_bits(v[j])));
+        ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)h, tmp);
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_a_full + 8 * grp);
     }
   } else if (lane == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -406,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const uint32_t d_tmem = tmem + b * (uint32_t)p.Npad;
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t gidx = it * p.nchunks + q;
-        const uint32_t s = (uint32_t)(gidx & 1), r = (uint32_t)(gidx >> 1);
+        const uint32_t s = (uint32_t)(gidx % kProdGroups), r = (uint32_t)(gidx / kProdGroups);
         if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag)) {
           aborted = true;
           break;
@@ -470,7 +501,14 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     if (e != cudaSuccess) return e;
   }
   if (!g_attr_set[dev]) {
-    e = cudaFuncSetAttribute(igemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMaxSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -488,9 +526,15 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.Npad = pl.Npad;
   p.KC = pl.KC;
   p.nchunks = pl.nchunks;
+  p.ntab = pl.ntab;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-  igemm_3xtf32_kernel<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  if (!pl.row)
+    igemm_3xtf32_kernel<false, false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  else if (g.DW == 1)
+    igemm_3xtf32_kernel<true, true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  else
+    igemm_3xtf32_kernel<true, false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
 

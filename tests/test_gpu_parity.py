@@ -250,3 +250,33 @@ def test_fused_workload_full_size_sampled():
     ref = oracle.conv3d_min_softmax_at(x, w, b, cols)
     assert_close(yc, ref, "fused full size sampled")
     assert torch.allclose(y.sum(dim=1), torch.ones((), device="cuda"), atol=1e-5)
+
+
+# ------------------------------------------- kernel-variant coverage
+
+@pytest.mark.parametrize("kw,dw,pw", [(5, 1, 0), (7, 1, 3), (8, 1, 2), (7, 2, 4), (6, 3, 1)])
+def test_tensor_core_row_mode_widths(kw, dw, pw):
+    # 5 <= KW <= 8 takes the row-ordered reduction on the tensor-core path
+    rng = np.random.default_rng(kw * 100 + dw * 10 + pw)
+    x = rng.standard_normal((2, 5, 6, 7, 41)).astype(np.float32)
+    w = ((rng.random((37, 5, 2, 3, kw)) - 0.5) * 0.3).astype(np.float32)
+    b = rng.standard_normal(37).astype(np.float32)
+    s, p, d = (1, 2, 1), (1, 1, pw), (2, 1, dw)
+    assert cf.algo_supported(2, 5, 37, x.shape[2:], w.shape[2:], s, p, d, cf.CONV_ALGO_IGEMM_3XTF32)
+    ref = oracle.conv_nd(x, w, b, s, p, d)
+    y = run_conv(x, w, b, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32).cpu().numpy()
+    assert_close(y, ref, f"row mode kw={kw} dw={dw} pw={pw}")
+
+
+def test_fused_staged_multi_image_blocks():
+    # output width <= 32, C_out <= 24, KW = 3: the staged kernel; OH = 6 makes a
+    # block of output rows span several images; W = 30 is not a multiple of 4
+    rng = np.random.default_rng(17)
+    for C_out, N in ((13, 5), (24, 9), (1, 3)):
+        x = rng.random((N, 2, 6, 9, 30)).astype(np.float32)
+        w = ((rng.random((C_out, 2, 2, 4, 3)) - 0.5) * 0.5).astype(np.float32)
+        b = ((rng.random(C_out) - 0.5) * 0.5).astype(np.float32)
+        ref = oracle.conv3d_min_softmax(x, w, b)
+        assert_close(run_fused(x, w, b).cpu().numpy(), ref, f"fused staged C_out={C_out} N={N}")
+        assert_close(run_fused(x, w, None).cpu().numpy(), oracle.conv3d_min_softmax(x, w, None),
+                     f"fused staged no bias C_out={C_out}")
