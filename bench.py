@@ -217,6 +217,32 @@ class OurRunner:
         return s.elapsed_time(e) / steps, h2d, hy.numel() * 4
 
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one
+# ncu capture, keyed by (kernel family, workload).  Each entry records the
+# SHA-256 of the kernel's source file at capture time; when the source has
+# changed since, the figure no longer describes the kernel and is reported as
+# null.  "batch" is the batch of the captured case: traffic is scaled by
+# N / batch when the capture used a smaller batch (traffic grows in proportion).
+KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "direct_ffma": "direct.cu", "fused_ffma": "fused.cu"}
+NCU_TRAFFIC = {}
+
+
+def source_sha(algo):
+    import hashlib
+    f = KERNEL_SOURCE.get(algo)
+    if f is None:
+        return None
+    path = os.path.join(ROOT, "implicit_gemm_convolution_fwd_gb300", "csrc", f)
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()
+
+
+def traffic_for(algo, wl):
+    e = NCU_TRAFFIC.get((algo, wl.name.split("[")[0]))
+    if e is None or e["sha256"] != source_sha(algo):
+        return None
+    return e["bytes"] * wl.N / e["batch"]
+
+
 def roofline_for(runner, peaks, ms, sustained=False):
     """Roofline entry for the one kernel a step launches."""
     wl = runner.wl
@@ -234,11 +260,13 @@ def roofline_for(runner, peaks, ms, sustained=False):
     t_mem = bytes_alg / (hbm_peak * 1e9)
     if t_mem > t_compute:
         return {"bound": "hbm", "achieved": bytes_alg / t / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "frac": (bytes_alg / t / 1e9) / hbm_peak, "traffic": None,
+                "frac": (bytes_alg / t / 1e9) / hbm_peak, "traffic": traffic_for(runner.algo, wl),
+                "algorithmic_bytes": bytes_alg,
                 "compute_frac": (flops / t / 1e12) / compute["peak"]}
     ach = flops / t / 1e12
     return {"bound": compute["bound"], "achieved": ach, "peak": compute["peak"], "unit": "TFLOP/s",
-            "frac": ach / compute["peak"], "traffic": None, "peak_note": compute["peak_note"],
+            "frac": ach / compute["peak"], "traffic": traffic_for(runner.algo, wl), "algorithmic_bytes": bytes_alg,
+            "peak_note": compute["peak_note"],
             "hbm_frac": (bytes_alg / t / 1e9) / hbm_peak}
 
 

@@ -223,43 +223,6 @@ __device__ __forceinline__ void gather_rows(const PosInfo &ps, const uint2 *tb, 
   }
 }
 
-// Prefetch into L2 the input rows that tile `tile` will read: for every output
-// row (n, od, oh) the tile touches and every (c, kd, kh), the span of input
-// columns its positions reach.  Addresses stay inside x.  Run by the 128
-// epilogue threads (t = 0..127) a couple of tiles ahead of the producers.
-__device__ void prefetch_tile_inputs(const IgemmParams &p, int64_t tile, int t) {
-  const Geom &g = p.g;
-  const int64_t m0 = tile * kTileM;
-  if (m0 >= p.M_total) return;
-  const int64_t m1 = min(m0 + kTileM - 1, p.M_total - 1);
-  const int64_t R0 = m0 / g.OW, R1 = m1 / g.OW;  // flattened output rows (n, od, oh)
-  const int per_row = (int)g.C * g.KD * g.KH;
-  const int64_t items = (R1 - R0 + 1) * per_row;
-  const int64_t HW = (int64_t)g.H * g.W;
-  const int64_t ODH = (int64_t)g.OD * g.OH;
-  for (int64_t i = t; i < items; i += kTileM) {
-    const int64_t ri = i / per_row;
-    int rest = (int)(i - ri * per_row);
-    const int c = rest / (g.KD * g.KH);
-    rest -= c * g.KD * g.KH;
-    const int kd = rest / g.KH, kh = rest - kd * g.KH;
-    const int64_t R = R0 + ri;
-    const int64_t n = R / ODH;
-    const int odoh = (int)(R - n * ODH);
-    const int od = odoh / g.OH, oh = odoh - od * g.OH;
-    const int id = od * g.SD - g.PD + kd * g.DD, ih = oh * g.SH - g.PH + kh * g.DH;
-    if ((unsigned)id >= (unsigned)g.D || (unsigned)ih >= (unsigned)g.H) continue;
-    const int owa = (R == R0) ? (int)(m0 - R0 * g.OW) : 0;
-    const int owb = (R == R1) ? (int)(m1 - R1 * g.OW) : g.OW - 1;
-    const int iwa = max(owa * g.SW - g.PW, 0);
-    const int iwb = min(owb * g.SW - g.PW + (g.KW - 1) * g.DW, g.W - 1);
-    if (iwa > iwb) continue;
-    const float *row = p.x + ((n * g.C + c) * g.D + id) * HW + (int64_t)ih * g.W;
-    for (int iw = iwa; iw <= iwb; iw += 32) asm volatile("prefetch.global.L2 [%0];" ::"l"(row + iw));
-    asm volatile("prefetch.global.L2 [%0];" ::"l"(row + iwb));
-  }
-}
-
 template <bool ROW, bool DW1>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -350,11 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    prefetch_tile_inputs(p, (int64_t)blockIdx.x + gridDim.x, tid);
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
       const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
-      prefetch_tile_inputs(p, tile + 2 * (int64_t)gridDim.x, tid);
       bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
