@@ -41,15 +41,16 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kEpiWarps = 4;
 constexpr int kProdGroups = 4;                         // one TMEM A stage per group
-constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20
-constexpr int kThreads = (kMmaWarp + 1) * 32;          // 672
+constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20: first of the issuer warps
+constexpr int kIssuers = 3;                            // one per 3xTF32 product
+constexpr int kThreads = (kMmaWarp + kIssuers) * 32;   // 736
 constexpr int kUnit = 16;                              // reduction columns per gather / TMEM store
 constexpr int kRowCols = 8;                            // row mode: columns per (c, kd, kh) row
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxNpad = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA per SM, so TMEM allocation never contends
-constexpr int kNumBars = 2 * kProdGroups + 5;
+constexpr int kNumBars = 2 * kProdGroups + 5;  // a_full[G], a_empty[G], d_full[2], d_empty[2], drain
 constexpr long long kWaitLimitCycles = 1ll << 32;  // about two seconds
 
 struct IgemmParams {
@@ -67,6 +68,7 @@ struct IgemmParams {
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
   int ntab;         // table entries (Kpad, or Kpad / 8 in row mode)
+  int nbuf;         // accumulator sets in TMEM (2: double-buffered)
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
@@ -77,7 +79,7 @@ struct IgemmParams {
 // otherwise the table holds one entry per reduction column.
 struct Plan {
   bool row;
-  int Kred, Kpad, Npad, KC, nchunks, ntab;
+  int Kred, Kpad, Npad, KC, nchunks, ntab, nbuf;
   size_t smem;
 };
 
@@ -90,7 +92,15 @@ bool make_plan_mode(const Geom &g, bool row, Plan *pl, const char **why) {
   pl->Kpad = (int)((kgemm + 31) / 32 * 32);
   pl->Npad = (int)((g.K + 31) / 32 * 32);
   pl->ntab = row ? pl->Kpad / kRowCols : pl->Kpad;
-  int kc = (int)((kTmemCols - 2 * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
+  // TMEM: kIssuers accumulators of Npad columns per buffer, then kProdGroups
+  // A stages of KC hi + KC lo columns.  Double-buffer the accumulators when
+  // that still leaves 32-column stages.
+  pl->nbuf = (2 * kIssuers * pl->Npad + 2 * kProdGroups * 32 <= (int)kTmemCols) ? 2 : 1;
+  int kc = (int)((kTmemCols - kIssuers * pl->nbuf * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
+  if (kc < kUnit) {
+    *why = "tensor memory too small for this C_out";
+    return false;
+  }
   if (kc > pl->Kpad) kc = pl->Kpad;
   pl->KC = kc;
   pl->nchunks = (pl->Kpad + kc - 1) / kc;
@@ -294,13 +304,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   if (tid == 0) {
     for (int s = 0; s < kProdGroups; ++s) {
       ptx::mbar_init(bar_a_full + 8 * s, 128);
-      ptx::mbar_init(bar_a_empty + 8 * s, 1);
+      ptx::mbar_init(bar_a_empty + 8 * s, kIssuers);
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(bar_d_full + 8 * b, 1);
+      ptx::mbar_init(bar_d_full + 8 * b, kIssuers);
       ptx::mbar_init(bar_d_empty + 8 * b, 128);
     }
-    ptx::mbar_init(bar_drain, 1);
+    ptx::mbar_init(bar_drain, kIssuers);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -308,14 +318,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t a_col0 = 2u * p.Npad;  // A stage s: hi at a_col0 + 2*KC*s, lo at + KC
+  // accumulator of product j (0: hi*hi, 1: hi*lo, 2: lo*hi) in buffer b at
+  // column (b * kIssuers + j) * Npad; A stage s: hi at a_col0 + 2*KC*s, lo at + KC
+  const uint32_t a_col0 = (uint32_t)(kIssuers * p.nbuf * p.Npad);
 
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
-      const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
+      const uint32_t b = (uint32_t)(it % p.nbuf), rb = (uint32_t)(it / p.nbuf);
       bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
@@ -324,19 +336,24 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const int64_t n = valid ? m / p.osp : 0;
       const int64_t pp = valid ? m - n * p.osp : 0;
       float *yp = p.y + n * g.K * p.osp + pp;
-      for (int c0 = 0; c0 < p.Npad; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
+      const uint32_t acc0 = tmem + lane_base + b * kIssuers * (uint32_t)p.Npad;
+      for (int c0 = 0; c0 < p.Npad; c0 += 16) {
+        uint32_t hh[16], hl[16], lh[16];
+        ptx::tmem_ld16(acc0 + c0, hh);
+        ptx::tmem_ld16(acc0 + (uint32_t)p.Npad + c0, hl);
+        ptx::tmem_ld16(acc0 + 2u * (uint32_t)p.Npad + c0, lh);
         ptx::tmem_wait_ld();
-        if (c0 + 32 >= p.Npad) {
+        if (c0 + 16 >= p.Npad) {
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar_d_empty + 8 * b);
         }
         if (valid) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
+          for (int j = 0; j < 16; ++j) {
             const int o = c0 + j;
-            if (o < g.K) __stcs(yp + (int64_t)o * p.osp, __uint_as_float(v[j]) + bias_s[o]);
+            // small correction terms first, then the main product and the bias
+            const float v = (__uint_as_float(hl[j]) + __uint_as_float(lh[j])) + __uint_as_float(hh[j]);
+            if (o < g.K) __stcs(yp + (int64_t)o * p.osp, v + bias_s[o]);
           }
         }
       }
@@ -386,16 +403,22 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::mbar_arrive(bar_a_full + 8 * grp);
     }
   } else if (lane == 0) {
-    // ------------------------------------------------------------ MMA issuer
+    // ------------------------------------------------------------ MMA issuers
+    // Issuer j (one thread per warp kMmaWarp + j) accumulates one of the three
+    // products over the whole reduction into its own accumulator, so the three
+    // instruction streams proceed in parallel: one thread cannot issue a
+    // tcgen05.mma much faster than one per ~140 cycles.
+    const int j = warp - kMmaWarp;
     const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
-    const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
+    const uint32_t bsm = ptx::smem_addr(j == 1 ? b_lo : b_hi);  // hi*lo uses B_lo
+    const uint32_t a_off = j == 2 ? (uint32_t)p.KC : 0u;          // lo*hi uses A_lo
     int64_t it = 0;
     bool aborted = false;
     for (int64_t tile = blockIdx.x; tile < p.tiles && !aborted; tile += gridDim.x, ++it) {
-      const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
+      const uint32_t b = (uint32_t)(it % p.nbuf), rb = (uint32_t)(it / p.nbuf);
       if (!wait_phase(bar_d_empty + 8 * b, (rb & 1) ^ 1, abort_flag)) break;
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem + b * (uint32_t)p.Npad;
+      const uint32_t d_tmem = tmem + (b * kIssuers + (uint32_t)j) * (uint32_t)p.Npad;
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t gidx = it * p.nchunks + q;
         const uint32_t s = (uint32_t)(gidx % kProdGroups), r = (uint32_t)(gidx / kProdGroups);
@@ -404,17 +427,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t a_hi = tmem + a_col0 + 2u * (uint32_t)p.KC * s;
-        const uint32_t a_lo = a_hi + (uint32_t)p.KC;
+        const uint32_t a = tmem + a_col0 + 2u * (uint32_t)p.KC * s + a_off;
         const int k0 = q * p.KC;
         const int ksteps = min(p.KC, p.Kpad - k0) / 8;
         for (int ks = 0; ks < ksteps; ++ks) {
           const uint32_t kbyte = (uint32_t)(k0 + ks * 8) * 32u;  // (k/4) core matrices of 128 B
-          const uint64_t dh = ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
-          const uint64_t dl = ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
-          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (q | ks) != 0);
-          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
-          ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
+          const uint64_t bd = ptx::smem_desc_noswizzle(bsm + kbyte, 128, SBO);
+          ptx::mma_tf32_ts(d_tmem, a + 8 * ks, bd, idesc, (q | ks) != 0);
         }
         ptx::mma_commit(bar_a_empty + 8 * s);
       }
@@ -422,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::mma_commit(bar_d_full + 8 * b);
     }
     if (*abort_flag) {
-      // drain: every MMA issued so far completes before TMEM is released
+      // drain: every MMA this thread issued completes before TMEM is released
       ptx::mma_commit(bar_drain);
       const long long t0 = clock64();
       while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
@@ -488,6 +507,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.KC = pl.KC;
   p.nchunks = pl.nchunks;
   p.ntab = pl.ntab;
+  p.nbuf = pl.nbuf;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
   if (!pl.row)
