@@ -41,9 +41,10 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kEpiWarps = 4;
 constexpr int kProdGroups = 4;                         // one TMEM A stage per group
-constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20: first of the issuer warps
-constexpr int kIssuers = 3;                            // one per 3xTF32 product
-constexpr int kThreads = (kMmaWarp + kIssuers) * 32;   // 736
+constexpr int kSlots = 2;                              // tile pipelines; consecutive tiles alternate
+constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20: first of the issuer warps (one per slot)
+constexpr int kThreads = (kMmaWarp + kSlots) * 32;     // 704
+constexpr int kChunkMax = 32;                          // K columns per chunk (registers hold one chunk)
 constexpr int kUnit = 16;                              // reduction columns per gather / TMEM store
 constexpr int kRowCols = 8;                            // row mode: columns per (c, kd, kh) row
 constexpr uint32_t kTmemCols = 512;
@@ -68,7 +69,6 @@ struct IgemmParams {
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
   int ntab;         // table entries (Kpad, or Kpad / 8 in row mode)
-  int nbuf;         // accumulator sets in TMEM (2: double-buffered)
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
@@ -79,7 +79,7 @@ struct IgemmParams {
 // otherwise the table holds one entry per reduction column.
 struct Plan {
   bool row;
-  int Kred, Kpad, Npad, KC, nchunks, ntab, nbuf;
+  int Kred, Kpad, Npad, KC, nchunks, ntab;
   size_t smem;
 };
 
@@ -92,15 +92,10 @@ bool make_plan_mode(const Geom &g, bool row, Plan *pl, const char **why) {
   pl->Kpad = (int)((kgemm + 31) / 32 * 32);
   pl->Npad = (int)((g.K + 31) / 32 * 32);
   pl->ntab = row ? pl->Kpad / kRowCols : pl->Kpad;
-  // TMEM: kIssuers accumulators of Npad columns per buffer, then kProdGroups
-  // A stages of KC hi + KC lo columns.  Double-buffer the accumulators when
-  // that still leaves 32-column stages.
-  pl->nbuf = (2 * kIssuers * pl->Npad + 2 * kProdGroups * 32 <= (int)kTmemCols) ? 2 : 1;
-  int kc = (int)((kTmemCols - kIssuers * pl->nbuf * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
-  if (kc < kUnit) {
-    *why = "tensor memory too small for this C_out";
-    return false;
-  }
+  // TMEM: one accumulator of Npad columns per slot, then kProdGroups A stages
+  // of KC hi + KC lo columns.
+  int kc = (int)((kTmemCols - kSlots * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
+  if (kc > kChunkMax) kc = kChunkMax;
   if (kc > pl->Kpad) kc = pl->Kpad;
   pl->KC = kc;
   pl->nchunks = (pl->Kpad + kc - 1) / kc;
@@ -304,13 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   if (tid == 0) {
     for (int s = 0; s < kProdGroups; ++s) {
       ptx::mbar_init(bar_a_full + 8 * s, 128);
-      ptx::mbar_init(bar_a_empty + 8 * s, kIssuers);
+      ptx::mbar_init(bar_a_empty + 8 * s, 1);
     }
     for (int b = 0; b < 2; ++b) {
-      ptx::mbar_init(bar_d_full + 8 * b, kIssuers);
+      ptx::mbar_init(bar_d_full + 8 * b, 1);
       ptx::mbar_init(bar_d_empty + 8 * b, 128);
     }
-    ptx::mbar_init(bar_drain, kIssuers);
+    ptx::mbar_init(bar_drain, kSlots);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -318,16 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // accumulator of product j (0: hi*hi, 1: hi*lo, 2: lo*hi) in buffer b at
-  // column (b * kIssuers + j) * Npad; A stage s: hi at a_col0 + 2*KC*s, lo at + KC
-  const uint32_t a_col0 = (uint32_t)(kIssuers * p.nbuf * p.Npad);
+  // slot b's accumulator at column b * Npad; A stage s: hi at a_col0 + 2*KC*s, lo at + KC.
+  // Slot b owns stages 2b and 2b + 1 and producer groups 2b and 2b + 1.
+  const uint32_t a_col0 = (uint32_t)(kSlots * p.Npad);
 
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     int64_t it = 0;
     for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
-      const uint32_t b = (uint32_t)(it % p.nbuf), rb = (uint32_t)(it / p.nbuf);
+      const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
       bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
@@ -336,67 +331,75 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const int64_t n = valid ? m / p.osp : 0;
       const int64_t pp = valid ? m - n * p.osp : 0;
       float *yp = p.y + n * g.K * p.osp + pp;
-      const uint32_t acc0 = tmem + lane_base + b * kIssuers * (uint32_t)p.Npad;
-      for (int c0 = 0; c0 < p.Npad; c0 += 16) {
-        uint32_t hh[16], hl[16], lh[16];
-        ptx::tmem_ld16(acc0 + c0, hh);
-        ptx::tmem_ld16(acc0 + (uint32_t)p.Npad + c0, hl);
-        ptx::tmem_ld16(acc0 + 2u * (uint32_t)p.Npad + c0, lh);
+      for (int c0 = 0; c0 < p.Npad; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
         ptx::tmem_wait_ld();
-        if (c0 + 16 >= p.Npad) {
+        if (c0 + 32 >= p.Npad) {
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar_d_empty + 8 * b);
         }
         if (valid) {
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
+          for (int j = 0; j < 32; ++j) {
             const int o = c0 + j;
-            // small correction terms first, then the main product and the bias
-            const float v = (__uint_as_float(hl[j]) + __uint_as_float(lh[j])) + __uint_as_float(hh[j]);
-            if (o < g.K) __stcs(yp + (int64_t)o * p.osp, v + bias_s[o]);
+            if (o < g.K) __stcs(yp + (int64_t)o * p.osp, __uint_as_float(v[j]) + bias_s[o]);
           }
         }
       }
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
-    // Group `grp` fills TMEM stage `grp` with chunks gidx = grp, grp + G, ...
-    // of the CTA's (tile, chunk) order, kUnit columns at a time.
+    // Group g serves slot b = g / 2 (the CTA's tiles it = b, b + 2, ...) and
+    // fills stage g with every other chunk of that slot's sequence.  A
+    // chunk's loads are issued before waiting for the stage to drain.
     const int grp = (warp - kEpiWarps) >> 2;
+    const int slot = grp >> 1, sel = grp & 1;
     const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * grp);
     const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
     const int64_t my_tiles = (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
-    const int64_t total_chunks = my_tiles * p.nchunks;
-    int64_t cur_it = -1;
+    const int64_t slot_tiles = (my_tiles - slot + 1) / 2;  // tiles it = slot, slot + 2, ... < my_tiles
+    const int64_t total = slot_tiles * p.nchunks;          // chunks of this slot
+    int64_t cur_li = -1;
     PosInfo ps;
-    for (int64_t gidx = grp; gidx < total_chunks; gidx += kProdGroups) {
-      const int64_t it = gidx / p.nchunks;
-      const int q = (int)(gidx - it * p.nchunks);
-      if (it != cur_it) {
-        ps = decode_position(p, blockIdx.x + it * gridDim.x, t);
-        cur_it = it;
+    for (int64_t lg = sel; lg < total; lg += 2) {
+      const int64_t li = lg / p.nchunks;
+      const int q = (int)(lg - li * p.nchunks);
+      if (li != cur_li) {
+        ps = decode_position(p, blockIdx.x + (2 * li + slot) * gridDim.x, t);
+        cur_li = li;
       }
       const int k0 = q * p.KC;
       const int ncols = min(p.KC, p.Kpad - k0);
-      const uint32_t r = (uint32_t)(gidx / kProdGroups);
+      float v[kChunkMax];
+#pragma unroll
+      for (int u = 0; u < kChunkMax / kUnit; ++u) {
+        if (u * kUnit < ncols) {
+          float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
+          if (ROW)
+            gather_rows<DW1>(ps, table + (k0 + u * kUnit) / kRowCols, g.KW, g.DW, vu);
+          else
+            gather_cols(ps, table + k0 + u * kUnit, vu);
+        }
+      }
+      const uint32_t r = (uint32_t)(lg >> 1);
       const bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
-      for (int h = 0; h < ncols; h += kUnit) {
-        float v[kUnit];
-        if (ROW)
-          gather_rows<DW1>(ps, table + (k0 + h) / kRowCols, g.KW, g.DW, v);
-        else
-          gather_cols(ps, table + k0 + h, v);
-        uint32_t tmp[kUnit];
 #pragma unroll
-        for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[j]);
-        ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)h, tmp);
+      for (int u = 0; u < kChunkMax / kUnit; ++u) {
+        if (u * kUnit < ncols) {
+          uint32_t tmp[kUnit];
 #pragma unroll
-        for (int j = 0; j < kUnit; ++j) tmp[j] = __float_as_uint(v[j] - __uint_as_float(tf32_hi_bits(v[j])));
-        ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)h, tmp);
+          for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
+          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
+#pragma unroll
+          for (int j = 0; j < kUnit; ++j)
+            tmp[j] = __float_as_uint(v[u * kUnit + j] - __uint_as_float(tf32_hi_bits(v[u * kUnit + j])));
+          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
+        }
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
@@ -404,41 +407,43 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     }
   } else if (lane == 0) {
     // ------------------------------------------------------------ MMA issuers
-    // Issuer j (one thread per warp kMmaWarp + j) accumulates one of the three
-    // products over the whole reduction into its own accumulator, so the three
-    // instruction streams proceed in parallel: one thread cannot issue a
-    // tcgen05.mma much faster than one per ~140 cycles.
-    const int j = warp - kMmaWarp;
+    // One thread per slot: a thread cannot issue a tcgen05.mma much faster
+    // than one per ~140 cycles, so two slots keep two instruction streams
+    // (two tiles) in flight.  Per K-step: D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi.
+    const int slot = warp - kMmaWarp;
     const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
-    const uint32_t bsm = ptx::smem_addr(j == 1 ? b_lo : b_hi);  // hi*lo uses B_lo
-    const uint32_t a_off = j == 2 ? (uint32_t)p.KC : 0u;          // lo*hi uses A_lo
-    int64_t it = 0;
+    const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
+    const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
+    const int64_t my_tiles = (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
     bool aborted = false;
-    for (int64_t tile = blockIdx.x; tile < p.tiles && !aborted; tile += gridDim.x, ++it) {
-      const uint32_t b = (uint32_t)(it % p.nbuf), rb = (uint32_t)(it / p.nbuf);
-      if (!wait_phase(bar_d_empty + 8 * b, (rb & 1) ^ 1, abort_flag)) break;
+    for (int64_t it = slot; it < my_tiles && !aborted; it += 2) {
+      const int64_t li = it >> 1;
+      if (!wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag)) break;
       ptx::tc_fence_after();
-      const uint32_t d_tmem = tmem + (b * kIssuers + (uint32_t)j) * (uint32_t)p.Npad;
       for (int q = 0; q < p.nchunks; ++q) {
-        const int64_t gidx = it * p.nchunks + q;
-        const uint32_t s = (uint32_t)(gidx % kProdGroups), r = (uint32_t)(gidx / kProdGroups);
+        const int64_t lg = li * p.nchunks + q;
+        const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
         if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag)) {
           aborted = true;
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t a = tmem + a_col0 + 2u * (uint32_t)p.KC * s + a_off;
+        const uint32_t a_hi = tmem + a_col0 + 2u * (uint32_t)p.KC * s;
+        const uint32_t a_lo = a_hi + (uint32_t)p.KC;
         const int k0 = q * p.KC;
         const int ksteps = min(p.KC, p.Kpad - k0) / 8;
         for (int ks = 0; ks < ksteps; ++ks) {
           const uint32_t kbyte = (uint32_t)(k0 + ks * 8) * 32u;  // (k/4) core matrices of 128 B
-          const uint64_t bd = ptx::smem_desc_noswizzle(bsm + kbyte, 128, SBO);
-          ptx::mma_tf32_ts(d_tmem, a + 8 * ks, bd, idesc, (q | ks) != 0);
+          const uint64_t dh = ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
+          const uint64_t dl = ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
+          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (q | ks) != 0);
+          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
+          ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
         }
         ptx::mma_commit(bar_a_empty + 8 * s);
       }
       if (aborted) break;
-      ptx::mma_commit(bar_d_full + 8 * b);
+      ptx::mma_commit(bar_d_full + 8 * slot);
     }
     if (*abort_flag) {
       // drain: every MMA this thread issued completes before TMEM is released
@@ -507,7 +512,6 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.KC = pl.KC;
   p.nchunks = pl.nchunks;
   p.ntab = pl.ntab;
-  p.nbuf = pl.nbuf;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
   if (!pl.row)
