@@ -184,15 +184,17 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
 // ---------------------------------------------------------------------------
 // Staged variant for the common shape (C_out <= 24, output width <= 32, KW = 3):
 // one persistent CTA per SM owns a contiguous block of (n, oh) output rows
-// (26 at a time, 2 per warp).  The input rows that block needs are streamed
+// (26 at a time, one per warp).  The input rows that block needs are streamed
 // through a ring of KD + 1 depth planes in shared memory with cp.async, one
 // plane ahead of the compute, so the FMA loop reads x from shared memory.
-// Lane mapping, register tile (12 channels x 4 columns) and the min / softmax
-// epilogue are the same as above.
-constexpr int kSWarps = 13;
+// A lane holds 6 channels x 4 columns (lane = channel group x column group),
+// which keeps registers low enough for 26 warps per SM to hide shared-memory
+// latency; the min / softmax epilogue is as above.
+constexpr int kSWarps = 26;
 constexpr int kSThreads = kSWarps * 32;
-constexpr int kSRows = 2 * kSWarps;  // output rows per block
-constexpr int kSNcg = 2;             // 2 x 12 = 24 channel slots
+constexpr int kSRows = kSWarps;      // output rows per block
+constexpr int kSCO = 6;              // channels per lane
+constexpr int kSNcg = 4;             // 4 x 6 = 24 channel slots
 constexpr int kSMaxSrows = 128;      // shared rows per channel per plane (output rows + halos)
 
 struct StagedParams {
@@ -220,10 +222,10 @@ __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commi
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(const StagedParams p) {
-  constexpr int NCH = kSNcg * kCO;  // 24
+  constexpr int NCH = kSNcg * kSCO;  // 24
   constexpr int NOWG = 8;
   extern __shared__ __align__(16) float sm[];
-  float *ws = sm;                 // [C*taps][2][12]
+  float *ws = sm;                 // [C*taps][4][6]
   float *ring = sm + p.w_floats;  // [ring][C][srows_max][WP]
   __shared__ int64_t srow_src[kSMaxSrows];  // input-row base offset of each shared row
   __shared__ int nsrows_s;
@@ -240,7 +242,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
   // zero the ring once so the row padding never holds stale bits
   for (uint32_t i = tid; i < (uint32_t)p.ring * p.slot_floats; i += kSThreads) ring[i] = 0.f;
 
-  const int owg = lane & 7, cg = (lane >> 3) & 1, rr = lane >> 4;
+  const int owg = lane & 7, cg = lane >> 3;
   const int ow0 = owg * 4;
   const int64_t r_begin = (int64_t)blockIdx.x * p.rows / gridDim.x;
   const int64_t r_end = (int64_t)(blockIdx.x + 1) * p.rows / gridDim.x;
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     for (int dd = 0; dd < g.KD; ++dd) issue_plane(dd);
 
     // this lane's output row and its shared-memory row
-    const int lr = 2 * warp + rr;
+    const int lr = warp;
     const bool row_ok = lr < nrows;
     const int lrc = row_ok ? lr : nrows - 1;
     const int64_t rabs = r0 + lrc;
@@ -295,9 +297,9 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     const int oh = (int)(rabs - n * g.OH);
     const int my_srow = lrc + (g.KH - 1) * (int)(n - n0);
 
-    float mins[kCO][kR];
+    float mins[kSCO][kR];
 #pragma unroll
-    for (int o = 0; o < kCO; ++o)
+    for (int o = 0; o < kSCO; ++o)
 #pragma unroll
       for (int r = 0; r < kR; ++r) mins[o][r] = INFINITY;
 
@@ -305,16 +307,16 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       cp_async_wait_all();
       __syncthreads();  // planes od .. od+KD-1 are in shared memory; plane od-1 is free
       if (od + g.KD < g.D) issue_plane(od + g.KD);
-      float acc[kCO][kR];
+      float acc[kSCO][kR];
 #pragma unroll
-      for (int o = 0; o < kCO; ++o)
+      for (int o = 0; o < kSCO; ++o)
 #pragma unroll
         for (int r = 0; r < kR; ++r) acc[o][r] = 0.f;
       for (int c = 0; c < g.C; ++c) {
         for (int kd = 0; kd < g.KD; ++kd) {
           const float *plane = ring + (size_t)((od + kd) % p.ring) * p.slot_floats +
                                (size_t)(c * p.srows_max + my_srow) * p.WP + ow0;
-          const float *wrow = ws + ((c * g.KD + kd) * g.KH) * 3 * NCH + cg * kCO;
+          const float *wrow = ws + ((c * g.KD + kd) * g.KH) * 3 * NCH + cg * kSCO;
 #pragma unroll 3
           for (int kh = 0; kh < g.KH; ++kh) {
             const float *xr = plane + kh * p.WP;
@@ -324,12 +326,12 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
             const float *wt = wrow + kh * 3 * NCH;
 #pragma unroll
             for (int kw = 0; kw < 3; ++kw) {
-              const float4 w0 = *reinterpret_cast<const float4 *>(wt + kw * NCH);
-              const float4 w1 = *reinterpret_cast<const float4 *>(wt + kw * NCH + 4);
-              const float4 w2 = *reinterpret_cast<const float4 *>(wt + kw * NCH + 8);
-              const float wv[kCO] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w, w2.x, w2.y, w2.z, w2.w};
+              const float2 w0 = *reinterpret_cast<const float2 *>(wt + kw * NCH);
+              const float2 w1 = *reinterpret_cast<const float2 *>(wt + kw * NCH + 2);
+              const float2 w2 = *reinterpret_cast<const float2 *>(wt + kw * NCH + 4);
+              const float wv[kSCO] = {w0.x, w0.y, w1.x, w1.y, w2.x, w2.y};
 #pragma unroll
-              for (int o = 0; o < kCO; ++o)
+              for (int o = 0; o < kSCO; ++o)
 #pragma unroll
                 for (int r = 0; r < kR; ++r) acc[o][r] = fmaf(wv[o], xv[r + kw], acc[o][r]);
             }
@@ -337,37 +339,39 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
         }
       }
 #pragma unroll
-      for (int o = 0; o < kCO; ++o)
+      for (int o = 0; o < kSCO; ++o)
 #pragma unroll
         for (int r = 0; r < kR; ++r) mins[o][r] = fminf(mins[o][r], acc[o][r]);
     }
 
-    // channel softmax per column; the channel-group partner is lane ^ 8
+    // channel softmax per column across the 4 channel-group lanes (xor 8, 16)
     const int64_t OHW = (int64_t)g.OH * g.OW;
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
-      float v[kCO];
+      float v[kSCO];
       float mx = -INFINITY;
 #pragma unroll
-      for (int o = 0; o < kCO; ++o) {
-        const int oc = cg * kCO + o;
+      for (int o = 0; o < kSCO; ++o) {
+        const int oc = cg * kSCO + o;
         v[o] = oc < g.K ? mins[o][r] + (p.bias ? __ldg(p.bias + oc) : 0.f) : -INFINITY;
         mx = fmaxf(mx, v[o]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, NOWG));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2 * NOWG));
       float ssum = 0.f;
 #pragma unroll
-      for (int o = 0; o < kCO; ++o) {
+      for (int o = 0; o < kSCO; ++o) {
         v[o] = expf(v[o] - mx);
         ssum += v[o];
       }
       ssum += __shfl_xor_sync(0xffffffffu, ssum, NOWG);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2 * NOWG);
       const int ow = ow0 + r;
       if (row_ok && ow < g.OW) {
         float *yo = p.y + n * g.K * OHW + (int64_t)oh * g.OW + ow;
 #pragma unroll
-        for (int o = 0; o < kCO; ++o) {
-          const int oc = cg * kCO + o;
+        for (int o = 0; o < kSCO; ++o) {
+          const int oc = cg * kSCO + o;
           if (oc < g.K) yo[(int64_t)oc * OHW] = v[o] / ssum;
         }
       }
@@ -378,13 +382,13 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 
 // Shared-memory plan of the staged variant; false when it does not apply.
 bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
-  if (g.K > kSNcg * kCO || g.OW > 32 || g.KW != 3) return false;
+  if (g.K > kSNcg * kSCO || g.OW > 32 || g.KW != 3) return false;
   const int64_t seg = (kSRows - 1) / g.OH + 2;  // images a block of kSRows rows can touch
   const int64_t srows64 = kSRows + (int64_t)(g.KH - 1) * seg;
   if (srows64 > kSMaxSrows) return false;
   const int srows = (int)srows64;
   const int WP = (g.W + 3) / 4 * 4 + 4;
-  const int64_t w_floats = (int64_t)g.C * g.taps() * kSNcg * kCO;
+  const int64_t w_floats = (int64_t)g.C * g.taps() * kSNcg * kSCO;
   const int64_t slot = (int64_t)g.C * srows * WP;
   const int ring = g.KD + 1;
   const int64_t bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot);

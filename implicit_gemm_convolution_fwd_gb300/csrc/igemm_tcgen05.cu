@@ -46,7 +46,6 @@ constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20: first of the issue
 constexpr int kThreads = (kMmaWarp + kSlots) * 32;     // 704
 constexpr int kChunkMax = 32;                          // K columns per chunk (registers hold one chunk)
 constexpr int kUnit = 16;                              // reduction columns per gather / TMEM store
-constexpr int kRowCols = 8;                            // row mode: columns per (c, kd, kh) row
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxNpad = 128;
 constexpr int kMaxSmem = 227 * 1024;
@@ -68,46 +67,13 @@ struct IgemmParams {
   int Npad;         // C_out rounded up to 32
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
-  int ntab;         // table entries (Kpad, or Kpad / 8 in row mode)
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
-// Row mode: the reduction is ordered as (c, kd, kh) rows of 8 columns, the
-// last 8 - KW columns of every row carrying zero weights.  A producer then
-// reads one table entry per row and KW consecutive input elements with
-// immediate offsets.  Used when 5 <= KW <= 8 (at most 3/8 padding);
-// otherwise the table holds one entry per reduction column.
 struct Plan {
-  bool row;
-  int Kred, Kpad, Npad, KC, nchunks, ntab;
+  int Kred, Kpad, Npad, KC, nchunks;
   size_t smem;
 };
-
-bool make_plan_mode(const Geom &g, bool row, Plan *pl, const char **why) {
-  const int64_t taps = (int64_t)g.KD * g.KH * g.KW;
-  const int64_t kred = g.C * taps;
-  const int64_t kgemm = row ? g.C * g.KD * g.KH * kRowCols : kred;
-  pl->row = row;
-  pl->Kred = (int)kred;
-  pl->Kpad = (int)((kgemm + 31) / 32 * 32);
-  pl->Npad = (int)((g.K + 31) / 32 * 32);
-  pl->ntab = row ? pl->Kpad / kRowCols : pl->Kpad;
-  // TMEM: one accumulator of Npad columns per slot, then kProdGroups A stages
-  // of KC hi + KC lo columns.
-  int kc = (int)((kTmemCols - kSlots * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
-  if (kc > kChunkMax) kc = kChunkMax;
-  if (kc > pl->Kpad) kc = pl->Kpad;
-  pl->KC = kc;
-  pl->nchunks = (pl->Kpad + kc - 1) / kc;
-  const size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->ntab * 8 + (size_t)pl->Npad * 4 + 16 +
-                      kNumBars * 8 + 16;
-  if (smem > (size_t)kMaxSmem) {
-    *why = "weights (hi + lo) do not fit in shared memory";
-    return false;
-  }
-  pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
-  return true;
-}
 
 bool make_plan(const Geom &g, Plan *pl, const char **why) {
   if (g.K > kMaxNpad) {
@@ -125,8 +91,34 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
     *why = "receptive-field offsets of one image exceed 2^31 elements";
     return false;
   }
-  if (g.KW >= 5 && g.KW <= kRowCols && make_plan_mode(g, true, pl, why)) return true;
-  return make_plan_mode(g, false, pl, why);
+  const int64_t kred = g.C * (int64_t)g.KD * g.KH * g.KW;
+  pl->Kred = (int)kred;
+  pl->Kpad = (int)((kred + 31) / 32 * 32);
+  pl->Npad = (int)((g.K + 31) / 32 * 32);
+  // TMEM: one accumulator of Npad columns per slot, then kProdGroups A stages
+  // of KC hi + KC lo columns.
+  int kc = (int)((kTmemCols - kSlots * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
+  if (kc > kChunkMax) kc = kChunkMax;
+  if (kc > pl->Kpad) kc = pl->Kpad;
+  pl->KC = kc;
+  pl->nchunks = (pl->Kpad + kc - 1) / kc;
+  const size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 +
+                      kNumBars * 8 + 16;
+  if (smem > (size_t)kMaxSmem) {
+    *why = "weights (hi + lo) do not fit in shared memory";
+    return false;
+  }
+  pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
+  return true;
+}
+
+// The CTA's tile order: its it-th tile (it = 0, 1, ...) is tile_of(p, it),
+// cyclic over the grid so that all SMs sweep the output together.
+__device__ __forceinline__ int64_t tile_of(const IgemmParams &p, int64_t it) {
+  return blockIdx.x + it * (int64_t)gridDim.x;
+}
+__device__ __forceinline__ int64_t cta_tile_count(const IgemmParams &p) {
+  return (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
 }
 
 // Bounded mbarrier wait.  Returns false (and raises the abort flag plus the
@@ -207,28 +199,6 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const uint2 *tb, 
   }
 }
 
-// Row mode: two rows of 8 columns; table entry per row = {input offset of the
-// row's first tap, kd | kh<<8 | pad<<31}.  DW1: unit dilation along W, so the
-// KW taps of a row are consecutive elements.
-template <bool DW1>
-__device__ __forceinline__ void gather_rows(const PosInfo &ps, const uint2 *tb, int KW, int DW,
-                                            float (&v)[kUnit]) {
-#pragma unroll
-  for (int rr = 0; rr < kUnit / kRowCols; ++rr) {
-    const uint2 e = tb[rr];
-    const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu;
-    const bool row_in = ps.warp_full ? !(e.y >> 31)
-                                     : (ps.valid && !(e.y >> 31) && (((ps.dm >> kd) & (ps.hm >> kh)) & 1u));
-    const float *rp = ps.xo + (int32_t)e.x;
-#pragma unroll
-    for (int kw = 0; kw < kRowCols; ++kw) {
-      const bool in = row_in && kw < KW && (ps.warp_full || ((ps.wm >> kw) & 1u));
-      v[rr * kRowCols + kw] = in ? __ldg(rp + (DW1 ? kw : kw * DW)) : 0.f;
-    }
-  }
-}
-
-template <bool ROW, bool DW1>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -237,7 +207,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   uint8_t *b_hi = smem;
   uint8_t *b_lo = smem + p.b_bytes;
   uint2 *table = reinterpret_cast<uint2 *>(smem + 2 * (size_t)p.b_bytes);
-  float *bias_s = reinterpret_cast<float *>(table + p.ntab);
+  float *bias_s = reinterpret_cast<float *>(table + p.Kpad);
   uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -254,35 +224,24 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   // ---- weights -> shared memory, split into TF32 hi / lo.  Word i of the
   // core-matrix layout holds B[n][k] with n = 8*(cm / (Kpad/4)) + row,
   // k = 4*(cm % (Kpad/4)) + col, so consecutive threads write consecutive
-  // words (conflict-free).  In row mode GEMM column k = 8*r + kw maps to
-  // weight element r*KW + kw (zero for kw >= KW).
+  // words (conflict-free).
   {
     const int kq = p.Kpad / 4;
     const int words = p.Npad * p.Kpad;
     for (int i = tid; i < words; i += kThreads) {
       const int cm = i >> 5, r = (i >> 2) & 7, cw = i & 3;
       const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
-      int kw_idx = k;
-      bool in = k < p.Kred;
-      if (ROW) {
-        const int rowk = k / kRowCols, kw = k - rowk * kRowCols;
-        kw_idx = rowk * g.KW + kw;
-        in = kw < g.KW && kw_idx < p.Kred;
-      }
-      const float v = (n < g.K && in) ? __ldg(p.w + (int64_t)n * p.Kred + kw_idx) : 0.f;
+      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kred + k) : 0.f;
       const float hi = __uint_as_float(tf32_hi_bits(v));
       reinterpret_cast<float *>(b_hi)[i] = hi;
       reinterpret_cast<float *>(b_lo)[i] = v - hi;
     }
-    // ---- reduction column (or row) -> (input offset, tap coordinates)
-    const int nent = ROW ? (int)(g.C * g.KD * g.KH) : p.Kred;
-    for (int kk = tid; kk < p.ntab; kk += kThreads) {
+    // ---- reduction column -> (input offset, tap coordinates)
+    for (int kk = tid; kk < p.Kpad; kk += kThreads) {
       uint2 e;
-      if (kk < nent) {
-        const int per_c = ROW ? g.KD * g.KH : taps;
-        const int c = kk / per_c, t = kk - c * per_c;
-        const int kw = ROW ? 0 : t % g.KW;
-        const int khd = ROW ? t : t / g.KW;
+      if (kk < p.Kred) {
+        const int c = kk / taps, t = kk - c * taps;
+        const int kw = t % g.KW, khd = t / g.KW;
         const int kd = khd / g.KH, kh = khd - kd * g.KH;
         e.x = (uint32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
         e.y = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
@@ -320,8 +279,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    int64_t it = 0;
-    for (int64_t tile = blockIdx.x; tile < p.tiles; tile += gridDim.x, ++it) {
+    const int64_t my_tiles = cta_tile_count(p);
+    for (int64_t it = 0; it < my_tiles; ++it) {
+      const int64_t tile = tile_of(p, it);
       const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
       bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
@@ -359,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * grp);
     const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
-    const int64_t my_tiles = (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const int64_t my_tiles = cta_tile_count(p);
     const int64_t slot_tiles = (my_tiles - slot + 1) / 2;  // tiles it = slot, slot + 2, ... < my_tiles
     const int64_t total = slot_tiles * p.nchunks;          // chunks of this slot
     int64_t cur_li = -1;
@@ -368,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const int64_t li = lg / p.nchunks;
       const int q = (int)(lg - li * p.nchunks);
       if (li != cur_li) {
-        ps = decode_position(p, blockIdx.x + (2 * li + slot) * gridDim.x, t);
+        ps = decode_position(p, tile_of(p, 2 * li + slot), t);
         cur_li = li;
       }
       const int k0 = q * p.KC;
@@ -378,10 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < kChunkMax / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          if (ROW)
-            gather_rows<DW1>(ps, table + (k0 + u * kUnit) / kRowCols, g.KW, g.DW, vu);
-          else
-            gather_cols(ps, table + k0 + u * kUnit, vu);
+          gather_cols(ps, table + k0 + u * kUnit, vu);
         }
       }
       const uint32_t r = (uint32_t)(lg >> 1);
@@ -414,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
     const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
     const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
-    const int64_t my_tiles = (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
+    const int64_t my_tiles = cta_tile_count(p);
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += 2) {
       const int64_t li = it >> 1;
@@ -486,14 +443,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     if (e != cudaSuccess) return e;
   }
   if (!g_attr_set[dev]) {
-    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kMaxSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMaxSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               kMaxSmem);
+    e = cudaFuncSetAttribute(igemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -511,15 +461,9 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.Npad = pl.Npad;
   p.KC = pl.KC;
   p.nchunks = pl.nchunks;
-  p.ntab = pl.ntab;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-  if (!pl.row)
-    igemm_3xtf32_kernel<false, false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
-  else if (g.DW == 1)
-    igemm_3xtf32_kernel<true, true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
-  else
-    igemm_3xtf32_kernel<true, false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  igemm_3xtf32_kernel<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
 

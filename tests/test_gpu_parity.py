@@ -255,8 +255,8 @@ def test_fused_workload_full_size_sampled():
 # ------------------------------------------- kernel-variant coverage
 
 @pytest.mark.parametrize("kw,dw,pw", [(5, 1, 0), (7, 1, 3), (8, 1, 2), (7, 2, 4), (6, 3, 1)])
-def test_tensor_core_row_mode_widths(kw, dw, pw):
-    # 5 <= KW <= 8 takes the row-ordered reduction on the tensor-core path
+def test_tensor_core_wide_kernels(kw, dw, pw):
+    # wide kernels along W with dilation and padding on the tensor-core path
     rng = np.random.default_rng(kw * 100 + dw * 10 + pw)
     x = rng.standard_normal((2, 5, 6, 7, 41)).astype(np.float32)
     w = ((rng.random((37, 5, 2, 3, kw)) - 0.5) * 0.3).astype(np.float32)
@@ -265,7 +265,7 @@ def test_tensor_core_row_mode_widths(kw, dw, pw):
     assert cf.algo_supported(2, 5, 37, x.shape[2:], w.shape[2:], s, p, d, cf.CONV_ALGO_IGEMM_3XTF32)
     ref = oracle.conv_nd(x, w, b, s, p, d)
     y = run_conv(x, w, b, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32).cpu().numpy()
-    assert_close(y, ref, f"row mode kw={kw} dw={dw} pw={pw}")
+    assert_close(y, ref, f"wide kernel kw={kw} dw={dw} pw={pw}")
 
 
 def test_fused_staged_multi_image_blocks():
