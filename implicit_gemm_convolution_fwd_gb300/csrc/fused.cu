@@ -195,6 +195,9 @@ constexpr int kSThreads = kSWarps * 32;
 constexpr int kSRows = kSWarps;      // output rows per block
 constexpr int kSCO = 6;              // channels per lane
 constexpr int kSNcg = 4;             // 4 x 6 = 24 channel slots
+constexpr int kSWTap = 8;            // floats per (row, channel group, tap): 6 channels + 2 pad
+constexpr int kSWStride = 3 * kSWTap;  // floats per (row, channel group)
+constexpr int kSWRow = kSNcg * kSWStride;  // floats per (c, kd, kh) weight row
 constexpr int kSMaxSrows = 128;      // shared rows per channel per plane (output rows + halos)
 
 struct StagedParams {
@@ -221,23 +224,32 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const float *src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
+// CT, KDT, KHT, WPT, SRT: compile-time C_in, KD, KH, shared row pitch and
+// shared rows per channel (0 = runtime); the benchmark shape is specialised
+// so that every shared-memory offset in the FMA loop is an immediate.
+template <int CT, int KDT, int KHT, int WPT, int SRT>
 __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(const StagedParams p) {
-  constexpr int NCH = kSNcg * kSCO;  // 24
   constexpr int NOWG = 8;
   extern __shared__ __align__(16) float sm[];
-  float *ws = sm;                 // [C*taps][4][6]
+  float *ws = sm;                 // [(c*KD + kd)*KH + kh][4 channel groups][kw][6 channels + 2 pad]
   float *ring = sm + p.w_floats;  // [ring][C][srows_max][WP]
   __shared__ int64_t srow_src[kSMaxSrows];  // input-row base offset of each shared row
   __shared__ int nsrows_s;
 
   const Geom &g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int taps = g.KD * g.KH * 3;
+  const int C = CT ? CT : (int)g.C, KD = KDT ? KDT : g.KD, KH = KHT ? KHT : g.KH;
+  const int WP = WPT ? WPT : p.WP, SR = SRT ? SRT : p.srows_max;
+  const int taps = KD * KH * 3;
   const int64_t HW = (int64_t)g.H * g.W;
 
-  for (int i = tid; i < (int)(g.C * taps) * NCH; i += kSThreads) {
-    const int o = i % NCH, ct = i / NCH;
-    ws[i] = o < g.K ? p.w[(int64_t)o * g.C * taps + ct] : 0.f;
+  for (int i = tid; i < C * KD * KH * kSWRow; i += kSThreads) {
+    const int row = i / kSWRow, rem = i - row * kSWRow;
+    const int cgi = rem / kSWStride, jj = rem - cgi * kSWStride;
+    float v = 0.f;
+    const int kw = jj / kSWTap, o = jj - kw * kSWTap, oc = cgi * kSCO + o;
+    if (o < kSCO && oc < g.K) v = p.w[(int64_t)oc * C * taps + row * 3 + kw];
+    ws[i] = v;
   }
   // zero the ring once so the row padding never holds stale bits
   for (uint32_t i = tid; i < (uint32_t)p.ring * p.slot_floats; i += kSThreads) ring[i] = 0.f;
@@ -303,41 +315,54 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 #pragma unroll
       for (int r = 0; r < kR; ++r) mins[o][r] = INFINITY;
 
+    int s_od = 0;  // ring slot of plane od
     for (int od = 0; od < g.OD; ++od) {
       cp_async_wait_all();
       __syncthreads();  // planes od .. od+KD-1 are in shared memory; plane od-1 is free
-      if (od + g.KD < g.D) issue_plane(od + g.KD);
+      if (od + KD < g.D) issue_plane(od + KD);
       float acc[kSCO][kR];
 #pragma unroll
       for (int o = 0; o < kSCO; ++o)
 #pragma unroll
         for (int r = 0; r < kR; ++r) acc[o][r] = 0.f;
-      for (int c = 0; c < g.C; ++c) {
-        for (int kd = 0; kd < g.KD; ++kd) {
-          const float *plane = ring + (size_t)((od + kd) % p.ring) * p.slot_floats +
-                               (size_t)(c * p.srows_max + my_srow) * p.WP + ow0;
-          const float *wrow = ws + ((c * g.KD + kd) * g.KH) * 3 * NCH + cg * kSCO;
-#pragma unroll 3
-          for (int kh = 0; kh < g.KH; ++kh) {
-            const float *xr = plane + kh * p.WP;
-            const float4 a = *reinterpret_cast<const float4 *>(xr);
-            const float2 b2 = *reinterpret_cast<const float2 *>(xr + 4);
-            const float xv[6] = {a.x, a.y, a.z, a.w, b2.x, b2.y};
-            const float *wt = wrow + kh * 3 * NCH;
+      const float *xlane = ring + (size_t)my_srow * WP + ow0;
+      const float *wlane = ws + cg * kSWStride;
 #pragma unroll
-            for (int kw = 0; kw < 3; ++kw) {
-              const float2 w0 = *reinterpret_cast<const float2 *>(wt + kw * NCH);
-              const float2 w1 = *reinterpret_cast<const float2 *>(wt + kw * NCH + 2);
-              const float2 w2 = *reinterpret_cast<const float2 *>(wt + kw * NCH + 4);
-              const float wv[kSCO] = {w0.x, w0.y, w1.x, w1.y, w2.x, w2.y};
+      for (int kd = 0; kd < (KDT ? KDT : 1); ++kd) {
+        for (int kdr = KDT ? kd : 0; kdr < (KDT ? kd + 1 : KD); ++kdr) {
+          int slot = s_od + kdr;
+          if (slot >= p.ring) slot -= p.ring;
+          const float *xplane = xlane + (size_t)slot * p.slot_floats;
 #pragma unroll
-              for (int o = 0; o < kSCO; ++o)
+          for (int c = 0; c < (CT ? CT : 1); ++c) {
+            for (int cr = CT ? c : 0; cr < (CT ? c + 1 : C); ++cr) {
+              const float *xc = xplane + cr * SR * WP;
+              const float *wc = wlane + ((cr * KD + kdr) * KH) * kSWRow;
 #pragma unroll
-                for (int r = 0; r < kR; ++r) acc[o][r] = fmaf(wv[o], xv[r + kw], acc[o][r]);
+              for (int kh = 0; kh < (KHT ? KHT : 1); ++kh) {
+                for (int khr = KHT ? kh : 0; khr < (KHT ? kh + 1 : KH); ++khr) {
+                  const float *xr = xc + khr * WP;
+                  const float4 a = *reinterpret_cast<const float4 *>(xr);
+                  const float2 b2 = *reinterpret_cast<const float2 *>(xr + 4);
+                  const float xv[6] = {a.x, a.y, a.z, a.w, b2.x, b2.y};
+                  const float *wt = wc + khr * kSWRow;
+#pragma unroll
+                  for (int kw = 0; kw < 3; ++kw) {
+                    const float4 q0 = *reinterpret_cast<const float4 *>(wt + kw * kSWTap);
+                    const float2 q1 = *reinterpret_cast<const float2 *>(wt + kw * kSWTap + 4);
+                    const float wv[kSCO] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y};
+#pragma unroll
+                    for (int o = 0; o < kSCO; ++o)
+#pragma unroll
+                      for (int r = 0; r < kR; ++r) acc[o][r] = fmaf(wv[o], xv[r + kw], acc[o][r]);
+                  }
+                }
+              }
             }
           }
         }
       }
+      s_od = (s_od + 1 == p.ring) ? 0 : s_od + 1;
 #pragma unroll
       for (int o = 0; o < kSCO; ++o)
 #pragma unroll
@@ -388,7 +413,7 @@ bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
   if (srows64 > kSMaxSrows) return false;
   const int srows = (int)srows64;
   const int WP = (g.W + 3) / 4 * 4 + 4;
-  const int64_t w_floats = (int64_t)g.C * g.taps() * kSNcg * kSCO;
+  const int64_t w_floats = (int64_t)g.C * g.KD * g.KH * kSWRow;
   const int64_t slot = (int64_t)g.C * srows * WP;
   const int ring = g.KD + 1;
   const int64_t bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot);
@@ -479,12 +504,14 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const size_t smem = 4 * ((size_t)sp.w_floats + (size_t)sp.ring * sp.slot_floats);
-    e = cudaFuncSetAttribute(fused_min_softmax_staged_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
+    // the benchmark shape (C_in 3, kernel 3^3, W 32 -> pitch 36, 30 shared rows) is specialised
+    const bool spec = g.C == 3 && g.KD == 3 && g.KH == 3 && sp.WP == 36 && sp.srows_max == 30;
+    auto kern = spec ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30> : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int64_t blocks = (p.rows + kSRows - 1) / kSRows;
     const int grid = (int)(blocks < sms ? blocks : sms);
-    fused_min_softmax_staged_kernel<<<grid, kSThreads, smem, stream>>>(sp);
+    kern<<<grid, kSThreads, smem, stream>>>(sp);
     return cudaGetLastError();
   }
   switch (pick_ncg(g.K)) {
