@@ -185,8 +185,10 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
 // Staged variant for the common shape (C_out <= 24, output width <= 32, KW = 3):
 // one persistent CTA per SM owns a contiguous block of (n, oh) output rows
 // (26 at a time, one per warp).  The input rows that block needs are streamed
-// through a ring of KD + 1 depth planes in shared memory with cp.async, one
-// plane ahead of the compute, so the FMA loop reads x from shared memory.
+// through a ring of KD + 2*NB - 1 depth planes in shared memory with cp.async:
+// while the block computes NB output depths from the planes it holds, the next
+// NB planes land in the other slots, so the block synchronises once per NB
+// depths and the FMA loop reads x from shared memory.
 // A lane holds 6 channels x 4 columns (lane = channel group x column group),
 // which keeps registers low enough for 26 warps per SM to hide shared-memory
 // latency; the min / softmax epilogue is as above.
@@ -209,7 +211,8 @@ struct StagedParams {
   int64_t rows;          // N * OH
   int WP;                // shared-memory row pitch (floats): W rounded up to 4, plus 4
   int srows_max;         // shared-memory rows per channel per plane
-  int ring;              // planes in the ring (KD + 1)
+  int ring;              // planes in the ring (KD + 2 * nb - 1)
+  int nb;                // output depths computed between two block-wide barriers
   int vec;               // 16-byte copies are legal
   uint32_t w_floats;     // weight region size (floats, multiple of 4)
   uint32_t slot_floats;  // one plane: C * srows_max * WP
@@ -298,7 +301,8 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       }
       cp_async_commit();
     };
-    for (int dd = 0; dd < g.KD; ++dd) issue_plane(dd);
+    // the first group's planes: 0 .. nb + KD - 2, one commit group per plane
+    for (int dd = 0; dd < p.nb + KD - 1 && dd < g.D; ++dd) issue_plane(dd);
 
     // this lane's output row and its shared-memory row
     const int lr = warp;
@@ -317,9 +321,11 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 
     int s_od = 0;  // ring slot of plane od
     for (int od = 0; od < g.OD; ++od) {
-      cp_async_wait_all();
-      __syncthreads();  // planes od .. od+KD-1 are in shared memory; plane od-1 is free
-      if (od + KD < g.D) issue_plane(od + KD);
+      if ((od % p.nb) == 0) {
+        cp_async_wait_all();
+        __syncthreads();  // this group's planes are in; the previous group's slots are free
+        for (int dd = od + p.nb + KD - 1; dd < od + 2 * p.nb + KD - 1 && dd < g.D; ++dd) issue_plane(dd);
+      }
       float acc[kSCO][kR];
 #pragma unroll
       for (int o = 0; o < kSCO; ++o)
@@ -415,9 +421,15 @@ bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
   const int WP = (g.W + 3) / 4 * 4 + 4;
   const int64_t w_floats = (int64_t)g.C * g.KD * g.KH * kSWRow;
   const int64_t slot = (int64_t)g.C * srows * WP;
-  const int ring = g.KD + 1;
-  const int64_t bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot);
-  if (bytes > kMaxSmemBytes) return false;
+  int nb = 4, ring = 0;
+  int64_t bytes = 0;
+  for (; nb >= 1; nb /= 2) {
+    ring = g.KD + 2 * nb - 1;
+    bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot);
+    if (bytes <= kMaxSmemBytes) break;
+  }
+  if (nb < 1) return false;
+  sp->nb = nb;
   sp->WP = WP;
   sp->srows_max = srows;
   sp->ring = ring;

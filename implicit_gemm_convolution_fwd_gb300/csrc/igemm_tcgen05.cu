@@ -179,22 +179,43 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   return ps;
 }
 
-// 16 consecutive reduction columns of one output position (0 for padded taps).
-// Column mode: table entry per column = {input offset, kd | kh<<8 | kw<<16 | pad<<31}.
-__device__ __forceinline__ void gather_cols(const PosInfo &ps, const uint2 *tb, float (&v)[kUnit]) {
+// 16 consecutive reduction columns [k0, k0 + 16) of one output position.
+// toff[k]: input offset of column k from the receptive field's origin;
+// ttap[k]: kd | kh << 8 | kw << 16 (bit 31: padding column past Kred).
+// Warps whose receptive fields are all inside the input read four offsets per
+// 16-byte shared load and skip every bounds test; only a unit that reaches the
+// padding columns checks them.
+__device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
+                                            int Kred, float (&v)[kUnit]) {
   if (ps.warp_full) {
+    const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
+    if (k0 + kUnit <= Kred) {
 #pragma unroll
-    for (int j = 0; j < kUnit; ++j) {
-      const uint2 e = tb[j];
-      v[j] = (e.y >> 31) ? 0.f : __ldg(ps.xo + (int32_t)e.x);
+      for (int q = 0; q < kUnit / 4; ++q) {
+        const int4 o = o4[q];
+        v[4 * q + 0] = __ldg(ps.xo + o.x);
+        v[4 * q + 1] = __ldg(ps.xo + o.y);
+        v[4 * q + 2] = __ldg(ps.xo + o.z);
+        v[4 * q + 3] = __ldg(ps.xo + o.w);
+      }
+    } else {
+#pragma unroll
+      for (int q = 0; q < kUnit / 4; ++q) {
+        const int4 o = o4[q];
+        const int k = k0 + 4 * q;
+        v[4 * q + 0] = k + 0 < Kred ? __ldg(ps.xo + o.x) : 0.f;
+        v[4 * q + 1] = k + 1 < Kred ? __ldg(ps.xo + o.y) : 0.f;
+        v[4 * q + 2] = k + 2 < Kred ? __ldg(ps.xo + o.z) : 0.f;
+        v[4 * q + 3] = k + 3 < Kred ? __ldg(ps.xo + o.w) : 0.f;
+      }
     }
   } else {
 #pragma unroll
     for (int j = 0; j < kUnit; ++j) {
-      const uint2 e = tb[j];
-      const uint32_t kd = e.y & 0xffu, kh = (e.y >> 8) & 0xffu, kw = (e.y >> 16) & 0xffu;
-      const bool in = ps.valid && !(e.y >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
-      v[j] = in ? __ldg(ps.xo + (int32_t)e.x) : 0.f;
+      const uint32_t e = ttap[k0 + j];
+      const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+      const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      v[j] = in ? __ldg(ps.xo + toff[k0 + j]) : 0.f;
     }
   }
 }
@@ -206,8 +227,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 
   uint8_t *b_hi = smem;
   uint8_t *b_lo = smem + p.b_bytes;
-  uint2 *table = reinterpret_cast<uint2 *>(smem + 2 * (size_t)p.b_bytes);
-  float *bias_s = reinterpret_cast<float *>(table + p.Kpad);
+  int32_t *toff = reinterpret_cast<int32_t *>(smem + 2 * (size_t)p.b_bytes);  // [Kpad]
+  uint32_t *ttap = reinterpret_cast<uint32_t *>(toff + p.Kpad);                // [Kpad]
+  float *bias_s = reinterpret_cast<float *>(ttap + p.Kpad);
   uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -238,18 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     }
     // ---- reduction column -> (input offset, tap coordinates)
     for (int kk = tid; kk < p.Kpad; kk += kThreads) {
-      uint2 e;
       if (kk < p.Kred) {
         const int c = kk / taps, t = kk - c * taps;
         const int kw = t % g.KW, khd = t / g.KW;
         const int kd = khd / g.KH, kh = khd - kd * g.KH;
-        e.x = (uint32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
-        e.y = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
+        toff[kk] = (int32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
+        ttap[kk] = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
       } else {
-        e.x = 0;
-        e.y = 0x80000000u;  // padding: contributes zero
+        toff[kk] = 0;
+        ttap[kk] = 0x80000000u;  // padding: contributes zero
       }
-      table[kk] = e;
     }
     for (int i = tid; i < p.Npad; i += kThreads) bias_s[i] = (p.bias && i < g.K) ? __ldg(p.bias + i) : 0.f;
   }
@@ -338,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < kChunkMax / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, table + k0 + u * kUnit, vu);
+          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, vu);
         }
       }
       const uint32_t r = (uint32_t)(lg >> 1);
