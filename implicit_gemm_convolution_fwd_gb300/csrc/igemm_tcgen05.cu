@@ -41,16 +41,17 @@ namespace {
 constexpr int kTileM = 128;
 constexpr int kEpiWarps = 4;
 constexpr int kProdGroups = 4;                         // one TMEM A stage per group
-constexpr int kSlots = 2;                              // tile pipelines; consecutive tiles alternate
+constexpr int kMaxSlots = 4;                           // tile pipelines; consecutive tiles rotate over them
 constexpr int kMmaWarp = kEpiWarps + 4 * kProdGroups;  // 20: first of the issuer warps (one per slot)
-constexpr int kThreads = (kMmaWarp + kSlots) * 32;     // 704
+constexpr int kThreads = (kMmaWarp + kMaxSlots) * 32;  // 768
 constexpr int kChunkMax = 32;                          // K columns per chunk (registers hold one chunk)
 constexpr int kUnit = 16;                              // reduction columns per gather / TMEM store
 constexpr uint32_t kTmemCols = 512;
 constexpr int kMaxNpad = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA per SM, so TMEM allocation never contends
-constexpr int kNumBars = 2 * kProdGroups + 5;  // a_full[G], a_empty[G], d_full[2], d_empty[2], drain
+constexpr int kMaxStages = 2 * kMaxSlots;     // two A stages per slot
+constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxSlots + 1;  // a_full, a_empty, d_full, d_empty, drain
 constexpr long long kWaitLimitCycles = 1ll << 32;  // about two seconds
 
 struct IgemmParams {
@@ -67,11 +68,12 @@ struct IgemmParams {
   int Npad;         // C_out rounded up to 32
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
+  int nslots;       // tile slots (2 or 4), each with an MMA-issuing thread and an accumulator
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
 struct Plan {
-  int Kred, Kpad, Npad, KC, nchunks;
+  int Kred, Kpad, Npad, KC, nchunks, nslots;
   size_t smem;
 };
 
@@ -95,9 +97,11 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
   pl->Kred = (int)kred;
   pl->Kpad = (int)((kred + 31) / 32 * 32);
   pl->Npad = (int)((g.K + 31) / 32 * 32);
-  // TMEM: one accumulator of Npad columns per slot, then kProdGroups A stages
-  // of KC hi + KC lo columns.
-  int kc = (int)((kTmemCols - kSlots * pl->Npad) / (2 * kProdGroups)) / kUnit * kUnit;
+  // TMEM: one accumulator of Npad columns per slot, then two A stages per
+  // slot of KC hi + KC lo columns.  Four slots (four MMA instruction streams)
+  // when the accumulators leave room for 16-column stages, else two.
+  pl->nslots = (kMaxSlots * pl->Npad + 2 * kMaxSlots * 2 * kUnit <= (int)kTmemCols) ? kMaxSlots : 2;
+  int kc = (int)((kTmemCols - pl->nslots * pl->Npad) / (2 * 2 * pl->nslots)) / kUnit * kUnit;
   if (kc > kChunkMax) kc = kChunkMax;
   if (kc > pl->Kpad) kc = pl->Kpad;
   pl->KC = kc;
@@ -220,6 +224,8 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
   }
 }
 
+// CH: register buffer of one chunk (>= KC): 16 for four slots, 32 for two.
+template <int CH>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -233,11 +239,12 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-  const uint32_t bar_a_full = ptx::smem_addr(bars + 0);                 // [kProdGroups]
-  const uint32_t bar_a_empty = ptx::smem_addr(bars + kProdGroups);      // [kProdGroups]
-  const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kProdGroups);   // [2]
-  const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kProdGroups + 2);  // [2]
-  const uint32_t bar_drain = ptx::smem_addr(bars + 2 * kProdGroups + 4);
+  const uint32_t bar_a_full = ptx::smem_addr(bars + 0);                                // [stages]
+  const uint32_t bar_a_empty = ptx::smem_addr(bars + kMaxStages);                      // [stages]
+  const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kMaxStages);                   // [slots]
+  const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kMaxStages + kMaxSlots);      // [slots]
+  const uint32_t bar_drain = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots);
+  const int nslots = p.nslots;
 
   const uint32_t SBO = (uint32_t)p.Kpad * 32;  // bytes between 8-row groups of B
   const int taps = g.KD * g.KH * g.KW;
@@ -276,15 +283,15 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   ptx::fence_proxy_async_smem();
   if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
   if (tid == 0) {
-    for (int s = 0; s < kProdGroups; ++s) {
+    for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(bar_a_full + 8 * s, 128);
       ptx::mbar_init(bar_a_empty + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kMaxSlots; ++b) {
       ptx::mbar_init(bar_d_full + 8 * b, 1);
       ptx::mbar_init(bar_d_empty + 8 * b, 128);
     }
-    ptx::mbar_init(bar_drain, kSlots);
+    ptx::mbar_init(bar_drain, nslots);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -293,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // slot b's accumulator at column b * Npad; A stage s: hi at a_col0 + 2*KC*s, lo at + KC.
-  // Slot b owns stages 2b and 2b + 1 and producer groups 2b and 2b + 1.
-  const uint32_t a_col0 = (uint32_t)(kSlots * p.Npad);
+  // Slot b owns stages 2b and 2b + 1; it is served by kProdGroups / nslots
+  // producer groups.
+  const uint32_t a_col0 = (uint32_t)(nslots * p.Npad);
 
   if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
@@ -302,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const int64_t my_tiles = cta_tile_count(p);
     for (int64_t it = 0; it < my_tiles; ++it) {
       const int64_t tile = tile_of(p, it);
-      const uint32_t b = (uint32_t)(it & 1), rb = (uint32_t)(it >> 1);
+      const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
       bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
@@ -330,43 +338,46 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     }
   } else if (warp < kMmaWarp) {
     // ------------------------------------------------------------ producers
-    // Group g serves slot b = g / 2 (the CTA's tiles it = b, b + 2, ...) and
-    // fills stage g with every other chunk of that slot's sequence.  A
-    // chunk's loads are issued before waiting for the stage to drain.
+    // Group grp serves slot grp / gps (the CTA's tiles it = slot, slot +
+    // nslots, ...): it takes the slot's chunks lg = sel, sel + gps, ... and
+    // puts chunk lg in the slot's stage lg & 1.  A chunk's loads are issued
+    // before waiting for its stage to drain.
     const int grp = (warp - kEpiWarps) >> 2;
-    const int slot = grp >> 1, sel = grp & 1;
+    const int gps = kProdGroups / nslots;  // producer groups per slot (1 or 2)
+    const int slot = grp / gps, sel = grp - slot * gps;
     const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * grp);
-    const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
     const int64_t my_tiles = cta_tile_count(p);
-    const int64_t slot_tiles = (my_tiles - slot + 1) / 2;  // tiles it = slot, slot + 2, ... < my_tiles
-    const int64_t total = slot_tiles * p.nchunks;          // chunks of this slot
+    const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
+    const int64_t total = slot_tiles * p.nchunks;                         // chunks of this slot
     int64_t cur_li = -1;
     PosInfo ps;
-    for (int64_t lg = sel; lg < total; lg += 2) {
+    for (int64_t lg = sel; lg < total; lg += gps) {
       const int64_t li = lg / p.nchunks;
       const int q = (int)(lg - li * p.nchunks);
       if (li != cur_li) {
-        ps = decode_position(p, tile_of(p, 2 * li + slot), t);
+        ps = decode_position(p, tile_of(p, li * nslots + slot), t);
         cur_li = li;
       }
+      const int stage = 2 * slot + (int)(lg & 1);
+      const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
+      const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
       const int k0 = q * p.KC;
       const int ncols = min(p.KC, p.Kpad - k0);
-      float v[kChunkMax];
+      float v[CH];
 #pragma unroll
-      for (int u = 0; u < kChunkMax / kUnit; ++u) {
+      for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
           gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, vu);
         }
       }
       const uint32_t r = (uint32_t)(lg >> 1);
-      const bool ok = wait_phase(bar_a_empty + 8 * grp, (r & 1) ^ 1, abort_flag);
+      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
 #pragma unroll
-      for (int u = 0; u < kChunkMax / kUnit; ++u) {
+      for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           uint32_t tmp[kUnit];
 #pragma unroll
@@ -380,21 +391,22 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       }
       ptx::tmem_wait_st();
       ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_a_full + 8 * grp);
+      ptx::mbar_arrive(bar_a_full + 8 * stage);
     }
-  } else if (lane == 0) {
+  } else if (lane == 0 && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread per slot: a thread cannot issue a tcgen05.mma much faster
-    // than one per ~140 cycles, so two slots keep two instruction streams
-    // (two tiles) in flight.  Per K-step: D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi.
+    // One thread per slot, in warps on different SM sub-partitions: a thread
+    // cannot issue a tcgen05.mma much faster than one per ~140 cycles, so the
+    // slots keep two or four instruction streams (tiles) in flight.
+    // Per K-step: D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi.
     const int slot = warp - kMmaWarp;
     const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
     const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
     const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
     const int64_t my_tiles = cta_tile_count(p);
     bool aborted = false;
-    for (int64_t it = slot; it < my_tiles && !aborted; it += 2) {
-      const int64_t li = it >> 1;
+    for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
+      const int64_t li = it / nslots;
       if (!wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag)) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
@@ -463,7 +475,9 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     if (e != cudaSuccess) return e;
   }
   if (!g_attr_set[dev]) {
-    e = cudaFuncSetAttribute(igemm_3xtf32_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
@@ -481,9 +495,13 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.Npad = pl.Npad;
   p.KC = pl.KC;
   p.nchunks = pl.nchunks;
+  p.nslots = pl.nslots;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-  igemm_3xtf32_kernel<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  if (pl.KC <= 16)
+    igemm_3xtf32_kernel<16><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  else
+    igemm_3xtf32_kernel<32><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
 
