@@ -159,13 +159,23 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   int64_t n = 0;
   int od = 0, oh = 0, ow = 0;
   if (ps.valid) {
-    const int64_t OHW = (int64_t)g.OH * g.OW;
-    n = m / p.osp;
-    const int64_t pp = m - n * p.osp;
-    od = (int)(pp / OHW);
-    const int rem = (int)(pp - (int64_t)od * OHW);
-    oh = rem / g.OW;
-    ow = rem - oh * g.OW;
+    if (p.M_total < ((int64_t)1 << 31)) {  // 32-bit divisions when every index fits
+      const uint32_t mm = (uint32_t)m, osp = (uint32_t)p.osp, OHW = (uint32_t)g.OH * (uint32_t)g.OW;
+      const uint32_t n32 = mm / osp, pp = mm - n32 * osp;
+      n = n32;
+      od = (int)(pp / OHW);
+      const uint32_t rem = pp - (uint32_t)od * OHW;
+      oh = (int)(rem / (uint32_t)g.OW);
+      ow = (int)(rem - (uint32_t)oh * (uint32_t)g.OW);
+    } else {
+      const int64_t OHW = (int64_t)g.OH * g.OW;
+      n = m / p.osp;
+      const int64_t pp = m - n * p.osp;
+      od = (int)(pp / OHW);
+      const int rem = (int)(pp - (int64_t)od * OHW);
+      oh = rem / g.OW;
+      ow = rem - oh * g.OW;
+    }
   }
   const int id0 = od * g.SD - g.PD, ih0 = oh * g.SH - g.PH, iw0 = ow * g.SW - g.PW;
   uint32_t dm = 0, hm = 0, wm = 0;
@@ -316,8 +326,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::tc_fence_after();
       const int64_t m = tile * kTileM + tid;
       const bool valid = m < p.M_total;
-      const int64_t n = valid ? m / p.osp : 0;
-      const int64_t pp = valid ? m - n * p.osp : 0;
+      int64_t n = 0, pp = 0;
+      if (valid) {
+        if (p.M_total < ((int64_t)1 << 31)) {
+          n = (uint32_t)m / (uint32_t)p.osp;
+          pp = m - n * p.osp;
+        } else {
+          n = m / p.osp;
+          pp = m - n * p.osp;
+        }
+      }
       float *yp = p.y + n * g.K * p.osp + pp;
       for (int c0 = 0; c0 < p.Npad; c0 += 32) {
         uint32_t v[32];
@@ -349,49 +367,50 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t my_tiles = cta_tile_count(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
-    const int64_t total = slot_tiles * p.nchunks;                         // chunks of this slot
-    int64_t cur_li = -1;
-    PosInfo ps;
-    for (int64_t lg = sel; lg < total; lg += gps) {
-      const int64_t li = lg / p.nchunks;
-      const int q = (int)(lg - li * p.nchunks);
-      if (li != cur_li) {
-        ps = decode_position(p, tile_of(p, li * nslots + slot), t);
-        cur_li = li;
-      }
-      const int stage = 2 * slot + (int)(lg & 1);
-      const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
-      const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
-      const int k0 = q * p.KC;
-      const int ncols = min(p.KC, p.Kpad - k0);
-      float v[CH];
+    bool aborted = false;
+    for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
+      const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
+      const int64_t lg0 = li * p.nchunks;  // slot-local index of the tile's first chunk
+      // this group's chunks of the tile: lg = lg0 + q with lg = sel (mod gps)
+      for (int q = (int)((sel - lg0 % gps + gps) % gps); q < p.nchunks; q += gps) {
+        const int64_t lg = lg0 + q;
+        const int stage = 2 * slot + (int)(lg & 1);
+        const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
+        const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
+        const int k0 = q * p.KC;
+        const int ncols = min(p.KC, p.Kpad - k0);
+        float v[CH];
 #pragma unroll
-      for (int u = 0; u < CH / kUnit; ++u) {
-        if (u * kUnit < ncols) {
-          float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, vu);
+        for (int u = 0; u < CH / kUnit; ++u) {
+          if (u * kUnit < ncols) {
+            float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
+            gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, vu);
+          }
         }
-      }
-      const uint32_t r = (uint32_t)(lg >> 1);
-      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int u = 0; u < CH / kUnit; ++u) {
-        if (u * kUnit < ncols) {
-          uint32_t tmp[kUnit];
-#pragma unroll
-          for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
-          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
-#pragma unroll
-          for (int j = 0; j < kUnit; ++j)
-            tmp[j] = __float_as_uint(v[u * kUnit + j] - __uint_as_float(tf32_hi_bits(v[u * kUnit + j])));
-          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
+        const uint32_t r = (uint32_t)(lg >> 1);
+        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          aborted = true;
+          break;
         }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < CH / kUnit; ++u) {
+          if (u * kUnit < ncols) {
+            uint32_t tmp[kUnit];
+#pragma unroll
+            for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
+            ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
+#pragma unroll
+            for (int j = 0; j < kUnit; ++j)
+              tmp[j] = __float_as_uint(v[u * kUnit + j] - __uint_as_float(tf32_hi_bits(v[u * kUnit + j])));
+            ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_a_full + 8 * stage);
       }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_a_full + 8 * stage);
     }
   } else if (lane == 0 && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
