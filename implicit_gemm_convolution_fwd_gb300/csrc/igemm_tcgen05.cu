@@ -367,77 +367,50 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t my_tiles = cta_tile_count(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
-    // This group's chunks, in order: (li, q) = slot-local tile, chunk index,
-    // taking every gps-th chunk of the slot's sequence lg = li * nchunks + q.
-    auto first_q = [&](int64_t li) -> int {
-      return gps == 1 ? 0 : (int)(((int64_t)sel - ((li * p.nchunks) & 1) + 2) & 1);
-    };
-    auto advance = [&](int64_t &li, int &q) -> bool {
-      q += gps;
-      while (q >= p.nchunks) {
-        if (++li >= slot_tiles) return false;
-        q = first_q(li);
-      }
-      return true;
-    };
-    int64_t li = 0;
-    int q = first_q(0);
-    bool have = slot_tiles > 0;
-    while (have && q >= p.nchunks) {
-      if (++li >= slot_tiles) have = false;
-      else q = first_q(li);
-    }
-    PosInfo ps = decode_position(p, tile_of(p, (have ? li : 0) * nslots + slot), t);
-    float v[CH];
-    auto gather = [&](const PosInfo &pos, int qq) {
-      const int k0 = qq * p.KC;
-      const int ncols = min(p.KC, p.Kpad - k0);
+    bool aborted = false;
+    for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
+      const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
+      const int64_t lg0 = li * p.nchunks;  // slot-local index of the tile's first chunk
+      // this group's chunks of the tile: lg = lg0 + q with lg = sel (mod gps)
+      for (int q = (int)((sel - lg0 % gps + gps) % gps); q < p.nchunks; q += gps) {
+        const int64_t lg = lg0 + q;
+        const int stage = 2 * slot + (int)(lg & 1);
+        const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
+        const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
+        const int k0 = q * p.KC;
+        const int ncols = min(p.KC, p.Kpad - k0);
+        float v[CH];
 #pragma unroll
-      for (int u = 0; u < CH / kUnit; ++u) {
-        if (u * kUnit < ncols) {
-          float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(pos, toff, ttap, k0 + u * kUnit, p.Kred, vu);
+        for (int u = 0; u < CH / kUnit; ++u) {
+          if (u * kUnit < ncols) {
+            float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
+            gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, vu);
+          }
         }
-      }
-    };
-    if (have) gather(ps, q);
-    while (have) {
-      const int64_t lg = li * p.nchunks + q;
-      const int stage = 2 * slot + (int)(lg & 1);
-      const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
-      const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
-      const int ncols = min(p.KC, p.Kpad - q * p.KC);
-      const uint32_t r = (uint32_t)(lg >> 1);
-      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int u = 0; u < CH / kUnit; ++u) {
-        if (u * kUnit < ncols) {
-          uint32_t tmp[kUnit];
-#pragma unroll
-          for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
-          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
-#pragma unroll
-          for (int j = 0; j < kUnit; ++j)
-            tmp[j] = __float_as_uint(v[u * kUnit + j] - __uint_as_float(tf32_hi_bits(v[u * kUnit + j])));
-          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
+        const uint32_t r = (uint32_t)(lg >> 1);
+        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          aborted = true;
+          break;
         }
+        ptx::tc_fence_after();
+#pragma unroll
+        for (int u = 0; u < CH / kUnit; ++u) {
+          if (u * kUnit < ncols) {
+            uint32_t tmp[kUnit];
+#pragma unroll
+            for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
+            ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
+#pragma unroll
+            for (int j = 0; j < kUnit; ++j)
+              tmp[j] = __float_as_uint(v[u * kUnit + j] - __uint_as_float(tf32_hi_bits(v[u * kUnit + j])));
+            ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
+          }
+        }
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_a_full + 8 * stage);
       }
-      // the next chunk's loads fly while this chunk's TMEM stores complete
-      int64_t li2 = li;
-      int q2 = q;
-      const bool have2 = advance(li2, q2);
-      if (have2) {
-        if (li2 != li) ps = decode_position(p, tile_of(p, li2 * nslots + slot), t);
-        gather(ps, q2);
-      }
-      ptx::tmem_wait_st();
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_a_full + 8 * stage);
-      li = li2;
-      q = q2;
-      have = have2;
     }
   } else if (lane == 0 && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
