@@ -254,8 +254,9 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     if (o < kSCO && oc < g.K) v = p.w[(int64_t)oc * C * taps + row * 3 + kw];
     ws[i] = v;
   }
-  // zero the ring once so the row padding never holds stale bits
-  for (uint32_t i = tid; i < (uint32_t)p.ring * p.slot_floats; i += kSThreads) ring[i] = 0.f;
+  // The ring is not cleared: the padding columns past W feed only output
+  // columns >= OW, which are never stored, and each column's softmax is
+  // independent of the others.
 
   const int owg = lane & 7, cg = lane >> 3;
   const int ow0 = owg * 4;
@@ -521,8 +522,8 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     auto kern = spec ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30> : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int64_t blocks = (p.rows + kSRows - 1) / kSRows;
-    const int grid = (int)(blocks < sms ? blocks : sms);
+    // every SM gets a contiguous share of the rows (processed 26 at a time)
+    const int grid = (int)(p.rows < sms ? p.rows : sms);
     kern<<<grid, kSThreads, smem, stream>>>(sp);
     return cudaGetLastError();
   }

@@ -402,8 +402,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
             for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
             ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
 #pragma unroll
-            for (int j = 0; j < kUnit; ++j)
-              tmp[j] = __float_as_uint(v[u * kUnit + j] - __uint_as_float(tf32_hi_bits(v[u * kUnit + j])));
+            for (int j = 0; j < kUnit; j += 2) {
+              float l0, l1;
+              ptx::sub_f32x2(v[u * kUnit + j], v[u * kUnit + j + 1], __uint_as_float(tf32_hi_bits(v[u * kUnit + j])),
+                             __uint_as_float(tf32_hi_bits(v[u * kUnit + j + 1])), l0, l1);
+              tmp[j] = __float_as_uint(l0);
+              tmp[j + 1] = __float_as_uint(l1);
+            }
             ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
           }
         }

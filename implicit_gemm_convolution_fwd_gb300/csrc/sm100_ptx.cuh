@@ -133,6 +133,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "memory");
 }
 
+// (a0 - b0, a1 - b1) with one packed f32x2 instruction, round to nearest.
+__device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
+  asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+      " sub.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}\n"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 // Shared-memory matrix descriptor, no swizzle ("interleaved" core matrices of
 // 8 rows x 16 bytes).  lbo: byte distance between core matrices adjacent in
 // K; sbo: byte distance between 8-row groups along M/N.
