@@ -218,6 +218,20 @@ struct StagedParams {
   uint32_t slot_floats;  // one plane: C * srows_max * WP
 };
 
+// Packed fp32 pairs (two adjacent output channels) for fma.rn.f32x2.
+__device__ __forceinline__ unsigned long long pack2(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack2(unsigned long long r, float &a, float &b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+// acc += w * x for both halves (round to nearest, no flush), one instruction.
+__device__ __forceinline__ void fma2(unsigned long long &acc, unsigned long long w, unsigned long long x) {
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w), "l"(x));
+}
+
 __device__ __forceinline__ void cp_async16(uint32_t dst, const float *src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
 }
@@ -327,11 +341,12 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
         __syncthreads();  // this group's planes are in; the previous group's slots are free
         for (int dd = od + p.nb + KD - 1; dd < od + 2 * p.nb + KD - 1 && dd < g.D; ++dd) issue_plane(dd);
       }
-      float acc[kSCO][kR];
+      // acc2[op][r]: channels (2*op, 2*op + 1) at column r, packed
+      unsigned long long acc2[kSCO / 2][kR];
 #pragma unroll
-      for (int o = 0; o < kSCO; ++o)
+      for (int op = 0; op < kSCO / 2; ++op)
 #pragma unroll
-        for (int r = 0; r < kR; ++r) acc[o][r] = 0.f;
+        for (int r = 0; r < kR; ++r) acc2[op][r] = 0ull;
       const float *xlane = ring + (size_t)my_srow * WP + ow0;
       const float *wlane = ws + cg * kSWStride;
 #pragma unroll
@@ -351,17 +366,20 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
                   const float *xr = xc + khr * WP;
                   const float4 a = *reinterpret_cast<const float4 *>(xr);
                   const float2 b2 = *reinterpret_cast<const float2 *>(xr + 4);
-                  const float xv[6] = {a.x, a.y, a.z, a.w, b2.x, b2.y};
+                  // each input value duplicated into both halves of a pair
+                  const unsigned long long xx[6] = {pack2(a.x, a.x), pack2(a.y, a.y), pack2(a.z, a.z),
+                                                    pack2(a.w, a.w), pack2(b2.x, b2.x), pack2(b2.y, b2.y)};
                   const float *wt = wc + khr * kSWRow;
 #pragma unroll
                   for (int kw = 0; kw < 3; ++kw) {
-                    const float4 q0 = *reinterpret_cast<const float4 *>(wt + kw * kSWTap);
-                    const float2 q1 = *reinterpret_cast<const float2 *>(wt + kw * kSWTap + 4);
-                    const float wv[kSCO] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y};
+                    // the tap's 6 channel weights are 3 aligned pairs in shared memory
+                    const ulonglong2 q0 = *reinterpret_cast<const ulonglong2 *>(wt + kw * kSWTap);
+                    const unsigned long long q1 = *reinterpret_cast<const unsigned long long *>(wt + kw * kSWTap + 4);
+                    const unsigned long long wp[kSCO / 2] = {q0.x, q0.y, q1};
 #pragma unroll
-                    for (int o = 0; o < kSCO; ++o)
+                    for (int op = 0; op < kSCO / 2; ++op)
 #pragma unroll
-                      for (int r = 0; r < kR; ++r) acc[o][r] = fmaf(wv[o], xv[r + kw], acc[o][r]);
+                      for (int r = 0; r < kR; ++r) fma2(acc2[op][r], wp[op], xx[r + kw]);
                   }
                 }
               }
@@ -371,9 +389,14 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       }
       s_od = (s_od + 1 == p.ring) ? 0 : s_od + 1;
 #pragma unroll
-      for (int o = 0; o < kSCO; ++o)
+      for (int op = 0; op < kSCO / 2; ++op)
 #pragma unroll
-        for (int r = 0; r < kR; ++r) mins[o][r] = fminf(mins[o][r], acc[o][r]);
+        for (int r = 0; r < kR; ++r) {
+          float c0, c1;
+          unpack2(acc2[op][r], c0, c1);
+          mins[2 * op][r] = fminf(mins[2 * op][r], c0);
+          mins[2 * op + 1][r] = fminf(mins[2 * op + 1][r], c1);
+        }
     }
 
     // channel softmax per column across the 4 channel-group lanes (xor 8, 16)
