@@ -313,6 +313,28 @@ def time_oracle(wl, target_macs):
     return 2.0 * macs / dt / 1e9, dt, threads, sample
 
 
+# ------------------------------------------------------------------ ranks
+
+def slowest_rank_ms(ms, world, device=None):
+    """Max over ranks of a per-rank step time (ms); identity for one rank.
+
+    Every rank runs an independent replica (the batch shards with no data
+    exchange), so the job's throughput is all ranks' work over the slowest
+    rank's time."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step, ms, world):
+    """Whole-job GFLOP/s: the work of all `world` replicas over the slowest step time."""
+    return world * flops_per_rank_step / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ main
 
 def main():
@@ -360,18 +382,11 @@ def main():
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
-    ms = sum(per_step) / len(per_step)
-    if world > 1:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * flops / (ms * 1e-3) / 1e9
+    ms = slowest_rank_ms(sum(per_step) / len(per_step), world, dev)
+    value = job_throughput(flops, ms, world)
 
     e2e_ms, h2d, d2h = runner.timed_e2e(max(3, args.steps // 4), 2)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = slowest_rank_ms(e2e_ms, world, dev)
     roof = roofline_for(runner, peaks, ms)
     roof["peak_source"] = peaks_src
     roof["kernel"] = runner.algo
@@ -415,7 +430,7 @@ def main():
                        "kernel": runner.algo, "gflop_per_step": flops / 1e9, "bytes_per_step": bytes_alg,
                        "gbs": bytes_alg / (ms * 1e-3) / 1e9, "ms_min": min(per_step),
                        "ms_median": statistics.median(per_step), "wall_s": wall},
-            "e2e": {"value": world * flops / (e2e_ms * 1e-3) / 1e9, "unit": "GFLOP/s", "ms_per_step": e2e_ms,
+            "e2e": {"value": job_throughput(flops, e2e_ms, world), "unit": "GFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": runner.launches_per_step() * args.steps,
             "roofline": roof, "clocks": clocks, "cpu_baseline": cpu, "per_config": per_config,
