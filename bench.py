@@ -224,7 +224,17 @@ class OurRunner:
 # null.  "batch" is the batch of the captured case: traffic is scaled by
 # N / batch when the capture used a smaller batch (traffic grows in proportion).
 KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "direct_ffma": "direct.cu", "fused_ffma": "fused.cu"}
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("igemm_3xtf32", "conv3d_asym"): {
+        "bytes": 50.510080e6 + 825.202944e6, "batch": 16,
+        "sha256": "6b4daee688d97909fafeb8138b3a7e53a53bc8453aa6521d120a57227d6462ab"},
+    ("igemm_3xtf32", "conv1d_long"): {
+        "bytes": 538.055168e6 + 311.408384e6, "batch": 4,
+        "sha256": "6b4daee688d97909fafeb8138b3a7e53a53bc8453aa6521d120a57227d6462ab"},
+    ("fused_ffma", "conv3d_min_softmax"): {
+        "bytes": 37.822720e6 + 0.020736e6, "batch": 128,
+        "sha256": "a0776aa5e37642ed20e44e4d616d828e4a0864cf59f2d8a44252bfc5c4012d2e"},
+}
 
 
 def source_sha(algo):
