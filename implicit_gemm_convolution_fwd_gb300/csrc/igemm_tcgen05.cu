@@ -9,23 +9,28 @@
 // never materialised in memory: producer warps gather it straight from x
 // into tensor memory.
 //
-// Per CTA (persistent, one per SM, 416 threads):
-//   warps 0-3   epilogue: tcgen05.ld the accumulator, add bias, store y
-//               (each warp store covers 32 consecutive output positions of
-//               one channel, i.e. 128 contiguous bytes)
-//   warps 4-7   producer group 0 \  each thread owns one output position (one
-//   warps 8-11  producer group 1 /  TMEM lane) of the 128-row tile; it gathers
-//               the position's receptive field for a chunk of K, splits every
-//               value into TF32 hi + lo (hi = top 10 mantissa bits, lo = exact
-//               remainder) and writes both to TMEM with tcgen05.st.  The two
-//               groups fill alternate chunk stages.
-//   warp 12     TMEM allocation; lane 0 issues the MMAs:
-//               D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi   (M=128, N=C_out pad 32, K=8 per MMA)
+// Per CTA (persistent, one per SM, 768 threads):
+//   warps 0-3    epilogue: tcgen05.ld the accumulator, add bias, store y
+//                (each warp store covers 32 consecutive output positions of
+//                one channel, i.e. 128 contiguous bytes)
+//   warps 4-19   producers, four groups of four warps.  A thread owns one
+//                output position (one TMEM lane) of a 128-row tile; it
+//                gathers the position's receptive field for a chunk of K,
+//                splits every value into TF32 hi + lo (hi = top 10 mantissa
+//                bits, lo = exact remainder) and writes both to TMEM with
+//                tcgen05.st.
+//   warps 20-23  lane 0 of each issues the MMAs of one tile slot:
+//                D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi   (M=128, N=C_out pad 32, K=8 per MMA)
+// A slot is an independent tile pipeline: its own issuing thread, TMEM
+// accumulator and two A stages.  A thread needs ~120-145 cycles to issue one
+// tcgen05.mma with N <= 128, so several issuing threads are what keeps the
+// tensor pipe busy: four slots when C_out pads to <= 64, else two (TMEM holds
+// 512 columns).  Consecutive tiles of a CTA rotate over the slots.
 // A (im2col tile) comes from TMEM, B (weights, split hi/lo once per CTA) from
-// shared memory in the K-major no-swizzle core-matrix layout, D double-buffered
-// in TMEM.  Hand-off between roles uses mbarriers; tcgen05.commit signals MMA
-// completion.  Every wait is bounded: on timeout the kernel raises a flag,
-// lets the other roles fall through, drains its MMAs and frees TMEM.
+// shared memory in the K-major no-swizzle core-matrix layout.  Hand-off
+// between roles uses mbarriers; tcgen05.commit signals MMA completion.  Every
+// wait is bounded: on timeout the kernel raises a flag, lets the other roles
+// fall through, drains its MMAs and frees TMEM.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -69,11 +74,12 @@ struct IgemmParams {
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
   int nslots;       // tile slots (2 or 4), each with an MMA-issuing thread and an accumulator
+  int tap_major;    // reduction ordered (tap, c) instead of (c, tap); padded convs with C_in % 4 == 0
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
 struct Plan {
-  int Kred, Kpad, Npad, KC, nchunks, nslots;
+  int Kred, Kpad, Npad, KC, nchunks, nslots, tap_major;
   size_t smem;
 };
 
@@ -97,6 +103,14 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
   pl->Kred = (int)kred;
   pl->Kpad = (int)((kred + 31) / 32 * 32);
   pl->Npad = (int)((g.K + 31) / 32 * 32);
+  // Reduction order.  (c, kd, kh, kw) keeps a row of KW taps contiguous; with
+  // C_in a multiple of 4 the order (kd, kh, kw, c) instead makes every group
+  // of 4 consecutive columns share one tap, so a position near the border
+  // tests the tap's bounds once per group rather than once per column.  It is
+  // used only for padded convolutions: without padding nearly every warp takes
+  // the unchecked path, where the channel-major order reads x with better
+  // locality (consecutive columns hit the same cache lines).
+  pl->tap_major = (g.C % 4 == 0 && (g.PD > 0 || g.PH > 0 || g.PW > 0)) ? 1 : 0;
   // TMEM: one accumulator of Npad columns per slot, then two A stages per
   // slot of KC hi + KC lo columns.  Four slots (four MMA instruction streams)
   // when the accumulators leave room for 16-column stages, else two.
@@ -200,7 +214,7 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
 // 16-byte shared load and skip every bounds test; only a unit that reaches the
 // padding columns checks them.
 __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
-                                            int Kred, float (&v)[kUnit]) {
+                                            int Kred, bool tap_major, float (&v)[kUnit]) {
   if (ps.warp_full) {
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
     if (k0 + kUnit <= Kred) {
@@ -222,6 +236,21 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
         v[4 * q + 2] = k + 2 < Kred ? __ldg(ps.xo + o.z) : 0.f;
         v[4 * q + 3] = k + 3 < Kred ? __ldg(ps.xo + o.w) : 0.f;
       }
+    }
+  } else if (tap_major) {
+    // columns 4q .. 4q+3 of the unit share one tap (and padding columns come
+    // in whole groups, since Kred is then a multiple of 4)
+    const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
+#pragma unroll
+    for (int q = 0; q < kUnit / 4; ++q) {
+      const uint32_t e = ttap[k0 + 4 * q];
+      const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+      const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      const int4 o = o4[q];
+      v[4 * q + 0] = in ? __ldg(ps.xo + o.x) : 0.f;
+      v[4 * q + 1] = in ? __ldg(ps.xo + o.y) : 0.f;
+      v[4 * q + 2] = in ? __ldg(ps.xo + o.z) : 0.f;
+      v[4 * q + 3] = in ? __ldg(ps.xo + o.w) : 0.f;
     }
   } else {
 #pragma unroll
@@ -270,7 +299,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     for (int i = tid; i < words; i += kThreads) {
       const int cm = i >> 5, r = (i >> 2) & 7, cw = i & 3;
       const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
-      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kred + k) : 0.f;
+      // w is [C_out][C_in][taps]; GEMM column k maps to (c, t) by the reduction order
+      int kmem = k;
+      if (p.tap_major && k < p.Kred) {
+        const int t = k / g.C;
+        kmem = (k - t * g.C) * taps + t;
+      }
+      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kred + kmem) : 0.f;
       const float hi = __uint_as_float(tf32_hi_bits(v));
       reinterpret_cast<float *>(b_hi)[i] = hi;
       reinterpret_cast<float *>(b_lo)[i] = v - hi;
@@ -278,7 +313,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     // ---- reduction column -> (input offset, tap coordinates)
     for (int kk = tid; kk < p.Kpad; kk += kThreads) {
       if (kk < p.Kred) {
-        const int c = kk / taps, t = kk - c * taps;
+        int c, t;
+        if (p.tap_major) {
+          t = kk / g.C;
+          c = kk - t * g.C;
+        } else {
+          c = kk / taps;
+          t = kk - c * taps;
+        }
         const int kw = t % g.KW, khd = t / g.KW;
         const int kd = khd / g.KH, kh = khd - kd * g.KH;
         toff[kk] = (int32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
@@ -337,20 +379,61 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         }
       }
       float *yp = p.y + n * g.K * p.osp + pp;
-      for (int c0 = 0; c0 < p.Npad; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
-        ptx::tmem_wait_ld();
-        if (c0 + 32 >= p.Npad) {
-          ptx::tc_fence_before();
-          ptx::mbar_arrive(bar_d_empty + 8 * b);
-        }
-        if (valid) {
+      // y[n, c0 + j, pos] = accumulator column c0 + j + bias, j < 32: a warp
+      // store covers 32 consecutive positions of one channel.
+      auto store32 = [&](const uint32_t (&v)[32], int c0) {
+        if (c0 + 32 <= g.K) {
+          float *q = yp + (int64_t)c0 * p.osp;
+          const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + c0);
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4) {
+            const float4 bb = b4[j4];
+            __stcs(q, __uint_as_float(v[4 * j4 + 0]) + bb.x);
+            q += p.osp;
+            __stcs(q, __uint_as_float(v[4 * j4 + 1]) + bb.y);
+            q += p.osp;
+            __stcs(q, __uint_as_float(v[4 * j4 + 2]) + bb.z);
+            q += p.osp;
+            __stcs(q, __uint_as_float(v[4 * j4 + 3]) + bb.w);
+            q += p.osp;
+          }
+        } else {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             const int o = c0 + j;
             if (o < g.K) __stcs(yp + (int64_t)o * p.osp, __uint_as_float(v[j]) + bias_s[o]);
           }
+        }
+      };
+      // With 16-column producer chunks there are registers to read 64
+      // accumulator columns before releasing the accumulator, which lets the
+      // slot's next tile start sooner; otherwise 32 at a time.
+      if (CH == 16) {
+        for (int c0 = 0; c0 < p.Npad; c0 += 64) {
+          uint32_t v[64];
+          const bool two = c0 + 32 < p.Npad;
+          ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, *reinterpret_cast<uint32_t (*)[32]>(v));
+          if (two) ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0 + 32, *reinterpret_cast<uint32_t (*)[32]>(v + 32));
+          ptx::tmem_wait_ld();
+          if (c0 + 64 >= p.Npad) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_d_empty + 8 * b);
+          }
+          if (valid) {
+            store32(*reinterpret_cast<const uint32_t (*)[32]>(v), c0);
+            if (two) store32(*reinterpret_cast<const uint32_t (*)[32]>(v + 32), c0 + 32);
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < p.Npad; c0 += 32) {
+          uint32_t v[32];
+          ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
+          ptx::tmem_wait_ld();
+          if (c0 + 32 >= p.Npad) {
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar_d_empty + 8 * b);
+          }
+          if (valid) store32(v, c0);
         }
       }
     }
@@ -367,54 +450,64 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t my_tiles = cta_tile_count(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
+    // Chunk q of a tile: gather its K columns into registers (loads only).
+    auto gather_chunk = [&](const PosInfo &ps, int q, float (&v)[CH]) {
+      const int k0 = q * p.KC;
+      const int ncols = min(p.KC, p.Kpad - k0);
+#pragma unroll
+      for (int u = 0; u < CH / kUnit; ++u) {
+        if (u * kUnit < ncols) {
+          float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
+          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0, vu);
+        }
+      }
+    };
+    // Slot-local chunk lg (= chunk q of its tile): wait for its stage to
+    // drain, split into hi / lo, store both to TMEM and signal the issuer.
+    // The lo part overwrites v in place (keeps the chunk within the register
+    // budget without spills).  False when the wait timed out.
+    auto put_chunk = [&](int64_t lg, int q, float (&v)[CH]) -> bool {
+      const int stage = 2 * slot + (int)(lg & 1);
+      const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
+      const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
+      const int ncols = min(p.KC, p.Kpad - q * p.KC);
+      const uint32_t r = (uint32_t)(lg >> 1);
+      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int u = 0; u < CH / kUnit; ++u) {
+        if (u * kUnit < ncols) {
+          uint32_t tmp[kUnit];
+#pragma unroll
+          for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
+          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
+#pragma unroll
+          for (int j = 0; j < kUnit; j += 2)
+            ptx::sub_f32x2(v[u * kUnit + j], v[u * kUnit + j + 1], __uint_as_float(tmp[j]),
+                           __uint_as_float(tmp[j + 1]), v[u * kUnit + j], v[u * kUnit + j + 1]);
+          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit),
+                         *reinterpret_cast<const uint32_t (*)[kUnit]>(v + u * kUnit));
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_a_full + 8 * stage);
+      return true;
+    };
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
       const int64_t lg0 = li * p.nchunks;  // slot-local index of the tile's first chunk
       // this group's chunks of the tile: lg = lg0 + q with lg = sel (mod gps)
-      for (int q = (int)((sel - lg0 % gps + gps) % gps); q < p.nchunks; q += gps) {
-        const int64_t lg = lg0 + q;
-        const int stage = 2 * slot + (int)(lg & 1);
-        const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
-        const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
-        const int k0 = q * p.KC;
-        const int ncols = min(p.KC, p.Kpad - k0);
+      int q = (int)((sel - lg0 % gps + gps) % gps);
+      for (; q < p.nchunks; q += gps) {
         float v[CH];
-#pragma unroll
-        for (int u = 0; u < CH / kUnit; ++u) {
-          if (u * kUnit < ncols) {
-            float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-            gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, vu);
-          }
-        }
-        const uint32_t r = (uint32_t)(lg >> 1);
-        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
+        gather_chunk(ps, q, v);
+        if (!put_chunk(lg0 + q, q, v)) {
           aborted = true;
           break;
         }
-        ptx::tc_fence_after();
-#pragma unroll
-        for (int u = 0; u < CH / kUnit; ++u) {
-          if (u * kUnit < ncols) {
-            uint32_t tmp[kUnit];
-#pragma unroll
-            for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
-            ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
-#pragma unroll
-            for (int j = 0; j < kUnit; j += 2) {
-              float l0, l1;
-              ptx::sub_f32x2(v[u * kUnit + j], v[u * kUnit + j + 1], __uint_as_float(tf32_hi_bits(v[u * kUnit + j])),
-                             __uint_as_float(tf32_hi_bits(v[u * kUnit + j + 1])), l0, l1);
-              tmp[j] = __float_as_uint(l0);
-              tmp[j + 1] = __float_as_uint(l1);
-            }
-            ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit), tmp);
-          }
-        }
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_a_full + 8 * stage);
       }
     }
   } else if (lane == 0 && warp - kMmaWarp < nslots) {
@@ -520,6 +613,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.KC = pl.KC;
   p.nchunks = pl.nchunks;
   p.nslots = pl.nslots;
+  p.tap_major = pl.tap_major;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
   if (pl.KC <= 16)
