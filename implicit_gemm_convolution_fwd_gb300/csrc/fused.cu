@@ -33,6 +33,11 @@ constexpr int kCO = 12;  // channels per thread
 constexpr int kR = 4;    // columns per thread
 constexpr int kMaxKW = 7;
 constexpr int kMaxSmemBytes = 200 * 1024;
+// A lane reads input columns ow0 .. ow0 + 5 of a shared row (ow0 <= 28) whatever
+// the input width, so the last row of a ring can be over-read by up to 26
+// floats when the row pitch is short; the shared-memory allocation carries
+// this many floats of slack past the last ring.
+constexpr int kRingSlackFloats = 32;
 
 struct FusedParams {
   const float *__restrict__ x;
@@ -449,7 +454,7 @@ bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
   int64_t bytes = 0;
   for (; nb >= 1; nb /= 2) {
     ring = g.KD + 2 * nb - 1;
-    bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot);
+    bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot + kRingSlackFloats);
     if (bytes <= kMaxSmemBytes) break;
   }
   if (nb < 1) return false;
@@ -539,7 +544,7 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    const size_t smem = 4 * ((size_t)sp.w_floats + (size_t)sp.ring * sp.slot_floats);
+    const size_t smem = 4 * ((size_t)sp.w_floats + (size_t)sp.ring * sp.slot_floats + kRingSlackFloats);
     // the benchmark shape (C_in 3, kernel 3^3, W 32 -> pitch 36, 30 shared rows) is specialised
     const bool spec = g.C == 3 && g.KD == 3 && g.KH == 3 && sp.WP == 36 && sp.srows_max == 30;
     auto kern = spec ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30> : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0>;

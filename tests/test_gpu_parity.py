@@ -280,3 +280,19 @@ def test_fused_staged_multi_image_blocks():
         assert_close(run_fused(x, w, b).cpu().numpy(), ref, f"fused staged C_out={C_out} N={N}")
         assert_close(run_fused(x, w, None).cpu().numpy(), oracle.conv3d_min_softmax(x, w, None),
                      f"fused staged no bias C_out={C_out}")
+
+
+def test_fused_narrow_rows_and_many_rows_per_sm():
+    # W = 8: a short shared-row pitch, so lanes of the garbage columns read
+    # past the last row of a ring (into the allocation's slack)
+    rng = np.random.default_rng(23)
+    x = rng.random((3, 2, 5, 6, 8)).astype(np.float32)
+    w = ((rng.random((7, 2, 3, 3, 3)) - 0.5) * 0.5).astype(np.float32)
+    b = ((rng.random(7) - 0.5) * 0.5).astype(np.float32)
+    assert_close(run_fused(x, w, b).cpu().numpy(), oracle.conv3d_min_softmax(x, w, b), "fused W=8")
+    # N * OH = 4200 rows: more rows per CTA than warps, so warps take several rows
+    x = rng.random((140, 3, 5, 32, 32)).astype(np.float32)
+    w = ((rng.random((24, 3, 3, 3, 3)) - 0.5) * 0.3).astype(np.float32)
+    b = ((rng.random(24) - 0.5) * 0.3).astype(np.float32)
+    y = run_fused(x, w, b).cpu().numpy()
+    assert_close(y, oracle.conv3d_min_softmax(x, w, b), "fused 4200 rows")
