@@ -245,6 +245,19 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const float *src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+// Wait until at most n of this thread's cp.async groups are pending (n clamped to [0, 7]).
+__device__ __forceinline__ void cp_async_wait_pending(int n) {
+  switch (n < 0 ? 0 : n) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    case 3: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    case 4: asm volatile("cp.async.wait_group 4;" ::: "memory"); break;
+    case 5: asm volatile("cp.async.wait_group 5;" ::: "memory"); break;
+    case 6: asm volatile("cp.async.wait_group 6;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 7;" ::: "memory"); break;
+  }
+}
 
 // CT, KDT, KHT, WPT, SRT: compile-time C_in, KD, KH, shared row pitch and
 // shared rows per channel (0 = runtime); the benchmark shape is specialised
@@ -265,14 +278,21 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
   const int taps = KD * KH * 3;
   const int64_t HW = (int64_t)g.H * g.W;
 
-  for (int i = tid; i < C * KD * KH * kSWRow; i += kSThreads) {
-    const int row = i / kSWRow, rem = i - row * kSWRow;
-    const int cgi = rem / kSWStride, jj = rem - cgi * kSWStride;
-    float v = 0.f;
-    const int kw = jj / kSWTap, o = jj - kw * kSWTap, oc = cgi * kSCO + o;
-    if (o < kSCO && oc < g.K) v = p.w[(int64_t)oc * C * taps + row * 3 + kw];
-    ws[i] = v;
-  }
+  __shared__ float bias_s[kSNcg * kSCO];
+  // weights (and bias) -> shared memory; run once, after the first input
+  // planes are requested, so that both loads are in flight together
+  auto stage_weights = [&]() {
+    for (int i = tid; i < C * KD * KH * kSWRow; i += kSThreads) {
+      const int row = i / kSWRow, rem = i - row * kSWRow;
+      const int cgi = rem / kSWStride, jj = rem - cgi * kSWStride;
+      float v = 0.f;
+      const int kw = jj / kSWTap, o = jj - kw * kSWTap, oc = cgi * kSCO + o;
+      if (o < kSCO && oc < g.K) v = p.w[(int64_t)oc * C * taps + row * 3 + kw];
+      ws[i] = v;
+    }
+    if (tid < kSNcg * kSCO) bias_s[tid] = (p.bias && tid < g.K) ? __ldg(p.bias + tid) : 0.f;
+  };
+  bool weights_staged = false;
   // The ring is not cleared: the padding columns past W feed only output
   // columns >= OW, which are never stored, and each column's softmax is
   // independent of the others.
@@ -288,41 +308,84 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     const int nrows = (int)min64(kSRows, r_end - r0);
     const int64_t n0 = r0 / g.OH;
     __syncthreads();  // the previous block's readers are done with the ring and the row table
-    if (tid == 0) {
-      // shared rows: per image in the block, its output rows plus KH-1 halo rows
-      int srow = 0;
-      for (int lr = 0; lr < nrows;) {
-        const int64_t r = r0 + lr;
-        const int64_t n = r / g.OH;
-        const int oh_lo = (int)(r - n * g.OH);
-        const int cnt = (int)min64(nrows - lr, g.OH - oh_lo);
-        for (int k = 0; k < cnt + g.KH - 1; ++k)
-          srow_src[srow + k] = n * g.C * g.D * HW + (int64_t)(oh_lo + k) * g.W;
-        srow += cnt + g.KH - 1;
-        lr += cnt;
+    // Shared rows: per image the block touches, its output rows plus KH - 1
+    // halo rows.  Thread s fills entry s by walking the (at most a few)
+    // image segments of the block.
+    const int oh_lo0 = (int)(r0 - n0 * g.OH);
+    if (tid < kSMaxSrows) {
+      int start = 0, rem = nrows, lo = oh_lo0;
+      int64_t n = n0;
+      while (rem > 0) {
+        const int cnt = min(rem, g.OH - lo);
+        const int len = cnt + g.KH - 1;
+        if (tid < start + len) {
+          srow_src[tid] = n * g.C * g.D * HW + (int64_t)(lo + tid - start) * g.W;
+          break;
+        }
+        start += len;
+        rem -= cnt;
+        ++n;
+        lo = 0;
       }
-      nsrows_s = srow;
+      if (tid == 0) {
+        int total = 0;
+        for (int rr = nrows, l = oh_lo0; rr > 0; l = 0) {
+          const int cnt = min(rr, g.OH - l);
+          total += cnt + g.KH - 1;
+          rr -= cnt;
+        }
+        nsrows_s = total;
+      }
     }
     __syncthreads();
     const int nsrows = nsrows_s;
 
+    // Copies of one input plane: thread -> (shared row s, 16-byte unit q),
+    // looping over the C channels (fixed strides), so that issuing a plane
+    // costs a few instructions per copy and no divisions.
+    const int per_plane_sq = nsrows * WQ;
+    const int sq0 = tid;
+    const int s0 = sq0 < per_plane_sq ? sq0 / WQ : 0, q0 = sq0 - s0 * WQ;
+    const int64_t src0 = sq0 < per_plane_sq ? srow_src[s0] + (int64_t)q0 * (p.vec ? 4 : 1) : 0;
+    const uint32_t dst0 = 4u * (uint32_t)(s0 * p.WP) + (p.vec ? 16u : 4u) * (uint32_t)q0;
+    const int64_t c_stride_src = (int64_t)g.D * HW;
+    const uint32_t c_stride_dst = 4u * (uint32_t)(p.srows_max * p.WP);
+    int slot_of_next = 0;  // ring slot of the next plane issued (planes are issued in order)
     auto issue_plane = [&](int dd) {
-      const uint32_t slot = ring_addr + 4u * (uint32_t)(dd % p.ring) * p.slot_floats;
-      const int per_c = nsrows * WQ;
-      for (int i = tid; i < (int)g.C * per_c; i += kSThreads) {
-        const int c = i / per_c, rest = i - c * per_c;
-        const int s = rest / WQ, q = rest - s * WQ;
-        const float *src = p.x + srow_src[s] + ((int64_t)c * g.D + dd) * HW;
-        const uint32_t dst = slot + 4u * (uint32_t)((c * p.srows_max + s) * p.WP);
-        if (p.vec)
-          cp_async16(dst + 16u * q, src + 4 * q);
-        else
-          cp_async4(dst + 4u * q, src + q);
+      const uint32_t slot = ring_addr + 4u * (uint32_t)slot_of_next * p.slot_floats;
+      slot_of_next = (slot_of_next + 1 == p.ring) ? 0 : slot_of_next + 1;
+      const int64_t dd_off = (int64_t)dd * HW;
+      if (sq0 < per_plane_sq) {
+        const float *src = p.x + src0 + dd_off;
+        uint32_t dst = slot + dst0;
+        for (int c = 0; c < C; ++c, src += c_stride_src, dst += c_stride_dst) {
+          if (p.vec)
+            cp_async16(dst, src);
+          else
+            cp_async4(dst, src);
+        }
+      }
+      // rare: more (row, unit) pairs than threads
+      for (int i = sq0 + kSThreads; i < per_plane_sq; i += kSThreads) {
+        const int si = i / WQ, qi = i - si * WQ;
+        const float *src = p.x + srow_src[si] + dd_off + (int64_t)qi * (p.vec ? 4 : 1);
+        uint32_t dst = slot + 4u * (uint32_t)(si * p.WP) + (p.vec ? 16u : 4u) * (uint32_t)qi;
+        for (int c = 0; c < C; ++c, src += c_stride_src, dst += c_stride_dst) {
+          if (p.vec)
+            cp_async16(dst, src);
+          else
+            cp_async4(dst, src);
+        }
       }
       cp_async_commit();
     };
     // the first group's planes: 0 .. nb + KD - 2, one commit group per plane
-    for (int dd = 0; dd < p.nb + KD - 1 && dd < g.D; ++dd) issue_plane(dd);
+    int issued = 0;  // commit groups issued in this block (one per plane)
+    for (int dd = 0; dd < p.nb + KD - 1 && dd < g.D; ++dd, ++issued) issue_plane(dd);
+    if (!weights_staged) {
+      stage_weights();
+      weights_staged = true;
+    }
 
     // this lane's output row and its shared-memory row
     const int lr = warp;
@@ -341,10 +404,19 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 
     int s_od = 0;  // ring slot of plane od
     for (int od = 0; od < g.OD; ++od) {
-      if ((od % p.nb) == 0) {
+      if ((od % p.nb) == 0 && od > 0) {
         cp_async_wait_all();
         __syncthreads();  // this group's planes are in; the previous group's slots are free
         for (int dd = od + p.nb + KD - 1; dd < od + 2 * p.nb + KD - 1 && dd < g.D; ++dd) issue_plane(dd);
+      } else if (od == 0) {
+        // first group: depth 0 starts as soon as its KD planes are in ...
+        cp_async_wait_pending(issued - KD);
+        __syncthreads();
+        for (int dd = p.nb + KD - 1; dd < 2 * p.nb + KD - 1 && dd < g.D; ++dd, ++issued) issue_plane(dd);
+      } else if (od == 1) {
+        // ... and depth 1 waits for the rest of the group's planes
+        cp_async_wait_pending(issued - (int)min64(p.nb + KD - 1, g.D));
+        __syncthreads();
       }
       // acc2[op][r]: channels (2*op, 2*op + 1) at column r, packed
       unsigned long long acc2[kSCO / 2][kR];
@@ -413,7 +485,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 #pragma unroll
       for (int o = 0; o < kSCO; ++o) {
         const int oc = cg * kSCO + o;
-        v[o] = oc < g.K ? mins[o][r] + (p.bias ? __ldg(p.bias + oc) : 0.f) : -INFINITY;
+        v[o] = oc < g.K ? mins[o][r] + bias_s[oc] : -INFINITY;
         mx = fmaxf(mx, v[o]);
       }
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, NOWG));
@@ -426,13 +498,14 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       }
       ssum += __shfl_xor_sync(0xffffffffu, ssum, NOWG);
       ssum += __shfl_xor_sync(0xffffffffu, ssum, 2 * NOWG);
+      const float inv = 1.f / ssum;
       const int ow = ow0 + r;
       if (row_ok && ow < g.OW) {
         float *yo = p.y + n * g.K * OHW + (int64_t)oh * g.OW + ow;
 #pragma unroll
         for (int o = 0; o < kSCO; ++o) {
           const int oc = cg * kSCO + o;
-          if (oc < g.K) yo[(int64_t)oc * OHW] = v[o] / ssum;
+          if (oc < g.K) yo[(int64_t)oc * OHW] = v[o] * inv;
         }
       }
     }
@@ -450,12 +523,16 @@ bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
   const int WP = (g.W + 3) / 4 * 4 + 4;
   const int64_t w_floats = (int64_t)g.C * g.KD * g.KH * kSWRow;
   const int64_t slot = (int64_t)g.C * srows * WP;
-  int nb = 4, ring = 0;
-  int64_t bytes = 0;
-  for (; nb >= 1; nb /= 2) {
-    ring = g.KD + 2 * nb - 1;
-    bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot + kRingSlackFloats);
-    if (bytes <= kMaxSmemBytes) break;
+  // output depths per block-wide barrier: the largest of 4, 2, 1 whose ring
+  // (KD + 2 * nb - 1 planes) fits (6 measured no faster than 4)
+  int nb = 0, ring = 0;
+  for (const int cand : {4, 2, 1}) {
+    ring = g.KD + 2 * cand - 1;
+    const int64_t bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot + kRingSlackFloats);
+    if (bytes <= kMaxSmemBytes) {
+      nb = cand;
+      break;
+    }
   }
   if (nb < 1) return false;
   sp->nb = nb;
