@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       float ssum = 0.f;
 #pragma unroll
       for (int o = 0; o < kSCO; ++o) {
-        v[o] = expf(v[o] - mx);
+        v[o] = __expf(v[o] - mx);
         ssum += v[o];
       }
       ssum += __shfl_xor_sync(0xffffffffu, ssum, NOWG);
