@@ -42,8 +42,8 @@ def _load():
         lib.oracle_conv_nd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, i32]
         lib.oracle_conv_nd_at.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, vp, i64, vp, i32]
         lib.oracle_input_read_counts.argtypes = [i32, vp, vp, vp, vp, vp, vp]
-        lib.oracle_conv3d_min_softmax.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32]
-        lib.oracle_conv3d_min_softmax_at.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, vp, i64, vp, i32]
+        lib.oracle_conv3d_min_softmax.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32]
+        lib.oracle_conv3d_min_softmax_at.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, vp, i64, vp, i32]
         for f in (lib.oracle_out_dims, lib.oracle_conv_nd, lib.oracle_conv_nd_at, lib.oracle_input_read_counts,
                   lib.oracle_conv3d_min_softmax, lib.oracle_conv3d_min_softmax_at):
             f.restype = i32
@@ -135,8 +135,16 @@ def input_read_counts(in_dims, k, stride, pad, dilation):
     return counts
 
 
-def conv3d_min_softmax(x, w, bias, nthreads=None):
-    """float64 [N, C_out, OH, OW]: softmax_o(min_d(conv3d(x, w) + b)), stride 1, pad 0, dilation 1."""
+def _kept_axes(min_dim):
+    """The two spatial output axes (0 = D, 1 = H, 2 = W) left after the min over tensor dim min_dim."""
+    if min_dim not in (2, 3, 4):
+        raise OracleError("min_dim must be 2, 3 or 4")
+    return [a for a in range(3) if a != min_dim - 2]
+
+
+def conv3d_min_softmax(x, w, bias, min_dim=2, nthreads=None):
+    """float64 softmax_o(min over tensor dim min_dim of conv3d(x, w) + b), stride 1, pad 0, dilation 1.
+    Shape [N, C_out, OH, OW] (min_dim 2), [N, C_out, OD, OW] (3) or [N, C_out, OD, OH] (4)."""
     x, w = _f32(x), _f32(w)
     b = None if bias is None else _f32(bias)
     N, C_in = x.shape[:2]
@@ -145,25 +153,28 @@ def conv3d_min_softmax(x, w, bias, nthreads=None):
     od = out_dims(x.shape[2:], w.shape[2:], (1, 1, 1), (0, 0, 0), (1, 1, 1))
     if min(od) <= 0:
         raise OracleError("non-positive output size")
-    y = np.empty((N, C_out, od[1], od[2]), np.float64)
+    ka, kb = _kept_axes(min_dim)
+    y = np.empty((N, C_out, od[ka], od[kb]), np.float64)
     rc = _load().oracle_conv3d_min_softmax(_ptr(x), _ptr(w), _ptr(b), _ptr(y), N, C_in, C_out, _ptr(ins),
-                                           _ptr(ks), nthreads or threads())
+                                           _ptr(ks), min_dim, nthreads or threads())
     if rc:
         raise OracleError("oracle_conv3d_min_softmax rejected its arguments")
     return y
 
 
-def conv3d_min_softmax_at(x, w, bias, cols, nthreads=None):
-    """float64 [len(cols), C_out]; cols are flat (n, h, w) indices of the [N, OH, OW] output grid."""
+def conv3d_min_softmax_at(x, w, bias, cols, min_dim=2, nthreads=None):
+    """float64 [len(cols), C_out]; cols are flat (n, a, b) indices of the [N, OA, OB] output grid
+    (a, b: the two spatial axes kept after the min over tensor dim min_dim)."""
     x, w = _f32(x), _f32(w)
     b = None if bias is None else _f32(bias)
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
     ins, ks = _i64(x.shape[2:]), _i64(w.shape[2:])
+    _kept_axes(min_dim)
     cols = _i64(cols)
     out = np.empty((cols.size, C_out), np.float64)
     rc = _load().oracle_conv3d_min_softmax_at(_ptr(x), _ptr(w), _ptr(b), N, C_in, C_out, _ptr(ins), _ptr(ks),
-                                              _ptr(cols), cols.size, _ptr(out), nthreads or threads())
+                                              min_dim, _ptr(cols), cols.size, _ptr(out), nthreads or threads())
     if rc:
         raise OracleError("oracle_conv3d_min_softmax_at rejected its arguments")
     return out

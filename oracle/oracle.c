@@ -16,8 +16,10 @@
  *   out_i = floor((in_i + 2*pad_i - dil_i*(k_i-1) - 1) / stride_i) + 1
  *   y[n,o,p] = b[o] + sum_c sum_k w[o,c,k] * x[n,c, p*stride + k*dil - pad]
  *              where a tap whose input coordinate falls outside [0, in_i) reads 0
- *   fused: z = conv (stride 1, pad 0, dil 1);  m[n,o,h,w] = min_d z[n,o,d,h,w];
- *          y[n,o,h,w] = exp(m - max_o m) / sum_o exp(m - max_o m)
+ *   fused: z = conv (stride 1, pad 0, dil 1);  m = min of z over one spatial
+ *          dim (depth on the page; height or width when asked), e.g.
+ *          m[n,o,h,w] = min_d z[n,o,d,h,w];
+ *          y = exp(m - max_o m) / sum_o exp(m - max_o m)
  *
  * Parity pins for every function live in tests/test_oracle.py (closed forms,
  * library cross-checks, the pages' worked shape values).
@@ -266,24 +268,26 @@ int oracle_input_read_counts(int ndim, const int64_t *in, const int64_t *k, cons
 typedef struct {
   const geom_t *g; /* 3-D geometry, stride 1, pad 0, dil 1 */
   const float *x, *w, *bias;
-  double *y;             /* [N, K, OH, OW] (full) or [count, K] (sampled) */
-  const int64_t *cols;   /* sampled (n, h, w) column indices, or NULL for all */
+  double *y;             /* [N, K, OA, OB] (full) or [count, K] (sampled) */
+  const int64_t *cols;   /* sampled (n, a, b) column indices, or NULL for all */
   int64_t ncols;
   double *scratch;       /* per-task m[K] buffers: ntasks x K */
+  int r, a, b;           /* spatial output axes (0 = D, 1 = H, 2 = W): reduced, kept, kept */
 } fused_ctx_t;
 
-/* Softmax over channels of min-over-depth conv, for one (n, h, w) column.
- * m_out: K doubles of workspace; res[o * res_stride] receives the result. */
-static void fused_column(const fused_ctx_t *c, int64_t n, int64_t h, int64_t wq, double *m, double *res,
+/* Softmax over channels of the conv's minimum along spatial axis r, for one
+ * (n, a, b) column (a, b: coordinates along the two kept axes, in order).
+ * m: K doubles of workspace; res[o * res_stride] receives the result. */
+static void fused_column(const fused_ctx_t *c, int64_t n, int64_t ia, int64_t ib, double *m, double *res,
                          int64_t res_stride) {
   const geom_t *g = c->g;
   int64_t op[MAXD];
   for (int64_t o = 0; o < g->K; ++o) {
     double mn = INFINITY;
-    for (int64_t dd = 0; dd < g->out[0]; ++dd) {
-      op[0] = dd;
-      op[1] = h;
-      op[2] = wq;
+    for (int64_t rr = 0; rr < g->out[c->r]; ++rr) {
+      op[c->r] = rr;
+      op[c->a] = ia;
+      op[c->b] = ib;
       double z = conv_point(g, c->x, c->w, c->bias, n, o, op);
       if (z < mn) mn = z;
     }
@@ -301,52 +305,57 @@ static void fused_task(void *vctx, int64_t task) {
   fused_ctx_t *c = (fused_ctx_t *)vctx;
   const geom_t *g = c->g;
   double *m = c->scratch + task * g->K;
-  int64_t OH = g->out[1], OW = g->out[2];
+  int64_t OA = g->out[c->a], OB = g->out[c->b];
   if (c->cols) {
     int64_t col = c->cols[task];
-    int64_t n = col / (OH * OW), h = (col / OW) % OH, wq = col % OW;
-    fused_column(c, n, h, wq, m, c->y + task * g->K, 1);
+    int64_t n = col / (OA * OB), ia = (col / OB) % OA, ib = col % OB;
+    fused_column(c, n, ia, ib, m, c->y + task * g->K, 1);
   } else {
-    int64_t n = task / (OH * OW), h = (task / OW) % OH, wq = task % OW;
-    /* y[n, o, h, w] */
-    fused_column(c, n, h, wq, m, c->y + n * g->K * OH * OW + h * OW + wq, OH * OW);
+    int64_t n = task / (OA * OB), ia = (task / OB) % OA, ib = task % OB;
+    /* y[n, o, a, b] */
+    fused_column(c, n, ia, ib, m, c->y + n * g->K * OA * OB + ia * OB + ib, OA * OB);
   }
 }
 
 static int fused_common(const float *x, const float *w, const float *bias, double *y, int64_t N, int64_t C_in,
-                        int64_t C_out, const int64_t *in3, const int64_t *k3, const int64_t *cols,
+                        int64_t C_out, const int64_t *in3, const int64_t *k3, int min_dim, const int64_t *cols,
                         int64_t ncols, int nthreads) {
   geom_t g;
   const int64_t one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
   if (!x || !w || !y || !in3 || !k3) return 1;
+  if (min_dim < 2 || min_dim > 4) return 1;
   if (make_geom(&g, 3, N, C_in, C_out, in3, k3, one, zero, one)) return 1;
-  int64_t ntasks = cols ? ncols : N * g.out[1] * g.out[2];
+  /* tensor dim min_dim of [N, C, D, H, W] is spatial axis min_dim - 2; the
+   * other two spatial axes stay, in their order */
+  const int r = min_dim - 2, a = (r == 0) ? 1 : 0, b = (r == 2) ? 1 : 2;
+  int64_t ntasks = cols ? ncols : N * g.out[a] * g.out[b];
   if (cols) {
     for (int64_t i = 0; i < ncols; ++i)
-      if (cols[i] < 0 || cols[i] >= N * g.out[1] * g.out[2]) return 1;
+      if (cols[i] < 0 || cols[i] >= N * g.out[a] * g.out[b]) return 1;
   }
   double *scratch = (double *)malloc(sizeof(double) * (size_t)(ntasks > 0 ? ntasks : 1) * (size_t)C_out);
   if (!scratch) return 1;
-  fused_ctx_t ctx = {&g, x, w, bias, y, cols, ncols, scratch};
+  fused_ctx_t ctx = {&g, x, w, bias, y, cols, ncols, scratch, r, a, b};
   run_tasks(fused_task, &ctx, ntasks, nthreads);
   free(scratch);
   return 0;
 }
 
-/* y (double, [N, C_out, OH, OW]) = softmax over channels of min over output
- * depth of conv3d(x, w) + bias (stride 1, pad 0, dilation 1).  in3 = (D,H,W),
- * k3 = (KD,KH,KW).  bias may be NULL. */
+/* y (double) = softmax over channels (dim 1) of the minimum over tensor dim
+ * min_dim (2 = depth, 3 = height, 4 = width) of conv3d(x, w) + bias (stride 1,
+ * pad 0, dilation 1): [N, C_out, OH, OW] for min_dim 2, [N, C_out, OD, OW] for
+ * 3, [N, C_out, OD, OH] for 4.  in3 = (D,H,W), k3 = (KD,KH,KW).  bias may be NULL. */
 int oracle_conv3d_min_softmax(const float *x, const float *w, const float *bias, double *y, int64_t N,
-                              int64_t C_in, int64_t C_out, const int64_t *in3, const int64_t *k3,
+                              int64_t C_in, int64_t C_out, const int64_t *in3, const int64_t *k3, int min_dim,
                               int nthreads) {
-  return fused_common(x, w, bias, y, N, C_in, C_out, in3, k3, NULL, 0, nthreads);
+  return fused_common(x, w, bias, y, N, C_in, C_out, in3, k3, min_dim, NULL, 0, nthreads);
 }
 
-/* Same, for selected columns only: out[i*C_out + o] = y[n, o, h, w] where
- * cols[i] = (n*OH + h)*OW + w. */
+/* Same, for selected columns only: out[i*C_out + o] = y[n, o, a, b] where
+ * cols[i] = (n*OA + a)*OB + b over the two kept output axes. */
 int oracle_conv3d_min_softmax_at(const float *x, const float *w, const float *bias, int64_t N, int64_t C_in,
-                                 int64_t C_out, const int64_t *in3, const int64_t *k3, const int64_t *cols,
-                                 int64_t ncols, double *out, int nthreads) {
+                                 int64_t C_out, const int64_t *in3, const int64_t *k3, int min_dim,
+                                 const int64_t *cols, int64_t ncols, double *out, int nthreads) {
   if (!cols || ncols < 0) return 1;
-  return fused_common(x, w, bias, out, N, C_in, C_out, in3, k3, cols, ncols, nthreads);
+  return fused_common(x, w, bias, out, N, C_in, C_out, in3, k3, min_dim, cols, ncols, nthreads);
 }

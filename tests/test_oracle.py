@@ -268,3 +268,49 @@ def test_fused_sampled_columns_equal_full():
     got = oracle.conv3d_min_softmax_at(x, w, b, cols)
     ref = y.transpose(0, 2, 3, 1).reshape(-1, C_out)[cols]
     assert np.array_equal(got, ref)
+
+
+# ------------------------------------------- fused, min over height or width
+
+@pytest.mark.parametrize("min_dim", [2, 3, 4])
+def test_fused_min_dim_matches_torch_float64(min_dim):
+    # torch.min(z, dim=min_dim) then softmax over dim 1, on the same 5-D conv
+    x, w, b = _fused_inputs(11 + min_dim, N=2, C_in=3, C_out=7, ins=(7, 6, 9), k=(3, 2, 4))
+    y = oracle.conv3d_min_softmax(x, w, b, min_dim)
+    z = F.conv3d(torch.from_numpy(x).double(), torch.from_numpy(w).double(), torch.from_numpy(b).double())
+    ref = torch.softmax(torch.min(z, dim=min_dim).values, dim=1).numpy()
+    assert y.shape == ref.shape
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("min_dim", [3, 4])
+def test_fused_min_dim_is_depth_min_of_permuted_problem(min_dim):
+    # min over H (W) of conv(x, w) = min over depth of conv(x', w') with the
+    # depth axis and the H (W) axis of both x and w exchanged; the kept axes
+    # come out in the permuted order
+    x, w, b = _fused_inputs(21 + min_dim, N=2, C_in=2, C_out=6, ins=(6, 8, 7), k=(2, 3, 4))
+    y = oracle.conv3d_min_softmax(x, w, b, min_dim)
+    xp = np.ascontiguousarray(np.swapaxes(x, 2, min_dim))
+    wp = np.ascontiguousarray(np.swapaxes(w, 2, min_dim))
+    yp = oracle.conv3d_min_softmax(xp, wp, b, 2)
+    if min_dim == 4:
+        yp = np.swapaxes(yp, 2, 3)  # (H, D) -> (D, H)
+    np.testing.assert_allclose(y, yp, rtol=1e-12, atol=1e-15)
+
+
+@pytest.mark.parametrize("min_dim", [3, 4])
+def test_fused_min_dim_rows_and_sampled_columns(min_dim):
+    x, w, b = _fused_inputs(31 + min_dim)
+    y = oracle.conv3d_min_softmax(x, w, b, min_dim)
+    assert np.abs(y.sum(axis=1) - 1.0).max() < 1e-12
+    N, C_out, OA, OB = y.shape
+    cols = np.array([0, 3, OA * OB - 1, OA * OB, N * OA * OB - 1], np.int64)
+    got = oracle.conv3d_min_softmax_at(x, w, b, cols, min_dim)
+    assert np.array_equal(got, y.transpose(0, 2, 3, 1).reshape(-1, C_out)[cols])
+
+
+def test_fused_rejects_bad_min_dim():
+    x, w, b = _fused_inputs(41)
+    for bad in (0, 1, 5):
+        with pytest.raises(oracle.OracleError):
+            oracle.conv3d_min_softmax(x, w, b, bad)
