@@ -154,7 +154,9 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
 
 
 def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None):
-    """softmax_o(min_d(conv3d(x, w) + bias)) for contiguous fp32 CUDA tensors (stride 1, no padding)."""
+    """softmax over channels of the min over tensor dim `min_dim` (2 = depth, 3 = height, 4 = width)
+    of conv3d(x, w) + bias, for contiguous fp32 CUDA tensors (stride 1, no padding).  The result
+    keeps the two other spatial dims: [N, C_out, OH, OW], [N, C_out, OD, OW] or [N, C_out, OD, OH]."""
     import torch
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x and w must be 5-D")

@@ -242,9 +242,7 @@ int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const f
   if (!x || !w || !y) return fail(CONV_ERR_NULL, "conv3d_min_softmax: descriptor pointer is NULL%s");
   if (!w->data || (x->dims[0] != 0 && (!x->data || !y->data)))
     return fail(CONV_ERR_NULL, "conv3d_min_softmax: tensor data is NULL%s");
-  if (min_dim == 3 || min_dim == 4)
-    return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: min_dim %s%lld not implemented (only 2)", "", min_dim);
-  if (min_dim != 2) return fail(CONV_ERR_ARG, "conv3d_min_softmax: min_dim must be 2, 3 or 4%s");
+  if (min_dim < 2 || min_dim > 4) return fail(CONV_ERR_ARG, "conv3d_min_softmax: min_dim must be 2, 3 or 4%s");
   for (int i = 0; i < 5; ++i) {
     if (x->dims[i] < (i == 0 ? 0 : 1) || x->dims[i] > kMaxDim)
       return fail(CONV_ERR_ARG, "conv3d_min_softmax: bad x dim%s");
@@ -265,13 +263,18 @@ int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const f
   int st = validate_conv(x->data, w->data, bias, yd, 3, x->dims[0], x->dims[1], w->dims[0], ins, ks, one, zero,
                          one, &g, y4);
   if (st != CONV_OK) return st;
-  if (y->dims[0] != g.N || y->dims[1] != g.K || y->dims[2] != g.OH || y->dims[3] != g.OW)
-    return fail(CONV_ERR_SHAPE, "conv3d_min_softmax: y dims must be [N, C_out, H_out, W_out]%s");
+  // the output keeps the two spatial axes other than min_dim, in order
+  const int64_t ya = (min_dim == 2) ? g.OH : g.OD, yb = (min_dim == 4) ? g.OH : g.OW;
+  if (y->dims[0] != g.N || y->dims[1] != g.K || y->dims[2] != ya || y->dims[3] != yb)
+    return fail(CONV_ERR_SHAPE,
+                "conv3d_min_softmax: y dims must be [N, C_out] + the conv's spatial output dims without dim "
+                "min_dim%s");
   const char *why = "";
-  if (!convfwd::fused_supported(g, &why))
+  if (!convfwd::fused_supported(g, min_dim, &why))
     return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
   if (g.N == 0) return CONV_OK;  // empty batch
-  cudaError_t e = convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream);
+  cudaError_t e =
+      convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: kernel launch");
   return CONV_OK;
 }

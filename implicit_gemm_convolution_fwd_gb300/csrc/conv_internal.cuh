@@ -31,12 +31,13 @@ bool direct_supported(const Geom &g, const char **why);
 cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias, float *y, const Geom &g,
                                cudaStream_t stream);
 
-// Fused conv3d -> min over output depth -> channel softmax.
+// Fused conv3d -> min over tensor dim min_dim (2 = depth, 3 = height,
+// 4 = width) -> channel softmax.
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
-                                     const Geom &g, cudaStream_t stream);
+                                     const Geom &g, int min_dim, cudaStream_t stream);
 // True when launch_fused_min_softmax supports this geometry (channel count,
-// kernel width, shared-memory footprint).
-bool fused_supported(const Geom &g, const char **why);
+// kernel extent along the output's last axis, shared-memory footprint).
+bool fused_supported(const Geom &g, int min_dim, const char **why);
 
 // Tensor-core implicit GEMM (tcgen05, 3xTF32).
 bool igemm_supported(const Geom &g, const char **why);

@@ -3,9 +3,11 @@
 // turns 1-2: for every (n, h, w) column the conv is evaluated at every output
 // depth, a running minimum per channel is kept, and the channel softmax is
 // taken with the maximum subtracted.  The 5-D conv intermediate never leaves
-// registers.
+// registers.  The page's module takes the min dimension as a constructor
+// argument; the generic kernel also reduces over height or width (min_dim 3,
+// 4) by giving the spatial axes roles: R (reduced), A (rows), B (columns).
 //
-// Mapping: one warp owns NROW output rows (n, oh) and a tile of NOWG*R output
+// Mapping: one warp owns NROW output rows (n, oa) and a tile of NOWG*R output
 // columns; lane = (row, channel group, column group).  A thread keeps a CO x R
 // register tile (CO output channels x R consecutive columns) of conv sums for
 // the current depth plus the running minima.  Weights for all channels sit in
@@ -39,19 +41,29 @@ constexpr int kMaxSmemBytes = 200 * 1024;
 // this many floats of slack past the last ring.
 constexpr int kRingSlackFloats = 32;
 
+// The three spatial output axes in the roles the kernel gives them: R is the
+// reduced (min) axis, A the row axis and B the column axis (consecutive
+// columns per thread).  For the page's min over depth, (R, A, B) = (D, H, W).
 struct FusedParams {
   const float *__restrict__ x;
   const float *__restrict__ w;
   const float *__restrict__ bias;
   float *__restrict__ y;
   Geom g;
-  int64_t rows;   // N * OH
-  int coltiles;   // ceil(OW / (NOWG * R))
+  int64_t rows;    // N * OA
+  int coltiles;    // ceil(OB / (NOWG * R))
+  int OR, OA, OB;  // output extents along R, A, B
+  int KR, KA, KB;  // kernel extents along R, A, B
+  int IB;          // input extent along B
+  int64_t sR, sA;  // input strides (elements) along R and A
+  int sB;          // input stride along B (1, or W when B is H)
+  int wR, wA, wB;  // weight offsets (within one input channel's taps) per step along R, A, B
 };
 
 // NCG channel groups per warp, NROW rows per warp, KWT = compile-time kernel
-// width (0: runtime, <= kMaxKW), VEC = 16-byte input loads (needs W % 4 == 0,
-// aligned x, KWT == 3).
+// extent along the column axis (0: runtime, <= kMaxKW), VEC = 16-byte input
+// loads (needs unit column stride, input extent along B % 4 == 0, aligned x,
+// KWT == 3).
 template <int NCG, int NROW, int KWT, bool VEC>
 __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedParams p) {
   constexpr int NOWG = 32 / (NCG * NROW);
@@ -60,16 +72,20 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
   extern __shared__ __align__(16) float ws[];  // [C*taps][NCG][kCO]
 
   const Geom &g = p.g;
-  const int KW = KWT ? KWT : g.KW;
-  const int taps = g.KD * g.KH * KW;
+  const int KW = KWT ? KWT : p.KB;  // kernel extent along the column axis
+  const int taps = g.KD * g.KH * g.KW;
 
-  // ---- stage weights: ws[(c*taps + t)*NCH + o] = w[o][c][t], zero for o >= K
+  // ---- stage weights: ws[((c*KR + kr)*KA + ka)*KB + kb][o] = w[o][c][tap (kr, ka, kb)],
+  // zero for o >= K
   {
     const int total = (int)(g.C * taps) * NCH;
     for (int i = threadIdx.x; i < total; i += 32) {
       const int o = i % NCH;
       const int ct = i / NCH;
-      ws[i] = o < g.K ? p.w[(int64_t)o * g.C * taps + ct] : 0.f;
+      const int c = ct / taps, t = ct - c * taps;
+      const int kr = t / (p.KA * KW), rem = t - kr * p.KA * KW;
+      const int ka = rem / KW, kb = rem - ka * KW;
+      ws[i] = o < g.K ? p.w[(int64_t)o * g.C * taps + c * taps + kr * p.wR + ka * p.wA + kb * p.wB] : 0.f;
     }
   }
   __syncwarp();
@@ -82,12 +98,12 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
   const int64_t row = (int64_t)(blockIdx.x / p.coltiles) * NROW + rr;
   const bool row_ok = row < p.rows;
   const int64_t rowc = row_ok ? row : p.rows - 1;
-  const int64_t n = rowc / g.OH;
-  const int oh = (int)(rowc % g.OH);
-  const int ow0 = (tile * NOWG + owg) * kR;
+  const int64_t n = rowc / p.OA;
+  const int oa = (int)(rowc % p.OA);
+  const int ob0 = (tile * NOWG + owg) * kR;
 
   const int64_t HW = (int64_t)g.H * g.W;
-  const float *xn = p.x + n * g.C * g.D * HW + (int64_t)oh * g.W + ow0;
+  const float *xn = p.x + n * g.C * g.D * HW + (int64_t)oa * p.sA + (int64_t)ob0 * p.sB;
 
   float mins[kCO][kR];
 #pragma unroll
@@ -95,7 +111,7 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
 #pragma unroll
     for (int r = 0; r < kR; ++r) mins[o][r] = INFINITY;
 
-  for (int od = 0; od < g.OD; ++od) {
+  for (int orr = 0; orr < p.OR; ++orr) {
     float acc[kCO][kR];
 #pragma unroll
     for (int o = 0; o < kCO; ++o)
@@ -103,23 +119,23 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
       for (int r = 0; r < kR; ++r) acc[o][r] = 0.f;
 
     for (int c = 0; c < g.C; ++c) {
-      for (int kd = 0; kd < g.KD; ++kd) {
-        const float *plane = xn + ((int64_t)c * g.D + od + kd) * HW;
-        const float *wrow = ws + ((c * g.KD + kd) * g.KH) * KW * NCH + cg * kCO;
+      for (int kr = 0; kr < p.KR; ++kr) {
+        const float *plane = xn + (int64_t)c * g.D * HW + (int64_t)(orr + kr) * p.sR;
+        const float *wrow = ws + ((c * p.KR + kr) * p.KA) * KW * NCH + cg * kCO;
 #pragma unroll 3
-        for (int kh = 0; kh < g.KH; ++kh) {
-          const float *xr = plane + (int64_t)kh * g.W;
+        for (int ka = 0; ka < p.KA; ++ka) {
+          const float *xr = plane + (int64_t)ka * p.sA;
           float xv[XW];
           if (VEC) {
-            // W % 4 == 0 and ow0 % 4 == 0: a 4-wide group is either fully
-            // inside the row or fully past its end
-            if (ow0 < g.W) {
+            // unit column stride, IB % 4 == 0 and ob0 % 4 == 0: a 4-wide group
+            // is either fully inside the row or fully past its end
+            if (ob0 < p.IB) {
               const float4 a = __ldg(reinterpret_cast<const float4 *>(xr));
               xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w;
             } else {
               xv[0] = 0.f, xv[1] = 0.f, xv[2] = 0.f, xv[3] = 0.f;
             }
-            if (ow0 + 4 < g.W) {
+            if (ob0 + 4 < p.IB) {
               const float2 b = __ldg(reinterpret_cast<const float2 *>(xr + 4));
               xv[4] = b.x, xv[5] = b.y;
             } else {
@@ -128,9 +144,9 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
           } else {
 #pragma unroll
             for (int j = 0; j < XW; ++j)
-              xv[j] = (j < kR + KW - 1 && ow0 + j < g.W) ? __ldg(xr + j) : 0.f;
+              xv[j] = (j < kR + KW - 1 && ob0 + j < p.IB) ? __ldg(xr + (int64_t)j * p.sB) : 0.f;
           }
-          const float *wt = wrow + kh * KW * NCH;
+          const float *wt = wrow + ka * KW * NCH;
 #pragma unroll
           for (int kw = 0; kw < (KWT ? KWT : kMaxKW); ++kw) {
             if (!KWT && kw >= KW) break;
@@ -153,7 +169,7 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
   }
 
   // ---- channel softmax for each of the R columns
-  const int64_t OHW = (int64_t)g.OH * g.OW;
+  const int64_t OAB = (int64_t)p.OA * p.OB;
 #pragma unroll
   for (int r = 0; r < kR; ++r) {
     float v[kCO];
@@ -174,13 +190,13 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
     }
 #pragma unroll
     for (int m = NOWG; m < NOWG * NCG; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-    const int ow = ow0 + r;
-    if (row_ok && ow < g.OW) {
-      float *yo = p.y + n * g.K * OHW + (int64_t)oh * g.OW + ow;
+    const int ob = ob0 + r;
+    if (row_ok && ob < p.OB) {
+      float *yo = p.y + n * g.K * OAB + (int64_t)oa * p.OB + ob;
 #pragma unroll
       for (int o = 0; o < kCO; ++o) {
         const int oc = cg * kCO + o;
-        if (oc < g.K) yo[(int64_t)oc * OHW] = v[o] / s;
+        if (oc < g.K) yo[(int64_t)oc * OAB] = v[o] / s;
       }
     }
   }
@@ -549,7 +565,7 @@ template <int NCG, int NROW, int KWT, bool VEC>
 cudaError_t launch_t(const FusedParams &p0, cudaStream_t stream) {
   constexpr int NOWG = 32 / (NCG * NROW);
   FusedParams p = p0;
-  p.coltiles = (p.g.OW + NOWG * kR - 1) / (NOWG * kR);
+  p.coltiles = (p.OB + NOWG * kR - 1) / (NOWG * kR);
   const int64_t rowgroups = (p.rows + NROW - 1) / NROW;
   const int64_t blocks = rowgroups * p.coltiles;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
@@ -565,9 +581,9 @@ cudaError_t launch_t(const FusedParams &p0, cudaStream_t stream) {
 
 template <int NCG, int NROW>
 cudaError_t launch_ncg(const FusedParams &p, cudaStream_t stream) {
-  const Geom &g = p.g;
-  if (g.KW == 3) {
-    const bool vec = (g.W % 4 == 0) && (((uintptr_t)p.x & 15u) == 0);
+  if (p.KB == 3) {
+    const bool vec = p.sB == 1 && (p.IB % 4 == 0) && (p.sA % 4 == 0) && (p.sR % 4 == 0) &&
+                     (((int64_t)p.g.D * p.g.H * p.g.W) % 4 == 0) && (((uintptr_t)p.x & 15u) == 0);
     return vec ? launch_t<NCG, NROW, 3, true>(p, stream) : launch_t<NCG, NROW, 3, false>(p, stream);
   }
   return launch_t<NCG, NROW, 0, false>(p, stream);
@@ -582,13 +598,14 @@ int pick_ncg(int64_t K) {
 
 }  // namespace
 
-bool fused_supported(const Geom &g, const char **why) {
+bool fused_supported(const Geom &g, int min_dim, const char **why) {
   if (g.K > 8 * kCO) {
     *why = "fused path: C_out above 96";
     return false;
   }
-  if (g.KW > kMaxKW) {
-    *why = "fused path: kernel width above 7";
+  // the kernel's column axis is W, or H when the min runs over W
+  if ((min_dim == 4 ? g.KH : g.KW) > kMaxKW) {
+    *why = "fused path: kernel extent along the output's last axis above 7";
     return false;
   }
   const int ncg = pick_ncg(g.K);
@@ -600,17 +617,36 @@ bool fused_supported(const Geom &g, const char **why) {
 }
 
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
-                                     const Geom &g, cudaStream_t stream) {
+                                     const Geom &g, int min_dim, cudaStream_t stream) {
   FusedParams p;
   p.x = x;
   p.w = w;
   p.bias = bias;
   p.y = y;
   p.g = g;
-  p.rows = g.N * (int64_t)g.OH;
   p.coltiles = 1;
+  // Axis roles.  Tensor dim min_dim of [N, C, D, H, W] is reduced; the output
+  // keeps the other two spatial axes in order, the last one contiguous.
+  const int64_t HW = (int64_t)g.H * g.W;
+  if (min_dim == 2) {  // (R, A, B) = (D, H, W)
+    p.OR = g.OD, p.OA = g.OH, p.OB = g.OW;
+    p.KR = g.KD, p.KA = g.KH, p.KB = g.KW;
+    p.IB = g.W, p.sR = HW, p.sA = g.W, p.sB = 1;
+    p.wR = g.KH * g.KW, p.wA = g.KW, p.wB = 1;
+  } else if (min_dim == 3) {  // (H, D, W)
+    p.OR = g.OH, p.OA = g.OD, p.OB = g.OW;
+    p.KR = g.KH, p.KA = g.KD, p.KB = g.KW;
+    p.IB = g.W, p.sR = g.W, p.sA = HW, p.sB = 1;
+    p.wR = g.KW, p.wA = g.KH * g.KW, p.wB = 1;
+  } else {  // min_dim 4: (W, D, H)
+    p.OR = g.OW, p.OA = g.OD, p.OB = g.OH;
+    p.KR = g.KW, p.KA = g.KD, p.KB = g.KH;
+    p.IB = g.H, p.sR = 1, p.sA = HW, p.sB = g.W;
+    p.wR = 1, p.wA = g.KH * g.KW, p.wB = g.KW;
+  }
+  p.rows = g.N * (int64_t)p.OA;
   StagedParams sp;
-  if (staged_plan(g, x, &sp)) {
+  if (min_dim == 2 && staged_plan(g, x, &sp)) {
     sp.x = x;
     sp.w = w;
     sp.bias = bias;

@@ -129,15 +129,18 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * Fused Conv3d -> min over one spatial dim of the conv output -> softmax over
  * channels (l2_p24 page, turns 1-2):
  *   z[n,o,d,h,w] = bias[o] + sum_{c,kd,kh,kw} w[o,c,kd,kh,kw] * x[n,c,d+kd,h+kh,w+kw]
- *   m[n,o,h,w]   = min_d z[n,o,d,h,w]                     (min_dim = 2, depth)
+ *   m[n,o,h,w]   = min_d z[n,o,d,h,w]                     (min_dim = 2, depth; the page's case)
  *   y[n,o,h,w]   = exp(m - max_o m) / sum_o exp(m - max_o m)
+ * The page's module takes the min dimension as a constructor argument; min_dim
+ * 3 reduces over height (m[n,o,d,w] = min_h z) and 4 over width (m[n,o,d,h]).
  * Conv hyper-parameters are fixed to stride 1, padding 0, dilation 1, groups 1.
  * The 5-D intermediate z is never written to memory.
  *   x->dims = [N, C_in, D, H, W], w->dims = [C_out, C_in, KD, KH, KW],
- *   bias: [C_out] device or NULL, y->dims must be [N, C_out, D-KD+1 ... ] with the
- *   reduced dim removed: for min_dim = 2, [N, C_out, H-KH+1, W-KW+1].
- * min_dim: 2 (depth) is implemented; 3 and 4 return CONV_ERR_UNSUPPORTED;
- * anything else CONV_ERR_ARG.  C_out is limited to 96.
+ *   bias: [C_out] device or NULL, y->dims = [N, C_out] followed by the conv's
+ *   spatial output dims (D-KD+1, H-KH+1, W-KW+1) without the reduced one:
+ *   [N, C_out, OH, OW] for min_dim 2, [N, C_out, OD, OW] for 3, [N, C_out, OD, OH] for 4.
+ * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  C_out is limited to 96 and the
+ * kernel extent along y's last axis to 7 (CONV_ERR_UNSUPPORTED otherwise).
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);

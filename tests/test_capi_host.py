@@ -105,9 +105,15 @@ def test_fused_validation_statuses(lib):
     y = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 30, 30))
     f = lib.conv3d_min_softmax
     assert f(None, ctypes.byref(w), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_NULL
-    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 3, None) == cf.CONV_ERR_UNSUPPORTED
-    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 4, None) == cf.CONV_ERR_UNSUPPORTED
+    # min_dim 3 / 4 keep (D, W) / (D, H): the [N, C_out, OH, OW] descriptor is the wrong shape for them
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 3, None) == cf.CONV_ERR_SHAPE
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 4, None) == cf.CONV_ERR_SHAPE
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 1, None) == cf.CONV_ERR_ARG
+    assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 5, None) == cf.CONV_ERR_ARG
+    # min over W: the kernel's column axis is H, so KH is limited to 7
+    wtall = T5(0x100000, (ctypes.c_int64 * 5)(24, 3, 3, 9, 3))
+    ytall = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 22, 24))
+    assert f(ctypes.byref(x), ctypes.byref(wtall), None, ctypes.byref(ytall), 4, None) == cf.CONV_ERR_UNSUPPORTED
     wbad = T5(0x100000, (ctypes.c_int64 * 5)(24, 4, 3, 3, 3))
     assert f(ctypes.byref(x), ctypes.byref(wbad), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE
     ybad = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 30, 29))

@@ -296,3 +296,38 @@ def test_fused_narrow_rows_and_many_rows_per_sm():
     b = ((rng.random(24) - 0.5) * 0.3).astype(np.float32)
     y = run_fused(x, w, b).cpu().numpy()
     assert_close(y, oracle.conv3d_min_softmax(x, w, b), "fused 4200 rows")
+
+
+# ------------------------------------- fused, min over height or width
+
+@pytest.mark.parametrize("min_dim", [3, 4])
+@pytest.mark.parametrize("C_out,k,shape", [(24, (3, 3, 3), (3, 3, 9, 11, 32)), (13, (2, 4, 3), (2, 2, 7, 10, 37)),
+                                           (49, (3, 3, 5), (2, 3, 6, 9, 12)), (5, (1, 5, 2), (3, 1, 4, 21, 6))])
+def test_fused_min_dim_small(min_dim, C_out, k, shape):
+    rng = np.random.default_rng(C_out * 7 + min_dim)
+    x = rng.random(shape).astype(np.float32)
+    w = ((rng.random((C_out, shape[1]) + k) - 0.5) * 0.4).astype(np.float32)
+    b = ((rng.random(C_out) - 0.5) * 0.4).astype(np.float32)
+    ref = oracle.conv3d_min_softmax(x, w, b, min_dim)
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    y = cf.conv3d_min_softmax(xt, wt, bt, min_dim)
+    torch.cuda.synchronize()
+    assert tuple(y.shape) == ref.shape
+    assert_close(y.cpu().numpy(), ref, f"fused min_dim={min_dim} C_out={C_out} k={k}")
+    y0 = cf.conv3d_min_softmax(xt, wt, None, min_dim).cpu().numpy()
+    assert_close(y0, oracle.conv3d_min_softmax(x, w, None, min_dim), f"fused min_dim={min_dim} no bias")
+
+
+@pytest.mark.parametrize("min_dim", [3, 4])
+def test_fused_min_dim_workload_sampled(min_dim):
+    # the benchmark's fused workload with the min over height / width instead of depth
+    wl, x, w, b = workload_inputs("conv3d_min_softmax")
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    y = cf.conv3d_min_softmax(xt, wt, bt, min_dim)
+    N, C_out, OA, OB = y.shape
+    rng = np.random.default_rng(40 + min_dim)
+    cols = np.unique(np.concatenate([rng.integers(0, N * OA * OB, 800), [0, OB - 1, OA * OB - 1, N * OA * OB - 1]]))
+    yc = y.permute(0, 2, 3, 1).reshape(-1, C_out)[torch.from_numpy(cols).cuda()].cpu().numpy()
+    ref = oracle.conv3d_min_softmax_at(x, w, b, cols, min_dim)
+    assert_close(yc, ref, f"fused min_dim={min_dim} full size sampled")
+    assert torch.allclose(y.sum(dim=1), torch.ones((), device="cuda"), atol=1e-5)
