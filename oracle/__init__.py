@@ -41,10 +41,14 @@ def _load():
         lib.oracle_out_dims.argtypes = [i32, vp, vp, vp, vp, vp, vp]
         lib.oracle_conv_nd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, i32]
         lib.oracle_conv_nd_at.argtypes = [vp, vp, vp, i32, i64, i64, i64, vp, vp, vp, vp, vp, vp, i64, vp, i32]
+        lib.oracle_conv_nd_grouped.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, vp, vp, vp, vp, vp, i32]
+        lib.oracle_conv_nd_grouped_at.argtypes = [vp, vp, vp, i32, i64, i64, i64, i64, vp, vp, vp, vp, vp, vp, i64,
+                                                  vp, i32]
         lib.oracle_input_read_counts.argtypes = [i32, vp, vp, vp, vp, vp, vp]
         lib.oracle_conv3d_min_softmax.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, vp, i32, i32]
         lib.oracle_conv3d_min_softmax_at.argtypes = [vp, vp, vp, i64, i64, i64, vp, vp, i32, vp, i64, vp, i32]
         for f in (lib.oracle_out_dims, lib.oracle_conv_nd, lib.oracle_conv_nd_at, lib.oracle_input_read_counts,
+                  lib.oracle_conv_nd_grouped, lib.oracle_conv_nd_grouped_at,
                   lib.oracle_conv3d_min_softmax, lib.oracle_conv3d_min_softmax_at):
             f.restype = i32
         _lib = lib
@@ -85,14 +89,14 @@ def out_dims(in_dims, k, stride, pad, dilation):
     return tuple(int(v) for v in out)
 
 
-def conv_nd(x, w, bias, stride, pad, dilation, nthreads=None):
-    """y = conv(x, w) + bias as float64, x [N,C_in,*in], w [C_out,C_in,*k]."""
+def conv_nd(x, w, bias, stride, pad, dilation, nthreads=None, groups=1):
+    """y = conv(x, w) + bias as float64, x [N,C_in,*in], w [C_out,C_in/groups,*k]."""
     x, w = _f32(x), _f32(w)
     b = None if bias is None else _f32(bias)
     nd = x.ndim - 2
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
-    if w.shape[1] != C_in or w.ndim != x.ndim:
+    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in or w.ndim != x.ndim:
         raise OracleError("weight shape mismatch")
     ins, ks = _i64(x.shape[2:]), _i64(w.shape[2:])
     s, p, d = _i64(stride), _i64(pad), _i64(dilation)
@@ -100,14 +104,14 @@ def conv_nd(x, w, bias, stride, pad, dilation, nthreads=None):
     if min(od) <= 0:
         raise OracleError("non-positive output size")
     y = np.empty((N, C_out) + od, np.float64)
-    rc = _load().oracle_conv_nd(_ptr(x), _ptr(w), _ptr(b), _ptr(y), nd, N, C_in, C_out, _ptr(ins), _ptr(ks),
-                                _ptr(s), _ptr(p), _ptr(d), nthreads or threads())
+    rc = _load().oracle_conv_nd_grouped(_ptr(x), _ptr(w), _ptr(b), _ptr(y), nd, N, C_in, C_out, groups, _ptr(ins),
+                                        _ptr(ks), _ptr(s), _ptr(p), _ptr(d), nthreads or threads())
     if rc:
-        raise OracleError("oracle_conv_nd rejected its arguments")
+        raise OracleError("oracle_conv_nd_grouped rejected its arguments")
     return y
 
 
-def conv_nd_at(x, w, bias, stride, pad, dilation, flat_idx, nthreads=None):
+def conv_nd_at(x, w, bias, stride, pad, dilation, flat_idx, nthreads=None, groups=1):
     """y.flat[flat_idx] (float64) for the conv above, each output computed on its own."""
     x, w = _f32(x), _f32(w)
     b = None if bias is None else _f32(bias)
@@ -118,10 +122,11 @@ def conv_nd_at(x, w, bias, stride, pad, dilation, flat_idx, nthreads=None):
     s, p, d = _i64(stride), _i64(pad), _i64(dilation)
     idx = _i64(flat_idx)
     out = np.empty(idx.shape, np.float64)
-    rc = _load().oracle_conv_nd_at(_ptr(x), _ptr(w), _ptr(b), nd, N, C_in, C_out, _ptr(ins), _ptr(ks), _ptr(s),
-                                   _ptr(p), _ptr(d), _ptr(idx), idx.size, _ptr(out), nthreads or threads())
+    rc = _load().oracle_conv_nd_grouped_at(_ptr(x), _ptr(w), _ptr(b), nd, N, C_in, C_out, groups, _ptr(ins),
+                                           _ptr(ks), _ptr(s), _ptr(p), _ptr(d), _ptr(idx), idx.size, _ptr(out),
+                                           nthreads or threads())
     if rc:
-        raise OracleError("oracle_conv_nd_at rejected its arguments")
+        raise OracleError("oracle_conv_nd_grouped_at rejected its arguments")
     return out
 
 

@@ -15,7 +15,10 @@
  * Definitions implemented (all accumulation in double):
  *   out_i = floor((in_i + 2*pad_i - dil_i*(k_i-1) - 1) / stride_i) + 1
  *   y[n,o,p] = b[o] + sum_c sum_k w[o,c,k] * x[n,c, p*stride + k*dil - pad]
- *              where a tap whose input coordinate falls outside [0, in_i) reads 0
+ *              where a tap whose input coordinate falls outside [0, in_i) reads 0;
+ *              with G groups (the pages' modules take a groups argument, left
+ *              at 1 there), c runs over the C_in/G channels of o's group
+ *              (grp = o / (C_out/G)) and x's channel is grp*C_in/G + c
  *   fused: z = conv (stride 1, pad 0, dil 1);  m = min of z over one spatial
  *          dim (depth on the page; height or width when asked), e.g.
  *          m[n,o,h,w] = min_d z[n,o,d,h,w];
@@ -53,19 +56,22 @@ int oracle_out_dims(int ndim, const int64_t *in, const int64_t *k, const int64_t
 
 typedef struct {
   int ndim;
-  int64_t N, C, K;
+  int64_t N, C, K; /* C: input channels per group; K: all output channels */
+  int64_t G;       /* groups: output channel o reads input channels [(o / (K/G)) * C, +C) */
   int64_t in[MAXD], k[MAXD], s[MAXD], p[MAXD], d[MAXD], out[MAXD];
   int64_t in_size, k_size, out_size; /* products over the spatial dims */
 } geom_t;
 
-static int make_geom(geom_t *g, int ndim, int64_t N, int64_t C, int64_t K, const int64_t *in,
+static int make_geom(geom_t *g, int ndim, int64_t N, int64_t C, int64_t K, int64_t G, const int64_t *in,
                      const int64_t *k, const int64_t *s, const int64_t *p, const int64_t *d) {
-  if (ndim < 1 || ndim > MAXD || N <= 0 || C <= 0 || K <= 0) return 1;
+  if (ndim < 1 || ndim > MAXD || N <= 0 || C <= 0 || K <= 0 || G <= 0) return 1;
+  if (C % G != 0 || K % G != 0) return 1;
   memset(g, 0, sizeof(*g));
   g->ndim = ndim;
   g->N = N;
-  g->C = C;
+  g->C = C / G;
   g->K = K;
+  g->G = G;
   if (oracle_out_dims(ndim, in, k, s, p, d, g->out)) return 1;
   g->in_size = g->k_size = g->out_size = 1;
   for (int i = 0; i < ndim; ++i) {
@@ -104,13 +110,16 @@ static int64_t tap_input_offset(const geom_t *g, const int64_t *op, const int64_
   return off;
 }
 
-/* One output value y[n,o,op] in double. */
+/* One output value y[n,o,op] in double.  With groups, output channel o sums
+ * over the C input channels of its group (grp = o / (K/G)), whose weights are
+ * w[o][0..C). */
 static double conv_point(const geom_t *g, const float *x, const float *w, const float *bias, int64_t n,
                          int64_t o, const int64_t *op) {
   double acc = bias ? (double)bias[o] : 0.0;
   int64_t kp[MAXD];
+  const int64_t grp = o / (g->K / g->G);
   for (int64_t c = 0; c < g->C; ++c) {
-    const float *xc = x + (n * g->C + c) * g->in_size;
+    const float *xc = x + (n * g->G * g->C + grp * g->C + c) * g->in_size;
     const float *wc = w + (o * g->C + c) * g->k_size;
     for (int64_t t = 0; t < g->k_size; ++t) {
       unflatten(t, g->ndim, g->k, kp);
@@ -184,17 +193,25 @@ static void conv_task(void *vctx, int64_t task) { /* task = n*K + o */
   }
 }
 
-/* y (double, [N, C_out, out...]) = conv(x, w) + bias.  bias may be NULL.
+/* y (double, [N, C_out, out...]) = conv(x, w) + bias with `groups` channel
+ * groups (w: [C_out, C_in/groups, k...]).  bias may be NULL.
  * Returns 0, or 1 on bad arguments / non-positive output size. */
-int oracle_conv_nd(const float *x, const float *w, const float *bias, double *y, int ndim, int64_t N,
-                   int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s,
-                   const int64_t *p, const int64_t *d, int nthreads) {
+int oracle_conv_nd_grouped(const float *x, const float *w, const float *bias, double *y, int ndim, int64_t N,
+                           int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in, const int64_t *k,
+                           const int64_t *s, const int64_t *p, const int64_t *d, int nthreads) {
   geom_t g;
   if (!x || !w || !y) return 1;
-  if (make_geom(&g, ndim, N, C_in, C_out, in, k, s, p, d)) return 1;
+  if (make_geom(&g, ndim, N, C_in, C_out, groups, in, k, s, p, d)) return 1;
   conv_ctx_t ctx = {&g, x, w, bias, y};
   run_tasks(conv_task, &ctx, N * C_out, nthreads);
   return 0;
+}
+
+/* The same with one group. */
+int oracle_conv_nd(const float *x, const float *w, const float *bias, double *y, int ndim, int64_t N,
+                   int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s,
+                   const int64_t *p, const int64_t *d, int nthreads) {
+  return oracle_conv_nd_grouped(x, w, bias, y, ndim, N, C_in, C_out, 1, in, k, s, p, d, nthreads);
 }
 
 /* ------------------------------------------------------- conv (sampled) */
@@ -224,20 +241,29 @@ static void pts_task(void *vctx, int64_t task) {
   }
 }
 
-/* out[i] = y.flat[idx[i]] for the same y as oracle_conv_nd, computed one by one.
- * Returns 1 on bad arguments or an index outside y. */
-int oracle_conv_nd_at(const float *x, const float *w, const float *bias, int ndim, int64_t N, int64_t C_in,
-                      int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s, const int64_t *p,
-                      const int64_t *d, const int64_t *idx, int64_t count, double *out, int nthreads) {
+/* out[i] = y.flat[idx[i]] for the same y as oracle_conv_nd_grouped, computed
+ * one by one.  Returns 1 on bad arguments or an index outside y. */
+int oracle_conv_nd_grouped_at(const float *x, const float *w, const float *bias, int ndim, int64_t N,
+                              int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in, const int64_t *k,
+                              const int64_t *s, const int64_t *p, const int64_t *d, const int64_t *idx,
+                              int64_t count, double *out, int nthreads) {
   geom_t g;
   if (!x || !w || !idx || !out || count < 0) return 1;
-  if (make_geom(&g, ndim, N, C_in, C_out, in, k, s, p, d)) return 1;
+  if (make_geom(&g, ndim, N, C_in, C_out, groups, in, k, s, p, d)) return 1;
   int64_t total = N * C_out * g.out_size;
   for (int64_t i = 0; i < count; ++i)
     if (idx[i] < 0 || idx[i] >= total) return 1;
   pts_ctx_t ctx = {&g, x, w, bias, idx, out, count};
   run_tasks(pts_task, &ctx, (count + PTS_PER_TASK - 1) / PTS_PER_TASK, nthreads);
   return 0;
+}
+
+/* The same with one group. */
+int oracle_conv_nd_at(const float *x, const float *w, const float *bias, int ndim, int64_t N, int64_t C_in,
+                      int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s, const int64_t *p,
+                      const int64_t *d, const int64_t *idx, int64_t count, double *out, int nthreads) {
+  return oracle_conv_nd_grouped_at(x, w, bias, ndim, N, C_in, C_out, 1, in, k, s, p, d, idx, count, out,
+                                   nthreads);
 }
 
 /* ------------------------------------------------- read counter (pins A14) */
@@ -249,7 +275,7 @@ int oracle_input_read_counts(int ndim, const int64_t *in, const int64_t *k, cons
                              const int64_t *p, const int64_t *d, int64_t *counts) {
   geom_t g;
   if (!counts) return 1;
-  if (make_geom(&g, ndim, 1, 1, 1, in, k, s, p, d)) return 1;
+  if (make_geom(&g, ndim, 1, 1, 1, 1, in, k, s, p, d)) return 1;
   memset(counts, 0, sizeof(int64_t) * (size_t)g.in_size);
   int64_t op[MAXD], kp[MAXD];
   for (int64_t pflat = 0; pflat < g.out_size; ++pflat) {
@@ -324,7 +350,7 @@ static int fused_common(const float *x, const float *w, const float *bias, doubl
   const int64_t one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
   if (!x || !w || !y || !in3 || !k3) return 1;
   if (min_dim < 2 || min_dim > 4) return 1;
-  if (make_geom(&g, 3, N, C_in, C_out, in3, k3, one, zero, one)) return 1;
+  if (make_geom(&g, 3, N, C_in, C_out, 1, in3, k3, one, zero, one)) return 1;
   /* tensor dim min_dim of [N, C, D, H, W] is spatial axis min_dim - 2; the
    * other two spatial axes stay, in their order */
   const int r = min_dim - 2, a = (r == 0) ? 1 : 0, b = (r == 2) ? 1 : 2;

@@ -314,3 +314,65 @@ def test_fused_rejects_bad_min_dim():
     for bad in (0, 1, 5):
         with pytest.raises(oracle.OracleError):
             oracle.conv3d_min_softmax(x, w, b, bad)
+
+
+# ---------------------------------------------------------------- groups
+
+@pytest.mark.parametrize("nd,groups,C_in,C_out", [(1, 2, 4, 6), (2, 3, 6, 3), (3, 2, 4, 4), (2, 5, 5, 10),
+                                                  (3, 4, 4, 8)])
+def test_grouped_matches_torch_float64(nd, groups, C_in, C_out):
+    rng = _rng(100 + nd * 10 + groups)
+    ins = tuple(int(v) for v in rng.integers(5, 9, nd))
+    k = tuple(int(v) for v in rng.integers(1, 4, nd))
+    s = tuple(int(v) for v in rng.integers(1, 3, nd))
+    p = tuple(int(v) for v in rng.integers(0, 2, nd))
+    d = tuple(int(v) for v in rng.integers(1, 3, nd))
+    x = rng.standard_normal((2, C_in) + ins).astype(np.float32)
+    w = rng.standard_normal((C_out, C_in // groups) + k).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    y = oracle.conv_nd(x, w, b, s, p, d, groups=groups)
+    ref = TORCH_CONV[nd](torch.from_numpy(x).double(), torch.from_numpy(w).double(), torch.from_numpy(b).double(),
+                         stride=s, padding=p, dilation=d, groups=groups).numpy()
+    np.testing.assert_allclose(y, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_grouped_is_concatenation_of_per_group_convs():
+    rng = _rng(120)
+    groups, C_in, C_out = 3, 6, 9
+    x = rng.standard_normal((2, C_in, 7, 6)).astype(np.float32)
+    w = rng.standard_normal((C_out, C_in // groups, 3, 2)).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    y = oracle.conv_nd(x, w, b, (1, 2), (1, 0), (2, 1), groups=groups)
+    cg, kg = C_in // groups, C_out // groups
+    for g in range(groups):
+        part = oracle.conv_nd(x[:, g * cg:(g + 1) * cg], w[g * kg:(g + 1) * kg], b[g * kg:(g + 1) * kg],
+                              (1, 2), (1, 0), (2, 1))
+        assert np.array_equal(y[:, g * kg:(g + 1) * kg], part)
+
+
+def test_depthwise_delta_kernel_shifts_each_channel():
+    # groups = C_in = C_out, w = 1 at one tap: y[n, c, p] = x[n, c, p*s + k0*d - pad] (0 in the padding)
+    rng = _rng(121)
+    C, L, k, s, p, d, k0 = 5, 23, 4, 2, 3, 2, 2
+    x = rng.standard_normal((3, C, L)).astype(np.float32)
+    w = np.zeros((C, 1, k), np.float32)
+    w[:, 0, k0] = 1.0
+    y = oracle.conv_nd(x, w, None, (s,), (p,), (d,), groups=C)
+    (OL,) = oracle.out_dims((L,), (k,), (s,), (p,), (d,))
+    ref = np.zeros((3, C, OL))
+    for j in range(OL):
+        q = j * s + k0 * d - p
+        if 0 <= q < L:
+            ref[:, :, j] = x[:, :, q]
+    assert np.array_equal(y, ref)
+
+
+def test_grouped_sampled_equals_full_and_rejects_bad_groups():
+    rng = _rng(122)
+    x = rng.standard_normal((2, 4, 9)).astype(np.float32)
+    w = rng.standard_normal((6, 2, 3)).astype(np.float32)
+    y = oracle.conv_nd(x, w, None, (2,), (1,), (1,), groups=2)
+    idx = np.array([0, 7, y.size // 2, y.size - 1], np.int64)
+    assert np.array_equal(oracle.conv_nd_at(x, w, None, (2,), (1,), (1,), idx, groups=2), y.reshape(-1)[idx])
+    with pytest.raises(oracle.OracleError):
+        oracle.conv_nd(x, w, None, (2,), (1,), (1,), groups=3)

@@ -28,6 +28,8 @@ MUTANTS = {
     "tap_dim_order_reversed": ("off = off * g->in[i] + q;", "off = off + q * (i == 0 ? 1 : g->in[0]);"),
     "min_axis_always_depth": ("const int r = min_dim - 2,", "const int r = 0 * min_dim,"),
     "kept_axes_swapped": ("a = (r == 0) ? 1 : 0, b = (r == 2) ? 1 : 2;", "b = (r == 0) ? 1 : 0, a = (r == 2) ? 1 : 2;"),
+    "group_offset_dropped": ("(n * g->G * g->C + grp * g->C + c)", "(n * g->G * g->C + c)"),
+    "group_of_channel_wrong": ("const int64_t grp = o / (g->K / g->G);", "const int64_t grp = o % g->G;"),
 }
 
 CHILD = r"""
@@ -39,6 +41,7 @@ checks = [t.test_page_worked_shapes, t.test_out_dims_brute_force_count, t.test_r
           t.test_fused_matches_torch_float64, t.test_fused_single_depth_is_softmax_of_conv]
 checks += [lambda s=s: t.test_matches_torch_float64(s) for s in range(6)]
 checks += [lambda m=m: t.test_fused_min_dim_matches_torch_float64(m) for m in (2, 3, 4)]
+checks += [lambda a=a: t.test_grouped_matches_torch_float64(*a) for a in ((1, 2, 4, 6), (2, 3, 6, 3), (3, 4, 4, 8))]
 checks += [lambda nd=nd: t.test_delta_kernel_selects_one_input(nd) for nd in (1, 2, 3)]
 checks += [lambda nd=nd: t.test_all_ones_counts_in_bounds_taps(nd) for nd in (1, 3)]
 failed = 0
