@@ -18,7 +18,8 @@ CONV_ALGO_AUTO, CONV_ALGO_DIRECT_FFMA, CONV_ALGO_IGEMM_3XTF32 = 0, 1, 2
 ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV_ALGO_IGEMM_3XTF32: "igemm_3xtf32"}
 
 # every symbol include/convfwd.h declares
-EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
+EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_select_algo",
+            "conv_algo_supported",
             "conv3d_min_softmax",
             "conv_status_string", "conv_last_error", "conv_device_status")
 
@@ -54,6 +55,7 @@ def load(path: str | None = None):
     lib.conv_out_dims.argtypes = [i32, arr, arr, arr, arr, arr, arr]
     lib.conv_fwd_nd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, arr, arr, arr, arr, arr, vp]
     lib.conv_fwd_nd_ex.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, arr, arr, arr, arr, arr, i32, vp]
+    lib.conv_fwd_nd_grouped.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, i32, vp]
     lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
@@ -126,8 +128,9 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CONV_ALGO_AUTO, stream=None):
-    """y = conv(x, w) + bias for contiguous fp32 CUDA tensors x [N,C_in,*in], w [C_out,C_in,*k]."""
+def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CONV_ALGO_AUTO, stream=None,
+                groups=1):
+    """y = conv(x, w) + bias for contiguous fp32 CUDA tensors x [N,C_in,*in], w [C_out,C_in/groups,*k]."""
     import torch
     nd = x.dim() - 2
     if nd not in (1, 2, 3) or w.dim() != x.dim():
@@ -138,17 +141,17 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
-    if w.shape[1] != C_in:
-        raise ValueError("w.shape[1] must equal x.shape[1] (groups = 1)")
+    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in:
+        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
     od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
     if out is None:
         out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
     elif tuple(out.shape) != (N, C_out) + od or not out.is_contiguous():
         raise ValueError("out has the wrong shape or is not contiguous")
     lib = load()
-    st = lib.conv_fwd_nd_ex(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
-                            nd, N, C_in, C_out, _arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d),
-                            int(algo), _stream_handle(stream))
+    st = lib.conv_fwd_nd_grouped(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                 out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
+                                 _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), int(algo), _stream_handle(stream))
     _check(st)
     return out
 

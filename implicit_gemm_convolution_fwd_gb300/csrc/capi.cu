@@ -73,12 +73,15 @@ int compute_out_dims(int ndim, const int64_t *in, const int64_t *k, const int64_
 // counts of x, w and y.
 int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k,
               const int64_t *s, const int64_t *p, const int64_t *d, Geom *g, int64_t *xe, int64_t *we,
-              int64_t *ye) {
+              int64_t *ye, int64_t groups = 1) {
   int64_t out[3];
   int st = compute_out_dims(ndim, in, k, s, p, d, out);
   if (st != CONV_OK) return st;
   if (N < 0 || N > kMaxDim || C_in < 1 || C_in > kMaxDim || C_out < 1 || C_out > kMaxDim)
     return fail(CONV_ERR_ARG, "conv: N must be in [0, 2^31), C_in and C_out in [1, 2^31)%s");
+  if (groups < 1 || groups > kMaxDim || C_in % groups != 0 || C_out % groups != 0)
+    return fail(CONV_ERR_ARG, "conv: groups must be >= 1 and divide C_in and C_out%s");
+  const int64_t Cg = C_in / groups;  // input channels per group (w's second dim)
   const int64_t lim = INT64_MAX / 8;
   int64_t in_sp = 1, out_sp = 1, k_sp = 1, t;
   for (int i = 0; i < ndim; ++i) {
@@ -86,11 +89,11 @@ int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *i
         !mul_ok(k_sp, k[i], lim, &k_sp))
       return fail(CONV_ERR_ARG, "conv: tensor size overflows int64%s");
   }
-  if (!mul_ok(N, C_in, lim, &t) || !mul_ok(t, in_sp, lim, xe) || !mul_ok(C_out, C_in, lim, &t) ||
+  if (!mul_ok(N, C_in, lim, &t) || !mul_ok(t, in_sp, lim, xe) || !mul_ok(C_out, Cg, lim, &t) ||
       !mul_ok(t, k_sp, lim, we) || !mul_ok(N, C_out, lim, &t) || !mul_ok(t, out_sp, lim, ye))
     return fail(CONV_ERR_ARG, "conv: tensor size overflows int64%s");
-  if (k_sp > kMaxDim || C_in * k_sp > kMaxDim)
-    return fail(CONV_ERR_ARG, "conv: reduction length C_in*prod(k) must fit in int32%s");
+  if (k_sp > kMaxDim || Cg * k_sp > kMaxDim)
+    return fail(CONV_ERR_ARG, "conv: reduction length (C_in/groups)*prod(k) must fit in int32%s");
   // Embed into 3-D with leading singleton dims.
   const int off = 3 - ndim;
   int gi[3] = {1, 1, 1}, go[3] = {1, 1, 1}, gk[3] = {1, 1, 1}, gs[3] = {1, 1, 1}, gp[3] = {0, 0, 0},
@@ -104,8 +107,9 @@ int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *i
     gd[off + i] = (int)d[i];
   }
   g->N = N;
-  g->C = C_in;
-  g->K = C_out;
+  g->C = Cg;
+  g->K = C_out / groups;
+  g->G = groups;
   g->D = gi[0], g->H = gi[1], g->W = gi[2];
   g->OD = go[0], g->OH = go[1], g->OW = go[2];
   g->KD = gk[0], g->KH = gk[1], g->KW = gk[2];
@@ -120,9 +124,10 @@ int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *i
 // (the fused entry point writes a reduced 4-D output).
 int validate_conv(const float *x, const float *w, const float *bias, const float *y, int ndim, int64_t N,
                   int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s,
-                  const int64_t *p, const int64_t *d, Geom *g, int64_t y_elems_override = -1) {
+                  const int64_t *p, const int64_t *d, Geom *g, int64_t y_elems_override = -1,
+                  int64_t groups = 1) {
   int64_t xe, we, ye;
-  int st = make_geom(ndim, N, C_in, C_out, in, k, s, p, d, g, &xe, &we, &ye);
+  int st = make_geom(ndim, N, C_in, C_out, in, k, s, p, d, g, &xe, &we, &ye, groups);
   if (st != CONV_OK) return st;
   // an empty batch has empty x and y, which may be NULL
   if (!w || (N > 0 && (!x || !y))) return fail(CONV_ERR_NULL, "conv: x, w and y must be non-NULL%s");
@@ -198,23 +203,41 @@ int conv_select_algo(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int
   return CONV_OK;
 }
 
-int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
-                   int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
-                   const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,
-                   conv_stream_t stream) {
+int conv_fwd_nd_grouped(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                        int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                        const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,
+                        conv_stream_t stream) {
   g_last_error[0] = 0;
   Geom g;
-  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g);
+  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, -1,
+                         groups);
   if (st != CONV_OK) return st;
   if (algo == CONV_ALGO_AUTO) algo = choose_algo(g);
   st = check_algo(g, algo);
   if (st != CONV_OK) return st;
   if (g.N == 0) return CONV_OK;  // empty batch: nothing to compute
   cudaStream_t s = (cudaStream_t)stream;
-  cudaError_t e = algo == CONV_ALGO_DIRECT_FFMA ? convfwd::launch_direct_ffma(x, w, bias, y, g, s)
-                                                : convfwd::launch_igemm_3xtf32(x, w, bias, y, g, s);
+  cudaError_t e = cudaSuccess;
+  if (algo == CONV_ALGO_DIRECT_FFMA) {
+    e = convfwd::launch_direct_ffma(x, w, bias, y, g, s);  // all groups in one grid
+  } else {
+    // one persistent launch per group on views of x, w, bias and y (the
+    // kernel's batch strides span all groups' channels)
+    const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
+    for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
+      e = convfwd::launch_igemm_3xtf32(x + grp * xg, w + grp * wg, bias ? bias + grp * g.K : nullptr, y + grp * yg,
+                                       g, s);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd: kernel launch");
   return CONV_OK;
+}
+
+int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                   int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
+                   const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,
+                   conv_stream_t stream) {
+  return conv_fwd_nd_grouped(x, w, bias, y, ndim, N, C_in, C_out, 1, in_dims, k_dims, stride, pad, dilation, algo,
+                             stream);
 }
 
 int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in_dims,

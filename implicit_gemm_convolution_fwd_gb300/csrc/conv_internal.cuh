@@ -9,17 +9,23 @@ namespace convfwd {
 // A convolution problem in a uniform 3-D view: 1-D and 2-D problems are
 // embedded with leading singleton dims (size 1, kernel 1, stride 1, pad 0,
 // dilation 1), which leaves the sum in the l1_p60 / l1_p76 pages unchanged.
+// With G > 1 groups, C and K count the channels of one group: x has G*C
+// channels, y and w have G*K, and output channel grp*K + o reads input
+// channels [grp*C, grp*C + C).
 struct Geom {
-  int64_t N, C, K;             // batch, input channels, output channels
+  int64_t N, C, K;             // batch, input channels per group, output channels per group
+  int64_t G;                   // groups (1: a plain convolution)
   int D, H, W;                 // input spatial dims
   int OD, OH, OW;              // output spatial dims
   int KD, KH, KW;              // kernel dims
   int SD, SH, SW;              // stride
   int PD, PH, PW;              // zero padding (symmetric)
   int DD, DH, DW;              // dilation
-  int64_t in_spatial() const { return (int64_t)D * H * W; }
-  int64_t out_spatial() const { return (int64_t)OD * OH * OW; }
-  int taps() const { return KD * KH * KW; }
+  __host__ __device__ int64_t x_batch_stride() const { return G * C * (int64_t)D * H * W; }  // elements between images of x
+  __host__ __device__ int64_t y_batch_stride() const { return G * K * (int64_t)OD * OH * OW; }
+  __host__ __device__ int64_t in_spatial() const { return (int64_t)D * H * W; }
+  __host__ __device__ int64_t out_spatial() const { return (int64_t)OD * OH * OW; }
+  __host__ __device__ int taps() const { return KD * KH * KW; }
 };
 
 // Device-side status word written by kernels whose bounded waits gave up.

@@ -34,13 +34,18 @@ struct DirectParams {
   int64_t items;  // N * OD * OH * ceil(OW / R)
   int owg;        // ceil(OW / R)
   int cchunk;     // input channels per weight chunk
+  int kblocks;    // channel blocks of kCO per group: ceil(K / kCO)
 };
 
 __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParams p) {
   __shared__ __align__(16) float ws[kSmemFloats];  // [cc][tap][kCO]
   const Geom &g = p.g;
   const int taps = g.KD * g.KH * g.KW;
-  const int o0 = blockIdx.y * kCO;
+  // blockIdx.y = (group, channel block within the group); o0 is the block's
+  // first output channel within its group
+  const int grp = blockIdx.y / p.kblocks;
+  const int o0 = (blockIdx.y - grp * p.kblocks) * kCO;
+  const int64_t ob = (int64_t)grp * g.K;  // the group's first output channel in y and w
 
   const int64_t item = (int64_t)blockIdx.x * kThreads + threadIdx.x;
   const bool active = item < p.items;
@@ -68,12 +73,12 @@ __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParam
       const int o = i % kCO;
       const int ct = i / kCO;  // cc*taps + tap
       const int64_t og = o0 + o;
-      ws[i] = og < g.K ? p.w[(og * g.C + c0) * taps + ct] : 0.f;
+      ws[i] = og < g.K ? p.w[((ob + og) * g.C + c0) * taps + ct] : 0.f;
     }
     __syncthreads();
     if (!active) continue;
     for (int cc = 0; cc < cc_n; ++cc) {
-      const float *xc = p.x + ((n * g.C + c0 + cc) * g.D) * HW;
+      const float *xc = p.x + n * g.x_batch_stride() + ((grp * g.C + c0 + cc) * g.D) * HW;
       for (int kd = 0; kd < g.KD; ++kd) {
         const int id = od * g.SD + kd * g.DD - g.PD;
         if ((unsigned)id >= (unsigned)g.D) continue;
@@ -107,8 +112,8 @@ __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParam
   for (int o = 0; o < kCO; ++o) {
     const int64_t og = o0 + o;
     if (og >= g.K) break;
-    const float b = p.bias ? __ldg(p.bias + og) : 0.f;
-    float *yo = p.y + (n * g.K + og) * osp + ((int64_t)od * g.OH + oh) * g.OW;
+    const float b = p.bias ? __ldg(p.bias + ob + og) : 0.f;
+    float *yo = p.y + n * g.y_batch_stride() + (ob + og) * osp + ((int64_t)od * g.OH + oh) * g.OW;
 #pragma unroll
     for (int r = 0; r < kR; ++r)
       if (ow0 + r < g.OW) yo[ow0 + r] = acc[o][r] + b;
@@ -122,8 +127,8 @@ bool direct_supported(const Geom &g, const char **why) {
     *why = "direct path: kernel volume above 1024 taps";
     return false;
   }
-  if ((g.K + kCO - 1) / kCO > 65535) {
-    *why = "direct path: C_out above 524280";
+  if (g.G * ((g.K + kCO - 1) / kCO) > 65535) {
+    *why = "direct path: more than 65535 blocks of 8 output channels (over all groups)";
     return false;
   }
   const int64_t items = g.N * (int64_t)g.OD * g.OH * ((g.OW + kR - 1) / kR);
@@ -147,7 +152,8 @@ cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias
   const int taps = g.taps();
   p.cchunk = (int)(g.C < kSmemFloats / (taps * kCO) ? g.C : kSmemFloats / (taps * kCO));
   const int64_t gx = (p.items + kThreads - 1) / kThreads;
-  const int64_t gy = (g.K + kCO - 1) / kCO;
+  p.kblocks = (int)((g.K + kCO - 1) / kCO);
+  const int64_t gy = g.G * p.kblocks;
   if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidConfiguration;
   dim3 grid((unsigned)gx, (unsigned)gy);
   direct_ffma_kernel<<<grid, kThreads, 0, stream>>>(p);

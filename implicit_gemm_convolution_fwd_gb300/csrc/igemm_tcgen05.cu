@@ -202,7 +202,7 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   const bool full = ps.valid && dm == (1u << g.KD) - 1u && hm == (1u << g.KH) - 1u && wm == (1u << g.KW) - 1u;
   ps.warp_full = __all_sync(0xffffffffu, full);
   const int64_t HW = (int64_t)g.H * g.W;
-  const int64_t xoff = n * g.C * HW * g.D + (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;
+  const int64_t xoff = n * g.x_batch_stride() + (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;
   ps.xo = p.x + (ps.valid ? xoff : 0);
   return ps;
 }
@@ -378,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
           pp = m - n * p.osp;
         }
       }
-      float *yp = p.y + n * g.K * p.osp + pp;
+      float *yp = p.y + n * g.G * g.K * p.osp + pp;  // batch stride spans all groups' channels
       // y[n, c0 + j, pos] = accumulator column c0 + j + bias, j < 32: a warp
       // store covers 32 consecutive positions of one channel.
       auto store32 = [&](const uint32_t (&v)[32], int c0) {

@@ -111,6 +111,24 @@ CONVFWD_API int conv_fwd_nd_ex(const float *x, const float *w, const float *bias
                    const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,
                    conv_stream_t stream);
 
+/*
+ * Grouped convolution (the pages' modules take a groups argument, left at 1
+ * there): C_in and C_out split into `groups` equal groups; output channel
+ * o = grp*(C_out/groups) + j sums over input channels grp*(C_in/groups) ...
+ * (grp+1)*(C_in/groups) - 1 only:
+ *   y[n,o,p] = bias[o] + sum_{c<C_in/groups} sum_k w[o,c,k] * x[n, grp*C_in/groups + c, p*stride + k*dilation - pad]
+ *   w [C_out, C_in/groups, k_dims...]   device, fp32; x, bias, y as for conv_fwd_nd.
+ * groups = 1 is conv_fwd_nd_ex.  groups must be >= 1 and divide C_in and C_out
+ * (CONV_ERR_ARG otherwise).  `algo` as for conv_fwd_nd_ex; the planner judges
+ * one group's problem (C_in/groups input and C_out/groups output channels).
+ * The direct family runs all groups in one launch; the tensor-core family
+ * launches once per group on the stream.
+ */
+CONVFWD_API int conv_fwd_nd_grouped(const float *x, const float *w, const float *bias, float *y, int ndim,
+                                    int64_t N, int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                                    const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                                    const int64_t *dilation, int algo, conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */

@@ -137,3 +137,15 @@ def test_algo_supported_queries(lib):
     assert not cf.algo_supported(1, 1, 1, (9999,), (1025,), 1, 0, 1, cf.CONV_ALGO_DIRECT_FFMA)
     with pytest.raises(cf.ConvError):
         cf.algo_supported(1, 1, 1, (2,), (3,), 1, 0, 1, cf.CONV_ALGO_DIRECT_FFMA)
+
+
+def test_grouped_validation_statuses(lib):
+    A = cf._arr
+    f = lib.conv_fwd_nd_grouped
+    args = lambda C_in, C_out, groups: (0x1000, 0x2000, None, 0x10000000, 1, 1, C_in, C_out, groups, A((8,)), A((3,)),
+                                        A((1,)), A((0,)), A((1,)), 0, None)
+    assert f(*args(4, 6, 0)) == cf.CONV_ERR_ARG     # groups < 1
+    assert f(*args(4, 6, 3)) == cf.CONV_ERR_ARG     # 3 does not divide C_in = 4
+    assert f(*args(6, 4, 3)) == cf.CONV_ERR_ARG     # 3 does not divide C_out = 4
+    assert "groups" in lib.conv_last_error().decode()
+

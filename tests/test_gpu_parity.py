@@ -331,3 +331,59 @@ def test_fused_min_dim_workload_sampled(min_dim):
     ref = oracle.conv3d_min_softmax_at(x, w, b, cols, min_dim)
     assert_close(yc, ref, f"fused min_dim={min_dim} full size sampled")
     assert torch.allclose(y.sum(dim=1), torch.ones((), device="cuda"), atol=1e-5)
+
+
+# ------------------------------------------------------------------ groups
+
+def run_grouped(x, w, b, s, p, d, groups, algo=cf.CONV_ALGO_AUTO):
+    xt, wt = torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda()
+    bt = None if b is None else torch.from_numpy(b).cuda()
+    y = cf.conv_fwd_nd(xt, wt, bt, s, p, d, algo=algo, groups=groups)
+    torch.cuda.synchronize()
+    return y.cpu().numpy()
+
+
+@pytest.mark.parametrize("algo", [cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_IGEMM_3XTF32])
+@pytest.mark.parametrize("nd,groups,C_in,C_out,k,s,p,d", [
+    (1, 2, 8, 40, (5,), (2,), (1,), (3,)),
+    (2, 3, 24, 48, (3, 3), (1, 2), (1, 1), (1, 1)),
+    (3, 4, 16, 64, (3, 3, 3), (1, 1, 1), (1, 0, 1), (1, 2, 1)),
+    (3, 2, 6, 34, (2, 3, 5), (1, 1, 2), (0, 1, 2), (1, 1, 1)),
+])
+def test_grouped_conv_both_families(algo, nd, groups, C_in, C_out, k, s, p, d):
+    rng = np.random.default_rng(groups * 100 + nd * 10 + algo)
+    ins = {1: (77,), 2: (13, 19), 3: (6, 9, 11)}[nd]
+    x = rng.standard_normal((2, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in // groups) + k) - 0.5) * 0.4).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv_nd(x, w, b, s, p, d, groups=groups)
+    assert_close(run_grouped(x, w, b, s, p, d, groups, algo), ref, f"grouped nd={nd} G={groups} algo={algo}")
+    assert_close(run_grouped(x, w, None, s, p, d, groups, algo), oracle.conv_nd(x, w, None, s, p, d, groups=groups),
+                 f"grouped no bias nd={nd} G={groups} algo={algo}")
+
+
+def test_depthwise_conv():
+    # groups = C_in = C_out: one input channel per output channel (direct family)
+    rng = np.random.default_rng(77)
+    C = 32
+    x = rng.standard_normal((3, C, 17, 23)).astype(np.float32)
+    w = rng.standard_normal((C, 1, 3, 3)).astype(np.float32)
+    b = rng.standard_normal(C).astype(np.float32)
+    ref = oracle.conv_nd(x, w, b, (1, 1), (1, 1), (1, 1), groups=C)
+    assert_close(run_grouped(x, w, b, (1, 1), (1, 1), (1, 1), C), ref, "depthwise 3x3")
+    # channel multiplier 2
+    w2 = rng.standard_normal((2 * C, 1, 5, 1)).astype(np.float32)
+    ref2 = oracle.conv_nd(x, w2, None, (2, 1), (2, 0), (1, 1), groups=C)
+    assert_close(run_grouped(x, w2, None, (2, 1), (2, 0), (1, 1), C), ref2, "depthwise multiplier 2")
+
+
+def test_grouped_planner_takes_tensor_cores_per_group():
+    # 4 groups of 16 -> 32 channels, 3^3 taps: each group's reduction is 432 long, so AUTO
+    # picks the tensor-core family and launches it once per group
+    rng = np.random.default_rng(78)
+    x = rng.random((2, 64, 10, 18, 20)).astype(np.float32)
+    w = ((rng.random((128, 16, 3, 3, 3)) - 0.5) * 0.1).astype(np.float32)
+    b = ((rng.random(128) - 0.5) * 0.1).astype(np.float32)
+    assert cf.select_algo(2, 16, 32, x.shape[2:], w.shape[2:], 1, 1, 1) == cf.CONV_ALGO_IGEMM_3XTF32
+    ref = oracle.conv_nd(x, w, b, (1, 1, 1), (1, 1, 1), (1, 1, 1), groups=4)
+    assert_close(run_grouped(x, w, b, (1, 1, 1), (1, 1, 1), (1, 1, 1), 4), ref, "grouped tensor-core AUTO")
