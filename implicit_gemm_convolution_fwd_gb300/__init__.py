@@ -18,7 +18,8 @@ CONV_ALGO_AUTO, CONV_ALGO_DIRECT_FFMA, CONV_ALGO_IGEMM_3XTF32 = 0, 1, 2
 ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV_ALGO_IGEMM_3XTF32: "igemm_3xtf32"}
 
 # every symbol include/convfwd.h declares
-EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_select_algo",
+EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_fwd_nd_channels_last",
+            "conv_select_algo",
             "conv_algo_supported",
             "conv3d_min_softmax",
             "conv_status_string", "conv_last_error", "conv_device_status")
@@ -56,6 +57,8 @@ def load(path: str | None = None):
     lib.conv_fwd_nd.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, arr, arr, arr, arr, arr, vp]
     lib.conv_fwd_nd_ex.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, arr, arr, arr, arr, arr, i32, vp]
     lib.conv_fwd_nd_grouped.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, i32, vp]
+    lib.conv_fwd_nd_channels_last.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, i32,
+                                              vp]
     lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
@@ -128,16 +131,33 @@ def _stream_handle(stream):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
+def _channels_last_view(t):
+    """The [N, *spatial, C] tensor whose memory a channels-last [N, C, *spatial] tensor occupies, or None."""
+    nd = t.dim() - 2
+    v = t.permute(0, *range(2, nd + 2), 1)
+    return v if v.is_contiguous() else None
+
+
 def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CONV_ALGO_AUTO, stream=None,
-                groups=1):
-    """y = conv(x, w) + bias for contiguous fp32 CUDA tensors x [N,C_in,*in], w [C_out,C_in/groups,*k]."""
+                groups=1, channels_last=False):
+    """y = conv(x, w) + bias for fp32 CUDA tensors x [N,C_in,*in], w [C_out,C_in/groups,*k].
+    Default layout: contiguous (N C D H W).  channels_last=True: x, w (and out) keep their logical
+    shapes but are stored channels last (torch.channels_last / channels_last_3d, i.e. N D H W C);
+    the returned y is allocated the same way."""
     import torch
     nd = x.dim() - 2
     if nd not in (1, 2, 3) or w.dim() != x.dim():
         raise ValueError("x and w must be 3-D, 4-D or 5-D tensors of the same rank")
     for t in (x, w) + ((bias,) if bias is not None else ()):
-        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
-            raise ValueError("tensors must be contiguous float32 CUDA tensors")
+        if not (t.is_cuda and t.dtype == torch.float32):
+            raise ValueError("tensors must be float32 CUDA tensors")
+    if bias is not None and not bias.is_contiguous():
+        raise ValueError("bias must be contiguous")
+    if channels_last:
+        if _channels_last_view(x) is None or _channels_last_view(w) is None:
+            raise ValueError("channels_last=True needs x and w stored channels last")
+    elif not (x.is_contiguous() and w.is_contiguous()):
+        raise ValueError("x and w must be contiguous (or pass channels_last=True)")
     s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
@@ -145,13 +165,19 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
         raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
     od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
     if out is None:
-        out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
-    elif tuple(out.shape) != (N, C_out) + od or not out.is_contiguous():
-        raise ValueError("out has the wrong shape or is not contiguous")
+        if channels_last:
+            out = torch.empty((N,) + od + (C_out,), device=x.device, dtype=torch.float32).permute(0, nd + 1,
+                                                                                              *range(1, nd + 1))
+        else:
+            out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
+    elif tuple(out.shape) != (N, C_out) + od or (
+            _channels_last_view(out) is None if channels_last else not out.is_contiguous()):
+        raise ValueError("out has the wrong shape or memory layout")
     lib = load()
-    st = lib.conv_fwd_nd_grouped(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
-                                 out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
-                                 _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), int(algo), _stream_handle(stream))
+    fn = lib.conv_fwd_nd_channels_last if channels_last else lib.conv_fwd_nd_grouped
+    st = fn(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(), nd, N, C_in,
+            C_out, int(groups), _arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), int(algo),
+            _stream_handle(stream))
     _check(st)
     return out
 

@@ -110,6 +110,7 @@ int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *i
   g->C = Cg;
   g->K = C_out / groups;
   g->G = groups;
+  g->cl = 0;
   g->D = gi[0], g->H = gi[1], g->W = gi[2];
   g->OD = go[0], g->OH = go[1], g->OW = go[2];
   g->KD = gk[0], g->KH = gk[1], g->KW = gk[2];
@@ -229,6 +230,33 @@ int conv_fwd_nd_grouped(const float *x, const float *w, const float *bias, float
                                        g, s);
   }
   if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd: kernel launch");
+  return CONV_OK;
+}
+
+int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                              int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                              const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                              const int64_t *dilation, int algo, conv_stream_t stream) {
+  g_last_error[0] = 0;
+  Geom g;
+  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, -1,
+                         groups);
+  if (st != CONV_OK) return st;
+  g.cl = 1;
+  if (algo == CONV_ALGO_DIRECT_FFMA)
+    return fail(CONV_ERR_UNSUPPORTED, "conv: channels-last tensors run on the tensor-core family only%s");
+  const char *why = "";
+  if (!convfwd::igemm_supported(g, &why))
+    return fail(CONV_ERR_UNSUPPORTED, "conv: tensor-core path cannot run this channels-last shape: %s", why);
+  if (algo != CONV_ALGO_AUTO && algo != CONV_ALGO_IGEMM_3XTF32)
+    return fail(CONV_ERR_ARG, "conv: unknown algo %s%lld", "", algo);
+  if (g.N == 0) return CONV_OK;
+  // one launch per group on channel offsets of x, w, bias and y
+  cudaError_t e = cudaSuccess;
+  for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
+    e = convfwd::launch_igemm_3xtf32(x + grp * g.C, w + grp * g.K * g.C * g.taps(), bias ? bias + grp * g.K : nullptr,
+                                     y + grp * g.K, g, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_channels_last: kernel launch");
   return CONV_OK;
 }
 

@@ -15,6 +15,7 @@ namespace convfwd {
 struct Geom {
   int64_t N, C, K;             // batch, input channels per group, output channels per group
   int64_t G;                   // groups (1: a plain convolution)
+  int cl;                      // memory layout: 0 = N C D H W (PyTorch default), 1 = N D H W C (channels last)
   int D, H, W;                 // input spatial dims
   int OD, OH, OW;              // output spatial dims
   int KD, KH, KW;              // kernel dims

@@ -74,7 +74,10 @@ struct IgemmParams {
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
   int nslots;       // tile slots (2 or 4), each with an MMA-issuing thread and an accumulator
-  int tap_major;    // reduction ordered (tap, c) instead of (c, tap); padded convs with C_in % 4 == 0
+  int tap_major;    // reduction ordered (tap, c) instead of (c, tap); padded convs with C_in % 4 == 0,
+                    // and always for channels-last tensors
+  int vec4;         // channels last with 16-byte aligned groups of 4 channels: float4 gathers
+  int vec_store;    // channels last with 16-byte aligned output rows: float4 stores
   uint32_t b_bytes; // Npad * Kpad * 4
 };
 
@@ -93,8 +96,8 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
     return false;
   }
   const int64_t HW = (int64_t)g.H * g.W, DHW = HW * g.D;
-  const int64_t max_off = (g.C - 1) * DHW + (int64_t)(g.KD - 1) * g.DD * HW + (int64_t)(g.KH - 1) * g.DH * g.W +
-                          (int64_t)(g.KW - 1) * g.DW;
+  const int64_t tap_span = (int64_t)(g.KD - 1) * g.DD * HW + (int64_t)(g.KH - 1) * g.DH * g.W + (int64_t)(g.KW - 1) * g.DW;
+  const int64_t max_off = g.cl ? tap_span * g.G * g.C + (g.C - 1) : (g.C - 1) * DHW + tap_span;
   if (max_off >= (int64_t)1 << 31) {
     *why = "receptive-field offsets of one image exceed 2^31 elements";
     return false;
@@ -111,6 +114,9 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
   // the unchecked path, where the channel-major order reads x with better
   // locality (consecutive columns hit the same cache lines).
   pl->tap_major = (g.C % 4 == 0 && (g.PD > 0 || g.PH > 0 || g.PW > 0)) ? 1 : 0;
+  // Channels-last tensors: (tap, c) is the weights' memory order and makes
+  // consecutive columns consecutive addresses.
+  if (g.cl) pl->tap_major = 1;
   // TMEM: one accumulator of Npad columns per slot, then two A stages per
   // slot of KC hi + KC lo columns.  Four slots (four MMA instruction streams)
   // when the accumulators leave room for 16-column stages, else two.
@@ -202,7 +208,8 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   const bool full = ps.valid && dm == (1u << g.KD) - 1u && hm == (1u << g.KH) - 1u && wm == (1u << g.KW) - 1u;
   ps.warp_full = __all_sync(0xffffffffu, full);
   const int64_t HW = (int64_t)g.H * g.W;
-  const int64_t xoff = n * g.x_batch_stride() + (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;
+  const int64_t pos = (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;  // may be negative (padding)
+  const int64_t xoff = g.cl ? (n * HW * g.D + pos) * (g.G * g.C) : n * g.x_batch_stride() + pos;
   ps.xo = p.x + (ps.valid ? xoff : 0);
   return ps;
 }
@@ -214,8 +221,27 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
 // 16-byte shared load and skip every bounds test; only a unit that reaches the
 // padding columns checks them.
 __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
-                                            int Kred, bool tap_major, float (&v)[kUnit]) {
-  if (ps.warp_full) {
+                                            int Kred, bool tap_major, bool vec4, float (&v)[kUnit]) {
+  if (vec4) {
+    // channels last, C % 4 == 0: columns 4q .. 4q+3 are 4 consecutive channels
+    // of one tap, 16-byte aligned; one test per group, one 16-byte load
+#pragma unroll
+    for (int q = 0; q < kUnit / 4; ++q) {
+      const int k = k0 + 4 * q;
+      bool in = k < Kred;
+      if (!ps.warp_full) {
+        const uint32_t e = ttap[k];
+        const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+        in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      }
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (in) a = __ldg(reinterpret_cast<const float4 *>(ps.xo + toff[k]));
+      v[4 * q + 0] = a.x;
+      v[4 * q + 1] = a.y;
+      v[4 * q + 2] = a.z;
+      v[4 * q + 3] = a.w;
+    }
+  } else if (ps.warp_full) {
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
     if (k0 + kUnit <= Kred) {
 #pragma unroll
@@ -301,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
       // w is [C_out][C_in][taps]; GEMM column k maps to (c, t) by the reduction order
       int kmem = k;
-      if (p.tap_major && k < p.Kred) {
+      if (p.tap_major && !g.cl && k < p.Kred) {
         const int t = k / g.C;
         kmem = (k - t * g.C) * taps + t;
       }
@@ -323,7 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         }
         const int kw = t % g.KW, khd = t / g.KW;
         const int kd = khd / g.KH, kh = khd - kd * g.KH;
-        toff[kk] = (int32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
+        const int64_t tpos = (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW;
+        toff[kk] = (int32_t)(g.cl ? tpos * (g.G * g.C) + c : c * DHW + tpos);
         ttap[kk] = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
       } else {
         toff[kk] = 0;
@@ -378,10 +405,31 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
           pp = m - n * p.osp;
         }
       }
-      float *yp = p.y + n * g.G * g.K * p.osp + pp;  // batch stride spans all groups' channels
+      // y[n, o, pos] (batch stride spans all groups' channels), or y[n, pos, o] channels last
+      float *yp = g.cl ? p.y + (n * p.osp + pp) * (g.G * g.K) : p.y + n * g.G * g.K * p.osp + pp;
       // y[n, c0 + j, pos] = accumulator column c0 + j + bias, j < 32: a warp
       // store covers 32 consecutive positions of one channel.
       auto store32 = [&](const uint32_t (&v)[32], int c0) {
+        if (g.cl) {
+          // one position's channels are contiguous: 16-byte stores when aligned
+          if (p.vec_store && c0 + 32 <= g.K) {
+            float4 *q4 = reinterpret_cast<float4 *>(yp + c0);
+            const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + c0);
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 bb = b4[j4];
+              __stcs(q4 + j4, make_float4(__uint_as_float(v[4 * j4 + 0]) + bb.x, __uint_as_float(v[4 * j4 + 1]) + bb.y,
+                                          __uint_as_float(v[4 * j4 + 2]) + bb.z, __uint_as_float(v[4 * j4 + 3]) + bb.w));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const int o = c0 + j;
+              if (o < g.K) __stcs(yp + o, __uint_as_float(v[j]) + bias_s[o]);
+            }
+          }
+          return;
+        }
         if (c0 + 32 <= g.K) {
           float *q = yp + (int64_t)c0 * p.osp;
           const float4 *b4 = reinterpret_cast<const float4 *>(bias_s + c0);
@@ -458,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0, vu);
+          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0, p.vec4 != 0, vu);
         }
       }
     };
@@ -614,6 +662,8 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
   p.nchunks = pl.nchunks;
   p.nslots = pl.nslots;
   p.tap_major = pl.tap_major;
+  p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
+  p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)y & 15u) == 0) ? 1 : 0;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
   if (pl.KC <= 16)

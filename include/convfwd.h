@@ -129,6 +129,25 @@ CONVFWD_API int conv_fwd_nd_grouped(const float *x, const float *w, const float 
                                     const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
                                     const int64_t *dilation, int algo, conv_stream_t stream);
 
+/*
+ * Channels-last layout: the same convolution (groups included) on tensors
+ * stored N (D) (H) W C, i.e. PyTorch's channels_last / channels_last_3d memory
+ * format; dims are still passed in the logical N, C, spatial order.
+ *   x [N, in_dims..., C_in]   w [C_out, k_dims..., C_in/groups]   y [N, out_dims..., C_out]
+ *   bias [C_out] or NULL.  Everything else as conv_fwd_nd_grouped.
+ * The reduction runs tap by tap with the channels innermost, so with
+ * C_in/groups % 4 == 0 and 16-byte aligned x each gather is one 16-byte load
+ * of 4 channels, and each output position's channels are written as one
+ * contiguous run.  Only the tensor-core family runs this layout: algo must be
+ * CONV_ALGO_AUTO or CONV_ALGO_IGEMM_3XTF32; CONV_ALGO_DIRECT_FFMA and shapes
+ * the tensor-core path does not take return CONV_ERR_UNSUPPORTED.
+ */
+CONVFWD_API int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias, float *y, int ndim,
+                                          int64_t N, int64_t C_in, int64_t C_out, int64_t groups,
+                                          const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                                          const int64_t *pad, const int64_t *dilation, int algo,
+                                          conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */

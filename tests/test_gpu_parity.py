@@ -387,3 +387,42 @@ def test_grouped_planner_takes_tensor_cores_per_group():
     assert cf.select_algo(2, 16, 32, x.shape[2:], w.shape[2:], 1, 1, 1) == cf.CONV_ALGO_IGEMM_3XTF32
     ref = oracle.conv_nd(x, w, b, (1, 1, 1), (1, 1, 1), (1, 1, 1), groups=4)
     assert_close(run_grouped(x, w, b, (1, 1, 1), (1, 1, 1), (1, 1, 1), 4), ref, "grouped tensor-core AUTO")
+
+
+# ------------------------------------------------------- channels last
+
+def to_channels_last(a):
+    """A CUDA tensor with a's logical shape [N, C, *sp] stored as [N, *sp, C]."""
+    nd = a.ndim - 2
+    t = torch.from_numpy(np.ascontiguousarray(np.moveaxis(a, 1, -1))).cuda()
+    return t.permute(0, nd + 1, *range(1, nd + 1))
+
+
+@pytest.mark.parametrize("nd,groups,C_in,C_out,k,s,p,d,N", [
+    (3, 1, 8, 64, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),    # padded, C % 4 == 0: 16-byte gathers
+    (3, 1, 32, 32, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), 1),   # the second sweep's channels (K = 864)
+    (3, 1, 3, 64, (3, 5, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2),    # the headline's channel count: scalar gathers
+    (2, 2, 24, 96, (3, 3), (2, 1), (1, 2), (1, 2), 3),
+    (1, 1, 64, 128, (3,), (3,), (0,), (4,), 2),                       # the long Conv1d's geometry, short
+    (2, 1, 6, 20, (5, 2), (1, 1), (2, 0), (1, 1), 1),                 # C_out not a multiple of 4: scalar stores
+])
+def test_channels_last_conv(nd, groups, C_in, C_out, k, s, p, d, N):
+    rng = np.random.default_rng(C_in * 13 + C_out + nd)
+    ins = {1: (301,), 2: (14, 17), 3: (7, 12, 13)}[nd]
+    x = rng.standard_normal((N, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in // groups) + k) - 0.5) * 0.3).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv_nd(x, w, b, s, p, d, groups=groups)
+    y = cf.conv_fwd_nd(to_channels_last(x), to_channels_last(w), torch.from_numpy(b).cuda(), s, p, d,
+                       groups=groups, channels_last=True)
+    torch.cuda.synchronize()
+    assert y.permute(0, *range(2, nd + 2), 1).is_contiguous()
+    assert_close(y.cpu().numpy(), ref, f"channels last nd={nd} C_in={C_in} C_out={C_out} G={groups}")
+
+
+def test_channels_last_rejects_direct_family():
+    x = to_channels_last(np.zeros((1, 4, 9), np.float32))
+    w = to_channels_last(np.zeros((8, 4, 3), np.float32))
+    with pytest.raises(cf.ConvError) as e:
+        cf.conv_fwd_nd(x, w, None, 1, 0, 1, algo=cf.CONV_ALGO_DIRECT_FFMA, channels_last=True)
+    assert e.value.status == cf.CONV_ERR_UNSUPPORTED
