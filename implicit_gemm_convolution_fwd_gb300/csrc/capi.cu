@@ -126,17 +126,17 @@ int make_geom(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *i
 int validate_conv(const float *x, const float *w, const float *bias, const float *y, int ndim, int64_t N,
                   int64_t C_in, int64_t C_out, const int64_t *in, const int64_t *k, const int64_t *s,
                   const int64_t *p, const int64_t *d, Geom *g, int64_t y_elems_override = -1,
-                  int64_t groups = 1) {
+                  int64_t groups = 1, int esize = 4) {
   int64_t xe, we, ye;
   int st = make_geom(ndim, N, C_in, C_out, in, k, s, p, d, g, &xe, &we, &ye, groups);
   if (st != CONV_OK) return st;
   // an empty batch has empty x and y, which may be NULL
   if (!w || (N > 0 && (!x || !y))) return fail(CONV_ERR_NULL, "conv: x, w and y must be non-NULL%s");
   if (y_elems_override >= 0) ye = y_elems_override;
-  if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)y | (uintptr_t)bias) & 3u)
-    return fail(CONV_ERR_ARG, "conv: x, w, bias, y must be 4-byte aligned%s");
-  if (ranges_overlap(y, ye * 4, x, xe * 4) || ranges_overlap(y, ye * 4, w, we * 4) ||
-      ranges_overlap(y, ye * 4, bias, C_out * 4))
+  if (((uintptr_t)x | (uintptr_t)w | (uintptr_t)y | (uintptr_t)bias) & (uintptr_t)(esize - 1))
+    return fail(CONV_ERR_ARG, "conv: x, w, bias, y must be aligned to their element size%s");
+  if (ranges_overlap(y, ye * esize, x, xe * esize) || ranges_overlap(y, ye * esize, w, we * esize) ||
+      ranges_overlap(y, ye * esize, bias, C_out * esize))
     return fail(CONV_ERR_ARG, "conv: y overlaps an input buffer%s");
   return CONV_OK;
 }
@@ -257,6 +257,27 @@ int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias,
     e = convfwd::launch_igemm_3xtf32(x + grp * g.C, w + grp * g.K * g.C * g.taps(), bias ? bias + grp * g.K : nullptr,
                                      y + grp * g.K, g, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_channels_last: kernel launch");
+  return CONV_OK;
+}
+
+int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim, int64_t N,
+                     int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                     const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream) {
+  g_last_error[0] = 0;
+  Geom g;
+  int st = validate_conv((const float *)x, (const float *)w, (const float *)bias, (const float *)y, ndim, N, C_in,
+                         C_out, in_dims, k_dims, stride, pad, dilation, &g, -1, groups, 2);
+  if (st != CONV_OK) return st;
+  const char *why = "";
+  if (!convfwd::igemm_bf16_supported(g, &why))
+    return fail(CONV_ERR_UNSUPPORTED, "conv_fwd_nd_bf16: the tensor-core path cannot run this shape: %s", why);
+  if (g.N == 0) return CONV_OK;
+  const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
+  cudaError_t e = cudaSuccess;
+  for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
+    e = convfwd::launch_igemm_bf16(x + grp * xg, w + grp * wg, bias ? bias + grp * g.K : nullptr, y + grp * yg, g,
+                                   (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_bf16: kernel launch");
   return CONV_OK;
 }
 

@@ -1,0 +1,319 @@
+// BF16 variant of the implicit-GEMM kernel: x, w and bias in bfloat16, the
+// products and their sum in fp32 (tensor-core accumulator), y rounded once to
+// bfloat16 (round to nearest even) at the store.  The conv sum is the one in
+// the l1_p60 page (turn 1); the pages weigh BF16 against fp32 accuracy and
+// keep fp32, so this path is the lower-precision option next to 3xTF32.
+//
+// Structure as the 3xTF32 kernel (same warp roles, slots, tables and waits);
+// what changes:
+//   * no hi/lo split: a gathered value is stored once, two bf16 per 32-bit
+//     TMEM column, so one 32-column chunk of K fills 16 TMEM columns;
+//   * one tcgen05.mma kind::f16 per 16 reduction columns (K = 16);
+//   * B holds one bf16 copy of the weights: core matrices of 8 rows x 8 bf16,
+//     LBO = 128 bytes along K, SBO = Kpad * 16 bytes along N.
+// This file is included inside igemm_tcgen05.cu's anonymous namespace.
+
+constexpr int kBfChunk = 32;  // reduction columns per chunk (16 TMEM columns)
+
+struct PlanBf16 {
+  int Kred, Kpad, Npad, nchunks, nslots, tap_major;
+  size_t smem;
+};
+
+bool make_plan_bf16(const Geom &g, PlanBf16 *pl, const char **why) {
+  if (g.K > kMaxNpad) {
+    *why = "C_out (per group) above 128";
+    return false;
+  }
+  if (g.KD > 32 || g.KH > 32 || g.KW > 32) {
+    *why = "a kernel dimension above 32";
+    return false;
+  }
+  if (g.cl) {
+    *why = "channels-last layout is fp32 only";
+    return false;
+  }
+  const int64_t HW = (int64_t)g.H * g.W, DHW = HW * g.D;
+  const int64_t max_off = (g.C - 1) * DHW + (int64_t)(g.KD - 1) * g.DD * HW + (int64_t)(g.KH - 1) * g.DH * g.W +
+                          (int64_t)(g.KW - 1) * g.DW;
+  if (max_off >= (int64_t)1 << 31) {
+    *why = "receptive-field offsets of one image exceed 2^31 elements";
+    return false;
+  }
+  const int64_t kred = g.C * (int64_t)g.KD * g.KH * g.KW;
+  pl->Kred = (int)kred;
+  pl->Kpad = (int)((kred + kBfChunk - 1) / kBfChunk * kBfChunk);
+  pl->Npad = (int)((g.K + 31) / 32 * 32);
+  // TMEM: one accumulator of Npad columns per slot, two A stages of 16 columns per slot
+  pl->nslots = (kMaxSlots * pl->Npad + 2 * kMaxSlots * (kBfChunk / 2) <= (int)kTmemCols) ? kMaxSlots : 2;
+  pl->nchunks = pl->Kpad / kBfChunk;
+  pl->tap_major = (g.C % 4 == 0 && (g.PD > 0 || g.PH > 0 || g.PW > 0)) ? 1 : 0;
+  const size_t smem = (size_t)pl->Npad * pl->Kpad * 2 + (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 +
+                      kNumBars * 8 + 16;
+  if (smem > (size_t)kMaxSmem) {
+    *why = "weights do not fit in shared memory";
+    return false;
+  }
+  pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
+  return true;
+}
+
+// 16 consecutive reduction columns of one output position as bf16 bit
+// patterns (zero-extended to 32 bits); same tables and paths as gather_cols.
+__device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16_t *xo, const int32_t *toff,
+                                                 const uint32_t *ttap, int k0, int Kred, bool tap_major,
+                                                 uint32_t (&v)[kUnit]) {
+  if (ps.warp_full) {
+    const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
+#pragma unroll
+    for (int q = 0; q < kUnit / 4; ++q) {
+      const int4 o = o4[q];
+      const int k = k0 + 4 * q;
+      v[4 * q + 0] = k + 0 < Kred ? (uint32_t)__ldg(xo + o.x) : 0u;
+      v[4 * q + 1] = k + 1 < Kred ? (uint32_t)__ldg(xo + o.y) : 0u;
+      v[4 * q + 2] = k + 2 < Kred ? (uint32_t)__ldg(xo + o.z) : 0u;
+      v[4 * q + 3] = k + 3 < Kred ? (uint32_t)__ldg(xo + o.w) : 0u;
+    }
+  } else if (tap_major) {
+    const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
+#pragma unroll
+    for (int q = 0; q < kUnit / 4; ++q) {
+      const uint32_t e = ttap[k0 + 4 * q];
+      const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+      const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      const int4 o = o4[q];
+      v[4 * q + 0] = in ? (uint32_t)__ldg(xo + o.x) : 0u;
+      v[4 * q + 1] = in ? (uint32_t)__ldg(xo + o.y) : 0u;
+      v[4 * q + 2] = in ? (uint32_t)__ldg(xo + o.z) : 0u;
+      v[4 * q + 3] = in ? (uint32_t)__ldg(xo + o.w) : 0u;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < kUnit; ++j) {
+      const uint32_t e = ttap[k0 + j];
+      const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+      const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      v[j] = in ? (uint32_t)__ldg(xo + toff[k0 + j]) : 0u;
+    }
+  }
+}
+
+__device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
+
+__global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Geom &g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  uint8_t *b_s = smem;
+  int32_t *toff = reinterpret_cast<int32_t *>(smem + p.b_bytes);  // [Kpad]
+  uint32_t *ttap = reinterpret_cast<uint32_t *>(toff + p.Kpad);    // [Kpad]
+  float *bias_s = reinterpret_cast<float *>(ttap + p.Kpad);
+  uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const uint32_t bar_a_full = ptx::smem_addr(bars + 0);
+  const uint32_t bar_a_empty = ptx::smem_addr(bars + kMaxStages);
+  const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kMaxStages);
+  const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kMaxStages + kMaxSlots);
+  const uint32_t bar_drain = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots);
+  const int nslots = p.nslots;
+
+  const uint32_t SBO = (uint32_t)p.Kpad * 16;  // bytes between 8-row groups of B
+  const int taps = g.KD * g.KH * g.KW;
+  const int64_t HW = (int64_t)g.H * g.W, DHW = HW * g.D;
+
+  // ---- weights -> shared memory as bf16 pairs.  32-bit word i of the
+  // core-matrix layout holds B[n][k], B[n][k+1] with n = 8*(cm / (Kpad/8)) +
+  // row, k = 8*(cm % (Kpad/8)) + 2*pair (cm = i / 32, row = (i / 4) % 8,
+  // pair = i % 4): consecutive threads write consecutive words.
+  {
+    const int kq8 = p.Kpad / 8;
+    const int words = p.Npad * p.Kpad / 2;
+    for (int i = tid; i < words; i += kThreads) {
+      const int cm = i >> 5, r = (i >> 2) & 7, pr = i & 3;
+      const int n = (cm / kq8) * 8 + r, k = (cm % kq8) * 8 + pr * 2;
+      uint32_t word = 0;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int kk = k + h;
+        if (n < g.K && kk < p.Kred) {
+          int kmem = kk;
+          if (p.tap_major) {
+            const int t = kk / g.C;
+            kmem = (kk - t * g.C) * taps + t;
+          }
+          word |= (uint32_t)__ldg(p.wh + (int64_t)n * p.Kred + kmem) << (16 * h);
+        }
+      }
+      reinterpret_cast<uint32_t *>(b_s)[i] = word;
+    }
+    for (int kk = tid; kk < p.Kpad; kk += kThreads) {
+      if (kk < p.Kred) {
+        int c, t;
+        if (p.tap_major) {
+          t = kk / g.C;
+          c = kk - t * g.C;
+        } else {
+          c = kk / taps;
+          t = kk - c * taps;
+        }
+        const int kw = t % g.KW, khd = t / g.KW;
+        const int kd = khd / g.KH, kh = khd - kd * g.KH;
+        toff[kk] = (int32_t)(c * DHW + (int64_t)kd * g.DD * HW + (int64_t)kh * g.DH * g.W + (int64_t)kw * g.DW);
+        ttap[kk] = (uint32_t)kd | ((uint32_t)kh << 8) | ((uint32_t)kw << 16);
+      } else {
+        toff[kk] = 0;
+        ttap[kk] = 0x80000000u;
+      }
+    }
+    for (int i = tid; i < p.Npad; i += kThreads)
+      bias_s[i] = (p.bh && i < g.K) ? bf16_bits_to_float(__ldg(p.bh + i)) : 0.f;
+  }
+  ptx::fence_proxy_async_smem();
+  if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+  if (tid == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      ptx::mbar_init(bar_a_full + 8 * s, 128);
+      ptx::mbar_init(bar_a_empty + 8 * s, 1);
+    }
+    for (int b = 0; b < kMaxSlots; ++b) {
+      ptx::mbar_init(bar_d_full + 8 * b, 1);
+      ptx::mbar_init(bar_d_empty + 8 * b, 128);
+    }
+    ptx::mbar_init(bar_drain, nslots);
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // slot b: accumulator at column b * Npad; A stage s (2 per slot) at a_col0 + 16 * s
+  const uint32_t a_col0 = (uint32_t)(nslots * p.Npad);
+
+  if (warp < kEpiWarps) {
+    // ------------------------------------------------------------ epilogue
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int64_t my_tiles = cta_tile_count(p);
+    for (int64_t it = 0; it < my_tiles; ++it) {
+      const int64_t tile = tile_of(p, it);
+      const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
+      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const int64_t m = tile * kTileM + tid;
+      const bool valid = m < p.M_total;
+      int64_t n = 0, pp = 0;
+      if (valid) {
+        n = m / p.osp;
+        pp = m - n * p.osp;
+      }
+      uint16_t *yp = p.yh + n * g.G * g.K * p.osp + pp;
+      for (int c0 = 0; c0 < p.Npad; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
+        ptx::tmem_wait_ld();
+        if (c0 + 32 >= p.Npad) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d_empty + 8 * b);
+        }
+        if (valid) {
+          uint16_t *q = yp + (int64_t)c0 * p.osp;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (c0 + j < g.K) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]) + bias_s[c0 + j]);
+              __stcs(reinterpret_cast<unsigned short *>(q), __bfloat16_as_ushort(h));
+            }
+            q += p.osp;
+          }
+        }
+      }
+    }
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ producers
+    const int grp = (warp - kEpiWarps) >> 2;
+    const int gps = kProdGroups / nslots;
+    const int slot = grp / gps, sel = grp - slot * gps;
+    const int t = tid - 32 * kEpiWarps - 128 * grp;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const int64_t my_tiles = cta_tile_count(p);
+    const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;
+    bool aborted = false;
+    for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
+      const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
+      const uint16_t *xo = p.xh + (ps.valid ? ps.xoff : 0);
+      const int64_t lg0 = li * p.nchunks;
+      for (int q = (int)((sel - lg0 % gps + gps) % gps); q < p.nchunks; q += gps) {
+        const int64_t lg = lg0 + q;
+        const int stage = 2 * slot + (int)(lg & 1);
+        const int k0 = q * kBfChunk;
+        uint32_t packed[kBfChunk / 2];
+#pragma unroll
+        for (int u = 0; u < kBfChunk / kUnit; ++u) {
+          uint32_t v[kUnit];
+          gather_cols_bf16(ps, xo, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0, v);
+#pragma unroll
+          for (int j = 0; j < kUnit / 2; ++j) packed[u * (kUnit / 2) + j] = __byte_perm(v[2 * j], v[2 * j + 1], 0x5410);
+        }
+        const uint32_t r = (uint32_t)(lg >> 1);
+        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
+          aborted = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        ptx::tmem_st16(tmem + lane_base + a_col0 + (uint32_t)(16 * stage), packed);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_a_full + 8 * stage);
+      }
+    }
+  } else if (lane == 0 && warp - kMmaWarp < nslots) {
+    // ------------------------------------------------------------ MMA issuers
+    const int slot = warp - kMmaWarp;
+    const uint32_t idesc = ptx::idesc_bf16(kTileM, (uint32_t)p.Npad);
+    const uint32_t bsa = ptx::smem_addr(b_s);
+    const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
+    const int64_t my_tiles = cta_tile_count(p);
+    bool aborted = false;
+    for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
+      const int64_t li = it / nslots;
+      if (!wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag)) break;
+      ptx::tc_fence_after();
+      for (int q = 0; q < p.nchunks; ++q) {
+        const int64_t lg = li * p.nchunks + q;
+        const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
+        if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag)) {
+          aborted = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a = tmem + a_col0 + 16u * s;
+#pragma unroll
+        for (int ks = 0; ks < kBfChunk / 16; ++ks) {
+          const uint32_t kbyte = (uint32_t)((q * kBfChunk + ks * 16) / 8) * 128u;  // core matrices along K
+          const uint64_t bd = ptx::smem_desc_noswizzle(bsa + kbyte, 128, SBO);
+          ptx::mma_f16_ts(d_tmem, a + 8u * ks, bd, idesc, (q | ks) != 0);
+        }
+        ptx::mma_commit(bar_a_empty + 8 * s);
+      }
+      if (aborted) break;
+      ptx::mma_commit(bar_d_full + 8 * slot);
+    }
+    if (*abort_flag) {
+      ptx::mma_commit(bar_drain);
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}

@@ -31,6 +31,7 @@
 // between roles uses mbarriers; tcgen05.commit signals MMA completion.  Every
 // wait is bounded: on timeout the kernel raises a flag, lets the other roles
 // fall through, drains its MMAs and frees TMEM.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -64,6 +65,11 @@ struct IgemmParams {
   const float *__restrict__ w;
   const float *__restrict__ bias;
   float *__restrict__ y;
+  // the BF16 kernel's tensors (bfloat16 bit patterns); unused by the 3xTF32 kernel
+  const uint16_t *__restrict__ xh;
+  const uint16_t *__restrict__ wh;
+  const uint16_t *__restrict__ bh;
+  uint16_t *__restrict__ yh;
   Geom g;
   int64_t M_total;  // N * OD * OH * OW
   int64_t osp;      // OD * OH * OW
@@ -166,6 +172,7 @@ __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_ui
 // One producer thread's output position within a tile.
 struct PosInfo {
   const float *xo;      // x at the receptive field's origin (may lie in the padding)
+  int64_t xoff;         // the same as an element offset from x
   uint32_t dm, hm, wm;  // bit k set: tap k along D / H / W lands inside the input
   bool valid;           // the position exists (last tile may be partial)
   bool warp_full;       // every lane's receptive field is entirely inside the input
@@ -210,6 +217,7 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   const int64_t HW = (int64_t)g.H * g.W;
   const int64_t pos = (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;  // may be negative (padding)
   const int64_t xoff = g.cl ? (n * HW * g.D + pos) * (g.G * g.C) : n * g.x_batch_stride() + pos;
+  ps.xoff = xoff;
   ps.xo = p.x + (ps.valid ? xoff : 0);
   return ps;
 }
@@ -616,7 +624,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   }
 }
 
+#include "igemm_bf16.cuh"
+
 int g_num_sms[64] = {0};
+bool g_attr_bf16_set[64] = {false};
 bool g_attr_set[64] = {false};
 
 }  // namespace
@@ -670,6 +681,51 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     igemm_3xtf32_kernel<16><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   else
     igemm_3xtf32_kernel<32><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+bool igemm_bf16_supported(const Geom &g, const char **why) {
+  PlanBf16 pl;
+  return make_plan_bf16(g, &pl, why);
+}
+
+cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, const Geom &g,
+                              cudaStream_t stream) {
+  PlanBf16 pl;
+  const char *why = "";
+  if (!make_plan_bf16(g, &pl, &why)) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (g_num_sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  if (!g_attr_bf16_set[dev]) {
+    e = cudaFuncSetAttribute(igemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e != cudaSuccess) return e;
+    g_attr_bf16_set[dev] = true;
+  }
+  IgemmParams p = {};
+  p.xh = x;
+  p.wh = w;
+  p.bh = bias;
+  p.yh = y;
+  p.g = g;
+  p.osp = (int64_t)g.OD * g.OH * g.OW;
+  p.M_total = g.N * p.osp;
+  p.tiles = (p.M_total + kTileM - 1) / kTileM;
+  p.Kred = pl.Kred;
+  p.Kpad = pl.Kpad;
+  p.Npad = pl.Npad;
+  p.KC = kBfChunk;
+  p.nchunks = pl.nchunks;
+  p.nslots = pl.nslots;
+  p.tap_major = pl.tap_major;
+  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 2);
+  const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+  igemm_bf16_kernel<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -77,6 +77,17 @@ __device__ __forceinline__ void mma_tf32_ts(uint32_t d_tmem, uint32_t a_tmem, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16 (both operands BF16 per the
+// instruction descriptor), fp32 accumulator, single CTA.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive (once) on an mbarrier when all previously issued tcgen05 async
 // operations of this thread have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
@@ -159,6 +170,16 @@ __host__ __device__ constexpr uint32_t idesc_tf32(uint32_t M, uint32_t N) {
   return (1u << 4)           // D format: F32
          | (2u << 7)         // A format: TF32
          | (2u << 10)        // B format: TF32
+         | ((N >> 3) << 17)  // N / 8
+         | ((M >> 4) << 24); // M / 16
+}
+
+// Instruction descriptor for kind::f16 with BF16 A and B (the same type for
+// both operands), fp32 accumulator, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
+  return (1u << 4)           // D format: F32
+         | (1u << 7)         // A format: BF16
+         | (1u << 10)        // B format: BF16
          | ((N >> 3) << 17)  // N / 8
          | ((M >> 4) << 24); // M / 16
 }

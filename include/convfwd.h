@@ -148,6 +148,24 @@ CONVFWD_API int conv_fwd_nd_channels_last(const float *x, const float *w, const 
                                           const int64_t *pad, const int64_t *dilation, int algo,
                                           conv_stream_t stream);
 
+/*
+ * BFloat16 tensors (the pages discuss BF16 tensor cores and keep fp32 for the
+ * 1e-4 tolerance; this is the lower-precision option):
+ *   x, w, bias, y hold bfloat16 bit patterns (uint16_t), same shapes and
+ *   layout as conv_fwd_nd_grouped (contiguous N C spatial).
+ * The products and their sum are formed in fp32 on the tensor cores (one
+ * kind::f16 MMA per 16 reduction columns, no operand split); the bias is
+ * added in fp32 and y is rounded once to bfloat16 (nearest even).  Hence
+ * |y - exact| <= 2^-9 |exact| + (fp32 accumulation error) for every element.
+ * Runs on the tensor-core family only: C_out/groups <= 128 and the weights
+ * of one group (C_out/groups x C_in/groups x prod(k) bf16) within shared
+ * memory, else CONV_ERR_UNSUPPORTED.  All pointers 2-byte aligned.
+ */
+CONVFWD_API int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim,
+                                 int64_t N, int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                                 const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                                 const int64_t *dilation, conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */

@@ -426,3 +426,61 @@ def test_channels_last_rejects_direct_family():
     with pytest.raises(cf.ConvError) as e:
         cf.conv_fwd_nd(x, w, None, 1, 0, 1, algo=cf.CONV_ALGO_DIRECT_FFMA, channels_last=True)
     assert e.value.status == cf.CONV_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ bf16
+
+def bf16_inputs(x, w, b):
+    """The bfloat16 tensors (CUDA) and their exact values as float32 arrays for the oracle."""
+    xt, wt = torch.from_numpy(x).to(torch.bfloat16), torch.from_numpy(w).to(torch.bfloat16)
+    bt = None if b is None else torch.from_numpy(b).to(torch.bfloat16)
+    back = lambda t: None if t is None else t.float().numpy()
+    return (xt.cuda(), wt.cuda(), None if bt is None else bt.cuda()), (back(xt), back(wt), back(bt))
+
+
+def assert_bf16_close(y, ref, S, K, what):
+    """y rounded once to bf16 from an fp32 sum: |y - ref| <= 2^-8 |ref| + K 2^-23 S, with S the sum of
+    |w||x| (+|b|) per output (half an ulp of bf16 at the output, doubled, plus an fp32 summation bound)."""
+    y = y.float().cpu().numpy().astype(np.float64)
+    tol = 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -23 * S
+    err = np.abs(y - ref)
+    assert (err <= tol).all(), f"{what}: max excess {(err - tol).max():.3e}, max err {err.max():.3e}"
+
+
+@pytest.mark.parametrize("nd,groups,C_in,C_out,k,s,p,d", [
+    (1, 1, 64, 128, (3,), (3,), (0,), (4,)),
+    (2, 2, 24, 48, (3, 3), (1, 2), (1, 1), (1, 1)),
+    (3, 1, 3, 64, (3, 5, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1)),
+    (3, 1, 8, 32, (3, 5, 7), (1, 2, 2), (1, 2, 3), (2, 1, 1)),
+    (3, 1, 32, 40, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1)),
+])
+def test_bf16_conv(nd, groups, C_in, C_out, k, s, p, d):
+    rng = np.random.default_rng(C_in + C_out * 3 + nd)
+    ins = {1: (517,), 2: (15, 22), 3: (9, 14, 16)}[nd]
+    x = rng.random((2, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in // groups) + k) - 0.5) * 0.2).astype(np.float32)
+    b = ((rng.random(C_out) - 0.5) * 0.2).astype(np.float32)
+    (xt, wt, bt), (xf, wf, bf) = bf16_inputs(x, w, b)
+    y = cf.conv_fwd_nd(xt, wt, bt, s, p, d, groups=groups)
+    torch.cuda.synchronize()
+    assert y.dtype == torch.bfloat16
+    ref = oracle.conv_nd(xf, wf, bf, s, p, d, groups=groups)
+    S = oracle.conv_nd(np.abs(xf), np.abs(wf), np.abs(bf), s, p, d, groups=groups)
+    K = (C_in // groups) * int(np.prod(k))
+    assert_bf16_close(y, ref, S, K, f"bf16 nd={nd} C_in={C_in} C_out={C_out}")
+
+
+def test_bf16_exact_on_small_integers():
+    # integer inputs and weights: every product and partial sum is exact in
+    # fp32 and every output is an integer below 256, exactly representable in
+    # bf16; any mistake in the operand packing or the descriptors shows as a
+    # mismatch
+    rng = np.random.default_rng(5)
+    x = rng.integers(0, 3, (2, 4, 6, 9, 11)).astype(np.float32)
+    w = rng.integers(-1, 2, (20, 4, 2, 3, 3)).astype(np.float32)
+    b = rng.integers(-2, 3, 20).astype(np.float32)
+    (xt, wt, bt), (xf, wf, bf) = bf16_inputs(x, w, b)
+    y = cf.conv_fwd_nd(xt, wt, bt, 1, (0, 1, 1), 1).float().cpu().numpy()
+    ref = oracle.conv_nd(xf, wf, bf, (1, 1, 1), (0, 1, 1), (1, 1, 1))
+    assert np.abs(ref).max() < 256
+    assert np.array_equal(y, ref)
