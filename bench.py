@@ -268,16 +268,23 @@ def roofline_for(runner, peaks, ms, sustained=False):
         compute = {"bound": "alu", "peak": peak, "peak_note": "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"}
     t_compute = flops / (compute["peak"] * 1e12)
     t_mem = bytes_alg / (hbm_peak * 1e9)
+    # the fraction against the faster of the two fp32-accurate pipes, whichever
+    # the kernel uses, so that the choice of path cannot flatter the number
+    ffma_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12
+    tf32x3_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"] * BF16_TO_TF32 / 3.0
+    best = max(ffma_peak, tf32x3_peak)
+    t_best = max(flops / (best * 1e12), t_mem)
+    frac_best = t_best / t
     if t_mem > t_compute:
         return {"bound": "hbm", "achieved": bytes_alg / t / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "frac": (bytes_alg / t / 1e9) / hbm_peak, "traffic": traffic_for(runner.algo, wl),
                 "algorithmic_bytes": bytes_alg,
-                "compute_frac": (flops / t / 1e12) / compute["peak"]}
+                "compute_frac": (flops / t / 1e12) / compute["peak"], "frac_best_path": frac_best}
     ach = flops / t / 1e12
     return {"bound": compute["bound"], "achieved": ach, "peak": compute["peak"], "unit": "TFLOP/s",
             "frac": ach / compute["peak"], "traffic": traffic_for(runner.algo, wl), "algorithmic_bytes": bytes_alg,
             "peak_note": compute["peak_note"],
-            "hbm_frac": (bytes_alg / t / 1e9) / hbm_peak}
+            "hbm_frac": (bytes_alg / t / 1e9) / hbm_peak, "frac_best_path": frac_best}
 
 
 # ----------------------------------------------------------- oracle legs
@@ -415,7 +422,8 @@ def main():
             rf = roofline_for(r, peaks, m)
             per_config[name] = {"algo": r.algo, "ms": m, "ms_min": min(times), "gflops": f / (m * 1e-3) / 1e9,
                                 "gbs": bts / (m * 1e-3) / 1e9, "roofline_bound": rf["bound"],
-                                "roofline_frac": rf["frac"], "roofline_peak": rf["peak"], "unit": rf["unit"]}
+                                "roofline_frac": rf["frac"], "roofline_peak": rf["peak"], "unit": rf["unit"],
+                                "roofline_frac_best_path": rf["frac_best_path"]}
             del r
             torch.cuda.empty_cache()
 
