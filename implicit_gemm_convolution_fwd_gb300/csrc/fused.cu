@@ -229,7 +229,14 @@ struct StagedParams {
   const float *__restrict__ bias;
   float *__restrict__ y;
   Geom g;
-  int64_t rows;          // N * OH
+  int64_t rows;          // N * OA
+  // axis roles as in FusedParams, with the column axis always W: (R, A) =
+  // (D, H) for the min over depth, (H, D) for the min over height
+  int OR, OA;            // output extents along R and A
+  int KR, KA;            // kernel extents along R and A
+  int IR;                // input extent along R (planes)
+  int64_t sR, sA;        // input strides along R and A
+  int wR, wA;            // weight offsets per step along R and A
   int WP;                // shared-memory row pitch (floats): W rounded up to 4, plus 4
   int srows_max;         // shared-memory rows per channel per plane
   int ring;              // planes in the ring (KD + 2 * nb - 1)
@@ -275,9 +282,11 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
   }
 }
 
-// CT, KDT, KHT, WPT, SRT: compile-time C_in, KD, KH, shared row pitch and
-// shared rows per channel (0 = runtime); the benchmark shape is specialised
-// so that every shared-memory offset in the FMA loop is an immediate.
+// CT, KDT, KHT, WPT, SRT: compile-time C_in, KR, KA (the kernel extents along
+// the reduced and row axes: KD, KH for the min over depth), shared row pitch
+// and shared rows per channel (0 = runtime); the benchmark shape is
+// specialised so that every shared-memory offset in the FMA loop is an
+// immediate.  Names below follow the min over depth (planes = depth).
 template <int CT, int KDT, int KHT, int WPT, int SRT>
 __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(const StagedParams p) {
   constexpr int NOWG = 8;
@@ -289,7 +298,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 
   const Geom &g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int C = CT ? CT : (int)g.C, KD = KDT ? KDT : g.KD, KH = KHT ? KHT : g.KH;
+  const int C = CT ? CT : (int)g.C, KD = KDT ? KDT : p.KR, KH = KHT ? KHT : p.KA;
   const int WP = WPT ? WPT : p.WP, SR = SRT ? SRT : p.srows_max;
   const int taps = KD * KH * 3;
   const int64_t HW = (int64_t)g.H * g.W;
@@ -303,7 +312,11 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       const int cgi = rem / kSWStride, jj = rem - cgi * kSWStride;
       float v = 0.f;
       const int kw = jj / kSWTap, o = jj - kw * kSWTap, oc = cgi * kSCO + o;
-      if (o < kSCO && oc < g.K) v = p.w[(int64_t)oc * C * taps + row * 3 + kw];
+      if (o < kSCO && oc < g.K) {
+        const int c = row / (KD * KH), rem2 = row - c * KD * KH;
+        const int kr = rem2 / KH, ka = rem2 - kr * KH;
+        v = p.w[(int64_t)oc * C * taps + c * taps + kr * p.wR + ka * p.wA + kw];
+      }
       ws[i] = v;
     }
     if (tid < kSNcg * kSCO) bias_s[tid] = (p.bias && tid < g.K) ? __ldg(p.bias + tid) : 0.f;
@@ -322,20 +335,20 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 
   for (int64_t r0 = r_begin; r0 < r_end; r0 += kSRows) {
     const int nrows = (int)min64(kSRows, r_end - r0);
-    const int64_t n0 = r0 / g.OH;
+    const int64_t n0 = r0 / p.OA;
     __syncthreads();  // the previous block's readers are done with the ring and the row table
     // Shared rows: per image the block touches, its output rows plus KH - 1
     // halo rows.  Thread s fills entry s by walking the (at most a few)
     // image segments of the block.
-    const int oh_lo0 = (int)(r0 - n0 * g.OH);
+    const int oh_lo0 = (int)(r0 - n0 * p.OA);
     if (tid < kSMaxSrows) {
       int start = 0, rem = nrows, lo = oh_lo0;
       int64_t n = n0;
       while (rem > 0) {
-        const int cnt = min(rem, g.OH - lo);
-        const int len = cnt + g.KH - 1;
+        const int cnt = min(rem, p.OA - lo);
+        const int len = cnt + KH - 1;
         if (tid < start + len) {
-          srow_src[tid] = n * g.C * g.D * HW + (int64_t)(lo + tid - start) * g.W;
+          srow_src[tid] = n * g.C * g.D * HW + (int64_t)(lo + tid - start) * p.sA;
           break;
         }
         start += len;
@@ -346,8 +359,8 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       if (tid == 0) {
         int total = 0;
         for (int rr = nrows, l = oh_lo0; rr > 0; l = 0) {
-          const int cnt = min(rr, g.OH - l);
-          total += cnt + g.KH - 1;
+          const int cnt = min(rr, p.OA - l);
+          total += cnt + KH - 1;
           rr -= cnt;
         }
         nsrows_s = total;
@@ -370,7 +383,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     auto issue_plane = [&](int dd) {
       const uint32_t slot = ring_addr + 4u * (uint32_t)slot_of_next * p.slot_floats;
       slot_of_next = (slot_of_next + 1 == p.ring) ? 0 : slot_of_next + 1;
-      const int64_t dd_off = (int64_t)dd * HW;
+      const int64_t dd_off = (int64_t)dd * p.sR;
       if (sq0 < per_plane_sq) {
         const float *src = p.x + src0 + dd_off;
         uint32_t dst = slot + dst0;
@@ -397,7 +410,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     };
     // the first group's planes: 0 .. nb + KD - 2, one commit group per plane
     int issued = 0;  // commit groups issued in this block (one per plane)
-    for (int dd = 0; dd < p.nb + KD - 1 && dd < g.D; ++dd, ++issued) issue_plane(dd);
+    for (int dd = 0; dd < p.nb + KD - 1 && dd < p.IR; ++dd, ++issued) issue_plane(dd);
     if (!weights_staged) {
       stage_weights();
       weights_staged = true;
@@ -408,9 +421,9 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     const bool row_ok = lr < nrows;
     const int lrc = row_ok ? lr : nrows - 1;
     const int64_t rabs = r0 + lrc;
-    const int64_t n = rabs / g.OH;
-    const int oh = (int)(rabs - n * g.OH);
-    const int my_srow = lrc + (g.KH - 1) * (int)(n - n0);
+    const int64_t n = rabs / p.OA;
+    const int oh = (int)(rabs - n * p.OA);
+    const int my_srow = lrc + (KH - 1) * (int)(n - n0);
 
     float mins[kSCO][kR];
 #pragma unroll
@@ -419,19 +432,19 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       for (int r = 0; r < kR; ++r) mins[o][r] = INFINITY;
 
     int s_od = 0;  // ring slot of plane od
-    for (int od = 0; od < g.OD; ++od) {
+    for (int od = 0; od < p.OR; ++od) {
       if ((od % p.nb) == 0 && od > 0) {
         cp_async_wait_all();
         __syncthreads();  // this group's planes are in; the previous group's slots are free
-        for (int dd = od + p.nb + KD - 1; dd < od + 2 * p.nb + KD - 1 && dd < g.D; ++dd) issue_plane(dd);
+        for (int dd = od + p.nb + KD - 1; dd < od + 2 * p.nb + KD - 1 && dd < p.IR; ++dd) issue_plane(dd);
       } else if (od == 0) {
         // first group: depth 0 starts as soon as its KD planes are in ...
         cp_async_wait_pending(issued - KD);
         __syncthreads();
-        for (int dd = p.nb + KD - 1; dd < 2 * p.nb + KD - 1 && dd < g.D; ++dd, ++issued) issue_plane(dd);
+        for (int dd = p.nb + KD - 1; dd < 2 * p.nb + KD - 1 && dd < p.IR; ++dd, ++issued) issue_plane(dd);
       } else if (od == 1) {
         // ... and depth 1 waits for the rest of the group's planes
-        cp_async_wait_pending(issued - (int)min64(p.nb + KD - 1, g.D));
+        cp_async_wait_pending(issued - (int)min64(p.nb + KD - 1, p.IR));
         __syncthreads();
       }
       // acc2[op][r]: channels (2*op, 2*op + 1) at column r, packed
@@ -493,7 +506,7 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     }
 
     // channel softmax per column across the 4 channel-group lanes (xor 8, 16)
-    const int64_t OHW = (int64_t)g.OH * g.OW;
+    const int64_t OHW = (int64_t)p.OA * g.OW;
 #pragma unroll
     for (int r = 0; r < kR; ++r) {
       float v[kSCO];
@@ -531,19 +544,20 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 
 // Shared-memory plan of the staged variant; false when it does not apply.
 bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
+  // sp's axis fields (OR, OA, KR, KA, IR, sR, sA, wR, wA) are filled by the caller
   if (g.K > kSNcg * kSCO || g.OW > 32 || g.KW != 3) return false;
-  const int64_t seg = (kSRows - 1) / g.OH + 2;  // images a block of kSRows rows can touch
-  const int64_t srows64 = kSRows + (int64_t)(g.KH - 1) * seg;
+  const int64_t seg = (kSRows - 1) / sp->OA + 2;  // images a block of kSRows rows can touch
+  const int64_t srows64 = kSRows + (int64_t)(sp->KA - 1) * seg;
   if (srows64 > kSMaxSrows) return false;
   const int srows = (int)srows64;
   const int WP = (g.W + 3) / 4 * 4 + 4;
-  const int64_t w_floats = (int64_t)g.C * g.KD * g.KH * kSWRow;
+  const int64_t w_floats = (int64_t)g.C * sp->KR * sp->KA * kSWRow;
   const int64_t slot = (int64_t)g.C * srows * WP;
   // output depths per block-wide barrier: the largest of 4, 2, 1 whose ring
   // (KD + 2 * nb - 1 planes) fits (6 measured no faster than 4)
   int nb = 0, ring = 0;
   for (const int cand : {4, 2, 1}) {
-    ring = g.KD + 2 * cand - 1;
+    ring = sp->KR + 2 * cand - 1;
     const int64_t bytes = 4 * ((w_floats + 3) / 4 * 4 + ring * slot + kRingSlackFloats);
     if (bytes <= kMaxSmemBytes) {
       nb = cand;
@@ -646,7 +660,11 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
   }
   p.rows = g.N * (int64_t)p.OA;
   StagedParams sp;
-  if (min_dim == 2 && staged_plan(g, x, &sp)) {
+  // the staged kernel keeps W as its column axis: the min over depth or height
+  sp.OR = p.OR, sp.OA = p.OA, sp.KR = p.KR, sp.KA = p.KA;
+  sp.IR = (min_dim == 2) ? g.D : g.H;
+  sp.sR = p.sR, sp.sA = p.sA, sp.wR = p.wR, sp.wA = p.wA;
+  if (min_dim != 4 && staged_plan(g, x, &sp)) {
     sp.x = x;
     sp.w = w;
     sp.bias = bias;
@@ -658,9 +676,12 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const size_t smem = 4 * ((size_t)sp.w_floats + (size_t)sp.ring * sp.slot_floats + kRingSlackFloats);
-    // the benchmark shape (C_in 3, kernel 3^3, W 32 -> pitch 36, 30 shared rows) is specialised
-    const bool spec = g.C == 3 && g.KD == 3 && g.KH == 3 && sp.WP == 36 && sp.srows_max == 30;
-    auto kern = spec ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30> : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0>;
+    // the benchmark shape (C_in 3, kernel 3^3, W 32 -> pitch 36) is specialised: 30 shared
+    // rows for the min over depth (blocks span <= 2 images of 30 rows), 32 over height (22)
+    const bool spec3 = g.C == 3 && sp.KR == 3 && sp.KA == 3 && sp.WP == 36;
+    auto kern = (spec3 && sp.srows_max == 30)   ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30>
+                : (spec3 && sp.srows_max == 32) ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 32>
+                                                : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // every SM gets a contiguous share of the rows (processed 26 at a time)
