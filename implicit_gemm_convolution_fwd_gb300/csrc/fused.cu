@@ -287,7 +287,9 @@ __device__ __forceinline__ void cp_async_wait_pending(int n) {
 // and shared rows per channel (0 = runtime); the benchmark shape is
 // specialised so that every shared-memory offset in the FMA loop is an
 // immediate.  Names below follow the min over depth (planes = depth).
-template <int CT, int KDT, int KHT, int WPT, int SRT>
+// SKIP: warps without a row of the block skip the FMA work (worth it when the
+// CTAs' row shares are well below the warp count; it costs a few registers).
+template <int CT, int KDT, int KHT, int WPT, int SRT, bool SKIP>
 __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(const StagedParams p) {
   constexpr int NOWG = 8;
   extern __shared__ __align__(16) float sm[];
@@ -447,62 +449,66 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
         cp_async_wait_pending(issued - (int)min64(p.nb + KD - 1, p.IR));
         __syncthreads();
       }
-      // acc2[op][r]: channels (2*op, 2*op + 1) at column r, packed
-      unsigned long long acc2[kSCO / 2][kR];
+      // with SKIP, a warp without a row of this block (the CTA's share is
+      // smaller than its warp count) only takes part in the copies and barriers
+      if (!SKIP || row_ok) {
+        // acc2[op][r]: channels (2*op, 2*op + 1) at column r, packed
+        unsigned long long acc2[kSCO / 2][kR];
 #pragma unroll
-      for (int op = 0; op < kSCO / 2; ++op)
+        for (int op = 0; op < kSCO / 2; ++op)
 #pragma unroll
-        for (int r = 0; r < kR; ++r) acc2[op][r] = 0ull;
-      const float *xlane = ring + (size_t)my_srow * WP + ow0;
-      const float *wlane = ws + cg * kSWStride;
+          for (int r = 0; r < kR; ++r) acc2[op][r] = 0ull;
+        const float *xlane = ring + (size_t)my_srow * WP + ow0;
+        const float *wlane = ws + cg * kSWStride;
 #pragma unroll
-      for (int kd = 0; kd < (KDT ? KDT : 1); ++kd) {
-        for (int kdr = KDT ? kd : 0; kdr < (KDT ? kd + 1 : KD); ++kdr) {
-          int slot = s_od + kdr;
-          if (slot >= p.ring) slot -= p.ring;
-          const float *xplane = xlane + (size_t)slot * p.slot_floats;
+        for (int kd = 0; kd < (KDT ? KDT : 1); ++kd) {
+          for (int kdr = KDT ? kd : 0; kdr < (KDT ? kd + 1 : KD); ++kdr) {
+            int slot = s_od + kdr;
+            if (slot >= p.ring) slot -= p.ring;
+            const float *xplane = xlane + (size_t)slot * p.slot_floats;
 #pragma unroll
-          for (int c = 0; c < (CT ? CT : 1); ++c) {
-            for (int cr = CT ? c : 0; cr < (CT ? c + 1 : C); ++cr) {
-              const float *xc = xplane + cr * SR * WP;
-              const float *wc = wlane + ((cr * KD + kdr) * KH) * kSWRow;
+            for (int c = 0; c < (CT ? CT : 1); ++c) {
+              for (int cr = CT ? c : 0; cr < (CT ? c + 1 : C); ++cr) {
+                const float *xc = xplane + cr * SR * WP;
+                const float *wc = wlane + ((cr * KD + kdr) * KH) * kSWRow;
 #pragma unroll
-              for (int kh = 0; kh < (KHT ? KHT : 1); ++kh) {
-                for (int khr = KHT ? kh : 0; khr < (KHT ? kh + 1 : KH); ++khr) {
-                  const float *xr = xc + khr * WP;
-                  const float4 a = *reinterpret_cast<const float4 *>(xr);
-                  const float2 b2 = *reinterpret_cast<const float2 *>(xr + 4);
-                  // each input value duplicated into both halves of a pair
-                  const unsigned long long xx[6] = {pack2(a.x, a.x), pack2(a.y, a.y), pack2(a.z, a.z),
-                                                    pack2(a.w, a.w), pack2(b2.x, b2.x), pack2(b2.y, b2.y)};
-                  const float *wt = wc + khr * kSWRow;
+                for (int kh = 0; kh < (KHT ? KHT : 1); ++kh) {
+                  for (int khr = KHT ? kh : 0; khr < (KHT ? kh + 1 : KH); ++khr) {
+                    const float *xr = xc + khr * WP;
+                    const float4 a = *reinterpret_cast<const float4 *>(xr);
+                    const float2 b2 = *reinterpret_cast<const float2 *>(xr + 4);
+                    // each input value duplicated into both halves of a pair
+                    const unsigned long long xx[6] = {pack2(a.x, a.x), pack2(a.y, a.y), pack2(a.z, a.z),
+                                                      pack2(a.w, a.w), pack2(b2.x, b2.x), pack2(b2.y, b2.y)};
+                    const float *wt = wc + khr * kSWRow;
 #pragma unroll
-                  for (int kw = 0; kw < 3; ++kw) {
-                    // the tap's 6 channel weights are 3 aligned pairs in shared memory
-                    const ulonglong2 q0 = *reinterpret_cast<const ulonglong2 *>(wt + kw * kSWTap);
-                    const unsigned long long q1 = *reinterpret_cast<const unsigned long long *>(wt + kw * kSWTap + 4);
-                    const unsigned long long wp[kSCO / 2] = {q0.x, q0.y, q1};
+                    for (int kw = 0; kw < 3; ++kw) {
+                      // the tap's 6 channel weights are 3 aligned pairs in shared memory
+                      const ulonglong2 q0 = *reinterpret_cast<const ulonglong2 *>(wt + kw * kSWTap);
+                      const unsigned long long q1 = *reinterpret_cast<const unsigned long long *>(wt + kw * kSWTap + 4);
+                      const unsigned long long wp[kSCO / 2] = {q0.x, q0.y, q1};
 #pragma unroll
-                    for (int op = 0; op < kSCO / 2; ++op)
+                      for (int op = 0; op < kSCO / 2; ++op)
 #pragma unroll
-                      for (int r = 0; r < kR; ++r) fma2(acc2[op][r], wp[op], xx[r + kw]);
+                        for (int r = 0; r < kR; ++r) fma2(acc2[op][r], wp[op], xx[r + kw]);
+                    }
                   }
                 }
               }
             }
           }
         }
+#pragma unroll
+        for (int op = 0; op < kSCO / 2; ++op)
+#pragma unroll
+          for (int r = 0; r < kR; ++r) {
+            float c0, c1;
+            unpack2(acc2[op][r], c0, c1);
+            mins[2 * op][r] = fminf(mins[2 * op][r], c0);
+            mins[2 * op + 1][r] = fminf(mins[2 * op + 1][r], c1);
+          }
       }
       s_od = (s_od + 1 == p.ring) ? 0 : s_od + 1;
-#pragma unroll
-      for (int op = 0; op < kSCO / 2; ++op)
-#pragma unroll
-        for (int r = 0; r < kR; ++r) {
-          float c0, c1;
-          unpack2(acc2[op][r], c0, c1);
-          mins[2 * op][r] = fminf(mins[2 * op][r], c0);
-          mins[2 * op + 1][r] = fminf(mins[2 * op + 1][r], c1);
-        }
     }
 
     // channel softmax per column across the 4 channel-group lanes (xor 8, 16)
@@ -679,9 +685,9 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     // the benchmark shape (C_in 3, kernel 3^3, W 32 -> pitch 36) is specialised: 30 shared
     // rows for the min over depth (blocks span <= 2 images of 30 rows), 32 over height (22)
     const bool spec3 = g.C == 3 && sp.KR == 3 && sp.KA == 3 && sp.WP == 36;
-    auto kern = (spec3 && sp.srows_max == 30)   ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30>
-                : (spec3 && sp.srows_max == 32) ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 32>
-                                                : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0>;
+    auto kern = (spec3 && sp.srows_max == 30)   ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 30, false>
+                : (spec3 && sp.srows_max == 32) ? fused_min_softmax_staged_kernel<3, 3, 3, 36, 32, true>
+                                                : fused_min_softmax_staged_kernel<0, 0, 0, 0, 0, true>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     // every SM gets a contiguous share of the rows (processed 26 at a time)
