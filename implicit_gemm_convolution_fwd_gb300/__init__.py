@@ -19,7 +19,7 @@ ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV
 
 # every symbol include/convfwd.h declares
 EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_fwd_nd_channels_last",
-            "conv_fwd_nd_bf16",
+            "conv_fwd_nd_bf16", "conv_fwd_nd_f16",
             "conv_select_algo",
             "conv_algo_supported",
             "conv3d_min_softmax",
@@ -61,6 +61,7 @@ def load(path: str | None = None):
     lib.conv_fwd_nd_channels_last.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, i32,
                                               vp]
     lib.conv_fwd_nd_bf16.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp]
+    lib.conv_fwd_nd_f16.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp]
     lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
@@ -146,20 +147,21 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     Default layout: contiguous (N C D H W).  channels_last=True: x, w (and out) keep their logical
     shapes but are stored channels last (torch.channels_last / channels_last_3d, i.e. N D H W C);
     the returned y is allocated the same way.
-    bfloat16 x, w (and bias): the BF16 tensor-core path, fp32 accumulation, bfloat16 y (contiguous
-    layout only; `algo` must be AUTO)."""
+    bfloat16 or float16 x, w (and bias): the 16-bit tensor-core path, fp32 accumulation, y in the
+    input dtype (contiguous layout only; `algo` must be AUTO)."""
     import torch
     nd = x.dim() - 2
     if nd not in (1, 2, 3) or w.dim() != x.dim():
         raise ValueError("x and w must be 3-D, 4-D or 5-D tensors of the same rank")
     dt = x.dtype
-    if dt not in (torch.float32, torch.bfloat16):
-        raise ValueError("tensors must be float32 or bfloat16")
+    half = (torch.bfloat16, torch.float16)
+    if dt not in (torch.float32,) + half:
+        raise ValueError("tensors must be float32, bfloat16 or float16")
     for t in (x, w) + ((bias,) if bias is not None else ()):
         if not (t.is_cuda and t.dtype == dt):
-            raise ValueError("x, w and bias must be CUDA tensors of one dtype (float32 or bfloat16)")
-    if dt == torch.bfloat16 and (channels_last or algo != CONV_ALGO_AUTO):
-        raise ValueError("bfloat16 tensors take the contiguous layout and algo=AUTO")
+            raise ValueError("x, w and bias must be CUDA tensors of one dtype")
+    if dt in half and (channels_last or algo != CONV_ALGO_AUTO):
+        raise ValueError("16-bit tensors take the contiguous layout and algo=AUTO")
     if bias is not None and not bias.is_contiguous():
         raise ValueError("bias must be contiguous")
     if channels_last:
@@ -174,8 +176,8 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
         raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
     od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
     if out is None:
-        if dt == torch.bfloat16:
-            out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.bfloat16)
+        if dt in half:
+            out = torch.empty((N, C_out) + od, device=x.device, dtype=dt)
         elif channels_last:
             out = torch.empty((N,) + od + (C_out,), device=x.device, dtype=torch.float32).permute(0, nd + 1,
                                                                                               *range(1, nd + 1))
@@ -189,9 +191,10 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     lib = load()
     b = None if bias is None else bias.data_ptr()
     dims = (_arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d))
-    if dt == torch.bfloat16:
-        st = lib.conv_fwd_nd_bf16(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups),
-                                  *dims, _stream_handle(stream))
+    if dt in half:
+        fn = lib.conv_fwd_nd_bf16 if dt == torch.bfloat16 else lib.conv_fwd_nd_f16
+        st = fn(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups), *dims,
+                _stream_handle(stream))
     else:
         fn = lib.conv_fwd_nd_channels_last if channels_last else lib.conv_fwd_nd_grouped
         st = fn(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups), *dims, int(algo),

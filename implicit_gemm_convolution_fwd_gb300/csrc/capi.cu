@@ -260,9 +260,11 @@ int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias,
   return CONV_OK;
 }
 
-int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim, int64_t N,
-                     int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
-                     const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream) {
+// 16-bit tensors (bfloat16 or float16 bit patterns) on the tensor cores.
+static int conv_fwd_16bit(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim, int64_t N,
+                          int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                          const int64_t *stride, const int64_t *pad, const int64_t *dilation, bool fp16,
+                          conv_stream_t stream, const char *name) {
   g_last_error[0] = 0;
   Geom g;
   int st = validate_conv((const float *)x, (const float *)w, (const float *)bias, (const float *)y, ndim, N, C_in,
@@ -270,15 +272,31 @@ int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias,
   if (st != CONV_OK) return st;
   const char *why = "";
   if (!convfwd::igemm_bf16_supported(g, &why))
-    return fail(CONV_ERR_UNSUPPORTED, "conv_fwd_nd_bf16: the tensor-core path cannot run this shape: %s", why);
+    return fail(CONV_ERR_UNSUPPORTED, fp16 ? "conv_fwd_nd_f16: the tensor-core path cannot run this shape: %s"
+                                           : "conv_fwd_nd_bf16: the tensor-core path cannot run this shape: %s",
+                why);
   if (g.N == 0) return CONV_OK;
   const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
   cudaError_t e = cudaSuccess;
   for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
     e = convfwd::launch_igemm_bf16(x + grp * xg, w + grp * wg, bias ? bias + grp * g.K : nullptr, y + grp * yg, g,
-                                   (cudaStream_t)stream);
-  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_bf16: kernel launch");
+                                   fp16, (cudaStream_t)stream);
+  if (e != cudaSuccess) return fail_cuda(e, name);
   return CONV_OK;
+}
+
+int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim, int64_t N,
+                     int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                     const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream) {
+  return conv_fwd_16bit(x, w, bias, y, ndim, N, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation, false,
+                        stream, "conv_fwd_nd_bf16");
+}
+
+int conv_fwd_nd_f16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim, int64_t N,
+                    int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                    const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream) {
+  return conv_fwd_16bit(x, w, bias, y, ndim, N, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation, true,
+                        stream, "conv_fwd_nd_f16");
 }
 
 int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,

@@ -46,10 +46,11 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
 // kernel extent along the output's last axis, shared-memory footprint).
 bool fused_supported(const Geom &g, int min_dim, const char **why);
 
-// Tensor-core implicit GEMM on bfloat16 tensors (bit patterns), fp32 accumulation, bf16 output.
+// Tensor-core implicit GEMM on 16-bit tensors (bfloat16, or float16 when fp16; bit patterns),
+// fp32 accumulation, output in the input type.
 bool igemm_bf16_supported(const Geom &g, const char **why);
 cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, const Geom &g,
-                              cudaStream_t stream);
+                              bool fp16, cudaStream_t stream);
 
 // Tensor-core implicit GEMM (tcgen05, 3xTF32).
 bool igemm_supported(const Geom &g, const char **why);

@@ -1,6 +1,7 @@
-// BF16 variant of the implicit-GEMM kernel: x, w and bias in bfloat16, the
-// products and their sum in fp32 (tensor-core accumulator), y rounded once to
-// bfloat16 (round to nearest even) at the store.  The conv sum is the one in
+// 16-bit variant of the implicit-GEMM kernel: x, w and bias in bfloat16 (or
+// float16, template HALF), the products and their sum in fp32 (tensor-core
+// accumulator), y rounded once to the input type (round to nearest even) at
+// the store.  The conv sum is the one in
 // the l1_p60 page (turn 1); the pages weigh BF16 against fp32 accuracy and
 // keep fp32, so this path is the lower-precision option next to 3xTF32.
 //
@@ -100,6 +101,17 @@ __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+template <bool HALF>
+__device__ __forceinline__ float bits16_to_float(unsigned short b) {
+  return HALF ? __half2float(__ushort_as_half(b)) : bf16_bits_to_float(b);
+}
+template <bool HALF>
+__device__ __forceinline__ unsigned short float_to_bits16(float f) {
+  return HALF ? __half_as_ushort(__float2half_rn(f)) : __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+
+// HALF = false: bfloat16 tensors; true: float16 tensors (A and B always of one type).
+template <bool HALF>
 __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -168,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
       }
     }
     for (int i = tid; i < p.Npad; i += kThreads)
-      bias_s[i] = (p.bh && i < g.K) ? bf16_bits_to_float(__ldg(p.bh + i)) : 0.f;
+      bias_s[i] = (p.bh && i < g.K) ? bits16_to_float<HALF>(__ldg(p.bh + i)) : 0.f;
   }
   ptx::fence_proxy_async_smem();
   if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
@@ -223,8 +235,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
             if (c0 + j < g.K) {
-              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]) + bias_s[c0 + j]);
-              __stcs(reinterpret_cast<unsigned short *>(q), __bfloat16_as_ushort(h));
+              __stcs(reinterpret_cast<unsigned short *>(q),
+                     float_to_bits16<HALF>(__uint_as_float(v[j]) + bias_s[c0 + j]));
             }
             q += p.osp;
           }
@@ -273,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
   } else if (lane == 0 && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
     const int slot = warp - kMmaWarp;
-    const uint32_t idesc = ptx::idesc_bf16(kTileM, (uint32_t)p.Npad);
+    const uint32_t idesc = HALF ? ptx::idesc_f16(kTileM, (uint32_t)p.Npad) : ptx::idesc_bf16(kTileM, (uint32_t)p.Npad);
     const uint32_t bsa = ptx::smem_addr(b_s);
     const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
     const int64_t my_tiles = cta_tile_count(p);

@@ -32,6 +32,7 @@
 // wait is bounded: on timeout the kernel raises a flag, lets the other roles
 // fall through, drains its MMAs and frees TMEM.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -628,6 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 
 int g_num_sms[64] = {0};
 bool g_attr_bf16_set[64] = {false};
+bool g_attr_f16_set[64] = {false};
 bool g_attr_set[64] = {false};
 
 }  // namespace
@@ -690,7 +692,7 @@ bool igemm_bf16_supported(const Geom &g, const char **why) {
 }
 
 cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, const Geom &g,
-                              cudaStream_t stream) {
+                              bool fp16, cudaStream_t stream) {
   PlanBf16 pl;
   const char *why = "";
   if (!make_plan_bf16(g, &pl, &why)) return cudaErrorInvalidValue;
@@ -702,10 +704,12 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
     e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
   }
-  if (!g_attr_bf16_set[dev]) {
-    e = cudaFuncSetAttribute(igemm_bf16_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+  bool &attr_set = fp16 ? g_attr_f16_set[dev] : g_attr_bf16_set[dev];
+  if (!attr_set) {
+    e = cudaFuncSetAttribute(fp16 ? igemm_bf16_kernel<true> : igemm_bf16_kernel<false>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
-    g_attr_bf16_set[dev] = true;
+    attr_set = true;
   }
   IgemmParams p = {};
   p.xh = x;
@@ -725,7 +729,10 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
   p.tap_major = pl.tap_major;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 2);
   const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-  igemm_bf16_kernel<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  if (fp16)
+    igemm_bf16_kernel<true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  else
+    igemm_bf16_kernel<false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
 

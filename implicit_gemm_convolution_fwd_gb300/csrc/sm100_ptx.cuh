@@ -184,5 +184,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16(uint32_t M, uint32_t N) {
          | ((M >> 4) << 24); // M / 16
 }
 
+// Instruction descriptor for kind::f16 with FP16 A and B, fp32 accumulator,
+// both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(uint32_t M, uint32_t N) {
+  return (1u << 4)           // D format: F32
+         | (0u << 7)         // A format: F16
+         | (0u << 10)        // B format: F16
+         | ((N >> 3) << 17)  // N / 8
+         | ((M >> 4) << 24); // M / 16
+}
+
 }  // namespace ptx
 }  // namespace convfwd

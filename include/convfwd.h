@@ -166,6 +166,15 @@ CONVFWD_API int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uin
                                  const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
                                  const int64_t *dilation, conv_stream_t stream);
 
+/* The same for IEEE float16 tensors (x, w, bias, y hold float16 bit
+ * patterns): one rounding of the fp32 sum to float16 at the store, so
+ * |y - exact| <= 2^-11 |exact| + (fp32 accumulation error) while the result
+ * stays inside the float16 range. */
+CONVFWD_API int conv_fwd_nd_f16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim,
+                                int64_t N, int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                                const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                                const int64_t *dilation, conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */

@@ -430,19 +430,20 @@ def test_channels_last_rejects_direct_family():
 
 # ------------------------------------------------------------------ bf16
 
-def bf16_inputs(x, w, b):
-    """The bfloat16 tensors (CUDA) and their exact values as float32 arrays for the oracle."""
-    xt, wt = torch.from_numpy(x).to(torch.bfloat16), torch.from_numpy(w).to(torch.bfloat16)
-    bt = None if b is None else torch.from_numpy(b).to(torch.bfloat16)
+def bf16_inputs(x, w, b, dtype=torch.bfloat16):
+    """The 16-bit tensors (CUDA) and their exact values as float32 arrays for the oracle."""
+    xt, wt = torch.from_numpy(x).to(dtype), torch.from_numpy(w).to(dtype)
+    bt = None if b is None else torch.from_numpy(b).to(dtype)
     back = lambda t: None if t is None else t.float().numpy()
     return (xt.cuda(), wt.cuda(), None if bt is None else bt.cuda()), (back(xt), back(wt), back(bt))
 
 
-def assert_bf16_close(y, ref, S, K, what):
-    """y rounded once to bf16 from an fp32 sum: |y - ref| <= 2^-8 |ref| + K 2^-23 S, with S the sum of
-    |w||x| (+|b|) per output (half an ulp of bf16 at the output, doubled, plus an fp32 summation bound)."""
+def assert_bf16_close(y, ref, S, K, what, mant=8):
+    """y rounded once to a 16-bit type with `mant` fraction bits (bf16 7, fp16 10) from an fp32 sum:
+    |y - ref| <= 2^-mant |ref| + K 2^-23 S, with S the sum of |w||x| (+|b|) per output (half an ulp at
+    the output, doubled, plus an fp32 summation bound).  mant = 8 is the bf16 bound."""
     y = y.float().cpu().numpy().astype(np.float64)
-    tol = 2.0 ** -8 * np.abs(ref) + K * 2.0 ** -23 * S
+    tol = 2.0 ** -mant * np.abs(ref) + K * 2.0 ** -23 * S
     err = np.abs(y - ref)
     assert (err <= tol).all(), f"{what}: max excess {(err - tol).max():.3e}, max err {err.max():.3e}"
 
@@ -484,3 +485,37 @@ def test_bf16_exact_on_small_integers():
     ref = oracle.conv_nd(xf, wf, bf, (1, 1, 1), (0, 1, 1), (1, 1, 1))
     assert np.abs(ref).max() < 256
     assert np.array_equal(y, ref)
+
+
+@pytest.mark.parametrize("nd,groups,C_in,C_out,k,s,p,d", [
+    (1, 1, 64, 128, (3,), (3,), (0,), (4,)),
+    (3, 1, 3, 64, (3, 5, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1)),
+    (2, 3, 12, 48, (3, 2), (2, 1), (1, 0), (1, 2)),
+])
+def test_f16_conv(nd, groups, C_in, C_out, k, s, p, d):
+    rng = np.random.default_rng(C_in * 5 + C_out + nd)
+    ins = {1: (517,), 2: (15, 22), 3: (9, 14, 16)}[nd]
+    x = rng.random((2, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in // groups) + k) - 0.5) * 0.2).astype(np.float32)
+    b = ((rng.random(C_out) - 0.5) * 0.2).astype(np.float32)
+    (xt, wt, bt), (xf, wf, bf) = bf16_inputs(x, w, b, torch.float16)
+    y = cf.conv_fwd_nd(xt, wt, bt, s, p, d, groups=groups)
+    torch.cuda.synchronize()
+    assert y.dtype == torch.float16
+    ref = oracle.conv_nd(xf, wf, bf, s, p, d, groups=groups)
+    S = oracle.conv_nd(np.abs(xf), np.abs(wf), np.abs(bf), s, p, d, groups=groups)
+    K = (C_in // groups) * int(np.prod(k))
+    assert_bf16_close(y, ref, S, K, f"f16 nd={nd} C_in={C_in} C_out={C_out}", mant=10)
+
+
+def test_f16_exact_on_small_integers():
+    rng = np.random.default_rng(6)
+    x = rng.integers(0, 4, (2, 4, 6, 9, 11)).astype(np.float32)
+    w = rng.integers(-2, 3, (20, 4, 2, 3, 3)).astype(np.float32)
+    b = rng.integers(-3, 4, 20).astype(np.float32)
+    (xt, wt, bt), (xf, wf, bf) = bf16_inputs(x, w, b, torch.float16)
+    y = cf.conv_fwd_nd(xt, wt, bt, 1, (0, 1, 1), 1).float().cpu().numpy()
+    ref = oracle.conv_nd(xf, wf, bf, (1, 1, 1), (0, 1, 1), (1, 1, 1))
+    assert np.abs(ref).max() < 2048
+    assert np.array_equal(y, ref)
+
