@@ -217,6 +217,71 @@ class OurRunner:
         return s.elapsed_time(e) / steps, h2d, hy.numel() * 4
 
 
+class VariantRunner(OurRunner):
+    """A benchmark workload run through one of the library's other entry points:
+    16-bit tensors, the min over another dim, channels-last tensors or groups."""
+
+    def __init__(self, wl, device, dtype=None, min_dim=None, channels_last=False, groups=1):
+        super().__init__(wl, device)
+        torch = self.torch
+        self.dtype, self.channels_last, self.groups = dtype, channels_last, groups
+        self.min_dim = wl.min_dim if min_dim is None else min_dim
+        if groups > 1:
+            self.w = self.w[:, :wl.C_in // groups].contiguous()
+        if dtype is not None:
+            self.x, self.w = self.x.to(dtype), self.w.to(dtype)
+            self.b = None if self.b is None else self.b.to(dtype)
+            self.y = self.y.to(dtype)
+        if channels_last:
+            fmt = {3: torch.channels_last, 5: torch.channels_last_3d}[self.x.dim()]
+            self.x, self.w = self.x.to(memory_format=fmt), self.w.to(memory_format=fmt)
+            self.y = self.y.to(memory_format=fmt)
+        if wl.kind == "fused":
+            od = self.out_dims
+            keep = [od[i] for i in range(3) if i != self.min_dim - 2]
+            self.y = torch.empty((wl.N, wl.C_out, keep[0], keep[1]), device=device)
+
+    def step(self):
+        if self.wl.kind == "fused":
+            self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.min_dim, out=self.y, stream=self.stream)
+        else:
+            self.cf.conv_fwd_nd(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation, out=self.y,
+                                stream=self.stream, groups=self.groups, channels_last=self.channels_last)
+
+
+# (name, workload, options): the other entry points on the benchmark workloads
+VARIANTS = [
+    ("conv3d_asym[bf16]", "conv3d_asym", {"dtype": "bfloat16"}),
+    ("conv3d_asym[fp16]", "conv3d_asym", {"dtype": "float16"}),
+    ("conv1d_long[bf16]", "conv1d_long", {"dtype": "bfloat16"}),
+    ("conv3d_min_softmax[min_dim=3]", "conv3d_min_softmax", {"min_dim": 3}),
+    ("conv3d_min_softmax[min_dim=4]", "conv3d_min_softmax", {"min_dim": 4}),
+    ("conv3d_sweep_b[channels_last]", "conv3d_sweep_b", {"channels_last": True}),
+    ("conv3d_sweep_b[groups=2]", "conv3d_sweep_b", {"groups": 2}),
+]
+
+
+def run_variants(dev, peaks, steps):
+    """ms and throughput of each VARIANTS entry (CUDA events, L2 flushed, median)."""
+    import torch
+    out = {}
+    for name, wname, opts in VARIANTS:
+        o = dict(opts)
+        if "dtype" in o:
+            o["dtype"] = getattr(torch, o["dtype"])
+        r = VariantRunner(synth.WORKLOADS[wname], dev, **o)
+        times = r.timed(steps, 3)
+        m = statistics.median(times)
+        flops, _, _, _ = problem_counts(r.wl, r.out_dims)
+        flops /= r.groups  # each output channel sums over C_in / groups input channels
+        entry = {"ms": m, "ms_min": min(times), "tflops": flops / (m * 1e-3) / 1e12}
+        if r.dtype is not None:
+            entry["frac_of_measured_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
+        out[name] = entry
+        del r
+    return out
+
+
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch from one
 # ncu capture, keyed by (kernel family, workload).  Each entry records the
 # SHA-256 of the kernel's source file at capture time; when the source has
@@ -362,6 +427,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=HEADLINE, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-extra", action="store_true", help="skip the per-config table")
+    ap.add_argument("--no-variants", action="store_true", help="skip the other entry points' table")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small cases for profiler captures)")
@@ -426,6 +492,10 @@ def main():
                                 "roofline_frac_best_path": rf["frac_best_path"]}
             del r
             torch.cuda.empty_cache()
+    variants = {}
+    if not args.no_extra and not args.no_variants and rank == 0:
+        variants = run_variants(dev, peaks, max(5, args.steps // 4))
+        torch.cuda.empty_cache()
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -451,7 +521,7 @@ def main():
             "e2e": {"value": job_throughput(flops, e2e_ms, world), "unit": "GFLOP/s", "ms_per_step": e2e_ms,
                     "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
             "gpu_launches": runner.launches_per_step() * args.steps,
-            "roofline": roof, "clocks": clocks, "cpu_baseline": cpu, "per_config": per_config,
+            "roofline": roof, "clocks": clocks, "cpu_baseline": cpu, "per_config": per_config, "other_entry_points": variants,
         }
         print(json.dumps(line))
     if world > 1:

@@ -75,8 +75,12 @@ struct IgemmParams {
   int64_t M_total;  // N * OD * OH * OW
   int64_t osp;      // OD * OH * OW
   int64_t tiles;    // ceil(M_total / 128)
-  int Kred;         // reduction length of w: C_in * taps
-  int Kpad;         // padded reduction length in the GEMM (multiple of 32)
+  int Kred;         // reduction columns of this pass (all of C_in * taps when one pass holds them)
+  int Kfull;        // the whole reduction length C_in * taps (row length of w)
+  int k_begin;      // first reduction column of this pass
+  int accumulate;   // later passes add the accumulator to y instead of the bias
+  int64_t y_chans;  // channels per image of y (batch / position stride; all groups and blocks)
+  int Kpad;         // padded reduction length of this pass (multiple of 32)
   int Npad;         // C_out rounded up to 32
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
@@ -90,12 +94,17 @@ struct IgemmParams {
 
 struct Plan {
   int Kred, Kpad, Npad, KC, nchunks, nslots, tap_major;
-  size_t smem;
+  int kpass;    // reduction columns per pass (multiple of 32); Kred when one pass holds them all
+  int npasses;  // ceil(Kred / kpass)
+  size_t smem;  // shared memory of a full pass
 };
 
+// g.K is the output channels of one launch (<= 128; the host splits wider
+// layers into channel blocks).  A reduction whose weights (hi + lo) exceed
+// shared memory runs in passes of kpass columns, the later ones adding into y.
 bool make_plan(const Geom &g, Plan *pl, const char **why) {
   if (g.K > kMaxNpad) {
-    *why = "C_out above 128";
+    *why = "C_out above 128 in one launch";
     return false;
   }
   if (g.KD > 32 || g.KH > 32 || g.KW > 32) {
@@ -132,13 +141,19 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
   if (kc > kChunkMax) kc = kChunkMax;
   if (kc > pl->Kpad) kc = pl->Kpad;
   pl->KC = kc;
-  pl->nchunks = (pl->Kpad + kc - 1) / kc;
-  const size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 +
-                      kNumBars * 8 + 16;
-  if (smem > (size_t)kMaxSmem) {
-    *why = "weights (hi + lo) do not fit in shared memory";
+  // columns per pass: B hi + lo (8 * Npad bytes per column) and the two
+  // tables (8 bytes per column) beside the bias and the barriers
+  const size_t fixed = (size_t)pl->Npad * 4 + 16 + kNumBars * 8 + 16;
+  const int kmax = (int)((kMaxSmem - fixed) / ((size_t)8 * pl->Npad + 8)) / 32 * 32;
+  if (kmax < 32) {
+    *why = "no reduction pass fits in shared memory";
     return false;
   }
+  pl->kpass = pl->Kpad < kmax ? pl->Kpad : kmax;
+  pl->npasses = (pl->Kred + pl->kpass - 1) / pl->kpass;
+  if (pl->npasses > 1) pl->Kpad = pl->kpass;
+  pl->nchunks = (pl->Kpad + kc - 1) / kc;
+  const size_t smem = (size_t)2 * pl->Npad * pl->Kpad * 4 + (size_t)pl->Kpad * 8 + fixed;
   pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
   return true;
 }
@@ -299,7 +314,9 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
 }
 
 // CH: register buffer of one chunk (>= KC): 16 for four slots, 32 for two.
-template <int CH>
+// ACC: a later reduction pass (adds into y; instantiated separately so that
+// the single-pass kernels keep their registers).
+template <int CH, bool ACC>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -334,13 +351,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     for (int i = tid; i < words; i += kThreads) {
       const int cm = i >> 5, r = (i >> 2) & 7, cw = i & 3;
       const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
-      // w is [C_out][C_in][taps]; GEMM column k maps to (c, t) by the reduction order
-      int kmem = k;
+      // w is [C_out][C_in][taps]; GEMM column kg = k_begin + k maps to (c, t) by the reduction order
+      const int kg = p.k_begin + k;
+      int kmem = kg;
       if (p.tap_major && !g.cl && k < p.Kred) {
-        const int t = k / g.C;
-        kmem = (k - t * g.C) * taps + t;
+        const int t = kg / g.C;
+        kmem = (kg - t * g.C) * taps + t;
       }
-      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kred + kmem) : 0.f;
+      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kfull + kmem) : 0.f;
       const float hi = __uint_as_float(tf32_hi_bits(v));
       reinterpret_cast<float *>(b_hi)[i] = hi;
       reinterpret_cast<float *>(b_lo)[i] = v - hi;
@@ -348,13 +366,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     // ---- reduction column -> (input offset, tap coordinates)
     for (int kk = tid; kk < p.Kpad; kk += kThreads) {
       if (kk < p.Kred) {
+        const int kg = p.k_begin + kk;
         int c, t;
         if (p.tap_major) {
-          t = kk / g.C;
-          c = kk - t * g.C;
+          t = kg / g.C;
+          c = kg - t * g.C;
         } else {
-          c = kk / taps;
-          t = kk - c * taps;
+          c = kg / taps;
+          t = kg - c * taps;
         }
         const int kw = t % g.KW, khd = t / g.KW;
         const int kd = khd / g.KH, kh = khd - kd * g.KH;
@@ -366,7 +385,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         ttap[kk] = 0x80000000u;  // padding: contributes zero
       }
     }
-    for (int i = tid; i < p.Npad; i += kThreads) bias_s[i] = (p.bias && i < g.K) ? __ldg(p.bias + i) : 0.f;
+    for (int i = tid; i < p.Npad; i += kThreads)
+      bias_s[i] = (p.bias && !ACC && i < g.K) ? __ldg(p.bias + i) : 0.f;
   }
   ptx::fence_proxy_async_smem();
   if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
@@ -415,10 +435,20 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         }
       }
       // y[n, o, pos] (batch stride spans all groups' channels), or y[n, pos, o] channels last
-      float *yp = g.cl ? p.y + (n * p.osp + pp) * (g.G * g.K) : p.y + n * g.G * g.K * p.osp + pp;
+      float *yp = g.cl ? p.y + (n * p.osp + pp) * p.y_chans : p.y + n * p.y_chans * p.osp + pp;
       // y[n, c0 + j, pos] = accumulator column c0 + j + bias, j < 32: a warp
       // store covers 32 consecutive positions of one channel.
       auto store32 = [&](const uint32_t (&v)[32], int c0) {
+        if (ACC) {
+          // a later reduction pass: add to what the earlier passes stored
+          const int64_t ostride = g.cl ? 1 : p.osp;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int o = c0 + j;
+            if (o < g.K) yp[o * ostride] += __uint_as_float(v[j]);
+          }
+          return;
+        }
         if (g.cl) {
           // one position's channels are contiguous: 16-byte stores when aligned
           if (p.vec_store && c0 + 32 <= g.K) {
@@ -636,14 +666,13 @@ bool g_attr_set[64] = {false};
 
 bool igemm_supported(const Geom &g, const char **why) {
   Plan pl;
-  return make_plan(g, &pl, why);
+  Geom gb = g;
+  if (gb.K > kMaxNpad) gb.K = kMaxNpad;  // wider layers run in channel blocks of 128
+  return make_plan(gb, &pl, why);
 }
 
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
                                 cudaStream_t stream) {
-  Plan pl;
-  const char *why = "";
-  if (!make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -653,37 +682,65 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     if (e != cudaSuccess) return e;
   }
   if (!g_attr_set[dev]) {
-    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     g_attr_set[dev] = true;
   }
-  IgemmParams p;
-  p.x = x;
-  p.w = w;
-  p.bias = bias;
-  p.y = y;
-  p.g = g;
-  p.osp = (int64_t)g.OD * g.OH * g.OW;
-  p.M_total = g.N * p.osp;
-  p.tiles = (p.M_total + kTileM - 1) / kTileM;
-  p.Kred = pl.Kred;
-  p.Kpad = pl.Kpad;
-  p.Npad = pl.Npad;
-  p.KC = pl.KC;
-  p.nchunks = pl.nchunks;
-  p.nslots = pl.nslots;
-  p.tap_major = pl.tap_major;
-  p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
-  p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)y & 15u) == 0) ? 1 : 0;
-  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
-  const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-  if (pl.KC <= 16)
-    igemm_3xtf32_kernel<16><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
-  else
-    igemm_3xtf32_kernel<32><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
-  return cudaGetLastError();
+  const int64_t osp = (int64_t)g.OD * g.OH * g.OW;
+  const int64_t kfull = g.C * (int64_t)g.taps();
+  // Output channels in blocks of at most 128 (one accumulator tile), each over
+  // the reduction in passes that fit shared memory; every launch is a whole
+  // persistent kernel on views of w, bias and y.
+  for (int64_t o0 = 0; o0 < g.K; o0 += kMaxNpad) {
+    Geom gb = g;
+    gb.K = g.K - o0 < kMaxNpad ? g.K - o0 : kMaxNpad;
+    Plan pl;
+    const char *why = "";
+    if (!make_plan(gb, &pl, &why)) return cudaErrorInvalidValue;
+    for (int pass = 0; pass < pl.npasses; ++pass) {
+      const int k_begin = pass * pl.kpass;
+      const int kred = (int)(kfull - k_begin < pl.kpass ? kfull - k_begin : pl.kpass);
+      IgemmParams p = {};
+      p.x = x;
+      p.w = w + o0 * kfull;
+      p.bias = bias ? bias + o0 : nullptr;
+      p.y = y + (g.cl ? o0 : o0 * osp);
+      p.g = gb;
+      p.osp = osp;
+      p.M_total = g.N * p.osp;
+      p.tiles = (p.M_total + kTileM - 1) / kTileM;
+      p.Kred = kred;
+      p.Kfull = (int)kfull;
+      p.k_begin = k_begin;
+      p.accumulate = pass > 0;
+      p.y_chans = g.G * g.K;
+      p.Kpad = (kred + 31) / 32 * 32;
+      p.Npad = pl.Npad;
+      p.KC = pl.KC;
+      p.nchunks = (p.Kpad + pl.KC - 1) / pl.KC;
+      p.nslots = pl.nslots;
+      p.tap_major = pl.tap_major;
+      p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
+      p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)p.y & 15u) == 0) ? 1 : 0;
+      p.b_bytes = (uint32_t)((size_t)pl.Npad * p.Kpad * 4);
+      const size_t smem_need = (size_t)2 * pl.Npad * p.Kpad * 4 + (size_t)p.Kpad * 8 + (size_t)pl.Npad * 4 + 16 +
+                               kNumBars * 8 + 16;
+      const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
+      const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+      auto kern = pl.KC <= 16 ? (pass ? igemm_3xtf32_kernel<16, true> : igemm_3xtf32_kernel<16, false>)
+                              : (pass ? igemm_3xtf32_kernel<32, true> : igemm_3xtf32_kernel<32, false>);
+      kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+  }
+  return cudaSuccess;
 }
 
 bool igemm_bf16_supported(const Geom &g, const char **why) {
@@ -721,6 +778,8 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
   p.M_total = g.N * p.osp;
   p.tiles = (p.M_total + kTileM - 1) / kTileM;
   p.Kred = pl.Kred;
+  p.Kfull = pl.Kred;
+  p.y_chans = g.G * g.K;
   p.Kpad = pl.Kpad;
   p.Npad = pl.Npad;
   p.KC = kBfChunk;

@@ -519,3 +519,28 @@ def test_f16_exact_on_small_integers():
     assert np.abs(ref).max() < 2048
     assert np.array_equal(y, ref)
 
+
+
+# --------------------------- tensor cores past one tile of channels / weights
+
+@pytest.mark.parametrize("C_in,C_out,k,pad,channels_last", [
+    (64, 64, (3, 3, 3), (1, 1, 1), False),    # K = 1728: weights (hi + lo) need 4 passes of shared memory
+    (12, 200, (2, 3, 3), (0, 1, 1), False),   # 200 output channels: blocks of 128 and 72
+    (48, 150, (3, 3, 3), (1, 0, 1), True),    # both, channels last
+])
+def test_tensor_core_reduction_passes_and_channel_blocks(C_in, C_out, k, pad, channels_last):
+    rng = np.random.default_rng(C_in * 3 + C_out)
+    x = rng.standard_normal((2, C_in, 6, 9, 10)).astype(np.float32)
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    s, d = (1, 1, 1), (1, 1, 1)
+    assert cf.select_algo(2, C_in, C_out, x.shape[2:], k, s, pad, d) == cf.CONV_ALGO_IGEMM_3XTF32
+    ref = oracle.conv_nd(x, w, b, s, pad, d)
+    if channels_last:
+        y = cf.conv_fwd_nd(to_channels_last(x), to_channels_last(w), torch.from_numpy(b).cuda(), s, pad, d,
+                           channels_last=True)
+    else:
+        y = cf.conv_fwd_nd(torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda(), torch.from_numpy(b).cuda(), s,
+                           pad, d, algo=cf.CONV_ALGO_IGEMM_3XTF32)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, f"tensor cores C_in={C_in} C_out={C_out} k={k}")
