@@ -143,11 +143,14 @@ int validate_conv(const float *x, const float *w, const float *bias, const float
 
 // Planner: the tensor-core path where the reduction is a real dense
 // contraction (K = C_in*taps and C_out large enough to fill an MMA tile), the
-// FFMA direct path otherwise.
+// FFMA direct path otherwise.  Layers that need many tensor-core launches
+// (channel blocks x reduction passes, each re-gathering x) measured no faster
+// than the direct path beyond about six, so they take the direct path.
 int choose_algo(const Geom &g) {
   const int64_t red = g.C * (int64_t)g.taps();
   const char *why = nullptr;
-  if (red >= 64 && g.K >= 16 && convfwd::igemm_supported(g, &why)) return CONV_ALGO_IGEMM_3XTF32;
+  if (red >= 64 && g.K >= 16 && convfwd::igemm_supported(g, &why) && convfwd::igemm_launches(g) <= 6)
+    return CONV_ALGO_IGEMM_3XTF32;
   return CONV_ALGO_DIRECT_FFMA;
 }
 

@@ -52,8 +52,10 @@ bool igemm_bf16_supported(const Geom &g, const char **why);
 cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, const Geom &g,
                               bool fp16, cudaStream_t stream);
 
-// Tensor-core implicit GEMM (tcgen05, 3xTF32).
+// Tensor-core implicit GEMM (tcgen05, 3xTF32).  igemm_launches: kernel launches
+// one group takes (channel blocks x reduction passes), 0 when unsupported.
 bool igemm_supported(const Geom &g, const char **why);
+int igemm_launches(const Geom &g);
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
                                 cudaStream_t stream);
 cudaError_t read_and_clear_device_status(unsigned *flags);

@@ -671,6 +671,15 @@ bool igemm_supported(const Geom &g, const char **why) {
   return make_plan(gb, &pl, why);
 }
 
+int igemm_launches(const Geom &g) {
+  Plan pl;
+  Geom gb = g;
+  if (gb.K > kMaxNpad) gb.K = kMaxNpad;
+  const char *why = "";
+  if (!make_plan(gb, &pl, &why)) return 0;
+  return (int)((g.K + kMaxNpad - 1) / kMaxNpad) * pl.npasses;
+}
+
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
                                 cudaStream_t stream) {
   int dev = 0;

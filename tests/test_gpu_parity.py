@@ -523,18 +523,19 @@ def test_f16_exact_on_small_integers():
 
 # --------------------------- tensor cores past one tile of channels / weights
 
-@pytest.mark.parametrize("C_in,C_out,k,pad,channels_last", [
-    (64, 64, (3, 3, 3), (1, 1, 1), False),    # K = 1728: weights (hi + lo) need 4 passes of shared memory
-    (12, 200, (2, 3, 3), (0, 1, 1), False),   # 200 output channels: blocks of 128 and 72
-    (48, 150, (3, 3, 3), (1, 0, 1), True),    # both, channels last
+@pytest.mark.parametrize("C_in,C_out,k,pad,channels_last,planned", [
+    (64, 64, (3, 3, 3), (1, 1, 1), False, True),    # K = 1728: weights (hi + lo) need 4 passes of shared memory
+    (12, 200, (2, 3, 3), (0, 1, 1), False, True),   # 200 output channels: blocks of 128 and 72
+    (48, 150, (3, 3, 3), (1, 0, 1), True, False),   # both (12 launches: the planner prefers FFMA), channels last
 ])
-def test_tensor_core_reduction_passes_and_channel_blocks(C_in, C_out, k, pad, channels_last):
+def test_tensor_core_reduction_passes_and_channel_blocks(C_in, C_out, k, pad, channels_last, planned):
     rng = np.random.default_rng(C_in * 3 + C_out)
     x = rng.standard_normal((2, C_in, 6, 9, 10)).astype(np.float32)
     w = ((rng.random((C_out, C_in) + k) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))).astype(np.float32)
     b = rng.standard_normal(C_out).astype(np.float32)
     s, d = (1, 1, 1), (1, 1, 1)
-    assert cf.select_algo(2, C_in, C_out, x.shape[2:], k, s, pad, d) == cf.CONV_ALGO_IGEMM_3XTF32
+    expect = cf.CONV_ALGO_IGEMM_3XTF32 if planned else cf.CONV_ALGO_DIRECT_FFMA
+    assert cf.select_algo(2, C_in, C_out, x.shape[2:], k, s, pad, d) == expect
     ref = oracle.conv_nd(x, w, b, s, pad, d)
     if channels_last:
         y = cf.conv_fwd_nd(to_channels_last(x), to_channels_last(w), torch.from_numpy(b).cuda(), s, pad, d,
