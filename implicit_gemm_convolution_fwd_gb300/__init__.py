@@ -19,7 +19,7 @@ ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV
 
 # every symbol include/convfwd.h declares
 EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_fwd_nd_channels_last",
-            "conv_fwd_nd_bf16", "conv_fwd_nd_f16",
+            "conv_fwd_nd_bf16", "conv_fwd_nd_f16", "conv_workspace_bytes", "conv_fwd_nd_ws",
             "conv_select_algo",
             "conv_algo_supported",
             "conv3d_min_softmax",
@@ -62,6 +62,10 @@ def load(path: str | None = None):
                                               vp]
     lib.conv_fwd_nd_bf16.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp]
     lib.conv_fwd_nd_f16.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp]
+    lib.conv_workspace_bytes.argtypes = [i32, i64, i64, i64, i64, arr, arr, arr, arr, arr,
+                                         ctypes.POINTER(ctypes.c_size_t)]
+    lib.conv_fwd_nd_ws.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp,
+                                   ctypes.c_size_t, vp]
     lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
@@ -223,6 +227,44 @@ def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None):
     yd = Tensor4(out.data_ptr(), (ctypes.c_int64 * 4)(*out.shape))
     st = load().conv3d_min_softmax(ctypes.byref(xd), ctypes.byref(wd), None if bias is None else bias.data_ptr(),
                                    ctypes.byref(yd), int(min_dim), _stream_handle(stream))
+    _check(st)
+    return out
+
+
+def workspace_bytes(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1, groups=1) -> int:
+    """Bytes of device workspace conv_fwd_nd_ws can use for this problem (0: none needed)."""
+    nd = len(in_dims)
+    b = ctypes.c_size_t(0)
+    _check(load().conv_workspace_bytes(nd, N, C_in, C_out, int(groups), _arr(in_dims), _arr(k_dims),
+                                       _arr(_tuple(stride, nd)), _arr(_tuple(pad, nd)), _arr(_tuple(dilation, nd)),
+                                       ctypes.byref(b)))
+    return int(b.value)
+
+
+def conv_fwd_nd_ws(x, w, bias=None, stride=1, pad=0, dilation=1, workspace=None, out=None, stream=None, groups=1):
+    """conv_fwd_nd (fp32, contiguous) with a caller workspace for streamed weights: `workspace` is a CUDA
+    tensor of at least workspace_bytes(...) bytes (allocated here when None and the problem needs one)."""
+    import torch
+    nd = x.dim() - 2
+    s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[0]
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous float32 CUDA tensors")
+    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in:
+        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
+    need = workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    if out is None:
+        out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
+    wsp = None if workspace is None else workspace.data_ptr()
+    wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    st = load().conv_fwd_nd_ws(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
+                               nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s),
+                               _arr(p), _arr(d), wsp, wsb, _stream_handle(stream))
     _check(st)
     return out
 

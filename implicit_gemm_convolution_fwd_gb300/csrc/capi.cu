@@ -302,6 +302,52 @@ int conv_fwd_nd_f16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, 
                         stream, "conv_fwd_nd_f16");
 }
 
+int conv_workspace_bytes(int ndim, int64_t N, int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                         const int64_t *k_dims, const int64_t *stride, const int64_t *pad, const int64_t *dilation,
+                         size_t *bytes) {
+  g_last_error[0] = 0;
+  if (!bytes) return fail(CONV_ERR_NULL, "conv_workspace_bytes: bytes is NULL%s");
+  Geom g;
+  int64_t xe, we, ye;
+  int st = make_geom(ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, &xe, &we, &ye, groups);
+  if (st != CONV_OK) return st;
+  *bytes = convfwd::igemm_stream_bytes_one_group(g) * (size_t)g.G;
+  return CONV_OK;
+}
+
+int conv_fwd_nd_ws(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N, int64_t C_in,
+                   int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                   const int64_t *pad, const int64_t *dilation, void *workspace, size_t workspace_bytes,
+                   conv_stream_t stream) {
+  g_last_error[0] = 0;
+  Geom g;
+  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, -1,
+                         groups);
+  if (st != CONV_OK) return st;
+  const size_t one = convfwd::igemm_stream_bytes_one_group(g);
+  if (one == 0 || !workspace)  // nothing to stream: the plain call
+    return conv_fwd_nd_grouped(x, w, bias, y, ndim, N, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation,
+                               CONV_ALGO_AUTO, stream);
+  if (workspace_bytes < one * (size_t)g.G)
+    return fail(CONV_ERR_ARG, "conv_fwd_nd_ws: workspace smaller than conv_workspace_bytes%s");
+  if ((uintptr_t)workspace & 255u) return fail(CONV_ERR_ARG, "conv_fwd_nd_ws: workspace must be 256-byte aligned%s");
+  const int64_t ye = g.N * g.G * g.K * g.out_spatial(), xe = g.N * g.G * g.C * g.in_spatial();
+  const int64_t we = g.G * g.K * g.C * g.taps();
+  const int64_t wsb = (int64_t)(one * (size_t)g.G);
+  if (ranges_overlap(workspace, wsb, x, xe * 4) || ranges_overlap(workspace, wsb, w, we * 4) ||
+      ranges_overlap(workspace, wsb, y, ye * 4) || ranges_overlap(workspace, wsb, bias, g.G * g.K * 4))
+    return fail(CONV_ERR_ARG, "conv_fwd_nd_ws: workspace overlaps a tensor%s");
+  if (g.N == 0) return CONV_OK;
+  const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
+  float *wsf = static_cast<float *>(workspace);
+  cudaError_t e = cudaSuccess;
+  for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
+    e = convfwd::launch_igemm_3xtf32(x + grp * xg, w + grp * wg, bias ? bias + grp * g.K : nullptr, y + grp * yg, g,
+                                     (cudaStream_t)stream, wsf + grp * (int64_t)(one / 4));
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_ws: kernel launch");
+  return CONV_OK;
+}
+
 int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
                    int64_t C_in, int64_t C_out, const int64_t *in_dims, const int64_t *k_dims,
                    const int64_t *stride, const int64_t *pad, const int64_t *dilation, int algo,

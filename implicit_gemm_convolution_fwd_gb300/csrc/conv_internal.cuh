@@ -56,8 +56,13 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
 // one group takes (channel blocks x reduction passes), 0 when unsupported.
 bool igemm_supported(const Geom &g, const char **why);
 int igemm_launches(const Geom &g);
+// Streamed weights: workspace bytes one group needs (0: the layer does not use them).
+size_t igemm_stream_bytes_one_group(const Geom &g);
+// ws: device workspace of igemm_stream_bytes_one_group(g) bytes for streamed
+// weights, or nullptr (then layers whose weights exceed shared memory run in
+// reduction passes).
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                cudaStream_t stream);
+                                cudaStream_t stream, float *ws = nullptr);
 cudaError_t read_and_clear_device_status(unsigned *flags);
 
 }  // namespace convfwd

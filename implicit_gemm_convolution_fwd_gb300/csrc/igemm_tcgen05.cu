@@ -58,7 +58,8 @@ constexpr int kMaxNpad = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA per SM, so TMEM allocation never contends
 constexpr int kMaxStages = 2 * kMaxSlots;     // two A stages per slot
-constexpr int kNumBars = 2 * kMaxStages + 2 * kMaxSlots + 1;  // a_full, a_empty, d_full, d_empty, drain
+// a_full, a_empty [stages], d_full, d_empty [slots], drain, b_full [stages] (streamed weights)
+constexpr int kNumBars = 3 * kMaxStages + 2 * kMaxSlots + 1;
 constexpr long long kWaitLimitCycles = 1ll << 32;  // about two seconds
 
 struct IgemmParams {
@@ -89,7 +90,12 @@ struct IgemmParams {
                     // and always for channels-last tensors
   int vec4;         // channels last with 16-byte aligned groups of 4 channels: float4 gathers
   int vec_store;    // channels last with 16-byte aligned output rows: float4 stores
-  uint32_t b_bytes; // Npad * Kpad * 4
+  uint32_t b_bytes; // Npad * Kpad * 4; with streamed weights the whole B stage region
+  // streamed weights: B chunks prepared once (hi then lo, each in the core-matrix
+  // layout of one chunk) in a workspace and copied per chunk into the A stage's
+  // twin B stage with a bulk copy
+  const float *__restrict__ wsp;  // this launch's chunks: chunk q at wsp + q * sb_stage_bytes / 4
+  uint32_t sb_stage_bytes;        // 2 * Npad * KC * 4
 };
 
 struct Plan {
@@ -315,16 +321,17 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
 
 // CH: register buffer of one chunk (>= KC): 16 for four slots, 32 for two.
 // ACC: a later reduction pass (adds into y; instantiated separately so that
-// the single-pass kernels keep their registers).
-template <int CH, bool ACC>
+// the single-pass kernels keep their registers).  SB: streamed weights (see
+// IgemmParams::wsp): no resident weight matrix, any reduction length in one pass.
+template <int CH, bool ACC, bool SB>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  uint8_t *b_hi = smem;
-  uint8_t *b_lo = smem + p.b_bytes;
-  int32_t *toff = reinterpret_cast<int32_t *>(smem + 2 * (size_t)p.b_bytes);  // [Kpad]
+  uint8_t *b_hi = smem;              // resident weights: hi [Npad x Kpad]; streamed: the B stages
+  uint8_t *b_lo = smem + p.b_bytes;  // resident weights: lo
+  int32_t *toff = reinterpret_cast<int32_t *>(smem + (SB ? 1 : 2) * (size_t)p.b_bytes);  // [Kpad]
   uint32_t *ttap = reinterpret_cast<uint32_t *>(toff + p.Kpad);                // [Kpad]
   float *bias_s = reinterpret_cast<float *>(ttap + p.Kpad);
   uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
@@ -335,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kMaxStages);                   // [slots]
   const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kMaxStages + kMaxSlots);      // [slots]
   const uint32_t bar_drain = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots);
+  const uint32_t bar_b_full = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots + 1);  // [stages]
   const int nslots = p.nslots;
 
   const uint32_t SBO = (uint32_t)p.Kpad * 32;  // bytes between 8-row groups of B
@@ -347,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   // words (conflict-free).
   {
     const int kq = p.Kpad / 4;
-    const int words = p.Npad * p.Kpad;
+    const int words = SB ? 0 : p.Npad * p.Kpad;  // streamed weights arrive per chunk
     for (int i = tid; i < words; i += kThreads) {
       const int cm = i >> 5, r = (i >> 2) & 7, cw = i & 3;
       const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
@@ -394,6 +402,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(bar_a_full + 8 * s, 128);
       ptx::mbar_init(bar_a_empty + 8 * s, 1);
+      ptx::mbar_init(bar_b_full + 8 * s, 1);
     }
     for (int b = 0; b < kMaxSlots; ++b) {
       ptx::mbar_init(bar_d_full + 8 * b, 1);
@@ -553,6 +562,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     // drain, split into hi / lo, store both to TMEM and signal the issuer.
     // The lo part overwrites v in place (keeps the chunk within the register
     // budget without spills).  False when the wait timed out.
+    // streamed weights: the group's thread 0 brings chunk q's B into the
+    // stage; it remembers its last copy to wait for it before leaving
+    int sb_last_stage = -1;
+    uint32_t sb_last_parity = 0;
     auto put_chunk = [&](int64_t lg, int q, float (&v)[CH]) -> bool {
       const int stage = 2 * slot + (int)(lg & 1);
       const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
@@ -562,6 +575,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
       if (!__all_sync(0xffffffffu, ok)) return false;
       ptx::tc_fence_after();
+      if (SB && t == 0) {
+        // the stage's MMAs are done: its B half is free too
+        ptx::mbar_arrive_expect_tx(bar_b_full + 8 * stage, p.sb_stage_bytes);
+        ptx::bulk_copy_g2s(ptx::smem_addr(b_hi + (size_t)stage * p.sb_stage_bytes),
+                           p.wsp + (size_t)q * (p.sb_stage_bytes / 4), p.sb_stage_bytes, bar_b_full + 8 * stage);
+        sb_last_stage = stage;
+        sb_last_parity = r & 1;
+      }
 #pragma unroll
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
@@ -597,6 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         }
       }
     }
+    if (SB && sb_last_stage >= 0) {
+      // no bulk copy of ours may still be landing when the CTA exits (bounded)
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(bar_b_full + 8 * sb_last_stage, sb_last_parity) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
   } else if (lane == 0 && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
     // One thread per slot, in warps on different SM sub-partitions: a thread
@@ -616,7 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t lg = li * p.nchunks + q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
-        if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag)) {
+        if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag) ||
+            (SB && !wait_phase(bar_b_full + 8 * s, r & 1, abort_flag))) {
           aborted = true;
           break;
         }
@@ -625,10 +653,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         const uint32_t a_lo = a_hi + (uint32_t)p.KC;
         const int k0 = q * p.KC;
         const int ksteps = min(p.KC, p.Kpad - k0) / 8;
+        // streamed: the stage holds chunk q only (hi, then lo), 8-row groups KC * 32 bytes apart
+        const uint32_t sb_hi = bhi + s * p.sb_stage_bytes, sb_lo = sb_hi + p.sb_stage_bytes / 2;
         for (int ks = 0; ks < ksteps; ++ks) {
           const uint32_t kbyte = (uint32_t)(k0 + ks * 8) * 32u;  // (k/4) core matrices of 128 B
-          const uint64_t dh = ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
-          const uint64_t dl = ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
+          const uint64_t dh = SB ? ptx::smem_desc_noswizzle(sb_hi + 256u * ks, 128, (uint32_t)p.KC * 32)
+                                 : ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
+          const uint64_t dl = SB ? ptx::smem_desc_noswizzle(sb_lo + 256u * ks, 128, (uint32_t)p.KC * 32)
+                                 : ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
           ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (q | ks) != 0);
           ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
           ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
@@ -652,6 +684,37 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   if (warp == kMmaWarp) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+// Streamed weights, prepared once per call: chunk q of the reduction (KC
+// columns) as the tensor cores read it from shared memory, hi then lo, each
+// [Npad x KC] in core matrices of 8 rows x 4 floats (LBO 128 bytes along K,
+// SBO KC * 32 bytes along N).  Column kg maps to w's memory order as in the
+// kernel's resident staging.
+__global__ void split_weights_kernel(const float *__restrict__ w, float *__restrict__ ws, int K, int C, int taps,
+                                     int Kfull, int Npad, int KC, int nchunks, int tap_major) {
+  const int64_t per_chunk = (int64_t)Npad * KC;
+  const int64_t total = per_chunk * nchunks;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int q = (int)(i / per_chunk);
+    const int e = (int)(i - (int64_t)q * per_chunk);
+    const int n = e / KC, kl = e - n * KC;
+    const int kg = q * KC + kl;
+    float v = 0.f;
+    if (n < K && kg < Kfull) {
+      int kmem = kg;
+      if (tap_major) {
+        const int t = kg / C;
+        kmem = (kg - t * C) * taps + t;
+      }
+      v = __ldg(w + (int64_t)n * Kfull + kmem);
+    }
+    const float hi = __uint_as_float(tf32_hi_bits(v));
+    const int64_t o = ((int64_t)(n / 8) * (KC / 4) + kl / 4) * 32 + (n % 8) * 4 + (kl % 4);
+    float *chunk = ws + (int64_t)q * 2 * per_chunk;
+    chunk[o] = hi;
+    chunk[per_chunk + o] = v - hi;
   }
 }
 
@@ -680,8 +743,23 @@ int igemm_launches(const Geom &g) {
   return (int)((g.K + kMaxNpad - 1) / kMaxNpad) * pl.npasses;
 }
 
+// Workspace bytes for streamed weights (one group), or 0 when the layer does
+// not need them (its weights fit in shared memory, or it spans channel blocks).
+size_t igemm_stream_bytes_one_group(const Geom &g) {
+  if (g.K > kMaxNpad) return 0;
+  Plan pl;
+  const char *why = "";
+  if (!make_plan(g, &pl, &why) || pl.npasses <= 1) return 0;
+  const int64_t kfull = g.C * (int64_t)g.taps();
+  const int64_t kpad = (kfull + 31) / 32 * 32;
+  const size_t smem = (size_t)pl.nslots * 2 * 2 * pl.Npad * pl.KC * 4 + (size_t)kpad * 8 + (size_t)pl.Npad * 4 +
+                      16 + kNumBars * 8 + 16;
+  if (smem > (size_t)kMaxSmem) return 0;  // the column tables alone would not fit
+  return (size_t)pl.Npad * kpad * 8;
+}
+
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                cudaStream_t stream) {
+                                cudaStream_t stream, float *ws) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -691,18 +769,67 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     if (e != cudaSuccess) return e;
   }
   if (!g_attr_set[dev]) {
-    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e != cudaSuccess) return e;
+    const void *kerns[] = {(const void *)igemm_3xtf32_kernel<16, false, false>,
+                           (const void *)igemm_3xtf32_kernel<32, false, false>,
+                           (const void *)igemm_3xtf32_kernel<16, true, false>,
+                           (const void *)igemm_3xtf32_kernel<32, true, false>,
+                           (const void *)igemm_3xtf32_kernel<16, false, true>,
+                           (const void *)igemm_3xtf32_kernel<32, false, true>};
+    for (const void *k : kerns) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+      if (e != cudaSuccess) return e;
+    }
     g_attr_set[dev] = true;
   }
   const int64_t osp = (int64_t)g.OD * g.OH * g.OW;
   const int64_t kfull = g.C * (int64_t)g.taps();
+  if (ws && igemm_stream_bytes_one_group(g) > 0) {
+    // streamed weights: prepare the chunks, then one pass over the whole reduction
+    Plan pl;
+    const char *why = "";
+    if (!make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
+    const int kpad = (int)((kfull + 31) / 32 * 32);
+    const int nchunks = kpad / pl.KC;
+    const int64_t total = (int64_t)pl.Npad * pl.KC * nchunks;
+    const int threads = 256;
+    const int64_t blocks64 = (total + threads - 1) / threads;
+    const int blocks = (int)(blocks64 < 4096 ? blocks64 : 4096);
+    split_weights_kernel<<<blocks, threads, 0, stream>>>(w, ws, (int)g.K, (int)g.C, g.taps(), (int)kfull, pl.Npad,
+                                                         pl.KC, nchunks, pl.tap_major && !g.cl);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    IgemmParams p = {};
+    p.x = x;
+    p.w = w;
+    p.bias = bias;
+    p.y = y;
+    p.g = g;
+    p.osp = osp;
+    p.M_total = g.N * p.osp;
+    p.tiles = (p.M_total + kTileM - 1) / kTileM;
+    p.Kred = (int)kfull;
+    p.Kfull = (int)kfull;
+    p.k_begin = 0;
+    p.accumulate = 0;
+    p.y_chans = g.G * g.K;
+    p.Kpad = kpad;
+    p.Npad = pl.Npad;
+    p.KC = pl.KC;
+    p.nchunks = nchunks;
+    p.nslots = pl.nslots;
+    p.tap_major = pl.tap_major;
+    p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
+    p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)y & 15u) == 0) ? 1 : 0;
+    p.wsp = ws;
+    p.sb_stage_bytes = (uint32_t)(2 * pl.Npad * pl.KC * 4);
+    p.b_bytes = (uint32_t)(pl.nslots * 2) * p.sb_stage_bytes;
+    const size_t smem_need = (size_t)p.b_bytes + (size_t)kpad * 8 + (size_t)pl.Npad * 4 + 16 + kNumBars * 8 + 16;
+    const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
+    const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+    auto kern = pl.KC <= 16 ? igemm_3xtf32_kernel<16, false, true> : igemm_3xtf32_kernel<32, false, true>;
+    kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
   // Output channels in blocks of at most 128 (one accumulator tile), each over
   // the reduction in passes that fit shared memory; every launch is a whole
   // persistent kernel on views of w, bias and y.
@@ -742,8 +869,8 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
                                kNumBars * 8 + 16;
       const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
       const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-      auto kern = pl.KC <= 16 ? (pass ? igemm_3xtf32_kernel<16, true> : igemm_3xtf32_kernel<16, false>)
-                              : (pass ? igemm_3xtf32_kernel<32, true> : igemm_3xtf32_kernel<32, false>);
+      auto kern = pl.KC <= 16 ? (pass ? igemm_3xtf32_kernel<16, true, false> : igemm_3xtf32_kernel<16, false, false>)
+                              : (pass ? igemm_3xtf32_kernel<32, true, false> : igemm_3xtf32_kernel<32, false, false>);
       kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;

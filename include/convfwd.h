@@ -175,6 +175,34 @@ CONVFWD_API int conv_fwd_nd_f16(const uint16_t *x, const uint16_t *w, const uint
                                 const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
                                 const int64_t *dilation, conv_stream_t stream);
 
+/*
+ * Workspace for streamed weights.  The tensor-core family keeps one group's
+ * weights (split into TF32 hi and lo) in shared memory; when they do not fit
+ * it runs the reduction in several passes (each re-reading x and adding into
+ * y) or leaves the layer to the direct family.  With a caller workspace the
+ * weights are split once into it, in the order the tensor cores read them, and
+ * brought into shared memory chunk by chunk with bulk copies, so the whole
+ * reduction runs in one pass.
+ * conv_workspace_bytes writes the bytes conv_fwd_nd_ws can use for the problem
+ * (0 when its weights fit in shared memory, or a group has more than 128
+ * output channels, or the column tables of the reduction exceed shared memory).
+ */
+CONVFWD_API int conv_workspace_bytes(int ndim, int64_t N, int64_t C_in, int64_t C_out, int64_t groups,
+                                     const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                                     const int64_t *pad, const int64_t *dilation, size_t *bytes);
+
+/* conv_fwd_nd_grouped (AUTO) with a device workspace of at least
+ * conv_workspace_bytes bytes, 256-byte aligned, not overlapping x, w, bias or
+ * y; the library writes it before reading it on `stream`, so calls that share
+ * a workspace must be ordered (the same stream does that).  With workspace NULL
+ * or a problem that needs none, it is conv_fwd_nd_grouped; a workspace smaller
+ * than needed is CONV_ERR_ARG. */
+CONVFWD_API int conv_fwd_nd_ws(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                               int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                               const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                               const int64_t *dilation, void *workspace, size_t workspace_bytes,
+                               conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */

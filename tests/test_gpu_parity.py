@@ -545,3 +545,31 @@ def test_tensor_core_reduction_passes_and_channel_blocks(C_in, C_out, k, pad, ch
                            pad, d, algo=cf.CONV_ALGO_IGEMM_3XTF32)
     torch.cuda.synchronize()
     assert_close(y.cpu().numpy(), ref, f"tensor cores C_in={C_in} C_out={C_out} k={k}")
+
+
+# ---------------------------------------------------------- streamed weights
+
+@pytest.mark.parametrize("C_in,C_out,k,pad,groups", [
+    (64, 64, (3, 3, 3), (1, 1, 1), 1),     # K = 1728 with 64 channels: 4 shared-memory passes without a workspace
+    (64, 128, (3, 3, 3), (1, 1, 1), 1),    # 128 channels: two issuer slots, 32-column chunks
+    (96, 48, (3, 3, 3), (0, 1, 1), 2),     # two groups, each with its own part of the workspace
+    (40, 20, (5, 5, 5), (2, 2, 2), 1),     # K = 5000: a reduction length not a multiple of 32
+])
+def test_streamed_weights_workspace(C_in, C_out, k, pad, groups):
+    rng = np.random.default_rng(C_in + 7 * C_out + groups)
+    x = rng.standard_normal((2, C_in, 5, 8, 9)).astype(np.float32)
+    w = ((rng.random((C_out, C_in // groups) + k) - 0.5) * 2 / np.sqrt(C_in // groups * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    s, d = (1, 1, 1), (1, 1, 1)
+    need = cf.workspace_bytes(2, C_in, C_out, x.shape[2:], k, s, pad, d, groups)
+    assert need > 0
+    ws = torch.full((need + 256,), 255, dtype=torch.uint8, device="cuda")  # garbage: the call must write it
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    y = cf.conv_fwd_nd_ws(xt, wt, bt, s, pad, d, workspace=ws, groups=groups)
+    torch.cuda.synchronize()
+    ref = oracle.conv_nd(x, w, b, s, pad, d, groups=groups)
+    assert_close(y.cpu().numpy(), ref, f"streamed weights C_in={C_in} C_out={C_out} k={k} G={groups}")
+    assert cf.device_status() == 0
+    with pytest.raises(cf.ConvError) as e:
+        cf.conv_fwd_nd_ws(xt, wt, bt, s, pad, d, workspace=ws[:need // 2], groups=groups)
+    assert e.value.status == cf.CONV_ERR_ARG
