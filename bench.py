@@ -221,10 +221,15 @@ class VariantRunner(OurRunner):
     """A benchmark workload run through one of the library's other entry points:
     16-bit tensors, the min over another dim, channels-last tensors or groups."""
 
-    def __init__(self, wl, device, dtype=None, min_dim=None, channels_last=False, groups=1):
+    def __init__(self, wl, device, dtype=None, min_dim=None, channels_last=False, groups=1, workspace=False):
         super().__init__(wl, device)
         torch = self.torch
         self.dtype, self.channels_last, self.groups = dtype, channels_last, groups
+        self.ws = None
+        if workspace:
+            need = self.cf.workspace_bytes(wl.N, wl.C_in, wl.C_out, wl.in_dims, wl.k_dims, wl.stride, wl.pad,
+                                           wl.dilation)
+            self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
         self.min_dim = wl.min_dim if min_dim is None else min_dim
         if groups > 1:
             self.w = self.w[:, :wl.C_in // groups].contiguous()
@@ -244,6 +249,9 @@ class VariantRunner(OurRunner):
     def step(self):
         if self.wl.kind == "fused":
             self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.min_dim, out=self.y, stream=self.stream)
+        elif self.ws is not None:
+            self.cf.conv_fwd_nd_ws(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation,
+                                   workspace=self.ws, out=self.y, stream=self.stream)
         else:
             self.cf.conv_fwd_nd(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation, out=self.y,
                                 stream=self.stream, groups=self.groups, channels_last=self.channels_last)
@@ -258,6 +266,8 @@ VARIANTS = [
     ("conv3d_min_softmax[min_dim=4]", "conv3d_min_softmax", {"min_dim": 4}),
     ("conv3d_sweep_b[channels_last]", "conv3d_sweep_b", {"channels_last": True}),
     ("conv3d_sweep_b[groups=2]", "conv3d_sweep_b", {"groups": 2}),
+    ("conv3d_wide_k[workspace]", "conv3d_wide_k", {"workspace": True}),
+    ("conv3d_wide_k[no workspace]", "conv3d_wide_k", {}),
 ]
 
 
@@ -275,6 +285,9 @@ def run_variants(dev, peaks, steps):
         flops, _, _, _ = problem_counts(r.wl, r.out_dims)
         flops /= r.groups  # each output channel sums over C_in / groups input channels
         entry = {"ms": m, "ms_min": min(times), "tflops": flops / (m * 1e-3) / 1e12}
+        if r.dtype is None and r.wl.kind == "conv":
+            tf32x3 = peaks["bf16_tflops"] * BF16_TO_TF32 / 3.0
+            entry["frac_of_3xtf32_peak"] = entry["tflops"] / tf32x3
         if r.dtype is not None:
             entry["frac_of_measured_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
         out[name] = entry

@@ -162,4 +162,9 @@ WORKLOADS = {
     "conv3d_sweep_b_dil": Workload(
         "conv3d_sweep_b_dil", "conv", 8, 32, 32, (48, 48, 48), (3, 3, 3), (1, 1, 1), (1, 1, 1), (2, 1, 1), True,
         "normal", "Conv3d sweep, large K, alternative reading with dilation (2,1,1)"),
+    # not one of the pages' shapes: a layer whose weights (K = 1728 x 128) exceed
+    # shared memory, for the streamed-weights entry point
+    "conv3d_wide_k": Workload(
+        "conv3d_wide_k", "conv", 4, 64, 128, (32, 32, 32), (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), True,
+        "normal", "Conv3d 64 -> 128 channels, k=3^3, pad 1: x[4,64,32,32,32] N(0,1) (weights exceed shared memory)"),
 }
