@@ -19,7 +19,7 @@ ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV
 
 # every symbol include/convfwd.h declares
 EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_fwd_nd_channels_last",
-            "conv_fwd_nd_bf16", "conv_fwd_nd_f16", "conv_workspace_bytes", "conv_fwd_nd_ws",
+            "conv_fwd_nd_bf16", "conv_fwd_nd_f16", "conv_workspace_bytes", "conv_fwd_nd_ws", "conv_fwd_nd_ws_noalloc",
             "conv_select_algo",
             "conv_algo_supported",
             "conv3d_min_softmax",
@@ -66,6 +66,7 @@ def load(path: str | None = None):
                                          ctypes.POINTER(ctypes.c_size_t)]
     lib.conv_fwd_nd_ws.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp,
                                    ctypes.c_size_t, vp]
+    lib.conv_fwd_nd_ws_noalloc.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp]
     lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
@@ -265,6 +266,26 @@ def conv_fwd_nd_ws(x, w, bias=None, stride=1, pad=0, dilation=1, workspace=None,
     st = load().conv_fwd_nd_ws(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
                                nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s),
                                _arr(p), _arr(d), wsp, wsb, _stream_handle(stream))
+    _check(st)
+    return out
+
+
+def conv_fwd_nd_noalloc(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, stream=None, groups=1):
+    """conv_fwd_nd_ws with the library's static scratch instead of a caller workspace (no allocation)."""
+    import torch
+    nd = x.dim() - 2
+    s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[0]
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous float32 CUDA tensors")
+    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    if out is None:
+        out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
+    st = load().conv_fwd_nd_ws_noalloc(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                       out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
+                                       _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), _stream_handle(stream))
     _check(st)
     return out
 

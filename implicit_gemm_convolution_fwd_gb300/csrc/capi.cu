@@ -170,6 +170,24 @@ int check_algo(const Geom &g, int algo) {
   }
 }
 
+// Scratch of conv_fwd_nd_ws_noalloc: a file-scope device array (no allocation
+// at call time), its address looked up once per device.
+static __device__ __align__(256) unsigned char g_noalloc_ws[16u << 20];
+void *g_noalloc_ws_ptr[64] = {nullptr};
+
+int noalloc_ws_address(void **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_ws_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(CONV_ERR_UNSUPPORTED, "conv_fwd_nd_ws_noalloc: device index above 63%s");
+  if (!g_noalloc_ws_ptr[dev]) {
+    e = cudaGetSymbolAddress(&g_noalloc_ws_ptr[dev], g_noalloc_ws);
+    if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_ws_noalloc: cudaGetSymbolAddress");
+  }
+  *out = g_noalloc_ws_ptr[dev];
+  return CONV_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -346,6 +364,28 @@ int conv_fwd_nd_ws(const float *x, const float *w, const float *bias, float *y, 
                                      (cudaStream_t)stream, wsf + grp * (int64_t)(one / 4));
   if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_ws: kernel launch");
   return CONV_OK;
+}
+
+int conv_fwd_nd_ws_noalloc(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                           int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                           const int64_t *stride, const int64_t *pad, const int64_t *dilation, conv_stream_t stream) {
+  g_last_error[0] = 0;
+  Geom g;
+  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, -1,
+                         groups);
+  if (st != CONV_OK) return st;
+  const size_t need = convfwd::igemm_stream_bytes_one_group(g) * (size_t)g.G;
+  if (need == 0)
+    return conv_fwd_nd_grouped(x, w, bias, y, ndim, N, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation,
+                               CONV_ALGO_AUTO, stream);
+  if (need > sizeof(g_noalloc_ws))
+    return fail(CONV_ERR_UNSUPPORTED, "conv_fwd_nd_ws_noalloc: needs %s%lld bytes of scratch, the static buffer holds %lld",
+                "", (long long)need, (long long)sizeof(g_noalloc_ws));
+  void *ws = nullptr;
+  st = noalloc_ws_address(&ws);
+  if (st != CONV_OK) return st;
+  return conv_fwd_nd_ws(x, w, bias, y, ndim, N, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation, ws,
+                        sizeof(g_noalloc_ws), stream);
 }
 
 int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,

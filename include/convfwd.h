@@ -203,6 +203,22 @@ CONVFWD_API int conv_fwd_nd_ws(const float *x, const float *w, const float *bias
                                const int64_t *dilation, void *workspace, size_t workspace_bytes,
                                conv_stream_t stream);
 
+/*
+ * conv_fwd_nd_ws without a caller workspace and without allocating: the
+ * streamed weights go to a 16 MiB scratch array that the library holds in
+ * device memory from load time (a file-scope device array; its address is
+ * looked up once per device).  The paper has no counterpart of this entry
+ * point; it exists for callers that cannot allocate device memory.
+ * Problems that need more scratch than the array holds return
+ * CONV_ERR_UNSUPPORTED; problems that need none are conv_fwd_nd_grouped.  The
+ * scratch is shared by every call on the device, so calls that use it must be
+ * ordered (issue them on one stream).
+ */
+CONVFWD_API int conv_fwd_nd_ws_noalloc(const float *x, const float *w, const float *bias, float *y, int ndim,
+                                       int64_t N, int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                                       const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                                       const int64_t *dilation, conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */
