@@ -60,18 +60,18 @@ def load_peaks():
                 "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
 
 
-def problem_counts(wl, out_dims):
-    """Algorithmic FLOPs (2 per MAC, padded taps included) and compulsory bytes."""
+def problem_counts(wl, out_dims, esize=4):
+    """Algorithmic FLOPs (2 per MAC, padded taps included) and compulsory bytes (esize bytes per element)."""
     out_sp = int(np.prod(out_dims))
     k_sp = int(np.prod(wl.k_dims))
     flops = 2.0 * wl.N * wl.C_out * out_sp * wl.C_in * k_sp
-    x_b = 4.0 * wl.N * wl.C_in * int(np.prod(wl.in_dims))
-    w_b = 4.0 * wl.C_out * wl.C_in * k_sp
-    b_b = 4.0 * wl.C_out if wl.bias else 0.0
+    x_b = float(esize) * wl.N * wl.C_in * int(np.prod(wl.in_dims))
+    w_b = float(esize) * wl.C_out * wl.C_in * k_sp
+    b_b = float(esize) * wl.C_out if wl.bias else 0.0
     if wl.kind == "fused":
-        y_b = 4.0 * wl.N * wl.C_out * out_dims[1] * out_dims[2]
+        y_b = float(esize) * wl.N * wl.C_out * out_dims[1] * out_dims[2]
     else:
-        y_b = 4.0 * wl.N * wl.C_out * out_sp
+        y_b = float(esize) * wl.N * wl.C_out * out_sp
     return flops, x_b + w_b + b_b + y_b, x_b + w_b + b_b, y_b
 
 
@@ -191,10 +191,11 @@ class OurRunner:
     def timed_e2e(self, steps, warmup):
         """Same call with H2D of the step's inputs (pinned) and D2H of its output inside the timing."""
         torch = self.torch
-        hx = torch.from_numpy(self.host["x"]).pin_memory()
-        hw = torch.from_numpy(self.host["w"]).pin_memory()
-        hb = None if self.host["b"] is None else torch.from_numpy(self.host["b"]).pin_memory()
-        hy = torch.empty(self.y.shape, dtype=torch.float32).pin_memory()
+        # host copies in the device tensors' dtype (the call's own input type)
+        hx = torch.from_numpy(self.host["x"]).to(self.x.dtype).pin_memory()
+        hw = torch.from_numpy(self.host["w"]).to(self.w.dtype).pin_memory()
+        hb = None if self.host["b"] is None else torch.from_numpy(self.host["b"]).to(self.b.dtype).pin_memory()
+        hy = torch.empty(self.y.shape, dtype=self.y.dtype).pin_memory()
 
         def one():
             self.x.copy_(hx, non_blocking=True)
@@ -213,8 +214,8 @@ class OurRunner:
             one()
         e.record(self.stream)
         torch.cuda.synchronize()
-        h2d = hx.numel() * 4 + hw.numel() * 4 + (0 if hb is None else hb.numel() * 4)
-        return s.elapsed_time(e) / steps, h2d, hy.numel() * 4
+        nbytes = lambda t: 0 if t is None else t.numel() * t.element_size()
+        return s.elapsed_time(e) / steps, nbytes(hx) + nbytes(hw) + nbytes(hb), nbytes(hy)
 
 
 class VariantRunner(OurRunner):
@@ -271,6 +272,11 @@ VARIANTS = [
 ]
 
 
+def cf_workspace_needed(r):
+    wl = r.wl
+    return r.cf.workspace_bytes(wl.N, wl.C_in, wl.C_out, wl.in_dims, wl.k_dims, wl.stride, wl.pad, wl.dilation) > 0
+
+
 def run_variants(dev, peaks, steps):
     """ms and throughput of each VARIANTS entry (CUDA events, L2 flushed, median)."""
     import torch
@@ -301,7 +307,9 @@ def run_variants(dev, peaks, steps):
 # changed since, the figure no longer describes the kernel and is reported as
 # null.  "batch" is the batch of the captured case: traffic is scaled by
 # N / batch when the capture used a smaller batch (traffic grows in proportion).
-KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "direct_ffma": "direct.cu", "fused_ffma": "fused.cu"}
+KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "igemm_tcgen05.cu",
+                 "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
+                 "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
     ("igemm_3xtf32", "conv3d_asym"): {
         "bytes": 50.635520e6 + 826.322432e6, "batch": 16,
@@ -334,13 +342,16 @@ def traffic_for(algo, wl):
 def roofline_for(runner, peaks, ms, sustained=False):
     """Roofline entry for the one kernel a step launches."""
     wl = runner.wl
-    flops, bytes_alg, _, _ = problem_counts(wl, runner.out_dims)
+    flops, bytes_alg, _, _ = problem_counts(wl, runner.out_dims, runner.y.element_size())
     t = ms * 1e-3
     hbm_peak = peaks["hbm_gbs"]
-    if runner.algo == "igemm_3xtf32":
+    if runner.algo in ("igemm_3xtf32", "igemm_3xtf32_streamed"):
         bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
         peak = bf16 * BF16_TO_TF32 / 3.0  # three TF32 products per fp32 MAC
         compute = {"bound": "tensor", "peak": peak, "peak_note": "TF32 = measured bf16 x 1.1/2.25, /3 for 3xTF32"}
+    elif runner.algo in ("igemm_bf16", "igemm_fp16"):
+        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
+        compute = {"bound": "tensor", "peak": peak, "peak_note": "measured dense bf16 (fp16 the same rate)"}
     else:
         peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12
         compute = {"bound": "alu", "peak": peak, "peak_note": "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"}
@@ -444,6 +455,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the workload's batch size (small cases for profiler captures)")
+    ap.add_argument("--dtype", choices=["f32", "bf16", "fp16"], default="f32",
+                    help="run the workload on 16-bit tensors (the 16-bit tensor-core entry points)")
+    ap.add_argument("--workspace", action="store_true",
+                    help="run the workload through conv_fwd_nd_ws (streamed weights when they exceed shared memory)")
     args = ap.parse_args()
     rank, world, local = env_rank()
     wl = synth.WORKLOADS[args.workload]
@@ -464,8 +479,16 @@ def main():
     __graft_entry__.build()
     peaks, peaks_src = load_peaks()
 
-    runner = OurRunner(wl, dev)
-    flops, bytes_alg, in_b, out_b = problem_counts(wl, runner.out_dims)
+    if args.dtype != "f32" or args.workspace:
+        dt = {"f32": None, "bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
+        runner = VariantRunner(wl, dev, dtype=dt, workspace=args.workspace)
+        if dt is not None:
+            runner.algo = "igemm_" + args.dtype
+        elif runner.ws is not None and cf_workspace_needed(runner):
+            runner.algo = "igemm_3xtf32_streamed"
+    else:
+        runner = OurRunner(wl, dev)
+    flops, bytes_alg, in_b, out_b = problem_counts(wl, runner.out_dims, runner.y.element_size())
     # warm-up, then EXACTLY K timed steps bracketed by barrier + synchronize
     runner.timed(0, args.warmup)
     if world > 1:
@@ -522,7 +545,7 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "GFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded counter-based generator)",
+            "vs_baseline": None, "dtype": args.dtype, "data": "synthetic (seeded counter-based generator)",
             "config": {"workload": wl.name, "description": wl.description, "global_batch": wl.N * world,
                        "in_dims": list(wl.in_dims), "k_dims": list(wl.k_dims), "C_in": wl.C_in, "C_out": wl.C_out,
                        "stride": list(wl.stride), "pad": list(wl.pad), "dilation": list(wl.dilation),
