@@ -312,14 +312,20 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
     ("igemm_3xtf32", "conv3d_asym"): {
-        "bytes": 50.635520e6 + 826.322432e6, "batch": 16,
-        "sha256": "3d88fa5260360d22cb4b8ae54d65ba4b10a5d8eb47a2fe5826c747846380e5fe"},
+        "bytes": 50.513152e6 + 825.599488e6, "batch": 16,
+        "sha256": "60af4ea4545ab83a5906cf4a935e2df02f3acf1d550a467fbc4a5481ba6dd214"},
     ("igemm_3xtf32", "conv1d_long"): {
-        "bytes": 537.242112e6 + 307.349248e6, "batch": 4,
-        "sha256": "3d88fa5260360d22cb4b8ae54d65ba4b10a5d8eb47a2fe5826c747846380e5fe"},
+        "bytes": 537.251584e6 + 307.757568e6, "batch": 4,
+        "sha256": "60af4ea4545ab83a5906cf4a935e2df02f3acf1d550a467fbc4a5481ba6dd214"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {
+        "bytes": 35.405824e6 + 7.943936e6, "batch": 4,
+        "sha256": "60af4ea4545ab83a5906cf4a935e2df02f3acf1d550a467fbc4a5481ba6dd214"},
+    ("igemm_bf16", "conv3d_asym"): {
+        "bytes": 25.287424e6 + 385.313536e6, "batch": 16,
+        "sha256": "45b54c1a27cbf949cc78b634c582c4b25fb1a10c205e156f901a31a26acb6e2f"},
     ("fused_ffma", "conv3d_min_softmax"): {
-        "bytes": 37.814784e6 + 0.002560e6, "batch": 128,
-        "sha256": "bcf69ed2bfb05ba33c1044831a013c839217635f640eff81a3c71aec63fd6fe9"},
+        "bytes": 37.816320e6 + 0.001792e6, "batch": 128,
+        "sha256": "a3c8d352595b1412f32ddeb3d8a71383c322d0155fb883f3a6335d030c445a9c"},
 }
 
 
