@@ -120,6 +120,134 @@ __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParam
   }
 }
 
+// Depthwise-style groups (one input channel per group, fewer than kCO output
+// channels per group): the channel tile above would leave most of its lanes
+// idle, so each thread here computes kR consecutive outputs of one output
+// channel, reading that channel's taps through the read-only cache.  Grid:
+// one 1-D range per (n, output channel) plane, blocks_per_plane blocks each.
+__global__ void __launch_bounds__(kThreads) depthwise_kernel(const DirectParams p, int64_t items_per_plane,
+                                                             int64_t blocks_per_plane) {
+  const Geom &g = p.g;
+  const int64_t plane = blockIdx.x / blocks_per_plane;  // n * (G * K) + oc
+  const int64_t item = (blockIdx.x - plane * blocks_per_plane) * kThreads + threadIdx.x;
+  if (item >= items_per_plane) return;
+  const int64_t GK = g.G * g.K;
+  const int64_t n = plane / GK;
+  const int64_t oc = plane - n * GK;
+  const int64_t grp = oc / g.K;  // its input channel (one per group)
+  int64_t rest = item;
+  const int owg = (int)(rest % p.owg);
+  rest /= p.owg;
+  const int oh = (int)(rest % g.OH);
+  const int od = (int)(rest / g.OH);
+  const int ow0 = owg * kR;
+  const int taps = g.KD * g.KH * g.KW;
+  const int64_t HW = (int64_t)g.H * g.W;
+  const float *xc = p.x + n * g.x_batch_stride() + grp * g.C * g.D * HW;
+  const float *wo = p.w + oc * taps;
+  const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+  float acc[kR];
+#pragma unroll
+  for (int r = 0; r < kR; ++r) acc[r] = 0.f;
+  for (int kd = 0; kd < g.KD; ++kd) {
+    const int id = od * g.SD + kd * g.DD - g.PD;
+    if ((unsigned)id >= (unsigned)g.D) continue;
+    for (int kh = 0; kh < g.KH; ++kh) {
+      const int ih = oh * g.SH + kh * g.DH - g.PH;
+      if ((unsigned)ih >= (unsigned)g.H) continue;
+      const float *row = xc + (int64_t)id * HW + (int64_t)ih * g.W;
+      const float *wt = wo + (kd * g.KH + kh) * g.KW;
+      for (int kw = 0; kw < g.KW; ++kw) {
+        const float wv = __ldg(wt + kw);
+#pragma unroll
+        for (int r = 0; r < kR; ++r) {
+          const int iw = (ow0 + r) * g.SW + kw * g.DW - g.PW;
+          if ((unsigned)iw < (unsigned)g.W) acc[r] = fmaf(wv, __ldg(row + iw), acc[r]);
+        }
+      }
+    }
+  }
+  float *yo = p.y + n * g.y_batch_stride() + oc * g.out_spatial() + ((int64_t)od * g.OH + oh) * g.OW;
+#pragma unroll
+  for (int r = 0; r < kR; ++r)
+    if (ow0 + r < g.OW) yo[ow0 + r] = acc[r] + b;
+}
+
+// Depthwise-style groups with stride 1 and dilation 1 (the common case): a
+// block computes a 4 x 8 x 32 output tile of one (n, output channel) plane
+// from its input tile staged in shared memory (zero padding filled in), each
+// thread 4 consecutive outputs along W; every input value is read from global
+// memory once per tile instead of once per tap.
+constexpr int kDwTD = 4, kDwTH = 8, kDwTW = 32, kDwMaxK = 7;
+constexpr int kDwThreads = kDwTD * kDwTH * (kDwTW / kR);  // 256
+constexpr int kDwTile = (kDwTD + kDwMaxK - 1) * (kDwTH + kDwMaxK - 1) * (kDwTW + kDwMaxK - 1);
+
+__global__ void __launch_bounds__(kDwThreads) depthwise_tiled_kernel(const DirectParams p, int tiles_d, int tiles_h,
+                                                                     int tiles_w) {
+  __shared__ float xs[kDwTile];
+  __shared__ float ws[kDwMaxK * kDwMaxK * kDwMaxK];
+  const Geom &g = p.g;
+  const int64_t tiles = (int64_t)tiles_d * tiles_h * tiles_w;
+  const int64_t plane = blockIdx.x / tiles;  // n * (G * K) + oc
+  int64_t tl = blockIdx.x - plane * tiles;
+  const int tw = (int)(tl % tiles_w);
+  tl /= tiles_w;
+  const int th = (int)(tl % tiles_h);
+  const int td = (int)(tl / tiles_h);
+  const int64_t GK = g.G * g.K;
+  const int64_t n = plane / GK;
+  const int64_t oc = plane - n * GK;
+  const int64_t grp = oc / g.K;
+  const int taps = g.KD * g.KH * g.KW;
+  const int64_t HW = (int64_t)g.H * g.W;
+  const float *xc = p.x + n * g.x_batch_stride() + grp * g.C * g.D * HW;
+  // input tile origin and extents (stride 1, dilation 1)
+  const int d0 = td * kDwTD - g.PD, h0 = th * kDwTH - g.PH, w0 = tw * kDwTW - g.PW;
+  const int ID = kDwTD + g.KD - 1, IH = kDwTH + g.KH - 1, IW = kDwTW + g.KW - 1;
+  // rows of the input tile, 4 at a time, 64 columns per row per pass (IW <= 38)
+  for (int r = threadIdx.x >> 6; r < ID * IH; r += kDwThreads >> 6) {
+    const int id = r / IH, ih = r - id * IH;
+    const int d = d0 + id, h = h0 + ih;
+    const bool row_in = (unsigned)d < (unsigned)g.D && (unsigned)h < (unsigned)g.H;
+    const float *src = xc + (int64_t)d * HW + (int64_t)h * g.W;
+    const int iw = threadIdx.x & 63;
+    if (iw < IW) {
+      const int w = w0 + iw;
+      xs[r * IW + iw] = (row_in && (unsigned)w < (unsigned)g.W) ? __ldg(src + w) : 0.f;
+    }
+  }
+  for (int i = threadIdx.x; i < taps; i += kDwThreads) ws[i] = __ldg(p.w + oc * taps + i);
+  __syncthreads();
+  const int t = threadIdx.x;
+  const int lw = (t % (kDwTW / kR)) * kR, lh = (t / (kDwTW / kR)) % kDwTH, ld = t / ((kDwTW / kR) * kDwTH);
+  const int od = td * kDwTD + ld, oh = th * kDwTH + lh, ow0 = tw * kDwTW + lw;
+  if (od >= g.OD || oh >= g.OH || ow0 >= g.OW) return;
+  float acc[kR];
+#pragma unroll
+  for (int r = 0; r < kR; ++r) acc[r] = 0.f;
+  for (int kd = 0; kd < g.KD; ++kd)
+    for (int kh = 0; kh < g.KH; ++kh) {
+      const float *row = xs + ((ld + kd) * IH + (lh + kh)) * IW + lw;
+      const float *wt = ws + (kd * g.KH + kh) * g.KW;
+      float xv[kR + kDwMaxK - 1];
+#pragma unroll
+      for (int j = 0; j < kR + kDwMaxK - 1; ++j)
+        if (j < kR + g.KW - 1) xv[j] = row[j];
+#pragma unroll
+      for (int kw = 0; kw < kDwMaxK; ++kw) {
+        if (kw >= g.KW) break;
+        const float wv = wt[kw];
+#pragma unroll
+        for (int r = 0; r < kR; ++r) acc[r] = fmaf(wv, xv[r + kw], acc[r]);
+      }
+    }
+  const float b = p.bias ? __ldg(p.bias + oc) : 0.f;
+  float *yo = p.y + n * g.y_batch_stride() + oc * g.out_spatial() + ((int64_t)od * g.OH + oh) * g.OW;
+#pragma unroll
+  for (int r = 0; r < kR; ++r)
+    if (ow0 + r < g.OW) yo[ow0 + r] = acc[r] + b;
+}
+
 }  // namespace
 
 bool direct_supported(const Geom &g, const char **why) {
@@ -132,6 +260,14 @@ bool direct_supported(const Geom &g, const char **why) {
     return false;
   }
   const int64_t items = g.N * (int64_t)g.OD * g.OH * ((g.OW + kR - 1) / kR);
+  if (g.C == 1 && g.K < kCO) {
+    const int64_t per_plane = ((int64_t)g.OD * g.OH * ((g.OW + kR - 1) / kR) + kThreads - 1) / kThreads;
+    if (g.N * g.G * g.K * per_plane > 0x7fffffff) {
+      *why = "direct path: too many output blocks for one depthwise grid";
+      return false;
+    }
+    return true;
+  }
   if ((items + kThreads - 1) / kThreads > 0x7fffffff) {
     *why = "direct path: too many output rows for one grid";
     return false;
@@ -148,6 +284,23 @@ cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias
   p.y = y;
   p.g = g;
   p.owg = (g.OW + kR - 1) / kR;
+  const bool unit = g.SD == 1 && g.SH == 1 && g.SW == 1 && g.DD == 1 && g.DH == 1 && g.DW == 1;
+  // the tiled kernel when a tile row is mostly used (output width >= 24)
+  if (g.C == 1 && g.K < kCO && unit && g.KD <= kDwMaxK && g.KH <= kDwMaxK && g.KW <= kDwMaxK && g.OW >= 24) {
+    const int td = (g.OD + kDwTD - 1) / kDwTD, th = (g.OH + kDwTH - 1) / kDwTH, tw = (g.OW + kDwTW - 1) / kDwTW;
+    const int64_t blocks = g.N * g.G * g.K * (int64_t)td * th * tw;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    depthwise_tiled_kernel<<<(unsigned)blocks, kDwThreads, 0, stream>>>(p, td, th, tw);
+    return cudaGetLastError();
+  }
+  if (g.C == 1 && g.K < kCO) {
+    const int64_t items = (int64_t)g.OD * g.OH * p.owg;
+    const int64_t bpp = (items + kThreads - 1) / kThreads;
+    const int64_t blocks = g.N * g.G * g.K * bpp;
+    if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    depthwise_kernel<<<(unsigned)blocks, kThreads, 0, stream>>>(p, items, bpp);
+    return cudaGetLastError();
+  }
   p.items = g.N * (int64_t)g.OD * g.OH * p.owg;
   const int taps = g.taps();
   p.cchunk = (int)(g.C < kSmemFloats / (taps * kCO) ? g.C : kSmemFloats / (taps * kCO));

@@ -573,3 +573,17 @@ def test_streamed_weights_workspace(C_in, C_out, k, pad, groups):
     with pytest.raises(cf.ConvError) as e:
         cf.conv_fwd_nd_ws(xt, wt, bt, s, pad, d, workspace=ws[:need // 2], groups=groups)
     assert e.value.status == cf.CONV_ERR_ARG
+
+
+@pytest.mark.parametrize("C,mult,ins,k,pad", [
+    (16, 1, (9, 13, 37), (3, 3, 3), (1, 1, 1)),   # tiles cut by every output edge
+    (8, 3, (5, 17, 70), (3, 5, 7), (1, 2, 3)),    # channel multiplier 3, a 3x5x7 kernel
+    (4, 1, (3, 4, 5), (1, 1, 1), (0, 0, 0)),      # 1x1x1 depthwise: a per-channel scale plus bias
+])
+def test_depthwise_3d_tiled(C, mult, ins, k, pad):
+    rng = np.random.default_rng(C * 11 + mult)
+    x = rng.standard_normal((2, C) + ins).astype(np.float32)
+    w = rng.standard_normal((C * mult, 1) + k).astype(np.float32)
+    b = rng.standard_normal(C * mult).astype(np.float32)
+    ref = oracle.conv_nd(x, w, b, (1, 1, 1), pad, (1, 1, 1), groups=C)
+    assert_close(run_grouped(x, w, b, (1, 1, 1), pad, (1, 1, 1), C), ref, f"depthwise 3-D C={C} x{mult} k={k}")
