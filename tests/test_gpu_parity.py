@@ -587,3 +587,46 @@ def test_depthwise_3d_tiled(C, mult, ins, k, pad):
     b = rng.standard_normal(C * mult).astype(np.float32)
     ref = oracle.conv_nd(x, w, b, (1, 1, 1), pad, (1, 1, 1), groups=C)
     assert_close(run_grouped(x, w, b, (1, 1, 1), pad, (1, 1, 1), C), ref, f"depthwise 3-D C={C} x{mult} k={k}")
+
+
+# ------------------------------------------ empty batches and side streams
+
+def test_empty_batch_every_entry_point():
+    x = torch.empty((0, 8, 6, 7, 9), device="cuda")
+    w = torch.randn((16, 4, 3, 3, 3), device="cuda")
+    assert tuple(cf.conv_fwd_nd(x, w, None, 1, 1, 1, groups=2).shape) == (0, 16, 6, 7, 9)
+    xcl = x.to(memory_format=torch.channels_last_3d)
+    wcl = torch.randn((16, 8, 3, 3, 3), device="cuda").to(memory_format=torch.channels_last_3d)
+    assert tuple(cf.conv_fwd_nd(xcl, wcl, None, 1, 1, 1, channels_last=True).shape) == (0, 16, 6, 7, 9)
+    xh, wh = x.to(torch.bfloat16), w.to(torch.bfloat16)
+    assert tuple(cf.conv_fwd_nd(xh, wh, None, 1, 1, 1, groups=2).shape) == (0, 16, 6, 7, 9)
+    wbig = torch.randn((64, 8, 7, 7, 7), device="cuda")
+    assert tuple(cf.conv_fwd_nd_ws(x, wbig, None, 1, 3, 1).shape) == (0, 64, 6, 7, 9)
+    xf = torch.empty((0, 3, 5, 8, 8), device="cuda")
+    wf = torch.randn((24, 3, 3, 3, 3), device="cuda")
+    for md in (2, 3, 4):
+        y = cf.conv3d_min_softmax(xf, wf, None, md)
+        assert y.shape[0] == 0 and y.shape[1] == 24
+
+
+def test_side_stream_matches_default_stream_for_each_family():
+    rng = np.random.default_rng(31)
+    x = torch.from_numpy(rng.standard_normal((2, 16, 6, 9, 10)).astype(np.float32)).cuda()
+    w = torch.from_numpy(((rng.random((32, 16, 3, 3, 3)) - 0.5) * 0.1).astype(np.float32)).cuda()
+    wide = torch.from_numpy(((rng.random((64, 64, 3, 3, 3)) - 0.5) * 0.05).astype(np.float32)).cuda()
+    xw = torch.from_numpy(rng.standard_normal((2, 64, 5, 8, 9)).astype(np.float32)).cuda()
+    calls = [
+        lambda st: cf.conv_fwd_nd(x, w, None, 1, 1, 1, algo=cf.CONV_ALGO_IGEMM_3XTF32, stream=st),
+        lambda st: cf.conv_fwd_nd(x, w, None, 1, 1, 1, algo=cf.CONV_ALGO_DIRECT_FFMA, stream=st),
+        lambda st: cf.conv_fwd_nd(x.to(torch.bfloat16), w.to(torch.bfloat16), None, 1, 1, 1, stream=st),
+        lambda st: cf.conv_fwd_nd_ws(xw, wide, None, 1, 1, 1, stream=st),
+        lambda st: cf.conv_fwd_nd(x, w[:, :4].contiguous(), None, 1, 1, 1, groups=4, stream=st),
+    ]
+    st = torch.cuda.Stream()
+    for call in calls:
+        ref = call(None)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(st):
+            got = call(st)
+        st.synchronize()
+        assert torch.equal(got, ref)
