@@ -198,7 +198,7 @@ const char *conv_status_string(int status) {
     case CONV_ERR_NULL: return "CONV_ERR_NULL: a required pointer is NULL";
     case CONV_ERR_ARG: return "CONV_ERR_ARG: argument out of range or misaligned";
     case CONV_ERR_SHAPE: return "CONV_ERR_SHAPE: non-positive output size or inconsistent shapes";
-    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED: valid request not implemented by this build";
+    case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED: valid request not implemented by this library";
     case CONV_ERR_CUDA: return "CONV_ERR_CUDA: CUDA runtime error";
     default: return "unknown conv status";
   }

@@ -51,7 +51,7 @@ typedef enum {
   CONV_ERR_NULL = 1,        /* a required pointer is NULL */
   CONV_ERR_ARG = 2,         /* a size/hyper-parameter is out of range, or a pointer is misaligned */
   CONV_ERR_SHAPE = 3,       /* an output size is <= 0, or descriptor shapes disagree */
-  CONV_ERR_UNSUPPORTED = 4, /* valid request that this build does not implement */
+  CONV_ERR_UNSUPPORTED = 4, /* valid request that this library does not implement */
   CONV_ERR_CUDA = 5         /* a CUDA runtime call failed (see conv_last_error) */
 } conv_status_t;
 
