@@ -282,9 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         ptx::mbar_arrive(bar_a_full + 8 * stage);
       }
     }
-  } else if (lane == 0 && warp - kMmaWarp < nslots) {
+  } else if (warp >= kMmaWarp && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
-    const int slot = warp - kMmaWarp;
+    // the whole warp runs the loop (warp-uniform values); one elected lane issues
+    const int slot = __shfl_sync(0xffffffffu, warp - kMmaWarp, 0);
     const uint32_t idesc = HALF ? ptx::idesc_f16(kTileM, (uint32_t)p.Npad) : ptx::idesc_bf16(kTileM, (uint32_t)p.Npad);
     const uint32_t bsa = ptx::smem_addr(b_s);
     const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
@@ -292,33 +293,40 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
       const int64_t li = it / nslots;
-      if (!wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t lg = li * p.nchunks + q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
-        if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag)) {
+        if (!__all_sync(0xffffffffu, wait_phase(bar_a_full + 8 * s, r & 1, abort_flag))) {
           aborted = true;
           break;
         }
         ptx::tc_fence_after();
         const uint32_t a = tmem + a_col0 + 16u * s;
+        if (ptx::elect_one()) {
 #pragma unroll
-        for (int ks = 0; ks < kBfChunk / 16; ++ks) {
-          const uint32_t kbyte = (uint32_t)((q * kBfChunk + ks * 16) / 8) * 128u;  // core matrices along K
-          const uint64_t bd = ptx::smem_desc_noswizzle(bsa + kbyte, 128, SBO);
-          ptx::mma_f16_ts(d_tmem, a + 8u * ks, bd, idesc, (q | ks) != 0);
+          for (int ks = 0; ks < kBfChunk / 16; ++ks) {
+            const uint32_t kbyte = (uint32_t)((q * kBfChunk + ks * 16) / 8) * 128u;  // core matrices along K
+            const uint64_t bd = ptx::smem_desc_noswizzle(bsa + kbyte, 128, SBO);
+            ptx::mma_f16_ts(d_tmem, a + 8u * ks, bd, idesc, (q | ks) != 0);
+          }
+          ptx::mma_commit(bar_a_empty + 8 * s);
         }
-        ptx::mma_commit(bar_a_empty + 8 * s);
+        __syncwarp();
       }
       if (aborted) break;
-      ptx::mma_commit(bar_d_full + 8 * slot);
+      if (ptx::elect_one()) ptx::mma_commit(bar_d_full + 8 * slot);
+      __syncwarp();
     }
     if (*abort_flag) {
-      ptx::mma_commit(bar_drain);
-      const long long t0 = clock64();
-      while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+      if (ptx::elect_one()) {
+        ptx::mma_commit(bar_drain);
+        const long long t0 = clock64();
+        while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+        }
       }
+      __syncwarp();
     }
   }
 

@@ -174,19 +174,26 @@ __device__ __forceinline__ int64_t cta_tile_count(const IgemmParams &p) {
 }
 
 // Bounded mbarrier wait.  Returns false (and raises the abort flag plus the
-// device status bit on timeout) when the phase did not complete.
-__device__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
+// device status bit on timeout) when the phase did not complete.  The first
+// test is inline; the polling loop, which reads the abort flag and the clock
+// every 16 polls, is out of line so that the roles' loops stay short.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
   const long long t0 = clock64();
-  for (;;) {
+  for (uint32_t i = 1;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      *abort_flag = 1;
-      atomicOr(&g_device_status, kStatusIgemmWatchdog);
-      return false;
+    if ((i & 15u) == 0) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        *abort_flag = 1;
+        atomicOr(&g_device_status, kStatusIgemmWatchdog);
+        return false;
+      }
     }
   }
+}
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  return wait_phase_slow(bar, parity, abort_flag);
 }
 
 __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_uint(v) & 0xffffe000u; }
@@ -624,13 +631,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       while (!ptx::mbar_try_wait(bar_b_full + 8 * sb_last_stage, sb_last_parity) && clock64() - t0 < kWaitLimitCycles) {
       }
     }
-  } else if (lane == 0 && warp - kMmaWarp < nslots) {
+  } else if (warp >= kMmaWarp && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
-    // One thread per slot, in warps on different SM sub-partitions: a thread
-    // cannot issue a tcgen05.mma much faster than one per ~140 cycles, so the
-    // slots keep two or four instruction streams (tiles) in flight.
+    // One warp per slot, on different SM sub-partitions: a thread cannot issue
+    // a tcgen05.mma much faster than one per ~140 cycles, so the slots keep
+    // two or four instruction streams (tiles) in flight.  The whole warp runs
+    // the loop (its values stay warp-uniform); one elected lane issues.
     // Per K-step: D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi.
-    const int slot = warp - kMmaWarp;
+    const int slot = __shfl_sync(0xffffffffu, warp - kMmaWarp, 0);
     const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
     const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
     const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
@@ -638,13 +646,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
       const int64_t li = it / nslots;
-      if (!wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag)) break;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t lg = li * p.nchunks + q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
-        if (!wait_phase(bar_a_full + 8 * s, r & 1, abort_flag) ||
-            (SB && !wait_phase(bar_b_full + 8 * s, r & 1, abort_flag))) {
+        bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag);
+        if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) {
           aborted = true;
           break;
         }
@@ -655,27 +664,34 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         const int ksteps = min(p.KC, p.Kpad - k0) / 8;
         // streamed: the stage holds chunk q only (hi, then lo), 8-row groups KC * 32 bytes apart
         const uint32_t sb_hi = bhi + s * p.sb_stage_bytes, sb_lo = sb_hi + p.sb_stage_bytes / 2;
-        for (int ks = 0; ks < ksteps; ++ks) {
-          const uint32_t kbyte = (uint32_t)(k0 + ks * 8) * 32u;  // (k/4) core matrices of 128 B
-          const uint64_t dh = SB ? ptx::smem_desc_noswizzle(sb_hi + 256u * ks, 128, (uint32_t)p.KC * 32)
-                                 : ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
-          const uint64_t dl = SB ? ptx::smem_desc_noswizzle(sb_lo + 256u * ks, 128, (uint32_t)p.KC * 32)
-                                 : ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
-          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (q | ks) != 0);
-          ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
-          ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
+        if (ptx::elect_one()) {
+          for (int ks = 0; ks < ksteps; ++ks) {
+            const uint32_t kbyte = (uint32_t)(k0 + ks * 8) * 32u;  // (k/4) core matrices of 128 B
+            const uint64_t dh = SB ? ptx::smem_desc_noswizzle(sb_hi + 256u * ks, 128, (uint32_t)p.KC * 32)
+                                   : ptx::smem_desc_noswizzle(bhi + kbyte, 128, SBO);
+            const uint64_t dl = SB ? ptx::smem_desc_noswizzle(sb_lo + 256u * ks, 128, (uint32_t)p.KC * 32)
+                                   : ptx::smem_desc_noswizzle(blo + kbyte, 128, SBO);
+            ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (q | ks) != 0);
+            ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
+            ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
+          }
+          ptx::mma_commit(bar_a_empty + 8 * s);
         }
-        ptx::mma_commit(bar_a_empty + 8 * s);
+        __syncwarp();
       }
       if (aborted) break;
-      ptx::mma_commit(bar_d_full + 8 * slot);
+      if (ptx::elect_one()) ptx::mma_commit(bar_d_full + 8 * slot);
+      __syncwarp();
     }
     if (*abort_flag) {
-      // drain: every MMA this thread issued completes before TMEM is released
-      ptx::mma_commit(bar_drain);
-      const long long t0 = clock64();
-      while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+      // drain: every MMA this warp issued completes before TMEM is released
+      if (ptx::elect_one()) {
+        ptx::mma_commit(bar_drain);
+        const long long t0 = clock64();
+        while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+        }
       }
+      __syncwarp();
     }
   }
 
