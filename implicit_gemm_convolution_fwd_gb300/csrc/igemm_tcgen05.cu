@@ -508,36 +508,17 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
           }
         }
       };
-      // With 16-column producer chunks there are registers to read 64
-      // accumulator columns before releasing the accumulator, which lets the
-      // slot's next tile start sooner; otherwise 32 at a time.
-      if (CH == 16) {
-        for (int c0 = 0; c0 < p.Npad; c0 += 64) {
-          uint32_t v[64];
-          const bool two = c0 + 32 < p.Npad;
-          ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, *reinterpret_cast<uint32_t (*)[32]>(v));
-          if (two) ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0 + 32, *reinterpret_cast<uint32_t (*)[32]>(v + 32));
-          ptx::tmem_wait_ld();
-          if (c0 + 64 >= p.Npad) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_d_empty + 8 * b);
-          }
-          if (valid) {
-            store32(*reinterpret_cast<const uint32_t (*)[32]>(v), c0);
-            if (two) store32(*reinterpret_cast<const uint32_t (*)[32]>(v + 32), c0 + 32);
-          }
+      // 32 accumulator columns at a time; the accumulator is released after
+      // the last read, before the last stores.
+      for (int c0 = 0; c0 < p.Npad; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
+        ptx::tmem_wait_ld();
+        if (c0 + 32 >= p.Npad) {
+          ptx::tc_fence_before();
+          ptx::mbar_arrive(bar_d_empty + 8 * b);
         }
-      } else {
-        for (int c0 = 0; c0 < p.Npad; c0 += 32) {
-          uint32_t v[32];
-          ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
-          ptx::tmem_wait_ld();
-          if (c0 + 32 >= p.Npad) {
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar_d_empty + 8 * b);
-          }
-          if (valid) store32(v, c0);
-        }
+        if (valid) store32(v, c0);
       }
     }
   } else if (warp < kMmaWarp) {
@@ -593,16 +574,19 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 #pragma unroll
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
-          uint32_t tmp[kUnit];
 #pragma unroll
-          for (int j = 0; j < kUnit; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + j]);
-          ptx::tmem_st16(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit), tmp);
+          for (int h = 0; h < kUnit; h += 8) {
+            uint32_t tmp[8];
 #pragma unroll
-          for (int j = 0; j < kUnit; j += 2)
-            ptx::sub_f32x2(v[u * kUnit + j], v[u * kUnit + j + 1], __uint_as_float(tmp[j]),
-                           __uint_as_float(tmp[j + 1]), v[u * kUnit + j], v[u * kUnit + j + 1]);
-          ptx::tmem_st16(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit),
-                         *reinterpret_cast<const uint32_t (*)[kUnit]>(v + u * kUnit));
+            for (int j = 0; j < 8; ++j) tmp[j] = tf32_hi_bits(v[u * kUnit + h + j]);
+            ptx::tmem_st8(tmem + lane_base + a_hi_col + (uint32_t)(u * kUnit + h), tmp);
+#pragma unroll
+            for (int j = 0; j < 8; j += 2)
+              ptx::sub_f32x2(v[u * kUnit + h + j], v[u * kUnit + h + j + 1], __uint_as_float(tmp[j]),
+                             __uint_as_float(tmp[j + 1]), v[u * kUnit + h + j], v[u * kUnit + h + j + 1]);
+            ptx::tmem_st8(tmem + lane_base + a_lo_col + (uint32_t)(u * kUnit + h),
+                          *reinterpret_cast<const uint32_t (*)[8]>(v + u * kUnit + h));
+          }
         }
       }
       ptx::tmem_wait_st();
