@@ -312,17 +312,17 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
     ("igemm_3xtf32", "conv3d_asym"): {
-        "bytes": 50.513152e6 + 825.599488e6, "batch": 16,
-        "sha256": "60af4ea4545ab83a5906cf4a935e2df02f3acf1d550a467fbc4a5481ba6dd214"},
+        "bytes": 50.514944e6 + 824.356864e6, "batch": 16,
+        "sha256": "5cd77b48a8b388bf116e8401e41aa729374868ada2cfe8c8f47a541570ee040b"},
     ("igemm_3xtf32", "conv1d_long"): {
-        "bytes": 537.251584e6 + 307.757568e6, "batch": 4,
-        "sha256": "60af4ea4545ab83a5906cf4a935e2df02f3acf1d550a467fbc4a5481ba6dd214"},
+        "bytes": 537.358848e6 + 307.654400e6, "batch": 4,
+        "sha256": "5cd77b48a8b388bf116e8401e41aa729374868ada2cfe8c8f47a541570ee040b"},
     ("igemm_3xtf32_streamed", "conv3d_wide_k"): {
-        "bytes": 35.405824e6 + 7.943936e6, "batch": 4,
-        "sha256": "60af4ea4545ab83a5906cf4a935e2df02f3acf1d550a467fbc4a5481ba6dd214"},
+        "bytes": 35.452416e6 + 7.261952e6, "batch": 4,
+        "sha256": "5cd77b48a8b388bf116e8401e41aa729374868ada2cfe8c8f47a541570ee040b"},
     ("igemm_bf16", "conv3d_asym"): {
-        "bytes": 25.287424e6 + 385.313536e6, "batch": 16,
-        "sha256": "45b54c1a27cbf949cc78b634c582c4b25fb1a10c205e156f901a31a26acb6e2f"},
+        "bytes": 25.291008e6 + 385.082368e6, "batch": 16,
+        "sha256": "774361edea968caa26c5e257fce9aa06e9f7e958be7eda241bbff529ac6a793f"},
     ("fused_ffma", "conv3d_min_softmax"): {
         "bytes": 37.816320e6 + 0.001792e6, "batch": 128,
         "sha256": "a3c8d352595b1412f32ddeb3d8a71383c322d0155fb883f3a6335d030c445a9c"},
