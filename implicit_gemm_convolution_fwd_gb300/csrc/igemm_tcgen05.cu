@@ -594,12 +594,37 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::mbar_arrive(bar_a_full + 8 * stage);
       return true;
     };
+    // full chunks of a warp whose receptive fields are all inside the input:
+    // four offsets per shared load, no tests
+    auto gather_full = [&](const PosInfo &ps, int q, float (&v)[CH]) {
+      const int4 *o4 = reinterpret_cast<const int4 *>(toff + q * CH);
+#pragma unroll
+      for (int i = 0; i < CH / 4; ++i) {
+        const int4 o = o4[i];
+        v[4 * i + 0] = __ldg(ps.xo + o.x);
+        v[4 * i + 1] = __ldg(ps.xo + o.y);
+        v[4 * i + 2] = __ldg(ps.xo + o.z);
+        v[4 * i + 3] = __ldg(ps.xo + o.w);
+      }
+    };
+    const int nfull = (CH == 16 && p.KC == CH && !p.vec4) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
       const int64_t lg0 = li * p.nchunks;  // slot-local index of the tile's first chunk
       // this group's chunks of the tile: lg = lg0 + q with lg = sel (mod gps)
       int q = (int)((sel - lg0 % gps + gps) % gps);
+      if (CH == 16 && ps.warp_full) {
+        for (; q < nfull; q += gps) {
+          float v[CH];
+          gather_full(ps, q, v);
+          if (!put_chunk(lg0 + q, q, v)) {
+            aborted = true;
+            break;
+          }
+        }
+        if (aborted) break;
+      }
       for (; q < p.nchunks; q += gps) {
         float v[CH];
         gather_chunk(ps, q, v);
