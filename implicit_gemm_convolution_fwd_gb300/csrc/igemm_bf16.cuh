@@ -257,9 +257,41 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
       const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
       const uint16_t *xo = p.xh + (ps.valid ? ps.xoff : 0);
       const int64_t lg0 = li * p.nchunks;
-      for (int q = (int)((sel - lg0 % gps + gps) % gps); q < p.nchunks; q += gps) {
+      // chunk q (slot-local lg = lg0 + q): wait for its stage, store, signal the issuer
+      auto put = [&](int q, const uint32_t (&packed)[kBfChunk / 2]) -> bool {
         const int64_t lg = lg0 + q;
         const int stage = 2 * slot + (int)(lg & 1);
+        const uint32_t r = (uint32_t)(lg >> 1);
+        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        ptx::tc_fence_after();
+        ptx::tmem_st16(tmem + lane_base + a_col0 + (uint32_t)(16 * stage), packed);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar_a_full + 8 * stage);
+        return true;
+      };
+      int q = (int)((sel - lg0 % gps + gps) % gps);
+      if (ps.warp_full) {
+        // full chunks of an interior warp: four offsets per shared load, no tests
+        const int nfull = p.Kred / kBfChunk;
+        for (; q < nfull; q += gps) {
+          uint32_t packed[kBfChunk / 2];
+          const int4 *o4 = reinterpret_cast<const int4 *>(toff + q * kBfChunk);
+#pragma unroll
+          for (int i = 0; i < kBfChunk / 4; ++i) {
+            const int4 o = o4[i];
+            packed[2 * i] = __byte_perm(__ldg(xo + o.x), __ldg(xo + o.y), 0x5410);
+            packed[2 * i + 1] = __byte_perm(__ldg(xo + o.z), __ldg(xo + o.w), 0x5410);
+          }
+          if (!put(q, packed)) {
+            aborted = true;
+            break;
+          }
+        }
+        if (aborted) break;
+      }
+      for (; q < p.nchunks; q += gps) {
         const int k0 = q * kBfChunk;
         uint32_t packed[kBfChunk / 2];
 #pragma unroll
@@ -269,17 +301,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
 #pragma unroll
           for (int j = 0; j < kUnit / 2; ++j) packed[u * (kUnit / 2) + j] = __byte_perm(v[2 * j], v[2 * j + 1], 0x5410);
         }
-        const uint32_t r = (uint32_t)(lg >> 1);
-        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
-        if (!__all_sync(0xffffffffu, ok)) {
+        if (!put(q, packed)) {
           aborted = true;
           break;
         }
-        ptx::tc_fence_after();
-        ptx::tmem_st16(tmem + lane_base + a_col0 + (uint32_t)(16 * stage), packed);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar_a_full + 8 * stage);
       }
     }
   } else if (warp >= kMmaWarp && warp - kMmaWarp < nslots) {
