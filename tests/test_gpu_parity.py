@@ -471,6 +471,42 @@ def test_bf16_conv(nd, groups, C_in, C_out, k, s, p, d):
     assert_bf16_close(y, ref, S, K, f"bf16 nd={nd} C_in={C_in} C_out={C_out}")
 
 
+# Interior warps take a separate loop over the chunks that end before the
+# reduction's padding columns; the rest of the tile (and every border warp) goes
+# through the tested gather.  These shapes put that hand-off at every place it
+# can fall: no partial chunk at all (reduction a multiple of 32), one partial
+# chunk, interior and border warps in the same tile, and two issuer slots.
+FAST_LOOP_CASES = [
+    # C_in, C_out, k, pad, in dims
+    (16, 48, (2, 2, 2), (0, 0, 0), (5, 12, 70)),    # 128 columns: every chunk full
+    (3, 64, (3, 5, 7), (0, 0, 0), (4, 9, 75)),      # 315 columns: one partial chunk
+    (5, 40, (3, 3, 3), (0, 1, 1), (4, 9, 70)),      # 135 columns, border and interior warps
+    (8, 96, (2, 2, 2), (0, 0, 0), (4, 10, 67)),     # 64 columns, two slots
+    (12, 24, (1, 3, 3), (0, 1, 0), (3, 11, 90)),    # 108 columns, padding along H only
+]
+
+
+@pytest.mark.parametrize("C_in,C_out,k,pad,ins", FAST_LOOP_CASES)
+def test_tensor_core_full_chunk_loop(C_in, C_out, k, pad, ins):
+    rng = np.random.default_rng(C_in * 1000 + C_out)
+    x = rng.standard_normal((2, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    s, d = (1, 1, 1), (1, 1, 1)
+    assert supported(x, w, s, pad, d, cf.CONV_ALGO_IGEMM_3XTF32)
+    ref = oracle.conv_nd(x, w, b, s, pad, d)
+    y = run_conv(x, w, b, s, pad, d, cf.CONV_ALGO_IGEMM_3XTF32).cpu().numpy()
+    assert_close(y, ref, f"fp32 C_in={C_in} C_out={C_out} k={k} pad={pad}")
+    # the 16-bit kernel has the same split between the two loops (32-column chunks)
+    xs = (rng.random((2, C_in) + ins) - 0.5).astype(np.float32)
+    (xt, wt, bt), (xf, wf, bf) = bf16_inputs(xs, w, b)
+    yb = cf.conv_fwd_nd(xt, wt, bt, s, pad, d)
+    torch.cuda.synchronize()
+    refb = oracle.conv_nd(xf, wf, bf, s, pad, d)
+    S = oracle.conv_nd(np.abs(xf), np.abs(wf), np.abs(bf), s, pad, d)
+    assert_bf16_close(yb, refb, S, C_in * int(np.prod(k)), f"bf16 C_in={C_in} C_out={C_out} k={k} pad={pad}")
+
+
 def test_bf16_exact_on_small_integers():
     # integer inputs and weights: every product and partial sum is exact in
     # fp32 and every output is an integer below 256, exactly representable in
