@@ -312,17 +312,17 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
     ("igemm_3xtf32", "conv3d_asym"): {
-        "bytes": 50.514944e6 + 824.356864e6, "batch": 16,
-        "sha256": "5cd77b48a8b388bf116e8401e41aa729374868ada2cfe8c8f47a541570ee040b"},
+        "bytes": 50.506752e6 + 823.865088e6, "batch": 16,
+        "sha256": "2b7ddb1f65a6bd847d4a156cfd04e3234728493724ca74c17ce87fb718117e34"},
     ("igemm_3xtf32", "conv1d_long"): {
-        "bytes": 537.358848e6 + 307.654400e6, "batch": 4,
-        "sha256": "5cd77b48a8b388bf116e8401e41aa729374868ada2cfe8c8f47a541570ee040b"},
+        "bytes": 537.312256e6 + 307.603200e6, "batch": 4,
+        "sha256": "2b7ddb1f65a6bd847d4a156cfd04e3234728493724ca74c17ce87fb718117e34"},
     ("igemm_3xtf32_streamed", "conv3d_wide_k"): {
-        "bytes": 35.452416e6 + 7.261952e6, "batch": 4,
-        "sha256": "5cd77b48a8b388bf116e8401e41aa729374868ada2cfe8c8f47a541570ee040b"},
+        "bytes": 35.406592e6 + 7.307008e6, "batch": 4,
+        "sha256": "2b7ddb1f65a6bd847d4a156cfd04e3234728493724ca74c17ce87fb718117e34"},
     ("igemm_bf16", "conv3d_asym"): {
-        "bytes": 25.291008e6 + 385.082368e6, "batch": 16,
-        "sha256": "774361edea968caa26c5e257fce9aa06e9f7e958be7eda241bbff529ac6a793f"},
+        "bytes": 25.295104e6 + 385.971200e6, "batch": 16,
+        "sha256": "8fd5ded5d1087519bef2cadf4f06f9820337ea091e045c84fc32bf28f52e637b"},
     ("fused_ffma", "conv3d_min_softmax"): {
         "bytes": 37.816320e6 + 0.001792e6, "batch": 128,
         "sha256": "a3c8d352595b1412f32ddeb3d8a71383c322d0155fb883f3a6335d030c445a9c"},
