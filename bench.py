@@ -313,13 +313,13 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
 NCU_TRAFFIC = {
     ("igemm_3xtf32", "conv3d_asym"): {
         "bytes": 50.506752e6 + 823.865088e6, "batch": 16,
-        "sha256": "2b7ddb1f65a6bd847d4a156cfd04e3234728493724ca74c17ce87fb718117e34"},
+        "sha256": "8e7ede1ad79decdf91ba8c60cf40bd448479020c3241a8df8336baa8fd51255d"},
     ("igemm_3xtf32", "conv1d_long"): {
         "bytes": 537.312256e6 + 307.603200e6, "batch": 4,
-        "sha256": "2b7ddb1f65a6bd847d4a156cfd04e3234728493724ca74c17ce87fb718117e34"},
+        "sha256": "8e7ede1ad79decdf91ba8c60cf40bd448479020c3241a8df8336baa8fd51255d"},
     ("igemm_3xtf32_streamed", "conv3d_wide_k"): {
         "bytes": 35.406592e6 + 7.307008e6, "batch": 4,
-        "sha256": "2b7ddb1f65a6bd847d4a156cfd04e3234728493724ca74c17ce87fb718117e34"},
+        "sha256": "8e7ede1ad79decdf91ba8c60cf40bd448479020c3241a8df8336baa8fd51255d"},
     ("igemm_bf16", "conv3d_asym"): {
         "bytes": 25.295104e6 + 385.971200e6, "batch": 16,
         "sha256": "8fd5ded5d1087519bef2cadf4f06f9820337ea091e045c84fc32bf28f52e637b"},

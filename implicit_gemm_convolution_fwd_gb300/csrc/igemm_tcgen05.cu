@@ -19,9 +19,10 @@
 //                splits every value into TF32 hi + lo (hi = top 10 mantissa
 //                bits, lo = exact remainder) and writes both to TMEM with
 //                tcgen05.st.
-//   warps 20-23  lane 0 of each issues the MMAs of one tile slot:
+//   warps 20-23  one per tile slot: the whole warp runs the slot's chunk loop
+//                and one elected lane issues its MMAs:
 //                D += A_hi*B_hi + A_hi*B_lo + A_lo*B_hi   (M=128, N=C_out pad 32, K=8 per MMA)
-// A slot is an independent tile pipeline: its own issuing thread, TMEM
+// A slot is an independent tile pipeline: its own issuing warp, TMEM
 // accumulator and two A stages.  A thread needs ~120-145 cycles to issue one
 // tcgen05.mma with N <= 128, so several issuing threads are what keeps the
 // tensor pipe busy: four slots when C_out pads to <= 64, else two (TMEM holds
@@ -85,7 +86,7 @@ struct IgemmParams {
   int Npad;         // C_out rounded up to 32
   int KC;           // K columns per pipeline chunk (multiple of 16)
   int nchunks;      // ceil(Kpad / KC)
-  int nslots;       // tile slots (2 or 4), each with an MMA-issuing thread and an accumulator
+  int nslots;       // tile slots (2 or 4), each with an MMA-issuing warp and an accumulator
   int tap_major;    // reduction ordered (tap, c) instead of (c, tap); padded convs with C_in % 4 == 0,
                     // and always for channels-last tensors
   int vec4;         // channels last with 16-byte aligned groups of 4 channels: float4 gathers
