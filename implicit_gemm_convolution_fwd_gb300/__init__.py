@@ -20,6 +20,7 @@ ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV
 # every symbol include/convfwd.h declares
 EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_grouped", "conv_fwd_nd_channels_last",
             "conv_fwd_nd_bf16", "conv_fwd_nd_f16", "conv_workspace_bytes", "conv_fwd_nd_ws", "conv_fwd_nd_ws_noalloc",
+            "conv_host_workspace_bytes", "conv_fwd_nd_host",
             "conv_select_algo",
             "conv_algo_supported",
             "conv3d_min_softmax",
@@ -67,6 +68,10 @@ def load(path: str | None = None):
     lib.conv_fwd_nd_ws.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp,
                                    ctypes.c_size_t, vp]
     lib.conv_fwd_nd_ws_noalloc.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, vp]
+    lib.conv_host_workspace_bytes.argtypes = [i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, i64,
+                                              ctypes.POINTER(ctypes.c_size_t)]
+    lib.conv_fwd_nd_host.argtypes = [vp, vp, vp, vp, i32, i64, i64, i64, i64, arr, arr, arr, arr, arr, i64, vp,
+                                     ctypes.c_size_t, vp]
     lib.conv_select_algo.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, ctypes.POINTER(ctypes.c_int)]
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
@@ -286,6 +291,49 @@ def conv_fwd_nd_noalloc(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, 
     st = load().conv_fwd_nd_ws_noalloc(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
                                        out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
                                        _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), _stream_handle(stream))
+    _check(st)
+    return out
+
+
+def host_workspace_bytes(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1, groups=1, chunk=0) -> int:
+    """Bytes of device workspace conv_fwd_nd_host needs for this problem and batch chunk."""
+    nd = len(in_dims)
+    b = ctypes.c_size_t(0)
+    _check(load().conv_host_workspace_bytes(nd, N, C_in, C_out, int(groups), _arr(in_dims), _arr(k_dims),
+                                            _arr(_tuple(stride, nd)), _arr(_tuple(pad, nd)),
+                                            _arr(_tuple(dilation, nd)), int(chunk), ctypes.byref(b)))
+    return int(b.value)
+
+
+def conv_fwd_nd_host(x, w, bias=None, stride=1, pad=0, dilation=1, groups=1, chunk=0, workspace=None, out=None,
+                     stream=None, device=None):
+    """conv_fwd_nd on HOST tensors (contiguous float32 CPU tensors; page-locked ones let the copies overlap
+    the compute): the batch goes through the device in chunks of `chunk` images (0: one chunk), copies in
+    and out overlapping the convolution.  `workspace`: a CUDA uint8 tensor of at least
+    host_workspace_bytes(...) bytes (allocated here when None).  Returns y on the host once `stream` has
+    completed (the call itself does not wait)."""
+    import torch
+    nd = x.dim() - 2
+    s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[0]
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not (t.device.type == "cpu" and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous float32 CPU tensors")
+    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in:
+        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if workspace is None:
+        need = host_workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups, chunk)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    if out is None:
+        out = torch.empty((N, C_out) + od, dtype=torch.float32, pin_memory=x.is_pinned())
+    with torch.cuda.device(dev):
+        st = load().conv_fwd_nd_host(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                     out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
+                                     _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), int(chunk), workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), _stream_handle(stream))
     _check(st)
     return out
 

@@ -3,6 +3,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <mutex>
+
 #include <cuda_runtime.h>
 
 #include "../../include/convfwd.h"
@@ -187,6 +189,69 @@ int noalloc_ws_address(void **out) {
   *out = g_noalloc_ws_ptr[dev];
   return CONV_OK;
 }
+
+// ---- host-buffer entry point: two copy streams and the events that order
+// them against the compute, created on a device's first call and kept.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t x_ready[2] = {}, comp_done[2] = {}, y_drained[2] = {};
+};
+HostPipe g_host_pipe[64];
+std::mutex g_host_pipe_mutex;
+
+int host_pipe(HostPipe **out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_host: cudaGetDevice");
+  if (dev < 0 || dev >= 64) return fail(CONV_ERR_UNSUPPORTED, "conv_fwd_nd_host: device index above 63%s");
+  std::lock_guard<std::mutex> lock(g_host_pipe_mutex);
+  HostPipe &hp = g_host_pipe[dev];
+  if (!hp.ready) {
+    e = cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking);
+    for (int i = 0; i < 2 && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&hp.x_ready[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.comp_done[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.y_drained[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_host: creating its streams and events");
+    hp.ready = true;
+  }
+  *out = &hp;
+  return CONV_OK;
+}
+
+// Workspace of conv_fwd_nd_host: w, bias, two x chunks, two y chunks, each
+// section 256-byte aligned.
+struct HostLayout {
+  size_t w_off, b_off, x_off[2], y_off[2], total;
+  int64_t x_per, y_per;  // elements of one image of x and of y
+};
+
+HostLayout host_layout(const Geom &g, int64_t chunk) {
+  auto up = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  HostLayout L;
+  L.x_per = g.G * g.C * g.in_spatial();
+  L.y_per = g.G * g.K * g.out_spatial();
+  size_t off = 0;
+  L.w_off = off;
+  off += up((size_t)(g.G * g.K * g.C * g.taps()) * 4);
+  L.b_off = off;
+  off += up((size_t)(g.G * g.K) * 4);
+  for (int i = 0; i < 2; ++i) {
+    L.x_off[i] = off;
+    off += up((size_t)(chunk * L.x_per) * 4);
+  }
+  for (int i = 0; i < 2; ++i) {
+    L.y_off[i] = off;
+    off += up((size_t)(chunk * L.y_per) * 4);
+  }
+  L.total = off;
+  return L;
+}
+
+int64_t host_chunk(int64_t N, int64_t chunk) { return (chunk <= 0 || chunk > N) ? (N > 0 ? N : 1) : chunk; }
 
 }  // namespace
 
@@ -386,6 +451,78 @@ int conv_fwd_nd_ws_noalloc(const float *x, const float *w, const float *bias, fl
   if (st != CONV_OK) return st;
   return conv_fwd_nd_ws(x, w, bias, y, ndim, N, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation, ws,
                         sizeof(g_noalloc_ws), stream);
+}
+
+int conv_host_workspace_bytes(int ndim, int64_t N, int64_t C_in, int64_t C_out, int64_t groups,
+                              const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                              const int64_t *pad, const int64_t *dilation, int64_t chunk, size_t *bytes) {
+  g_last_error[0] = 0;
+  if (!bytes) return fail(CONV_ERR_NULL, "conv_host_workspace_bytes: bytes is NULL%s");
+  Geom g;
+  int64_t xe, we, ye;
+  int st = make_geom(ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, &xe, &we, &ye, groups);
+  if (st != CONV_OK) return st;
+  *bytes = host_layout(g, host_chunk(N, chunk)).total;
+  return CONV_OK;
+}
+
+int conv_fwd_nd_host(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                     int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims, const int64_t *k_dims,
+                     const int64_t *stride, const int64_t *pad, const int64_t *dilation, int64_t chunk,
+                     void *workspace, size_t workspace_bytes, conv_stream_t stream) {
+  g_last_error[0] = 0;
+  Geom g;
+  int st = validate_conv(x, w, bias, y, ndim, N, C_in, C_out, in_dims, k_dims, stride, pad, dilation, &g, -1,
+                         groups);
+  if (st != CONV_OK) return st;
+  if (!workspace) return fail(CONV_ERR_NULL, "conv_fwd_nd_host: workspace is NULL%s");
+  if (g.N == 0) return CONV_OK;  // empty batch: nothing to copy or compute
+  if ((uintptr_t)workspace & 255u) return fail(CONV_ERR_ARG, "conv_fwd_nd_host: workspace must be 256-byte aligned%s");
+  chunk = host_chunk(N, chunk);
+  const HostLayout L = host_layout(g, chunk);
+  if (workspace_bytes < L.total)
+    return fail(CONV_ERR_ARG, "conv_fwd_nd_host: workspace smaller than conv_host_workspace_bytes%s");
+  HostPipe *hp = nullptr;
+  st = host_pipe(&hp);
+  if (st != CONV_OK) return st;
+  cudaStream_t s = (cudaStream_t)stream;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  float *wd = reinterpret_cast<float *>(ws + L.w_off);
+  float *bd = bias ? reinterpret_cast<float *>(ws + L.b_off) : nullptr;
+  const int64_t we = g.G * g.K * g.C * g.taps();
+  // weights and bias travel on the compute stream, ahead of the first chunk
+  cudaError_t e = cudaMemcpyAsync(wd, w, (size_t)we * 4, cudaMemcpyHostToDevice, s);
+  if (e == cudaSuccess && bias) e = cudaMemcpyAsync(bd, bias, (size_t)(g.G * g.K) * 4, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_host: weight copy");
+  for (int64_t n0 = 0, i = 0; n0 < N; n0 += chunk, ++i) {
+    const int slot = (int)(i & 1);
+    const int64_t nb = N - n0 < chunk ? N - n0 : chunk;
+    float *xd = reinterpret_cast<float *>(ws + L.x_off[slot]);
+    float *yd = reinterpret_cast<float *>(ws + L.y_off[slot]);
+    // x chunk into its slot once the conv that last read the slot is done
+    e = cudaStreamWaitEvent(hp->h2d, hp->comp_done[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(xd, x + n0 * L.x_per, (size_t)(nb * L.x_per) * 4, cudaMemcpyHostToDevice, hp->h2d);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->x_ready[slot], hp->h2d);
+    // the conv waits for its input and for the slot's previous output to leave
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->x_ready[slot], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->y_drained[slot], 0);
+    if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_host: input copy");
+    st = conv_fwd_nd_grouped(xd, wd, bd, yd, ndim, nb, C_in, C_out, groups, in_dims, k_dims, stride, pad, dilation,
+                             CONV_ALGO_AUTO, stream);
+    if (st != CONV_OK) return st;
+    e = cudaEventRecord(hp->comp_done[slot], s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hp->d2h, hp->comp_done[slot], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(y + n0 * L.y_per, yd, (size_t)(nb * L.y_per) * 4, cudaMemcpyDeviceToHost, hp->d2h);
+    if (e == cudaSuccess) e = cudaEventRecord(hp->y_drained[slot], hp->d2h);
+    if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_host: output copy");
+  }
+  // `stream` completes after the last output copies
+  e = cudaStreamWaitEvent(s, hp->y_drained[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(s, hp->y_drained[1], 0);
+  if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_host: final wait");
+  return CONV_OK;
 }
 
 int conv_fwd_nd_ex(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,

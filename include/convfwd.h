@@ -219,6 +219,43 @@ CONVFWD_API int conv_fwd_nd_ws_noalloc(const float *x, const float *w, const flo
                                        const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
                                        const int64_t *dilation, conv_stream_t stream);
 
+/*
+ * Host buffers in, host buffer out.  x, w, bias and y are HOST pointers with the
+ * layouts of conv_fwd_nd_grouped.  The call copies w and bias to the device,
+ * then runs the batch through the device in chunks of `chunk` images (chunk <= 0
+ * or > N: one chunk).  The host-to-device copy of chunk i+1 and the
+ * device-to-host copy of chunk i-1 run on two library streams while chunk i is
+ * convolved on `stream` (conv_fwd_nd_grouped, AUTO), so the copies overlap the
+ * compute.  The forward convolution itself is the one of the pages' modules
+ * (l1_p60 and l1_p76 pages); the chunked host interface has no counterpart
+ * there.
+ *
+ * workspace: device memory of at least conv_host_workspace_bytes bytes (for the
+ * same arguments and chunk), 256-byte aligned; it holds w, bias and two chunks
+ * each of x and y.  The copies overlap only when x and y are page-locked
+ * (cudaHostAlloc, cudaHostRegister or a pinned torch tensor); pageable memory
+ * works but serialises.  All work is enqueued and the call returns without
+ * synchronising: y is complete once `stream` has completed (the stream waits
+ * for the last device-to-host copy).  The library's two copy streams and their
+ * events are created on the first call on each device and kept; calls that
+ * share a workspace must be ordered on one stream, and calls from several host
+ * threads on one device must not run concurrently.
+ *
+ * Errors: CONV_ERR_NULL (x, w or y NULL with N > 0, workspace NULL),
+ * CONV_ERR_ARG (bad sizes, a workspace too small or misaligned, y overlapping
+ * an input), the statuses of conv_fwd_nd_grouped for the chunks, CONV_ERR_CUDA
+ * for a failed copy, event or stream call.
+ */
+CONVFWD_API int conv_host_workspace_bytes(int ndim, int64_t N, int64_t C_in, int64_t C_out, int64_t groups,
+                                          const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
+                                          const int64_t *pad, const int64_t *dilation, int64_t chunk,
+                                          size_t *bytes);
+CONVFWD_API int conv_fwd_nd_host(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
+                                 int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
+                                 const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
+                                 const int64_t *dilation, int64_t chunk, void *workspace, size_t workspace_bytes,
+                                 conv_stream_t stream);
+
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
  * for an invalid problem. */

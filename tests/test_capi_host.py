@@ -149,3 +149,33 @@ def test_grouped_validation_statuses(lib):
     assert f(*args(6, 4, 3)) == cf.CONV_ERR_ARG     # 3 does not divide C_out = 4
     assert "groups" in lib.conv_last_error().decode()
 
+
+
+def test_host_entry_point_workspace_and_statuses(lib):
+    A = cf._arr
+    nbytes = ctypes.c_size_t(0)
+    dims = lambda: (A((6, 9, 11)), A((3, 5, 7)), A((1, 1, 1)), A((0, 0, 0)), A((1, 1, 1)))
+    # workspace: w (64*3*105 floats) and bias, then two x chunks and two y chunks, 256-byte sections
+    up = lambda v: (v + 255) // 256 * 256
+    out_sp = 4 * 5 * 5
+    for chunk, nb in ((0, 10), (3, 3), (10, 10), (25, 10), (-1, 10)):
+        assert lib.conv_host_workspace_bytes(3, 10, 3, 64, 1, *dims(), chunk, ctypes.byref(nbytes)) == cf.CONV_OK
+        want = up(64 * 3 * 105 * 4) + up(64 * 4) + 2 * up(nb * 3 * 594 * 4) + 2 * up(nb * 64 * out_sp * 4)
+        assert nbytes.value == want, (chunk, nbytes.value, want)
+    assert lib.conv_host_workspace_bytes(3, 10, 3, 64, 1, *dims(), 2, None) == cf.CONV_ERR_NULL
+    assert lib.conv_host_workspace_bytes(3, 10, 3, 64, 4, *dims(), 2, ctypes.byref(nbytes)) == cf.CONV_ERR_ARG
+    # the call itself: argument errors are reported before any copy or stream work
+    f = lib.conv_fwd_nd_host
+    x, w, y = 0x1000, 0x100000, 0x10000000
+    ws = 0x7f0000000000
+    big = 1 << 40
+    assert f(x, w, None, y, 3, 10, 3, 64, 1, *dims(), 2, None, big, None) == cf.CONV_ERR_NULL   # no workspace
+    assert f(x, w, None, y, 3, 10, 3, 64, 1, *dims(), 2, ws + 16, big, None) == cf.CONV_ERR_ARG  # misaligned
+    assert f(x, w, None, y, 3, 10, 3, 64, 1, *dims(), 2, ws, 1024, None) == cf.CONV_ERR_ARG     # too small
+    assert "conv_host_workspace_bytes" in lib.conv_last_error().decode()
+    assert f(None, w, None, y, 3, 10, 3, 64, 1, *dims(), 2, ws, big, None) == cf.CONV_ERR_NULL
+    assert f(x, w, None, x, 3, 10, 3, 64, 1, *dims(), 2, ws, big, None) == cf.CONV_ERR_ARG     # y overlaps x
+    assert f(x, w, None, y, 3, 10, 3, 64, 1, A((6, 9, 2)), A((3, 5, 7)), A((1, 1, 1)), A((0, 0, 0)), A((1, 1, 1)),
+             2, ws, big, None) == cf.CONV_ERR_SHAPE                                            # empty output
+    # an empty batch needs no device work at all
+    assert f(None, w, None, None, 3, 0, 3, 64, 1, *dims(), 2, ws, big, None) == cf.CONV_OK

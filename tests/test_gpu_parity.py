@@ -666,3 +666,55 @@ def test_side_stream_matches_default_stream_for_each_family():
             got = call(st)
         st.synchronize()
         assert torch.equal(got, ref)
+
+
+# ------------------------------------------------- host buffers, chunked batch
+
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("shape", [
+    # N, C_in, C_out, groups, in dims, k, stride, pad, dilation, chunk, bias
+    (5, 3, 64, 1, (6, 10, 13), (3, 5, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1), 2, True),    # tensor cores, ragged chunk
+    (4, 8, 12, 2, (7, 9, 8), (3, 3, 3), (1, 2, 1), (1, 1, 1), (1, 1, 2), 1, False),     # direct kernel, grouped
+    (3, 64, 128, 1, (301,), (3,), (3,), (0,), (4,), 0, True),                          # one chunk, Conv1d
+])
+def test_host_buffers_match_device_call(shape, pinned):
+    N, C_in, C_out, groups, ins, k, s, p, d, chunk, with_bias = shape
+    rng = np.random.default_rng(N * 100 + C_in)
+    x = torch.from_numpy(rng.standard_normal((N, C_in) + ins).astype(np.float32))
+    w = torch.from_numpy(((rng.random((C_out, C_in // groups) + k) - 0.5) * 0.3).astype(np.float32))
+    b = torch.from_numpy(rng.standard_normal(C_out).astype(np.float32)) if with_bias else None
+    if pinned:
+        x, w = x.pin_memory(), w.pin_memory()
+        b = None if b is None else b.pin_memory()
+    y = cf.conv_fwd_nd_host(x, w, b, s, p, d, groups=groups, chunk=chunk)
+    torch.cuda.synchronize()
+    assert y.device.type == "cpu" and y.is_pinned() == pinned
+    yd = cf.conv_fwd_nd(x.cuda(), w.cuda(), None if b is None else b.cuda(), s, p, d, groups=groups)
+    torch.cuda.synchronize()
+    # same kernels on each chunk: the same arithmetic as the one-call device path
+    assert torch.equal(y, yd.cpu())
+    ref = oracle.conv_nd(x.numpy(), w.numpy(), None if b is None else b.numpy(), s, p, d, groups=groups)
+    assert_close(y.numpy(), ref, f"host buffers {shape}")
+
+
+def test_host_buffers_reused_workspace_and_stream_order():
+    # two calls on one stream sharing one workspace: the second waits for the first's copies
+    rng = np.random.default_rng(7)
+    s, p, d = (1, 1, 1), (0, 1, 1), (1, 1, 1)
+    xs = [torch.from_numpy(rng.standard_normal((6, 4, 5, 8, 9)).astype(np.float32)).pin_memory() for _ in range(2)]
+    w = torch.from_numpy(((rng.random((32, 4, 3, 3, 3)) - 0.5) * 0.3).astype(np.float32)).pin_memory()
+    need = cf.host_workspace_bytes(6, 4, 32, (5, 8, 9), (3, 3, 3), s, p, d, 1, 2)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    st = torch.cuda.Stream()
+    ys = [cf.conv_fwd_nd_host(xx, w, None, s, p, d, chunk=2, workspace=ws, stream=st) for xx in xs]
+    st.synchronize()
+    for xx, y in zip(xs, ys):
+        assert_close(y.numpy(), oracle.conv_nd(xx.numpy(), w.numpy(), None, s, p, d), "reused workspace")
+
+
+def test_host_buffers_empty_batch():
+    x = torch.empty((0, 3, 6, 7, 8))
+    w = torch.ones((4, 3, 2, 2, 2))
+    y = cf.conv_fwd_nd_host(x, w, None, 1, 0, 1, chunk=3)
+    torch.cuda.synchronize()
+    assert tuple(y.shape) == (0, 4, 5, 6, 7)
