@@ -260,10 +260,11 @@ class VariantRunner(OurRunner):
         torch = self.torch
         self.dtype, self.channels_last, self.groups = dtype, channels_last, groups
         self.ws = None
+        self.ws_stream = 0  # workspace bytes for streamed weights
         if workspace:
-            need = self.cf.workspace_bytes(wl.N, wl.C_in, wl.C_out, wl.in_dims, wl.k_dims, wl.stride, wl.pad,
-                                           wl.dilation)
-            self.ws = torch.empty(max(need, 1), dtype=torch.uint8, device=device)
+            self.ws_stream = self.cf.workspace_bytes(wl.N, wl.C_in, wl.C_out, wl.in_dims, wl.k_dims, wl.stride,
+                                                     wl.pad, wl.dilation)
+            self.ws = torch.empty(max(self.ws_stream, 1), dtype=torch.uint8, device=device)
         self.min_dim = wl.min_dim if min_dim is None else min_dim
         if groups > 1:
             self.w = self.w[:, :wl.C_in // groups].contiguous()
@@ -279,6 +280,10 @@ class VariantRunner(OurRunner):
             od = self.out_dims
             keep = [od[i] for i in range(3) if i != self.min_dim - 2]
             self.y = torch.empty((wl.N, wl.C_out, keep[0], keep[1]), device=device)
+
+    def launches_per_step(self):
+        # streamed weights: the weight split runs before the conv kernel
+        return 1 + (self.ws is not None and self.ws_stream > 0)
 
     def step(self):
         if self.wl.kind == "fused":
@@ -303,11 +308,6 @@ VARIANTS = [
     ("conv3d_wide_k[workspace]", "conv3d_wide_k", {"workspace": True}),
     ("conv3d_wide_k[no workspace]", "conv3d_wide_k", {}),
 ]
-
-
-def cf_workspace_needed(r):
-    wl = r.wl
-    return r.cf.workspace_bytes(wl.N, wl.C_in, wl.C_out, wl.in_dims, wl.k_dims, wl.stride, wl.pad, wl.dilation) > 0
 
 
 def run_variants(dev, peaks, steps):
@@ -523,7 +523,7 @@ def main():
         runner = VariantRunner(wl, dev, dtype=dt, workspace=args.workspace)
         if dt is not None:
             runner.algo = "igemm_" + args.dtype
-        elif runner.ws is not None and cf_workspace_needed(runner):
+        elif runner.ws is not None and runner.ws_stream > 0:
             runner.algo = "igemm_3xtf32_streamed"
     else:
         runner = OurRunner(wl, dev)
