@@ -86,6 +86,38 @@ def test_random_small(algo, nd, seed):
     assert_close(y, ref, f"nd={nd} seed={seed} algo={cf.ALGO_NAMES[algo]}")
 
 
+def random_tc_case(seed):
+    """A random problem for the tensor-core family with room for interior warps: C_in 1-40 (multiples of 4
+    and not), C_out 16-128 (one or two issuer slots), kernels up to 5, padding 0-2, strides and dilations
+    up to 2, spatial sizes up to a few thousand positions per image."""
+    rng = np.random.default_rng(50_000 + seed)
+    nd = int(rng.integers(1, 4))
+    C_in = int(rng.choice([1, 3, 4, 5, 8, 12, 16, 24, 40]))
+    C_out = int(rng.integers(16, 129))
+    k = tuple(int(v) for v in rng.integers(1, 6, nd))
+    s = tuple(int(v) for v in rng.integers(1, 3, nd))
+    p = tuple(int(v) for v in rng.integers(0, 3, nd))
+    d = tuple(int(v) for v in rng.integers(1, 3, nd))
+    lo = {1: 200, 2: 14, 3: 6}[nd]
+    hi = {1: 3000, 2: 60, 3: 18}[nd]
+    ins = tuple(max(int(rng.integers(lo, hi)), (k[i] - 1) * d[i] + 1) for i in range(nd))
+    N = int(rng.integers(1, 4))
+    x = rng.standard_normal((N, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32) if seed % 3 else None
+    return x, w, b, s, p, d
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_tensor_core_shapes(seed):
+    x, w, b, s, p, d = random_tc_case(seed)
+    if not supported(x, w, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32):
+        pytest.skip("shape not supported by the tensor-core family")
+    ref = oracle.conv_nd(x, w, b, s, p, d)
+    y = run_conv(x, w, b, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32).cpu().numpy()
+    assert_close(y, ref, f"tensor cores seed={seed} x={x.shape} w={w.shape} s={s} p={p} d={d}")
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 def test_edge_geometries(algo):
     rng = np.random.default_rng(5)
