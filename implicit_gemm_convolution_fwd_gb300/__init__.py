@@ -263,6 +263,8 @@ def conv_fwd_nd_ws(x, w, bias=None, stride=1, pad=0, dilation=1, workspace=None,
     need = workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        if stream is not None:
+            workspace.record_stream(stream)  # not reused before the call's work on `stream` is done
     od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
     if out is None:
         out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
@@ -326,6 +328,9 @@ def conv_fwd_nd_host(x, w, bias=None, stride=1, pad=0, dilation=1, groups=1, chu
     if workspace is None:
         need = host_workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups, chunk)
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+        # the copies run on the library's own streams too: keep the block until `stream` (which waits
+        # for them) is done
+        workspace.record_stream(torch.cuda.current_stream(dev) if stream is None else stream)
     od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
     if out is None:
         out = torch.empty((N, C_out) + od, dtype=torch.float32, pin_memory=x.is_pinned())

@@ -196,6 +196,7 @@ struct HostPipe {
   bool ready = false;
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t x_ready[2] = {}, comp_done[2] = {}, y_drained[2] = {};
+  std::mutex enqueue;  // one call at a time records and waits on the events
 };
 HostPipe g_host_pipe[64];
 std::mutex g_host_pipe_mutex;
@@ -485,6 +486,8 @@ int conv_fwd_nd_host(const float *x, const float *w, const float *bias, float *y
   HostPipe *hp = nullptr;
   st = host_pipe(&hp);
   if (st != CONV_OK) return st;
+  // the events are shared by every call on the device: enqueue one call at a time
+  std::lock_guard<std::mutex> lock(hp->enqueue);
   cudaStream_t s = (cudaStream_t)stream;
   uint8_t *ws = static_cast<uint8_t *>(workspace);
   float *wd = reinterpret_cast<float *>(ws + L.w_off);

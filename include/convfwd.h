@@ -238,8 +238,8 @@ CONVFWD_API int conv_fwd_nd_ws_noalloc(const float *x, const float *w, const flo
  * synchronising: y is complete once `stream` has completed (the stream waits
  * for the last device-to-host copy).  The library's two copy streams and their
  * events are created on the first call on each device and kept; calls that
- * share a workspace must be ordered on one stream, and calls from several host
- * threads on one device must not run concurrently.
+ * share a workspace must be ordered on one stream.  Calls from several host
+ * threads are safe: each call enqueues its work under a per-device lock.
  *
  * Errors: CONV_ERR_NULL (x, w or y NULL with N > 0, workspace NULL),
  * CONV_ERR_ARG (bad sizes, a workspace too small or misaligned, y overlapping

@@ -744,6 +744,31 @@ def test_host_buffers_reused_workspace_and_stream_order():
         assert_close(y.numpy(), oracle.conv_nd(xx.numpy(), w.numpy(), None, s, p, d), "reused workspace")
 
 
+def test_host_buffers_from_concurrent_threads():
+    # ctypes drops the GIL during the call, so these enqueue concurrently; each has its own stream
+    # and workspace, and the library's per-device lock keeps their event records apart
+    import threading
+    rng = np.random.default_rng(11)
+    s, p, d = (1, 1, 1), (1, 1, 1), (1, 1, 1)
+    w = torch.from_numpy(((rng.random((24, 8, 3, 3, 3)) - 0.5) * 0.3).astype(np.float32)).pin_memory()
+    xs = [torch.from_numpy(rng.standard_normal((5, 8, 6, 9, 12)).astype(np.float32)).pin_memory() for _ in range(4)]
+    out = [None] * len(xs)
+
+    def run(i):
+        st = torch.cuda.Stream()
+        for _ in range(3):
+            out[i] = cf.conv_fwd_nd_host(xs[i], w, None, s, p, d, chunk=2, stream=st)
+        st.synchronize()
+
+    threads = [threading.Thread(target=run, args=(i,)) for i in range(len(xs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    for xx, y in zip(xs, out):
+        assert_close(y.numpy(), oracle.conv_nd(xx.numpy(), w.numpy(), None, s, p, d), "concurrent host calls")
+
+
 def test_host_buffers_empty_batch():
     x = torch.empty((0, 3, 6, 7, 8))
     w = torch.ones((4, 3, 2, 2, 2))
