@@ -376,3 +376,58 @@ def test_grouped_sampled_equals_full_and_rejects_bad_groups():
     assert np.array_equal(oracle.conv_nd_at(x, w, None, (2,), (1,), (1,), idx, groups=2), y.reshape(-1)[idx])
     with pytest.raises(oracle.OracleError):
         oracle.conv_nd(x, w, None, (2,), (1,), (1,), groups=3)
+
+
+# ---------------------------------------- second formulation: dense im2col
+
+def im2col_conv(x, w, b, stride, pad, dilation, groups=1):
+    """The same convolution as an explicit matrix product, written independently of the oracle:
+    one column per (batch, output position) holding its zero-padded receptive field (c, k...),
+    multiplied by the weights as a [C_out/groups, C_in/groups * prod(k)] matrix per group."""
+    x = x.astype(np.float64)
+    w = w.astype(np.float64)
+    N, C_in = x.shape[:2]
+    C_out, Cg = w.shape[:2]
+    nd = x.ndim - 2
+    ks, ins = w.shape[2:], x.shape[2:]
+    outs = [(ins[i] + 2 * pad[i] - dilation[i] * (ks[i] - 1) - 1) // stride[i] + 1 for i in range(nd)]
+    xp = np.pad(x, [(0, 0), (0, 0)] + [(pad[i], pad[i]) for i in range(nd)])
+    taps = list(itertools.product(*[range(k) for k in ks]))
+    positions = list(itertools.product(*[range(o) for o in outs]))
+    y = np.zeros((N, C_out, len(positions)))
+    Kg = C_out // groups
+    for g in range(groups):
+        cols = np.zeros((Cg * len(taps), N * len(positions)))
+        for n in range(N):
+            for j, pos in enumerate(positions):
+                r = 0
+                for c in range(Cg):
+                    for t in taps:
+                        idx = tuple(pos[i] * stride[i] + t[i] * dilation[i] for i in range(nd))
+                        cols[r, n * len(positions) + j] = xp[(n, g * Cg + c) + idx]
+                        r += 1
+        wm = w[g * Kg:(g + 1) * Kg].reshape(Kg, -1)
+        y[:, g * Kg:(g + 1) * Kg, :] = (wm @ cols).reshape(Kg, N, len(positions)).transpose(1, 0, 2)
+    if b is not None:
+        y += b.astype(np.float64)[None, :, None]
+    return y.reshape((N, C_out) + tuple(outs))
+
+
+@pytest.mark.parametrize("seed", range(9))
+def test_matches_dense_im2col_formulation(seed):
+    rng = np.random.default_rng(700 + seed)
+    nd = 1 + seed % 3
+    groups = 1 + seed % 2
+    Cg, Kg = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+    k = tuple(int(v) for v in rng.integers(1, 4, nd))
+    s = tuple(int(v) for v in rng.integers(1, 3, nd))
+    p = tuple(int(v) for v in rng.integers(0, 3, nd))
+    d = tuple(int(v) for v in rng.integers(1, 3, nd))
+    ins = tuple(int(rng.integers((k[i] - 1) * d[i] + 1, (k[i] - 1) * d[i] + 7)) for i in range(nd))
+    x = rng.standard_normal((2, Cg * groups) + ins).astype(np.float32)
+    w = rng.standard_normal((Kg * groups, Cg) + k).astype(np.float32)
+    b = rng.standard_normal(Kg * groups).astype(np.float32)
+    ref = im2col_conv(x, w, b, s, p, d, groups)
+    got = oracle.conv_nd(x, w, b, s, p, d, groups=groups)
+    assert got.shape == ref.shape
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
