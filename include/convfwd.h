@@ -244,7 +244,9 @@ CONVFWD_API int conv_fwd_nd_ws_noalloc(const float *x, const float *w, const flo
  * Errors: CONV_ERR_NULL (x, w or y NULL with N > 0, workspace NULL),
  * CONV_ERR_ARG (bad sizes, a workspace too small or misaligned, y overlapping
  * an input), the statuses of conv_fwd_nd_grouped for the chunks, CONV_ERR_CUDA
- * for a failed copy, event or stream call.
+ * for a failed copy, event or stream call.  Argument errors are found before
+ * anything is enqueued; a CUDA error on a later chunk can leave the chunks
+ * before it already copied into y.
  */
 CONVFWD_API int conv_host_workspace_bytes(int ndim, int64_t N, int64_t C_in, int64_t C_out, int64_t groups,
                                           const int64_t *in_dims, const int64_t *k_dims, const int64_t *stride,
