@@ -179,3 +179,28 @@ def test_host_entry_point_workspace_and_statuses(lib):
              2, ws, big, None) == cf.CONV_ERR_SHAPE                                            # empty output
     # an empty batch needs no device work at all
     assert f(None, w, None, None, 3, 0, 3, 64, 1, *dims(), 2, ws, big, None) == cf.CONV_OK
+
+
+def test_bindings_reject_bad_tensors_before_any_device_call(lib):
+    # host-only: every check below fires before the binding touches CUDA
+    import torch
+    x = torch.zeros((1, 4, 10))
+    w = torch.zeros((6, 4, 3))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        cf.conv_fwd_nd(x, w)                                       # CPU tensors on the device entry point
+    with pytest.raises(ValueError, match="same rank"):
+        cf.conv_fwd_nd(x, torch.zeros((6, 4, 3, 3)))
+    with pytest.raises(ValueError, match="float32, bfloat16 or float16"):
+        cf.conv_fwd_nd(x.double(), w.double())
+    with pytest.raises(ValueError, match="CPU tensors"):
+        cf.conv_fwd_nd_host(x.double(), w.double())                # host entry point: fp32 only
+    with pytest.raises(ValueError, match="CPU tensors"):
+        cf.conv_fwd_nd_host(x[:, :, ::2], w)                       # non-contiguous
+    with pytest.raises(ValueError, match="groups"):
+        cf.conv_fwd_nd_host(x, w, groups=3)
+    with pytest.raises(ValueError, match="groups"):
+        cf.conv_fwd_nd_host(x, torch.zeros((6, 3, 3)), groups=2)   # w.shape[1] must be C_in / groups
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        cf.conv_fwd_nd_ws(x, w)
+    with pytest.raises(ValueError, match="5-D"):
+        cf.conv3d_min_softmax(x, w)
