@@ -345,14 +345,14 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
     ("igemm_3xtf32", "conv3d_asym"): {
-        "bytes": 50.506752e6 + 823.865088e6, "batch": 16,
-        "sha256": "8e7ede1ad79decdf91ba8c60cf40bd448479020c3241a8df8336baa8fd51255d"},
+        "bytes": 50.511360e6 + 823.297792e6, "batch": 16,
+        "sha256": "94ca812ded6f0bc0df015f85db896e9b3bd3b9cb8736e53a81de583a0ed6d38f"},
     ("igemm_3xtf32", "conv1d_long"): {
-        "bytes": 537.312256e6 + 307.603200e6, "batch": 4,
-        "sha256": "8e7ede1ad79decdf91ba8c60cf40bd448479020c3241a8df8336baa8fd51255d"},
+        "bytes": 537.328640e6 + 307.182592e6, "batch": 4,
+        "sha256": "94ca812ded6f0bc0df015f85db896e9b3bd3b9cb8736e53a81de583a0ed6d38f"},
     ("igemm_3xtf32_streamed", "conv3d_wide_k"): {
-        "bytes": 35.406592e6 + 7.307008e6, "batch": 4,
-        "sha256": "8e7ede1ad79decdf91ba8c60cf40bd448479020c3241a8df8336baa8fd51255d"},
+        "bytes": 35.426560e6 + 7.363328e6, "batch": 4,
+        "sha256": "94ca812ded6f0bc0df015f85db896e9b3bd3b9cb8736e53a81de583a0ed6d38f"},
     ("igemm_bf16", "conv3d_asym"): {
         "bytes": 25.295104e6 + 385.971200e6, "batch": 16,
         "sha256": "8fd5ded5d1087519bef2cadf4f06f9820337ea091e045c84fc32bf28f52e637b"},

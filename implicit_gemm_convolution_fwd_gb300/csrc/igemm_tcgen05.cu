@@ -608,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         v[4 * i + 3] = __ldg(ps.xo + o.w);
       }
     };
-    const int nfull = (CH == 16 && p.KC == CH && !p.vec4) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
+    const int nfull = (p.KC == CH && !p.vec4) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
@@ -628,7 +628,12 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       }
       for (; q < p.nchunks; q += gps) {
         float v[CH];
-        gather_chunk(ps, q, v);
+        // 32-column chunks have no loop of their own (a second copy of the
+        // loop spills): interior warps pick the unchecked gather per chunk
+        if (CH == 32 && ps.warp_full && q < nfull)
+          gather_full(ps, q, v);
+        else
+          gather_chunk(ps, q, v);
         if (!put_chunk(lg0 + q, q, v)) {
           aborted = true;
           break;
