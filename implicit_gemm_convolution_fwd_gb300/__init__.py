@@ -137,11 +137,50 @@ def algo_supported(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1,
     return True
 
 
-def _stream_handle(stream):
+def _stream_handle(stream, device=None):
+    """The cudaStream_t of `stream` (default: the current stream of `device`).  A stream given
+    explicitly must belong to `device` when one is named."""
     import torch
     if stream is None:
-        stream = torch.cuda.current_stream()
+        stream = torch.cuda.current_stream(device)
+    elif device is not None and stream.device != device:
+        raise ValueError(f"the stream is on {stream.device}, the tensors on {device}")
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _one_cuda_device(*tensors):
+    """The single CUDA device holding every tensor given (None entries are skipped).
+
+    The library launches on the calling thread's current device; the bindings make the tensors'
+    device current for the call, so all of them must live on it."""
+    devs = set()
+    for t in tensors:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("x, w, bias and out must be CUDA tensors")
+        devs.add(t.device)
+    if len(devs) != 1:
+        raise ValueError(f"x, w, bias and out must be on one CUDA device, got {sorted(map(str, devs))}")
+    return devs.pop()
+
+
+def _check_groups(C_in, C_out, w_c, groups):
+    if groups < 1 or C_in % groups or C_out % groups or w_c * groups != C_in:
+        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
+
+
+def _check_out(out, shape, dtype, channels_last=False):
+    """`out` must have exactly `shape` and `dtype` and the layout the call writes."""
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out has shape {tuple(out.shape)}, the call writes {tuple(shape)}")
+    if out.dtype != dtype:
+        raise ValueError(f"out has dtype {out.dtype}, the call writes {dtype}")
+    if channels_last:
+        if _channels_last_view(out) is None:
+            raise ValueError("out must be stored channels last")
+    elif not out.is_contiguous():
+        raise ValueError("out must be contiguous")
 
 
 def _channels_last_view(t):
@@ -158,7 +197,8 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     shapes but are stored channels last (torch.channels_last / channels_last_3d, i.e. N D H W C);
     the returned y is allocated the same way.
     bfloat16 or float16 x, w (and bias): the 16-bit tensor-core path, fp32 accumulation, y in the
-    input dtype (contiguous layout only; `algo` must be AUTO)."""
+    input dtype (contiguous layout only; `algo` must be AUTO).
+    Every tensor must be on one CUDA device; the call runs with that device current."""
     import torch
     nd = x.dim() - 2
     if nd not in (1, 2, 3) or w.dim() != x.dim():
@@ -170,10 +210,11 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     for t in (x, w) + ((bias,) if bias is not None else ()):
         if not (t.is_cuda and t.dtype == dt):
             raise ValueError("x, w and bias must be CUDA tensors of one dtype")
+    dev = _one_cuda_device(x, w, bias, out)
     if dt in half and (channels_last or algo != CONV_ALGO_AUTO):
         raise ValueError("16-bit tensors take the contiguous layout and algo=AUTO")
-    if bias is not None and not bias.is_contiguous():
-        raise ValueError("bias must be contiguous")
+    if bias is not None and (not bias.is_contiguous() or tuple(bias.shape) != (w.shape[0],)):
+        raise ValueError("bias must be a contiguous [C_out] tensor")
     if channels_last:
         if _channels_last_view(x) is None or _channels_last_view(w) is None:
             raise ValueError("channels_last=True needs x and w stored channels last")
@@ -182,33 +223,30 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
-    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in:
-        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
+    _check_groups(C_in, C_out, w.shape[1], groups)
     od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
     if out is None:
         if dt in half:
-            out = torch.empty((N, C_out) + od, device=x.device, dtype=dt)
+            out = torch.empty((N, C_out) + od, device=dev, dtype=dt)
         elif channels_last:
-            out = torch.empty((N,) + od + (C_out,), device=x.device, dtype=torch.float32).permute(0, nd + 1,
-                                                                                              *range(1, nd + 1))
+            out = torch.empty((N,) + od + (C_out,), device=dev, dtype=torch.float32).permute(0, nd + 1,
+                                                                                          *range(1, nd + 1))
         else:
-            out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
-    elif tuple(out.shape) != (N, C_out) + od or (
-            _channels_last_view(out) is None if channels_last else not out.is_contiguous()):
-        raise ValueError("out has the wrong shape or memory layout")
-    elif out.dtype != dt:
-        raise ValueError("out must have the dtype of x")
+            out = torch.empty((N, C_out) + od, device=dev, dtype=torch.float32)
+    else:
+        _check_out(out, (N, C_out) + od, dt, channels_last)
     lib = load()
     b = None if bias is None else bias.data_ptr()
     dims = (_arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d))
-    if dt in half:
-        fn = lib.conv_fwd_nd_bf16 if dt == torch.bfloat16 else lib.conv_fwd_nd_f16
-        st = fn(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups), *dims,
-                _stream_handle(stream))
-    else:
-        fn = lib.conv_fwd_nd_channels_last if channels_last else lib.conv_fwd_nd_grouped
-        st = fn(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups), *dims, int(algo),
-                _stream_handle(stream))
+    with torch.cuda.device(dev):
+        if dt in half:
+            fn = lib.conv_fwd_nd_bf16 if dt == torch.bfloat16 else lib.conv_fwd_nd_f16
+            st = fn(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups), *dims,
+                    _stream_handle(stream, dev))
+        else:
+            fn = lib.conv_fwd_nd_channels_last if channels_last else lib.conv_fwd_nd_grouped
+            st = fn(x.data_ptr(), w.data_ptr(), b, out.data_ptr(), nd, N, C_in, C_out, int(groups), *dims, int(algo),
+                    _stream_handle(stream, dev))
     _check(st)
     return out
 
@@ -216,23 +254,31 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
 def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None):
     """softmax over channels of the min over tensor dim `min_dim` (2 = depth, 3 = height, 4 = width)
     of conv3d(x, w) + bias, for contiguous fp32 CUDA tensors (stride 1, no padding).  The result
-    keeps the two other spatial dims: [N, C_out, OH, OW], [N, C_out, OD, OW] or [N, C_out, OD, OH]."""
+    keeps the two other spatial dims: [N, C_out, OH, OW], [N, C_out, OD, OW] or [N, C_out, OD, OH].
+    The conv's output dims come from the library (conv_out_dims)."""
     import torch
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x and w must be 5-D")
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError("x, w and bias must be contiguous float32 CUDA tensors")
+    dev = _one_cuda_device(x, w, bias, out)
     N, C_out = x.shape[0], w.shape[0]
-    od = [x.shape[2 + i] - w.shape[2 + i] + 1 for i in range(3)]
-    if min_dim in (2, 3, 4):
-        keep = [od[i] for i in range(3) if i != min_dim - 2]
-    else:
-        keep = od[1:]
+    od = out_dims(x.shape[2:], w.shape[2:], 1, 0, 1)
+    # min_dim outside 2..4 is refused by the library (CONV_ERR_ARG); the buffer shape is then moot
+    keep = [od[i] for i in range(3) if i != min_dim - 2] if min_dim in (2, 3, 4) else list(od[1:])
+    shape = (N, C_out, keep[0], keep[1])
     if out is None:
-        out = torch.empty((N, C_out, max(keep[0], 1), max(keep[1], 1)), device=x.device, dtype=torch.float32)
+        out = torch.empty(shape, device=dev, dtype=torch.float32)
+    else:
+        _check_out(out, shape, torch.float32)
     xd = Tensor5(x.data_ptr(), (ctypes.c_int64 * 5)(*x.shape))
     wd = Tensor5(w.data_ptr(), (ctypes.c_int64 * 5)(*w.shape))
     yd = Tensor4(out.data_ptr(), (ctypes.c_int64 * 4)(*out.shape))
-    st = load().conv3d_min_softmax(ctypes.byref(xd), ctypes.byref(wd), None if bias is None else bias.data_ptr(),
-                                   ctypes.byref(yd), int(min_dim), _stream_handle(stream))
+    with torch.cuda.device(dev):
+        st = load().conv3d_min_softmax(ctypes.byref(xd), ctypes.byref(wd),
+                                       None if bias is None else bias.data_ptr(), ctypes.byref(yd), int(min_dim),
+                                       _stream_handle(stream, dev))
     _check(st)
     return out
 
@@ -247,52 +293,66 @@ def workspace_bytes(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1
     return int(b.value)
 
 
+def _fp32_device_problem(x, w, bias, out, stride, pad, dilation, groups):
+    """Shared checks of the fp32 contiguous entry points: tensors, groups, the output buffer.
+    Returns (device, nd, (s, p, d), N, C_in, C_out, out_dims)."""
+    import torch
+    nd = x.dim() - 2
+    if nd not in (1, 2, 3) or w.dim() != x.dim():
+        raise ValueError("x and w must be 3-D, 4-D or 5-D tensors of the same rank")
+    for t in (x, w) + ((bias,) if bias is not None else ()):
+        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
+            raise ValueError("tensors must be contiguous float32 CUDA tensors")
+    dev = _one_cuda_device(x, w, bias, out)
+    N, C_in = x.shape[:2]
+    C_out = w.shape[0]
+    if bias is not None and tuple(bias.shape) != (C_out,):
+        raise ValueError("bias must be a [C_out] tensor")
+    _check_groups(C_in, C_out, w.shape[1], groups)
+    hp = (_tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd))
+    od = out_dims(x.shape[2:], w.shape[2:], *hp)
+    if out is not None:
+        _check_out(out, (N, C_out) + od, torch.float32)
+    return dev, nd, hp, N, C_in, C_out, od
+
+
 def conv_fwd_nd_ws(x, w, bias=None, stride=1, pad=0, dilation=1, workspace=None, out=None, stream=None, groups=1):
     """conv_fwd_nd (fp32, contiguous) with a caller workspace for streamed weights: `workspace` is a CUDA
     tensor of at least workspace_bytes(...) bytes (allocated here when None and the problem needs one)."""
     import torch
-    nd = x.dim() - 2
-    s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
-    N, C_in = x.shape[:2]
-    C_out = w.shape[0]
-    for t in (x, w) + ((bias,) if bias is not None else ()):
-        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
-            raise ValueError("tensors must be contiguous float32 CUDA tensors")
-    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in:
-        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
+    dev, nd, (s, p, d), N, C_in, C_out, od = _fp32_device_problem(x, w, bias, out, stride, pad, dilation, groups)
     need = workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups)
     if workspace is None and need:
-        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+        workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         if stream is not None:
             workspace.record_stream(stream)  # not reused before the call's work on `stream` is done
-    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    if workspace is not None and workspace.device != dev:
+        raise ValueError("the workspace must be on the tensors' device")
     if out is None:
-        out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
+        out = torch.empty((N, C_out) + od, device=dev, dtype=torch.float32)
     wsp = None if workspace is None else workspace.data_ptr()
     wsb = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    st = load().conv_fwd_nd_ws(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(), out.data_ptr(),
-                               nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]), _arr(w.shape[2:]), _arr(s),
-                               _arr(p), _arr(d), wsp, wsb, _stream_handle(stream))
+    with torch.cuda.device(dev):
+        st = load().conv_fwd_nd_ws(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                   out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
+                                   _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), wsp, wsb,
+                                   _stream_handle(stream, dev))
     _check(st)
     return out
 
 
 def conv_fwd_nd_noalloc(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, stream=None, groups=1):
-    """conv_fwd_nd_ws with the library's static scratch instead of a caller workspace (no allocation)."""
+    """conv_fwd_nd_ws with the library's static scratch instead of a caller workspace: the library
+    allocates nothing (pass `out` to keep the whole call free of allocation)."""
     import torch
-    nd = x.dim() - 2
-    s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
-    N, C_in = x.shape[:2]
-    C_out = w.shape[0]
-    for t in (x, w) + ((bias,) if bias is not None else ()):
-        if not (t.is_cuda and t.dtype == torch.float32 and t.is_contiguous()):
-            raise ValueError("tensors must be contiguous float32 CUDA tensors")
-    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    dev, nd, (s, p, d), N, C_in, C_out, od = _fp32_device_problem(x, w, bias, out, stride, pad, dilation, groups)
     if out is None:
-        out = torch.empty((N, C_out) + od, device=x.device, dtype=torch.float32)
-    st = load().conv_fwd_nd_ws_noalloc(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
-                                       out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
-                                       _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), _stream_handle(stream))
+        out = torch.empty((N, C_out) + od, device=dev, dtype=torch.float32)
+    with torch.cuda.device(dev):
+        st = load().conv_fwd_nd_ws_noalloc(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
+                                           out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
+                                           _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d),
+                                           _stream_handle(stream, dev))
     _check(st)
     return out
 
@@ -312,33 +372,46 @@ def conv_fwd_nd_host(x, w, bias=None, stride=1, pad=0, dilation=1, groups=1, chu
     """conv_fwd_nd on HOST tensors (contiguous float32 CPU tensors; page-locked ones let the copies overlap
     the compute): the batch goes through the device in chunks of `chunk` images (0: one chunk), copies in
     and out overlapping the convolution.  `workspace`: a CUDA uint8 tensor of at least
-    host_workspace_bytes(...) bytes (allocated here when None).  Returns y on the host once `stream` has
-    completed (the call itself does not wait)."""
+    host_workspace_bytes(...) bytes on `device` (allocated here when None).  Returns y on the host once
+    `stream` has completed (the call itself does not wait)."""
     import torch
     nd = x.dim() - 2
+    if nd not in (1, 2, 3) or w.dim() != x.dim():
+        raise ValueError("x and w must be 3-D, 4-D or 5-D tensors of the same rank")
     s, p, d = _tuple(stride, nd), _tuple(pad, nd), _tuple(dilation, nd)
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
     for t in (x, w) + ((bias,) if bias is not None else ()):
         if not (t.device.type == "cpu" and t.dtype == torch.float32 and t.is_contiguous()):
             raise ValueError("tensors must be contiguous float32 CPU tensors")
-    if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in:
-        raise ValueError("groups must divide C_in and C_out, and w.shape[1] must be C_in / groups")
+    if bias is not None and tuple(bias.shape) != (C_out,):
+        raise ValueError("bias must be a [C_out] tensor")
+    _check_groups(C_in, C_out, w.shape[1], groups)
+    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    if out is not None:
+        if out.device.type != "cpu":
+            raise ValueError("out must be a CPU tensor")
+        _check_out(out, (N, C_out) + od, torch.float32)
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    if dev.type != "cuda":
+        raise ValueError("device must be a CUDA device")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
     if workspace is None:
         need = host_workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups, chunk)
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         # the copies run on the library's own streams too: keep the block until `stream` (which waits
         # for them) is done
         workspace.record_stream(torch.cuda.current_stream(dev) if stream is None else stream)
-    od = out_dims(x.shape[2:], w.shape[2:], s, p, d)
+    elif workspace.device != dev:
+        raise ValueError("the workspace must be on `device`")
     if out is None:
         out = torch.empty((N, C_out) + od, dtype=torch.float32, pin_memory=x.is_pinned())
     with torch.cuda.device(dev):
         st = load().conv_fwd_nd_host(x.data_ptr(), w.data_ptr(), None if bias is None else bias.data_ptr(),
                                      out.data_ptr(), nd, N, C_in, C_out, int(groups), _arr(x.shape[2:]),
                                      _arr(w.shape[2:]), _arr(s), _arr(p), _arr(d), int(chunk), workspace.data_ptr(),
-                                     workspace.numel() * workspace.element_size(), _stream_handle(stream))
+                                     workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     _check(st)
     return out
 

@@ -199,6 +199,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 
 __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_uint(v) & 0xffffe000u; }
 
+// The n lowest bits set, 0 <= n <= 32 (a kernel extent of 32 taps fills the word).
+__device__ __forceinline__ uint32_t low_bits(int n) { return n >= 32 ? 0xffffffffu : (1u << n) - 1u; }
+
 // One producer thread's output position within a tile.
 struct PosInfo {
   const float *xo;      // x at the receptive field's origin (may lie in the padding)
@@ -242,7 +245,7 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   ps.dm = dm;
   ps.hm = hm;
   ps.wm = wm;
-  const bool full = ps.valid && dm == (1u << g.KD) - 1u && hm == (1u << g.KH) - 1u && wm == (1u << g.KW) - 1u;
+  const bool full = ps.valid && dm == low_bits(g.KD) && hm == low_bits(g.KH) && wm == low_bits(g.KW);
   ps.warp_full = __all_sync(0xffffffffu, full);
   const int64_t HW = (int64_t)g.H * g.W;
   const int64_t pos = (int64_t)id0 * HW + (int64_t)ih0 * g.W + iw0;  // may be negative (padding)

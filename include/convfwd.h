@@ -14,8 +14,13 @@
  *   - Pointers named x, w, bias, y are DEVICE pointers.  Dimension/hyper-
  *     parameter arrays (in_dims, k_dims, stride, pad, dilation, out_dims) and
  *     the descriptor structs are HOST memory, read during the call only.
- *   - The caller owns every buffer.  The library allocates no device memory and
- *     keeps no pointer after the call returns.  y must not overlap x, w or bias.
+ *   - The caller owns every buffer and the library keeps no pointer to one after
+ *     the call returns.  y must not overlap x, w or bias.  No call allocates
+ *     device memory.  Two things are held by the library itself: a 16 MiB
+ *     file-scope device array (the scratch of conv_fwd_nd_ws_noalloc), which
+ *     every device that loads the library holds until the process exits; and,
+ *     from the first conv_fwd_nd_host call on a device, two copy streams and
+ *     six events on that device, kept until exit.
  *   - All device work is enqueued on `stream` (NULL = legacy default stream);
  *     calls return without synchronising.  Errors from kernels that already
  *     ran surface at the caller's next synchronisation (cudaStreamSynchronize).

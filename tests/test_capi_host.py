@@ -1,10 +1,20 @@
 """Host-only checks of the C-ABI library: it loads, exports every symbol that
 include/convfwd.h declares, and rejects invalid requests with the documented
 status before touching a device.  No compute call runs here.
+
+Several checks hand the library made-up device addresses and rely on its host
+validation to refuse the call first.  So that a validation regression can never
+turn one of them into a kernel launch on a real GPU, the checks run in a child
+pytest process that sees no CUDA device (CUDA_VISIBLE_DEVICES=""): there a call
+that got past validation fails with CONV_ERR_CUDA instead of launching.  In
+any other process the module runs only the test that starts that child.
 """
 import ctypes
 import os
 import re
+import subprocess
+import sys
+import types
 
 import numpy as np
 import pytest
@@ -14,6 +24,24 @@ import oracle
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 HEADER = os.path.join(ROOT, "include", "convfwd.h")
+DEVICELESS = os.environ.get("CUDA_VISIBLE_DEVICES") == ""
+CHILD_RUNNER = "test_host_checks_run_in_a_deviceless_child"
+
+
+@pytest.fixture(autouse=True)
+def _deviceless_only(request):
+    if not DEVICELESS and request.node.name != CHILD_RUNNER:
+        pytest.skip("runs in the child process that sees no CUDA device")
+
+
+def test_host_checks_run_in_a_deviceless_child():
+    if DEVICELESS:
+        pytest.skip("this is the child")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider", os.path.abspath(__file__)],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-6000:] + r.stderr[-3000:]
+    assert " passed" in r.stdout and " failed" not in r.stdout
 
 
 @pytest.fixture(scope="module")
@@ -204,3 +232,66 @@ def test_bindings_reject_bad_tensors_before_any_device_call(lib):
         cf.conv_fwd_nd_ws(x, w)
     with pytest.raises(ValueError, match="5-D"):
         cf.conv3d_min_softmax(x, w)
+
+
+def test_noalloc_rejects_oversize_before_any_device_work(lib):
+    # two groups of 432 -> 128 channels, 3^3 taps: 2 x 128 x 11680 x 8 bytes (24 MB) of streamed weights
+    A = cf._arr
+    assert cf.workspace_bytes(1, 864, 256, (12, 12, 12), (3, 3, 3), 1, 0, 1, groups=2) > 16 << 20
+    st = lib.conv_fwd_nd_ws_noalloc(0x1000, 0x40000000, None, 0x80000000, 3, 1, 864, 256, 2, A((12, 12, 12)),
+                                    A((3, 3, 3)), A((1, 1, 1)), A((0, 0, 0)), A((1, 1, 1)), None)
+    assert st == cf.CONV_ERR_UNSUPPORTED
+    assert "scratch" in lib.conv_last_error().decode()
+
+
+def test_a_call_past_validation_cannot_launch_here(lib):
+    # the guard this module relies on: valid arguments reach the CUDA runtime, which sees no device
+    import torch
+    assert not torch.cuda.is_available()
+    A = cf._arr
+    st = lib.conv_fwd_nd_ex(0x1000, 0x2000, None, 0x10000000, 1, 1, 1, 1, A((8,)), A((3,)), A((1,)), A((0,)),
+                            A((1,)), cf.CONV_ALGO_DIRECT_FFMA, None)
+    assert st == cf.CONV_ERR_CUDA
+
+
+def _fake_cuda(index, shape=(1,)):
+    import torch
+    return types.SimpleNamespace(is_cuda=True, device=torch.device("cuda", index), shape=shape)
+
+
+def test_bindings_reject_tensors_on_different_devices(lib):
+    import torch
+    assert cf._one_cuda_device(_fake_cuda(0), _fake_cuda(0), None) == torch.device("cuda", 0)
+    with pytest.raises(ValueError, match="one CUDA device"):
+        cf._one_cuda_device(_fake_cuda(0), _fake_cuda(1))
+    with pytest.raises(ValueError, match="one CUDA device"):
+        cf._one_cuda_device(_fake_cuda(0), None, _fake_cuda(0), _fake_cuda(2))
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        cf._one_cuda_device(_fake_cuda(0), torch.zeros(1))
+
+
+def test_bindings_check_out_shape_dtype_and_layout(lib):
+    import torch
+    cf._check_out(torch.zeros((2, 3, 4)), (2, 3, 4), torch.float32)
+    with pytest.raises(ValueError, match="shape"):
+        cf._check_out(torch.zeros((2, 3, 5)), (2, 3, 4), torch.float32)   # a too-small or too-large out
+    with pytest.raises(ValueError, match="dtype"):
+        cf._check_out(torch.zeros((2, 3, 4), dtype=torch.float16), (2, 3, 4), torch.float32)
+    with pytest.raises(ValueError, match="contiguous"):
+        cf._check_out(torch.zeros((2, 4, 3)).transpose(1, 2), (2, 3, 4), torch.float32)
+    cl = torch.zeros((1, 5, 2, 3, 4)).to(memory_format=torch.channels_last_3d)
+    cf._check_out(cl, (1, 5, 2, 3, 4), torch.float32, channels_last=True)
+    with pytest.raises(ValueError, match="channels last"):
+        cf._check_out(torch.zeros((1, 5, 2, 3, 4)), (1, 5, 2, 3, 4), torch.float32, channels_last=True)
+
+
+def test_workspace_bindings_check_groups_and_out(lib):
+    import torch
+    x = torch.zeros((1, 4, 10))
+    with pytest.raises(ValueError, match="groups"):
+        cf._check_groups(4, 6, 4, 2)          # w.shape[1] must be C_in / groups
+    with pytest.raises(ValueError, match="groups"):
+        cf._check_groups(4, 6, 1, 4)          # 4 does not divide C_out = 6
+    cf._check_groups(4, 6, 2, 2)
+    with pytest.raises(ValueError, match="CUDA tensors"):
+        cf.conv_fwd_nd_noalloc(x, torch.zeros((6, 4, 3)))
