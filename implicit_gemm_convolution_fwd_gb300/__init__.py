@@ -23,7 +23,7 @@ EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_group
             "conv_host_workspace_bytes", "conv_fwd_nd_host",
             "conv_select_algo",
             "conv_algo_supported",
-            "conv3d_min_softmax",
+            "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma",
             "conv_status_string", "conv_last_error", "conv_device_status")
 
 
@@ -39,6 +39,11 @@ class Tensor5(ctypes.Structure):
 
 class Tensor4(ctypes.Structure):
     _fields_ = [("data", ctypes.c_void_p), ("dims", ctypes.c_int64 * 4)]
+
+
+class PeakResult(ctypes.Structure):
+    _fields_ = [("flops", ctypes.c_double), ("seconds", ctypes.c_double), ("event_ms", ctypes.c_double),
+                ("sm_mhz", ctypes.c_double), ("cycles_per_op", ctypes.c_double), ("ctas", ctypes.c_int)]
 
 
 _lib = None
@@ -76,13 +81,15 @@ def load(path: str | None = None):
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
                                        ctypes.POINTER(Tensor4), i32, vp]
+    lib.conv_peak_mma.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(PeakResult), vp]
+    lib.conv_peak_ffma.argtypes = [i32, i32, ctypes.POINTER(PeakResult), vp]
     lib.conv_status_string.argtypes = [i32]
     lib.conv_status_string.restype = ctypes.c_char_p
     lib.conv_last_error.argtypes = []
     lib.conv_last_error.restype = ctypes.c_char_p
     lib.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     for f in ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
-              "conv3d_min_softmax",
+              "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma",
               "conv_device_status"):
         getattr(lib, f).restype = i32
     _lib = lib
@@ -414,6 +421,29 @@ def conv_fwd_nd_host(x, w, bias=None, stride=1, pad=0, dilation=1, groups=1, chu
                                      workspace.numel() * workspace.element_size(), _stream_handle(stream, dev))
     _check(st)
     return out
+
+
+def _peak_dict(r):
+    return {"tflops": r.flops / r.seconds / 1e12 if r.seconds > 0 else 0.0, "seconds": r.seconds,
+            "event_ms": r.event_ms, "sm_mhz": r.sm_mhz, "cycles_per_op": r.cycles_per_op, "ctas": r.ctas,
+            "flops": r.flops}
+
+
+def peak_mma(kind="tf32", n=128, issuers=2, a_in_tmem=True, iters=20000, stream=None) -> dict:
+    """Measured tensor-core rate: back-to-back tcgen05.mma (M=128, N=n, one K step) from `issuers` warps
+    per SM on resident operands.  kind "tf32" or "bf16".  Synchronises the stream."""
+    r = PeakResult()
+    k = {"tf32": 0, "bf16": 1}[kind]
+    _check(load().conv_peak_mma(k, int(n), int(issuers), int(bool(a_in_tmem)), int(iters), ctypes.byref(r),
+                                _stream_handle(stream)))
+    return _peak_dict(r)
+
+
+def peak_ffma(packed=False, iters=4000, stream=None) -> dict:
+    """Measured FP32 FMA rate over every resident thread (scalar or packed f32x2).  Synchronises the stream."""
+    r = PeakResult()
+    _check(load().conv_peak_ffma(int(bool(packed)), int(iters), ctypes.byref(r), _stream_handle(stream)))
+    return _peak_dict(r)
 
 
 def device_status() -> int:

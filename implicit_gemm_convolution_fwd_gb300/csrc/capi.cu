@@ -1,5 +1,6 @@
 // C ABI entry points: argument validation, output-size arithmetic, kernel
 // family selection and dispatch.  Nothing here touches tensor data on the host.
+#include <stdarg.h>
 #include <stdio.h>
 #include <string.h>
 
@@ -255,6 +256,14 @@ HostLayout host_layout(const Geom &g, int64_t chunk) {
 int64_t host_chunk(int64_t N, int64_t chunk) { return (chunk <= 0 || chunk > N) ? (N > 0 ? N : 1) : chunk; }
 
 }  // namespace
+
+int convfwd::report_error(int status, const char *fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+  va_end(ap);
+  return status;
+}
 
 extern "C" {
 

@@ -65,4 +65,8 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
                                 cudaStream_t stream, float *ws = nullptr);
 cudaError_t read_and_clear_device_status(unsigned *flags);
 
+// Sets the calling thread's conv_last_error() text (printf format) and returns
+// `status`; CONV_OK with an empty message clears it.
+int report_error(int status, const char *fmt, ...);
+
 }  // namespace convfwd

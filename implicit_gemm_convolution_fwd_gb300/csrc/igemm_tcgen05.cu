@@ -258,11 +258,15 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
 // 16 consecutive reduction columns [k0, k0 + 16) of one output position.
 // toff[k]: input offset of column k from the receptive field's origin;
 // ttap[k]: kd | kh << 8 | kw << 16 (bit 31: padding column past Kred).
+// tap4: the reduction runs tap by tap over a channel count that is a
+// multiple of 4, so every aligned group of 4 columns shares one tap (and
+// padding columns come in whole groups).  Otherwise a group can straddle two
+// taps whose in-bounds tests differ, and each column is tested on its own.
 // Warps whose receptive fields are all inside the input read four offsets per
 // 16-byte shared load and skip every bounds test; only a unit that reaches the
 // padding columns checks them.
 __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
-                                            int Kred, bool tap_major, bool vec4, float (&v)[kUnit]) {
+                                            int Kred, bool tap4, bool vec4, float (&v)[kUnit]) {
   if (vec4) {
     // channels last, C % 4 == 0: columns 4q .. 4q+3 are 4 consecutive channels
     // of one tap, 16-byte aligned; one test per group, one 16-byte load
@@ -304,7 +308,7 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
         v[4 * q + 3] = k + 3 < Kred ? __ldg(ps.xo + o.w) : 0.f;
       }
     }
-  } else if (tap_major) {
+  } else if (tap4) {
     // columns 4q .. 4q+3 of the unit share one tap (and padding columns come
     // in whole groups, since Kred is then a multiple of 4)
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
@@ -546,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0, p.vec4 != 0, vu);
+          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0 && g.C % 4 == 0, p.vec4 != 0, vu);
         }
       }
     };

@@ -297,6 +297,42 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);
 
+/*
+ * Peak-rate microbenchmarks (diagnostics; not part of the convolution).  The
+ * pages reason about their kernels against the FP32 and tensor-core peaks of
+ * the GPU they name (l1_p60 page turn 1; l1_p76 page turn 2); these measure
+ * the corresponding peaks of the GPU at hand, at the clock it runs, so that
+ * roofline fractions rest on measured denominators.
+ *
+ * conv_peak_mma: one persistent CTA per SM; `issuers` (1-4) warps each issue
+ * `iters` (1-262144) back-to-back tcgen05.mma of shape M = 128 x N = n
+ * (16-256, a multiple of 16) x one K step, from one elected thread, on
+ * operands resident on chip: kind 0 = kind::tf32 (K = 8), kind 1 = kind::f16
+ * with BF16 operands (K = 16); A from tensor memory (a_in_tmem != 0) or shared
+ * memory, B from shared memory; fp32 accumulation in tensor memory.
+ * conv_peak_ffma: every resident thread runs 16 independent fp32 multiply-add
+ * chains, scalar fma.rn.f32 (packed == 0) or fma.rn.f32x2 on pairs (packed != 0),
+ * `iters` (1-1048576) rounds of 64 multiply-adds each.
+ * Both launch the kernel once untimed and once timed, synchronise `stream`
+ * before returning, and fill *out.  They allocate no device memory (their
+ * per-CTA stamps live in file-scope device arrays, so concurrent calls on one
+ * device race).  Errors: CONV_ERR_NULL, CONV_ERR_ARG for out-of-range
+ * arguments, CONV_ERR_CUDA (also when a bounded wait inside the MMA kernel gave up).
+ */
+typedef struct {
+  double flops;         /* operations of the timed launch (2 per multiply-add) */
+  double seconds;       /* earliest CTA start to latest CTA end, device global timer */
+  double event_ms;      /* the timed launch by CUDA events on `stream` */
+  double sm_mhz;        /* median over CTAs of SM clock cycles / global-timer ns during each CTA's run */
+  double cycles_per_op; /* MMA: SM cycles per MMA instruction on one SM; FFMA: SM cycles per warp-wide FMA
+                           instruction on one SM */
+  int ctas;             /* CTAs launched */
+} conv_peak_result_t;
+
+CONVFWD_API int conv_peak_mma(int kind, int n, int issuers, int a_in_tmem, int iters, conv_peak_result_t *out,
+                              conv_stream_t stream);
+CONVFWD_API int conv_peak_ffma(int packed, int iters, conv_peak_result_t *out, conv_stream_t stream);
+
 /* Static description of a status code. */
 CONVFWD_API const char *conv_status_string(int status);
 

@@ -437,6 +437,10 @@ def to_channels_last(a):
     (2, 2, 24, 96, (3, 3), (2, 1), (1, 2), (1, 2), 3),
     (1, 1, 64, 128, (3,), (3,), (0,), (4,), 2),                       # the long Conv1d's geometry, short
     (2, 1, 6, 20, (5, 2), (1, 1), (2, 0), (1, 1), 1),                 # C_out not a multiple of 4: scalar stores
+    # C_in % 4 != 0 with padding on every axis: groups of 4 reduction columns straddle taps whose
+    # in-bounds tests differ, so border positions must test every column on its own
+    (3, 1, 3, 40, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),
+    (2, 1, 5, 32, (3, 3), (2, 1), (1, 2), (1, 2), 2),
 ])
 def test_channels_last_conv(nd, groups, C_in, C_out, k, s, p, d, N):
     rng = np.random.default_rng(C_in * 13 + C_out + nd)
