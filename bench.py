@@ -10,10 +10,15 @@ L2 is flushed (a 2x-L2 buffer is written) before every step, outside the
 per-step CUDA events.  The line also carries:
   e2e          the same metric with the step's inputs copied host->device from
                pinned memory and the output copied back, inside the timing;
-  roofline     the dominant kernel's achieved rate against the measured peak;
+  roofline     the dominant kernel's achieved rate against its pipe's peak,
+               measured in the same run by the library's microbenchmarks
+               (tcgen05.mma TF32 / BF16, FP32 FMA; scaled to the SM's maximum
+               clock) or, for HBM-bound kernels, the measured copy bandwidth;
+  pipe_peaks   those measured peaks, with the clock of each measurement;
   cpu_baseline the fp64 oracle timed on a bounded sample on the host cores;
   per_config   the other workloads (fused conv3d+min+softmax, long Conv1d,
-               the two sweep shapes, the tiny Conv1d), each timed the same way.
+               the two sweep shapes, the tiny Conv1d), each timed the same way,
+               each with its own oracle timing on a smaller bounded sample.
 With --impl reference the oracle itself is the measured implementation.
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the problem shards by batch with no exchange); value sums all ranks' work
@@ -41,9 +46,10 @@ HEADLINE = "conv3d_asym"
 EXTRA = ["conv3d_min_softmax", "conv1d_long", "conv3d_sweep_a", "conv3d_sweep_b", "conv1d_tiny"]
 METRIC = "conv GFLOP/s and % of GB300 roofline (fp32/TF32 or HBM) per config, 1 GPU"
 PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
-SM_COUNT_NOMINAL, FP32_LANES_PER_SM, SM_MAX_MHZ_NOMINAL = 152, 128, 2070.0
-BF16_TO_TF32 = 1.1 / 2.25  # nominal dense tensor-core ratio TF32 : BF16
+SM_MAX_MHZ_NOMINAL = 2070.0
+BF16_TO_TF32 = 1.1 / 2.25  # nominal dense tensor-core ratio TF32 : BF16 (for the secondary, derived figure)
 CPU_BASELINE_MACS = 8e9     # ~10-20 s of the oracle on the host cores
+CONFIG_ORACLE_MACS = 2e9    # ~1-3 s of the oracle per extra config
 REFERENCE_STEP_MACS = 1e9   # one reference-arm step: a ~1-2 s slab of the workload
 
 
@@ -58,6 +64,26 @@ def load_peaks():
     except Exception:
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
                 "sm_max_mhz": SM_MAX_MHZ_NOMINAL}, "fallback"
+
+
+def measure_pipe_peaks(cf, sm_max_mhz):
+    """Peak rates of the pipes the kernels use, measured here by the library's microbenchmarks
+    (conv_peak_mma, conv_peak_ffma), each scaled from the SM clock of its own run to the SM's
+    maximum clock: the conservative denominator for a kernel timed at any clock up to it."""
+    out = {}
+    runs = {
+        "tf32": [cf.peak_mma("tf32", 256, iss, True, 4000) for iss in (2, 4)],
+        "bf16": [cf.peak_mma("bf16", 256, iss, True, 4000) for iss in (2, 4)],
+        "ffma": [cf.peak_ffma(packed, 3000) for packed in (False, True)],
+    }
+    for name, rs in runs.items():
+        r = max(rs, key=lambda d: d["tflops"])
+        scale = sm_max_mhz / r["sm_mhz"] if r["sm_mhz"] > 0 else 1.0
+        out[name] = {"tflops": r["tflops"] * scale, "measured_tflops": r["tflops"], "measured_mhz": r["sm_mhz"],
+                     "scaled_to_mhz": sm_max_mhz, "cycles_per_op": r["cycles_per_op"]}
+    out["tf32x3"] = {"tflops": out["tf32"]["tflops"] / 3.0, "note": "three TF32 products per fp32 multiply-add"}
+    out["source"] = "microbenchmark"
+    return out
 
 
 def problem_counts(wl, out_dims, esize=4):
@@ -310,7 +336,7 @@ VARIANTS = [
 ]
 
 
-def run_variants(dev, peaks, steps):
+def run_variants(dev, peaks, pipes, steps):
     """ms and throughput of each VARIANTS entry (CUDA events, L2 flushed, median)."""
     import torch
     out = {}
@@ -325,10 +351,12 @@ def run_variants(dev, peaks, steps):
         flops /= r.groups  # each output channel sums over C_in / groups input channels
         entry = {"ms": m, "ms_min": min(times), "tflops": flops / (m * 1e-3) / 1e12}
         if r.dtype is None and r.wl.kind == "conv":
-            tf32x3 = peaks["bf16_tflops"] * BF16_TO_TF32 / 3.0
-            entry["frac_of_3xtf32_peak"] = entry["tflops"] / tf32x3
+            entry["frac_of_3xtf32_peak"] = entry["tflops"] / pipes["tf32x3"]["tflops"]
         if r.dtype is not None:
-            entry["frac_of_measured_bf16_peak"] = entry["tflops"] / peaks["bf16_tflops"]
+            entry["frac_of_bf16_peak"] = entry["tflops"] / pipes["bf16"]["tflops"]
+            entry["frac_of_cublas_bf16"] = entry["tflops"] / peaks["bf16_tflops"]
+        if r.dtype is None and r.wl.kind == "fused":
+            entry["frac_of_ffma_peak"] = entry["tflops"] / pipes["ffma"]["tflops"]
         out[name] = entry
         del r
     return out
@@ -378,41 +406,43 @@ def traffic_for(algo, wl):
     return e["bytes"] * wl.N / e["batch"]
 
 
-def roofline_for(runner, peaks, ms, sustained=False):
-    """Roofline entry for the one kernel a step launches."""
+def roofline_for(runner, peaks, pipes, ms):
+    """Roofline entry for the one kernel a step launches.  Compute peaks are the measured pipe peaks
+    (`pipes`, see measure_pipe_peaks); HBM is MEASURED_PEAKS.json's copy bandwidth."""
     wl = runner.wl
     flops, bytes_alg, _, _ = problem_counts(wl, runner.out_dims, runner.y.element_size())
     t = ms * 1e-3
     hbm_peak = peaks["hbm_gbs"]
     if runner.algo in ("igemm_3xtf32", "igemm_3xtf32_streamed"):
-        bf16 = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        peak = bf16 * BF16_TO_TF32 / 3.0  # three TF32 products per fp32 MAC
-        compute = {"bound": "tensor", "peak": peak, "peak_note": "TF32 = measured bf16 x 1.1/2.25, /3 for 3xTF32"}
+        compute = {"bound": "tensor", "peak": pipes["tf32x3"]["tflops"],
+                   "peak_note": "measured TF32 tcgen05.mma rate / 3 products (3xTF32)",
+                   "derived_peak": peaks["bf16_tflops"] * BF16_TO_TF32 / 3.0}
     elif runner.algo in ("igemm_bf16", "igemm_fp16"):
-        peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"]
-        compute = {"bound": "tensor", "peak": peak, "peak_note": "measured dense bf16 (fp16 the same rate)"}
+        compute = {"bound": "tensor", "peak": pipes["bf16"]["tflops"],
+                   "peak_note": "measured BF16 tcgen05.mma rate (FP16 the same)", "derived_peak": peaks["bf16_tflops"]}
     else:
-        peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12
-        compute = {"bound": "alu", "peak": peak, "peak_note": "152 SMs x 128 FP32 lanes x 2 x 2070 MHz"}
+        compute = {"bound": "alu", "peak": pipes["ffma"]["tflops"], "peak_note": "measured FP32 FMA rate",
+                   "derived_peak": None}
     t_compute = flops / (compute["peak"] * 1e12)
     t_mem = bytes_alg / (hbm_peak * 1e9)
     # the fraction against the faster of the two fp32-accurate pipes, whichever
     # the kernel uses, so that the choice of path cannot flatter the number
-    ffma_peak = SM_COUNT_NOMINAL * FP32_LANES_PER_SM * 2 * SM_MAX_MHZ_NOMINAL * 1e6 / 1e12
-    tf32x3_peak = peaks["bf16_tflops_sustained" if sustained else "bf16_tflops"] * BF16_TO_TF32 / 3.0
-    best = max(ffma_peak, tf32x3_peak)
+    best = max(pipes["ffma"]["tflops"], pipes["tf32x3"]["tflops"])
     t_best = max(flops / (best * 1e12), t_mem)
     frac_best = t_best / t
+    common = {"traffic": traffic_for(runner.algo, wl), "algorithmic_bytes": bytes_alg, "frac_best_path": frac_best,
+              "peak_source": pipes["source"], "peak_mhz": pipes["tf32"]["scaled_to_mhz"]}
     if t_mem > t_compute:
-        return {"bound": "hbm", "achieved": bytes_alg / t / 1e9, "peak": hbm_peak, "unit": "GB/s",
-                "frac": (bytes_alg / t / 1e9) / hbm_peak, "traffic": traffic_for(runner.algo, wl),
-                "algorithmic_bytes": bytes_alg,
-                "compute_frac": (flops / t / 1e12) / compute["peak"], "frac_best_path": frac_best}
+        return dict(common, bound="hbm", achieved=bytes_alg / t / 1e9, peak=hbm_peak, unit="GB/s",
+                    frac=(bytes_alg / t / 1e9) / hbm_peak, compute_frac=(flops / t / 1e12) / compute["peak"],
+                    peak_note="measured copy bandwidth (MEASURED_PEAKS.json)")
     ach = flops / t / 1e12
-    return {"bound": compute["bound"], "achieved": ach, "peak": compute["peak"], "unit": "TFLOP/s",
-            "frac": ach / compute["peak"], "traffic": traffic_for(runner.algo, wl), "algorithmic_bytes": bytes_alg,
-            "peak_note": compute["peak_note"],
-            "hbm_frac": (bytes_alg / t / 1e9) / hbm_peak, "frac_best_path": frac_best}
+    out = dict(common, bound=compute["bound"], achieved=ach, peak=compute["peak"], unit="TFLOP/s",
+               frac=ach / compute["peak"], peak_note=compute["peak_note"], hbm_frac=(bytes_alg / t / 1e9) / hbm_peak)
+    if compute["derived_peak"]:
+        out["derived_peak"] = compute["derived_peak"]
+        out["frac_of_derived_peak"] = ach / compute["derived_peak"]
+    return out
 
 
 # ----------------------------------------------------------- oracle legs
@@ -516,7 +546,10 @@ def main():
 
     import __graft_entry__
     __graft_entry__.build()
+    import implicit_gemm_convolution_fwd_gb300 as cf
     peaks, peaks_src = load_peaks()
+    sm_max_mhz = float(peaks.get("sm_max_mhz") or SM_MAX_MHZ_NOMINAL)
+    pipes = measure_pipe_peaks(cf, sm_max_mhz)  # before the timed region
 
     if args.dtype != "f32" or args.workspace:
         dt = {"f32": None, "bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
@@ -549,8 +582,8 @@ def main():
 
     e2e_ms, h2d, d2h = runner.timed_e2e(max(3, args.steps // 4), 2)
     e2e_ms = slowest_rank_ms(e2e_ms, world, dev)
-    roof = roofline_for(runner, peaks, ms)
-    roof["peak_source"] = peaks_src
+    roof = roofline_for(runner, peaks, pipes, ms)
+    roof["hbm_peak_source"] = peaks_src
     roof["kernel"] = runner.algo
     clocks = clk.summary()
 
@@ -565,16 +598,18 @@ def main():
             m = statistics.median(times)
             m_warm = statistics.median(r.timed(max(5, args.steps // 4), 2, flush=False))
             f, bts, _, _ = problem_counts(r.wl, r.out_dims)
-            rf = roofline_for(r, peaks, m)
+            rf = roofline_for(r, peaks, pipes, m)
             per_config[name] = {"algo": r.algo, "ms": m, "ms_min": min(times), "gflops": f / (m * 1e-3) / 1e9,
                                 "gbs": bts / (m * 1e-3) / 1e9, "roofline_bound": rf["bound"],
                                 "roofline_frac": rf["frac"], "roofline_peak": rf["peak"], "unit": rf["unit"],
                                 "roofline_frac_best_path": rf["frac_best_path"], "ms_l2_warm": m_warm}
+            if "frac_of_derived_peak" in rf:
+                per_config[name]["roofline_frac_of_derived_peak"] = rf["frac_of_derived_peak"]
             del r
             torch.cuda.empty_cache()
     variants = {}
     if not args.no_extra and not args.no_variants and rank == 0:
-        variants = run_variants(dev, peaks, max(5, args.steps // 4))
+        variants = run_variants(dev, peaks, pipes, max(5, args.steps // 4))
         torch.cuda.empty_cache()
 
     cpu = None
@@ -582,6 +617,11 @@ def main():
         v, dt, threads, sample = time_oracle(wl, CPU_BASELINE_MACS)
         cpu = {"value": v, "unit": "GFLOP/s", "cores": threads, "kind": "oracle", "sample": sample,
                "seconds": dt}
+        # the oracle beside every other config too, on a smaller bounded sample each
+        for name, entry in per_config.items():
+            cv, cdt, cthreads, csample = time_oracle(synth.WORKLOADS[name], CONFIG_ORACLE_MACS)
+            entry["cpu_baseline"] = {"value": cv, "unit": "GFLOP/s", "cores": cthreads, "kind": "oracle",
+                                     "sample": csample, "seconds": cdt, "gpu_over_cpu": entry["gflops"] / cv}
 
     if world > 1:
         dist.barrier()
@@ -605,6 +645,7 @@ def main():
                              else "pinned host copies around the device call")},
             "gpu_launches": runner.launches_per_step() * args.steps,
             "roofline": roof, "clocks": clocks, "cpu_baseline": cpu, "per_config": per_config, "other_entry_points": variants,
+            "pipe_peaks": pipes,
         }
         print(json.dumps(line))
     if world > 1:
