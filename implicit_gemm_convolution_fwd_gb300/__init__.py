@@ -23,7 +23,7 @@ EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_group
             "conv_host_workspace_bytes", "conv_fwd_nd_host",
             "conv_select_algo",
             "conv_algo_supported",
-            "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma",
+            "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma", "conv_debug_set_wait_limit",
             "conv_status_string", "conv_last_error", "conv_device_status")
 
 
@@ -88,8 +88,9 @@ def load(path: str | None = None):
     lib.conv_last_error.argtypes = []
     lib.conv_last_error.restype = ctypes.c_char_p
     lib.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+    lib.conv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
     for f in ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
-              "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma",
+              "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma", "conv_debug_set_wait_limit",
               "conv_device_status"):
         getattr(lib, f).restype = i32
     _lib = lib
@@ -444,6 +445,12 @@ def peak_ffma(packed=False, iters=4000, stream=None) -> dict:
     r = PeakResult()
     _check(load().conv_peak_ffma(int(bool(packed)), int(iters), ctypes.byref(r), _stream_handle(stream)))
     return _peak_dict(r)
+
+
+def set_wait_limit(cycles: int = 0):
+    """Test hook: tensor-core launches from now on give up a pipeline wait after `cycles` SM clock cycles
+    (0 restores the default, about two seconds).  Process-wide."""
+    _check(load().conv_debug_set_wait_limit(int(cycles)))
 
 
 def device_status() -> int:

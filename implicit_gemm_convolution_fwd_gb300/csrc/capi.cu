@@ -607,6 +607,13 @@ int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const f
   return CONV_OK;
 }
 
+int conv_debug_set_wait_limit(long long cycles) {
+  g_last_error[0] = 0;
+  if (cycles > 0 && cycles < 64) return fail(CONV_ERR_ARG, "conv_debug_set_wait_limit: at least 64 cycles%s");
+  convfwd::set_wait_limit(cycles);
+  return CONV_OK;
+}
+
 int conv_device_status(unsigned int *flags) {
   g_last_error[0] = 0;
   if (!flags) return fail(CONV_ERR_NULL, "conv_device_status: flags is NULL%s");

@@ -64,6 +64,9 @@ size_t igemm_stream_bytes_one_group(const Geom &g);
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
                                 cudaStream_t stream, float *ws = nullptr);
 cudaError_t read_and_clear_device_status(unsigned *flags);
+// Clock cycles after which the tensor-core kernels' pipeline waits give up,
+// for launches from now on (cycles <= 0: the default, about two seconds).
+void set_wait_limit(long long cycles);
 
 // Sets the calling thread's conv_last_error() text (printf format) and returns
 // `status`; CONV_OK with an empty message clears it.

@@ -37,6 +37,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "conv_internal.cuh"
 #include "sm100_ptx.cuh"
 
@@ -59,8 +61,8 @@ constexpr int kMaxNpad = 128;
 constexpr int kMaxSmem = 227 * 1024;
 constexpr int kMinSmem = 116 * 1024;  // keeps one CTA per SM, so TMEM allocation never contends
 constexpr int kMaxStages = 2 * kMaxSlots;     // two A stages per slot
-// a_full, a_empty [stages], d_full, d_empty [slots], drain, b_full [stages] (streamed weights)
-constexpr int kNumBars = 3 * kMaxStages + 2 * kMaxSlots + 1;
+// a_full, a_empty [stages], d_full, d_empty [slots], b_full [stages] (streamed weights), drain [slots]
+constexpr int kNumBars = 3 * kMaxStages + 3 * kMaxSlots;
 constexpr long long kWaitLimitCycles = 1ll << 32;  // about two seconds
 
 struct IgemmParams {
@@ -97,6 +99,10 @@ struct IgemmParams {
   // twin B stage with a bulk copy
   const float *__restrict__ wsp;  // this launch's chunks: chunk q at wsp + q * sb_stage_bytes / 4
   uint32_t sb_stage_bytes;        // 2 * Npad * KC * 4
+  // clock cycles after which a pipeline wait gives up (kWaitLimitCycles unless
+  // a test shortened it); the waits that guard TMEM release always use
+  // kWaitLimitCycles
+  long long wait_limit;
 };
 
 struct Plan {
@@ -177,14 +183,18 @@ __device__ __forceinline__ int64_t cta_tile_count(const IgemmParams &p) {
 // Bounded mbarrier wait.  Returns false (and raises the abort flag plus the
 // device status bit on timeout) when the phase did not complete.  The first
 // test is inline; the polling loop, which reads the abort flag and the clock
-// every 16 polls, is out of line so that the roles' loops stay short.
-__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+// every 16 polls (every poll when a test has shortened the limit: one poll
+// can block for a few thousand cycles), is out of line so that the roles'
+// loops stay short.
+__device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                             long long limit) {
   const long long t0 = clock64();
+  const uint32_t check_mask = limit < kWaitLimitCycles ? 0u : 15u;
   for (uint32_t i = 1;; ++i) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0) {
+    if ((i & check_mask) == 0) {
       if (*abort_flag) return false;
-      if (clock64() - t0 > kWaitLimitCycles) {
+      if (clock64() - t0 > limit) {
         *abort_flag = 1;
         atomicOr(&g_device_status, kStatusIgemmWatchdog);
         return false;
@@ -192,9 +202,10 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
     }
   }
 }
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag) {
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
+                                           long long limit) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, abort_flag);
+  return wait_phase_slow(bar, parity, abort_flag, limit);
 }
 
 __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_uint(v) & 0xffffe000u; }
@@ -356,8 +367,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   const uint32_t bar_a_empty = ptx::smem_addr(bars + kMaxStages);                      // [stages]
   const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kMaxStages);                   // [slots]
   const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kMaxStages + kMaxSlots);      // [slots]
-  const uint32_t bar_drain = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots);
-  const uint32_t bar_b_full = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots + 1);  // [stages]
+  const uint32_t bar_b_full = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots);      // [stages]
+  const uint32_t bar_drain = ptx::smem_addr(bars + 3 * kMaxStages + 2 * kMaxSlots);       // [slots]
   const int nslots = p.nslots;
 
   const uint32_t SBO = (uint32_t)p.Kpad * 32;  // bytes between 8-row groups of B
@@ -420,10 +431,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::mbar_init(bar_b_full + 8 * s, 1);
     }
     for (int b = 0; b < kMaxSlots; ++b) {
+      ptx::mbar_init(bar_drain + 8 * b, 1);
       ptx::mbar_init(bar_d_full + 8 * b, 1);
       ptx::mbar_init(bar_d_empty + 8 * b, 128);
     }
-    ptx::mbar_init(bar_drain, nslots);
     *abort_flag = 0;
     ptx::fence_mbar_init();
   }
@@ -443,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     for (int64_t it = 0; it < my_tiles; ++it) {
       const int64_t tile = tile_of(p, it);
       const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
-      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag);
+      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const int64_t m = tile * kTileM + tid;
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
       const int ncols = min(p.KC, p.Kpad - q * p.KC);
       const uint32_t r = (uint32_t)(lg >> 1);
-      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag);
+      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit);
       if (!__all_sync(0xffffffffu, ok)) return false;
       ptx::tc_fence_after();
       if (SB && t == 0) {
@@ -668,13 +679,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
       const int64_t li = it / nslots;
-      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag))) break;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag, p.wait_limit))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t lg = li * p.nchunks + q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
-        bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag);
-        if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag);
+        bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit);
+        if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag, p.wait_limit);
         if (!__all_sync(0xffffffffu, ok)) {
           aborted = true;
           break;
@@ -708,9 +719,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     if (*abort_flag) {
       // drain: every MMA this warp issued completes before TMEM is released
       if (ptx::elect_one()) {
-        ptx::mma_commit(bar_drain);
+        ptx::mma_commit(bar_drain + 8 * slot);
         const long long t0 = clock64();
-        while (!ptx::mbar_try_wait(bar_drain, 0) && clock64() - t0 < kWaitLimitCycles) {
+        while (!ptx::mbar_try_wait(bar_drain + 8 * slot, 0) && clock64() - t0 < kWaitLimitCycles) {
         }
       }
       __syncwarp();
@@ -759,6 +770,8 @@ __global__ void split_weights_kernel(const float *__restrict__ w, float *__restr
 #include "igemm_bf16.cuh"
 
 int g_num_sms[64] = {0};
+// the pipeline waits' limit for the next launches (set_wait_limit)
+std::atomic<long long> g_wait_limit{kWaitLimitCycles};
 bool g_attr_bf16_set[64] = {false};
 bool g_attr_f16_set[64] = {false};
 bool g_attr_set[64] = {false};
@@ -837,6 +850,8 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     IgemmParams p = {};
+  p.wait_limit = g_wait_limit.load();
+    p.wait_limit = g_wait_limit.load();
     p.x = x;
     p.w = w;
     p.bias = bias;
@@ -881,6 +896,9 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       const int k_begin = pass * pl.kpass;
       const int kred = (int)(kfull - k_begin < pl.kpass ? kfull - k_begin : pl.kpass);
       IgemmParams p = {};
+  p.wait_limit = g_wait_limit.load();
+      p.wait_limit = g_wait_limit.load();
+    p.wait_limit = g_wait_limit.load();
       p.x = x;
       p.w = w + o0 * kfull;
       p.bias = bias ? bias + o0 : nullptr;
@@ -943,6 +961,7 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
     attr_set = true;
   }
   IgemmParams p = {};
+  p.wait_limit = g_wait_limit.load();
   p.xh = x;
   p.wh = w;
   p.bh = bias;
@@ -968,6 +987,8 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
     igemm_bf16_kernel<false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
+
+void set_wait_limit(long long cycles) { g_wait_limit.store(cycles > 0 ? cycles : kWaitLimitCycles); }
 
 cudaError_t read_and_clear_device_status(unsigned *flags) {
   cudaError_t e = cudaDeviceSynchronize();

@@ -339,6 +339,21 @@ CONVFWD_API const char *conv_status_string(int status);
 /* Reason for the most recent non-OK return on the calling thread ("" if none). */
 CONVFWD_API const char *conv_last_error(void);
 
+/*
+ * Test hook for the bounded waits (the paper has no counterpart): sets, for
+ * every tensor-core launch made after the call in this process, the number
+ * of SM clock cycles after which a pipeline wait inside the kernel gives up
+ * (cycles <= 0 restores the default, about two seconds; 1-63 is CONV_ERR_ARG).
+ * A kernel whose wait gives up stops its work, lets every role fall through,
+ * waits for its own MMAs and copies with the full default limit, frees its
+ * tensor memory, sets bit 0 of the device status word and returns: its output
+ * is incomplete, and conv_device_status() reports it.  A limit of a few
+ * hundred cycles makes the waits run out on purpose, so that tests can check
+ * that this path leaves the device usable.  Process-wide; set it only while
+ * no other thread launches convolutions.
+ */
+CONVFWD_API int conv_debug_set_wait_limit(long long cycles);
+
 /* Synchronises the current device, then returns and clears the device-side
  * status word: 0 when no kernel gave up on a bounded wait since the last call,
  * else a bit set per kernel family that did (bit 0: tensor-core path).  Writes
