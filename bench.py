@@ -281,9 +281,11 @@ class VariantRunner(OurRunner):
     """A benchmark workload run through one of the library's other entry points:
     16-bit tensors, the min over another dim, channels-last tensors or groups."""
 
-    def __init__(self, wl, device, dtype=None, min_dim=None, channels_last=False, groups=1, workspace=False):
+    def __init__(self, wl, device, dtype=None, min_dim=None, channels_last=False, groups=1, workspace=False,
+                 fused_algo=None):
         super().__init__(wl, device)
         torch = self.torch
+        self.fused_algo = self.cf.CONV_ALGO_AUTO if fused_algo is None else getattr(self.cf, fused_algo)
         self.dtype, self.channels_last, self.groups = dtype, channels_last, groups
         self.ws = None
         self.ws_stream = 0  # workspace bytes for streamed weights
@@ -313,7 +315,8 @@ class VariantRunner(OurRunner):
 
     def step(self):
         if self.wl.kind == "fused":
-            self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.min_dim, out=self.y, stream=self.stream)
+            self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.min_dim, out=self.y, stream=self.stream,
+                                       algo=self.fused_algo)
         elif self.ws is not None:
             self.cf.conv_fwd_nd_ws(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation,
                                    workspace=self.ws, out=self.y, stream=self.stream)
@@ -329,6 +332,7 @@ VARIANTS = [
     ("conv1d_long[bf16]", "conv1d_long", {"dtype": "bfloat16"}),
     ("conv3d_min_softmax[min_dim=3]", "conv3d_min_softmax", {"min_dim": 3}),
     ("conv3d_min_softmax[min_dim=4]", "conv3d_min_softmax", {"min_dim": 4}),
+    ("conv3d_min_softmax[tensor cores]", "conv3d_min_softmax", {"fused_algo": "CONV_ALGO_IGEMM_3XTF32"}),
     ("conv3d_sweep_b[channels_last]", "conv3d_sweep_b", {"channels_last": True}),
     ("conv3d_sweep_b[groups=2]", "conv3d_sweep_b", {"groups": 2}),
     ("conv3d_wide_k[workspace]", "conv3d_wide_k", {"workspace": True}),
@@ -356,7 +360,10 @@ def run_variants(dev, peaks, pipes, steps):
             entry["frac_of_bf16_peak"] = entry["tflops"] / pipes["bf16"]["tflops"]
             entry["frac_of_cublas_bf16"] = entry["tflops"] / peaks["bf16_tflops"]
         if r.dtype is None and r.wl.kind == "fused":
-            entry["frac_of_ffma_peak"] = entry["tflops"] / pipes["ffma"]["tflops"]
+            if r.fused_algo == r.cf.CONV_ALGO_IGEMM_3XTF32:
+                entry["frac_of_3xtf32_peak"] = entry["tflops"] / pipes["tf32x3"]["tflops"]
+            else:
+                entry["frac_of_ffma_peak"] = entry["tflops"] / pipes["ffma"]["tflops"]
         out[name] = entry
         del r
     return out

@@ -23,7 +23,8 @@ EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_group
             "conv_host_workspace_bytes", "conv_fwd_nd_host",
             "conv_select_algo",
             "conv_algo_supported",
-            "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma", "conv_debug_set_wait_limit",
+            "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv_peak_mma", "conv_peak_ffma",
+            "conv_debug_set_wait_limit",
             "conv_status_string", "conv_last_error", "conv_device_status")
 
 
@@ -81,6 +82,8 @@ def load(path: str | None = None):
     lib.conv_algo_supported.argtypes = [i32, i64, i64, i64, arr, arr, arr, arr, arr, i32]
     lib.conv3d_min_softmax.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
                                        ctypes.POINTER(Tensor4), i32, vp]
+    lib.conv3d_min_softmax_ex.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
+                                          ctypes.POINTER(Tensor4), i32, i32, vp]
     lib.conv_peak_mma.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(PeakResult), vp]
     lib.conv_peak_ffma.argtypes = [i32, i32, ctypes.POINTER(PeakResult), vp]
     lib.conv_status_string.argtypes = [i32]
@@ -90,7 +93,8 @@ def load(path: str | None = None):
     lib.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.conv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
     for f in ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
-              "conv3d_min_softmax", "conv_peak_mma", "conv_peak_ffma", "conv_debug_set_wait_limit",
+              "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv_peak_mma", "conv_peak_ffma",
+            "conv_debug_set_wait_limit",
               "conv_device_status"):
         getattr(lib, f).restype = i32
     _lib = lib
@@ -259,11 +263,12 @@ def conv_fwd_nd(x, w, bias=None, stride=1, pad=0, dilation=1, out=None, algo=CON
     return out
 
 
-def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None):
+def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None, algo=CONV_ALGO_AUTO):
     """softmax over channels of the min over tensor dim `min_dim` (2 = depth, 3 = height, 4 = width)
     of conv3d(x, w) + bias, for contiguous fp32 CUDA tensors (stride 1, no padding).  The result
     keeps the two other spatial dims: [N, C_out, OH, OW], [N, C_out, OD, OW] or [N, C_out, OD, OH].
-    The conv's output dims come from the library (conv_out_dims)."""
+    The conv's output dims come from the library (conv_out_dims).  `algo`: CONV_ALGO_AUTO (the planner),
+    CONV_ALGO_DIRECT_FFMA or CONV_ALGO_IGEMM_3XTF32."""
     import torch
     if x.dim() != 5 or w.dim() != 5:
         raise ValueError("x and w must be 5-D")
@@ -284,9 +289,9 @@ def conv3d_min_softmax(x, w, bias=None, min_dim=2, out=None, stream=None):
     wd = Tensor5(w.data_ptr(), (ctypes.c_int64 * 5)(*w.shape))
     yd = Tensor4(out.data_ptr(), (ctypes.c_int64 * 4)(*out.shape))
     with torch.cuda.device(dev):
-        st = load().conv3d_min_softmax(ctypes.byref(xd), ctypes.byref(wd),
-                                       None if bias is None else bias.data_ptr(), ctypes.byref(yd), int(min_dim),
-                                       _stream_handle(stream, dev))
+        st = load().conv3d_min_softmax_ex(ctypes.byref(xd), ctypes.byref(wd),
+                                          None if bias is None else bias.data_ptr(), ctypes.byref(yd), int(min_dim),
+                                          int(algo), _stream_handle(stream, dev))
     _check(st)
     return out
 

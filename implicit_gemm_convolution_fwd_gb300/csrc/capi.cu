@@ -566,6 +566,11 @@ int conv_fwd_nd(const float *x, const float *w, const float *bias, float *y, int
 
 int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream) {
+  return conv3d_min_softmax_ex(x, w, bias, y, min_dim, CONV_ALGO_AUTO, stream);
+}
+
+int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
+                          int min_dim, int algo, conv_stream_t stream) {
   g_last_error[0] = 0;
   if (!x || !w || !y) return fail(CONV_ERR_NULL, "conv3d_min_softmax: descriptor pointer is NULL%s");
   if (!w->data || (x->dims[0] != 0 && (!x->data || !y->data)))
@@ -597,12 +602,27 @@ int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const f
     return fail(CONV_ERR_SHAPE,
                 "conv3d_min_softmax: y dims must be [N, C_out] + the conv's spatial output dims without dim "
                 "min_dim%s");
-  const char *why = "";
-  if (!convfwd::fused_supported(g, min_dim, &why))
-    return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
+  const char *why = "", *why_tc = "";
+  const bool ffma_ok = convfwd::fused_supported(g, min_dim, &why);
+  const bool tc_ok = convfwd::igemm_fused_supported(g, min_dim, &why_tc);
+  // planner: the FFMA kernels for short reductions over few channels (the
+  // page's C_in = 3, C_out = 24 shape among them), where the tensor-core
+  // kernel's im2col gather costs more than the FFMAs; the tensor-core kernel
+  // for longer reductions or more channels; whichever runs otherwise
+  if (algo == CONV_ALGO_AUTO)
+    algo = tc_ok && !(ffma_ok && convfwd::fused_ffma_preferred(g)) ? CONV_ALGO_IGEMM_3XTF32 : CONV_ALGO_DIRECT_FFMA;
+  if (algo == CONV_ALGO_DIRECT_FFMA) {
+    if (!ffma_ok) return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
+  } else if (algo == CONV_ALGO_IGEMM_3XTF32) {
+    if (!tc_ok) return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why_tc);
+  } else {
+    return fail(CONV_ERR_ARG, "conv3d_min_softmax: unknown algo %s%lld", "", algo);
+  }
   if (g.N == 0) return CONV_OK;  // empty batch
   cudaError_t e =
-      convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream);
+      algo == CONV_ALGO_IGEMM_3XTF32
+          ? convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream)
+          : convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream);
   if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: kernel launch");
   return CONV_OK;
 }

@@ -45,6 +45,15 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
 // True when launch_fused_min_softmax supports this geometry (channel count,
 // kernel extent along the output's last axis, shared-memory footprint).
 bool fused_supported(const Geom &g, int min_dim, const char **why);
+// True when the FFMA fused kernel measures faster than the tensor-core one on
+// this geometry (both able to run it).
+bool fused_ffma_preferred(const Geom &g);
+
+// The same fused op on the tensor cores (3xTF32): min over depth only,
+// C_out <= 32, weights resident in one pass.
+bool igemm_fused_supported(const Geom &g, int min_dim, const char **why);
+cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
+                                           cudaStream_t stream);
 
 // Tensor-core implicit GEMM on 16-bit tensors (bfloat16, or float16 when fp16; bit patterns),
 // fp32 accumulation, output in the input type.

@@ -636,6 +636,19 @@ bool fused_supported(const Geom &g, int min_dim, const char **why) {
   return true;
 }
 
+bool fused_ffma_preferred(const Geom &g) {
+  // Measured on GB300 against the tensor-core fused kernel on [N, C_in, 24,
+  // 32, 32] inputs with 3x3x3 kernels and N * C_in held near 384: the FFMA
+  // kernel wins for C_out <= 24 (two channel groups) up to C_in = 8 (0.21
+  // against 0.49 ms at C_in = 3, 0.33 against 0.47 at C_in = 8) and loses from
+  // C_in = 12 on (1.10 against 0.47); with four channel groups (C_out = 32
+  // runs 48 channels) it wins only at C_in = 1 (0.61 against 0.65) and loses
+  // from C_in = 3 on (0.66 against 0.49).
+  const int64_t kred = g.C * g.taps();
+  const int ncg = pick_ncg(g.K);
+  return (ncg <= 2 && kred <= 256) || kred <= 32;
+}
+
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
                                      const Geom &g, int min_dim, cudaStream_t stream) {
   FusedParams p;

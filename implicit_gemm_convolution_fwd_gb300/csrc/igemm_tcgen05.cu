@@ -103,6 +103,11 @@ struct IgemmParams {
   // a test shortened it); the waits that guard TMEM release always use
   // kWaitLimitCycles
   long long wait_limit;
+  // fused conv3d -> min over depth -> channel softmax (the FUSED kernel): a
+  // column is (image, block of 128 positions of the output plane); each CTA
+  // runs its columns' OD depth tiles back to back
+  int64_t columns;  // N * hw_tiles
+  int hw_tiles;     // ceil(OH * OW / 128)
 };
 
 struct Plan {
@@ -172,11 +177,20 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
 }
 
 // The CTA's tile order: its it-th tile (it = 0, 1, ...) is tile_of(p, it),
-// cyclic over the grid so that all SMs sweep the output together.
+// cyclic over the grid so that all SMs sweep the output together.  FUSED:
+// the CTA takes columns blockIdx.x, + gridDim.x, ... and runs each column's
+// OD depth tiles consecutively; tile id = column * OD + depth.
+template <bool FUSED = false>
 __device__ __forceinline__ int64_t tile_of(const IgemmParams &p, int64_t it) {
+  if (FUSED) {
+    const int64_t od = p.g.OD, c = it / od;
+    return (blockIdx.x + c * (int64_t)gridDim.x) * od + (it - c * od);
+  }
   return blockIdx.x + it * (int64_t)gridDim.x;
 }
+template <bool FUSED = false>
 __device__ __forceinline__ int64_t cta_tile_count(const IgemmParams &p) {
+  if (FUSED) return (p.columns - blockIdx.x + gridDim.x - 1) / gridDim.x * p.g.OD;
   return (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
 }
 
@@ -222,11 +236,22 @@ struct PosInfo {
   bool warp_full;       // every lane's receptive field is entirely inside the input
 };
 
+template <bool FUSED = false>
 __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t tile, int t) {
   const Geom &g = p.g;
   PosInfo ps;
-  const int64_t m = tile * kTileM + t;
-  ps.valid = m < p.M_total;
+  int64_t m;
+  if (FUSED) {
+    // tile = column * OD + depth; row t is position hw_tile * 128 + t of the (image, depth) plane
+    const int64_t col = tile / g.OD, ohw = (int64_t)g.OH * g.OW;
+    const int64_t d = tile - col * g.OD, img = col / p.hw_tiles;
+    const int64_t pp = (col - img * p.hw_tiles) * kTileM + t;
+    ps.valid = pp < ohw;
+    m = img * p.osp + d * ohw + (ps.valid ? pp : 0);
+  } else {
+    m = tile * kTileM + t;
+    ps.valid = m < p.M_total;
+  }
   int64_t n = 0;
   int od = 0, oh = 0, ow = 0;
   if (ps.valid) {
@@ -349,7 +374,11 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
 // ACC: a later reduction pass (adds into y; instantiated separately so that
 // the single-pass kernels keep their registers).  SB: streamed weights (see
 // IgemmParams::wsp): no resident weight matrix, any reduction length in one pass.
-template <int CH, bool ACC, bool SB>
+// FUSED: the conv3d -> min over depth -> channel softmax of the l2_p24 page
+// (turns 1-2): tiles of one (image, depth) plane, depth tiles of a column
+// consecutive, and an epilogue that keeps each position's running minimum
+// over depth in registers and writes only the softmax of the last one.
+template <int CH, bool ACC, bool SB, bool FUSED = false>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -447,7 +476,68 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   // producer groups.
   const uint32_t a_col0 = (uint32_t)(nslots * p.Npad);
 
-  if (warp < kEpiWarps) {
+  if (FUSED && warp < kEpiWarps) {
+    // ------------------------------------------------------------ fused epilogue
+    // Lane tid owns position hw_tile * 128 + tid of its column's plane; over
+    // the column's OD depth tiles it keeps min_d conv[n, o, d, pos] for each
+    // channel o < K <= 32, then adds the bias (min(z + b) = min(z) + b: x ->
+    // fl(x + b) is monotone), takes the softmax over o with the maximum
+    // subtracted, and writes y[n, o, pos]: a warp store covers 32
+    // consecutive positions of one channel.
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const int64_t my_tiles = cta_tile_count<true>(p);
+    const int OD = g.OD, K = g.K;
+    const int64_t ohw = (int64_t)g.OH * g.OW;
+    float mn[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) mn[j] = 0.f;
+    for (int64_t it = 0; it < my_tiles; ++it) {
+      const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
+      const bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const int64_t d = it % OD;
+      // the accumulator in two halves of 16 columns (fewer live registers)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        uint32_t v[16];
+        ptx::tmem_ld16(tmem + lane_base + b * p.Npad + 16 * h, v);
+        ptx::tmem_wait_ld();
+        if (d == 0) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mn[16 * h + j] = __uint_as_float(v[j]);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) mn[16 * h + j] = fminf(mn[16 * h + j], __uint_as_float(v[j]));
+        }
+      }
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_d_empty + 8 * b);
+      if (d == OD - 1) {
+        const int64_t col = tile_of<true>(p, it) / OD, img = col / p.hw_tiles;
+        const int64_t pp = (col - img * p.hw_tiles) * kTileM + tid;
+        if (pp < ohw) {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            mn[j] += bias_s[j];
+            if (j < K) mx = fmaxf(mx, mn[j]);
+          }
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            mn[j] = j < K ? expf(mn[j] - mx) : 0.f;
+            sum += mn[j];
+          }
+          const float inv = 1.f / sum;
+          float *yp = p.y + img * (int64_t)K * ohw + pp;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < K) __stcs(yp + (int64_t)j * ohw, mn[j] * inv);
+        }
+      }
+    }
+  } else if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int64_t my_tiles = cta_tile_count(p);
@@ -551,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const int slot = grp / gps, sel = grp - slot * gps;
     const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const int64_t my_tiles = cta_tile_count(p);
+    const int64_t my_tiles = cta_tile_count<FUSED>(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
     // Chunk q of a tile: gather its K columns into registers (loads only).
     auto gather_chunk = [&](const PosInfo &ps, int q, float (&v)[CH]) {
@@ -629,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const int nfull = (p.KC == CH && !p.vec4) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
-      const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
+      const PosInfo ps = decode_position<FUSED>(p, tile_of<FUSED>(p, li * nslots + slot), t);
       const int64_t lg0 = li * p.nchunks;  // slot-local index of the tile's first chunk
       // this group's chunks of the tile: lg = lg0 + q with lg = sel (mod gps)
       int q = (int)((sel - lg0 % gps + gps) % gps);
@@ -675,7 +765,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
     const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
     const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
-    const int64_t my_tiles = cta_tile_count(p);
+    const int64_t my_tiles = cta_tile_count<FUSED>(p);
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
       const int64_t li = it / nslots;
@@ -775,6 +865,7 @@ std::atomic<long long> g_wait_limit{kWaitLimitCycles};
 bool g_attr_bf16_set[64] = {false};
 bool g_attr_f16_set[64] = {false};
 bool g_attr_set[64] = {false};
+bool g_attr_fused_set[64] = {false};
 
 }  // namespace
 
@@ -933,6 +1024,76 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     }
   }
   return cudaSuccess;
+}
+
+bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {
+  Plan pl;
+  if (min_dim != 2) {
+    *why = "tensor-core fused path: the min runs over depth only";
+    return false;
+  }
+  if (g.K > 32) {
+    *why = "tensor-core fused path: C_out above 32";
+    return false;
+  }
+  if (g.cl) {
+    *why = "tensor-core fused path: channels-last input";
+    return false;
+  }
+  if (!make_plan(g, &pl, why)) return false;
+  if (pl.npasses != 1 || pl.KC != 16) {
+    *why = "tensor-core fused path: the weights must fit in one pass";
+    return false;
+  }
+  return true;
+}
+
+cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
+                                           cudaStream_t stream) {
+  Plan pl;
+  const char *why = "";
+  if (!igemm_fused_supported(g, 2, &why) || !make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (g_num_sms[dev] == 0) {
+    e = cudaDeviceGetAttribute(&g_num_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+  }
+  if (!g_attr_fused_set[dev]) {
+    e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kMaxSmem);
+    if (e != cudaSuccess) return e;
+    g_attr_fused_set[dev] = true;
+  }
+  IgemmParams p = {};
+  p.wait_limit = g_wait_limit.load();
+  p.x = x;
+  p.w = w;
+  p.bias = bias;
+  p.y = y;
+  p.g = g;
+  p.osp = (int64_t)g.OD * g.OH * g.OW;
+  p.M_total = g.N * p.osp;
+  p.hw_tiles = (int)(((int64_t)g.OH * g.OW + kTileM - 1) / kTileM);
+  p.columns = g.N * p.hw_tiles;
+  p.tiles = p.columns * g.OD;
+  p.Kred = pl.Kred;
+  p.Kfull = pl.Kred;
+  p.k_begin = 0;
+  p.accumulate = 0;
+  p.y_chans = g.K;
+  p.Kpad = pl.Kpad;
+  p.Npad = pl.Npad;
+  p.KC = pl.KC;
+  p.nchunks = pl.nchunks;
+  p.nslots = pl.nslots;
+  p.tap_major = pl.tap_major;
+  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
+  const int64_t grid = p.columns < g_num_sms[dev] ? p.columns : g_num_sms[dev];
+  igemm_3xtf32_kernel<16, false, false, true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 bool igemm_bf16_supported(const Geom &g, const char **why) {

@@ -291,11 +291,24 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  *   bias: [C_out] device or NULL, y->dims = [N, C_out] followed by the conv's
  *   spatial output dims (D-KD+1, H-KH+1, W-KW+1) without the reduced one:
  *   [N, C_out, OH, OW] for min_dim 2, [N, C_out, OD, OW] for 3, [N, C_out, OD, OH] for 4.
- * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  C_out is limited to 96 and the
- * kernel extent along y's last axis to 7 (CONV_ERR_UNSUPPORTED otherwise).
+ * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  Two kernel families: the FFMA
+ * kernels (C_out up to 96, a kernel extent along y's last axis up to 7) and a
+ * tensor-core kernel (3xTF32 implicit GEMM whose epilogue keeps each
+ * position's running minimum over depth in registers; min_dim 2, C_out <= 32,
+ * weights that fit in shared memory).  Where both run, the planner takes the
+ * FFMA kernels for short reductions over few channels (C_out <= 24 with
+ * C_in * |kernel| <= 256, or C_in * |kernel| <= 32) and the tensor-core kernel
+ * otherwise.  Shapes neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);
+
+/* conv3d_min_softmax with an explicit kernel family: CONV_ALGO_AUTO (the
+ * planner), CONV_ALGO_DIRECT_FFMA (the FFMA kernels) or CONV_ALGO_IGEMM_3XTF32
+ * (the tensor-core kernel); a family that cannot run the shape returns
+ * CONV_ERR_UNSUPPORTED, an unknown value CONV_ERR_ARG. */
+CONVFWD_API int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias,
+                                      conv_tensor4_t *y, int min_dim, int algo, conv_stream_t stream);
 
 /*
  * Peak-rate microbenchmarks (diagnostics; not part of the convolution).  The

@@ -234,26 +234,72 @@ def test_indexing_beyond_int32():
 
 # ------------------------------------------------------------------ fused
 
-def run_fused(x, w, b):
+FFMA, TC = cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_IGEMM_3XTF32
+
+
+def run_fused(x, w, b, algo=cf.CONV_ALGO_AUTO):
     xt = torch.from_numpy(x).cuda()
     wt = torch.from_numpy(w).cuda()
     bt = None if b is None else torch.from_numpy(b).cuda()
-    y = cf.conv3d_min_softmax(xt, wt, bt, 2)
+    y = cf.conv3d_min_softmax(xt, wt, bt, 2, algo=algo)
     torch.cuda.synchronize()
     return y
 
 
-@pytest.mark.parametrize("C_out", [1, 5, 12, 13, 24, 25, 48, 49, 96])
+@pytest.mark.parametrize("algo", [FFMA, TC])
+@pytest.mark.parametrize("C_out", [1, 5, 12, 13, 24, 25, 32, 48, 49, 96])
 @pytest.mark.parametrize("k", [(3, 3, 3), (2, 3, 5)])
-def test_fused_small(C_out, k):
+def test_fused_small(C_out, k, algo):
+    if algo == TC and C_out > 32:
+        pytest.skip("the tensor-core fused kernel takes C_out <= 32")
     rng = np.random.default_rng(C_out * 10 + k[2])
     x = rng.random((3, 3, 7, 11, 37)).astype(np.float32)  # W=37: scalar path, 2 column tiles
     w = (rng.random((C_out, 3) + k).astype(np.float32) - 0.5) * 0.4
     b = (rng.random(C_out).astype(np.float32) - 0.5) * 0.4
     ref = oracle.conv3d_min_softmax(x, w, b)
-    y = run_fused(x, w, b).cpu().numpy()
-    assert_close(y, ref, f"fused C_out={C_out} k={k}")
+    y = run_fused(x, w, b, algo).cpu().numpy()
+    assert_close(y, ref, f"fused C_out={C_out} k={k} algo={algo}")
     assert np.abs(y.sum(axis=1) - 1).max() < 1e-5
+
+
+@pytest.mark.parametrize("shape,C_in,C_out,k", [
+    ((2, 3, 3, 17, 13), 3, 24, (3, 3, 3)),    # one output depth: the min over a single plane
+    ((1, 2, 9, 40, 45), 2, 20, (4, 5, 2)),     # 1 image, planes of 36 x 44 = 1584 positions (12.4 tiles)
+    ((5, 4, 6, 12, 12), 4, 32, (2, 2, 2)),     # C_out = 32 (every accumulator column), 121-position planes
+    ((3, 1, 30, 5, 7), 1, 7, (1, 1, 1)),       # 1x1x1 kernel, 30 depth tiles per column
+])
+def test_fused_tensor_core_geometries(shape, C_in, C_out, k):
+    rng = np.random.default_rng(sum(shape) + C_out)
+    x = rng.standard_normal(shape).astype(np.float32)
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 0.5).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv3d_min_softmax(x, w, b)
+    assert_close(run_fused(x, w, b, TC).cpu().numpy(), ref, f"fused tensor cores {shape} k={k}")
+    assert_close(run_fused(x, w, None, TC).cpu().numpy(), oracle.conv3d_min_softmax(x, w, None),
+                 f"fused tensor cores no bias {shape}")
+
+
+def test_fused_planner_takes_the_measured_family():
+    """AUTO must equal one family bit for bit: FFMA on the page's C_in = 3, C_out = 24 shape
+    (reduced batch), the tensor cores for C_out = 32 over C_in = 8 (the two differ in rounding)."""
+    wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
+    auto, ffma, tc = (run_fused(x, w, b, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
+    assert (auto == ffma).all() and not (auto == tc).all()
+    rng = np.random.default_rng(11)
+    x = rng.random((2, 8, 10, 20, 20)).astype(np.float32)
+    w = ((rng.random((32, 8, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
+    auto, ffma, tc = (run_fused(x, w, None, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
+    assert (auto == tc).all() and not (auto == ffma).all()
+
+
+def test_fused_tensor_core_refuses_what_it_cannot_run():
+    x = torch.zeros((1, 3, 5, 9, 9), device="cuda")
+    with pytest.raises(cf.ConvError) as e:
+        cf.conv3d_min_softmax(x, torch.zeros((33, 3, 3, 3, 3), device="cuda"), None, 2, algo=TC)
+    assert e.value.status == cf.CONV_ERR_UNSUPPORTED
+    with pytest.raises(cf.ConvError) as e:
+        cf.conv3d_min_softmax(x, torch.zeros((8, 3, 3, 3, 3), device="cuda"), None, 3, algo=TC)
+    assert e.value.status == cf.CONV_ERR_UNSUPPORTED
 
 
 def test_fused_vector_path_and_ragged_rows():
@@ -266,15 +312,17 @@ def test_fused_vector_path_and_ragged_rows():
     assert_close(run_fused(x, w, None).cpu().numpy(), oracle.conv3d_min_softmax(x, w, None), "fused no bias")
 
 
-def test_fused_workload_reduced_batch_full_compare():
+@pytest.mark.parametrize("algo", [FFMA, TC])
+def test_fused_workload_reduced_batch_full_compare(algo):
     wl, x, w, b = workload_inputs("conv3d_min_softmax", 4)
     ref = oracle.conv3d_min_softmax(x, w, b)
-    assert_close(run_fused(x, w, b).cpu().numpy(), ref, "fused workload N=4")
+    assert_close(run_fused(x, w, b, algo).cpu().numpy(), ref, f"fused workload N=4 algo={algo}")
 
 
-def test_fused_workload_full_size_sampled():
+@pytest.mark.parametrize("algo", [cf.CONV_ALGO_AUTO, FFMA])
+def test_fused_workload_full_size_sampled(algo):
     wl, x, w, b = workload_inputs("conv3d_min_softmax")
-    y = run_fused(x, w, b)
+    y = run_fused(x, w, b, algo)
     N, C_out, OH, OW = y.shape
     rng = np.random.default_rng(9)
     cols = np.unique(np.concatenate([rng.integers(0, N * OH * OW, 1500), [0, OW - 1, OH * OW - 1, N * OH * OW - 1]]))
