@@ -30,7 +30,15 @@ struct Geom {
 };
 
 // Device-side status word written by kernels whose bounded waits gave up.
-enum : unsigned { kStatusIgemmWatchdog = 1u };
+enum : unsigned {
+  kStatusIgemmWatchdog = 1u,
+  // beside bit 0, the wait that gave up first in a CTA
+  kWaitSiteAEmpty = 1u << 8,   // producers: an A stage to drain
+  kWaitSiteAFull = 1u << 9,    // MMA issuer: an A stage to fill
+  kWaitSiteBFull = 1u << 10,   // MMA issuer: streamed weights to land
+  kWaitSiteDFull = 1u << 11,   // epilogue: an accumulator to complete
+  kWaitSiteDEmpty = 1u << 12,  // MMA issuer: an accumulator to drain
+};
 
 // Launchers (return cudaSuccess or the launch error).  All validation happens
 // before these are called.

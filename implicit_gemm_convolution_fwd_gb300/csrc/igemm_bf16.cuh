@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     for (int64_t it = 0; it < my_tiles; ++it) {
       const int64_t tile = tile_of(p, it);
       const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
-      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit);
+      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit, kWaitSiteDFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const int64_t m = tile * kTileM + tid;
@@ -262,7 +262,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         const int64_t lg = lg0 + q;
         const int stage = 2 * slot + (int)(lg & 1);
         const uint32_t r = (uint32_t)(lg >> 1);
-        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit);
+        const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit, kWaitSiteAEmpty);
         if (!__all_sync(0xffffffffu, ok)) return false;
         ptx::tc_fence_after();
         ptx::tmem_st16(tmem + lane_base + a_col0 + (uint32_t)(16 * stage), packed);
@@ -318,12 +318,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
       const int64_t li = it / nslots;
-      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag, p.wait_limit))) break;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag, p.wait_limit,
+                                                  kWaitSiteDEmpty))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t lg = li * p.nchunks + q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
-        if (!__all_sync(0xffffffffu, wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit))) {
+        if (!__all_sync(0xffffffffu, wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteAFull))) {
           aborted = true;
           break;
         }

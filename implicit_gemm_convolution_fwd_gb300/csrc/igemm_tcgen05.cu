@@ -201,7 +201,7 @@ __device__ __forceinline__ int64_t cta_tile_count(const IgemmParams &p) {
 // can block for a few thousand cycles), is out of line so that the roles'
 // loops stay short.
 __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                             long long limit) {
+                                             long long limit, uint32_t site) {
   const long long t0 = clock64();
   const uint32_t check_mask = limit < kWaitLimitCycles ? 0u : 15u;
   for (uint32_t i = 1;; ++i) {
@@ -210,16 +210,16 @@ __device__ __noinline__ bool wait_phase_slow(uint32_t bar, uint32_t parity, vola
       if (*abort_flag) return false;
       if (clock64() - t0 > limit) {
         *abort_flag = 1;
-        atomicOr(&g_device_status, kStatusIgemmWatchdog);
+        atomicOr(&g_device_status, kStatusIgemmWatchdog | site);
         return false;
       }
     }
   }
 }
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volatile int *abort_flag,
-                                           long long limit) {
+                                           long long limit, uint32_t site) {
   if (ptx::mbar_try_wait(bar, parity)) return true;
-  return wait_phase_slow(bar, parity, abort_flag, limit);
+  return wait_phase_slow(bar, parity, abort_flag, limit, site);
 }
 
 __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_uint(v) & 0xffffe000u; }
@@ -493,7 +493,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     for (int j = 0; j < 32; ++j) mn[j] = 0.f;
     for (int64_t it = 0; it < my_tiles; ++it) {
       const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
-      const bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit);
+      const bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit, kWaitSiteDFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const int64_t d = it % OD;
@@ -544,7 +544,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     for (int64_t it = 0; it < my_tiles; ++it) {
       const int64_t tile = tile_of(p, it);
       const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
-      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit);
+      bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit, kWaitSiteDFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const int64_t m = tile * kTileM + tid;
@@ -669,7 +669,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
       const int ncols = min(p.KC, p.Kpad - q * p.KC);
       const uint32_t r = (uint32_t)(lg >> 1);
-      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit);
+      const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit, kWaitSiteAEmpty);
       if (!__all_sync(0xffffffffu, ok)) return false;
       ptx::tc_fence_after();
       if (SB && t == 0) {
@@ -769,13 +769,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     bool aborted = false;
     for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
       const int64_t li = it / nslots;
-      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag, p.wait_limit))) break;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag, p.wait_limit,
+                                                  kWaitSiteDEmpty))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
         const int64_t lg = li * p.nchunks + q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
-        bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit);
-        if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag, p.wait_limit);
+        bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteAFull);
+        if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteBFull);
         if (!__all_sync(0xffffffffu, ok)) {
           aborted = true;
           break;
@@ -941,7 +942,6 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     IgemmParams p = {};
-  p.wait_limit = g_wait_limit.load();
     p.wait_limit = g_wait_limit.load();
     p.x = x;
     p.w = w;
@@ -987,9 +987,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       const int k_begin = pass * pl.kpass;
       const int kred = (int)(kfull - k_begin < pl.kpass ? kfull - k_begin : pl.kpass);
       IgemmParams p = {};
-  p.wait_limit = g_wait_limit.load();
       p.wait_limit = g_wait_limit.load();
-    p.wait_limit = g_wait_limit.load();
       p.x = x;
       p.w = w + o0 * kfull;
       p.bias = bias ? bias + o0 : nullptr;

@@ -369,7 +369,11 @@ CONVFWD_API int conv_debug_set_wait_limit(long long cycles);
 
 /* Synchronises the current device, then returns and clears the device-side
  * status word: 0 when no kernel gave up on a bounded wait since the last call,
- * else a bit set per kernel family that did (bit 0: tensor-core path).  Writes
+ * else bit 0 (a tensor-core kernel gave up) plus, per CTA that gave up, the
+ * wait that ran out first: bit 8 producers waiting for an A stage to drain,
+ * bit 9 the MMA issuer waiting for an A stage to fill, bit 10 the issuer
+ * waiting for streamed weights, bit 11 the epilogue waiting for an
+ * accumulator, bit 12 the issuer waiting for an accumulator to drain.  Writes
  * the word to *flags and returns CONV_OK, or CONV_ERR_CUDA. */
 CONVFWD_API int conv_device_status(unsigned int *flags);
 

@@ -348,6 +348,57 @@ def test_tensor_core_wide_kernels(kw, dw, pw):
     assert_close(y, ref, f"wide kernel kw={kw} dw={dw} pw={pw}")
 
 
+# Wide kernels along W at unit stride over several parities of the row, plane
+# and batch strides, and the same tensors 4 bytes into a buffer: the gather
+# may assume nothing about the alignment of a receptive field's first tap.
+TAP_ROW_CASES = [
+    # C_in, C_out, k, s, p, d, in dims, N
+    (3, 64, (3, 5, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1), (6, 12, 64), 2),   # the headline's kernel, even rows
+    (3, 20, (2, 3, 6), (1, 1, 1), (0, 0, 0), (1, 1, 1), (5, 10, 40), 2),   # OW = 35: positions of both parities per warp
+    (3, 33, (3, 3, 5), (1, 1, 1), (1, 1, 2), (1, 1, 1), (6, 10, 32), 2),   # padding: border and interior warps
+    (2, 16, (1, 3, 8), (1, 2, 1), (0, 0, 0), (1, 1, 1), (1, 20, 70), 3),   # KW = 8, stride along H
+    (6, 24, (1, 1, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1), (1, 1, 1000), 3),  # a Conv1d
+    (2, 40, (2, 2, 5), (1, 1, 1), (0, 0, 0), (2, 2, 1), (7, 9, 30), 2),    # KW = 5, dilation along D and H
+    (1, 8, (1, 1, 6), (1, 1, 1), (0, 0, 0), (1, 1, 1), (3, 4, 50), 2),     # KW = 6, one channel
+    (1, 12, (1, 1, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1), (3, 5, 31), 3),    # odd batch stride
+    (4, 28, (1, 1, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1), (2, 3, 33), 2),    # odd row stride
+]
+
+
+@pytest.mark.parametrize("C_in,C_out,k,s,p,d,ins,N", TAP_ROW_CASES)
+def test_tensor_core_kw_geometries(C_in, C_out, k, s, p, d, ins, N):
+    rng = np.random.default_rng(C_in * 1000 + C_out * 10 + k[2])
+    x = rng.standard_normal((N, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 2 / np.sqrt(C_in * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    assert supported(x, w, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32)
+    ref = oracle.conv_nd(x, w, b, s, p, d)
+    y = run_conv(x, w, b, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32).cpu().numpy()
+    assert_close(y, ref, f"kw geometry C_in={C_in} k={k} ins={ins}")
+    # the same tensor one float into a buffer (4-byte aligned only)
+    buf = torch.empty(x.size + 1, device="cuda")
+    xm = buf[1:].view(x.shape)
+    xm.copy_(torch.from_numpy(x))
+    ym = cf.conv_fwd_nd(xm, torch.from_numpy(w).cuda(), torch.from_numpy(b).cuda(), s, p, d,
+                        algo=cf.CONV_ALGO_IGEMM_3XTF32)
+    assert_close(ym.cpu().numpy(), ref, f"kw geometry, x 4-byte aligned, C_in={C_in} k={k}")
+
+
+def test_tensor_core_non_finite_input_stays_in_its_receptive_fields():
+    """Infinite inputs reach only the outputs whose receptive fields hold them: no padding
+    column of the reduction reads x (0 * inf would make NaN of a finite output)."""
+    rng = np.random.default_rng(5)
+    x = rng.standard_normal((1, 3, 4, 8, 20)).astype(np.float32)
+    x[..., 7:9] = np.inf  # W positions 7 and 8: outside the fields of output columns 0 and 9..13
+    w = ((rng.random((16, 3, 2, 3, 7)) - 0.5) * 0.3).astype(np.float32)
+    s, p, d = (1, 1, 1), (0, 0, 0), (1, 1, 1)
+    ref = oracle.conv_nd(x, w, None, s, p, d)
+    y = run_conv(x, w, None, s, p, d, cf.CONV_ALGO_IGEMM_3XTF32).cpu().numpy().astype(np.float64)
+    finite = np.isfinite(ref)
+    assert (np.isfinite(y) == finite).all()
+    assert_close(np.where(finite, y, 0.0), np.where(finite, ref, 0.0), "finite outputs beside inf inputs")
+
+
 def test_fused_staged_multi_image_blocks():
     # output width <= 32, C_out <= 24, KW = 3: the staged kernel; OH = 6 makes a
     # block of output rows span several images; W = 30 is not a multiple of 4

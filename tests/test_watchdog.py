@@ -46,7 +46,10 @@ def test_short_wait_limit_aborts_cleanly_and_the_next_call_is_correct():
         torch.cuda.synchronize()  # the kernel returned
     finally:
         cf.set_wait_limit(0)
-    assert cf.device_status() & 1, "a wait of a few hundred cycles should have given up"
+    st = cf.device_status()
+    assert st & 1, "a wait of a few hundred cycles should have given up"
+    assert st & 0x1f00, f"the status word names no wait site: {st:#x}"
+    assert st & ~0x1f01 == 0, f"unknown status bits: {st:#x}"
     # the status word was read and cleared; the device and the library still work
     assert cf.device_status() == 0
     ref = oracle.conv_nd(x, w, b, s, p, d)
