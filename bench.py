@@ -161,19 +161,23 @@ class ClockSampler:
 # --------------------------------------------------------------- our arm
 
 class OurRunner:
-    def __init__(self, wl, device):
+    def __init__(self, wl, device, fused_algo="auto"):
         import torch
         import implicit_gemm_convolution_fwd_gb300 as cf
         self.torch, self.cf, self.wl, self.dev = torch, cf, wl, device
+        # the fused op's kernel family: the planner (which takes the FFMA kernel on the
+        # benchmark's fused workload, as a parity test checks), or one family forced
+        self.fused_code = {"auto": cf.CONV_ALGO_AUTO, "ffma": cf.CONV_ALGO_DIRECT_FFMA,
+                           "tc": cf.CONV_ALGO_IGEMM_3XTF32}[fused_algo]
         x, w, b = wl.make_inputs(seed=0)
         self.host = {"x": x, "w": w, "b": b}
         self.x = torch.from_numpy(x).to(device)
         self.w = torch.from_numpy(w).to(device)
         self.b = None if b is None else torch.from_numpy(b).to(device)
         if wl.kind == "fused":
-            self.out_dims = (x.shape[2] - w.shape[2] + 1, x.shape[3] - w.shape[3] + 1, x.shape[4] - w.shape[4] + 1)
+            self.out_dims = cf.out_dims(wl.in_dims, wl.k_dims, 1, 0, 1)
             self.y = torch.empty((wl.N, wl.C_out, self.out_dims[1], self.out_dims[2]), device=device)
-            self.algo = "fused_ffma"
+            self.algo = "fused_igemm_3xtf32" if fused_algo == "tc" else "fused_ffma"
         else:
             self.out_dims = cf.out_dims(wl.in_dims, wl.k_dims, wl.stride, wl.pad, wl.dilation)
             self.y = torch.empty((wl.N, wl.C_out) + tuple(self.out_dims), device=device)
@@ -188,7 +192,8 @@ class OurRunner:
 
     def step(self):
         if self.wl.kind == "fused":
-            self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.wl.min_dim, out=self.y, stream=self.stream)
+            self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.wl.min_dim, out=self.y, stream=self.stream,
+                                       algo=self.fused_code)
         else:
             self.cf.conv_fwd_nd(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation, out=self.y,
                                 stream=self.stream)
@@ -282,10 +287,9 @@ class VariantRunner(OurRunner):
     16-bit tensors, the min over another dim, channels-last tensors or groups."""
 
     def __init__(self, wl, device, dtype=None, min_dim=None, channels_last=False, groups=1, workspace=False,
-                 fused_algo=None):
-        super().__init__(wl, device)
+                 fused_algo="auto"):
+        super().__init__(wl, device, fused_algo)
         torch = self.torch
-        self.fused_algo = self.cf.CONV_ALGO_AUTO if fused_algo is None else getattr(self.cf, fused_algo)
         self.dtype, self.channels_last, self.groups = dtype, channels_last, groups
         self.ws = None
         self.ws_stream = 0  # workspace bytes for streamed weights
@@ -316,7 +320,7 @@ class VariantRunner(OurRunner):
     def step(self):
         if self.wl.kind == "fused":
             self.cf.conv3d_min_softmax(self.x, self.w, self.b, self.min_dim, out=self.y, stream=self.stream,
-                                       algo=self.fused_algo)
+                                       algo=self.fused_code)
         elif self.ws is not None:
             self.cf.conv_fwd_nd_ws(self.x, self.w, self.b, self.wl.stride, self.wl.pad, self.wl.dilation,
                                    workspace=self.ws, out=self.y, stream=self.stream)
@@ -332,7 +336,7 @@ VARIANTS = [
     ("conv1d_long[bf16]", "conv1d_long", {"dtype": "bfloat16"}),
     ("conv3d_min_softmax[min_dim=3]", "conv3d_min_softmax", {"min_dim": 3}),
     ("conv3d_min_softmax[min_dim=4]", "conv3d_min_softmax", {"min_dim": 4}),
-    ("conv3d_min_softmax[tensor cores]", "conv3d_min_softmax", {"fused_algo": "CONV_ALGO_IGEMM_3XTF32"}),
+    ("conv3d_min_softmax[tensor cores]", "conv3d_min_softmax", {"fused_algo": "tc"}),
     ("conv3d_sweep_b[channels_last]", "conv3d_sweep_b", {"channels_last": True}),
     ("conv3d_sweep_b[groups=2]", "conv3d_sweep_b", {"groups": 2}),
     ("conv3d_wide_k[workspace]", "conv3d_wide_k", {"workspace": True}),
@@ -360,7 +364,7 @@ def run_variants(dev, peaks, pipes, steps):
             entry["frac_of_bf16_peak"] = entry["tflops"] / pipes["bf16"]["tflops"]
             entry["frac_of_cublas_bf16"] = entry["tflops"] / peaks["bf16_tflops"]
         if r.dtype is None and r.wl.kind == "fused":
-            if r.fused_algo == r.cf.CONV_ALGO_IGEMM_3XTF32:
+            if r.fused_code == r.cf.CONV_ALGO_IGEMM_3XTF32:
                 entry["frac_of_3xtf32_peak"] = entry["tflops"] / pipes["tf32x3"]["tflops"]
             else:
                 entry["frac_of_ffma_peak"] = entry["tflops"] / pipes["ffma"]["tflops"]
@@ -376,6 +380,7 @@ def run_variants(dev, peaks, pipes, steps):
 # null.  "batch" is the batch of the captured case: traffic is scaled by
 # N / batch when the capture used a smaller batch (traffic grows in proportion).
 KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "igemm_tcgen05.cu",
+                 "fused_igemm_3xtf32": "igemm_tcgen05.cu",
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
@@ -420,7 +425,7 @@ def roofline_for(runner, peaks, pipes, ms):
     flops, bytes_alg, _, _ = problem_counts(wl, runner.out_dims, runner.y.element_size())
     t = ms * 1e-3
     hbm_peak = peaks["hbm_gbs"]
-    if runner.algo in ("igemm_3xtf32", "igemm_3xtf32_streamed"):
+    if runner.algo in ("igemm_3xtf32", "igemm_3xtf32_streamed", "fused_igemm_3xtf32"):
         compute = {"bound": "tensor", "peak": pipes["tf32x3"]["tflops"],
                    "peak_note": "measured TF32 tcgen05.mma rate / 3 products (3xTF32)",
                    "derived_peak": peaks["bf16_tflops"] * BF16_TO_TF32 / 3.0}
@@ -533,6 +538,8 @@ def main():
                     help="override the workload's batch size (small cases for profiler captures)")
     ap.add_argument("--dtype", choices=["f32", "bf16", "fp16"], default="f32",
                     help="run the workload on 16-bit tensors (the 16-bit tensor-core entry points)")
+    ap.add_argument("--fused-algo", choices=["auto", "ffma", "tc"], default="auto",
+                    help="kernel family of a fused workload (auto: the library's planner)")
     ap.add_argument("--workspace", action="store_true",
                     help="run the workload through conv_fwd_nd_ws (streamed weights when they exceed shared memory)")
     args = ap.parse_args()
@@ -566,7 +573,7 @@ def main():
         elif runner.ws is not None and runner.ws_stream > 0:
             runner.algo = "igemm_3xtf32_streamed"
     else:
-        runner = OurRunner(wl, dev)
+        runner = OurRunner(wl, dev, args.fused_algo)
     flops, bytes_alg, in_b, out_b = problem_counts(wl, runner.out_dims, runner.y.element_size())
     # warm-up, then EXACTLY K timed steps bracketed by barrier + synchronize
     runner.timed(0, args.warmup)

@@ -329,13 +329,19 @@ def _fp32_device_problem(x, w, bias, out, stride, pad, dilation, groups):
     return dev, nd, hp, N, C_in, C_out, od
 
 
-def conv_fwd_nd_ws(x, w, bias=None, stride=1, pad=0, dilation=1, workspace=None, out=None, stream=None, groups=1):
+def conv_fwd_nd_ws(x, w, bias=None, stride=1, pad=0, dilation=1, workspace=None, out=None, stream=None, groups=1,
+                   no_workspace=False):
     """conv_fwd_nd (fp32, contiguous) with a caller workspace for streamed weights: `workspace` is a CUDA
-    tensor of at least workspace_bytes(...) bytes (allocated here when None and the problem needs one)."""
+    tensor of at least workspace_bytes(...) bytes (allocated here when None and the problem needs one).
+    no_workspace=True passes none (NULL): a layer whose weights exceed shared memory then runs in
+    several passes, and nothing is allocated."""
     import torch
     dev, nd, (s, p, d), N, C_in, C_out, od = _fp32_device_problem(x, w, bias, out, stride, pad, dilation, groups)
     need = workspace_bytes(N, C_in, C_out, x.shape[2:], w.shape[2:], s, p, d, groups)
-    if workspace is None and need:
+    if no_workspace:
+        if workspace is not None:
+            raise ValueError("no_workspace=True takes no workspace")
+    elif workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=dev)
         if stream is not None:
             workspace.record_stream(stream)  # not reused before the call's work on `stream` is done

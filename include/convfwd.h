@@ -15,12 +15,22 @@
  *     parameter arrays (in_dims, k_dims, stride, pad, dilation, out_dims) and
  *     the descriptor structs are HOST memory, read during the call only.
  *   - The caller owns every buffer and the library keeps no pointer to one after
- *     the call returns.  y must not overlap x, w or bias.  No call allocates
- *     device memory.  Two things are held by the library itself: a 16 MiB
+ *     the call returns.  y must not overlap x, w or bias.  One kind of call
+ *     allocates device memory: conv_fwd_nd, conv_fwd_nd_ex, conv_fwd_nd_grouped
+ *     and conv_fwd_nd_host, on a tensor-core layer whose weights exceed shared
+ *     memory (conv_workspace_bytes > 0), take a stream-ordered block of that
+ *     size for the split weights (allocated on `stream` from a memory pool of
+ *     the library's, or from the device's default pool while `stream` is being
+ *     captured into a graph, and freed on `stream` after the call's last
+ *     launch; if the allocation fails, the layer runs in several passes
+ *     instead).  conv_fwd_nd_ws, conv_fwd_nd_ws_noalloc and every other call
+ *     allocate nothing.  Things held by the library itself: a 16 MiB
  *     file-scope device array (the scratch of conv_fwd_nd_ws_noalloc), which
- *     every device that loads the library holds until the process exits; and,
- *     from the first conv_fwd_nd_host call on a device, two copy streams and
- *     six events on that device, kept until exit.
+ *     every device that loads the library holds until the process exits; from
+ *     the first allocating call on a device, that memory pool, which keeps up
+ *     to 64 MiB reserved between calls; and, from the first conv_fwd_nd_host
+ *     call on a device, two copy streams and six events on that device, kept
+ *     until exit.
  *   - All device work is enqueued on `stream` (NULL = legacy default stream);
  *     calls return without synchronising.  Errors from kernels that already
  *     ran surface at the caller's next synchronisation (cudaStreamSynchronize).
@@ -182,12 +192,13 @@ CONVFWD_API int conv_fwd_nd_f16(const uint16_t *x, const uint16_t *w, const uint
 
 /*
  * Workspace for streamed weights.  The tensor-core family keeps one group's
- * weights (split into TF32 hi and lo) in shared memory; when they do not fit
- * it runs the reduction in several passes (each re-reading x and adding into
- * y) or leaves the layer to the direct family.  With a caller workspace the
- * weights are split once into it, in the order the tensor cores read them, and
- * brought into shared memory chunk by chunk with bulk copies, so the whole
- * reduction runs in one pass.
+ * weights (split into TF32 hi and lo) in shared memory; when they do not fit,
+ * the weights are split once into a workspace, in the order the tensor cores
+ * read them, and brought into shared memory chunk by chunk with bulk copies,
+ * so the whole reduction runs in one pass.  The workspace is the caller's
+ * (conv_fwd_nd_ws) or a stream-ordered allocation of the call (conv_fwd_nd and
+ * the other allocating calls); without one the reduction runs in several
+ * passes, each re-reading x and adding into y.
  * conv_workspace_bytes writes the bytes conv_fwd_nd_ws can use for the problem
  * (0 when its weights fit in shared memory, or a group has more than 128
  * output channels, or the column tables of the reduction exceed shared memory).
@@ -199,9 +210,11 @@ CONVFWD_API int conv_workspace_bytes(int ndim, int64_t N, int64_t C_in, int64_t 
 /* conv_fwd_nd_grouped (AUTO) with a device workspace of at least
  * conv_workspace_bytes bytes, 256-byte aligned, not overlapping x, w, bias or
  * y; the library writes it before reading it on `stream`, so calls that share
- * a workspace must be ordered (the same stream does that).  With workspace NULL
- * or a problem that needs none, it is conv_fwd_nd_grouped; a workspace smaller
- * than needed is CONV_ERR_ARG. */
+ * a workspace must be ordered (the same stream does that).  With a problem that
+ * needs none it is conv_fwd_nd_grouped; with workspace NULL it is
+ * conv_fwd_nd_grouped without its allocation (a layer whose weights exceed
+ * shared memory then runs in several passes); a workspace smaller than needed
+ * is CONV_ERR_ARG. */
 CONVFWD_API int conv_fwd_nd_ws(const float *x, const float *w, const float *bias, float *y, int ndim, int64_t N,
                                int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,
                                const int64_t *k_dims, const int64_t *stride, const int64_t *pad,
@@ -265,7 +278,9 @@ CONVFWD_API int conv_fwd_nd_host(const float *x, const float *w, const float *bi
 
 /* The kernel family conv_fwd_nd would use for this problem (host only, no
  * device access).  Writes *algo_out and returns CONV_OK, or an error status
- * for an invalid problem. */
+ * for an invalid problem.  (A call that cannot stream weights, conv_fwd_nd_ws
+ * without a workspace, may take the direct family instead for a layer whose
+ * weights exceed shared memory.) */
 CONVFWD_API int conv_select_algo(int ndim, int64_t N, int64_t C_in, int64_t C_out, const int64_t *in_dims,
                      const int64_t *k_dims, const int64_t *stride, const int64_t *pad, const int64_t *dilation,
                      int *algo_out);

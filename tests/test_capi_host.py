@@ -158,6 +158,10 @@ def test_select_algo_host_only(lib):
     assert cf.select_algo(2, 4, 8, (1024,), (3,), 3, 0, 4) == cf.CONV_ALGO_DIRECT_FFMA
     a = cf.select_algo(64, 64, 128, (524280,), (3,), 3, 0, 4)
     assert a in (cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_IGEMM_3XTF32)
+    # weights beyond shared memory (64 -> 128 channels, 3x3x3): conv_fwd_nd streams them in one
+    # tensor-core pass, so the planner takes the tensor cores, not the direct path
+    assert cf.workspace_bytes(4, 64, 128, (32, 32, 32), (3, 3, 3), 1, 1, 1) > 0
+    assert cf.select_algo(4, 64, 128, (32, 32, 32), (3, 3, 3), 1, 1, 1) == cf.CONV_ALGO_IGEMM_3XTF32
 
 
 def test_algo_supported_queries(lib):

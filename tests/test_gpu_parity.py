@@ -744,6 +744,66 @@ def test_streamed_weights_workspace(C_in, C_out, k, pad, groups):
     with pytest.raises(cf.ConvError) as e:
         cf.conv_fwd_nd_ws(xt, wt, bt, s, pad, d, workspace=ws[:need // 2], groups=groups)
     assert e.value.status == cf.CONV_ERR_ARG
+    # the plain call streams them too, from a stream-ordered block of its own (on a side stream
+    # here, so the block's lifetime follows that stream); no workspace: passes of shared memory
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        yp = cf.conv_fwd_nd(xt, wt, bt, s, pad, d, groups=groups, stream=side)
+    yn = cf.conv_fwd_nd_ws(xt, wt, bt, s, pad, d, groups=groups, no_workspace=True)
+    torch.cuda.synchronize()
+    assert_close(yp.cpu().numpy(), ref, f"plain call, streamed weights C_in={C_in} k={k} G={groups}")
+    assert_close(yn.cpu().numpy(), ref, f"no workspace, passes C_in={C_in} k={k} G={groups}")
+    if cf.select_algo(2, C_in, C_out, x.shape[2:], k, s, pad, d) == cf.CONV_ALGO_IGEMM_3XTF32 and groups == 1:
+        assert torch.equal(yp, y), "the plain call's streamed weights must match the caller-workspace call"
+
+
+def test_cuda_graph_capture_and_replay():
+    """Each family launched inside a CUDA graph capture (the design replaces a tracing compiler with
+    graphs): a plain tensor-core layer, one with streamed weights (its block then comes from the
+    device's default pool, as graphs need) and an FFMA layer; replays match the eager results."""
+    rng = np.random.default_rng(21)
+    cases = [((2, 3, 6, 12, 40), (32, 3, 3, 5, 7), 0),   # tensor cores, weights resident
+             ((1, 64, 4, 6, 6), (128, 64, 3, 3, 3), 1),  # tensor cores, streamed weights
+             ((2, 4, 300), (8, 4, 3), 0)]                # FFMA direct
+    for xs, ws_, pad in cases:
+        x = torch.from_numpy(rng.standard_normal(xs).astype(np.float32)).cuda()
+        w = torch.from_numpy(((rng.random(ws_) - 0.5) * 0.1).astype(np.float32)).cuda()
+        ref = cf.conv_fwd_nd(x, w, None, 1, pad, 1)
+        y = torch.empty_like(ref)
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            cf.conv_fwd_nd(x, w, None, 1, pad, 1, out=y)  # warm-up outside the capture
+        torch.cuda.current_stream().wait_stream(side)
+        with torch.cuda.graph(g):
+            cf.conv_fwd_nd(x, w, None, 1, pad, 1, out=y)
+        y.zero_()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref), f"graph replay differs for x {xs}"
+        x.mul_(2.0)  # the graph reads x at replay time
+        g.replay()
+        ref2 = cf.conv_fwd_nd(x, w, None, 1, pad, 1)
+        torch.cuda.synchronize()
+        assert torch.equal(y, ref2)
+
+
+def test_plain_call_streamed_weights_release_their_block():
+    # a layer with streamed weights called many times: the stream-ordered blocks are freed
+    rng = np.random.default_rng(3)
+    x = torch.from_numpy(rng.standard_normal((1, 64, 4, 6, 6)).astype(np.float32)).cuda()
+    w = torch.from_numpy(((rng.random((128, 64, 3, 3, 3)) - 0.5) * 0.05).astype(np.float32)).cuda()
+    assert cf.workspace_bytes(1, 64, 128, (4, 6, 6), (3, 3, 3), 1, 1, 1) > 0
+    y = cf.conv_fwd_nd(x, w, None, 1, 1, 1)
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for _ in range(200):
+        cf.conv_fwd_nd(x, w, None, 1, 1, 1, out=y)
+    torch.cuda.synchronize()
+    assert free0 - torch.cuda.mem_get_info()[0] < 64 << 20
 
 
 @pytest.mark.parametrize("C,mult,ins,k,pad", [
