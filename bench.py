@@ -384,21 +384,15 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {
-        "bytes": 50.511360e6 + 823.297792e6, "batch": 16,
-        "sha256": "94ca812ded6f0bc0df015f85db896e9b3bd3b9cb8736e53a81de583a0ed6d38f"},
-    ("igemm_3xtf32", "conv1d_long"): {
-        "bytes": 537.328640e6 + 307.182592e6, "batch": 4,
-        "sha256": "94ca812ded6f0bc0df015f85db896e9b3bd3b9cb8736e53a81de583a0ed6d38f"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {
-        "bytes": 35.426560e6 + 7.363328e6, "batch": 4,
-        "sha256": "94ca812ded6f0bc0df015f85db896e9b3bd3b9cb8736e53a81de583a0ed6d38f"},
-    ("igemm_bf16", "conv3d_asym"): {
-        "bytes": 25.295104e6 + 385.971200e6, "batch": 16,
-        "sha256": "8fd5ded5d1087519bef2cadf4f06f9820337ea091e045c84fc32bf28f52e637b"},
-    ("fused_ffma", "conv3d_min_softmax"): {
-        "bytes": 37.816320e6 + 0.001792e6, "batch": 128,
-        "sha256": "a3c8d352595b1412f32ddeb3d8a71383c322d0155fb883f3a6335d030c445a9c"},
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.769920e6 + 823.994880e6, "batch": 16, "sha256": "d9c2f39efd15a6585f8b1d7d9ea33154b2e2d3c5b6f643ac78dd9f212b3037f6"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.318144e6 + 307.582464e6, "batch": 4, "sha256": "d9c2f39efd15a6585f8b1d7d9ea33154b2e2d3c5b6f643ac78dd9f212b3037f6"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492800e6 + 0.090368e6, "batch": 8, "sha256": "d9c2f39efd15a6585f8b1d7d9ea33154b2e2d3c5b6f643ac78dd9f212b3037f6"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.446144e6 + 69.001728e6, "batch": 8, "sha256": "d9c2f39efd15a6585f8b1d7d9ea33154b2e2d3c5b6f643ac78dd9f212b3037f6"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.407616e6 + 7.979776e6, "batch": 4, "sha256": "d9c2f39efd15a6585f8b1d7d9ea33154b2e2d3c5b6f643ac78dd9f212b3037f6"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.839360e6 + 0.005888e6, "batch": 128, "sha256": "d9c2f39efd15a6585f8b1d7d9ea33154b2e2d3c5b6f643ac78dd9f212b3037f6"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.304832e6 + 385.616384e6, "batch": 16, "sha256": "713a6ba4556de466bf4e773355f04577074382d587bec99daebe58dd9b4c20b4"},
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.817600e6 + 0.002048e6, "batch": 128, "sha256": "fbf69429d02cf5dd77ef9f988d5467b9670468fb4599ba89f8a971c594977726"},
+    ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051968e6, "batch": 2, "sha256": "ef79ff89c6a99a86c33cde2383bd3a0d8edd97a3441d69c6d46b99b4389d2019"},
 }
 
 
