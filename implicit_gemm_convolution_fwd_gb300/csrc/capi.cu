@@ -2,6 +2,7 @@
 // family selection and dispatch.  Nothing here touches tensor data on the host.
 #include <stdarg.h>
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <mutex>
@@ -25,6 +26,29 @@ int fail(int status, const char *fmt, const char *detail = nullptr, long long a 
 int fail_cuda(cudaError_t e, const char *where) {
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
   return CONV_ERR_CUDA;
+}
+
+// CONVFWD_LOG=1 in the environment: one line per launching call on stderr
+// with the problem and the plan (kernel family, tiles, reduction padding,
+// slots, passes, whether the weights stream).  Read once per process.
+bool log_enabled() {
+  static const bool on = [] {
+    const char *e = getenv("CONVFWD_LOG");
+    return e && *e && strcmp(e, "0") != 0;
+  }();
+  return on;
+}
+
+void log_plan(const char *entry, const Geom &g, const char *family, bool streamed) {
+  if (!log_enabled()) return;
+  char detail[256] = "";
+  if (strncmp(family, "igemm_3xtf32", 12) == 0) convfwd::describe_igemm_plan(g, streamed, detail, sizeof(detail));
+  fprintf(stderr,
+          "convfwd: %s N=%lld C_in=%lld C_out=%lld groups=%lld in=%dx%dx%d k=%dx%dx%d s=%dx%dx%d p=%dx%dx%d "
+          "d=%dx%dx%d out=%dx%dx%d%s -> %s %s\n",
+          entry, (long long)g.N, (long long)(g.G * g.C), (long long)(g.G * g.K), (long long)g.G, g.D, g.H, g.W, g.KD,
+          g.KH, g.KW, g.SD, g.SH, g.SW, g.PD, g.PH, g.PW, g.DD, g.DH, g.DW, g.OD, g.OH, g.OW,
+          g.cl ? " channels-last" : "", family, detail);
 }
 
 constexpr int64_t kMaxDim = 0x7fffffff;  // every size must fit a signed 32-bit int
@@ -363,6 +387,7 @@ static int conv_grouped_impl(const float *x, const float *w, const float *bias, 
   cudaStream_t s = (cudaStream_t)stream;
   cudaError_t e = cudaSuccess;
   if (algo == CONV_ALGO_DIRECT_FFMA) {
+    log_plan("conv_fwd_nd", g, "direct_ffma", false);
     e = convfwd::launch_direct_ffma(x, w, bias, y, g, s);  // all groups in one grid
   } else {
     // A layer whose weights exceed shared memory streams them, split once per
@@ -377,6 +402,7 @@ static int conv_grouped_impl(const float *x, const float *w, const float *bias, 
       wsp = nullptr;
       (void)cudaGetLastError();
     }
+    log_plan("conv_fwd_nd", g, "igemm_3xtf32", wsp != nullptr);
     // one persistent launch per group on views of x, w, bias and y (the
     // kernel's batch strides span all groups' channels); the groups reuse wsp
     // in stream order
@@ -419,6 +445,7 @@ int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias,
   if (algo != CONV_ALGO_AUTO && algo != CONV_ALGO_IGEMM_3XTF32)
     return fail(CONV_ERR_ARG, "conv: unknown algo %s%lld", "", algo);
   if (g.N == 0) return CONV_OK;
+  log_plan("conv_fwd_nd_channels_last", g, "igemm_3xtf32", false);
   // one launch per group on channel offsets of x, w, bias and y
   cudaError_t e = cudaSuccess;
   for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
@@ -444,6 +471,7 @@ static int conv_fwd_16bit(const uint16_t *x, const uint16_t *w, const uint16_t *
                                            : "conv_fwd_nd_bf16: the tensor-core path cannot run this shape: %s",
                 why);
   if (g.N == 0) return CONV_OK;
+  log_plan(name, g, fp16 ? "igemm_f16" : "igemm_bf16", false);
   const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
   cudaError_t e = cudaSuccess;
   for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
@@ -503,6 +531,7 @@ int conv_fwd_nd_ws(const float *x, const float *w, const float *bias, float *y, 
       ranges_overlap(workspace, wsb, y, ye * 4) || ranges_overlap(workspace, wsb, bias, g.G * g.K * 4))
     return fail(CONV_ERR_ARG, "conv_fwd_nd_ws: workspace overlaps a tensor%s");
   if (g.N == 0) return CONV_OK;
+  log_plan("conv_fwd_nd_ws", g, "igemm_3xtf32", true);
   const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
   float *wsf = static_cast<float *>(workspace);
   cudaError_t e = cudaSuccess;
@@ -691,6 +720,9 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
     return fail(CONV_ERR_ARG, "conv3d_min_softmax: unknown algo %s%lld", "", algo);
   }
   if (g.N == 0) return CONV_OK;  // empty batch
+  log_plan(min_dim == 2 ? "conv3d_min_softmax(min over depth)" : min_dim == 3 ? "conv3d_min_softmax(min over height)"
+                                                                             : "conv3d_min_softmax(min over width)",
+           g, algo == CONV_ALGO_IGEMM_3XTF32 ? "fused igemm_3xtf32" : "fused ffma", false);
   cudaError_t e =
       algo == CONV_ALGO_IGEMM_3XTF32
           ? convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream)

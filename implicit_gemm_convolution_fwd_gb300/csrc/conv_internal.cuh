@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stddef.h>
 #include <stdint.h>
 
 namespace convfwd {
@@ -80,6 +81,9 @@ size_t igemm_stream_bytes_one_group(const Geom &g);
 // reduction passes).
 cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bias, float *y, const Geom &g,
                                 cudaStream_t stream, float *ws = nullptr);
+// One line of plan details for CONVFWD_LOG (tiles, reduction padding, slots,
+// passes, whether the weights stream).
+void describe_igemm_plan(const Geom &g, bool streamed, char *buf, size_t n);
 cudaError_t read_and_clear_device_status(unsigned *flags);
 // Clock cycles after which the tensor-core kernels' pipeline waits give up,
 // for launches from now on (cycles <= 0: the default, about two seconds).

@@ -36,6 +36,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdio.h>
 
 #include <atomic>
 
@@ -1022,6 +1023,24 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     }
   }
   return cudaSuccess;
+}
+
+void describe_igemm_plan(const Geom &g, bool streamed, char *buf, size_t n) {
+  Plan pl;
+  Geom gb = g;
+  if (gb.K > kMaxNpad) gb.K = kMaxNpad;
+  const char *why = "";
+  if (!make_plan(gb, &pl, &why)) {
+    snprintf(buf, n, "unsupported (%s)", why);
+    return;
+  }
+  const int64_t tiles = (g.N * g.out_spatial() + kTileM - 1) / kTileM;
+  const int64_t blocks = (g.K + kMaxNpad - 1) / kMaxNpad;
+  snprintf(buf, n,
+           "tiles=%lld Kred=%d Kpad=%d Npad=%d KC=%d slots=%d order=%s passes=%d channel_blocks=%lld weights=%s "
+           "smem=%zu",
+           (long long)tiles, pl.Kred, pl.Kpad, pl.Npad, pl.KC, pl.nslots, pl.tap_major ? "tap-major" : "channel-major",
+           streamed ? 1 : pl.npasses, (long long)blocks, streamed ? "streamed" : "resident", pl.smem);
 }
 
 bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {

@@ -41,6 +41,11 @@
  *   - Kernels never trap or assert.  Waits inside kernels are bounded; if one
  *     gives up, the kernel records it in a device-side status word that
  *     conv_device_status() reads.
+ *   - With CONVFWD_LOG=1 in the environment (read once per process), every
+ *     call that launches kernels writes one line to stderr: the entry point,
+ *     the problem, the kernel family and, for the tensor-core family, the plan
+ *     (tiles, reduction length and padding, column order, slots, passes,
+ *     channel blocks, resident or streamed weights, shared memory).
  */
 #ifndef CONVFWD_H
 #define CONVFWD_H

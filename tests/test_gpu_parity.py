@@ -791,6 +791,79 @@ def test_cuda_graph_capture_and_replay():
         assert torch.equal(y, ref2)
 
 
+def test_concurrent_streams_and_threads():
+    """Calls from four host threads, each on its own stream, interleaved: streamed-weight layers
+    (blocks from the library's pool), resident-weight layers and the host-buffer pipeline.  Every
+    result equals the same call made alone (each family is deterministic)."""
+    import threading
+    rng = np.random.default_rng(33)
+    shapes = [((1, 64, 4, 6, 6), (128, 64, 3, 3, 3), 1), ((2, 3, 6, 12, 40), (64, 3, 3, 5, 7), 0)]
+    inputs = []
+    for t in range(4):
+        xs, ws_, pad = shapes[t % 2]
+        x = torch.from_numpy(rng.standard_normal(xs).astype(np.float32)).cuda()
+        w = torch.from_numpy(((rng.random(ws_) - 0.5) * 0.1).astype(np.float32)).cuda()
+        inputs.append((x, w, pad))
+    alone = [cf.conv_fwd_nd(x, w, None, 1, pad, 1) for x, w, pad in inputs]
+    xh = torch.from_numpy(rng.standard_normal((4, 3, 6, 12, 40)).astype(np.float32)).pin_memory()
+    wh = torch.from_numpy(((rng.random((32, 3, 3, 5, 7)) - 0.5) * 0.1).astype(np.float32))
+    host_alone = cf.conv_fwd_nd_host(xh, wh, None, 1, 0, 1, chunk=1)
+    torch.cuda.synchronize()
+    results, errors = [None] * 4, []
+
+    def worker(t):
+        try:
+            st = torch.cuda.Stream()
+            x, w, pad = inputs[t]
+            with torch.cuda.stream(st):
+                for _ in range(5):
+                    y = cf.conv_fwd_nd(x, w, None, 1, pad, 1, stream=st)
+                yh = cf.conv_fwd_nd_host(xh, wh, None, 1, 0, 1, chunk=1, stream=st)
+            st.synchronize()
+            results[t] = (y, yh)
+        except Exception as e:  # reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(4)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    assert not errors, errors
+    for t in range(4):
+        assert torch.equal(results[t][0], alone[t]), f"thread {t}"
+        assert torch.equal(results[t][1], host_alone), f"thread {t} host path"
+    assert cf.device_status() == 0
+
+
+def test_plan_log_names_the_family_and_plan():
+    """CONVFWD_LOG=1: one stderr line per launching call with the problem and the plan."""
+    import subprocess, sys, os
+    code = ("import torch, implicit_gemm_convolution_fwd_gb300 as cf\n"
+            "x = torch.rand(2, 3, 6, 12, 40, device='cuda'); w = torch.rand(64, 3, 3, 5, 7, device='cuda')\n"
+            "cf.conv_fwd_nd(x, w, None, 1, 0, 1)\n"
+            "cf.conv_fwd_nd(torch.rand(1, 4, 99, device='cuda'), torch.rand(8, 4, 3, device='cuda'), None, 1, 0, 1)\n"
+            "cf.conv_fwd_nd(torch.rand(1, 64, 4, 6, 6, device='cuda'), torch.rand(128, 64, 3, 3, 3, device='cuda'),"
+            " None, 1, 1, 1)\n"
+            "x = torch.rand(2, 3, 8, 10, 10, device='cuda'); w = torch.rand(24, 3, 3, 3, 3, device='cuda')\n"
+            "cf.conv3d_min_softmax(x, w, None, 2)\n"
+            "torch.cuda.synchronize()\n")
+    env = dict(os.environ, CONVFWD_LOG="1")
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=300,
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stderr.splitlines() if l.startswith("convfwd: ")]
+    assert len(lines) == 4, r.stderr[-2000:]
+    assert "-> igemm_3xtf32 tiles=" in lines[0] and "Kred=315" in lines[0] and "weights=resident" in lines[0]
+    assert "-> direct_ffma" in lines[1]
+    assert "weights=streamed" in lines[2] and "passes=1" in lines[2]
+    assert "conv3d_min_softmax(min over depth)" in lines[3] and "-> fused ffma" in lines[3]
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
+                       env={k: v for k, v in os.environ.items() if k != "CONVFWD_LOG"},
+                       cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    assert r.returncode == 0 and "convfwd: " not in r.stderr
+
+
 def test_plain_call_streamed_weights_release_their_block():
     # a layer with streamed weights called many times: the stream-ordered blocks are freed
     rng = np.random.default_rng(3)
