@@ -723,10 +723,23 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
   log_plan(min_dim == 2 ? "conv3d_min_softmax(min over depth)" : min_dim == 3 ? "conv3d_min_softmax(min over height)"
                                                                              : "conv3d_min_softmax(min over width)",
            g, algo == CONV_ALGO_IGEMM_3XTF32 ? "fused igemm_3xtf32" : "fused ffma", false);
-  cudaError_t e =
-      algo == CONV_ALGO_IGEMM_3XTF32
-          ? convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream)
-          : convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream);
+  cudaError_t e = cudaSuccess;
+  if (algo == CONV_ALGO_IGEMM_3XTF32) {
+    // weights beyond shared memory stream from a stream-ordered block, as in conv_fwd_nd
+    const size_t sb = convfwd::igemm_fused_stream_bytes(g);
+    float *wsp = nullptr;
+    if (sb > 0) {
+      e = alloc_stream_ws(reinterpret_cast<void **>(&wsp), sb, (cudaStream_t)stream);
+      if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: weight workspace");
+    }
+    e = convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream, wsp);
+    if (wsp) {
+      const cudaError_t ef = cudaFreeAsync(wsp, (cudaStream_t)stream);
+      if (e == cudaSuccess) e = ef;
+    }
+  } else {
+    e = convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream);
+  }
   if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: kernel launch");
   return CONV_OK;
 }

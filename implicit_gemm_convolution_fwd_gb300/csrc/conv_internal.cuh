@@ -59,10 +59,12 @@ bool fused_supported(const Geom &g, int min_dim, const char **why);
 bool fused_ffma_preferred(const Geom &g);
 
 // The same fused op on the tensor cores (3xTF32): min over depth only,
-// C_out <= 32, weights resident in one pass.
+// C_out <= 32, weights resident in shared memory or streamed from ws (a
+// device workspace of igemm_fused_stream_bytes(g) bytes; 0 = resident).
 bool igemm_fused_supported(const Geom &g, int min_dim, const char **why);
+size_t igemm_fused_stream_bytes(const Geom &g);
 cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                           cudaStream_t stream);
+                                           cudaStream_t stream, float *ws = nullptr);
 
 // Tensor-core implicit GEMM on 16-bit tensors (bfloat16, or float16 when fp16; bit patterns),
 // fp32 accumulation, output in the input type.

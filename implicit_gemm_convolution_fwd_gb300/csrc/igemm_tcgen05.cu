@@ -1058,18 +1058,31 @@ bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {
     return false;
   }
   if (!make_plan(g, &pl, why)) return false;
-  if (pl.npasses != 1 || pl.KC != 16) {
-    *why = "tensor-core fused path: the weights must fit in one pass";
+  if (pl.KC != 16) {
+    *why = "tensor-core fused path: no 16-column stages";
+    return false;
+  }
+  if (pl.npasses != 1 && igemm_stream_bytes_one_group(g) == 0) {
+    *why = "tensor-core fused path: the weights neither fit in shared memory nor stream";
     return false;
   }
   return true;
 }
 
+size_t igemm_fused_stream_bytes(const Geom &g) {
+  Plan pl;
+  const char *why = "";
+  if (!make_plan(g, &pl, &why) || pl.npasses == 1) return 0;
+  return igemm_stream_bytes_one_group(g);
+}
+
 cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                           cudaStream_t stream) {
+                                           cudaStream_t stream, float *ws) {
   Plan pl;
   const char *why = "";
   if (!igemm_fused_supported(g, 2, &why) || !make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
+  const bool streamed = pl.npasses != 1;
+  if (streamed && !ws) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1081,9 +1094,13 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   if (!g_attr_fused_set[dev]) {
     e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kMaxSmem);
     if (e != cudaSuccess) return e;
     g_attr_fused_set[dev] = true;
   }
+  const int64_t kfull = g.C * (int64_t)g.taps();
   IgemmParams p = {};
   p.wait_limit = g_wait_limit.load();
   p.x = x;
@@ -1096,19 +1113,43 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.hw_tiles = (int)(((int64_t)g.OH * g.OW + kTileM - 1) / kTileM);
   p.columns = g.N * p.hw_tiles;
   p.tiles = p.columns * g.OD;
-  p.Kred = pl.Kred;
-  p.Kfull = pl.Kred;
+  p.Kfull = (int)kfull;
   p.k_begin = 0;
   p.accumulate = 0;
   p.y_chans = g.K;
-  p.Kpad = pl.Kpad;
   p.Npad = pl.Npad;
   p.KC = pl.KC;
-  p.nchunks = pl.nchunks;
   p.nslots = pl.nslots;
   p.tap_major = pl.tap_major;
-  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   const int64_t grid = p.columns < g_num_sms[dev] ? p.columns : g_num_sms[dev];
+  if (streamed) {
+    // the whole reduction in one pass, its weights split once into ws and
+    // brought in chunk by chunk (as for the plain conv's streamed weights)
+    const int kpad = (int)((kfull + 31) / 32 * 32);
+    const int nchunks = kpad / pl.KC;
+    const int64_t total = (int64_t)pl.Npad * pl.KC * nchunks;
+    const int threads = 256;
+    const int64_t blocks64 = (total + threads - 1) / threads;
+    const int blocks = (int)(blocks64 < 4096 ? blocks64 : 4096);
+    split_weights_kernel<<<blocks, threads, 0, stream>>>(w, ws, (int)g.K, (int)g.C, g.taps(), (int)kfull, pl.Npad,
+                                                         pl.KC, nchunks, pl.tap_major);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    p.Kred = (int)kfull;
+    p.Kpad = kpad;
+    p.nchunks = nchunks;
+    p.wsp = ws;
+    p.sb_stage_bytes = (uint32_t)(2 * pl.Npad * pl.KC * 4);
+    p.b_bytes = (uint32_t)(pl.nslots * 2) * p.sb_stage_bytes;
+    const size_t smem_need = (size_t)p.b_bytes + (size_t)kpad * 8 + (size_t)pl.Npad * 4 + 16 + kNumBars * 8 + 16;
+    const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
+    igemm_3xtf32_kernel<16, false, true, true><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  p.Kred = pl.Kred;
+  p.Kpad = pl.Kpad;
+  p.nchunks = pl.nchunks;
+  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   igemm_3xtf32_kernel<16, false, false, true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }

@@ -18,8 +18,9 @@
  *     the call returns.  y must not overlap x, w or bias.  One kind of call
  *     allocates device memory: conv_fwd_nd, conv_fwd_nd_ex, conv_fwd_nd_grouped
  *     and conv_fwd_nd_host, on a tensor-core layer whose weights exceed shared
- *     memory (conv_workspace_bytes > 0), take a stream-ordered block of that
- *     size for the split weights (allocated on `stream` from a memory pool of
+ *     memory (conv_workspace_bytes > 0), and conv3d_min_softmax(_ex) on the
+ *     tensor-core kernel in the same case, take a stream-ordered block for the
+ *     split weights (allocated on `stream` from a memory pool of
  *     the library's, or from the device's default pool while `stream` is being
  *     captured into a graph, and freed on `stream` after the call's last
  *     launch; if the allocation fails, the layer runs in several passes
@@ -314,8 +315,9 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  Two kernel families: the FFMA
  * kernels (C_out up to 96, a kernel extent along y's last axis up to 7) and a
  * tensor-core kernel (3xTF32 implicit GEMM whose epilogue keeps each
- * position's running minimum over depth in registers; min_dim 2, C_out <= 32,
- * weights that fit in shared memory).  Where both run, the planner takes the
+ * position's running minimum over depth in registers; min_dim 2, C_out <= 32;
+ * weights that exceed shared memory stream through a stream-ordered block of
+ * the call, as for conv_fwd_nd).  Where both run, the planner takes the
  * FFMA kernels for short reductions over few channels (C_out <= 24 with
  * C_in * |kernel| <= 256, or C_in * |kernel| <= 32) and the tensor-core kernel
  * otherwise.  Shapes neither family runs are CONV_ERR_UNSUPPORTED.

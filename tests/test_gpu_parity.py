@@ -131,6 +131,8 @@ def test_edge_geometries(algo):
         ((1, 2, 3, 3, 3), (2, 2, 3, 3, 3), (1, 1, 1), (2, 2, 2), (1, 1, 1)),  # pad 2 around 3^3
         ((2, 1, 7, 1, 9), (3, 1, 2, 1, 4), (2, 1, 1), (1, 0, 2), (2, 1, 2)),  # singleton H
         ((1, 4, 130), (67, 4, 3), (1,), (1,), (1,)),                  # C_out not a multiple of any tile
+        ((1, 4, 200), (16, 4, 32), (1,), (3,), (1,)),                 # 32 taps along W (a full 32-bit tap mask), padded
+        ((1, 2, 3, 40, 8), (16, 2, 1, 32, 3), (1, 1, 1), (0, 2, 1), (1, 1, 1)),  # 32 taps along H, padded
     ]
     for xs, ws, s, p, d in cases:
         x = rng.standard_normal(xs).astype(np.float32)
@@ -277,6 +279,30 @@ def test_fused_tensor_core_geometries(shape, C_in, C_out, k):
     assert_close(run_fused(x, w, b, TC).cpu().numpy(), ref, f"fused tensor cores {shape} k={k}")
     assert_close(run_fused(x, w, None, TC).cpu().numpy(), oracle.conv3d_min_softmax(x, w, None),
                  f"fused tensor cores no bias {shape}")
+
+
+@pytest.mark.parametrize("shape,C_out,k", [
+    ((2, 64, 6, 10, 12), 32, (3, 3, 3)),    # 1728 reduction columns: weights (hi + lo) exceed shared memory
+    ((1, 40, 5, 9, 140), 20, (3, 3, 3)),    # 1080 columns, rows of 138 outputs (2 column tiles per row)
+    ((2, 128, 4, 6, 7), 7, (2, 2, 2)),      # 1024 columns, 7 channels
+])
+def test_fused_tensor_core_streamed_weights(shape, C_out, k):
+    rng = np.random.default_rng(shape[1] + C_out)
+    x = rng.standard_normal(shape).astype(np.float32)
+    w = ((rng.random((C_out, shape[1]) + k) - 0.5) * 2 / np.sqrt(shape[1] * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv3d_min_softmax(x, w, b)
+    y = run_fused(x, w, b, TC).cpu().numpy()
+    assert_close(y, ref, f"fused tensor cores, streamed weights {shape} C_out={C_out}")
+    # long reductions: the planner takes the tensor cores (where the FFMA kernels can hold the
+    # weights at all, they must agree with the oracle too)
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    try:
+        yf = cf.conv3d_min_softmax(xt, wt, bt, 2, algo=FFMA)
+        assert_close(yf.cpu().numpy(), ref, f"fused FFMA {shape} C_out={C_out}")
+    except cf.ConvError as e:
+        assert e.status == cf.CONV_ERR_UNSUPPORTED
+    assert torch.equal(cf.conv3d_min_softmax(xt, wt, bt, 2), torch.from_numpy(y).cuda())
 
 
 def test_fused_planner_takes_the_measured_family():
