@@ -256,10 +256,12 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
       const uint16_t *xo = p.xh + (ps.valid ? ps.xoff : 0);
-      const int64_t lg0 = li * p.nchunks;
+      // slot-local index of the tile's first chunk; only its low bits matter
+      // (stage and phase parity), so 32-bit arithmetic (wrapping) serves
+      const uint32_t lg0 = (uint32_t)li * (uint32_t)p.nchunks;
       // chunk q (slot-local lg = lg0 + q): wait for its stage, store, signal the issuer
       auto put = [&](int q, const uint32_t (&packed)[kBfChunk / 2]) -> bool {
-        const int64_t lg = lg0 + q;
+        const uint32_t lg = lg0 + (uint32_t)q;
         const int stage = 2 * slot + (int)(lg & 1);
         const uint32_t r = (uint32_t)(lg >> 1);
         const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit, kWaitSiteAEmpty);
@@ -271,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         ptx::mbar_arrive(bar_a_full + 8 * stage);
         return true;
       };
-      int q = (int)((sel - lg0 % gps + gps) % gps);
+      int q = (int)((sel - (int)(lg0 % (uint32_t)gps) + gps) % gps);
       if (ps.warp_full) {
         // full chunks of an interior warp: four offsets per shared load, no tests
         const int nfull = p.Kred / kBfChunk;
@@ -322,8 +324,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
                                                   kWaitSiteDEmpty))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
-        const int64_t lg = li * p.nchunks + q;
-        const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
+        const uint32_t lg = (uint32_t)li * (uint32_t)p.nchunks + (uint32_t)q;
+        const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = lg >> 1;
         if (!__all_sync(0xffffffffu, wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteAFull))) {
           aborted = true;
           break;

@@ -659,12 +659,13 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     // Slot-local chunk lg (= chunk q of its tile): wait for its stage to
     // drain, split into hi / lo, store both to TMEM and signal the issuer.
     // The lo part overwrites v in place (keeps the chunk within the register
-    // budget without spills).  False when the wait timed out.
+    // budget without spills).  False when the wait timed out.  full: the
+    // chunk is known to hold KC columns (no per-unit column test).
     // streamed weights: the group's thread 0 brings chunk q's B into the
     // stage; it remembers its last copy to wait for it before leaving
     int sb_last_stage = -1;
     uint32_t sb_last_parity = 0;
-    auto put_chunk = [&](int64_t lg, int q, float (&v)[CH]) -> bool {
+    auto put_chunk = [&](uint32_t lg, int q, float (&v)[CH], bool full = false) -> bool {
       const int stage = 2 * slot + (int)(lg & 1);
       const uint32_t a_hi_col = a_col0 + (uint32_t)(2 * p.KC * stage);
       const uint32_t a_lo_col = a_hi_col + (uint32_t)p.KC;
@@ -683,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       }
 #pragma unroll
       for (int u = 0; u < CH / kUnit; ++u) {
-        if (u * kUnit < ncols) {
+        if (full || u * kUnit < ncols) {
 #pragma unroll
           for (int h = 0; h < kUnit; h += 8) {
             uint32_t tmp[8];
@@ -721,14 +722,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position<FUSED>(p, tile_of<FUSED>(p, li * nslots + slot), t);
-      const int64_t lg0 = li * p.nchunks;  // slot-local index of the tile's first chunk
+      // slot-local index of the tile's first chunk; only its low bits matter
+      // (stage and phase parity), so 32-bit arithmetic (wrapping) serves
+      const uint32_t lg0 = (uint32_t)li * (uint32_t)p.nchunks;
       // this group's chunks of the tile: lg = lg0 + q with lg = sel (mod gps)
-      int q = (int)((sel - lg0 % gps + gps) % gps);
+      int q = (int)((sel - (int)(lg0 % (uint32_t)gps) + gps) % gps);
       if (CH == 16 && ps.warp_full) {
         for (; q < nfull; q += gps) {
           float v[CH];
           gather_full(ps, q, v);
-          if (!put_chunk(lg0 + q, q, v)) {
+          if (!put_chunk(lg0 + q, q, v, true)) {
             aborted = true;
             break;
           }
@@ -774,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
                                                   kWaitSiteDEmpty))) break;
       ptx::tc_fence_after();
       for (int q = 0; q < p.nchunks; ++q) {
-        const int64_t lg = li * p.nchunks + q;
+        const uint32_t lg = (uint32_t)li * (uint32_t)p.nchunks + (uint32_t)q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = (uint32_t)(lg >> 1);
         bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteAFull);
         if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteBFull);
