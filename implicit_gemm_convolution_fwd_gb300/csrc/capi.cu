@@ -711,7 +711,7 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
   // kernel's im2col gather costs more than the FFMAs; the tensor-core kernel
   // for longer reductions or more channels; whichever runs otherwise
   if (algo == CONV_ALGO_AUTO)
-    algo = tc_ok && !(ffma_ok && convfwd::fused_ffma_preferred(g)) ? CONV_ALGO_IGEMM_3XTF32 : CONV_ALGO_DIRECT_FFMA;
+    algo = tc_ok && !(ffma_ok && convfwd::fused_ffma_preferred(g, min_dim)) ? CONV_ALGO_IGEMM_3XTF32 : CONV_ALGO_DIRECT_FFMA;
   if (algo == CONV_ALGO_DIRECT_FFMA) {
     if (!ffma_ok) return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
   } else if (algo == CONV_ALGO_IGEMM_3XTF32) {
@@ -732,7 +732,7 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
       e = alloc_stream_ws(reinterpret_cast<void **>(&wsp), sb, (cudaStream_t)stream);
       if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: weight workspace");
     }
-    e = convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, (cudaStream_t)stream, wsp);
+    e = convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream, wsp);
     if (wsp) {
       const cudaError_t ef = cudaFreeAsync(wsp, (cudaStream_t)stream);
       if (e == cudaSuccess) e = ef;

@@ -56,15 +56,16 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
 bool fused_supported(const Geom &g, int min_dim, const char **why);
 // True when the FFMA fused kernel measures faster than the tensor-core one on
 // this geometry (both able to run it).
-bool fused_ffma_preferred(const Geom &g);
+bool fused_ffma_preferred(const Geom &g, int min_dim);
 
-// The same fused op on the tensor cores (3xTF32): min over depth only,
-// C_out <= 32, weights resident in shared memory or streamed from ws (a
-// device workspace of igemm_fused_stream_bytes(g) bytes; 0 = resident).
+// The same fused op on the tensor cores (3xTF32): min over depth, height or
+// width (min_dim 2, 3, 4), C_out <= 32, weights resident in shared memory or
+// streamed from ws (a device workspace of igemm_fused_stream_bytes(g) bytes;
+// 0 = resident).
 bool igemm_fused_supported(const Geom &g, int min_dim, const char **why);
 size_t igemm_fused_stream_bytes(const Geom &g);
 cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                           cudaStream_t stream, float *ws = nullptr);
+                                           int min_dim, cudaStream_t stream, float *ws = nullptr);
 
 // Tensor-core implicit GEMM on 16-bit tensors (bfloat16, or float16 when fp16; bit patterns),
 // fp32 accumulation, output in the input type.

@@ -636,17 +636,25 @@ bool fused_supported(const Geom &g, int min_dim, const char **why) {
   return true;
 }
 
-bool fused_ffma_preferred(const Geom &g) {
+bool fused_ffma_preferred(const Geom &g, int min_dim) {
   // Measured on GB300 against the tensor-core fused kernel on [N, C_in, 24,
-  // 32, 32] inputs with 3x3x3 kernels and N * C_in held near 384: the FFMA
-  // kernel wins for C_out <= 24 (two channel groups) up to C_in = 8 (0.21
-  // against 0.49 ms at C_in = 3, 0.33 against 0.47 at C_in = 8) and loses from
-  // C_in = 12 on (1.10 against 0.47); with four channel groups (C_out = 32
-  // runs 48 channels) it wins only at C_in = 1 (0.61 against 0.65) and loses
-  // from C_in = 3 on (0.66 against 0.49).
+  // 32, 32] inputs with 3x3x3 kernels and N * C_in held near 384 (FFMA /
+  // tensor cores, ms).  Min over depth: C_out = 24 (two channel groups of 12)
+  // 0.21 / 0.49 at C_in = 3, 0.33 / 0.48 at C_in = 8, 1.11 / 0.47 at C_in =
+  // 12; C_out = 32 (four groups, 48 channels run) 0.61 / 0.65 at C_in = 1,
+  // 0.66 / 0.49 at C_in = 3.  Min over height (the staged FFMA kernel):
+  // C_out = 24 0.28 / 0.35 at C_in = 4, 0.38 / 0.30 at C_in = 8; C_out = 32
+  // 0.58 / 0.52 already at C_in = 1.  Min over width (the generic FFMA
+  // kernel; the tensor-core tiles then step along height, a strided gather):
+  // C_out = 24 0.77 / 0.95 at C_in = 4, 1.45 / 0.92 at C_in = 8; C_out = 32
+  // 0.78 / 0.99 at C_in = 1, 1.09 / 1.07 at C_in = 3.
   const int64_t kred = g.C * g.taps();
   const int ncg = pick_ncg(g.K);
-  return (ncg <= 2 && kred <= 256) || kred <= 32;
+  switch (min_dim) {
+    case 2: return (ncg <= 2 && kred <= 256) || kred <= 32;
+    case 3: return ncg <= 2 && kred <= 128;
+    default: return (ncg <= 2 && kred <= 128) || kred <= 32;
+  }
 }
 
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,

@@ -108,7 +108,14 @@ struct IgemmParams {
   // column is (image, block of 128 positions of the output plane); each CTA
   // runs its columns' OD depth tiles back to back
   int64_t columns;  // N * hw_tiles
-  int hw_tiles;     // ceil(OH * OW / 128)
+  int hw_tiles;     // ceil(plane / 128)
+  // the reduced output dim (depth, height or width): R positions at stride sR
+  // in an image's flat output index; the kept plane (A x nB positions, A at
+  // stride sA, B at stride sB) is what y holds per image and channel
+  int R;
+  int64_t plane;
+  int nB;
+  int64_t sR, sA, sB;
 };
 
 struct Plan {
@@ -184,14 +191,14 @@ bool make_plan(const Geom &g, Plan *pl, const char **why) {
 template <bool FUSED = false>
 __device__ __forceinline__ int64_t tile_of(const IgemmParams &p, int64_t it) {
   if (FUSED) {
-    const int64_t od = p.g.OD, c = it / od;
+    const int64_t od = p.R, c = it / od;
     return (blockIdx.x + c * (int64_t)gridDim.x) * od + (it - c * od);
   }
   return blockIdx.x + it * (int64_t)gridDim.x;
 }
 template <bool FUSED = false>
 __device__ __forceinline__ int64_t cta_tile_count(const IgemmParams &p) {
-  if (FUSED) return (p.columns - blockIdx.x + gridDim.x - 1) / gridDim.x * p.g.OD;
+  if (FUSED) return (p.columns - blockIdx.x + gridDim.x - 1) / gridDim.x * p.R;
   return (p.tiles - blockIdx.x + gridDim.x - 1) / gridDim.x;
 }
 
@@ -243,12 +250,14 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   PosInfo ps;
   int64_t m;
   if (FUSED) {
-    // tile = column * OD + depth; row t is position hw_tile * 128 + t of the (image, depth) plane
-    const int64_t col = tile / g.OD, ohw = (int64_t)g.OH * g.OW;
-    const int64_t d = tile - col * g.OD, img = col / p.hw_tiles;
+    // tile = column * R + r; row t is position hw_tile * 128 + t of the kept
+    // plane, at index r of the reduced dim
+    const int64_t col = tile / p.R;
+    const int64_t r = tile - col * p.R, img = col / p.hw_tiles;
     const int64_t pp = (col - img * p.hw_tiles) * kTileM + t;
-    ps.valid = pp < ohw;
-    m = img * p.osp + d * ohw + (ps.valid ? pp : 0);
+    ps.valid = pp < p.plane;
+    const int64_t a = ps.valid ? pp / p.nB : 0, bb = ps.valid ? pp - a * p.nB : 0;
+    m = img * p.osp + r * p.sR + a * p.sA + bb * p.sB;
   } else {
     m = tile * kTileM + t;
     ps.valid = m < p.M_total;
@@ -479,16 +488,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 
   if (FUSED && warp < kEpiWarps) {
     // ------------------------------------------------------------ fused epilogue
-    // Lane tid owns position hw_tile * 128 + tid of its column's plane; over
-    // the column's OD depth tiles it keeps min_d conv[n, o, d, pos] for each
-    // channel o < K <= 32, then adds the bias (min(z + b) = min(z) + b: x ->
+    // Lane tid owns position hw_tile * 128 + tid of its column's kept plane;
+    // over the column's R tiles along the reduced dim it keeps
+    // min_r conv[n, o, r, pos] for each channel o < K <= 32, then adds the bias (min(z + b) = min(z) + b: x ->
     // fl(x + b) is monotone), takes the softmax over o with the maximum
     // subtracted, and writes y[n, o, pos]: a warp store covers 32
     // consecutive positions of one channel.
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
     const int64_t my_tiles = cta_tile_count<true>(p);
-    const int OD = g.OD, K = g.K;
-    const int64_t ohw = (int64_t)g.OH * g.OW;
+    const int R = p.R, K = g.K;  // R: the reduced extent (depth, height or width)
+    const int64_t plane = p.plane;
     float mn[32];
 #pragma unroll
     for (int j = 0; j < 32; ++j) mn[j] = 0.f;
@@ -497,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       const bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit, kWaitSiteDFull);
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
-      const int64_t d = it % OD;
+      const int64_t d = it % R;
       // the accumulator in two halves of 16 columns (fewer live registers)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
@@ -514,10 +523,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       }
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_d_empty + 8 * b);
-      if (d == OD - 1) {
-        const int64_t col = tile_of<true>(p, it) / OD, img = col / p.hw_tiles;
+      if (d == R - 1) {
+        const int64_t col = tile_of<true>(p, it) / R, img = col / p.hw_tiles;
         const int64_t pp = (col - img * p.hw_tiles) * kTileM + tid;
-        if (pp < ohw) {
+        if (pp < plane) {
           float mx = -INFINITY;
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
@@ -531,10 +540,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
             sum += mn[j];
           }
           const float inv = 1.f / sum;
-          float *yp = p.y + img * (int64_t)K * ohw + pp;
+          float *yp = p.y + img * (int64_t)K * plane + pp;
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j < K) __stcs(yp + (int64_t)j * ohw, mn[j] * inv);
+            if (j < K) __stcs(yp + (int64_t)j * plane, mn[j] * inv);
         }
       }
     }
@@ -1048,8 +1057,8 @@ void describe_igemm_plan(const Geom &g, bool streamed, char *buf, size_t n) {
 
 bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {
   Plan pl;
-  if (min_dim != 2) {
-    *why = "tensor-core fused path: the min runs over depth only";
+  if (min_dim < 2 || min_dim > 4) {
+    *why = "tensor-core fused path: min_dim must be 2, 3 or 4";
     return false;
   }
   if (g.K > 32) {
@@ -1080,10 +1089,10 @@ size_t igemm_fused_stream_bytes(const Geom &g) {
 }
 
 cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                           cudaStream_t stream, float *ws) {
+                                           int min_dim, cudaStream_t stream, float *ws) {
   Plan pl;
   const char *why = "";
-  if (!igemm_fused_supported(g, 2, &why) || !make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
+  if (!igemm_fused_supported(g, min_dim, &why) || !make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
   const bool streamed = pl.npasses != 1;
   if (streamed && !ws) return cudaErrorInvalidValue;
   int dev = 0;
@@ -1113,9 +1122,18 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.g = g;
   p.osp = (int64_t)g.OD * g.OH * g.OW;
   p.M_total = g.N * p.osp;
-  p.hw_tiles = (int)(((int64_t)g.OH * g.OW + kTileM - 1) / kTileM);
+  // the reduced dim and the kept plane (A, B in order) in the flat output index d * OH*OW + h * OW + w
+  const int64_t sD = (int64_t)g.OH * g.OW, sH = g.OW, sW = 1;
+  if (min_dim == 2) {
+    p.R = g.OD, p.sR = sD, p.nB = g.OW, p.sA = sH, p.sB = sW, p.plane = (int64_t)g.OH * g.OW;
+  } else if (min_dim == 3) {
+    p.R = g.OH, p.sR = sH, p.nB = g.OW, p.sA = sD, p.sB = sW, p.plane = (int64_t)g.OD * g.OW;
+  } else {
+    p.R = g.OW, p.sR = sW, p.nB = g.OH, p.sA = sD, p.sB = sH, p.plane = (int64_t)g.OD * g.OH;
+  }
+  p.hw_tiles = (int)((p.plane + kTileM - 1) / kTileM);
   p.columns = g.N * p.hw_tiles;
-  p.tiles = p.columns * g.OD;
+  p.tiles = p.columns * p.R;
   p.Kfull = (int)kfull;
   p.k_begin = 0;
   p.accumulate = 0;

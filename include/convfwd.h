@@ -315,12 +315,13 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  Two kernel families: the FFMA
  * kernels (C_out up to 96, a kernel extent along y's last axis up to 7) and a
  * tensor-core kernel (3xTF32 implicit GEMM whose epilogue keeps each
- * position's running minimum over depth in registers; min_dim 2, C_out <= 32;
+ * position's running minimum over the reduced dim in registers; C_out <= 32;
  * weights that exceed shared memory stream through a stream-ordered block of
- * the call, as for conv_fwd_nd).  Where both run, the planner takes the
- * FFMA kernels for short reductions over few channels (C_out <= 24 with
- * C_in * |kernel| <= 256, or C_in * |kernel| <= 32) and the tensor-core kernel
- * otherwise.  Shapes neither family runs are CONV_ERR_UNSUPPORTED.
+ * the call, as for conv_fwd_nd).  Where both run, the planner takes the FFMA
+ * kernels for short reductions over few channels and the tensor-core kernel
+ * otherwise; with K = C_in * |kernel| and C_out <= 24: FFMA for K <= 256 (min
+ * over depth) or K <= 128 (height, width); with more channels FFMA only for
+ * K <= 32 (depth, width).  Shapes neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);

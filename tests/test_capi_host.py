@@ -138,9 +138,10 @@ def test_fused_validation_statuses(lib):
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 4, None) == cf.CONV_ERR_SHAPE
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 1, None) == cf.CONV_ERR_ARG
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 5, None) == cf.CONV_ERR_ARG
-    # min over W: the kernel's column axis is H, so KH is limited to 7
-    wtall = T5(0x100000, (ctypes.c_int64 * 5)(24, 3, 3, 9, 3))
-    ytall = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 22, 24))
+    # min over W: the FFMA kernels' column axis is H, so KH is limited to 7, and the tensor-core
+    # kernel takes at most 32 channels: 40 channels with KH = 9 run on neither
+    wtall = T5(0x100000, (ctypes.c_int64 * 5)(40, 3, 3, 9, 3))
+    ytall = T4(0x40000000, (ctypes.c_int64 * 4)(2, 40, 22, 24))
     assert f(ctypes.byref(x), ctypes.byref(wtall), None, ctypes.byref(ytall), 4, None) == cf.CONV_ERR_UNSUPPORTED
     wbad = T5(0x100000, (ctypes.c_int64 * 5)(24, 4, 3, 3, 3))
     assert f(ctypes.byref(x), ctypes.byref(wbad), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE

@@ -318,14 +318,46 @@ def test_fused_planner_takes_the_measured_family():
     assert (auto == tc).all() and not (auto == ffma).all()
 
 
+@pytest.mark.parametrize("min_dim", [3, 4])
+def test_fused_planner_over_height_and_width(min_dim):
+    # the page's channel counts keep the FFMA kernels; 32 channels over C_in = 8 take the tensor cores
+    wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    auto, ffma = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, FFMA))
+    assert torch.equal(auto, ffma)
+    rng = np.random.default_rng(12)
+    xt = torch.from_numpy(rng.random((2, 8, 10, 20, 20)).astype(np.float32)).cuda()
+    wt = torch.from_numpy(((rng.random((32, 8, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)).cuda()
+    auto, tc = (cf.conv3d_min_softmax(xt, wt, None, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, TC))
+    assert torch.equal(auto, tc)
+
+
 def test_fused_tensor_core_refuses_what_it_cannot_run():
     x = torch.zeros((1, 3, 5, 9, 9), device="cuda")
-    with pytest.raises(cf.ConvError) as e:
-        cf.conv3d_min_softmax(x, torch.zeros((33, 3, 3, 3, 3), device="cuda"), None, 2, algo=TC)
-    assert e.value.status == cf.CONV_ERR_UNSUPPORTED
-    with pytest.raises(cf.ConvError) as e:
-        cf.conv3d_min_softmax(x, torch.zeros((8, 3, 3, 3, 3), device="cuda"), None, 3, algo=TC)
-    assert e.value.status == cf.CONV_ERR_UNSUPPORTED
+    for min_dim in (2, 3, 4):
+        with pytest.raises(cf.ConvError) as e:
+            cf.conv3d_min_softmax(x, torch.zeros((33, 3, 3, 3, 3), device="cuda"), None, min_dim, algo=TC)
+        assert e.value.status == cf.CONV_ERR_UNSUPPORTED
+
+
+@pytest.mark.parametrize("min_dim", [3, 4])
+@pytest.mark.parametrize("shape,C_out,k", [
+    ((2, 3, 7, 11, 37), 24, (3, 3, 3)),     # the page's channel counts on a ragged box
+    ((1, 5, 9, 40, 45), 32, (2, 5, 4)),     # 32 channels, kept planes of several 128-position tiles
+    ((3, 2, 30, 6, 5), 13, (3, 1, 2)),      # a long reduced axis when the min runs over height
+    ((2, 48, 5, 8, 9), 20, (3, 3, 3)),      # 1296 reduction columns: streamed weights
+])
+def test_fused_tensor_core_min_over_height_and_width(shape, C_out, k, min_dim):
+    rng = np.random.default_rng(shape[1] * 7 + C_out + min_dim)
+    x = rng.standard_normal(shape).astype(np.float32)
+    w = ((rng.random((C_out, shape[1]) + k) - 0.5) * 2 / np.sqrt(shape[1] * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv3d_min_softmax(x, w, b, min_dim)
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    y = cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=TC)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, f"fused tensor cores min_dim={min_dim} {shape} C_out={C_out}")
+    assert np.abs(y.sum(dim=1).cpu().numpy() - 1).max() < 1e-5
 
 
 def test_fused_vector_path_and_ragged_rows():
