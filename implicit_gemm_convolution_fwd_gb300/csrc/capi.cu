@@ -738,7 +738,19 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
       if (e == cudaSuccess) e = ef;
     }
   } else {
-    e = convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream);
+    // the min over width runs faster as a min over height of transposed copies of x and w
+    // (a stream-ordered block); without the block, on the generic kernel
+    const size_t tb = convfwd::fused_transpose_bytes(g, min_dim);
+    float *wsp = nullptr;
+    if (tb > 0 && alloc_stream_ws(reinterpret_cast<void **>(&wsp), tb, (cudaStream_t)stream) != cudaSuccess) {
+      wsp = nullptr;
+      (void)cudaGetLastError();
+    }
+    e = convfwd::launch_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream, wsp);
+    if (wsp) {
+      const cudaError_t ef = cudaFreeAsync(wsp, (cudaStream_t)stream);
+      if (e == cudaSuccess) e = ef;
+    }
   }
   if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: kernel launch");
   return CONV_OK;

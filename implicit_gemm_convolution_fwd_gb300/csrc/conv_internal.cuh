@@ -49,8 +49,13 @@ cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias
 
 // Fused conv3d -> min over tensor dim min_dim (2 = depth, 3 = height,
 // 4 = width) -> channel softmax.
+// ws: a device workspace of fused_transpose_bytes(g, min_dim) bytes, or
+// nullptr.  With it, the min over width runs as the min over height of x and
+// w transposed in their last two dims (the staged kernel); without it, on the
+// generic kernel.
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
-                                     const Geom &g, int min_dim, cudaStream_t stream);
+                                     const Geom &g, int min_dim, cudaStream_t stream, float *ws = nullptr);
+size_t fused_transpose_bytes(const Geom &g, int min_dim);
 // True when launch_fused_min_softmax supports this geometry (channel count,
 // kernel extent along the output's last axis, shared-memory footprint).
 bool fused_supported(const Geom &g, int min_dim, const char **why);

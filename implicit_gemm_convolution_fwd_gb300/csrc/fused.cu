@@ -549,6 +549,55 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 }
 
 // Shared-memory plan of the staged variant; false when it does not apply.
+// Batched transpose of the last two dims, in [B][R][C] -> out [B][C][R], in
+// 32 x 32 tiles through shared memory (both sides coalesced).  Block 32 x 8.
+__global__ void __launch_bounds__(256) transpose_last2_kernel(const float *__restrict__ in, float *__restrict__ out,
+                                                             int64_t B, int R, int C) {
+  __shared__ float t[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int64_t b = blockIdx.z; b < B; b += gridDim.z) {
+    const float *src = in + b * (int64_t)R * C;
+    float *dst = out + b * (int64_t)R * C;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int r = r0 + i, c = c0 + (int)threadIdx.x;
+      if (r < R && c < C) t[i][threadIdx.x] = src[(int64_t)r * C + c];
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8) {
+      const int c = c0 + i, r = r0 + (int)threadIdx.x;
+      if (r < R && c < C) dst[(int64_t)c * R + r] = t[threadIdx.x][i];
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_transpose_last2(const float *in, float *out, int64_t B, int R, int C, cudaStream_t stream) {
+  if (B == 0) return cudaSuccess;
+  const dim3 grid((unsigned)((C + 31) / 32), (unsigned)((R + 31) / 32), (unsigned)(B < 65535 ? B : 65535));
+  transpose_last2_kernel<<<grid, dim3(32, 8), 0, stream>>>(in, out, B, R, C);
+  return cudaGetLastError();
+}
+
+// The same problem with H and W exchanged (x and w transposed in their last two dims).
+Geom swap_hw(const Geom &g) {
+  Geom t = g;
+  t.H = g.W, t.W = g.H, t.OH = g.OW, t.OW = g.OH, t.KH = g.KW, t.KW = g.KH;
+  t.SH = g.SW, t.SW = g.SH, t.PH = g.PW, t.PW = g.PH, t.DH = g.DW, t.DW = g.DH;
+  return t;
+}
+
+// The staged kernel's axis fields for the min over depth (2) or height (3).
+void staged_axes(const Geom &g, int min_dim, StagedParams *sp) {
+  const int64_t HW = (int64_t)g.H * g.W;
+  if (min_dim == 2) {
+    sp->OR = g.OD, sp->OA = g.OH, sp->KR = g.KD, sp->KA = g.KH, sp->IR = g.D;
+    sp->sR = HW, sp->sA = g.W, sp->wR = g.KH * g.KW, sp->wA = g.KW;
+  } else {
+    sp->OR = g.OH, sp->OA = g.OD, sp->KR = g.KH, sp->KA = g.KD, sp->IR = g.H;
+    sp->sR = g.W, sp->sA = HW, sp->wR = g.KW, sp->wA = g.KH * g.KW;
+  }
+}
+
 bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
   // sp's axis fields (OR, OA, KR, KA, IR, sR, sA, wR, wA) are filled by the caller
   if (g.K > kSNcg * kSCO || g.OW > 32 || g.KW != 3) return false;
@@ -580,6 +629,11 @@ bool staged_plan(const Geom &g, const float *x, StagedParams *sp) {
   sp->slot_floats = (uint32_t)slot;
   return true;
 }
+
+// Byte offsets of the transposed copies of x and w in the workspace of the min
+// over width (256-byte sections).
+size_t transpose_x_bytes(const Geom &g) { return ((size_t)g.N * g.C * g.in_spatial() * 4 + 255) / 256 * 256; }
+size_t transpose_w_bytes(const Geom &g) { return ((size_t)g.K * g.C * g.taps() * 4 + 255) / 256 * 256; }
 
 template <int NCG, int NROW, int KWT, bool VEC>
 cudaError_t launch_t(const FusedParams &p0, cudaStream_t stream) {
@@ -636,6 +690,17 @@ bool fused_supported(const Geom &g, int min_dim, const char **why) {
   return true;
 }
 
+size_t fused_transpose_bytes(const Geom &g, int min_dim) {
+  if (min_dim != 4) return 0;
+  // the min over width of (x, w) is the min over height of (x, w) with H and
+  // W exchanged, which the staged kernel runs when its shape limits allow
+  const Geom t = swap_hw(g);
+  StagedParams sp;
+  staged_axes(t, 3, &sp);
+  if (!staged_plan(t, nullptr, &sp)) return 0;
+  return transpose_x_bytes(g) + transpose_w_bytes(g);
+}
+
 bool fused_ffma_preferred(const Geom &g, int min_dim) {
   // Measured on GB300 against the tensor-core fused kernel on [N, C_in, 24,
   // 32, 32] inputs with 3x3x3 kernels and N * C_in held near 384 (FFMA /
@@ -644,21 +709,34 @@ bool fused_ffma_preferred(const Geom &g, int min_dim) {
   // 12; C_out = 32 (four groups, 48 channels run) 0.61 / 0.65 at C_in = 1,
   // 0.66 / 0.49 at C_in = 3.  Min over height (the staged FFMA kernel):
   // C_out = 24 0.28 / 0.35 at C_in = 4, 0.38 / 0.30 at C_in = 8; C_out = 32
-  // 0.58 / 0.52 already at C_in = 1.  Min over width (the generic FFMA
-  // kernel; the tensor-core tiles then step along height, a strided gather):
-  // C_out = 24 0.77 / 0.95 at C_in = 4, 1.45 / 0.92 at C_in = 8; C_out = 32
-  // 0.78 / 0.99 at C_in = 1, 1.09 / 1.07 at C_in = 3.
+  // 0.58 / 0.52 already at C_in = 1.  Min over width (the tensor-core tiles
+  // then step along height, a strided gather): on the staged kernel through
+  // transposed copies, C_out = 24 0.25 / 1.07 at C_in = 3, 0.42 / 0.92 at
+  // C_in = 8, 2.03 / 1.39 at C_in = 12; on the generic kernel (no transposed
+  // plan, e.g. C_out = 32) 0.78 / 0.99 at C_in = 1, 1.09 / 1.07 at C_in = 3.
   const int64_t kred = g.C * g.taps();
   const int ncg = pick_ncg(g.K);
   switch (min_dim) {
     case 2: return (ncg <= 2 && kred <= 256) || kred <= 32;
     case 3: return ncg <= 2 && kred <= 128;
-    default: return (ncg <= 2 && kred <= 128) || kred <= 32;
+    default:
+      if (fused_transpose_bytes(g, 4) > 0) return (ncg <= 2 && kred <= 256) || kred <= 32;
+      return (ncg <= 2 && kred <= 128) || kred <= 32;
   }
 }
 
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
-                                     const Geom &g, int min_dim, cudaStream_t stream) {
+                                     const Geom &g, int min_dim, cudaStream_t stream, float *ws) {
+  if (min_dim == 4 && ws && fused_transpose_bytes(g, 4) > 0) {
+    // min over width: transpose x and w in their last two dims into ws, then
+    // the min over height of the transposed problem on the staged kernel; its
+    // output [N, C_out, OD, OW'] with OW' = OH is exactly y's layout
+    float *xt = ws, *wt = ws + transpose_x_bytes(g) / 4;
+    cudaError_t e = launch_transpose_last2(x, xt, g.N * g.C * g.D, g.H, g.W, stream);
+    if (e == cudaSuccess) e = launch_transpose_last2(w, wt, g.K * g.C * g.KD, g.KH, g.KW, stream);
+    if (e != cudaSuccess) return e;
+    return launch_fused_min_softmax(xt, wt, bias, y, swap_hw(g), 3, stream, nullptr);
+  }
   FusedParams p;
   p.x = x;
   p.w = w;
@@ -688,9 +766,7 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
   p.rows = g.N * (int64_t)p.OA;
   StagedParams sp;
   // the staged kernel keeps W as its column axis: the min over depth or height
-  sp.OR = p.OR, sp.OA = p.OA, sp.KR = p.KR, sp.KA = p.KA;
-  sp.IR = (min_dim == 2) ? g.D : g.H;
-  sp.sR = p.sR, sp.sA = p.sA, sp.wR = p.wR, sp.wA = p.wA;
+  if (min_dim != 4) staged_axes(g, min_dim, &sp);
   if (min_dim != 4 && staged_plan(g, x, &sp)) {
     sp.x = x;
     sp.w = w;

@@ -15,17 +15,18 @@
  *     parameter arrays (in_dims, k_dims, stride, pad, dilation, out_dims) and
  *     the descriptor structs are HOST memory, read during the call only.
  *   - The caller owns every buffer and the library keeps no pointer to one after
- *     the call returns.  y must not overlap x, w or bias.  One kind of call
- *     allocates device memory: conv_fwd_nd, conv_fwd_nd_ex, conv_fwd_nd_grouped
- *     and conv_fwd_nd_host, on a tensor-core layer whose weights exceed shared
- *     memory (conv_workspace_bytes > 0), and conv3d_min_softmax(_ex) on the
- *     tensor-core kernel in the same case, take a stream-ordered block for the
- *     split weights (allocated on `stream` from a memory pool of
- *     the library's, or from the device's default pool while `stream` is being
- *     captured into a graph, and freed on `stream` after the call's last
- *     launch; if the allocation fails, the layer runs in several passes
- *     instead).  conv_fwd_nd_ws, conv_fwd_nd_ws_noalloc and every other call
- *     allocate nothing.  Things held by the library itself: a 16 MiB
+ *     the call returns.  y must not overlap x, w or bias.  Some calls take one
+ *     stream-ordered block of device memory: conv_fwd_nd, conv_fwd_nd_ex,
+ *     conv_fwd_nd_grouped and conv_fwd_nd_host for a tensor-core layer whose
+ *     weights exceed shared memory (conv_workspace_bytes > 0: the split
+ *     weights), and conv3d_min_softmax(_ex) in the same case on its
+ *     tensor-core kernel, or for a min over width on its FFMA kernels
+ *     (transposed copies of x and w).  The block comes from a memory pool of
+ *     the library's (from the device's default pool while `stream` is being
+ *     captured into a graph), is allocated and freed on `stream`; if it
+ *     cannot be had, the call runs without it where it can (reduction passes,
+ *     the generic fused kernel) and returns CONV_ERR_CUDA otherwise.  conv_fwd_nd_ws, conv_fwd_nd_ws_noalloc and every other
+ *     call allocate nothing.  Things held by the library itself: a 16 MiB
  *     file-scope device array (the scratch of conv_fwd_nd_ws_noalloc), which
  *     every device that loads the library holds until the process exits; from
  *     the first allocating call on a device, that memory pool, which keeps up
@@ -319,9 +320,11 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * weights that exceed shared memory stream through a stream-ordered block of
  * the call, as for conv_fwd_nd).  Where both run, the planner takes the FFMA
  * kernels for short reductions over few channels and the tensor-core kernel
- * otherwise; with K = C_in * |kernel| and C_out <= 24: FFMA for K <= 256 (min
- * over depth) or K <= 128 (height, width); with more channels FFMA only for
- * K <= 32 (depth, width).  Shapes neither family runs are CONV_ERR_UNSUPPORTED.
+ * otherwise; with K = C_in * |kernel| and C_out <= 24: FFMA for K <= 256 over
+ * depth, and over width when the FFMA kernels run it as a min over height of
+ * transposed copies of x and w (kernel height 3, output height <= 32), else
+ * for K <= 128; with more channels FFMA only for K <= 32 (depth, width).
+ * Shapes neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);

@@ -489,6 +489,24 @@ def test_fused_narrow_rows_and_many_rows_per_sm():
 
 # ------------------------------------- fused, min over height or width
 
+@pytest.mark.parametrize("C_out,k,shape", [
+    (24, (3, 3, 3), (3, 3, 9, 32, 11)),    # the staged kernel on the transposed problem (KH = 3, OH <= 32)
+    (17, (2, 3, 4), (2, 2, 6, 34, 9)),     # OH = 32 exactly, odd channel count
+    (13, (2, 4, 3), (2, 2, 7, 10, 37)),    # KH = 4: the generic kernel
+    (24, (3, 3, 3), (2, 3, 5, 40, 12)),    # OH = 38 > 32: the generic kernel
+])
+def test_fused_ffma_min_over_width_paths(C_out, k, shape):
+    rng = np.random.default_rng(C_out + shape[3])
+    x = rng.random(shape).astype(np.float32)
+    w = ((rng.random((C_out, shape[1]) + k) - 0.5) * 0.4).astype(np.float32)
+    b = ((rng.random(C_out) - 0.5) * 0.4).astype(np.float32)
+    ref = oracle.conv3d_min_softmax(x, w, b, 4)
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    y = cf.conv3d_min_softmax(xt, wt, bt, 4, algo=FFMA)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, f"fused FFMA min over width C_out={C_out} k={k} {shape}")
+
+
 @pytest.mark.parametrize("min_dim", [3, 4])
 @pytest.mark.parametrize("C_out,k,shape", [(24, (3, 3, 3), (3, 3, 9, 11, 32)), (13, (2, 4, 3), (2, 2, 7, 10, 37)),
                                            (49, (3, 3, 5), (2, 3, 6, 9, 12)), (5, (1, 5, 2), (3, 1, 4, 21, 6))])
