@@ -725,16 +725,36 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
            g, algo == CONV_ALGO_IGEMM_3XTF32 ? "fused igemm_3xtf32" : "fused ffma", false);
   cudaError_t e = cudaSuccess;
   if (algo == CONV_ALGO_IGEMM_3XTF32) {
-    // weights beyond shared memory stream from a stream-ordered block, as in conv_fwd_nd
-    const size_t sb = convfwd::igemm_fused_stream_bytes(g);
+    // The min over width runs as the min over height of x and w transposed in
+    // their last two dims (its tiles then read rows of x, not columns); weights
+    // beyond shared memory stream, as in conv_fwd_nd.  Both live in one
+    // stream-ordered block (transposed copies first).
+    cudaStream_t s = (cudaStream_t)stream;
+    const Geom gt = min_dim == 4 ? convfwd::swap_hw_geom(g) : g;
+    size_t tb = min_dim == 4 ? convfwd::transposed_hw_bytes(g) : 0;
+    size_t sb = convfwd::igemm_fused_stream_bytes(gt);
     float *wsp = nullptr;
-    if (sb > 0) {
-      e = alloc_stream_ws(reinterpret_cast<void **>(&wsp), sb, (cudaStream_t)stream);
-      if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: weight workspace");
+    if (tb + sb > 0 && alloc_stream_ws(reinterpret_cast<void **>(&wsp), tb + sb, s) != cudaSuccess) {
+      (void)cudaGetLastError();
+      wsp = nullptr;
+      // without the transposed copies the min over width reads columns of x directly
+      tb = 0;
+      sb = convfwd::igemm_fused_stream_bytes(g);
+      if (sb > 0) {
+        e = alloc_stream_ws(reinterpret_cast<void **>(&wsp), sb, s);
+        if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: weight workspace");
+      }
     }
-    e = convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, (cudaStream_t)stream, wsp);
+    if (tb > 0) {
+      e = convfwd::transpose_hw(x->data, w->data, wsp, g, s);
+      if (e == cudaSuccess)
+        e = convfwd::launch_igemm_fused_min_softmax(wsp, wsp + convfwd::transposed_x_bytes(g) / 4, bias, yd, gt, 3, s,
+                                                    sb > 0 ? wsp + tb / 4 : nullptr);
+    } else {
+      e = convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, s, sb > 0 ? wsp : nullptr);
+    }
     if (wsp) {
-      const cudaError_t ef = cudaFreeAsync(wsp, (cudaStream_t)stream);
+      const cudaError_t ef = cudaFreeAsync(wsp, s);
       if (e == cudaSuccess) e = ef;
     }
   } else {

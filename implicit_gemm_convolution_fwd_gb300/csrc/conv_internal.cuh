@@ -56,6 +56,13 @@ cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
                                      const Geom &g, int min_dim, cudaStream_t stream, float *ws = nullptr);
 size_t fused_transpose_bytes(const Geom &g, int min_dim);
+// The problem with H and W exchanged, and x and w transposed in their last
+// two dims into ws (x at ws, w at ws + transposed_x_bytes(g) / 4 floats;
+// transposed_hw_bytes(g) bytes in all, 256-byte sections).
+Geom swap_hw_geom(const Geom &g);
+size_t transposed_x_bytes(const Geom &g);
+size_t transposed_hw_bytes(const Geom &g);
+cudaError_t transpose_hw(const float *x, const float *w, float *ws, const Geom &g, cudaStream_t stream);
 // True when launch_fused_min_softmax supports this geometry (channel count,
 // kernel extent along the output's last axis, shared-memory footprint).
 bool fused_supported(const Geom &g, int min_dim, const char **why);

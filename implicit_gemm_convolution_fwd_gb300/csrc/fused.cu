@@ -672,6 +672,16 @@ int pick_ncg(int64_t K) {
 
 }  // namespace
 
+Geom swap_hw_geom(const Geom &g) { return swap_hw(g); }
+size_t transposed_x_bytes(const Geom &g) { return transpose_x_bytes(g); }
+size_t transposed_hw_bytes(const Geom &g) { return transpose_x_bytes(g) + transpose_w_bytes(g); }
+
+cudaError_t transpose_hw(const float *x, const float *w, float *ws, const Geom &g, cudaStream_t stream) {
+  cudaError_t e = launch_transpose_last2(x, ws, g.N * g.C * g.D, g.H, g.W, stream);
+  if (e == cudaSuccess) e = launch_transpose_last2(w, ws + transpose_x_bytes(g) / 4, g.K * g.C * g.KD, g.KH, g.KW, stream);
+  return e;
+}
+
 bool fused_supported(const Geom &g, int min_dim, const char **why) {
   if (g.K > 8 * kCO) {
     *why = "fused path: C_out above 96";
@@ -709,19 +719,18 @@ bool fused_ffma_preferred(const Geom &g, int min_dim) {
   // 12; C_out = 32 (four groups, 48 channels run) 0.61 / 0.65 at C_in = 1,
   // 0.66 / 0.49 at C_in = 3.  Min over height (the staged FFMA kernel):
   // C_out = 24 0.28 / 0.35 at C_in = 4, 0.38 / 0.30 at C_in = 8; C_out = 32
-  // 0.58 / 0.52 already at C_in = 1.  Min over width (the tensor-core tiles
-  // then step along height, a strided gather): on the staged kernel through
-  // transposed copies, C_out = 24 0.25 / 1.07 at C_in = 3, 0.42 / 0.92 at
-  // C_in = 8, 2.03 / 1.39 at C_in = 12; on the generic kernel (no transposed
-  // plan, e.g. C_out = 32) 0.78 / 0.99 at C_in = 1, 1.09 / 1.07 at C_in = 3.
+  // 0.58 / 0.52 already at C_in = 1.  Min over width, both families on
+  // transposed copies (the min over height of the problem with H and W
+  // exchanged): C_out = 24 0.32 / 0.38 at C_in = 4, 0.41 / 0.33 at C_in = 8;
+  // where the staged kernel cannot take the transposed problem the FFMA
+  // family runs the generic kernel, slower than the tensor cores at every
+  // measured point (C_out = 32: 0.78 / 0.56 at C_in = 1).
   const int64_t kred = g.C * g.taps();
   const int ncg = pick_ncg(g.K);
   switch (min_dim) {
     case 2: return (ncg <= 2 && kred <= 256) || kred <= 32;
     case 3: return ncg <= 2 && kred <= 128;
-    default:
-      if (fused_transpose_bytes(g, 4) > 0) return (ncg <= 2 && kred <= 256) || kred <= 32;
-      return (ncg <= 2 && kred <= 128) || kred <= 32;
+    default: return fused_transpose_bytes(g, 4) > 0 && ncg <= 2 && kred <= 128;
   }
 }
 
@@ -731,11 +740,9 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     // min over width: transpose x and w in their last two dims into ws, then
     // the min over height of the transposed problem on the staged kernel; its
     // output [N, C_out, OD, OW'] with OW' = OH is exactly y's layout
-    float *xt = ws, *wt = ws + transpose_x_bytes(g) / 4;
-    cudaError_t e = launch_transpose_last2(x, xt, g.N * g.C * g.D, g.H, g.W, stream);
-    if (e == cudaSuccess) e = launch_transpose_last2(w, wt, g.K * g.C * g.KD, g.KH, g.KW, stream);
+    const cudaError_t e = transpose_hw(x, w, ws, g, stream);
     if (e != cudaSuccess) return e;
-    return launch_fused_min_softmax(xt, wt, bias, y, swap_hw(g), 3, stream, nullptr);
+    return launch_fused_min_softmax(ws, ws + transpose_x_bytes(g) / 4, bias, y, swap_hw(g), 3, stream, nullptr);
   }
   FusedParams p;
   p.x = x;

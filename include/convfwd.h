@@ -321,10 +321,11 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * the call, as for conv_fwd_nd).  Where both run, the planner takes the FFMA
  * kernels for short reductions over few channels and the tensor-core kernel
  * otherwise; with K = C_in * |kernel| and C_out <= 24: FFMA for K <= 256 over
- * depth, and over width when the FFMA kernels run it as a min over height of
- * transposed copies of x and w (kernel height 3, output height <= 32), else
- * for K <= 128; with more channels FFMA only for K <= 32 (depth, width).
- * Shapes neither family runs are CONV_ERR_UNSUPPORTED.
+ * depth and K <= 128 over height, and over width (which both families run as
+ * a min over height of x and w transposed in their last two dims) for
+ * K <= 128 when the FFMA kernels can take the transposed problem (kernel
+ * height 3, output height <= 32); with more channels FFMA only for K <= 32
+ * over depth.  Shapes neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);
