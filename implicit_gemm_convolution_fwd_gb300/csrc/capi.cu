@@ -745,14 +745,28 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
         if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: weight workspace");
       }
     }
+    const float *xk = x->data, *wk = w->data;
+    Geom gk = g;
+    int mk = min_dim;
     if (tb > 0) {
       e = convfwd::transpose_hw(x->data, w->data, wsp, g, s);
-      if (e == cudaSuccess)
-        e = convfwd::launch_igemm_fused_min_softmax(wsp, wsp + convfwd::transposed_x_bytes(g) / 4, bias, yd, gt, 3, s,
-                                                    sb > 0 ? wsp + tb / 4 : nullptr);
-    } else {
-      e = convfwd::launch_igemm_fused_min_softmax(x->data, w->data, bias, yd, g, min_dim, s, sb > 0 ? wsp : nullptr);
+      xk = wsp;
+      wk = wsp + convfwd::transposed_x_bytes(g) / 4;
+      gk = gt;
+      mk = 3;
     }
+    // at most 32 channels per launch: a wider layer runs block by block (min +
+    // bias into y), then one softmax pass over all channels
+    const int64_t plane = (int64_t)g.OD * g.OH * g.OW / (min_dim == 2 ? g.OD : min_dim == 3 ? g.OH : g.OW);
+    const bool blocks = g.K > 32;
+    for (int64_t c0 = 0; c0 < g.K && e == cudaSuccess; c0 += 32) {
+      Geom gb = gk;
+      gb.K = g.K - c0 < 32 ? g.K - c0 : 32;
+      e = convfwd::launch_igemm_fused_min_softmax(xk, wk + c0 * g.C * g.taps(), bias ? bias + c0 : nullptr,
+                                                  yd + c0 * plane, gb, mk, s, sb > 0 ? wsp + tb / 4 : nullptr,
+                                                  blocks, g.K);
+    }
+    if (blocks && e == cudaSuccess) e = convfwd::launch_channel_softmax(yd, g.N, g.K, plane, s);
     if (wsp) {
       const cudaError_t ef = cudaFreeAsync(wsp, s);
       if (e == cudaSuccess) e = ef;

@@ -71,13 +71,19 @@ bool fused_supported(const Geom &g, int min_dim, const char **why);
 bool fused_ffma_preferred(const Geom &g, int min_dim);
 
 // The same fused op on the tensor cores (3xTF32): min over depth, height or
-// width (min_dim 2, 3, 4), C_out <= 32, weights resident in shared memory or
-// streamed from ws (a device workspace of igemm_fused_stream_bytes(g) bytes;
-// 0 = resident).
+// width (min_dim 2, 3, 4), weights resident in shared memory or streamed from
+// ws (a device workspace of igemm_fused_stream_bytes(g) bytes; 0 = resident).
+// One launch takes C_out <= 32; wider layers run as blocks of 32 channels with
+// min_only (min + bias into y, whose images are y_chans channels apart) and
+// then launch_channel_softmax over all of them.
 bool igemm_fused_supported(const Geom &g, int min_dim, const char **why);
 size_t igemm_fused_stream_bytes(const Geom &g);
 cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                           int min_dim, cudaStream_t stream, float *ws = nullptr);
+                                           int min_dim, cudaStream_t stream, float *ws = nullptr,
+                                           bool min_only = false, int64_t y_chans = 0);
+// In place over y [N][C][plane]: y[n, :, p] = softmax over the C channels
+// (maximum subtracted).
+cudaError_t launch_channel_softmax(float *y, int64_t N, int64_t C, int64_t plane, cudaStream_t stream);
 
 // Tensor-core implicit GEMM on 16-bit tensors (bfloat16, or float16 when fp16; bit patterns),
 // fp32 accumulation, output in the input type.

@@ -116,6 +116,7 @@ struct IgemmParams {
   int64_t plane;
   int nB;
   int64_t sR, sA, sB;
+  int fused_min_only;  // a 32-channel block of a wider layer: write min + bias, no softmax
 };
 
 struct Plan {
@@ -527,23 +528,32 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         const int64_t col = tile_of<true>(p, it) / R, img = col / p.hw_tiles;
         const int64_t pp = (col - img * p.hw_tiles) * kTileM + tid;
         if (pp < plane) {
-          float mx = -INFINITY;
+          // y[n, o, pos]; images are y_chans channels apart (all blocks of a wider layer)
+          float *yp = p.y + img * p.y_chans * plane + pp;
+          if (p.fused_min_only) {
+            // one block of a layer wider than 32 channels: the softmax over all
+            // of them runs afterwards as a pass of its own
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            mn[j] += bias_s[j];
-            if (j < K) mx = fmaxf(mx, mn[j]);
+            for (int j = 0; j < 32; ++j)
+              if (j < K) yp[(int64_t)j * plane] = mn[j] + bias_s[j];
+          } else {
+            float mx = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              mn[j] += bias_s[j];
+              if (j < K) mx = fmaxf(mx, mn[j]);
+            }
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              mn[j] = j < K ? expf(mn[j] - mx) : 0.f;
+              sum += mn[j];
+            }
+            const float inv = 1.f / sum;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < K) __stcs(yp + (int64_t)j * plane, mn[j] * inv);
           }
-          float sum = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            mn[j] = j < K ? expf(mn[j] - mx) : 0.f;
-            sum += mn[j];
-          }
-          const float inv = 1.f / sum;
-          float *yp = p.y + img * (int64_t)K * plane + pp;
-#pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < K) __stcs(yp + (int64_t)j * plane, mn[j] * inv);
         }
       }
     }
@@ -1061,20 +1071,20 @@ bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {
     *why = "tensor-core fused path: min_dim must be 2, 3 or 4";
     return false;
   }
-  if (g.K > 32) {
-    *why = "tensor-core fused path: C_out above 32";
-    return false;
-  }
   if (g.cl) {
     *why = "tensor-core fused path: channels-last input";
     return false;
   }
-  if (!make_plan(g, &pl, why)) return false;
+  // layers wider than 32 channels run in blocks of 32 (the epilogue holds one
+  // position's channels in registers), then a channel-softmax pass
+  Geom gb = g;
+  if (gb.K > 32) gb.K = 32;
+  if (!make_plan(gb, &pl, why)) return false;
   if (pl.KC != 16) {
     *why = "tensor-core fused path: no 16-column stages";
     return false;
   }
-  if (pl.npasses != 1 && igemm_stream_bytes_one_group(g) == 0) {
+  if (pl.npasses != 1 && igemm_stream_bytes_one_group(gb) == 0) {
     *why = "tensor-core fused path: the weights neither fit in shared memory nor stream";
     return false;
   }
@@ -1083,16 +1093,19 @@ bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {
 
 size_t igemm_fused_stream_bytes(const Geom &g) {
   Plan pl;
+  Geom gb = g;
+  if (gb.K > 32) gb.K = 32;  // per channel block, reused block after block
   const char *why = "";
-  if (!make_plan(g, &pl, &why) || pl.npasses == 1) return 0;
-  return igemm_stream_bytes_one_group(g);
+  if (!make_plan(gb, &pl, &why) || pl.npasses == 1) return 0;
+  return igemm_stream_bytes_one_group(gb);
 }
 
 cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const float *bias, float *y, const Geom &g,
-                                           int min_dim, cudaStream_t stream, float *ws) {
+                                           int min_dim, cudaStream_t stream, float *ws, bool min_only,
+                                           int64_t y_chans) {
   Plan pl;
   const char *why = "";
-  if (!igemm_fused_supported(g, min_dim, &why) || !make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
+  if (g.K > 32 || !igemm_fused_supported(g, min_dim, &why) || !make_plan(g, &pl, &why)) return cudaErrorInvalidValue;
   const bool streamed = pl.npasses != 1;
   if (streamed && !ws) return cudaErrorInvalidValue;
   int dev = 0;
@@ -1137,7 +1150,8 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.Kfull = (int)kfull;
   p.k_begin = 0;
   p.accumulate = 0;
-  p.y_chans = g.K;
+  p.y_chans = y_chans > 0 ? y_chans : g.K;
+  p.fused_min_only = min_only ? 1 : 0;
   p.Npad = pl.Npad;
   p.KC = pl.KC;
   p.nslots = pl.nslots;

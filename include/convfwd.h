@@ -315,17 +315,20 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  *   [N, C_out, OH, OW] for min_dim 2, [N, C_out, OD, OW] for 3, [N, C_out, OD, OH] for 4.
  * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  Two kernel families: the FFMA
  * kernels (C_out up to 96, a kernel extent along y's last axis up to 7) and a
- * tensor-core kernel (3xTF32 implicit GEMM whose epilogue keeps each
- * position's running minimum over the reduced dim in registers; C_out <= 32;
- * weights that exceed shared memory stream through a stream-ordered block of
- * the call, as for conv_fwd_nd).  Where both run, the planner takes the FFMA
- * kernels for short reductions over few channels and the tensor-core kernel
- * otherwise; with K = C_in * |kernel| and C_out <= 24: FFMA for K <= 256 over
- * depth and K <= 128 over height, and over width (which both families run as
- * a min over height of x and w transposed in their last two dims) for
- * K <= 128 when the FFMA kernels can take the transposed problem (kernel
- * height 3, output height <= 32); with more channels FFMA only for K <= 32
- * over depth.  Shapes neither family runs are CONV_ERR_UNSUPPORTED.
+ * tensor-core kernel (any C_out, kernel extents up to 32; a 3xTF32 implicit
+ * GEMM whose epilogue keeps each
+ * position's running minimum over the reduced dim in registers, 32 channels
+ * per launch: wider layers run block by block, then one channel-softmax pass
+ * over y; weights that exceed shared memory stream through a stream-ordered
+ * block of the call, as for conv_fwd_nd).  The min over width runs, in both
+ * families where they can, as the min over height of x and w transposed in
+ * their last two dims (a stream-ordered block).  Where both families run, the
+ * planner takes the one measured faster for the shape class: the FFMA
+ * kernels for short reductions over few channels (with K = C_in * |kernel|
+ * and C_out <= 24: K <= 256 over depth, K <= 128 over height or width), the
+ * tensor cores for longer reductions and for 32 channels (one block), with
+ * narrower margins for wider layers (see the rule in the library source).
+ * Shapes neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);

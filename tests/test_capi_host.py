@@ -138,18 +138,17 @@ def test_fused_validation_statuses(lib):
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 4, None) == cf.CONV_ERR_SHAPE
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 1, None) == cf.CONV_ERR_ARG
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(y), 5, None) == cf.CONV_ERR_ARG
-    # min over W: the FFMA kernels' column axis is H, so KH is limited to 7, and the tensor-core
-    # kernel takes at most 32 channels: 40 channels with KH = 9 run on neither
-    wtall = T5(0x100000, (ctypes.c_int64 * 5)(40, 3, 3, 9, 3))
-    ytall = T4(0x40000000, (ctypes.c_int64 * 4)(2, 40, 22, 24))
-    assert f(ctypes.byref(x), ctypes.byref(wtall), None, ctypes.byref(ytall), 4, None) == cf.CONV_ERR_UNSUPPORTED
     wbad = T5(0x100000, (ctypes.c_int64 * 5)(24, 4, 3, 3, 3))
     assert f(ctypes.byref(x), ctypes.byref(wbad), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE
     ybad = T4(0x40000000, (ctypes.c_int64 * 4)(2, 24, 30, 29))
     assert f(ctypes.byref(x), ctypes.byref(w), None, ctypes.byref(ybad), 2, None) == cf.CONV_ERR_SHAPE
-    wbig = T5(0x100000, (ctypes.c_int64 * 5)(200, 3, 3, 3, 3))
-    ybig = T4(0x40000000, (ctypes.c_int64 * 4)(2, 200, 30, 30))
-    assert f(ctypes.byref(x), ctypes.byref(wbig), None, ctypes.byref(ybig), 2, None) == cf.CONV_ERR_UNSUPPORTED
+    # 200 channels (beyond the FFMA kernels) with a 40-wide kernel (beyond the tensor-core plan's 32)
+    xwide = T5(0x1000, (ctypes.c_int64 * 5)(2, 3, 24, 32, 64))
+    wbig = T5(0x100000, (ctypes.c_int64 * 5)(200, 3, 3, 3, 40))
+    ybig = T4(0x40000000, (ctypes.c_int64 * 4)(2, 200, 30, 25))
+    assert f(ctypes.byref(xwide), ctypes.byref(wbig), None, ctypes.byref(ybig), 2, None) == cf.CONV_ERR_UNSUPPORTED
+    ybig4 = T4(0x40000000, (ctypes.c_int64 * 4)(2, 200, 22, 30))  # the min over W keeps (D, H)
+    assert f(ctypes.byref(xwide), ctypes.byref(wbig), None, ctypes.byref(ybig4), 4, None) == cf.CONV_ERR_UNSUPPORTED
     xsmall = T5(0x1000, (ctypes.c_int64 * 5)(2, 3, 2, 32, 32))
     assert f(ctypes.byref(xsmall), ctypes.byref(w), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE
 

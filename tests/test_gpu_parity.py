@@ -332,12 +332,25 @@ def test_fused_planner_over_height_and_width(min_dim):
     assert torch.equal(auto, tc)
 
 
-def test_fused_tensor_core_refuses_what_it_cannot_run():
-    x = torch.zeros((1, 3, 5, 9, 9), device="cuda")
-    for min_dim in (2, 3, 4):
-        with pytest.raises(cf.ConvError) as e:
-            cf.conv3d_min_softmax(x, torch.zeros((33, 3, 3, 3, 3), device="cuda"), None, min_dim, algo=TC)
-        assert e.value.status == cf.CONV_ERR_UNSUPPORTED
+@pytest.mark.parametrize("min_dim", [2, 3, 4])
+@pytest.mark.parametrize("shape,C_out,k", [
+    ((2, 3, 6, 11, 37), 40, (3, 3, 3)),     # two channel blocks (32 + 8)
+    ((1, 4, 5, 9, 20), 100, (2, 3, 9)),     # four blocks, kernel extent 9 along W (beyond the FFMA kernels)
+    ((2, 40, 4, 7, 9), 70, (3, 3, 3)),      # blocks with streamed weights (1080 reduction columns)
+])
+def test_fused_tensor_core_wide_layers(shape, C_out, k, min_dim):
+    rng = np.random.default_rng(C_out + shape[1] + min_dim)
+    x = rng.standard_normal(shape).astype(np.float32)
+    w = ((rng.random((C_out, shape[1]) + k) - 0.5) * 2 / np.sqrt(shape[1] * np.prod(k))).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv3d_min_softmax(x, w, b, min_dim)
+    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
+    y = cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=TC)
+    yauto = cf.conv3d_min_softmax(xt, wt, bt, min_dim)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, f"fused tensor cores, {C_out} channels, min_dim={min_dim}")
+    assert_close(yauto.cpu().numpy(), ref, f"fused planner, {C_out} channels, min_dim={min_dim}")
+    assert np.abs(y.sum(dim=1).cpu().numpy() - 1).max() < 1e-5
 
 
 @pytest.mark.parametrize("min_dim", [3, 4])
