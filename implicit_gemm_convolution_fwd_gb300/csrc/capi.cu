@@ -445,12 +445,25 @@ int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias,
   if (algo != CONV_ALGO_AUTO && algo != CONV_ALGO_IGEMM_3XTF32)
     return fail(CONV_ERR_ARG, "conv: unknown algo %s%lld", "", algo);
   if (g.N == 0) return CONV_OK;
-  log_plan("conv_fwd_nd_channels_last", g, "igemm_3xtf32", false);
-  // one launch per group on channel offsets of x, w, bias and y
+  // weights beyond shared memory stream from a stream-ordered block, as in
+  // conv_fwd_nd (one pass instead of one per shared-memory load of weights)
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t sb = convfwd::igemm_stream_bytes_one_group(g);
+  float *wsp = nullptr;
+  if (sb > 0 && alloc_stream_ws(reinterpret_cast<void **>(&wsp), sb, s) != cudaSuccess) {
+    wsp = nullptr;
+    (void)cudaGetLastError();
+  }
+  log_plan("conv_fwd_nd_channels_last", g, "igemm_3xtf32", wsp != nullptr);
+  // one launch per group on channel offsets of x, w, bias and y (the groups reuse wsp in stream order)
   cudaError_t e = cudaSuccess;
   for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
     e = convfwd::launch_igemm_3xtf32(x + grp * g.C, w + grp * g.K * g.C * g.taps(), bias ? bias + grp * g.K : nullptr,
-                                     y + grp * g.K, g, (cudaStream_t)stream);
+                                     y + grp * g.K, g, s, wsp);
+  if (wsp) {
+    const cudaError_t ef = cudaFreeAsync(wsp, s);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) return fail_cuda(e, "conv_fwd_nd_channels_last: kernel launch");
   return CONV_OK;
 }

@@ -17,9 +17,10 @@
  *   - The caller owns every buffer and the library keeps no pointer to one after
  *     the call returns.  y must not overlap x, w or bias.  Some calls take one
  *     stream-ordered block of device memory: conv_fwd_nd, conv_fwd_nd_ex,
- *     conv_fwd_nd_grouped and conv_fwd_nd_host for a tensor-core layer whose
- *     weights exceed shared memory (conv_workspace_bytes > 0: the split
- *     weights), and conv3d_min_softmax(_ex) in the same case on its
+ *     conv_fwd_nd_grouped, conv_fwd_nd_channels_last and conv_fwd_nd_host for
+ *     a tensor-core layer whose weights exceed shared memory
+ *     (conv_workspace_bytes > 0: the split weights), and
+ *     conv3d_min_softmax(_ex) in the same case on its
  *     tensor-core kernel, or for a min over width on its FFMA kernels
  *     (transposed copies of x and w).  The block comes from a memory pool of
  *     the library's (from the device's default pool while `stream` is being

@@ -629,6 +629,9 @@ def to_channels_last(a):
     # in-bounds tests differ, so border positions must test every column on its own
     (3, 1, 3, 40, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), 2),
     (2, 1, 5, 32, (3, 3), (2, 1), (1, 2), (1, 2), 2),
+    # weights beyond shared memory: streamed from a stream-ordered block in one pass
+    (3, 1, 64, 128, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1), 1),
+    (3, 2, 96, 64, (3, 3, 3), (1, 1, 1), (0, 1, 1), (1, 1, 1), 1),
 ])
 def test_channels_last_conv(nd, groups, C_in, C_out, k, s, p, d, N):
     rng = np.random.default_rng(C_in * 13 + C_out + nd)
