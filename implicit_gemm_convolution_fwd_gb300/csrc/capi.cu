@@ -484,12 +484,25 @@ static int conv_fwd_16bit(const uint16_t *x, const uint16_t *w, const uint16_t *
                                            : "conv_fwd_nd_bf16: the tensor-core path cannot run this shape: %s",
                 why);
   if (g.N == 0) return CONV_OK;
-  log_plan(name, g, fp16 ? "igemm_f16" : "igemm_bf16", false);
+  // weights beyond shared memory stream from a stream-ordered block (reused
+  // by every channel block and group in stream order)
+  cudaStream_t s = (cudaStream_t)stream;
+  const size_t sb = convfwd::igemm_bf16_stream_bytes(g);
+  uint16_t *wsp = nullptr;
+  if (sb > 0) {
+    const cudaError_t ea = alloc_stream_ws(reinterpret_cast<void **>(&wsp), sb, s);
+    if (ea != cudaSuccess) return fail_cuda(ea, name);
+  }
+  log_plan(name, g, fp16 ? "igemm_f16" : "igemm_bf16", wsp != nullptr);
   const int64_t xg = g.C * g.in_spatial(), wg = g.K * g.C * g.taps(), yg = g.K * g.out_spatial();
   cudaError_t e = cudaSuccess;
   for (int64_t grp = 0; grp < g.G && e == cudaSuccess; ++grp)
     e = convfwd::launch_igemm_bf16(x + grp * xg, w + grp * wg, bias ? bias + grp * g.K : nullptr, y + grp * yg, g,
-                                   fp16, (cudaStream_t)stream);
+                                   fp16, s, wsp);
+  if (wsp) {
+    const cudaError_t ef = cudaFreeAsync(wsp, s);
+    if (e == cudaSuccess) e = ef;
+  }
   if (e != cudaSuccess) return fail_cuda(e, name);
   return CONV_OK;
 }

@@ -87,9 +87,13 @@ cudaError_t launch_channel_softmax(float *y, int64_t N, int64_t C, int64_t plane
 
 // Tensor-core implicit GEMM on 16-bit tensors (bfloat16, or float16 when fp16; bit patterns),
 // fp32 accumulation, output in the input type.
+// Layers with more than 128 output channels per group run in channel blocks
+// of 128; weights that exceed shared memory stream from ws, a device
+// workspace of igemm_bf16_stream_bytes(g) bytes (0: resident weights).
 bool igemm_bf16_supported(const Geom &g, const char **why);
+size_t igemm_bf16_stream_bytes(const Geom &g);
 cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, const Geom &g,
-                              bool fp16, cudaStream_t stream);
+                              bool fp16, cudaStream_t stream, uint16_t *ws = nullptr);
 
 // Tensor-core implicit GEMM (tcgen05, 3xTF32).  igemm_launches: kernel launches
 // one group takes (channel blocks x reduction passes), 0 when unsupported.

@@ -18,6 +18,7 @@ constexpr int kBfChunk = 32;  // reduction columns per chunk (16 TMEM columns)
 
 struct PlanBf16 {
   int Kred, Kpad, Npad, nchunks, nslots, tap_major;
+  int streamed;  // the weights exceed shared memory: chunk by chunk from a workspace
   size_t smem;
 };
 
@@ -49,11 +50,17 @@ bool make_plan_bf16(const Geom &g, PlanBf16 *pl, const char **why) {
   pl->nslots = (kMaxSlots * pl->Npad + 2 * kMaxSlots * (kBfChunk / 2) <= (int)kTmemCols) ? kMaxSlots : 2;
   pl->nchunks = pl->Kpad / kBfChunk;
   pl->tap_major = (g.C % 4 == 0 && (g.PD > 0 || g.PH > 0 || g.PW > 0)) ? 1 : 0;
-  const size_t smem = (size_t)pl->Npad * pl->Kpad * 2 + (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 +
-                      kNumBars * 8 + 16;
+  const size_t fixed = (size_t)pl->Kpad * 8 + (size_t)pl->Npad * 4 + 16 + kNumBars * 8 + 16;
+  size_t smem = (size_t)pl->Npad * pl->Kpad * 2 + fixed;
+  pl->streamed = 0;
   if (smem > (size_t)kMaxSmem) {
-    *why = "weights do not fit in shared memory";
-    return false;
+    // streamed weights: two B stages per slot of one chunk each (Npad x 32 bf16)
+    smem = (size_t)pl->nslots * 2 * pl->Npad * kBfChunk * 2 + fixed;
+    if (smem > (size_t)kMaxSmem) {
+      *why = "the reduction's column tables exceed shared memory";
+      return false;
+    }
+    pl->streamed = 1;
   }
   pl->smem = smem < (size_t)kMinSmem ? (size_t)kMinSmem : smem;
   return true;
@@ -110,14 +117,42 @@ __device__ __forceinline__ unsigned short float_to_bits16(float f) {
   return HALF ? __half_as_ushort(__float2half_rn(f)) : __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
 
+// Streamed weights, prepared once per call: chunk q of the reduction (32
+// columns) as the tensor cores read it from shared memory, [Npad x 32] 16-bit
+// values in core matrices of 8 rows x 8 (LBO 128 bytes along K, SBO 512 bytes
+// along N); column kg maps to w's memory order as in the resident staging.
+__global__ void split_weights_bf16_kernel(const uint16_t *__restrict__ w, uint16_t *__restrict__ ws, int K, int C,
+                                          int taps, int Kfull, int Npad, int nchunks, int tap_major) {
+  const int64_t per_chunk = (int64_t)Npad * kBfChunk;
+  const int64_t total = per_chunk * nchunks;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+    const int q = (int)(i / per_chunk);
+    const int e = (int)(i - (int64_t)q * per_chunk);
+    const int cm = e >> 6, r = (e >> 3) & 7, col = e & 7;  // core matrix (8 x 8), row, column
+    const int n = (cm / (kBfChunk / 8)) * 8 + r, k = (cm % (kBfChunk / 8)) * 8 + col;
+    const int kg = q * kBfChunk + k;
+    uint16_t v = 0;
+    if (n < K && kg < Kfull) {
+      int kmem = kg;
+      if (tap_major) {
+        const int t = kg / C;
+        kmem = (kg - t * C) * taps + t;
+      }
+      v = __ldg(w + (int64_t)n * Kfull + kmem);
+    }
+    ws[i] = v;
+  }
+}
+
 // HALF = false: bfloat16 tensors; true: float16 tensors (A and B always of one type).
-template <bool HALF>
+// SB: streamed weights (p.wsp: the prepared chunks, p.sb_stage_bytes each).
+template <bool HALF, bool SB>
 __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-  uint8_t *b_s = smem;
+  uint8_t *b_s = smem;  // resident weights, or (SB) one B stage per A stage
   int32_t *toff = reinterpret_cast<int32_t *>(smem + p.b_bytes);  // [Kpad]
   uint32_t *ttap = reinterpret_cast<uint32_t *>(toff + p.Kpad);    // [Kpad]
   float *bias_s = reinterpret_cast<float *>(ttap + p.Kpad);
@@ -128,6 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
   const uint32_t bar_a_empty = ptx::smem_addr(bars + kMaxStages);
   const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kMaxStages);
   const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kMaxStages + kMaxSlots);
+  const uint32_t bar_b_full = ptx::smem_addr(bars + 2 * kMaxStages + 2 * kMaxSlots);  // [stages] (SB)
   const uint32_t bar_drain = ptx::smem_addr(bars + 3 * kMaxStages + 2 * kMaxSlots);  // [slots]
   const int nslots = p.nslots;
 
@@ -141,7 +177,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
   // pair = i % 4): consecutive threads write consecutive words.
   {
     const int kq8 = p.Kpad / 8;
-    const int words = p.Npad * p.Kpad / 2;
+    const int words = SB ? 0 : p.Npad * p.Kpad / 2;  // streamed weights arrive per chunk
     for (int i = tid; i < words; i += kThreads) {
       const int cm = i >> 5, r = (i >> 2) & 7, pr = i & 3;
       const int n = (cm / kq8) * 8 + r, k = (cm % kq8) * 8 + pr * 2;
@@ -188,6 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     for (int s = 0; s < kMaxStages; ++s) {
       ptx::mbar_init(bar_a_full + 8 * s, 128);
       ptx::mbar_init(bar_a_empty + 8 * s, 1);
+      ptx::mbar_init(bar_b_full + 8 * s, 1);
     }
     for (int b = 0; b < kMaxSlots; ++b) {
       ptx::mbar_init(bar_drain + 8 * b, 1);
@@ -221,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         n = m / p.osp;
         pp = m - n * p.osp;
       }
-      uint16_t *yp = p.yh + n * g.G * g.K * p.osp + pp;
+      uint16_t *yp = p.yh + n * p.y_chans * p.osp + pp;  // images y_chans channels apart (all groups and blocks)
       for (int c0 = 0; c0 < p.Npad; c0 += 32) {
         uint32_t v[32];
         ptx::tmem_ld32(tmem + lane_base + b * p.Npad + c0, v);
@@ -252,6 +289,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t my_tiles = cta_tile_count(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;
+    // streamed weights: the group's thread 0 brings chunk q's B into the stage
+    // and remembers its last copy, to wait for it before leaving
+    int sb_last_stage = -1;
+    uint32_t sb_last_parity = 0;
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position(p, tile_of(p, li * nslots + slot), t);
@@ -267,6 +308,15 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         const bool ok = wait_phase(bar_a_empty + 8 * stage, (r & 1) ^ 1, abort_flag, p.wait_limit, kWaitSiteAEmpty);
         if (!__all_sync(0xffffffffu, ok)) return false;
         ptx::tc_fence_after();
+        if (SB && t == 0) {
+          // the stage's MMAs are done: its B half is free too
+          ptx::mbar_arrive_expect_tx(bar_b_full + 8 * stage, p.sb_stage_bytes);
+          ptx::bulk_copy_g2s(ptx::smem_addr(b_s + (size_t)stage * p.sb_stage_bytes),
+                             reinterpret_cast<const uint8_t *>(p.wsp) + (size_t)q * p.sb_stage_bytes, p.sb_stage_bytes,
+                             bar_b_full + 8 * stage);
+          sb_last_stage = stage;
+          sb_last_parity = r & 1;
+        }
         ptx::tmem_st16(tmem + lane_base + a_col0 + (uint32_t)(16 * stage), packed);
         ptx::tmem_wait_st();
         ptx::tc_fence_before();
@@ -309,6 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         }
       }
     }
+    if (SB && sb_last_stage >= 0) {
+      // no bulk copy of ours may still be landing when the CTA exits (bounded)
+      const long long t0 = clock64();
+      while (!ptx::mbar_try_wait(bar_b_full + 8 * sb_last_stage, sb_last_parity) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
   } else if (warp >= kMmaWarp && warp - kMmaWarp < nslots) {
     // ------------------------------------------------------------ MMA issuers
     // the whole warp runs the loop (warp-uniform values); one elected lane issues
@@ -326,7 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
       for (int q = 0; q < p.nchunks; ++q) {
         const uint32_t lg = (uint32_t)li * (uint32_t)p.nchunks + (uint32_t)q;
         const uint32_t s = (uint32_t)(2 * slot + (int)(lg & 1)), r = lg >> 1;
-        if (!__all_sync(0xffffffffu, wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteAFull))) {
+        bool ok = wait_phase(bar_a_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteAFull);
+        if (SB && ok) ok = wait_phase(bar_b_full + 8 * s, r & 1, abort_flag, p.wait_limit, kWaitSiteBFull);
+        if (!__all_sync(0xffffffffu, ok)) {
           aborted = true;
           break;
         }
@@ -336,7 +394,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
 #pragma unroll
           for (int ks = 0; ks < kBfChunk / 16; ++ks) {
             const uint32_t kbyte = (uint32_t)((q * kBfChunk + ks * 16) / 8) * 128u;  // core matrices along K
-            const uint64_t bd = ptx::smem_desc_noswizzle(bsa + kbyte, 128, SBO);
+            // streamed: the stage holds chunk q only, 8-row groups 512 bytes apart
+            const uint64_t bd = SB ? ptx::smem_desc_noswizzle(bsa + s * p.sb_stage_bytes + 256u * ks, 128, 512)
+                                   : ptx::smem_desc_noswizzle(bsa + kbyte, 128, SBO);
             ptx::mma_f16_ts(d_tmem, a + 8u * ks, bd, idesc, (q | ks) != 0);
           }
           ptx::mma_commit(bar_a_empty + 8 * s);

@@ -1191,14 +1191,22 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
 
 bool igemm_bf16_supported(const Geom &g, const char **why) {
   PlanBf16 pl;
-  return make_plan_bf16(g, &pl, why);
+  Geom gb = g;
+  if (gb.K > kMaxNpad) gb.K = kMaxNpad;  // wider layers run in channel blocks of 128
+  return make_plan_bf16(gb, &pl, why);
+}
+
+size_t igemm_bf16_stream_bytes(const Geom &g) {
+  PlanBf16 pl;
+  Geom gb = g;
+  if (gb.K > kMaxNpad) gb.K = kMaxNpad;
+  const char *why = "";
+  if (!make_plan_bf16(gb, &pl, &why) || !pl.streamed) return 0;
+  return (size_t)pl.Npad * pl.Kpad * 2;
 }
 
 cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, const Geom &g,
-                              bool fp16, cudaStream_t stream) {
-  PlanBf16 pl;
-  const char *why = "";
-  if (!make_plan_bf16(g, &pl, &why)) return cudaErrorInvalidValue;
+                              bool fp16, cudaStream_t stream, uint16_t *ws) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -1209,37 +1217,67 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
   }
   bool &attr_set = fp16 ? g_attr_f16_set[dev] : g_attr_bf16_set[dev];
   if (!attr_set) {
-    e = cudaFuncSetAttribute(fp16 ? igemm_bf16_kernel<true> : igemm_bf16_kernel<false>,
+    e = cudaFuncSetAttribute(fp16 ? igemm_bf16_kernel<true, false> : igemm_bf16_kernel<false, false>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fp16 ? igemm_bf16_kernel<true, true> : igemm_bf16_kernel<false, true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  IgemmParams p = {};
-  p.wait_limit = g_wait_limit.load();
-  p.xh = x;
-  p.wh = w;
-  p.bh = bias;
-  p.yh = y;
-  p.g = g;
-  p.osp = (int64_t)g.OD * g.OH * g.OW;
-  p.M_total = g.N * p.osp;
-  p.tiles = (p.M_total + kTileM - 1) / kTileM;
-  p.Kred = pl.Kred;
-  p.Kfull = pl.Kred;
-  p.y_chans = g.G * g.K;
-  p.Kpad = pl.Kpad;
-  p.Npad = pl.Npad;
-  p.KC = kBfChunk;
-  p.nchunks = pl.nchunks;
-  p.nslots = pl.nslots;
-  p.tap_major = pl.tap_major;
-  p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 2);
-  const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-  if (fp16)
-    igemm_bf16_kernel<true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
-  else
-    igemm_bf16_kernel<false><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
-  return cudaGetLastError();
+  const int64_t osp = (int64_t)g.OD * g.OH * g.OW;
+  const int64_t kfull = g.C * (int64_t)g.taps();
+  // output channels in blocks of at most 128 (one accumulator tile), each a
+  // whole persistent launch on views of w, bias and y
+  for (int64_t o0 = 0; o0 < g.K; o0 += kMaxNpad) {
+    Geom gb = g;
+    gb.K = g.K - o0 < kMaxNpad ? g.K - o0 : kMaxNpad;
+    PlanBf16 pl;
+    const char *why = "";
+    if (!make_plan_bf16(gb, &pl, &why)) return cudaErrorInvalidValue;
+    if (pl.streamed && !ws) return cudaErrorInvalidValue;
+    if (pl.streamed) {
+      // the block's weights in chunk order into ws (reused block after block, in stream order)
+      const int64_t total = (int64_t)pl.Npad * kBfChunk * pl.nchunks;
+      const int64_t blocks64 = (total + 255) / 256;
+      split_weights_bf16_kernel<<<(unsigned)(blocks64 < 4096 ? blocks64 : 4096), 256, 0, stream>>>(
+          w + o0 * kfull, ws, (int)gb.K, (int)g.C, g.taps(), (int)kfull, pl.Npad, pl.nchunks, pl.tap_major);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    IgemmParams p = {};
+    p.wait_limit = g_wait_limit.load();
+    p.xh = x;
+    p.wh = w + o0 * kfull;
+    p.bh = bias ? bias + o0 : nullptr;
+    p.yh = y + o0 * osp;
+    p.g = gb;
+    p.osp = osp;
+    p.M_total = g.N * p.osp;
+    p.tiles = (p.M_total + kTileM - 1) / kTileM;
+    p.Kred = pl.Kred;
+    p.Kfull = pl.Kred;
+    p.y_chans = g.G * g.K;
+    p.Kpad = pl.Kpad;
+    p.Npad = pl.Npad;
+    p.KC = kBfChunk;
+    p.nchunks = pl.nchunks;
+    p.nslots = pl.nslots;
+    p.tap_major = pl.tap_major;
+    p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 2);
+    if (pl.streamed) {
+      p.wsp = reinterpret_cast<const float *>(ws);
+      p.sb_stage_bytes = (uint32_t)(pl.Npad * kBfChunk * 2);
+      p.b_bytes = (uint32_t)(pl.nslots * 2) * p.sb_stage_bytes;
+    }
+    const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+    auto kern = fp16 ? (pl.streamed ? igemm_bf16_kernel<true, true> : igemm_bf16_kernel<true, false>)
+                     : (pl.streamed ? igemm_bf16_kernel<false, true> : igemm_bf16_kernel<false, false>);
+    kern<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 void set_wait_limit(long long cycles) { g_wait_limit.store(cycles > 0 ? cycles : kWaitLimitCycles); }

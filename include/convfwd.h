@@ -17,8 +17,9 @@
  *   - The caller owns every buffer and the library keeps no pointer to one after
  *     the call returns.  y must not overlap x, w or bias.  Some calls take one
  *     stream-ordered block of device memory: conv_fwd_nd, conv_fwd_nd_ex,
- *     conv_fwd_nd_grouped, conv_fwd_nd_channels_last and conv_fwd_nd_host for
- *     a tensor-core layer whose weights exceed shared memory
+ *     conv_fwd_nd_grouped, conv_fwd_nd_channels_last, conv_fwd_nd_bf16,
+ *     conv_fwd_nd_f16 and conv_fwd_nd_host for a tensor-core layer whose
+ *     weights exceed shared memory
  *     (conv_workspace_bytes > 0: the split weights), and
  *     conv3d_min_softmax(_ex) in the same case on its
  *     tensor-core kernel, or for a min over width on its FFMA kernels
@@ -180,9 +181,10 @@ CONVFWD_API int conv_fwd_nd_channels_last(const float *x, const float *w, const 
  * kind::f16 MMA per 16 reduction columns, no operand split); the bias is
  * added in fp32 and y is rounded once to bfloat16 (nearest even).  Hence
  * |y - exact| <= 2^-9 |exact| + (fp32 accumulation error) for every element.
- * Runs on the tensor-core family only: C_out/groups <= 128 and the weights
- * of one group (C_out/groups x C_in/groups x prod(k) bf16) within shared
- * memory, else CONV_ERR_UNSUPPORTED.  All pointers 2-byte aligned.
+ * Runs on the tensor-core family only: wider layers than 128 output channels
+ * per group in channel blocks of 128, weights that exceed shared memory
+ * streamed chunk by chunk from a stream-ordered block; kernel extents above 32
+ * are CONV_ERR_UNSUPPORTED.  All pointers 2-byte aligned.
  */
 CONVFWD_API int conv_fwd_nd_bf16(const uint16_t *x, const uint16_t *w, const uint16_t *bias, uint16_t *y, int ndim,
                                  int64_t N, int64_t C_in, int64_t C_out, int64_t groups, const int64_t *in_dims,

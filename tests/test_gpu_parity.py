@@ -681,6 +681,11 @@ def assert_bf16_close(y, ref, S, K, what, mant=8):
     (3, 1, 3, 64, (3, 5, 7), (1, 1, 1), (0, 0, 0), (1, 1, 1)),
     (3, 1, 8, 32, (3, 5, 7), (1, 2, 2), (1, 2, 3), (2, 1, 1)),
     (3, 1, 32, 40, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1)),
+    # beyond one resident launch: channel blocks of 128, streamed weights, both, and groups
+    (3, 1, 8, 200, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1)),
+    (3, 1, 64, 128, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1)),
+    (3, 1, 48, 160, (3, 3, 3), (1, 1, 1), (0, 1, 1), (1, 1, 1)),
+    (3, 2, 128, 256, (3, 3, 3), (1, 1, 1), (1, 1, 1), (1, 1, 1)),
 ])
 def test_bf16_conv(nd, groups, C_in, C_out, k, s, p, d):
     rng = np.random.default_rng(C_in + C_out * 3 + nd)
