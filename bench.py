@@ -384,23 +384,23 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.833920e6 + 824.226048e6, "batch": 16,
-        "sha256": "aa55ca073c966b0f5e4f1a8a82ee4955e0ce8c280c6d091d7494764be4e64ad0"},
-    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.296384e6 + 307.515392e6, "batch": 4,
-        "sha256": "aa55ca073c966b0f5e4f1a8a82ee4955e0ce8c280c6d091d7494764be4e64ad0"},
-    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492288e6 + 0.096768e6, "batch": 8,
-        "sha256": "aa55ca073c966b0f5e4f1a8a82ee4955e0ce8c280c6d091d7494764be4e64ad0"},
-    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.432832e6 + 66.749952e6, "batch": 8,
-        "sha256": "aa55ca073c966b0f5e4f1a8a82ee4955e0ce8c280c6d091d7494764be4e64ad0"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.406592e6 + 7.719680e6, "batch": 4,
-        "sha256": "aa55ca073c966b0f5e4f1a8a82ee4955e0ce8c280c6d091d7494764be4e64ad0"},
-    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.839104e6 + 0.006656e6, "batch": 128,
-        "sha256": "aa55ca073c966b0f5e4f1a8a82ee4955e0ce8c280c6d091d7494764be4e64ad0"},
-    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.300992e6 + 385.427712e6, "batch": 16,
-        "sha256": "ff3429dda88086f212bb34dcf1300b750845b90b04201fa36891acc214db6936"},
-    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.817344e6 + 0.001024e6, "batch": 128,
-        "sha256": "fbf69429d02cf5dd77ef9f988d5467b9670468fb4599ba89f8a971c594977726"},
-    ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051712e6, "batch": 2,
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.505984e6 + 824.212480e6, "batch": 16,
+        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.330176e6 + 307.265536e6, "batch": 4,
+        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492288e6 + 0.042240e6, "batch": 8,
+        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.432064e6 + 66.768896e6, "batch": 8,
+        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.406592e6 + 7.730944e6, "batch": 4,
+        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.846528e6 + 0.006144e6, "batch": 128,
+        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.303040e6 + 385.665536e6, "batch": 16,
+        "sha256": "e40ab8339f62ac16a7b63da4c60bb211d1927969a0ee55acfc41e2765ade8d8f"},
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.816832e6 + 0.000768e6, "batch": 128,
+        "sha256": "7e63a72762ddc040b9b21fe8069bf746346fd3113a6c47088e4a8fab33c61616"},
+    ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051968e6, "batch": 2,
         "sha256": "ef79ff89c6a99a86c33cde2383bd3a0d8edd97a3441d69c6d46b99b4389d2019"},
 }
 
