@@ -3,7 +3,9 @@
 Argument marshalling only: every step of the convolution runs in the CUDA
 library ``libconvfwd.so`` (built in-tree by ``build_lib.py``).  PyTorch is
 used for device memory and streams.  There is no CPU fallback: if the library
-is missing or a call fails, these functions raise.
+is missing or a call fails, these functions raise.  With ``CONVFWD_DEBUG=1``
+in the environment the debug build ``libconvfwd_debug.so`` is loaded instead
+(plan assertions, device bounds checks; see ``device_status``).
 """
 from __future__ import annotations
 
@@ -12,8 +14,15 @@ import os
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libconvfwd.so")
+DEBUG_LIB_PATH = os.path.join(HERE, "libconvfwd_debug.so")
 
-CONV_OK, CONV_ERR_NULL, CONV_ERR_ARG, CONV_ERR_SHAPE, CONV_ERR_UNSUPPORTED, CONV_ERR_CUDA = range(6)
+CONV_OK, CONV_ERR_NULL, CONV_ERR_ARG, CONV_ERR_SHAPE, CONV_ERR_UNSUPPORTED, CONV_ERR_CUDA, CONV_ERR_INTERNAL = range(7)
+CONV_BUILD_DEBUG = 1
+# device status bits (conv_device_status)
+STATUS_WATCHDOG = 1 << 0
+STATUS_BOUNDS_X, STATUS_BOUNDS_W, STATUS_BOUNDS_Y, STATUS_BOUNDS_WS, STATUS_BOUNDS_SHARED = (1 << 1, 1 << 2, 1 << 3,
+                                                                                          1 << 4, 1 << 5)
+STATUS_BOUNDS_ANY = STATUS_BOUNDS_X | STATUS_BOUNDS_W | STATUS_BOUNDS_Y | STATUS_BOUNDS_WS | STATUS_BOUNDS_SHARED
 CONV_ALGO_AUTO, CONV_ALGO_DIRECT_FFMA, CONV_ALGO_IGEMM_3XTF32 = 0, 1, 2
 ALGO_NAMES = {CONV_ALGO_AUTO: "auto", CONV_ALGO_DIRECT_FFMA: "direct_ffma", CONV_ALGO_IGEMM_3XTF32: "igemm_3xtf32"}
 
@@ -25,7 +34,8 @@ EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_group
             "conv_algo_supported",
             "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv_peak_mma", "conv_peak_ffma",
             "conv_debug_set_wait_limit",
-            "conv_status_string", "conv_last_error", "conv_device_status")
+            "conv_status_string", "conv_last_error", "conv_device_status",
+            "conv_build_flags", "conv_debug_first_bad_index", "conv_debug_shrink_bounds")
 
 
 class ConvError(RuntimeError):
@@ -50,12 +60,19 @@ class PeakResult(ctypes.Structure):
 _lib = None
 
 
+def debug_requested() -> bool:
+    """True when CONVFWD_DEBUG asks for the debug build."""
+    v = os.environ.get("CONVFWD_DEBUG", "")
+    return bool(v) and v != "0"
+
+
 def load(path: str | None = None):
-    """Load (once) and return the ctypes handle of libconvfwd.so; raises if absent."""
+    """Load (once) and return the ctypes handle of libconvfwd.so (libconvfwd_debug.so when CONVFWD_DEBUG=1);
+    raises if absent."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    path = path or (DEBUG_LIB_PATH if debug_requested() else LIB_PATH)
     if not os.path.exists(path):
         raise RuntimeError(f"CUDA library not built: {path} is missing (run build_lib.build())")
     lib = ctypes.CDLL(path)
@@ -92,10 +109,13 @@ def load(path: str | None = None):
     lib.conv_last_error.restype = ctypes.c_char_p
     lib.conv_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint)]
     lib.conv_debug_set_wait_limit.argtypes = [ctypes.c_longlong]
+    lib.conv_build_flags.argtypes = []
+    lib.conv_debug_first_bad_index.argtypes = [ctypes.POINTER(ctypes.c_longlong)]
+    lib.conv_debug_shrink_bounds.argtypes = [ctypes.c_longlong]
     for f in ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
               "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv_peak_mma", "conv_peak_ffma",
-            "conv_debug_set_wait_limit",
-              "conv_device_status"):
+              "conv_debug_set_wait_limit", "conv_device_status", "conv_build_flags",
+              "conv_debug_first_bad_index", "conv_debug_shrink_bounds"):
         getattr(lib, f).restype = i32
     _lib = lib
     return lib
@@ -465,7 +485,25 @@ def set_wait_limit(cycles: int = 0):
 
 
 def device_status() -> int:
-    """Synchronise and read/clear the device-side watchdog word (0 = no kernel gave up a wait)."""
+    """Synchronise and read/clear the device-side status word (0 = no kernel gave up a wait and, in the debug
+    build, no index fell outside its tensor)."""
     v = ctypes.c_uint(0)
     _check(load().conv_device_status(ctypes.byref(v)))
     return v.value
+
+
+def is_debug_build() -> bool:
+    """True when the loaded library is the debug build (plan assertions, device bounds checks)."""
+    return bool(load().conv_build_flags() & CONV_BUILD_DEBUG)
+
+
+def debug_first_bad_index() -> int:
+    """Debug build: the first out-of-range element index the last device_status() call found (-1: none)."""
+    v = ctypes.c_longlong(-1)
+    _check(load().conv_debug_first_bad_index(ctypes.byref(v)))
+    return v.value
+
+
+def debug_shrink_bounds(elems: int = 0):
+    """Debug-build test hook: the device checks treat the last `elems` elements of x as out of range (0 resets)."""
+    _check(load().conv_debug_shrink_bounds(int(elems)))

@@ -5,12 +5,15 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
+#include <vector>
 
 #include <cuda_runtime.h>
 
 #include "../../include/convfwd.h"
 #include "conv_internal.cuh"
+#include "debug_check.cuh"
 
 using convfwd::Geom;
 
@@ -24,9 +27,27 @@ int fail(int status, const char *fmt, const char *detail = nullptr, long long a 
 }
 
 int fail_cuda(cudaError_t e, const char *where) {
+  const char *plan = nullptr;
+  if (convfwd::take_plan_failure(&plan)) {
+    // a launcher's plan assertion (debug build) rather than a CUDA error
+    snprintf(g_last_error, sizeof(g_last_error), "%s: plan assertion failed: %s", where, plan);
+    return CONV_ERR_INTERNAL;
+  }
   snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", where, cudaGetErrorName(e), cudaGetErrorString(e));
   return CONV_ERR_CUDA;
 }
+
+// Debug build: the translation units' device debug words (registered at
+// load time), the test hook's shrink of the checked input extent, and the
+// first out-of-range index that conv_device_status last collected.
+std::vector<convfwd::DebugReader> &debug_readers() {
+  static std::vector<convfwd::DebugReader> r;
+  return r;
+}
+std::atomic<long long> g_debug_x_shrink{0};
+std::atomic<long long> g_debug_first_bad{-1};
+thread_local char g_plan_failure[384] = "";
+thread_local bool g_plan_failed = false;
 
 // CONVFWD_LOG=1 in the environment: one line per launching call on stderr
 // with the problem and the plan (kernel family, tiles, reduction padding,
@@ -179,9 +200,29 @@ int validate_conv(const float *x, const float *w, const float *bias, const float
 // path.
 // can_stream: the call can stream weights that exceed shared memory (it has
 // or may allocate a workspace), so such a layer runs in one pass.
+// CONVFWD_FORCE_ALGO=direct_ffma | igemm_3xtf32 in the environment (read once
+// per process): the family that fp32 calls with CONV_ALGO_AUTO (the plain and
+// fused convolutions, and conv_select_algo) take wherever it can run the
+// problem; elsewhere the planner decides.  Any other value is ignored, with
+// one line on stderr.
+int forced_algo() {
+  static const int f = [] {
+    const char *e = getenv("CONVFWD_FORCE_ALGO");
+    if (!e || !*e) return -1;
+    if (strcmp(e, "direct_ffma") == 0) return (int)CONV_ALGO_DIRECT_FFMA;
+    if (strcmp(e, "igemm_3xtf32") == 0) return (int)CONV_ALGO_IGEMM_3XTF32;
+    fprintf(stderr, "convfwd: CONVFWD_FORCE_ALGO=%s ignored (direct_ffma or igemm_3xtf32)\n", e);
+    return -1;
+  }();
+  return f;
+}
+
 int choose_algo(const Geom &g, bool can_stream) {
-  const int64_t red = g.C * (int64_t)g.taps();
   const char *why = nullptr;
+  const int forced = forced_algo();
+  if (forced == CONV_ALGO_DIRECT_FFMA && convfwd::direct_supported(g, &why)) return forced;
+  if (forced == CONV_ALGO_IGEMM_3XTF32 && convfwd::igemm_supported(g, &why)) return forced;
+  const int64_t red = g.C * (int64_t)g.taps();
   if (red < 64 || g.K < 16 || !convfwd::igemm_supported(g, &why)) return CONV_ALGO_DIRECT_FFMA;
   if (can_stream && convfwd::igemm_stream_bytes_one_group(g) > 0) return CONV_ALGO_IGEMM_3XTF32;
   return convfwd::igemm_launches(g) <= 6 ? CONV_ALGO_IGEMM_3XTF32 : CONV_ALGO_DIRECT_FFMA;
@@ -287,6 +328,24 @@ int64_t host_chunk(int64_t N, int64_t chunk) { return (chunk <= 0 || chunk > N) 
 
 }  // namespace
 
+void convfwd::register_debug_reader(DebugReader r) { debug_readers().push_back(r); }
+
+cudaError_t convfwd::plan_check_failed(const char *cond, const char *file, int line) {
+  const char *base = strrchr(file, '/');
+  snprintf(g_plan_failure, sizeof(g_plan_failure), "%s (%s:%d)", cond, base ? base + 1 : file, line);
+  g_plan_failed = true;
+  return cudaErrorInvalidConfiguration;
+}
+
+bool convfwd::take_plan_failure(const char **text) {
+  if (!g_plan_failed) return false;
+  g_plan_failed = false;
+  *text = g_plan_failure;
+  return true;
+}
+
+long long convfwd::debug_x_shrink() { return g_debug_x_shrink.load(); }
+
 int convfwd::report_error(int status, const char *fmt, ...) {
   va_list ap;
   va_start(ap, fmt);
@@ -305,6 +364,7 @@ const char *conv_status_string(int status) {
     case CONV_ERR_SHAPE: return "CONV_ERR_SHAPE: non-positive output size or inconsistent shapes";
     case CONV_ERR_UNSUPPORTED: return "CONV_ERR_UNSUPPORTED: valid request not implemented by this library";
     case CONV_ERR_CUDA: return "CONV_ERR_CUDA: CUDA runtime error";
+    case CONV_ERR_INTERNAL: return "CONV_ERR_INTERNAL: a plan assertion of the debug build failed";
     default: return "unknown conv status";
   }
 }
@@ -736,8 +796,14 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
   // page's C_in = 3, C_out = 24 shape among them), where the tensor-core
   // kernel's im2col gather costs more than the FFMAs; the tensor-core kernel
   // for longer reductions or more channels; whichever runs otherwise
-  if (algo == CONV_ALGO_AUTO)
-    algo = tc_ok && !(ffma_ok && convfwd::fused_ffma_preferred(g, min_dim)) ? CONV_ALGO_IGEMM_3XTF32 : CONV_ALGO_DIRECT_FFMA;
+  if (algo == CONV_ALGO_AUTO) {
+    const int forced = forced_algo();
+    if ((forced == CONV_ALGO_DIRECT_FFMA && ffma_ok) || (forced == CONV_ALGO_IGEMM_3XTF32 && tc_ok))
+      algo = forced;
+    else
+      algo = tc_ok && !(ffma_ok && convfwd::fused_ffma_preferred(g, min_dim)) ? CONV_ALGO_IGEMM_3XTF32
+                                                                              : CONV_ALGO_DIRECT_FFMA;
+  }
   if (algo == CONV_ALGO_DIRECT_FFMA) {
     if (!ffma_ok) return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
   } else if (algo == CONV_ALGO_IGEMM_3XTF32) {
@@ -828,7 +894,49 @@ int conv_device_status(unsigned int *flags) {
   if (!flags) return fail(CONV_ERR_NULL, "conv_device_status: flags is NULL%s");
   cudaError_t e = convfwd::read_and_clear_device_status(flags);
   if (e != cudaSuccess) return fail_cuda(e, "conv_device_status");
+  long long first = -1;
+  for (convfwd::DebugReader r : debug_readers()) {
+    unsigned b = 0;
+    long long f = -1;
+    e = r(&b, &f);
+    if (e != cudaSuccess) return fail_cuda(e, "conv_device_status: debug words");
+    *flags |= b;
+    if (first < 0 && f >= 0) first = f;
+  }
+  if (!debug_readers().empty()) g_debug_first_bad.store(first);
   return CONV_OK;
+}
+
+int conv_build_flags(void) {
+#ifdef CONVFWD_DEBUG
+  return CONV_BUILD_DEBUG;
+#else
+  return 0;
+#endif
+}
+
+int conv_debug_shrink_bounds(long long elems) {
+  g_last_error[0] = 0;
+#ifdef CONVFWD_DEBUG
+  if (elems < 0) return fail(CONV_ERR_ARG, "conv_debug_shrink_bounds: elems = %s%lld is negative", nullptr, elems);
+  g_debug_x_shrink.store(elems);
+  return CONV_OK;
+#else
+  (void)elems;
+  return fail(CONV_ERR_UNSUPPORTED, "conv_debug_shrink_bounds: this library was built without CONVFWD_DEBUG%s");
+#endif
+}
+
+int conv_debug_first_bad_index(long long *index) {
+  g_last_error[0] = 0;
+  if (!index) return fail(CONV_ERR_NULL, "conv_debug_first_bad_index: index is NULL%s");
+#ifdef CONVFWD_DEBUG
+  *index = g_debug_first_bad.load();
+  return CONV_OK;
+#else
+  *index = -1;
+  return fail(CONV_ERR_UNSUPPORTED, "conv_debug_first_bad_index: this library was built without CONVFWD_DEBUG%s");
+#endif
 }
 
 }  // extern "C"

@@ -16,6 +16,7 @@
 #include <stdint.h>
 
 #include "conv_internal.cuh"
+#include "debug_check.cuh"
 
 namespace convfwd {
 namespace {
@@ -35,6 +36,7 @@ struct DirectParams {
   int owg;        // ceil(OW / R)
   int cchunk;     // input channels per weight chunk
   int kblocks;    // channel blocks of kCO per group: ceil(K / kCO)
+  int64_t x_elems, w_elems, y_elems;  // extents the debug build's device checks use
 };
 
 __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParams p) {
@@ -73,7 +75,8 @@ __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParam
       const int o = i % kCO;
       const int ct = i / kCO;  // cc*taps + tap
       const int64_t og = o0 + o;
-      ws[i] = og < g.K ? p.w[((ob + og) * g.C + c0) * taps + ct] : 0.f;
+      const int64_t wi = ((ob + og) * g.C + c0) * taps + ct;
+      ws[i] = (og < g.K && CONV_DBG_OK(wi, p.w_elems, kStatusBoundsW)) ? p.w[wi] : 0.f;
     }
     __syncthreads();
     if (!active) continue;
@@ -92,7 +95,9 @@ __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParam
 #pragma unroll
             for (int r = 0; r < kR; ++r) {
               const int iw = (ow0 + r) * g.SW + kw * g.DW - g.PW;
-              xv[r] = ((unsigned)iw < (unsigned)g.W) ? __ldg(row + iw) : 0.f;
+              xv[r] = ((unsigned)iw < (unsigned)g.W && CONV_DBG_OK(row + iw - p.x, p.x_elems, kStatusBoundsX))
+                          ? __ldg(row + iw)
+                          : 0.f;
             }
             const float4 wa = *reinterpret_cast<const float4 *>(wt + kw * kCO);
             const float4 wb = *reinterpret_cast<const float4 *>(wt + kw * kCO + 4);
@@ -116,7 +121,7 @@ __global__ void __launch_bounds__(kThreads) direct_ffma_kernel(const DirectParam
     float *yo = p.y + n * g.y_batch_stride() + (ob + og) * osp + ((int64_t)od * g.OH + oh) * g.OW;
 #pragma unroll
     for (int r = 0; r < kR; ++r)
-      if (ow0 + r < g.OW) yo[ow0 + r] = acc[o][r] + b;
+      if (ow0 + r < g.OW && CONV_DBG_OK(yo + ow0 + r - p.y, p.y_elems, kStatusBoundsY)) yo[ow0 + r] = acc[o][r] + b;
   }
 }
 
@@ -158,11 +163,12 @@ __global__ void __launch_bounds__(kThreads) depthwise_kernel(const DirectParams 
       const float *row = xc + (int64_t)id * HW + (int64_t)ih * g.W;
       const float *wt = wo + (kd * g.KH + kh) * g.KW;
       for (int kw = 0; kw < g.KW; ++kw) {
-        const float wv = __ldg(wt + kw);
+        const float wv = CONV_DBG_OK(wt + kw - p.w, p.w_elems, kStatusBoundsW) ? __ldg(wt + kw) : 0.f;
 #pragma unroll
         for (int r = 0; r < kR; ++r) {
           const int iw = (ow0 + r) * g.SW + kw * g.DW - g.PW;
-          if ((unsigned)iw < (unsigned)g.W) acc[r] = fmaf(wv, __ldg(row + iw), acc[r]);
+          if ((unsigned)iw < (unsigned)g.W && CONV_DBG_OK(row + iw - p.x, p.x_elems, kStatusBoundsX))
+            acc[r] = fmaf(wv, __ldg(row + iw), acc[r]);
         }
       }
     }
@@ -170,7 +176,7 @@ __global__ void __launch_bounds__(kThreads) depthwise_kernel(const DirectParams 
   float *yo = p.y + n * g.y_batch_stride() + oc * g.out_spatial() + ((int64_t)od * g.OH + oh) * g.OW;
 #pragma unroll
   for (int r = 0; r < kR; ++r)
-    if (ow0 + r < g.OW) yo[ow0 + r] = acc[r] + b;
+    if (ow0 + r < g.OW && CONV_DBG_OK(yo + ow0 + r - p.y, p.y_elems, kStatusBoundsY)) yo[ow0 + r] = acc[r] + b;
 }
 
 // Depthwise-style groups with stride 1 and dilation 1 (the common case): a
@@ -213,10 +219,12 @@ __global__ void __launch_bounds__(kDwThreads) depthwise_tiled_kernel(const Direc
     const int iw = threadIdx.x & 63;
     if (iw < IW) {
       const int w = w0 + iw;
-      xs[r * IW + iw] = (row_in && (unsigned)w < (unsigned)g.W) ? __ldg(src + w) : 0.f;
+      const bool in = row_in && (unsigned)w < (unsigned)g.W && CONV_DBG_OK(src + w - p.x, p.x_elems, kStatusBoundsX);
+      if (CONV_DBG_OK(r * IW + iw, kDwTile, kStatusBoundsShared)) xs[r * IW + iw] = in ? __ldg(src + w) : 0.f;
     }
   }
-  for (int i = threadIdx.x; i < taps; i += kDwThreads) ws[i] = __ldg(p.w + oc * taps + i);
+  for (int i = threadIdx.x; i < taps; i += kDwThreads)
+    ws[i] = CONV_DBG_OK(oc * taps + i, p.w_elems, kStatusBoundsW) ? __ldg(p.w + oc * taps + i) : 0.f;
   __syncthreads();
   const int t = threadIdx.x;
   const int lw = (t % (kDwTW / kR)) * kR, lh = (t / (kDwTW / kR)) % kDwTH, ld = t / ((kDwTW / kR) * kDwTH);
@@ -245,7 +253,7 @@ __global__ void __launch_bounds__(kDwThreads) depthwise_tiled_kernel(const Direc
   float *yo = p.y + n * g.y_batch_stride() + oc * g.out_spatial() + ((int64_t)od * g.OH + oh) * g.OW;
 #pragma unroll
   for (int r = 0; r < kR; ++r)
-    if (ow0 + r < g.OW) yo[ow0 + r] = acc[r] + b;
+    if (ow0 + r < g.OW && CONV_DBG_OK(yo + ow0 + r - p.y, p.y_elems, kStatusBoundsY)) yo[ow0 + r] = acc[r] + b;
 }
 
 }  // namespace
@@ -284,12 +292,18 @@ cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias
   p.y = y;
   p.g = g;
   p.owg = (g.OW + kR - 1) / kR;
+  // the kernels index whole tensors (all groups) from these pointers
+  p.x_elems = g.N * g.x_batch_stride() - debug_x_shrink();
+  p.w_elems = g.G * g.K * g.C * g.taps();
+  p.y_elems = g.N * g.y_batch_stride();
+  CONV_PLAN_CHECK(!g.cl && (int64_t)g.taps() * kCO <= kSmemFloats);
   const bool unit = g.SD == 1 && g.SH == 1 && g.SW == 1 && g.DD == 1 && g.DH == 1 && g.DW == 1;
   // the tiled kernel when a tile row is mostly used (output width >= 24)
   if (g.C == 1 && g.K < kCO && unit && g.KD <= kDwMaxK && g.KH <= kDwMaxK && g.KW <= kDwMaxK && g.OW >= 24) {
     const int td = (g.OD + kDwTD - 1) / kDwTD, th = (g.OH + kDwTH - 1) / kDwTH, tw = (g.OW + kDwTW - 1) / kDwTW;
     const int64_t blocks = g.N * g.G * g.K * (int64_t)td * th * tw;
     if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
+    CONV_PLAN_CHECK((kDwTD + g.KD - 1) * (kDwTH + g.KH - 1) * (kDwTW + g.KW - 1) <= kDwTile && g.taps() <= 343);
     depthwise_tiled_kernel<<<(unsigned)blocks, kDwThreads, 0, stream>>>(p, td, th, tw);
     return cudaGetLastError();
   }
@@ -308,6 +322,7 @@ cudaError_t launch_direct_ffma(const float *x, const float *w, const float *bias
   p.kblocks = (int)((g.K + kCO - 1) / kCO);
   const int64_t gy = g.G * p.kblocks;
   if (gx > 0x7fffffff || gy > 65535) return cudaErrorInvalidConfiguration;
+  CONV_PLAN_CHECK(p.cchunk >= 1 && (int64_t)p.cchunk * taps * kCO <= kSmemFloats);
   dim3 grid((unsigned)gx, (unsigned)gy);
   direct_ffma_kernel<<<grid, kThreads, 0, stream>>>(p);
   return cudaGetLastError();

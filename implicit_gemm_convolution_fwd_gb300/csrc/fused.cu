@@ -25,6 +25,7 @@
 #include <stdint.h>
 
 #include "conv_internal.cuh"
+#include "debug_check.cuh"
 
 namespace convfwd {
 namespace {
@@ -58,6 +59,7 @@ struct FusedParams {
   int64_t sR, sA;  // input strides (elements) along R and A
   int sB;          // input stride along B (1, or W when B is H)
   int wR, wA, wB;  // weight offsets (within one input channel's taps) per step along R, A, B
+  int64_t x_elems, w_elems, y_elems;  // extents the debug build's device checks use
 };
 
 // NCG channel groups per warp, NROW rows per warp, KWT = compile-time kernel
@@ -85,7 +87,8 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
       const int c = ct / taps, t = ct - c * taps;
       const int kr = t / (p.KA * KW), rem = t - kr * p.KA * KW;
       const int ka = rem / KW, kb = rem - ka * KW;
-      ws[i] = o < g.K ? p.w[(int64_t)o * g.C * taps + c * taps + kr * p.wR + ka * p.wA + kb * p.wB] : 0.f;
+      const int64_t wi = (int64_t)o * g.C * taps + c * taps + kr * p.wR + ka * p.wA + kb * p.wB;
+      ws[i] = (o < g.K && CONV_DBG_OK(wi, p.w_elems, kStatusBoundsW)) ? p.w[wi] : 0.f;
     }
   }
   __syncwarp();
@@ -129,13 +132,14 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
           if (VEC) {
             // unit column stride, IB % 4 == 0 and ob0 % 4 == 0: a 4-wide group
             // is either fully inside the row or fully past its end
-            if (ob0 < p.IB) {
+            if (ob0 < p.IB && CONV_DBG_OK(xr - p.x, p.x_elems, kStatusBoundsX) &&
+                CONV_DBG_OK(xr + 3 - p.x, p.x_elems, kStatusBoundsX)) {
               const float4 a = __ldg(reinterpret_cast<const float4 *>(xr));
               xv[0] = a.x, xv[1] = a.y, xv[2] = a.z, xv[3] = a.w;
             } else {
               xv[0] = 0.f, xv[1] = 0.f, xv[2] = 0.f, xv[3] = 0.f;
             }
-            if (ob0 + 4 < p.IB) {
+            if (ob0 + 4 < p.IB && CONV_DBG_OK(xr + 5 - p.x, p.x_elems, kStatusBoundsX)) {
               const float2 b = __ldg(reinterpret_cast<const float2 *>(xr + 4));
               xv[4] = b.x, xv[5] = b.y;
             } else {
@@ -144,7 +148,10 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
           } else {
 #pragma unroll
             for (int j = 0; j < XW; ++j)
-              xv[j] = (j < kR + KW - 1 && ob0 + j < p.IB) ? __ldg(xr + (int64_t)j * p.sB) : 0.f;
+              xv[j] = (j < kR + KW - 1 && ob0 + j < p.IB &&
+                       CONV_DBG_OK(xr + (int64_t)j * p.sB - p.x, p.x_elems, kStatusBoundsX))
+                          ? __ldg(xr + (int64_t)j * p.sB)
+                          : 0.f;
           }
           const float *wt = wrow + ka * KW * NCH;
 #pragma unroll
@@ -196,7 +203,8 @@ __global__ void __launch_bounds__(32, 14) fused_min_softmax_kernel(const FusedPa
 #pragma unroll
       for (int o = 0; o < kCO; ++o) {
         const int oc = cg * kCO + o;
-        if (oc < g.K) yo[(int64_t)oc * OAB] = v[o] / s;
+        if (oc < g.K && CONV_DBG_OK(yo + (int64_t)oc * OAB - p.y, p.y_elems, kStatusBoundsY))
+          yo[(int64_t)oc * OAB] = v[o] / s;
       }
     }
   }
@@ -244,6 +252,7 @@ struct StagedParams {
   int vec;               // 16-byte copies are legal
   uint32_t w_floats;     // weight region size (floats, multiple of 4)
   uint32_t slot_floats;  // one plane: C * srows_max * WP
+  int64_t x_elems, w_elems, y_elems;  // extents the debug build's device checks use
 };
 
 // Packed fp32 pairs (two adjacent output channels) for fma.rn.f32x2.
@@ -317,7 +326,8 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       if (o < kSCO && oc < g.K) {
         const int c = row / (KD * KH), rem2 = row - c * KD * KH;
         const int kr = rem2 / KH, ka = rem2 - kr * KH;
-        v = p.w[(int64_t)oc * C * taps + c * taps + kr * p.wR + ka * p.wA + kw];
+        const int64_t wi = (int64_t)oc * C * taps + c * taps + kr * p.wR + ka * p.wA + kw;
+        if (CONV_DBG_OK(wi, p.w_elems, kStatusBoundsW)) v = p.w[wi];
       }
       ws[i] = v;
     }
@@ -382,6 +392,20 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
     const int64_t c_stride_src = (int64_t)g.D * HW;
     const uint32_t c_stride_dst = 4u * (uint32_t)(p.srows_max * p.WP);
     int slot_of_next = 0;  // ring slot of the next plane issued (planes are issued in order)
+    // one copy of x[src] into the ring (the debug build checks both ends)
+    auto copy_in = [&](uint32_t dst, const float *src) {
+#ifdef CONVFWD_DEBUG
+      const uint32_t nb = p.vec ? 16u : 4u;
+      if (!CONV_DBG_OK(src - p.x, p.x_elems, kStatusBoundsX) ||
+          !CONV_DBG_OK(src + nb / 4 - 1 - p.x, p.x_elems, kStatusBoundsX) ||
+          !CONV_DBG_OK(dst - ring_addr + nb - 1, 4ll * p.ring * p.slot_floats, kStatusBoundsShared))
+        return;
+#endif
+      if (p.vec)
+        cp_async16(dst, src);
+      else
+        cp_async4(dst, src);
+    };
     auto issue_plane = [&](int dd) {
       const uint32_t slot = ring_addr + 4u * (uint32_t)slot_of_next * p.slot_floats;
       slot_of_next = (slot_of_next + 1 == p.ring) ? 0 : slot_of_next + 1;
@@ -389,24 +413,14 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
       if (sq0 < per_plane_sq) {
         const float *src = p.x + src0 + dd_off;
         uint32_t dst = slot + dst0;
-        for (int c = 0; c < C; ++c, src += c_stride_src, dst += c_stride_dst) {
-          if (p.vec)
-            cp_async16(dst, src);
-          else
-            cp_async4(dst, src);
-        }
+        for (int c = 0; c < C; ++c, src += c_stride_src, dst += c_stride_dst) copy_in(dst, src);
       }
       // rare: more (row, unit) pairs than threads
       for (int i = sq0 + kSThreads; i < per_plane_sq; i += kSThreads) {
         const int si = i / WQ, qi = i - si * WQ;
         const float *src = p.x + srow_src[si] + dd_off + (int64_t)qi * (p.vec ? 4 : 1);
         uint32_t dst = slot + 4u * (uint32_t)(si * p.WP) + (p.vec ? 16u : 4u) * (uint32_t)qi;
-        for (int c = 0; c < C; ++c, src += c_stride_src, dst += c_stride_dst) {
-          if (p.vec)
-            cp_async16(dst, src);
-          else
-            cp_async4(dst, src);
-        }
+        for (int c = 0; c < C; ++c, src += c_stride_src, dst += c_stride_dst) copy_in(dst, src);
       }
       cp_async_commit();
     };
@@ -540,7 +554,8 @@ __global__ void __launch_bounds__(kSThreads, 1) fused_min_softmax_staged_kernel(
 #pragma unroll
         for (int o = 0; o < kSCO; ++o) {
           const int oc = cg * kSCO + o;
-          if (oc < g.K) yo[(int64_t)oc * OHW] = v[o] * inv;
+          if (oc < g.K && CONV_DBG_OK(yo + (int64_t)oc * OHW - p.y, p.y_elems, kStatusBoundsY))
+            yo[(int64_t)oc * OHW] = v[o] * inv;
         }
       }
     }
@@ -560,12 +575,14 @@ __global__ void __launch_bounds__(256) transpose_last2_kernel(const float *__res
     float *dst = out + b * (int64_t)R * C;
     for (int i = threadIdx.y; i < 32; i += 8) {
       const int r = r0 + i, c = c0 + (int)threadIdx.x;
-      if (r < R && c < C) t[i][threadIdx.x] = src[(int64_t)r * C + c];
+      if (r < R && c < C && CONV_DBG_OK(b * (int64_t)R * C + (int64_t)r * C + c, B * (int64_t)R * C, kStatusBoundsX))
+        t[i][threadIdx.x] = src[(int64_t)r * C + c];
     }
     __syncthreads();
     for (int i = threadIdx.y; i < 32; i += 8) {
       const int c = c0 + i, r = r0 + (int)threadIdx.x;
-      if (r < R && c < C) dst[(int64_t)c * R + r] = t[threadIdx.x][i];
+      if (r < R && c < C && CONV_DBG_OK(b * (int64_t)R * C + (int64_t)c * R + r, B * (int64_t)R * C, kStatusBoundsWs))
+        dst[(int64_t)c * R + r] = t[threadIdx.x][i];
     }
     __syncthreads();
   }
@@ -644,6 +661,7 @@ cudaError_t launch_t(const FusedParams &p0, cudaStream_t stream) {
   const int64_t blocks = rowgroups * p.coltiles;
   if (blocks > 0x7fffffff) return cudaErrorInvalidConfiguration;
   const size_t smem = sizeof(float) * (size_t)(p.g.C * p.g.taps()) * NCG * kCO;
+  CONV_PLAN_CHECK(smem <= (size_t)kMaxSmemBytes && p.g.K <= NCG * kCO && (!KWT || KWT == p.KB));
   auto kern = fused_min_softmax_kernel<NCG, NROW, KWT, VEC>;
   if (smem > 48 * 1024) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -682,6 +700,9 @@ __global__ void __launch_bounds__(256) channel_softmax_kernel(float *__restrict_
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t n = i / plane, pos = i - n * plane;
     float *q = y + n * C * plane + pos;
+    if (!CONV_DBG_OK(q - y, N * C * plane, kStatusBoundsY) ||
+        !CONV_DBG_OK(q + (C - 1) * plane - y, N * C * plane, kStatusBoundsY))
+      continue;
     float mx = -INFINITY;
     for (int64_t c = 0; c < C; ++c) mx = fmaxf(mx, q[c * plane]);
     float sum = 0.f;
@@ -819,6 +840,11 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     p.wR = 1, p.wA = g.KH * g.KW, p.wB = g.KW;
   }
   p.rows = g.N * (int64_t)p.OA;
+  p.x_elems = g.N * g.C * g.in_spatial() - debug_x_shrink();
+  p.w_elems = g.K * g.C * g.taps();
+  p.y_elems = g.N * g.K * (int64_t)p.OA * p.OB;
+  CONV_PLAN_CHECK(p.OR >= 1 && p.OA >= 1 && p.OB >= 1 && p.KB <= kMaxKW && g.G == 1 && !g.cl);
+  CONV_PLAN_CHECK((int64_t)p.OR * p.OA * p.OB == g.out_spatial());
   StagedParams sp;
   // the staged kernel keeps W as its column axis: the min over depth or height
   if (min_dim != 4) staged_axes(g, min_dim, &sp);
@@ -829,11 +855,17 @@ cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float
     sp.y = y;
     sp.g = g;
     sp.rows = p.rows;
+    sp.x_elems = p.x_elems;
+    sp.w_elems = p.w_elems;
+    sp.y_elems = p.y_elems;
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
     const size_t smem = 4 * ((size_t)sp.w_floats + (size_t)sp.ring * sp.slot_floats + kRingSlackFloats);
+    CONV_PLAN_CHECK(smem <= (size_t)kMaxSmemBytes && sp.nb >= 1 && sp.ring == sp.KR + 2 * sp.nb - 1);
+    CONV_PLAN_CHECK(sp.srows_max <= kSMaxSrows && sp.WP >= g.W + 4 && g.KW == 3 && g.K <= kSNcg * kSCO);
+    CONV_PLAN_CHECK(!sp.vec || ((g.W % 4) == 0 && ((uintptr_t)x & 15u) == 0));
     // the benchmark shape (C_in 3, kernel 3^3, W 32 -> pitch 36) is specialised: 30 shared
     // rows for the min over depth (blocks span <= 2 images of 30 rows), 32 over height (22)
     const bool spec3 = g.C == 3 && sp.KR == 3 && sp.KA == 3 && sp.WP == 36;

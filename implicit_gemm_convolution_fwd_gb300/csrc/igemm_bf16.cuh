@@ -66,6 +66,15 @@ bool make_plan_bf16(const Geom &g, PlanBf16 *pl, const char **why) {
   return true;
 }
 
+// x[xoff + o] as a zero-extended 16-bit pattern (the debug build first checks
+// that the index lies in x)
+__device__ __forceinline__ uint32_t ldxh(const PosInfo &ps, const uint16_t *xo, int32_t o) {
+#ifdef CONVFWD_DEBUG
+  if (!CONV_DBG_OK(ps.xoff + o, ps.xn, kStatusBoundsX)) return 0u;
+#endif
+  return (uint32_t)__ldg(xo + o);
+}
+
 // 16 consecutive reduction columns of one output position as bf16 bit
 // patterns (zero-extended to 32 bits); same tables and paths as gather_cols.
 __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16_t *xo, const int32_t *toff,
@@ -77,10 +86,10 @@ __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16
     for (int q = 0; q < kUnit / 4; ++q) {
       const int4 o = o4[q];
       const int k = k0 + 4 * q;
-      v[4 * q + 0] = k + 0 < Kred ? (uint32_t)__ldg(xo + o.x) : 0u;
-      v[4 * q + 1] = k + 1 < Kred ? (uint32_t)__ldg(xo + o.y) : 0u;
-      v[4 * q + 2] = k + 2 < Kred ? (uint32_t)__ldg(xo + o.z) : 0u;
-      v[4 * q + 3] = k + 3 < Kred ? (uint32_t)__ldg(xo + o.w) : 0u;
+      v[4 * q + 0] = k + 0 < Kred ? ldxh(ps, xo, o.x) : 0u;
+      v[4 * q + 1] = k + 1 < Kred ? ldxh(ps, xo, o.y) : 0u;
+      v[4 * q + 2] = k + 2 < Kred ? ldxh(ps, xo, o.z) : 0u;
+      v[4 * q + 3] = k + 3 < Kred ? ldxh(ps, xo, o.w) : 0u;
     }
   } else if (tap_major) {
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
@@ -90,10 +99,10 @@ __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16
       const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
       const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
       const int4 o = o4[q];
-      v[4 * q + 0] = in ? (uint32_t)__ldg(xo + o.x) : 0u;
-      v[4 * q + 1] = in ? (uint32_t)__ldg(xo + o.y) : 0u;
-      v[4 * q + 2] = in ? (uint32_t)__ldg(xo + o.z) : 0u;
-      v[4 * q + 3] = in ? (uint32_t)__ldg(xo + o.w) : 0u;
+      v[4 * q + 0] = in ? ldxh(ps, xo, o.x) : 0u;
+      v[4 * q + 1] = in ? ldxh(ps, xo, o.y) : 0u;
+      v[4 * q + 2] = in ? ldxh(ps, xo, o.z) : 0u;
+      v[4 * q + 3] = in ? ldxh(ps, xo, o.w) : 0u;
     }
   } else {
 #pragma unroll
@@ -101,7 +110,7 @@ __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16
       const uint32_t e = ttap[k0 + j];
       const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
       const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
-      v[j] = in ? (uint32_t)__ldg(xo + toff[k0 + j]) : 0u;
+      v[j] = in ? ldxh(ps, xo, toff[k0 + j]) : 0u;
     }
   }
 }
@@ -122,7 +131,8 @@ __device__ __forceinline__ unsigned short float_to_bits16(float f) {
 // values in core matrices of 8 rows x 8 (LBO 128 bytes along K, SBO 512 bytes
 // along N); column kg maps to w's memory order as in the resident staging.
 __global__ void split_weights_bf16_kernel(const uint16_t *__restrict__ w, uint16_t *__restrict__ ws, int K, int C,
-                                          int taps, int Kfull, int Npad, int nchunks, int tap_major) {
+                                          int taps, int Kfull, int Npad, int nchunks, int tap_major, int64_t w_elems,
+                                          int64_t ws_elems) {
   const int64_t per_chunk = (int64_t)Npad * kBfChunk;
   const int64_t total = per_chunk * nchunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -138,9 +148,9 @@ __global__ void split_weights_bf16_kernel(const uint16_t *__restrict__ w, uint16
         const int t = kg / C;
         kmem = (kg - t * C) * taps + t;
       }
-      v = __ldg(w + (int64_t)n * Kfull + kmem);
+      if (CONV_DBG_OK((int64_t)n * Kfull + kmem, w_elems, kStatusBoundsW)) v = __ldg(w + (int64_t)n * Kfull + kmem);
     }
-    ws[i] = v;
+    if (CONV_DBG_OK(i, ws_elems, kStatusBoundsWs)) ws[i] = v;
   }
 }
 
@@ -191,7 +201,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
             const int t = kk / g.C;
             kmem = (kk - t * g.C) * taps + t;
           }
-          word |= (uint32_t)__ldg(p.wh + (int64_t)n * p.Kred + kmem) << (16 * h);
+          if (CONV_DBG_OK((int64_t)n * p.Kred + kmem, p.w_elems, kStatusBoundsW))
+            word |= (uint32_t)__ldg(p.wh + (int64_t)n * p.Kred + kmem) << (16 * h);
         }
       }
       reinterpret_cast<uint32_t *>(b_s)[i] = word;
@@ -267,6 +278,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
           ptx::tc_fence_before();
           ptx::mbar_arrive(bar_d_empty + 8 * b);
         }
+#ifdef CONVFWD_DEBUG
+        if (valid) {
+          // this lane's stores of channels c0 .. c0 + 31 (< K): first and last index
+          const int64_t i0 = (yp - p.yh) + (int64_t)c0 * p.osp;
+          const int nk = min(32, (int)g.K - c0);
+          if (nk > 0 && (!CONV_DBG_OK(i0, p.y_elems, kStatusBoundsY) ||
+                         !CONV_DBG_OK(i0 + (int64_t)(nk - 1) * p.osp, p.y_elems, kStatusBoundsY)))
+            continue;
+        }
+#endif
         if (valid) {
           uint16_t *q = yp + (int64_t)c0 * p.osp;
 #pragma unroll
@@ -310,10 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
         ptx::tc_fence_after();
         if (SB && t == 0) {
           // the stage's MMAs are done: its B half is free too
-          ptx::mbar_arrive_expect_tx(bar_b_full + 8 * stage, p.sb_stage_bytes);
-          ptx::bulk_copy_g2s(ptx::smem_addr(b_s + (size_t)stage * p.sb_stage_bytes),
-                             reinterpret_cast<const uint8_t *>(p.wsp) + (size_t)q * p.sb_stage_bytes, p.sb_stage_bytes,
-                             bar_b_full + 8 * stage);
+          const int64_t e0 = (int64_t)q * (p.sb_stage_bytes / 2);  // 16-bit elements
+          if (CONV_DBG_OK(e0 + p.sb_stage_bytes / 2 - 1, p.ws_elems, kStatusBoundsWs)) {
+            ptx::mbar_arrive_expect_tx(bar_b_full + 8 * stage, p.sb_stage_bytes);
+            ptx::bulk_copy_g2s(ptx::smem_addr(b_s + (size_t)stage * p.sb_stage_bytes),
+                               reinterpret_cast<const uint8_t *>(p.wsp) + (size_t)q * p.sb_stage_bytes,
+                               p.sb_stage_bytes, bar_b_full + 8 * stage);
+          } else {
+            ptx::mbar_arrive(bar_b_full + 8 * stage);  // (debug build) the copy is dropped
+          }
           sb_last_stage = stage;
           sb_last_parity = r & 1;
         }
@@ -333,8 +359,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
 #pragma unroll
           for (int i = 0; i < kBfChunk / 4; ++i) {
             const int4 o = o4[i];
-            packed[2 * i] = __byte_perm(__ldg(xo + o.x), __ldg(xo + o.y), 0x5410);
-            packed[2 * i + 1] = __byte_perm(__ldg(xo + o.z), __ldg(xo + o.w), 0x5410);
+            packed[2 * i] = __byte_perm(ldxh(ps, xo, o.x), ldxh(ps, xo, o.y), 0x5410);
+            packed[2 * i + 1] = __byte_perm(ldxh(ps, xo, o.z), ldxh(ps, xo, o.w), 0x5410);
           }
           if (!put(q, packed)) {
             aborted = true;

@@ -41,6 +41,7 @@
 #include <atomic>
 
 #include "conv_internal.cuh"
+#include "debug_check.cuh"
 #include "sm100_ptx.cuh"
 
 namespace convfwd {
@@ -117,6 +118,9 @@ struct IgemmParams {
   int nB;
   int64_t sR, sA, sB;
   int fused_min_only;  // a 32-channel block of a wider layer: write min + bias, no softmax
+  // elements addressable from x / w (or wh) / y (or yh) / wsp as this launch
+  // receives them: what the debug build's device checks test indices against
+  int64_t x_elems, w_elems, y_elems, ws_elems;
 };
 
 struct Plan {
@@ -243,7 +247,18 @@ struct PosInfo {
   uint32_t dm, hm, wm;  // bit k set: tap k along D / H / W lands inside the input
   bool valid;           // the position exists (last tile may be partial)
   bool warp_full;       // every lane's receptive field is entirely inside the input
+#ifdef CONVFWD_DEBUG
+  int64_t xn;           // elements of x the launch may read
+#endif
 };
+
+// x[xoff + o] (the debug build first checks that the index lies in x)
+__device__ __forceinline__ float ldx(const PosInfo &ps, int32_t o) {
+#ifdef CONVFWD_DEBUG
+  if (!CONV_DBG_OK(ps.xoff + o, ps.xn, kStatusBoundsX)) return 0.f;
+#endif
+  return __ldg(ps.xo + o);
+}
 
 template <bool FUSED = false>
 __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t tile, int t) {
@@ -299,6 +314,9 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   const int64_t xoff = g.cl ? (n * HW * g.D + pos) * (g.G * g.C) : n * g.x_batch_stride() + pos;
   ps.xoff = xoff;
   ps.xo = p.x + (ps.valid ? xoff : 0);
+#ifdef CONVFWD_DEBUG
+  ps.xn = p.x_elems;
+#endif
   return ps;
 }
 
@@ -327,6 +345,10 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
         in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
       }
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#ifdef CONVFWD_DEBUG
+      if (in) in = CONV_DBG_OK(ps.xoff + toff[k], ps.xn, kStatusBoundsX) &&
+                   CONV_DBG_OK(ps.xoff + toff[k] + 3, ps.xn, kStatusBoundsX);
+#endif
       if (in) a = __ldg(reinterpret_cast<const float4 *>(ps.xo + toff[k]));
       v[4 * q + 0] = a.x;
       v[4 * q + 1] = a.y;
@@ -339,20 +361,20 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
 #pragma unroll
       for (int q = 0; q < kUnit / 4; ++q) {
         const int4 o = o4[q];
-        v[4 * q + 0] = __ldg(ps.xo + o.x);
-        v[4 * q + 1] = __ldg(ps.xo + o.y);
-        v[4 * q + 2] = __ldg(ps.xo + o.z);
-        v[4 * q + 3] = __ldg(ps.xo + o.w);
+        v[4 * q + 0] = ldx(ps, o.x);
+        v[4 * q + 1] = ldx(ps, o.y);
+        v[4 * q + 2] = ldx(ps, o.z);
+        v[4 * q + 3] = ldx(ps, o.w);
       }
     } else {
 #pragma unroll
       for (int q = 0; q < kUnit / 4; ++q) {
         const int4 o = o4[q];
         const int k = k0 + 4 * q;
-        v[4 * q + 0] = k + 0 < Kred ? __ldg(ps.xo + o.x) : 0.f;
-        v[4 * q + 1] = k + 1 < Kred ? __ldg(ps.xo + o.y) : 0.f;
-        v[4 * q + 2] = k + 2 < Kred ? __ldg(ps.xo + o.z) : 0.f;
-        v[4 * q + 3] = k + 3 < Kred ? __ldg(ps.xo + o.w) : 0.f;
+        v[4 * q + 0] = k + 0 < Kred ? ldx(ps, o.x) : 0.f;
+        v[4 * q + 1] = k + 1 < Kred ? ldx(ps, o.y) : 0.f;
+        v[4 * q + 2] = k + 2 < Kred ? ldx(ps, o.z) : 0.f;
+        v[4 * q + 3] = k + 3 < Kred ? ldx(ps, o.w) : 0.f;
       }
     }
   } else if (tap4) {
@@ -365,10 +387,10 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
       const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
       const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
       const int4 o = o4[q];
-      v[4 * q + 0] = in ? __ldg(ps.xo + o.x) : 0.f;
-      v[4 * q + 1] = in ? __ldg(ps.xo + o.y) : 0.f;
-      v[4 * q + 2] = in ? __ldg(ps.xo + o.z) : 0.f;
-      v[4 * q + 3] = in ? __ldg(ps.xo + o.w) : 0.f;
+      v[4 * q + 0] = in ? ldx(ps, o.x) : 0.f;
+      v[4 * q + 1] = in ? ldx(ps, o.y) : 0.f;
+      v[4 * q + 2] = in ? ldx(ps, o.z) : 0.f;
+      v[4 * q + 3] = in ? ldx(ps, o.w) : 0.f;
     }
   } else {
 #pragma unroll
@@ -376,7 +398,7 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
       const uint32_t e = ttap[k0 + j];
       const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
       const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
-      v[j] = in ? __ldg(ps.xo + toff[k0 + j]) : 0.f;
+      v[j] = in ? ldx(ps, toff[k0 + j]) : 0.f;
     }
   }
 }
@@ -432,7 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         const int t = kg / g.C;
         kmem = (kg - t * g.C) * taps + t;
       }
-      const float v = (n < g.K && k < p.Kred) ? __ldg(p.w + (int64_t)n * p.Kfull + kmem) : 0.f;
+      float v = 0.f;
+      if (n < g.K && k < p.Kred && CONV_DBG_OK((int64_t)n * p.Kfull + kmem, p.w_elems, kStatusBoundsW))
+        v = __ldg(p.w + (int64_t)n * p.Kfull + kmem);
       const float hi = __uint_as_float(tf32_hi_bits(v));
       reinterpret_cast<float *>(b_hi)[i] = hi;
       reinterpret_cast<float *>(b_lo)[i] = v - hi;
@@ -530,6 +554,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         if (pp < plane) {
           // y[n, o, pos]; images are y_chans channels apart (all blocks of a wider layer)
           float *yp = p.y + img * p.y_chans * plane + pp;
+#ifdef CONVFWD_DEBUG
+          {
+            const int64_t i0 = img * p.y_chans * plane + pp;
+            if (!CONV_DBG_OK(i0, p.y_elems, kStatusBoundsY) ||
+                !CONV_DBG_OK(i0 + (int64_t)(K - 1) * plane, p.y_elems, kStatusBoundsY))
+              continue;
+          }
+#endif
           if (p.fused_min_only) {
             // one block of a layer wider than 32 channels: the softmax over all
             // of them runs afterwards as a pass of its own
@@ -584,6 +616,16 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       // y[n, c0 + j, pos] = accumulator column c0 + j + bias, j < 32: a warp
       // store covers 32 consecutive positions of one channel.
       auto store32 = [&](const uint32_t (&v)[32], int c0) {
+#ifdef CONVFWD_DEBUG
+        {
+          // this lane's stores of channels c0 .. c0 + 31 (< K): first and last index
+          const int64_t i0 = (yp - p.y) + (g.cl ? (int64_t)c0 : (int64_t)c0 * p.osp);
+          const int nk = min(32, (int)g.K - c0);
+          const int64_t i1 = i0 + (int64_t)(nk - 1) * (g.cl ? 1 : p.osp);
+          if (nk > 0 && (!CONV_DBG_OK(i0, p.y_elems, kStatusBoundsY) || !CONV_DBG_OK(i1, p.y_elems, kStatusBoundsY)))
+            return;
+        }
+#endif
         if (ACC) {
           // a later reduction pass: add to what the earlier passes stored
           const int64_t ostride = g.cl ? 1 : p.osp;
@@ -695,9 +737,14 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::tc_fence_after();
       if (SB && t == 0) {
         // the stage's MMAs are done: its B half is free too
-        ptx::mbar_arrive_expect_tx(bar_b_full + 8 * stage, p.sb_stage_bytes);
-        ptx::bulk_copy_g2s(ptx::smem_addr(b_hi + (size_t)stage * p.sb_stage_bytes),
-                           p.wsp + (size_t)q * (p.sb_stage_bytes / 4), p.sb_stage_bytes, bar_b_full + 8 * stage);
+        const int64_t w0 = (int64_t)q * (p.sb_stage_bytes / 4);
+        if (CONV_DBG_OK(w0 + p.sb_stage_bytes / 4 - 1, p.ws_elems, kStatusBoundsWs)) {
+          ptx::mbar_arrive_expect_tx(bar_b_full + 8 * stage, p.sb_stage_bytes);
+          ptx::bulk_copy_g2s(ptx::smem_addr(b_hi + (size_t)stage * p.sb_stage_bytes), p.wsp + w0, p.sb_stage_bytes,
+                             bar_b_full + 8 * stage);
+        } else {
+          ptx::mbar_arrive(bar_b_full + 8 * stage);  // (debug build) the copy is dropped
+        }
         sb_last_stage = stage;
         sb_last_parity = r & 1;
       }
@@ -731,10 +778,10 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 #pragma unroll
       for (int i = 0; i < CH / 4; ++i) {
         const int4 o = o4[i];
-        v[4 * i + 0] = __ldg(ps.xo + o.x);
-        v[4 * i + 1] = __ldg(ps.xo + o.y);
-        v[4 * i + 2] = __ldg(ps.xo + o.z);
-        v[4 * i + 3] = __ldg(ps.xo + o.w);
+        v[4 * i + 0] = ldx(ps, o.x);
+        v[4 * i + 1] = ldx(ps, o.y);
+        v[4 * i + 2] = ldx(ps, o.z);
+        v[4 * i + 3] = ldx(ps, o.w);
       }
     };
     const int nfull = (p.KC == CH && !p.vec4) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
@@ -856,7 +903,8 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
 // SBO KC * 32 bytes along N).  Column kg maps to w's memory order as in the
 // kernel's resident staging.
 __global__ void split_weights_kernel(const float *__restrict__ w, float *__restrict__ ws, int K, int C, int taps,
-                                     int Kfull, int Npad, int KC, int nchunks, int tap_major) {
+                                     int Kfull, int Npad, int KC, int nchunks, int tap_major, int64_t w_elems,
+                                     int64_t ws_elems) {
   const int64_t per_chunk = (int64_t)Npad * KC;
   const int64_t total = per_chunk * nchunks;
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -871,11 +919,14 @@ __global__ void split_weights_kernel(const float *__restrict__ w, float *__restr
         const int t = kg / C;
         kmem = (kg - t * C) * taps + t;
       }
-      v = __ldg(w + (int64_t)n * Kfull + kmem);
+      if (CONV_DBG_OK((int64_t)n * Kfull + kmem, w_elems, kStatusBoundsW)) v = __ldg(w + (int64_t)n * Kfull + kmem);
     }
     const float hi = __uint_as_float(tf32_hi_bits(v));
     const int64_t o = ((int64_t)(n / 8) * (KC / 4) + kl / 4) * 32 + (n % 8) * 4 + (kl % 4);
-    float *chunk = ws + (int64_t)q * 2 * per_chunk;
+    const int64_t c0 = (int64_t)q * 2 * per_chunk;
+    if (!CONV_DBG_OK(c0 + o, ws_elems, kStatusBoundsWs) || !CONV_DBG_OK(c0 + per_chunk + o, ws_elems, kStatusBoundsWs))
+      continue;
+    float *chunk = ws + c0;
     chunk[o] = hi;
     chunk[per_chunk + o] = v - hi;
   }
@@ -890,6 +941,23 @@ bool g_attr_bf16_set[64] = {false};
 bool g_attr_f16_set[64] = {false};
 bool g_attr_set[64] = {false};
 bool g_attr_fused_set[64] = {false};
+
+// Elements addressable from a launch's x pointer (the group's first channel)
+// to the last element the launch may read; the debug build's test hook can
+// shrink it.
+int64_t x_extent(const Geom &g) {
+  const int64_t dhw = g.in_spatial();
+  const int64_t n = g.cl ? (g.N * dhw - 1) * g.G * g.C + g.C : (g.N - 1) * g.x_batch_stride() + g.C * dhw;
+  const int64_t s = debug_x_shrink();
+  return n > s ? n - s : 0;
+}
+// The same for y: kb channels of `plane` positions per image, images y_chans
+// channels apart.
+int64_t y_extent(const Geom &g, int64_t y_chans, int64_t kb, int64_t plane) {
+  return g.cl ? (g.N * plane - 1) * y_chans + kb : (g.N - 1) * y_chans * plane + kb * plane;
+}
+// TMEM columns a plan uses: one accumulator per slot plus two A stages (hi + lo) per slot.
+int tmem_cols_used(int nslots, int npad, int kc) { return nslots * npad + nslots * 2 * 2 * kc; }
 
 }  // namespace
 
@@ -960,8 +1028,12 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     const int threads = 256;
     const int64_t blocks64 = (total + threads - 1) / threads;
     const int blocks = (int)(blocks64 < 4096 ? blocks64 : 4096);
+    CONV_PLAN_CHECK(nchunks * pl.KC == kpad && pl.KC % 16 == 0);
+    CONV_PLAN_CHECK(tmem_cols_used(pl.nslots, pl.Npad, pl.KC) <= (int)kTmemCols);
+    CONV_PLAN_CHECK(((uintptr_t)ws & 15u) == 0);
     split_weights_kernel<<<blocks, threads, 0, stream>>>(w, ws, (int)g.K, (int)g.C, g.taps(), (int)kfull, pl.Npad,
-                                                         pl.KC, nchunks, pl.tap_major && !g.cl);
+                                                         pl.KC, nchunks, pl.tap_major && !g.cl, g.K * kfull,
+                                                         2 * total);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     IgemmParams p = {};
@@ -990,9 +1062,14 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     p.wsp = ws;
     p.sb_stage_bytes = (uint32_t)(2 * pl.Npad * pl.KC * 4);
     p.b_bytes = (uint32_t)(pl.nslots * 2) * p.sb_stage_bytes;
+    p.x_elems = x_extent(g);
+    p.w_elems = g.K * kfull;
+    p.y_elems = y_extent(g, p.y_chans, g.K, osp);
+    p.ws_elems = 2 * total;
     const size_t smem_need = (size_t)p.b_bytes + (size_t)kpad * 8 + (size_t)pl.Npad * 4 + 16 + kNumBars * 8 + 16;
     const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
     const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+    CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && p.sb_stage_bytes % 16 == 0 && grid >= 1);
     auto kern = pl.KC <= 16 ? igemm_3xtf32_kernel<16, false, true> : igemm_3xtf32_kernel<32, false, true>;
     kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
@@ -1033,10 +1110,18 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
       p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)p.y & 15u) == 0) ? 1 : 0;
       p.b_bytes = (uint32_t)((size_t)pl.Npad * p.Kpad * 4);
+      p.x_elems = x_extent(g);
+      p.w_elems = gb.K * kfull;
+      p.y_elems = y_extent(g, p.y_chans, gb.K, osp);
       const size_t smem_need = (size_t)2 * pl.Npad * p.Kpad * 4 + (size_t)p.Kpad * 8 + (size_t)pl.Npad * 4 + 16 +
                                kNumBars * 8 + 16;
       const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
       const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+      CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && grid >= 1 && kred > 0);
+      CONV_PLAN_CHECK(p.Kpad % 32 == 0 && p.nchunks * p.KC >= p.Kpad && p.KC % 16 == 0);
+      CONV_PLAN_CHECK(tmem_cols_used(pl.nslots, pl.Npad, pl.KC) <= (int)kTmemCols);
+      CONV_PLAN_CHECK(k_begin + kred <= kfull && (o0 + gb.K) <= g.K);
+      CONV_PLAN_CHECK(!p.vec4 || ((uintptr_t)x & 15u) == 0);
       auto kern = pl.KC <= 16 ? (pass ? igemm_3xtf32_kernel<16, true, false> : igemm_3xtf32_kernel<16, false, false>)
                               : (pass ? igemm_3xtf32_kernel<32, true, false> : igemm_3xtf32_kernel<32, false, false>);
       kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
@@ -1157,6 +1242,12 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.nslots = pl.nslots;
   p.tap_major = pl.tap_major;
   const int64_t grid = p.columns < g_num_sms[dev] ? p.columns : g_num_sms[dev];
+  p.x_elems = x_extent(g);
+  p.w_elems = g.K * kfull;
+  p.y_elems = (g.N - 1) * p.y_chans * p.plane + g.K * p.plane;
+  CONV_PLAN_CHECK(grid >= 1 && p.R >= 1 && (int64_t)p.hw_tiles * kTileM >= p.plane);
+  CONV_PLAN_CHECK(p.plane * p.R == p.osp && p.nB >= 1 && p.plane % p.nB == 0);
+  CONV_PLAN_CHECK(tmem_cols_used(pl.nslots, pl.Npad, pl.KC) <= (int)kTmemCols);
   if (streamed) {
     // the whole reduction in one pass, its weights split once into ws and
     // brought in chunk by chunk (as for the plain conv's streamed weights)
@@ -1166,8 +1257,9 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
     const int threads = 256;
     const int64_t blocks64 = (total + threads - 1) / threads;
     const int blocks = (int)(blocks64 < 4096 ? blocks64 : 4096);
+    CONV_PLAN_CHECK(nchunks * pl.KC == kpad && ((uintptr_t)ws & 15u) == 0);
     split_weights_kernel<<<blocks, threads, 0, stream>>>(w, ws, (int)g.K, (int)g.C, g.taps(), (int)kfull, pl.Npad,
-                                                         pl.KC, nchunks, pl.tap_major);
+                                                         pl.KC, nchunks, pl.tap_major, g.K * kfull, 2 * total);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     p.Kred = (int)kfull;
@@ -1176,8 +1268,10 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
     p.wsp = ws;
     p.sb_stage_bytes = (uint32_t)(2 * pl.Npad * pl.KC * 4);
     p.b_bytes = (uint32_t)(pl.nslots * 2) * p.sb_stage_bytes;
+    p.ws_elems = 2 * total;
     const size_t smem_need = (size_t)p.b_bytes + (size_t)kpad * 8 + (size_t)pl.Npad * 4 + 16 + kNumBars * 8 + 16;
     const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
+    CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem);
     igemm_3xtf32_kernel<16, false, true, true><<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
   }
@@ -1185,6 +1279,7 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.Kpad = pl.Kpad;
   p.nchunks = pl.nchunks;
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
+  CONV_PLAN_CHECK(pl.smem <= (size_t)kMaxSmem && pl.npasses == 1);
   igemm_3xtf32_kernel<16, false, false, true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -1240,8 +1335,10 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
       // the block's weights in chunk order into ws (reused block after block, in stream order)
       const int64_t total = (int64_t)pl.Npad * kBfChunk * pl.nchunks;
       const int64_t blocks64 = (total + 255) / 256;
+      CONV_PLAN_CHECK(((uintptr_t)ws & 15u) == 0 && pl.nchunks * kBfChunk == pl.Kpad);
       split_weights_bf16_kernel<<<(unsigned)(blocks64 < 4096 ? blocks64 : 4096), 256, 0, stream>>>(
-          w + o0 * kfull, ws, (int)gb.K, (int)g.C, g.taps(), (int)kfull, pl.Npad, pl.nchunks, pl.tap_major);
+          w + o0 * kfull, ws, (int)gb.K, (int)g.C, g.taps(), (int)kfull, pl.Npad, pl.nchunks, pl.tap_major,
+          gb.K * kfull, total);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
     }
@@ -1269,8 +1366,14 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
       p.wsp = reinterpret_cast<const float *>(ws);
       p.sb_stage_bytes = (uint32_t)(pl.Npad * kBfChunk * 2);
       p.b_bytes = (uint32_t)(pl.nslots * 2) * p.sb_stage_bytes;
+      p.ws_elems = (int64_t)pl.Npad * kBfChunk * pl.nchunks;
     }
+    p.x_elems = x_extent(g);
+    p.w_elems = gb.K * kfull;
+    p.y_elems = y_extent(g, p.y_chans, gb.K, osp);
     const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
+    CONV_PLAN_CHECK(pl.smem <= (size_t)kMaxSmem && grid >= 1 && pl.Kred == kfull && !g.cl);
+    CONV_PLAN_CHECK(pl.nchunks * kBfChunk >= pl.Kpad && pl.nslots * pl.Npad + pl.nslots * 2 * 16 <= (int)kTmemCols);
     auto kern = fp16 ? (pl.streamed ? igemm_bf16_kernel<true, true> : igemm_bf16_kernel<true, false>)
                      : (pl.streamed ? igemm_bf16_kernel<false, true> : igemm_bf16_kernel<false, false>);
     kern<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);

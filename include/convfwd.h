@@ -50,6 +50,12 @@
  *     the problem, the kernel family and, for the tensor-core family, the plan
  *     (tiles, reduction length and padding, column order, slots, passes,
  *     channel blocks, resident or streamed weights, shared memory).
+ *   - With CONVFWD_FORCE_ALGO=direct_ffma or =igemm_3xtf32 in the environment
+ *     (read once per process), fp32 calls made with CONV_ALGO_AUTO -- the
+ *     plain and grouped convolutions, conv3d_min_softmax, conv_select_algo --
+ *     take that kernel family wherever it can run the problem, and the
+ *     planner's choice elsewhere.  Other values are ignored (one line on
+ *     stderr).  An explicit algo argument always wins.
  */
 #ifndef CONVFWD_H
 #define CONVFWD_H
@@ -76,7 +82,8 @@ typedef enum {
   CONV_ERR_ARG = 2,         /* a size/hyper-parameter is out of range, or a pointer is misaligned */
   CONV_ERR_SHAPE = 3,       /* an output size is <= 0, or descriptor shapes disagree */
   CONV_ERR_UNSUPPORTED = 4, /* valid request that this library does not implement */
-  CONV_ERR_CUDA = 5         /* a CUDA runtime call failed (see conv_last_error) */
+  CONV_ERR_CUDA = 5,        /* a CUDA runtime call failed (see conv_last_error) */
+  CONV_ERR_INTERNAL = 6     /* debug build only: a launch plan failed one of its assertions (a library bug) */
 } conv_status_t;
 
 /* Kernel families.  AUTO lets the planner choose. */
@@ -406,9 +413,45 @@ CONVFWD_API int conv_debug_set_wait_limit(long long cycles);
  * wait that ran out first: bit 8 producers waiting for an A stage to drain,
  * bit 9 the MMA issuer waiting for an A stage to fill, bit 10 the issuer
  * waiting for streamed weights, bit 11 the epilogue waiting for an
- * accumulator, bit 12 the issuer waiting for an accumulator to drain.  Writes
+ * accumulator, bit 12 the issuer waiting for an accumulator to drain.  In a
+ * debug build (below) also the bounds checks since the last call: bit 1 an
+ * index outside x, bit 2 outside w or bias, bit 3 outside y, bit 4 outside a
+ * workspace, bit 5 outside a kernel's shared-memory staging buffer.  Writes
  * the word to *flags and returns CONV_OK, or CONV_ERR_CUDA. */
 CONVFWD_API int conv_device_status(unsigned int *flags);
+
+/*
+ * Debug build (the library compiled with -DCONVFWD_DEBUG, libconvfwd_debug.so
+ * beside libconvfwd.so; the Python binding loads it when CONVFWD_DEBUG=1 is in
+ * the environment).  The stand-in for a memory checker: same entry points,
+ * same results on correct inputs, slower.
+ *   - Host: every launcher asserts its plan before launching (shared memory
+ *     and tensor-memory budgets, chunk and stage sizes, alignment of the
+ *     addresses bulk copies and 16-byte accesses use, the tiles covering the
+ *     output); a failed assertion returns CONV_ERR_INTERNAL with the
+ *     condition in conv_last_error(), and nothing is launched.
+ *   - Device: every global index a kernel forms for x, w, bias, y or a
+ *     workspace (and the shared-memory index of the staged copies) is tested
+ *     against the extent of that tensor as the launch sees it.  An index
+ *     outside it sets a bit of the status word (above), the first such index
+ *     is kept, and the access is skipped (a load yields 0, a store or copy is
+ *     dropped): no kernel traps, and nothing outside a tensor is touched.
+ */
+#define CONV_BUILD_DEBUG 1
+/* CONV_BUILD_DEBUG when this library is the debug build, else 0. */
+CONVFWD_API int conv_build_flags(void);
+/* Debug build: the element index that the most recent conv_device_status()
+ * call found first out of range (-1: none).  CONV_ERR_UNSUPPORTED (and -1) in
+ * the release build; CONV_ERR_NULL when index is NULL. */
+CONVFWD_API int conv_debug_first_bad_index(long long *index);
+/* Debug-build test hook (the paper has no counterpart): the extent of x that
+ * the device checks allow is reduced by `elems` elements for launches made
+ * after the call (0 restores it), so that reads of the last elements of x --
+ * which exist -- register as out of range and are skipped.  A test of the
+ * checks that never touches memory outside a tensor.  Process-wide; set it
+ * only while no other thread launches convolutions.  CONV_ERR_ARG for elems <
+ * 0; CONV_ERR_UNSUPPORTED in the release build. */
+CONVFWD_API int conv_debug_shrink_bounds(long long elems);
 
 #ifdef __cplusplus
 }

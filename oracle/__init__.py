@@ -66,6 +66,19 @@ def _i64(seq):
     return np.ascontiguousarray(np.asarray(seq, dtype=np.int64))
 
 
+def _per_dim(v, nd):
+    """A hyper-parameter as nd int64 values: an int applies to every dim; a sequence must have nd entries
+    (the C routines read exactly nd)."""
+    a = np.atleast_1d(np.asarray(v, dtype=np.int64))
+    if a.ndim != 1:
+        raise OracleError("hyper-parameters must be an int or a flat sequence")
+    if a.size == 1 and nd > 1:
+        a = np.repeat(a, nd)
+    if a.size != nd:
+        raise OracleError(f"expected {nd} values per hyper-parameter, got {a.size}")
+    return np.ascontiguousarray(a)
+
+
 def _f32(a):
     a = np.ascontiguousarray(a, dtype=np.float32)
     return a
@@ -82,7 +95,7 @@ class OracleError(ValueError):
 def out_dims(in_dims, k, stride, pad, dilation):
     """Output size per dim: floor((L + 2p - d(k-1) - 1)/s) + 1 (may be <= 0)."""
     nd = len(in_dims)
-    arrs = [_i64(v) for v in (in_dims, k, stride, pad, dilation)]
+    arrs = [_per_dim(v, nd) for v in (in_dims, k, stride, pad, dilation)]
     out = np.zeros(nd, np.int64)
     if _load().oracle_out_dims(nd, *[_ptr(a) for a in arrs], _ptr(out)):
         raise OracleError("bad conv hyper-parameters")
@@ -99,7 +112,7 @@ def conv_nd(x, w, bias, stride, pad, dilation, nthreads=None, groups=1):
     if groups < 1 or C_in % groups or C_out % groups or w.shape[1] * groups != C_in or w.ndim != x.ndim:
         raise OracleError("weight shape mismatch")
     ins, ks = _i64(x.shape[2:]), _i64(w.shape[2:])
-    s, p, d = _i64(stride), _i64(pad), _i64(dilation)
+    s, p, d = _per_dim(stride, nd), _per_dim(pad, nd), _per_dim(dilation, nd)
     od = out_dims(x.shape[2:], w.shape[2:], stride, pad, dilation)
     if min(od) <= 0:
         raise OracleError("non-positive output size")
@@ -119,7 +132,7 @@ def conv_nd_at(x, w, bias, stride, pad, dilation, flat_idx, nthreads=None, group
     N, C_in = x.shape[:2]
     C_out = w.shape[0]
     ins, ks = _i64(x.shape[2:]), _i64(w.shape[2:])
-    s, p, d = _i64(stride), _i64(pad), _i64(dilation)
+    s, p, d = _per_dim(stride, nd), _per_dim(pad, nd), _per_dim(dilation, nd)
     idx = _i64(flat_idx)
     out = np.empty(idx.shape, np.float64)
     rc = _load().oracle_conv_nd_grouped_at(_ptr(x), _ptr(w), _ptr(b), nd, N, C_in, C_out, groups, _ptr(ins),
@@ -134,7 +147,7 @@ def input_read_counts(in_dims, k, stride, pad, dilation):
     """int64 array over the input positions of one channel: how many (output, tap) pairs read each."""
     nd = len(in_dims)
     counts = np.zeros(tuple(int(v) for v in in_dims), np.int64)
-    arrs = [_i64(v) for v in (in_dims, k, stride, pad, dilation)]
+    arrs = [_per_dim(v, nd) for v in (in_dims, k, stride, pad, dilation)]
     if _load().oracle_input_read_counts(nd, *[_ptr(a) for a in arrs], _ptr(counts)):
         raise OracleError("bad conv hyper-parameters")
     return counts

@@ -27,3 +27,18 @@ def pytest_collection_modifyitems(config, items):
     for it in items:
         if "gpu" in it.keywords:
             it.add_marker(skip)
+
+
+@pytest.fixture(autouse=True)
+def _debug_build_bounds_clean(request):
+    """With CONVFWD_DEBUG=1 (the debug build loaded), every GPU test must leave no
+    out-of-range index in the device status word."""
+    yield
+    if "gpu" not in request.node.keywords or os.environ.get("CONVFWD_DEBUG", "") in ("", "0"):
+        return
+    import implicit_gemm_convolution_fwd_gb300 as cf
+    if not cf.is_debug_build():
+        return
+    st = cf.device_status()
+    assert not (st & cf.STATUS_BOUNDS_ANY), (
+        f"debug build: an index fell outside its tensor (status {st:#x}, first index {cf.debug_first_bad_index()})")

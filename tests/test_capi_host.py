@@ -121,9 +121,62 @@ def test_validation_statuses(lib):
 
 
 def test_status_strings(lib):
-    for s in range(6):
+    for s in range(7):
         assert lib.conv_status_string(s).decode().startswith("CONV_")
+    assert b"INTERNAL" in lib.conv_status_string(cf.CONV_ERR_INTERNAL)
     assert b"unknown" in lib.conv_status_string(99)
+
+
+@pytest.fixture(scope="module")
+def debug_lib():
+    """The debug build (-DCONVFWD_DEBUG), loaded beside the release one (its own handle)."""
+    from implicit_gemm_convolution_fwd_gb300 import build_lib
+    d = ctypes.CDLL(build_lib.build(debug=True))
+    for h in (d,):
+        h.conv_build_flags.restype = ctypes.c_int
+        h.conv_debug_shrink_bounds.argtypes = [ctypes.c_longlong]
+        h.conv_debug_first_bad_index.argtypes = [ctypes.POINTER(ctypes.c_longlong)]
+        h.conv_last_error.restype = ctypes.c_char_p
+    return d
+
+
+def test_debug_library_exports_every_declared_symbol(debug_lib):
+    for name in declared_functions():
+        assert hasattr(debug_lib, name), name
+
+
+def test_build_flags_tell_the_builds_apart(lib, debug_lib):
+    assert lib.conv_build_flags() == 0
+    assert debug_lib.conv_build_flags() == cf.CONV_BUILD_DEBUG
+
+
+def test_debug_hooks(lib, debug_lib):
+    v = ctypes.c_longlong(7)
+    # release build: the hooks exist but refuse
+    assert lib.conv_debug_shrink_bounds(5) == cf.CONV_ERR_UNSUPPORTED
+    assert b"CONVFWD_DEBUG" in lib.conv_last_error()
+    assert lib.conv_debug_first_bad_index(ctypes.byref(v)) == cf.CONV_ERR_UNSUPPORTED and v.value == -1
+    assert lib.conv_debug_first_bad_index(None) == cf.CONV_ERR_NULL
+    # debug build: nothing recorded yet; the shrink takes non-negative counts
+    v.value = 7
+    assert debug_lib.conv_debug_first_bad_index(ctypes.byref(v)) == cf.CONV_OK and v.value == -1
+    assert debug_lib.conv_debug_shrink_bounds(-1) == cf.CONV_ERR_ARG
+    assert debug_lib.conv_debug_shrink_bounds(3) == cf.CONV_OK
+    assert debug_lib.conv_debug_shrink_bounds(0) == cf.CONV_OK
+
+
+def test_debug_build_validates_like_the_release_build(debug_lib):
+    dims = (ctypes.c_int64 * 3)(8, 8, 8)
+    k = (ctypes.c_int64 * 3)(3, 3, 3)
+    one = (ctypes.c_int64 * 3)(1, 1, 1)
+    zero = (ctypes.c_int64 * 3)(0, 0, 0)
+    vp = ctypes.c_void_p
+    f = debug_lib.conv_fwd_nd
+    f.argtypes = [vp, vp, vp, vp, ctypes.c_int, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64] + \
+        [ctypes.POINTER(ctypes.c_int64)] * 5 + [vp]
+    # NULL x with N > 0, then a C_in of 0: refused on the host, as in the release build
+    assert f(None, vp(0x1000), None, vp(0x2000), 3, 1, 2, 4, dims, k, one, zero, one, None) == cf.CONV_ERR_NULL
+    assert f(vp(0x1000), vp(0x1000), None, vp(0x2000), 3, 1, 0, 4, dims, k, one, zero, one, None) == cf.CONV_ERR_ARG
 
 
 def test_fused_validation_statuses(lib):
@@ -299,3 +352,27 @@ def test_workspace_bindings_check_groups_and_out(lib):
     cf._check_groups(4, 6, 2, 2)
     with pytest.raises(ValueError, match="CUDA tensors"):
         cf.conv_fwd_nd_noalloc(x, torch.zeros((6, 4, 3)))
+
+
+FORCE_PROBE = r"""
+import implicit_gemm_convolution_fwd_gb300 as cf
+head = cf.select_algo(16, 3, 64, (64, 64, 64), (3, 5, 7))       # the planner: tensor cores
+small = cf.select_algo(2, 4, 8, (1024,), (3,), 3, 0, 4)         # the planner: FFMA direct
+print(head, small)
+"""
+
+
+@pytest.mark.parametrize("value,expect", [
+    ("", (cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_DIRECT_FFMA)),
+    ("direct_ffma", (cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_DIRECT_FFMA)),
+    ("igemm_3xtf32", (cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_IGEMM_3XTF32)),
+    ("bogus", (cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_DIRECT_FFMA)),
+])
+def test_force_algo_environment_variable(lib, value, expect):
+    # read once per process, so each setting gets a process of its own
+    env = dict(os.environ, CONVFWD_FORCE_ALGO=value)
+    r = subprocess.run([sys.executable, "-c", FORCE_PROBE], env=env, cwd=ROOT, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert tuple(int(v) for v in r.stdout.split()) == expect
+    assert ("ignored" in r.stderr) == (value == "bogus")

@@ -431,3 +431,18 @@ def test_matches_dense_im2col_formulation(seed):
     got = oracle.conv_nd(x, w, b, s, p, d, groups=groups)
     assert got.shape == ref.shape
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+
+
+def test_per_dim_hyper_parameters_broadcast_or_must_match_the_rank():
+    # an int applies to every dim; a sequence of the wrong length is refused
+    # (the C routines read exactly one value per dim)
+    x = np.arange(2 * 3 * 5 * 6 * 7, dtype=np.float32).reshape(2, 3, 5, 6, 7) / 100
+    w = np.ones((4, 3, 2, 2, 2), np.float32)
+    a = oracle.conv_nd(x, w, None, 1, 0, 1)
+    b = oracle.conv_nd(x, w, None, (1, 1, 1), (0, 0, 0), (1, 1, 1))
+    assert np.array_equal(a, b)
+    assert oracle.out_dims((5, 6, 7), 2, 1, 0, 1) == (4, 5, 6)
+    with pytest.raises(oracle.OracleError):
+        oracle.conv_nd(x, w, None, (1, 1), 0, 1)
+    with pytest.raises(oracle.OracleError):
+        oracle.out_dims((5, 6, 7), (2, 2), 1, 0, 1)
