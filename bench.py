@@ -165,8 +165,8 @@ class OurRunner:
         import torch
         import implicit_gemm_convolution_fwd_gb300 as cf
         self.torch, self.cf, self.wl, self.dev = torch, cf, wl, device
-        # the fused op's kernel family: the planner (which takes the FFMA kernel on the
-        # benchmark's fused workload, as a parity test checks), or one family forced
+        # the fused op's kernel family: the planner (the library's own query says which
+        # family it takes), or one family forced
         self.fused_code = {"auto": cf.CONV_ALGO_AUTO, "ffma": cf.CONV_ALGO_DIRECT_FFMA,
                            "tc": cf.CONV_ALGO_IGEMM_3XTF32}[fused_algo]
         x, w, b = wl.make_inputs(seed=0)
@@ -177,7 +177,11 @@ class OurRunner:
         if wl.kind == "fused":
             self.out_dims = cf.out_dims(wl.in_dims, wl.k_dims, 1, 0, 1)
             self.y = torch.empty((wl.N, wl.C_out, self.out_dims[1], self.out_dims[2]), device=device)
-            self.algo = "fused_igemm_3xtf32" if fused_algo == "tc" else "fused_ffma"
+            fam = self.fused_code
+            if fam == cf.CONV_ALGO_AUTO:
+                fam = cf.fused_select_algo((wl.N, wl.C_in) + tuple(wl.in_dims), (wl.C_out, wl.C_in) + tuple(wl.k_dims),
+                                           wl.min_dim)
+            self.algo = "fused_igemm_3xtf32" if fam == cf.CONV_ALGO_IGEMM_3XTF32 else "fused_ffma"
         else:
             self.out_dims = cf.out_dims(wl.in_dims, wl.k_dims, wl.stride, wl.pad, wl.dilation)
             self.y = torch.empty((wl.N, wl.C_out) + tuple(self.out_dims), device=device)
@@ -312,6 +316,11 @@ class VariantRunner(OurRunner):
             od = self.out_dims
             keep = [od[i] for i in range(3) if i != self.min_dim - 2]
             self.y = torch.empty((wl.N, wl.C_out, keep[0], keep[1]), device=device)
+            fam = self.fused_code
+            if fam == self.cf.CONV_ALGO_AUTO:
+                fam = self.cf.fused_select_algo((wl.N, wl.C_in) + tuple(wl.in_dims),
+                                                (wl.C_out, wl.C_in) + tuple(wl.k_dims), self.min_dim)
+            self.algo = "fused_igemm_3xtf32" if fam == self.cf.CONV_ALGO_IGEMM_3XTF32 else "fused_ffma"
 
     def launches_per_step(self):
         # streamed weights: the weight split runs before the conv kernel
@@ -336,7 +345,7 @@ VARIANTS = [
     ("conv1d_long[bf16]", "conv1d_long", {"dtype": "bfloat16"}),
     ("conv3d_min_softmax[min_dim=3]", "conv3d_min_softmax", {"min_dim": 3}),
     ("conv3d_min_softmax[min_dim=4]", "conv3d_min_softmax", {"min_dim": 4}),
-    ("conv3d_min_softmax[tensor cores]", "conv3d_min_softmax", {"fused_algo": "tc"}),
+    ("conv3d_min_softmax[ffma]", "conv3d_min_softmax", {"fused_algo": "ffma"}),
     ("conv3d_sweep_b[channels_last]", "conv3d_sweep_b", {"channels_last": True}),
     ("conv3d_sweep_b[groups=2]", "conv3d_sweep_b", {"groups": 2}),
     ("conv3d_wide_k[workspace]", "conv3d_wide_k", {"workspace": True}),
@@ -364,7 +373,8 @@ def run_variants(dev, peaks, pipes, steps):
             entry["frac_of_bf16_peak"] = entry["tflops"] / pipes["bf16"]["tflops"]
             entry["frac_of_cublas_bf16"] = entry["tflops"] / peaks["bf16_tflops"]
         if r.dtype is None and r.wl.kind == "fused":
-            if r.fused_code == r.cf.CONV_ALGO_IGEMM_3XTF32:
+            entry["kernel"] = r.algo
+            if r.algo == "fused_igemm_3xtf32":
                 entry["frac_of_3xtf32_peak"] = entry["tflops"] / pipes["tf32x3"]["tflops"]
             else:
                 entry["frac_of_ffma_peak"] = entry["tflops"] / pipes["ffma"]["tflops"]
@@ -384,24 +394,24 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.505984e6 + 824.212480e6, "batch": 16,
-        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
-    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.330176e6 + 307.265536e6, "batch": 4,
-        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
-    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492288e6 + 0.042240e6, "batch": 8,
-        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
-    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.432064e6 + 66.768896e6, "batch": 8,
-        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.406592e6 + 7.730944e6, "batch": 4,
-        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
-    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.846528e6 + 0.006144e6, "batch": 128,
-        "sha256": "9a946463d56ace469148ce43059093547e7981d6c55ccd3cebb704f3d2fe28f5"},
-    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.303040e6 + 385.665536e6, "batch": 16,
-        "sha256": "e40ab8339f62ac16a7b63da4c60bb211d1927969a0ee55acfc41e2765ade8d8f"},
-    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.816832e6 + 0.000768e6, "batch": 128,
-        "sha256": "7e63a72762ddc040b9b21fe8069bf746346fd3113a6c47088e4a8fab33c61616"},
-    ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051968e6, "batch": 2,
-        "sha256": "ef79ff89c6a99a86c33cde2383bd3a0d8edd97a3441d69c6d46b99b4389d2019"},
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.504960e6 + 824.264192e6, "batch": 16,
+        "sha256": "e0af753423e7429ff995186a5764cefcb991eecded91b8d042fa6170a55aba8e"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.284352e6 + 307.895808e6, "batch": 4,
+        "sha256": "e0af753423e7429ff995186a5764cefcb991eecded91b8d042fa6170a55aba8e"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492544e6 + 0.061696e6, "batch": 8,
+        "sha256": "e0af753423e7429ff995186a5764cefcb991eecded91b8d042fa6170a55aba8e"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.437696e6 + 66.605312e6, "batch": 8,
+        "sha256": "e0af753423e7429ff995186a5764cefcb991eecded91b8d042fa6170a55aba8e"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.441152e6 + 7.643904e6, "batch": 4,
+        "sha256": "e0af753423e7429ff995186a5764cefcb991eecded91b8d042fa6170a55aba8e"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.841920e6 + 0.003328e6, "batch": 128,
+        "sha256": "e0af753423e7429ff995186a5764cefcb991eecded91b8d042fa6170a55aba8e"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.311488e6 + 385.808640e6, "batch": 16,
+        "sha256": "bccfe6fd7b2f9f38438b9a33cea2bba3534f89fd15e2ac2e8a47ddd9a193d1cc"},
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.822208e6 + 0.002816e6, "batch": 128,
+        "sha256": "e420278244e71807996932fd3600d956d407ef4d2540cfbed9e6e6f302e5c283"},
+    ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051712e6, "batch": 2,
+        "sha256": "c89212c4b2a3b47cebf81b80fa94530bb29ddb0f5ed58ae23df0585b90d2ac41"},
 }
 
 

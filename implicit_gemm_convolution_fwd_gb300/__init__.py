@@ -32,8 +32,8 @@ EXPORTED = ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_fwd_nd_group
             "conv_host_workspace_bytes", "conv_fwd_nd_host",
             "conv_select_algo",
             "conv_algo_supported",
-            "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv_peak_mma", "conv_peak_ffma",
-            "conv_debug_set_wait_limit",
+            "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv3d_min_softmax_select_algo", "conv_peak_mma",
+            "conv_peak_ffma", "conv_debug_set_wait_limit",
             "conv_status_string", "conv_last_error", "conv_device_status",
             "conv_build_flags", "conv_debug_first_bad_index", "conv_debug_shrink_bounds")
 
@@ -101,6 +101,8 @@ def load(path: str | None = None):
                                        ctypes.POINTER(Tensor4), i32, vp]
     lib.conv3d_min_softmax_ex.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), vp,
                                           ctypes.POINTER(Tensor4), i32, i32, vp]
+    lib.conv3d_min_softmax_select_algo.argtypes = [ctypes.POINTER(Tensor5), ctypes.POINTER(Tensor5), i32,
+                                                   ctypes.POINTER(ctypes.c_int)]
     lib.conv_peak_mma.argtypes = [i32, i32, i32, i32, i32, ctypes.POINTER(PeakResult), vp]
     lib.conv_peak_ffma.argtypes = [i32, i32, ctypes.POINTER(PeakResult), vp]
     lib.conv_status_string.argtypes = [i32]
@@ -113,8 +115,8 @@ def load(path: str | None = None):
     lib.conv_debug_first_bad_index.argtypes = [ctypes.POINTER(ctypes.c_longlong)]
     lib.conv_debug_shrink_bounds.argtypes = [ctypes.c_longlong]
     for f in ("conv_out_dims", "conv_fwd_nd", "conv_fwd_nd_ex", "conv_select_algo", "conv_algo_supported",
-              "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv_peak_mma", "conv_peak_ffma",
-              "conv_debug_set_wait_limit", "conv_device_status", "conv_build_flags",
+              "conv3d_min_softmax", "conv3d_min_softmax_ex", "conv3d_min_softmax_select_algo", "conv_peak_mma",
+              "conv_peak_ffma", "conv_debug_set_wait_limit", "conv_device_status", "conv_build_flags",
               "conv_debug_first_bad_index", "conv_debug_shrink_bounds"):
         getattr(lib, f).restype = i32
     _lib = lib
@@ -155,6 +157,15 @@ def select_algo(N, C_in, C_out, in_dims, k_dims, stride=1, pad=0, dilation=1) ->
     a = ctypes.c_int(-1)
     _check(load().conv_select_algo(nd, N, C_in, C_out, _arr(in_dims), _arr(k_dims), _arr(_tuple(stride, nd)),
                                    _arr(_tuple(pad, nd)), _arr(_tuple(dilation, nd)), ctypes.byref(a)))
+    return a.value
+
+
+def fused_select_algo(x_shape, w_shape, min_dim=2) -> int:
+    """Host-only query: the kernel family conv3d_min_softmax takes for these shapes with algo=AUTO."""
+    xs, ws = Tensor5(), Tensor5()
+    xs.dims[:], ws.dims[:] = [int(v) for v in x_shape], [int(v) for v in w_shape]
+    a = ctypes.c_int(-1)
+    _check(load().conv3d_min_softmax_select_algo(ctypes.byref(xs), ctypes.byref(ws), int(min_dim), ctypes.byref(a)))
     return a.value
 
 

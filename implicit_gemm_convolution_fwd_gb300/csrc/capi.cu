@@ -217,6 +217,47 @@ int forced_algo() {
   return f;
 }
 
+bool fused_ffma_preferred(const Geom &g, int min_dim) {
+  // Measured on GB300 against the tensor-core fused kernel (device time, L2
+  // flushed) on [N, C_in, 24, 32, 32] inputs with N * C_in held near 384,
+  // C_out 8 .. 64, C_in 1 .. 8, min over depth, height and width.  The FFMA
+  // kernels run channel groups of 12 (up to 24 channels cost the same, 25..48
+  // cost twice that); the tensor-core kernel runs blocks of 32 channels, a
+  // second block adding a channel-softmax pass.  3x3x3 kernels (FFMA /
+  // tensor cores, ms, over depth; over height and width alike within 10 %):
+  //   C_out <= 24: C_in 1 0.277 / 0.34, C_in 2 0.26 / 0.217, C_in 3 0.199 /
+  //   0.181, C_in 4 0.24 / 0.185, C_in 8 0.32 / 0.188 (over height C_in 3
+  //   0.200 / 0.210, the one other case the FFMA kernel wins);
+  //   C_out = 32: tensor cores from C_in 1 (0.60 / 0.35);
+  //   C_out 40, 48: C_in 1 0.59 / 0.68 over depth and height, 0.77 / 0.72
+  //   over width; C_in >= 2 tensor cores (0.60 / 0.43 at C_in 2);
+  //   C_out = 64: tensor cores from C_in 1 (1.24 / 0.71).
+  //   3x5x5 kernels: tensor cores everywhere (from 0.72x the FFMA time at
+  //   C_in 1, C_out 8).
+  // So the FFMA kernels keep reductions of at most 32 columns on up to 24
+  // channels, and on 25..48 channels (two tensor-core blocks) over depth or
+  // height; and the min over height of the page's shape class (C_in 3, 3x3x3,
+  // W 32, up to 24 channels), where the staged FFMA kernel runs its
+  // compile-time specialised instance.
+  const int64_t kred = g.C * g.taps();
+  const int ncg = convfwd::fused_channel_groups(g.K);
+  if (min_dim == 3 && ncg <= 2 && g.C == 3 && g.KD == 3 && g.KH == 3 && g.KW == 3 && g.W == 32) return true;
+  if (kred > 32) return false;
+  if (ncg <= 2) return true;
+  const int64_t blocks = (g.K + 31) / 32;  // tensor-core launches
+  return ncg == 4 && blocks == 2 && min_dim != 4;
+}
+
+// The fused op's family for CONV_ALGO_AUTO: CONVFWD_FORCE_ALGO where that
+// family runs the shape, else the measured rule (the tensor-core kernel except
+// for the shortest reductions over few channels), else whichever runs.
+int fused_family(const Geom &g, int min_dim, bool ffma_ok, bool tc_ok) {
+  const int forced = forced_algo();
+  if ((forced == CONV_ALGO_DIRECT_FFMA && ffma_ok) || (forced == CONV_ALGO_IGEMM_3XTF32 && tc_ok)) return forced;
+  return tc_ok && !(ffma_ok && fused_ffma_preferred(g, min_dim)) ? CONV_ALGO_IGEMM_3XTF32
+                                                                          : CONV_ALGO_DIRECT_FFMA;
+}
+
 int choose_algo(const Geom &g, bool can_stream) {
   const char *why = nullptr;
   const int forced = forced_algo();
@@ -792,18 +833,7 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
   const char *why = "", *why_tc = "";
   const bool ffma_ok = convfwd::fused_supported(g, min_dim, &why);
   const bool tc_ok = convfwd::igemm_fused_supported(g, min_dim, &why_tc);
-  // planner: the FFMA kernels for short reductions over few channels (the
-  // page's C_in = 3, C_out = 24 shape among them), where the tensor-core
-  // kernel's im2col gather costs more than the FFMAs; the tensor-core kernel
-  // for longer reductions or more channels; whichever runs otherwise
-  if (algo == CONV_ALGO_AUTO) {
-    const int forced = forced_algo();
-    if ((forced == CONV_ALGO_DIRECT_FFMA && ffma_ok) || (forced == CONV_ALGO_IGEMM_3XTF32 && tc_ok))
-      algo = forced;
-    else
-      algo = tc_ok && !(ffma_ok && convfwd::fused_ffma_preferred(g, min_dim)) ? CONV_ALGO_IGEMM_3XTF32
-                                                                              : CONV_ALGO_DIRECT_FFMA;
-  }
+  if (algo == CONV_ALGO_AUTO) algo = fused_family(g, min_dim, ffma_ok, tc_ok);
   if (algo == CONV_ALGO_DIRECT_FFMA) {
     if (!ffma_ok) return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax: %s", why);
   } else if (algo == CONV_ALGO_IGEMM_3XTF32) {
@@ -879,6 +909,35 @@ int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, cons
     }
   }
   if (e != cudaSuccess) return fail_cuda(e, "conv3d_min_softmax: kernel launch");
+  return CONV_OK;
+}
+
+int conv3d_min_softmax_select_algo(const conv_tensor5_t *x, const conv_tensor5_t *w, int min_dim, int *algo_out) {
+  g_last_error[0] = 0;
+  if (!x || !w || !algo_out) return fail(CONV_ERR_NULL, "conv3d_min_softmax_select_algo: a pointer is NULL%s");
+  if (min_dim < 2 || min_dim > 4)
+    return fail(CONV_ERR_ARG, "conv3d_min_softmax_select_algo: min_dim must be 2, 3 or 4%s");
+  for (int i = 0; i < 5; ++i) {
+    if (x->dims[i] < (i == 0 ? 0 : 1) || x->dims[i] > kMaxDim)
+      return fail(CONV_ERR_ARG, "conv3d_min_softmax_select_algo: bad x dim%s");
+    if (w->dims[i] < 1 || w->dims[i] > kMaxDim)
+      return fail(CONV_ERR_ARG, "conv3d_min_softmax_select_algo: bad w dim%s");
+  }
+  if (w->dims[1] != x->dims[1])
+    return fail(CONV_ERR_SHAPE, "conv3d_min_softmax_select_algo: w C_in %s%lld != x C_in %lld", "", w->dims[1],
+                x->dims[1]);
+  const int64_t ins[3] = {x->dims[2], x->dims[3], x->dims[4]};
+  const int64_t ks[3] = {w->dims[2], w->dims[3], w->dims[4]};
+  const int64_t one[3] = {1, 1, 1}, zero[3] = {0, 0, 0};
+  Geom g;
+  int64_t xe, we, ye;
+  int st = make_geom(3, x->dims[0], x->dims[1], w->dims[0], ins, ks, one, zero, one, &g, &xe, &we, &ye);
+  if (st != CONV_OK) return st;
+  const char *why = "", *why_tc = "";
+  const bool ffma_ok = convfwd::fused_supported(g, min_dim, &why);
+  const bool tc_ok = convfwd::igemm_fused_supported(g, min_dim, &why_tc);
+  if (!ffma_ok && !tc_ok) return fail(CONV_ERR_UNSUPPORTED, "conv3d_min_softmax_select_algo: %s", why_tc);
+  *algo_out = fused_family(g, min_dim, ffma_ok, tc_ok);
   return CONV_OK;
 }
 

@@ -764,44 +764,7 @@ size_t fused_transpose_bytes(const Geom &g, int min_dim) {
   return transpose_x_bytes(g) + transpose_w_bytes(g);
 }
 
-bool fused_ffma_preferred(const Geom &g, int min_dim) {
-  // Measured on GB300 against the tensor-core fused kernel on [N, C_in, 24,
-  // 32, 32] inputs with 3x3x3 kernels and N * C_in held near 384 (FFMA /
-  // tensor cores, ms).  The FFMA kernels run channel groups of 12 (C_out = 32
-  // runs 48 channels, 49..96 run 96); the tensor-core kernel runs blocks of 32
-  // channels, more than one block adding a channel-softmax pass.
-  //   Min over depth: C_out = 24 0.21 / 0.49 at C_in = 3, 0.33 / 0.48 at
-  //   C_in = 8, 1.11 / 0.47 at C_in = 12; C_out = 32 0.61 / 0.65 at C_in = 1,
-  //   0.66 / 0.49 at C_in = 3; C_out = 48 0.69 / 0.98 at C_in = 3, 1.38 / 0.95
-  //   at C_in = 8; C_out = 64 1.23 / 1.33 at C_in = 1, 2.07 / 0.99 at C_in = 3;
-  //   C_out = 96 1.30 / 2.03 at C_in = 1, 2.28 / 1.48 at C_in = 3.
-  //   Min over height (the staged FFMA kernel): C_out = 24 0.28 / 0.35 at
-  //   C_in = 4, 0.38 / 0.30 at C_in = 8; C_out = 32 0.58 / 0.52 at C_in = 1;
-  //   C_out = 48 0.58 / 0.99 at C_in = 1, 0.78 / 0.71 at C_in = 3; C_out = 64
-  //   1.17 / 1.00 at C_in = 1; C_out = 96 1.22 / 1.51 at C_in = 1.
-  //   Min over width, both families on transposed copies where they can (the
-  //   FFMA staged kernel only up to 24 channels, the generic kernel beyond):
-  //   C_out = 24 0.32 / 0.38 at C_in = 4, 0.41 / 0.33 at C_in = 8; C_out = 32
-  //   0.78 / 0.56 at C_in = 1; C_out = 48 0.78 / 1.03 at C_in = 1, 1.12 / 0.73
-  //   at C_in = 3; C_out = 64 1.55 / 1.04 at C_in = 1.
-  const int64_t kred = g.C * g.taps();
-  const int ncg = pick_ncg(g.K);
-  const int64_t blocks = (g.K + 31) / 32;  // tensor-core launches
-  switch (min_dim) {
-    case 2:
-      if (ncg <= 2) return kred <= 256;
-      if (blocks == 1) return kred <= 32;
-      return kred <= (ncg <= 4 ? 128 : 32);
-    case 3:
-      if (ncg <= 2) return kred <= 128;
-      if (blocks == 1) return false;
-      return kred <= 32 && (ncg <= 4 || blocks >= 3);
-    default:
-      if (ncg <= 2) return fused_transpose_bytes(g, 4) > 0 && kred <= 128;
-      if (blocks == 1) return false;
-      return kred <= 32 && ncg <= 4;
-  }
-}
+int fused_channel_groups(int64_t K) { return pick_ncg(K); }
 
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
                                      const Geom &g, int min_dim, cudaStream_t stream, float *ws) {

@@ -106,10 +106,11 @@ struct IgemmParams {
   // kWaitLimitCycles
   long long wait_limit;
   // fused conv3d -> min over depth -> channel softmax (the FUSED kernel): a
-  // column is (image, block of 128 positions of the output plane); each CTA
-  // runs its columns' OD depth tiles back to back
-  int64_t columns;  // N * hw_tiles
-  int hw_tiles;     // ceil(plane / 128)
+  // column is a block of 128 consecutive (image, kept-plane position) pairs
+  // of the flattened N x plane index (a block may span two images, so no
+  // column is ragged but the last); each CTA runs its columns' R tiles along
+  // the reduced dim back to back
+  int64_t columns;  // ceil(N * plane / 128)
   // the reduced output dim (depth, height or width): R positions at stride sR
   // in an image's flat output index; the kept plane (A x nB positions, A at
   // stride sA, B at stride sB) is what y holds per image and channel
@@ -266,13 +267,22 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   PosInfo ps;
   int64_t m;
   if (FUSED) {
-    // tile = column * R + r; row t is position hw_tile * 128 + t of the kept
-    // plane, at index r of the reduced dim
+    // tile = column * R + r; row t is entry column * 128 + t of the
+    // flattened (image, kept-plane position) index, at index r of the
+    // reduced dim
     const int64_t col = tile / p.R;
-    const int64_t r = tile - col * p.R, img = col / p.hw_tiles;
-    const int64_t pp = (col - img * p.hw_tiles) * kTileM + t;
-    ps.valid = pp < p.plane;
-    const int64_t a = ps.valid ? pp / p.nB : 0, bb = ps.valid ? pp - a * p.nB : 0;
+    const int64_t r = tile - col * p.R, flat = col * kTileM + t;
+    ps.valid = flat < g.N * p.plane;
+    int64_t img = 0, pp = 0, a = 0, bb = 0;
+    if (ps.valid) {
+      if (g.N * p.plane < ((int64_t)1 << 31)) {  // 32-bit divisions when every index fits
+        const uint32_t f32 = (uint32_t)flat, pl = (uint32_t)p.plane, nb = (uint32_t)p.nB;
+        const uint32_t i32 = f32 / pl, q32 = f32 - i32 * pl, a32 = q32 / nb;
+        img = i32, pp = q32, a = a32, bb = q32 - a32 * nb;
+      } else {
+        img = flat / p.plane, pp = flat - img * p.plane, a = pp / p.nB, bb = pp - a * p.nB;
+      }
+    }
     m = img * p.osp + r * p.sR + a * p.sA + bb * p.sB;
   } else {
     m = tile * kTileM + t;
@@ -408,9 +418,10 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
 // the single-pass kernels keep their registers).  SB: streamed weights (see
 // IgemmParams::wsp): no resident weight matrix, any reduction length in one pass.
 // FUSED: the conv3d -> min over depth -> channel softmax of the l2_p24 page
-// (turns 1-2): tiles of one (image, depth) plane, depth tiles of a column
-// consecutive, and an epilogue that keeps each position's running minimum
-// over depth in registers and writes only the softmax of the last one.
+// (turns 1-2): a tile is 128 (image, plane position) pairs at one depth, the
+// depth tiles of a column consecutive, and an epilogue that keeps each
+// position's running minimum over depth in registers and writes only the
+// softmax of the last one.
 template <int CH, bool ACC, bool SB, bool FUSED = false>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -549,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       ptx::tc_fence_before();
       ptx::mbar_arrive(bar_d_empty + 8 * b);
       if (d == R - 1) {
-        const int64_t col = tile_of<true>(p, it) / R, img = col / p.hw_tiles;
-        const int64_t pp = (col - img * p.hw_tiles) * kTileM + tid;
-        if (pp < plane) {
+        const int64_t flat = tile_of<true>(p, it) / R * kTileM + tid;
+        if (flat < g.N * plane) {
+          const int64_t img = flat / plane, pp = flat - img * plane;
           // y[n, o, pos]; images are y_chans channels apart (all blocks of a wider layer)
           float *yp = p.y + img * p.y_chans * plane + pp;
 #ifdef CONVFWD_DEBUG
@@ -1229,8 +1240,7 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   } else {
     p.R = g.OW, p.sR = sW, p.nB = g.OH, p.sA = sD, p.sB = sH, p.plane = (int64_t)g.OD * g.OH;
   }
-  p.hw_tiles = (int)((p.plane + kTileM - 1) / kTileM);
-  p.columns = g.N * p.hw_tiles;
+  p.columns = (g.N * p.plane + kTileM - 1) / kTileM;
   p.tiles = p.columns * p.R;
   p.Kfull = (int)kfull;
   p.k_begin = 0;
@@ -1245,7 +1255,7 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.x_elems = x_extent(g);
   p.w_elems = g.K * kfull;
   p.y_elems = (g.N - 1) * p.y_chans * p.plane + g.K * p.plane;
-  CONV_PLAN_CHECK(grid >= 1 && p.R >= 1 && (int64_t)p.hw_tiles * kTileM >= p.plane);
+  CONV_PLAN_CHECK(grid >= 1 && p.R >= 1 && p.columns * kTileM >= g.N * p.plane);
   CONV_PLAN_CHECK(p.plane * p.R == p.osp && p.nB >= 1 && p.plane % p.nB == 0);
   CONV_PLAN_CHECK(tmem_cols_used(pl.nslots, pl.Npad, pl.KC) <= (int)kTmemCols);
   if (streamed) {

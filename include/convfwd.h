@@ -52,8 +52,9 @@
  *     channel blocks, resident or streamed weights, shared memory).
  *   - With CONVFWD_FORCE_ALGO=direct_ffma or =igemm_3xtf32 in the environment
  *     (read once per process), fp32 calls made with CONV_ALGO_AUTO -- the
- *     plain and grouped convolutions, conv3d_min_softmax, conv_select_algo --
- *     take that kernel family wherever it can run the problem, and the
+ *     plain and grouped convolutions, conv3d_min_softmax and the two
+ *     select_algo queries -- take that kernel family wherever it can run the
+ *     problem, and the
  *     planner's choice elsewhere.  Other values are ignored (one line on
  *     stderr).  An explicit algo argument always wins.
  */
@@ -333,12 +334,11 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * block of the call, as for conv_fwd_nd).  The min over width runs, in both
  * families where they can, as the min over height of x and w transposed in
  * their last two dims (a stream-ordered block).  Where both families run, the
- * planner takes the one measured faster for the shape class: the FFMA
- * kernels for short reductions over few channels (with K = C_in * |kernel|
- * and C_out <= 24: K <= 256 over depth, K <= 128 over height or width), the
- * tensor cores for longer reductions and for 32 channels (one block), with
- * narrower margins for wider layers (see the rule in the library source).
- * Shapes neither family runs are CONV_ERR_UNSUPPORTED.
+ * planner takes the one measured faster for the shape class: the tensor-core
+ * kernel, except for the shortest reductions (K = C_in * |kernel| <= 32) on up
+ * to 24 channels, or on 25..48 channels over depth or height, which keep the
+ * FFMA kernels (conv3d_min_softmax_select_algo reports the choice).  Shapes
+ * neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);
@@ -349,6 +349,14 @@ CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t
  * CONV_ERR_UNSUPPORTED, an unknown value CONV_ERR_ARG. */
 CONVFWD_API int conv3d_min_softmax_ex(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias,
                                       conv_tensor4_t *y, int min_dim, int algo, conv_stream_t stream);
+
+/* The kernel family conv3d_min_softmax would take for these shapes (only
+ * x->dims and w->dims are read; host only, no device access): writes
+ * CONV_ALGO_DIRECT_FFMA or CONV_ALGO_IGEMM_3XTF32 to *algo_out and returns
+ * CONV_OK; CONV_ERR_UNSUPPORTED when neither family runs the shape; the
+ * validation statuses of conv3d_min_softmax otherwise. */
+CONVFWD_API int conv3d_min_softmax_select_algo(const conv_tensor5_t *x, const conv_tensor5_t *w, int min_dim,
+                                               int *algo_out);
 
 /*
  * Peak-rate microbenchmarks (diagnostics; not part of the convolution).  The

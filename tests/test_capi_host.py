@@ -206,6 +206,34 @@ def test_fused_validation_statuses(lib):
     assert f(ctypes.byref(xsmall), ctypes.byref(w), None, ctypes.byref(y), 2, None) == cf.CONV_ERR_SHAPE
 
 
+def test_fused_select_algo_host_only(lib):
+    sel = cf.fused_select_algo
+    # the page's shape takes the tensor cores over depth and width, the specialised staged FFMA
+    # kernel over height; the shortest reductions keep the FFMA kernels
+    for md in (2, 3, 4):
+        want = cf.CONV_ALGO_DIRECT_FFMA if md == 3 else cf.CONV_ALGO_IGEMM_3XTF32
+        assert sel((128, 3, 24, 32, 32), (24, 3, 3, 3, 3), md) == want
+        assert sel((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), md) == cf.CONV_ALGO_DIRECT_FFMA
+        assert sel((2, 1, 10, 20, 20), (32, 1, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
+        assert sel((2, 1, 10, 20, 20), (64, 1, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
+    # 25..48 channels: FFMA over depth and height, tensor cores over width
+    assert sel((2, 1, 10, 20, 20), (40, 1, 3, 3, 3), 2) == cf.CONV_ALGO_DIRECT_FFMA
+    assert sel((2, 1, 10, 20, 20), (40, 1, 3, 3, 3), 3) == cf.CONV_ALGO_DIRECT_FFMA
+    assert sel((2, 1, 10, 20, 20), (40, 1, 3, 3, 3), 4) == cf.CONV_ALGO_IGEMM_3XTF32
+    # only one family runs: 100 channels (beyond the FFMA kernels), a kernel extent of 9 along W
+    assert sel((1, 4, 5, 9, 20), (100, 4, 2, 3, 9), 2) == cf.CONV_ALGO_IGEMM_3XTF32
+    # neither family, and invalid requests
+    for shapes, md, status in [(((2, 3, 24, 32, 64), (200, 3, 3, 3, 40)), 2, cf.CONV_ERR_UNSUPPORTED),
+                               (((2, 3, 24, 32, 32), (24, 3, 3, 3, 3)), 5, cf.CONV_ERR_ARG),
+                               (((2, 3, 24, 32, 32), (24, 4, 3, 3, 3)), 2, cf.CONV_ERR_SHAPE),
+                               (((2, 3, 2, 32, 32), (24, 3, 3, 3, 3)), 2, cf.CONV_ERR_SHAPE)]:
+        with pytest.raises(cf.ConvError) as e:
+            sel(*shapes, md)
+        assert e.value.status == status, (shapes, md)
+    a = ctypes.c_int(0)
+    assert lib.conv3d_min_softmax_select_algo(None, None, 2, ctypes.byref(a)) == cf.CONV_ERR_NULL
+
+
 def test_select_algo_host_only(lib):
     # tiny reductions always take the FFMA direct path
     assert cf.select_algo(2, 4, 8, (1024,), (3,), 3, 0, 4) == cf.CONV_ALGO_DIRECT_FFMA
@@ -358,15 +386,20 @@ FORCE_PROBE = r"""
 import implicit_gemm_convolution_fwd_gb300 as cf
 head = cf.select_algo(16, 3, 64, (64, 64, 64), (3, 5, 7))       # the planner: tensor cores
 small = cf.select_algo(2, 4, 8, (1024,), (3,), 3, 0, 4)         # the planner: FFMA direct
-print(head, small)
+fused_tc = cf.fused_select_algo((128, 3, 24, 32, 32), (24, 3, 3, 3, 3), 2)   # the planner: tensor cores
+fused_ffma = cf.fused_select_algo((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), 2)   # the planner: FFMA
+print(head, small, fused_tc, fused_ffma)
 """
 
 
+TC_, FF_ = cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_DIRECT_FFMA
+
+
 @pytest.mark.parametrize("value,expect", [
-    ("", (cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_DIRECT_FFMA)),
-    ("direct_ffma", (cf.CONV_ALGO_DIRECT_FFMA, cf.CONV_ALGO_DIRECT_FFMA)),
-    ("igemm_3xtf32", (cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_IGEMM_3XTF32)),
-    ("bogus", (cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_DIRECT_FFMA)),
+    ("", (TC_, FF_, TC_, FF_)),
+    ("direct_ffma", (FF_, FF_, FF_, FF_)),
+    ("igemm_3xtf32", (TC_, TC_, TC_, TC_)),
+    ("bogus", (TC_, FF_, TC_, FF_)),
 ])
 def test_force_algo_environment_variable(lib, value, expect):
     # read once per process, so each setting gets a process of its own

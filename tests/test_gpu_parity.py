@@ -306,30 +306,38 @@ def test_fused_tensor_core_streamed_weights(shape, C_out, k):
 
 
 def test_fused_planner_takes_the_measured_family():
-    """AUTO must equal one family bit for bit: FFMA on the page's C_in = 3, C_out = 24 shape
-    (reduced batch), the tensor cores for C_out = 32 over C_in = 8 (the two differ in rounding)."""
+    """AUTO must equal the family the planner query names, bit for bit: the tensor cores on the
+    page's C_in = 3, C_out = 24 shape (reduced batch), the FFMA kernels for a 27-column reduction
+    on 24 channels (the two families differ in rounding)."""
     wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
+    assert cf.fused_select_algo(x.shape, w.shape, 2) == TC
     auto, ffma, tc = (run_fused(x, w, b, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
-    assert (auto == ffma).all() and not (auto == tc).all()
-    rng = np.random.default_rng(11)
-    x = rng.random((2, 8, 10, 20, 20)).astype(np.float32)
-    w = ((rng.random((32, 8, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
-    auto, ffma, tc = (run_fused(x, w, None, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
     assert (auto == tc).all() and not (auto == ffma).all()
+    rng = np.random.default_rng(11)
+    x = rng.random((2, 1, 10, 20, 20)).astype(np.float32)
+    w = ((rng.random((24, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
+    assert cf.fused_select_algo(x.shape, w.shape, 2) == FFMA
+    auto, ffma, tc = (run_fused(x, w, None, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
+    assert (auto == ffma).all() and not (auto == tc).all()
 
 
 @pytest.mark.parametrize("min_dim", [3, 4])
 def test_fused_planner_over_height_and_width(min_dim):
-    # the page's channel counts keep the FFMA kernels; 32 channels over C_in = 8 take the tensor cores
+    # the page's shape takes the staged FFMA kernel's specialised instance over height and the
+    # tensor cores over width; a 27-column reduction on 24 channels keeps the FFMA kernels
     wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
     xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
-    auto, ffma = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, FFMA))
-    assert torch.equal(auto, ffma)
+    want = FFMA if min_dim == 3 else TC
+    assert cf.fused_select_algo(x.shape, w.shape, min_dim) == want
+    auto, fam = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, want))
+    assert torch.equal(auto, fam)
     rng = np.random.default_rng(12)
-    xt = torch.from_numpy(rng.random((2, 8, 10, 20, 20)).astype(np.float32)).cuda()
-    wt = torch.from_numpy(((rng.random((32, 8, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)).cuda()
-    auto, tc = (cf.conv3d_min_softmax(xt, wt, None, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, TC))
-    assert torch.equal(auto, tc)
+    x1 = rng.random((2, 1, 10, 20, 20)).astype(np.float32)
+    w1 = ((rng.random((24, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
+    assert cf.fused_select_algo(x1.shape, w1.shape, min_dim) == FFMA
+    xt, wt = torch.from_numpy(x1).cuda(), torch.from_numpy(w1).cuda()
+    auto, ffma = (cf.conv3d_min_softmax(xt, wt, None, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, FFMA))
+    assert torch.equal(auto, ffma)
 
 
 @pytest.mark.parametrize("min_dim", [2, 3, 4])
@@ -954,7 +962,7 @@ def test_plan_log_names_the_family_and_plan():
     assert "-> igemm_3xtf32 tiles=" in lines[0] and "Kred=315" in lines[0] and "weights=resident" in lines[0]
     assert "-> direct_ffma" in lines[1]
     assert "weights=streamed" in lines[2] and "passes=1" in lines[2]
-    assert "conv3d_min_softmax(min over depth)" in lines[3] and "-> fused ffma" in lines[3]
+    assert "conv3d_min_softmax(min over depth)" in lines[3] and "-> fused igemm_3xtf32" in lines[3]
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=300,
                        env={k: v for k, v in os.environ.items() if k != "CONVFWD_LOG"},
                        cwd=os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
