@@ -333,15 +333,16 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
 // 16 consecutive reduction columns [k0, k0 + 16) of one output position.
 // toff[k]: input offset of column k from the receptive field's origin;
 // ttap[k]: kd | kh << 8 | kw << 16 (bit 31: padding column past Kred).
-// tap4: the reduction runs tap by tap over a channel count that is a
-// multiple of 4, so every aligned group of 4 columns shares one tap (and
-// padding columns come in whole groups).  Otherwise a group can straddle two
-// taps whose in-bounds tests differ, and each column is tested on its own.
+// tg (4, 8 or 16): the reduction runs tap by tap over a channel count that is
+// a multiple of tg, so every aligned group of tg columns shares one tap (and
+// padding columns come in whole groups): one in-bounds test per group.
+// tg = 1: a group of 4 can straddle two taps whose tests differ, and each
+// column is tested on its own.
 // Warps whose receptive fields are all inside the input read four offsets per
 // 16-byte shared load and skip every bounds test; only a unit that reaches the
 // padding columns checks them.
 __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
-                                            int Kred, bool tap4, bool vec4, float (&v)[kUnit]) {
+                                            int Kred, int tg, bool vec4, float (&v)[kUnit]) {
   if (vec4) {
     // channels last, C % 4 == 0: columns 4q .. 4q+3 are 4 consecutive channels
     // of one tap, 16-byte aligned; one test per group, one 16-byte load
@@ -387,15 +388,19 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
         v[4 * q + 3] = k + 3 < Kred ? ldx(ps, o.w) : 0.f;
       }
     }
-  } else if (tap4) {
-    // columns 4q .. 4q+3 of the unit share one tap (and padding columns come
-    // in whole groups, since Kred is then a multiple of 4)
+  } else if (tg >= 4) {
+    // columns 4q .. 4q+3 of the unit share one tap, and so do the groups of
+    // one tg-column block (padding columns come in whole groups, since Kred
+    // is then a multiple of tg): a test where a block starts
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
+    bool in = false;
 #pragma unroll
     for (int q = 0; q < kUnit / 4; ++q) {
-      const uint32_t e = ttap[k0 + 4 * q];
-      const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
-      const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      if (q == 0 || tg == 4 || (q == 2 && tg == 8)) {
+        const uint32_t e = ttap[k0 + 4 * q];
+        const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+        in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      }
       const int4 o = o4[q];
       v[4 * q + 0] = in ? ldx(ps, o.x) : 0.f;
       v[4 * q + 1] = in ? ldx(ps, o.y) : 0.f;
@@ -716,6 +721,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t my_tiles = cta_tile_count<FUSED>(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
+    // columns per in-bounds test of the tested gather: the largest of 16, 8, 4
+    // dividing C_in when the reduction is tap-major (warp-uniform)
+    const int tg = (p.tap_major && g.C % 4 == 0) ? (g.C % 16 == 0 ? 16 : g.C % 8 == 0 ? 8 : 4) : 1;
     // Chunk q of a tile: gather its K columns into registers (loads only).
     auto gather_chunk = [&](const PosInfo &ps, int q, float (&v)[CH]) {
       const int k0 = q * p.KC;
@@ -724,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0 && g.C % 4 == 0, p.vec4 != 0, vu);
+          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, tg, p.vec4 != 0, vu);
         }
       }
     };
