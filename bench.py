@@ -394,21 +394,21 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.595328e6 + 824.158464e6, "batch": 16,
-        "sha256": "324179416dc67af5c600c4a3ee8b0bb300c22cceff185370ec8a5a1d762deb68"},
-    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.338624e6 + 307.428608e6, "batch": 4,
-        "sha256": "324179416dc67af5c600c4a3ee8b0bb300c22cceff185370ec8a5a1d762deb68"},
-    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492032e6 + 0.049664e6, "batch": 8,
-        "sha256": "324179416dc67af5c600c4a3ee8b0bb300c22cceff185370ec8a5a1d762deb68"},
-    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.495040e6 + 66.813440e6, "batch": 8,
-        "sha256": "324179416dc67af5c600c4a3ee8b0bb300c22cceff185370ec8a5a1d762deb68"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.411712e6 + 8.306432e6, "batch": 4,
-        "sha256": "324179416dc67af5c600c4a3ee8b0bb300c22cceff185370ec8a5a1d762deb68"},
-    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.842176e6 + 0.002304e6, "batch": 128,
-        "sha256": "324179416dc67af5c600c4a3ee8b0bb300c22cceff185370ec8a5a1d762deb68"},
-    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.424128e6 + 385.913600e6, "batch": 16,
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.505984e6 + 824.218880e6, "batch": 16,
+        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.284352e6 + 307.303936e6, "batch": 4,
+        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492032e6 + 0.061440e6, "batch": 8,
+        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.433088e6 + 67.331584e6, "batch": 8,
+        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.417344e6 + 8.363776e6, "batch": 4,
+        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.840640e6 + 0.003072e6, "batch": 128,
+        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.294080e6 + 386.062592e6, "batch": 16,
         "sha256": "bccfe6fd7b2f9f38438b9a33cea2bba3534f89fd15e2ac2e8a47ddd9a193d1cc"},
-    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.817344e6 + 0.001792e6, "batch": 128,
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.822464e6 + 0.000768e6, "batch": 128,
         "sha256": "e420278244e71807996932fd3600d956d407ef4d2540cfbed9e6e6f302e5c283"},
     ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051712e6, "batch": 2,
         "sha256": "c89212c4b2a3b47cebf81b80fa94530bb29ddb0f5ed58ae23df0585b90d2ac41"},

@@ -220,32 +220,29 @@ int forced_algo() {
 bool fused_ffma_preferred(const Geom &g, int min_dim) {
   // Measured on GB300 against the tensor-core fused kernel (device time, L2
   // flushed) on [N, C_in, 24, 32, 32] inputs with N * C_in held near 384,
-  // C_out 8 .. 64, C_in 1 .. 8, min over depth, height and width.  The FFMA
-  // kernels run channel groups of 12 (up to 24 channels cost the same, 25..48
-  // cost twice that); the tensor-core kernel runs blocks of 32 channels, a
-  // second block adding a channel-softmax pass.  3x3x3 kernels (FFMA /
-  // tensor cores, ms, over depth; over height and width alike within 10 %):
-  //   C_out <= 24: C_in 1 0.277 / 0.34, C_in 2 0.26 / 0.217, C_in 3 0.199 /
-  //   0.181, C_in 4 0.24 / 0.185, C_in 8 0.32 / 0.188 (over height C_in 3
-  //   0.200 / 0.210, the one other case the FFMA kernel wins);
-  //   C_out = 32: tensor cores from C_in 1 (0.60 / 0.35);
-  //   C_out 40, 48: C_in 1 0.59 / 0.68 over depth and height, 0.77 / 0.72
-  //   over width; C_in >= 2 tensor cores (0.60 / 0.43 at C_in 2);
-  //   C_out = 64: tensor cores from C_in 1 (1.24 / 0.71).
-  //   3x5x5 kernels: tensor cores everywhere (from 0.72x the FFMA time at
-  //   C_in 1, C_out 8).
-  // So the FFMA kernels keep reductions of at most 32 columns on up to 24
-  // channels, and on 25..48 channels (two tensor-core blocks) over depth or
-  // height; and the min over height of the page's shape class (C_in 3, 3x3x3,
-  // W 32, up to 24 channels), where the staged FFMA kernel runs its
-  // compile-time specialised instance.
+  // C_out 8 .. 64, C_in 1 .. 8, 3x3x3 kernels, min over depth / height /
+  // width.  The FFMA kernels run channel groups of 12 (up to 24 channels cost
+  // the same, 25..48 twice that); the tensor-core kernel runs blocks of 32
+  // channels, a second block adding a channel-softmax pass.  FFMA / tensor
+  // cores, ms, over depth:
+  //   C_out <= 24: C_in 1 0.277 / 0.30, C_in 2 0.26 / 0.187, C_in 3 0.198 /
+  //   0.160, C_in 4 0.24 / 0.166, C_in 8 0.32 / 0.176;
+  //   C_out = 32: tensor cores from C_in 1 (0.59 / 0.31);
+  //   C_out 40, 48: C_in 1 0.59 / 0.61; from C_in 2 tensor cores (0.60 / 0.37);
+  //   C_out = 64: tensor cores from C_in 1 (1.22 / 0.64).
+  // Over height the C_in = 1 ratios are 0.98 (C_out <= 24) and 1.09 (40,
+  // 48); over width 0.98 and 0.86; every other point goes to the tensor cores
+  // by a wider margin.  3x5x5 kernels: tensor cores everywhere (from 0.72x the
+  // FFMA time at C_in 1, C_out 8, before the kernel's last two speed-ups).
+  // So the FFMA kernels keep only reductions of at most 32 columns: on up to
+  // 24 channels over depth, on 25..48 channels (two tensor-core blocks) over
+  // depth or height.
   const int64_t kred = g.C * g.taps();
+  if (kred > 32 || min_dim == 4) return false;
   const int ncg = convfwd::fused_channel_groups(g.K);
-  if (min_dim == 3 && ncg <= 2 && g.C == 3 && g.KD == 3 && g.KH == 3 && g.KW == 3 && g.W == 32) return true;
-  if (kred > 32) return false;
-  if (ncg <= 2) return true;
+  if (ncg <= 2) return min_dim == 2;
   const int64_t blocks = (g.K + 31) / 32;  // tensor-core launches
-  return ncg == 4 && blocks == 2 && min_dim != 4;
+  return ncg == 4 && blocks == 2;
 }
 
 // The fused op's family for CONV_ALGO_AUTO: CONVFWD_FORCE_ALGO where that

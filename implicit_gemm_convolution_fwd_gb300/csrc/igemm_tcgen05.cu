@@ -111,13 +111,13 @@ struct IgemmParams {
   // column is ragged but the last); each CTA runs its columns' R tiles along
   // the reduced dim back to back
   int64_t columns;  // ceil(N * plane / 128)
-  // the reduced output dim (depth, height or width): R positions at stride sR
-  // in an image's flat output index; the kept plane (A x nB positions, A at
-  // stride sA, B at stride sB) is what y holds per image and channel
+  // the reduced output axis rdim (0 = depth, 1 = height, 2 = width) has R
+  // positions; the kept plane (the other two axes in order, A x nB
+  // positions) is what y holds per image and channel
   int R;
+  int rdim;
   int64_t plane;
   int nB;
-  int64_t sR, sA, sB;
   int fused_min_only;  // a 32-channel block of a wider layer: write min + bias, no softmax
   // elements addressable from x / w (or wh) / y (or yh) / wsp as this launch
   // receives them: what the debug build's device checks test indices against
@@ -265,11 +265,13 @@ template <bool FUSED = false>
 __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t tile, int t) {
   const Geom &g = p.g;
   PosInfo ps;
-  int64_t m;
+  int64_t m = 0;
+  int64_t n = 0;
+  int od = 0, oh = 0, ow = 0;
   if (FUSED) {
     // tile = column * R + r; row t is entry column * 128 + t of the
     // flattened (image, kept-plane position) index, at index r of the
-    // reduced dim
+    // reduced dim; the output coordinates follow from (r, a, b) directly
     const int64_t col = tile / p.R;
     const int64_t r = tile - col * p.R, flat = col * kTileM + t;
     ps.valid = flat < g.N * p.plane;
@@ -283,14 +285,16 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
         img = flat / p.plane, pp = flat - img * p.plane, a = pp / p.nB, bb = pp - a * p.nB;
       }
     }
-    m = img * p.osp + r * p.sR + a * p.sA + bb * p.sB;
+    // the reduced axis is D, H or W (rdim 0, 1, 2); the kept A and B axes are the other two, in order
+    n = img;
+    od = (int)(p.rdim == 0 ? r : a);
+    oh = (int)(p.rdim == 1 ? r : (p.rdim == 0 ? a : bb));
+    ow = (int)(p.rdim == 2 ? r : bb);
   } else {
     m = tile * kTileM + t;
     ps.valid = m < p.M_total;
   }
-  int64_t n = 0;
-  int od = 0, oh = 0, ow = 0;
-  if (ps.valid) {
+  if (!FUSED && ps.valid) {
     if (p.M_total < ((int64_t)1 << 31)) {  // 32-bit divisions when every index fits
       const uint32_t mm = (uint32_t)m, osp = (uint32_t)p.osp, OHW = (uint32_t)g.OH * (uint32_t)g.OW;
       const uint32_t n32 = mm / osp, pp = mm - n32 * osp;
@@ -311,9 +315,14 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
   }
   const int id0 = od * g.SD - g.PD, ih0 = oh * g.SH - g.PH, iw0 = ow * g.SW - g.PW;
   uint32_t dm = 0, hm = 0, wm = 0;
-  for (int k = 0; k < g.KD; ++k) dm |= (uint32_t)((unsigned)(id0 + k * g.DD) < (unsigned)g.D) << k;
-  for (int k = 0; k < g.KH; ++k) hm |= (uint32_t)((unsigned)(ih0 + k * g.DH) < (unsigned)g.H) << k;
-  for (int k = 0; k < g.KW; ++k) wm |= (uint32_t)((unsigned)(iw0 + k * g.DW) < (unsigned)g.W) << k;
+  if (FUSED) {
+    // stride 1, no padding, no dilation: every tap of a valid position lies inside the input
+    dm = low_bits(g.KD), hm = low_bits(g.KH), wm = low_bits(g.KW);
+  } else {
+    for (int k = 0; k < g.KD; ++k) dm |= (uint32_t)((unsigned)(id0 + k * g.DD) < (unsigned)g.D) << k;
+    for (int k = 0; k < g.KH; ++k) hm |= (uint32_t)((unsigned)(ih0 + k * g.DH) < (unsigned)g.H) << k;
+    for (int k = 0; k < g.KW; ++k) wm |= (uint32_t)((unsigned)(iw0 + k * g.DW) < (unsigned)g.W) << k;
+  }
   ps.dm = dm;
   ps.hm = hm;
   ps.wm = wm;
@@ -1179,6 +1188,10 @@ bool igemm_fused_supported(const Geom &g, int min_dim, const char **why) {
     *why = "tensor-core fused path: channels-last input";
     return false;
   }
+  if (g.SD != 1 || g.SH != 1 || g.SW != 1 || g.PD || g.PH || g.PW || g.DD != 1 || g.DH != 1 || g.DW != 1 || g.G != 1) {
+    *why = "tensor-core fused path: stride 1, no padding, dilation 1 and one group only";
+    return false;
+  }
   // layers wider than 32 channels run in blocks of 32 (the epilogue holds one
   // position's channels in registers), then a channel-softmax pass
   Geom gb = g;
@@ -1239,14 +1252,14 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.g = g;
   p.osp = (int64_t)g.OD * g.OH * g.OW;
   p.M_total = g.N * p.osp;
-  // the reduced dim and the kept plane (A, B in order) in the flat output index d * OH*OW + h * OW + w
-  const int64_t sD = (int64_t)g.OH * g.OW, sH = g.OW, sW = 1;
+  // the reduced axis and the kept plane (the other two axes, in order)
+  p.rdim = min_dim - 2;
   if (min_dim == 2) {
-    p.R = g.OD, p.sR = sD, p.nB = g.OW, p.sA = sH, p.sB = sW, p.plane = (int64_t)g.OH * g.OW;
+    p.R = g.OD, p.nB = g.OW, p.plane = (int64_t)g.OH * g.OW;
   } else if (min_dim == 3) {
-    p.R = g.OH, p.sR = sH, p.nB = g.OW, p.sA = sD, p.sB = sW, p.plane = (int64_t)g.OD * g.OW;
+    p.R = g.OH, p.nB = g.OW, p.plane = (int64_t)g.OD * g.OW;
   } else {
-    p.R = g.OW, p.sR = sW, p.nB = g.OH, p.sA = sD, p.sB = sH, p.plane = (int64_t)g.OD * g.OH;
+    p.R = g.OW, p.nB = g.OH, p.plane = (int64_t)g.OD * g.OH;
   }
   p.columns = (g.N * p.plane + kTileM - 1) / kTileM;
   p.tiles = p.columns * p.R;

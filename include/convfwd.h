@@ -336,9 +336,9 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * their last two dims (a stream-ordered block).  Where both families run, the
  * planner takes the one measured faster for the shape class: the tensor-core
  * kernel, except for the shortest reductions (K = C_in * |kernel| <= 32) on up
- * to 24 channels, or on 25..48 channels over depth or height, which keep the
- * FFMA kernels (conv3d_min_softmax_select_algo reports the choice).  Shapes
- * neither family runs are CONV_ERR_UNSUPPORTED.
+ * to 24 channels over depth, or on 25..48 channels over depth or height, which
+ * keep the FFMA kernels (conv3d_min_softmax_select_algo reports the choice).
+ * Shapes neither family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);

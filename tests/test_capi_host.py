@@ -208,12 +208,12 @@ def test_fused_validation_statuses(lib):
 
 def test_fused_select_algo_host_only(lib):
     sel = cf.fused_select_algo
-    # the page's shape takes the tensor cores over depth and width, the specialised staged FFMA
-    # kernel over height; the shortest reductions keep the FFMA kernels
+    # the page's shape takes the tensor cores; a 27-column reduction on 24 channels keeps the
+    # FFMA kernels over depth
     for md in (2, 3, 4):
-        want = cf.CONV_ALGO_DIRECT_FFMA if md == 3 else cf.CONV_ALGO_IGEMM_3XTF32
-        assert sel((128, 3, 24, 32, 32), (24, 3, 3, 3, 3), md) == want
-        assert sel((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), md) == cf.CONV_ALGO_DIRECT_FFMA
+        assert sel((128, 3, 24, 32, 32), (24, 3, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
+        want = cf.CONV_ALGO_DIRECT_FFMA if md == 2 else cf.CONV_ALGO_IGEMM_3XTF32
+        assert sel((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), md) == want
         assert sel((2, 1, 10, 20, 20), (32, 1, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
         assert sel((2, 1, 10, 20, 20), (64, 1, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
     # 25..48 channels: FFMA over depth and height, tensor cores over width

@@ -323,21 +323,21 @@ def test_fused_planner_takes_the_measured_family():
 
 @pytest.mark.parametrize("min_dim", [3, 4])
 def test_fused_planner_over_height_and_width(min_dim):
-    # the page's shape takes the staged FFMA kernel's specialised instance over height and the
-    # tensor cores over width; a 27-column reduction on 24 channels keeps the FFMA kernels
+    # the page's shape takes the tensor cores over height and width too; a 27-column reduction on
+    # 40 channels keeps the FFMA kernels over height, not over width
     wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
     xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
-    want = FFMA if min_dim == 3 else TC
-    assert cf.fused_select_algo(x.shape, w.shape, min_dim) == want
-    auto, fam = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, want))
-    assert torch.equal(auto, fam)
+    assert cf.fused_select_algo(x.shape, w.shape, min_dim) == TC
+    auto, tc = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, TC))
+    assert torch.equal(auto, tc)
     rng = np.random.default_rng(12)
     x1 = rng.random((2, 1, 10, 20, 20)).astype(np.float32)
-    w1 = ((rng.random((24, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
-    assert cf.fused_select_algo(x1.shape, w1.shape, min_dim) == FFMA
+    w1 = ((rng.random((40, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
+    want = FFMA if min_dim == 3 else TC
+    assert cf.fused_select_algo(x1.shape, w1.shape, min_dim) == want
     xt, wt = torch.from_numpy(x1).cuda(), torch.from_numpy(w1).cuda()
-    auto, ffma = (cf.conv3d_min_softmax(xt, wt, None, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, FFMA))
-    assert torch.equal(auto, ffma)
+    auto, fam = (cf.conv3d_min_softmax(xt, wt, None, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, want))
+    assert torch.equal(auto, fam)
 
 
 @pytest.mark.parametrize("min_dim", [2, 3, 4])
@@ -761,6 +761,42 @@ def test_bf16_exact_on_small_integers():
     ref = oracle.conv_nd(xf, wf, bf, (1, 1, 1), (0, 1, 1), (1, 1, 1))
     assert np.abs(ref).max() < 256
     assert np.array_equal(y, ref)
+
+
+# 16-bit kernel, bit-exact on integer data across kernel widths 4..9 along W:
+# reductions that end a chunk early, a partial last tile (its border warps take
+# the per-column tested gather), streamed weights, channel blocks, strides and
+# dilations along one axis, padding, and fp16.
+WIDE_KW_16BIT_CASES = [
+    # nd, C_in, C_out, k, stride, pad, dilation, in dims, N
+    (3, 3, 64, (3, 5, 7), 1, 0, 1, (6, 9, 40), 2),         # the headline's kernel
+    (3, 5, 24, (2, 3, 5), 1, 0, 1, (5, 8, 23), 3),         # KW 5, partial last tile
+    (3, 2, 40, (1, 2, 6), (1, 1, 2), 0, 1, (3, 7, 41), 2),  # KW 6, stride 2 along W
+    (3, 4, 16, (2, 2, 8), 1, 0, 1, (4, 6, 30), 1),         # KW 8
+    (2, 7, 33, (3, 7), 1, 0, (2, 1), (15, 29), 2),          # 2-D, dilation along H only
+    (1, 9, 20, (7,), 2, 0, 1, (300,), 2),                   # 1-D, stride 2
+    (3, 64, 48, (3, 3, 5), 1, 0, 1, (5, 7, 20), 2),        # 2880 columns: weights stream
+    (3, 4, 160, (1, 3, 7), 1, 0, 1, (3, 8, 25), 2),        # two channel blocks
+    (3, 3, 16, (2, 3, 4), 1, 0, 1, (4, 7, 19), 2),         # KW 4
+    (3, 3, 16, (2, 3, 9), 1, 0, 1, (4, 7, 19), 2),         # KW 9
+    (3, 3, 16, (2, 3, 7), 1, 0, (1, 1, 2), (4, 7, 25), 2),  # dilation along W
+    (3, 3, 16, (2, 3, 7), 1, (0, 1, 3), 1, (4, 7, 19), 2),  # padded
+]
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("nd,C_in,C_out,k,s,p,d,ins,N", WIDE_KW_16BIT_CASES)
+def test_16bit_wide_kernels_exact(nd, C_in, C_out, k, s, p, d, ins, N, dtype):
+    rng = np.random.default_rng(C_in * 131 + C_out * 7 + k[-1])
+    x = rng.integers(0, 2, (N, C_in) + ins).astype(np.float32)
+    w = rng.integers(-1, 2, (C_out, C_in) + k).astype(np.float32)
+    b = rng.integers(-2, 3, C_out).astype(np.float32)
+    (xt, wt, bt), (xf, wf, bf) = bf16_inputs(x, w, b, dtype)
+    ref = oracle.conv_nd(xf, wf, bf, s, p, d)
+    # every output is an integer small enough for the 16-bit type (bf16: 8 significant bits)
+    assert np.abs(ref).max() < 256
+    y = cf.conv_fwd_nd(xt, wt, bt, s, p, d).float().cpu().numpy()
+    assert np.array_equal(y, ref), f"16-bit case nd={nd} C_in={C_in} k={k}: {np.abs(y - ref).max()}"
 
 
 @pytest.mark.parametrize("nd,groups,C_in,C_out,k,s,p,d", [
