@@ -343,6 +343,7 @@ VARIANTS = [
     ("conv3d_asym[bf16]", "conv3d_asym", {"dtype": "bfloat16"}),
     ("conv3d_asym[fp16]", "conv3d_asym", {"dtype": "float16"}),
     ("conv1d_long[bf16]", "conv1d_long", {"dtype": "bfloat16"}),
+    ("conv3d_sweep_b[bf16]", "conv3d_sweep_b", {"dtype": "bfloat16"}),
     ("conv3d_min_softmax[min_dim=3]", "conv3d_min_softmax", {"min_dim": 3}),
     ("conv3d_min_softmax[min_dim=4]", "conv3d_min_softmax", {"min_dim": 4}),
     ("conv3d_min_softmax[ffma]", "conv3d_min_softmax", {"fused_algo": "ffma"}),

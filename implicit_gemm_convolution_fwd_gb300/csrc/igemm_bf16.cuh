@@ -78,7 +78,7 @@ __device__ __forceinline__ uint32_t ldxh(const PosInfo &ps, const uint16_t *xo, 
 // 16 consecutive reduction columns of one output position as bf16 bit
 // patterns (zero-extended to 32 bits); same tables and paths as gather_cols.
 __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16_t *xo, const int32_t *toff,
-                                                 const uint32_t *ttap, int k0, int Kred, bool tap_major,
+                                                 const uint32_t *ttap, int k0, int Kred, int tg,
                                                  uint32_t (&v)[kUnit]) {
   if (ps.warp_full) {
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
@@ -91,13 +91,17 @@ __device__ __forceinline__ void gather_cols_bf16(const PosInfo &ps, const uint16
       v[4 * q + 2] = k + 2 < Kred ? ldxh(ps, xo, o.z) : 0u;
       v[4 * q + 3] = k + 3 < Kred ? ldxh(ps, xo, o.w) : 0u;
     }
-  } else if (tap_major) {
+  } else if (tg >= 4) {
+    // tap-major over C_in a multiple of tg: one test per tg-column block
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
+    bool in = false;
 #pragma unroll
     for (int q = 0; q < kUnit / 4; ++q) {
-      const uint32_t e = ttap[k0 + 4 * q];
-      const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
-      const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      if (q == 0 || tg == 4 || (q == 2 && tg == 8)) {
+        const uint32_t e = ttap[k0 + 4 * q];
+        const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+        in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      }
       const int4 o = o4[q];
       v[4 * q + 0] = in ? ldxh(ps, xo, o.x) : 0u;
       v[4 * q + 1] = in ? ldxh(ps, xo, o.y) : 0u;
@@ -310,6 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const int64_t my_tiles = cta_tile_count(p);
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;
+    // columns per in-bounds test of the tested gather (tap-major: the largest
+    // of 16, 8, 4 dividing C_in; else each column)
+    const int tg = p.tap_major ? (g.C % 16 == 0 ? 16 : g.C % 8 == 0 ? 8 : 4) : 1;
     // streamed weights: the group's thread 0 brings chunk q's B into the stage
     // and remembers its last copy, to wait for it before leaving
     int sb_last_stage = -1;
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
 #pragma unroll
         for (int u = 0; u < kBfChunk / kUnit; ++u) {
           uint32_t v[kUnit];
-          gather_cols_bf16(ps, xo, toff, ttap, k0 + u * kUnit, p.Kred, p.tap_major != 0, v);
+          gather_cols_bf16(ps, xo, toff, ttap, k0 + u * kUnit, p.Kred, tg, v);
 #pragma unroll
           for (int j = 0; j < kUnit / 2; ++j) packed[u * (kUnit / 2) + j] = __byte_perm(v[2 * j], v[2 * j + 1], 0x5410);
         }
