@@ -395,21 +395,21 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.505984e6 + 824.218880e6, "batch": 16,
-        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
-    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.284352e6 + 307.303936e6, "batch": 4,
-        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
-    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.492032e6 + 0.061440e6, "batch": 8,
-        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
-    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.433088e6 + 67.331584e6, "batch": 8,
-        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.417344e6 + 8.363776e6, "batch": 4,
-        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
-    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.840640e6 + 0.003072e6, "batch": 128,
-        "sha256": "c390ecf4e98d6f8cbb8bcf79088319e46867bcc1206f7f34e29b60c546acdb1b"},
-    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.294080e6 + 386.062592e6, "batch": 16,
-        "sha256": "bccfe6fd7b2f9f38438b9a33cea2bba3534f89fd15e2ac2e8a47ddd9a193d1cc"},
-    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.822464e6 + 0.000768e6, "batch": 128,
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.817024e6 + 823.936512e6, "batch": 16,
+        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.320960e6 + 307.175680e6, "batch": 4,
+        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.493056e6 + 0.068864e6, "batch": 8,
+        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.499648e6 + 67.123200e6, "batch": 8,
+        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.418624e6 + 8.438784e6, "batch": 4,
+        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.840896e6 + 0.003584e6, "batch": 128,
+        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.323520e6 + 385.913088e6, "batch": 16,
+        "sha256": "2986faafe4ddbf1021cc4da72daec446b859c65765d5d7c9d147e092a6162ae3"},
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.822464e6 + 0.000256e6, "batch": 128,
         "sha256": "e420278244e71807996932fd3600d956d407ef4d2540cfbed9e6e6f302e5c283"},
     ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051712e6, "batch": 2,
         "sha256": "c89212c4b2a3b47cebf81b80fa94530bb29ddb0f5ed58ae23df0585b90d2ac41"},

@@ -261,11 +261,47 @@ __device__ __forceinline__ float ldx(const PosInfo &ps, int32_t o) {
   return __ldg(ps.xo + o);
 }
 
+// An output position as mixed-radix digits (image, od, oh, ow); n >= N means
+// past the last position.
+struct OutPos {
+  int64_t n;
+  int od, oh, ow;
+};
+
+// The digits of flat output index m (divisions).
+__device__ __forceinline__ OutPos decode_out(const IgemmParams &p, int64_t m) {
+  const Geom &g = p.g;
+  OutPos o;
+  if (m < ((int64_t)1 << 31) && p.osp < ((int64_t)1 << 31)) {  // 32-bit divisions when they fit
+    const uint32_t mm = (uint32_t)m, osp = (uint32_t)p.osp, OHW = (uint32_t)g.OH * (uint32_t)g.OW;
+    const uint32_t n32 = mm / osp, pp = mm - n32 * osp;
+    o.n = n32;
+    o.od = (int)(pp / OHW);
+    const uint32_t rem = pp - (uint32_t)o.od * OHW;
+    o.oh = (int)(rem / (uint32_t)g.OW);
+    o.ow = (int)(rem - (uint32_t)o.oh * (uint32_t)g.OW);
+  } else {
+    const int64_t OHW = (int64_t)g.OH * g.OW;
+    o.n = m / p.osp;
+    const int64_t pp = m - o.n * p.osp;
+    o.od = (int)(pp / OHW);
+    const int rem = (int)(pp - (int64_t)o.od * OHW);
+    o.oh = rem / g.OW;
+    o.ow = rem - o.oh * g.OW;
+  }
+  return o;
+}
+
+template <bool FUSED = false>
+__device__ __forceinline__ PosInfo position_info(const IgemmParams &p, bool valid, int64_t n, int od, int oh,
+                                                 int ow);
+
+// The producer-side description of row t of a tile (FUSED: the tile's column
+// and reduced index; otherwise 128 consecutive flat output positions).
 template <bool FUSED = false>
 __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t tile, int t) {
   const Geom &g = p.g;
-  PosInfo ps;
-  int64_t m = 0;
+  bool valid;
   int64_t n = 0;
   int od = 0, oh = 0, ow = 0;
   if (FUSED) {
@@ -274,9 +310,9 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
     // reduced dim; the output coordinates follow from (r, a, b) directly
     const int64_t col = tile / p.R;
     const int64_t r = tile - col * p.R, flat = col * kTileM + t;
-    ps.valid = flat < g.N * p.plane;
+    valid = flat < g.N * p.plane;
     int64_t img = 0, pp = 0, a = 0, bb = 0;
-    if (ps.valid) {
+    if (valid) {
       if (g.N * p.plane < ((int64_t)1 << 31)) {  // 32-bit divisions when every index fits
         const uint32_t f32 = (uint32_t)flat, pl = (uint32_t)p.plane, nb = (uint32_t)p.nB;
         const uint32_t i32 = f32 / pl, q32 = f32 - i32 * pl, a32 = q32 / nb;
@@ -291,32 +327,26 @@ __device__ __forceinline__ PosInfo decode_position(const IgemmParams &p, int64_t
     oh = (int)(p.rdim == 1 ? r : (p.rdim == 0 ? a : bb));
     ow = (int)(p.rdim == 2 ? r : bb);
   } else {
-    m = tile * kTileM + t;
-    ps.valid = m < p.M_total;
+    const OutPos o = decode_out(p, tile * kTileM + t);
+    valid = o.n < g.N;
+    if (valid) n = o.n, od = o.od, oh = o.oh, ow = o.ow;
   }
-  if (!FUSED && ps.valid) {
-    if (p.M_total < ((int64_t)1 << 31)) {  // 32-bit divisions when every index fits
-      const uint32_t mm = (uint32_t)m, osp = (uint32_t)p.osp, OHW = (uint32_t)g.OH * (uint32_t)g.OW;
-      const uint32_t n32 = mm / osp, pp = mm - n32 * osp;
-      n = n32;
-      od = (int)(pp / OHW);
-      const uint32_t rem = pp - (uint32_t)od * OHW;
-      oh = (int)(rem / (uint32_t)g.OW);
-      ow = (int)(rem - (uint32_t)oh * (uint32_t)g.OW);
-    } else {
-      const int64_t OHW = (int64_t)g.OH * g.OW;
-      n = m / p.osp;
-      const int64_t pp = m - n * p.osp;
-      od = (int)(pp / OHW);
-      const int rem = (int)(pp - (int64_t)od * OHW);
-      oh = rem / g.OW;
-      ow = rem - oh * g.OW;
-    }
-  }
+  return position_info<FUSED>(p, valid, n, od, oh, ow);
+}
+
+// Receptive-field origin, border masks and the warp-wide interior test of
+// output position (n, od, oh, ow); an invalid position reads nothing.
+template <bool FUSED>
+__device__ __forceinline__ PosInfo position_info(const IgemmParams &p, bool valid, int64_t n, int od, int oh,
+                                                 int ow) {
+  const Geom &g = p.g;
+  PosInfo ps;
+  ps.valid = valid;
   const int id0 = od * g.SD - g.PD, ih0 = oh * g.SH - g.PH, iw0 = ow * g.SW - g.PW;
   uint32_t dm = 0, hm = 0, wm = 0;
-  if (FUSED) {
-    // stride 1, no padding, no dilation: every tap of a valid position lies inside the input
+  if (FUSED || (g.PD == 0 && g.PH == 0 && g.PW == 0)) {
+    // no padding: every tap of a valid position lies inside the input (the
+    // output size is the largest for which the last tap of the last position does)
     dm = low_bits(g.KD), hm = low_bits(g.KH), wm = low_bits(g.KW);
   } else {
     for (int k = 0; k < g.KD; ++k) dm |= (uint32_t)((unsigned)(id0 + k * g.DD) < (unsigned)g.D) << k;
@@ -1145,7 +1175,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
                                kNumBars * 8 + 16;
       const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
       const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
-      CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && grid >= 1 && kred > 0);
+        CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && grid >= 1 && kred > 0);
       CONV_PLAN_CHECK(p.Kpad % 32 == 0 && p.nchunks * p.KC >= p.Kpad && p.KC % 16 == 0);
       CONV_PLAN_CHECK(tmem_cols_used(pl.nslots, pl.Npad, pl.KC) <= (int)kTmemCols);
       CONV_PLAN_CHECK(k_begin + kred <= kfull && (o0 + gb.K) <= g.K);
