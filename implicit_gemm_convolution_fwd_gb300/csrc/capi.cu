@@ -217,42 +217,22 @@ int forced_algo() {
   return f;
 }
 
-bool fused_ffma_preferred(const Geom &g, int min_dim) {
-  // Measured on GB300 against the tensor-core fused kernel (device time, L2
-  // flushed) on [N, C_in, 24, 32, 32] inputs with N * C_in held near 384,
-  // C_out 8 .. 64, C_in 1 .. 8, 3x3x3 kernels, min over depth / height /
-  // width.  The FFMA kernels run channel groups of 12 (up to 24 channels cost
-  // the same, 25..48 twice that); the tensor-core kernel runs blocks of 32
-  // channels, a second block adding a channel-softmax pass.  FFMA / tensor
-  // cores, ms, over depth:
-  //   C_out <= 24: C_in 1 0.277 / 0.30, C_in 2 0.26 / 0.187, C_in 3 0.198 /
-  //   0.160, C_in 4 0.24 / 0.166, C_in 8 0.32 / 0.176;
-  //   C_out = 32: tensor cores from C_in 1 (0.59 / 0.31);
-  //   C_out 40, 48: C_in 1 0.59 / 0.61; from C_in 2 tensor cores (0.60 / 0.37);
-  //   C_out = 64: tensor cores from C_in 1 (1.22 / 0.64).
-  // Over height the C_in = 1 ratios are 0.98 (C_out <= 24) and 1.09 (40,
-  // 48); over width 0.98 and 0.86; every other point goes to the tensor cores
-  // by a wider margin.  3x5x5 kernels: tensor cores everywhere (from 0.72x the
-  // FFMA time at C_in 1, C_out 8, before the kernel's last two speed-ups).
-  // So the FFMA kernels keep only reductions of at most 32 columns: on up to
-  // 24 channels over depth, on 25..48 channels (two tensor-core blocks) over
-  // depth or height.
-  const int64_t kred = g.C * g.taps();
-  if (kred > 32 || min_dim == 4) return false;
-  const int ncg = convfwd::fused_channel_groups(g.K);
-  if (ncg <= 2) return min_dim == 2;
-  const int64_t blocks = (g.K + 31) / 32;  // tensor-core launches
-  return ncg == 4 && blocks == 2;
-}
 
 // The fused op's family for CONV_ALGO_AUTO: CONVFWD_FORCE_ALGO where that
-// family runs the shape, else the measured rule (the tensor-core kernel except
-// for the shortest reductions over few channels), else whichever runs.
+// family runs the shape, else the tensor-core kernel wherever it runs, else the
+// FFMA kernels.  Measured on GB300 against the FFMA kernels (device time, L2
+// flushed) on [N, C_in, 24, 32, 32] inputs with N * C_in held near 384, 3x3x3
+// kernels, C_out 8 .. 64, C_in 1 .. 8, min over depth, height and width: the
+// tensor cores took every point, from 0.87x the FFMA time (C_in 1, up to 24
+// channels) to 0.07x (C_in 8, 64 channels); over depth, FFMA / tensor cores
+// in ms: C_out 24 at C_in 1 0.283 / 0.248, C_in 3 (the page's shape) 0.200 /
+// 0.107, C_in 8 0.320 / 0.179; C_out 48 at C_in 1 0.593 / 0.495.
 int fused_family(const Geom &g, int min_dim, bool ffma_ok, bool tc_ok) {
+  (void)g;
+  (void)min_dim;
   const int forced = forced_algo();
   if ((forced == CONV_ALGO_DIRECT_FFMA && ffma_ok) || (forced == CONV_ALGO_IGEMM_3XTF32 && tc_ok)) return forced;
-  return tc_ok && !(ffma_ok && fused_ffma_preferred(g, min_dim)) ? CONV_ALGO_IGEMM_3XTF32
-                                                                          : CONV_ALGO_DIRECT_FFMA;
+  return tc_ok ? CONV_ALGO_IGEMM_3XTF32 : CONV_ALGO_DIRECT_FFMA;
 }
 
 int choose_algo(const Geom &g, bool can_stream) {

@@ -66,9 +66,6 @@ cudaError_t transpose_hw(const float *x, const float *w, float *ws, const Geom &
 // True when launch_fused_min_softmax supports this geometry (channel count,
 // kernel extent along the output's last axis, shared-memory footprint).
 bool fused_supported(const Geom &g, int min_dim, const char **why);
-// Channel groups of 12 the FFMA fused kernels compute for C_out = K (1, 2, 4
-// or 8): their cost grows with it.
-int fused_channel_groups(int64_t K);
 
 // The same fused op on the tensor cores (3xTF32): min over depth, height or
 // width (min_dim 2, 3, 4), weights resident in shared memory or streamed from

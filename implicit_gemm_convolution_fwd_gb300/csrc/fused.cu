@@ -764,7 +764,6 @@ size_t fused_transpose_bytes(const Geom &g, int min_dim) {
   return transpose_x_bytes(g) + transpose_w_bytes(g);
 }
 
-int fused_channel_groups(int64_t K) { return pick_ncg(K); }
 
 cudaError_t launch_fused_min_softmax(const float *x, const float *w, const float *bias, float *y,
                                      const Geom &g, int min_dim, cudaStream_t stream, float *ws) {

@@ -119,6 +119,9 @@ struct IgemmParams {
   int64_t plane;
   int nB;
   int fused_min_only;  // a 32-channel block of a wider layer: write min + bias, no softmax
+  // fused_slab_kernel: slab columns (padded to 16 / real), the kernel extent
+  // along the reduced axis, ring slabs
+  int slab_cols, slab_real, slab_kr, nslabs;
   // elements addressable from x / w (or wh) / y (or yh) / wsp as this launch
   // receives them: what the debug build's device checks test indices against
   int64_t x_elems, w_elems, y_elems, ws_elems;
@@ -417,11 +420,17 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
         v[4 * q + 3] = ldx(ps, o.w);
       }
     } else {
+      // the unit reaching the padding columns: groups of 4 wholly past the
+      // reduction load nothing (a warp-uniform branch)
 #pragma unroll
       for (int q = 0; q < kUnit / 4; ++q) {
-        const int4 o = o4[q];
         const int k = k0 + 4 * q;
-        v[4 * q + 0] = k + 0 < Kred ? ldx(ps, o.x) : 0.f;
+        if (k >= Kred) {
+          v[4 * q + 0] = v[4 * q + 1] = v[4 * q + 2] = v[4 * q + 3] = 0.f;
+          continue;
+        }
+        const int4 o = o4[q];
+        v[4 * q + 0] = ldx(ps, o.x);
         v[4 * q + 1] = k + 1 < Kred ? ldx(ps, o.y) : 0.f;
         v[4 * q + 2] = k + 2 < Kred ? ldx(ps, o.z) : 0.f;
         v[4 * q + 3] = k + 3 < Kred ? ldx(ps, o.w) : 0.f;
@@ -453,6 +462,89 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
       const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
       const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
       v[j] = in ? ldx(ps, toff[k0 + j]) : 0.f;
+    }
+  }
+}
+
+// The fused epilogue (warps 0-3).  Lane tid owns entry column * 128 + tid of
+// the flattened (image, kept-plane position) index; over the column's R tiles
+// along the reduced dim it keeps min_r conv[n, o, r, pos] for each channel
+// o < K <= 32, then adds the bias (min(z + b) = min(z) + b: x -> fl(x + b) is
+// monotone), takes the softmax over o with the maximum subtracted, and writes
+// y[n, o, pos]: a warp store covers 32 consecutive positions of one channel.
+// Tiles rotate over nslots accumulators (tile it in accumulator it % nslots).
+__device__ __forceinline__ void fused_epilogue(const IgemmParams &p, uint32_t tmem, uint32_t bar_d_full,
+                                               uint32_t bar_d_empty, volatile int *abort_flag, const float *bias_s,
+                                               int nslots, int warp, int tid) {
+  const Geom &g = p.g;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const int64_t my_tiles = cta_tile_count<true>(p);
+  const int R = p.R, K = g.K;  // R: the reduced extent (depth, height or width)
+  const int64_t plane = p.plane;
+  float mn[32];
+#pragma unroll
+  for (int j = 0; j < 32; ++j) mn[j] = 0.f;
+  for (int64_t it = 0; it < my_tiles; ++it) {
+    const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
+    const bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit, kWaitSiteDFull);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    ptx::tc_fence_after();
+    const int64_t d = it % R;
+    // the accumulator in two halves of 16 columns (fewer live registers)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      uint32_t v[16];
+      ptx::tmem_ld16(tmem + lane_base + b * p.Npad + 16 * h, v);
+      ptx::tmem_wait_ld();
+      if (d == 0) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mn[16 * h + j] = __uint_as_float(v[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) mn[16 * h + j] = fminf(mn[16 * h + j], __uint_as_float(v[j]));
+      }
+    }
+    ptx::tc_fence_before();
+    ptx::mbar_arrive(bar_d_empty + 8 * b);
+    if (d == R - 1) {
+      const int64_t flat = tile_of<true>(p, it) / R * kTileM + tid;
+      if (flat < g.N * plane) {
+        const int64_t img = flat / plane, pp = flat - img * plane;
+        // y[n, o, pos]; images are y_chans channels apart (all blocks of a wider layer)
+        float *yp = p.y + img * p.y_chans * plane + pp;
+#ifdef CONVFWD_DEBUG
+        {
+          const int64_t i0 = img * p.y_chans * plane + pp;
+          if (!CONV_DBG_OK(i0, p.y_elems, kStatusBoundsY) ||
+              !CONV_DBG_OK(i0 + (int64_t)(K - 1) * plane, p.y_elems, kStatusBoundsY))
+            continue;
+        }
+#endif
+        if (p.fused_min_only) {
+          // one block of a layer wider than 32 channels: the softmax over all
+          // of them runs afterwards as a pass of its own
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < K) yp[(int64_t)j * plane] = mn[j] + bias_s[j];
+        } else {
+          float mx = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            mn[j] += bias_s[j];
+            if (j < K) mx = fmaxf(mx, mn[j]);
+          }
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            mn[j] = j < K ? expf(mn[j] - mx) : 0.f;
+            sum += mn[j];
+          }
+          const float inv = 1.f / sum;
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j < K) __stcs(yp + (int64_t)j * plane, mn[j] * inv);
+        }
+      }
     }
   }
 }
@@ -567,83 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
   const uint32_t a_col0 = (uint32_t)(nslots * p.Npad);
 
   if (FUSED && warp < kEpiWarps) {
-    // ------------------------------------------------------------ fused epilogue
-    // Lane tid owns position hw_tile * 128 + tid of its column's kept plane;
-    // over the column's R tiles along the reduced dim it keeps
-    // min_r conv[n, o, r, pos] for each channel o < K <= 32, then adds the bias (min(z + b) = min(z) + b: x ->
-    // fl(x + b) is monotone), takes the softmax over o with the maximum
-    // subtracted, and writes y[n, o, pos]: a warp store covers 32
-    // consecutive positions of one channel.
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    const int64_t my_tiles = cta_tile_count<true>(p);
-    const int R = p.R, K = g.K;  // R: the reduced extent (depth, height or width)
-    const int64_t plane = p.plane;
-    float mn[32];
-#pragma unroll
-    for (int j = 0; j < 32; ++j) mn[j] = 0.f;
-    for (int64_t it = 0; it < my_tiles; ++it) {
-      const uint32_t b = (uint32_t)(it % nslots), rb = (uint32_t)(it / nslots);
-      const bool ok = wait_phase(bar_d_full + 8 * b, rb & 1, abort_flag, p.wait_limit, kWaitSiteDFull);
-      if (!__all_sync(0xffffffffu, ok)) break;
-      ptx::tc_fence_after();
-      const int64_t d = it % R;
-      // the accumulator in two halves of 16 columns (fewer live registers)
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        uint32_t v[16];
-        ptx::tmem_ld16(tmem + lane_base + b * p.Npad + 16 * h, v);
-        ptx::tmem_wait_ld();
-        if (d == 0) {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) mn[16 * h + j] = __uint_as_float(v[j]);
-        } else {
-#pragma unroll
-          for (int j = 0; j < 16; ++j) mn[16 * h + j] = fminf(mn[16 * h + j], __uint_as_float(v[j]));
-        }
-      }
-      ptx::tc_fence_before();
-      ptx::mbar_arrive(bar_d_empty + 8 * b);
-      if (d == R - 1) {
-        const int64_t flat = tile_of<true>(p, it) / R * kTileM + tid;
-        if (flat < g.N * plane) {
-          const int64_t img = flat / plane, pp = flat - img * plane;
-          // y[n, o, pos]; images are y_chans channels apart (all blocks of a wider layer)
-          float *yp = p.y + img * p.y_chans * plane + pp;
-#ifdef CONVFWD_DEBUG
-          {
-            const int64_t i0 = img * p.y_chans * plane + pp;
-            if (!CONV_DBG_OK(i0, p.y_elems, kStatusBoundsY) ||
-                !CONV_DBG_OK(i0 + (int64_t)(K - 1) * plane, p.y_elems, kStatusBoundsY))
-              continue;
-          }
-#endif
-          if (p.fused_min_only) {
-            // one block of a layer wider than 32 channels: the softmax over all
-            // of them runs afterwards as a pass of its own
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < K) yp[(int64_t)j * plane] = mn[j] + bias_s[j];
-          } else {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              mn[j] += bias_s[j];
-              if (j < K) mx = fmaxf(mx, mn[j]);
-            }
-            float sum = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              mn[j] = j < K ? expf(mn[j] - mx) : 0.f;
-              sum += mn[j];
-            }
-            const float inv = 1.f / sum;
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < K) __stcs(yp + (int64_t)j * plane, mn[j] * inv);
-          }
-        }
-      }
-    }
+    fused_epilogue(p, tmem, bar_d_full, bar_d_empty, abort_flag, bias_s, nslots, warp, tid);
   } else if (warp < kEpiWarps) {
     // ------------------------------------------------------------ epilogue
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
@@ -990,6 +1006,226 @@ __global__ void split_weights_kernel(const float *__restrict__ w, float *__restr
   }
 }
 
+// The fused op with slabs (launched when a slab fits: see fused_slab_plan).
+// Along the reduced axis, tile d of a column reads input planes d .. d + KR - 1
+// (KR: the kernel extent along that axis; stride 1, no padding).  The
+// receptive-field columns one plane contributes, (c, ka, kb) over the other
+// two kernel dims -- a slab -- are the same for the KR tiles that read the
+// plane, so each plane's slab is gathered once into a ring of NS slabs in TMEM
+// and tile d accumulates sum_kr A(slab d + kr) * B_kr, with B_kr the weights
+// at kernel offset kr along the reduced axis (resident in shared memory, split
+// into TF32 hi / lo).  The four producer groups fill slabs round-robin; a
+// slab's ring slot is free again once its KR readers' MMAs have completed
+// (edge planes with fewer readers pre-arrive the missing counts).  The
+// epilogue is the fused one; the MMAs are the 3xTF32 products of the main
+// kernel.
+__global__ void __launch_bounds__(kThreads, 1) fused_slab_kernel(const IgemmParams p) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const Geom &g = p.g;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int Sp = p.slab_cols, Sc = p.slab_real, KR = p.slab_kr, NS = p.nslabs;
+  const int rd = p.rdim;
+  const int KA = rd == 0 ? g.KH : g.KD, KB = rd == 2 ? g.KH : g.KW;
+  const int64_t HW = (int64_t)g.H * g.W, DHW = HW * g.D;
+  // input strides along the reduced axis and the kept A and B axes
+  const int64_t sRin = rd == 0 ? HW : rd == 1 ? (int64_t)g.W : 1;
+  const int64_t sAin = rd == 0 ? (int64_t)g.W : HW;
+  const int64_t sBin = rd == 2 ? (int64_t)g.W : 1;
+  const uint32_t blk_bytes = (uint32_t)(p.Npad * Sp * 4);  // one weight block (hi or lo)
+
+  uint8_t *b_hi = smem;                 // [KR][Npad x Sp] core-matrix layout
+  uint8_t *b_lo = smem + p.b_bytes;     // b_bytes = KR * blk_bytes
+  int32_t *toff = reinterpret_cast<int32_t *>(smem + 2 * (size_t)p.b_bytes);  // [Sp]
+  float *bias_s = reinterpret_cast<float *>(toff + Sp);
+  uint64_t *bars = reinterpret_cast<uint64_t *>((reinterpret_cast<uintptr_t>(bias_s + p.Npad) + 15) & ~(uintptr_t)15);
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + kNumBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const uint32_t bar_s_full = ptx::smem_addr(bars + 0);                           // [NS]
+  const uint32_t bar_s_empty = ptx::smem_addr(bars + kMaxStages);                 // [NS]
+  const uint32_t bar_d_full = ptx::smem_addr(bars + 2 * kMaxStages);              // [slots]
+  const uint32_t bar_d_empty = ptx::smem_addr(bars + 2 * kMaxStages + kMaxSlots);  // [slots]
+  const uint32_t bar_drain = ptx::smem_addr(bars + 3 * kMaxStages + 2 * kMaxSlots);
+  constexpr int nslots = kMaxSlots;
+
+  // ---- weights: block kr, word i -> B[n][k] as in the main kernel (Kpad = Sp)
+  {
+    const int kq = Sp / 4, per_blk = p.Npad * Sp;
+    const int taps = g.KD * g.KH * g.KW;
+    for (int i = tid; i < KR * per_blk; i += kThreads) {
+      const int blk = i / per_blk, e = i - blk * per_blk;
+      const int cm = e >> 5, r = (e >> 2) & 7, cw = e & 3;
+      const int n = (cm / kq) * 8 + r, k = (cm % kq) * 4 + cw;
+      float v = 0.f;
+      if (n < g.K && k < Sc) {
+        const int c = k / (KA * KB), rem = k - c * KA * KB, ka = rem / KB, kb = rem - ka * KB;
+        const int kd = rd == 0 ? blk : ka, kh = rd == 0 ? ka : rd == 1 ? blk : kb, kw = rd == 2 ? blk : kb;
+        const int64_t wi = (int64_t)n * p.Kfull + (int64_t)c * taps + (kd * g.KH + kh) * g.KW + kw;
+        if (CONV_DBG_OK(wi, p.w_elems, kStatusBoundsW)) v = __ldg(p.w + wi);
+      }
+      const float hi = __uint_as_float(tf32_hi_bits(v));
+      reinterpret_cast<float *>(b_hi)[i] = hi;
+      reinterpret_cast<float *>(b_lo)[i] = v - hi;
+    }
+    for (int k = tid; k < Sp; k += kThreads) {
+      int32_t o = 0;
+      if (k < Sc) {
+        const int c = k / (KA * KB), rem = k - c * KA * KB, ka = rem / KB, kb = rem - ka * KB;
+        o = (int32_t)(c * DHW + ka * sAin + kb * sBin);
+      }
+      toff[k] = o;
+    }
+    for (int i = tid; i < p.Npad; i += kThreads) bias_s[i] = (p.bias && i < g.K) ? __ldg(p.bias + i) : 0.f;
+  }
+  ptx::fence_proxy_async_smem();
+  if (warp == kMmaWarp) ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+  if (tid == 0) {
+    for (int s = 0; s < kMaxStages; ++s) {
+      ptx::mbar_init(bar_s_full + 8 * s, 128);
+      ptx::mbar_init(bar_s_empty + 8 * s, (uint32_t)KR);
+    }
+    for (int b = 0; b < kMaxSlots; ++b) {
+      ptx::mbar_init(bar_drain + 8 * b, 1);
+      ptx::mbar_init(bar_d_full + 8 * b, 1);
+      ptx::mbar_init(bar_d_empty + 8 * b, 128);
+    }
+    *abort_flag = 0;
+    ptx::fence_mbar_init();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // TMEM: accumulator b at column b * Npad; slab s at slab_col0 + 2 * Sp * s (hi), + Sp (lo)
+  const uint32_t slab_col0 = (uint32_t)(nslots * p.Npad);
+  const int64_t ncols = (p.columns - blockIdx.x + gridDim.x - 1) / gridDim.x;  // this CTA's columns
+  const int P = p.R + KR - 1;                                                   // input planes per column
+
+  if (warp < kEpiWarps) {
+    fused_epilogue(p, tmem, bar_d_full, bar_d_empty, abort_flag, bias_s, nslots, warp, tid);
+  } else if (warp < kMmaWarp) {
+    // ------------------------------------------------------------ producers
+    const int grp = (warp - kEpiWarps) >> 2;
+    const int t = tid - 32 * kEpiWarps - 128 * grp;  // TMEM lane / row of the tile
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    int64_t cur_j = -1, base = 0;
+    bool valid = false;
+    const int64_t total = ncols * P;
+    for (int64_t sidx = grp; sidx < total; sidx += kProdGroups) {
+      const int64_t j = sidx / P;
+      const int pl = (int)(sidx - j * P);
+      if (j != cur_j) {
+        // row t of column j: entry col * 128 + t of the flattened (image, kept position) index
+        cur_j = j;
+        const int64_t flat = (blockIdx.x + j * (int64_t)gridDim.x) * kTileM + t;
+        valid = flat < g.N * p.plane;
+        const int64_t img = valid ? flat / p.plane : 0, pp = valid ? flat - img * p.plane : 0;
+        const int64_t a = pp / p.nB, bb = pp - a * p.nB;
+        base = img * g.x_batch_stride() + a * sAin + bb * sBin;
+      }
+      const int64_t xoff = base + (int64_t)pl * sRin;
+      const uint32_t s = (uint32_t)(sidx % NS), q = (uint32_t)(sidx / NS);
+      const bool ok = wait_phase(bar_s_empty + 8 * s, (q & 1) ^ 1, abort_flag, p.wait_limit, kWaitSiteAEmpty);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      ptx::tc_fence_after();
+      const uint32_t col = slab_col0 + 2u * (uint32_t)Sp * s;
+      for (int u = 0; u < Sp / kUnit; ++u) {
+        float v[kUnit];
+#pragma unroll
+        for (int jj = 0; jj < kUnit; ++jj) {
+          const int k = u * kUnit + jj;
+          float x = 0.f;
+          if (valid && k < Sc) {
+            const int64_t xi = xoff + toff[k];
+            if (CONV_DBG_OK(xi, p.x_elems, kStatusBoundsX)) x = __ldg(p.x + xi);
+          }
+          v[jj] = x;
+        }
+#pragma unroll
+        for (int h = 0; h < kUnit; h += 8) {
+          uint32_t tmp[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) tmp[jj] = tf32_hi_bits(v[h + jj]);
+          ptx::tmem_st8(tmem + lane_base + col + (uint32_t)(u * kUnit + h), tmp);
+#pragma unroll
+          for (int jj = 0; jj < 8; jj += 2)
+            ptx::sub_f32x2(v[h + jj], v[h + jj + 1], __uint_as_float(tmp[jj]), __uint_as_float(tmp[jj + 1]), v[h + jj],
+                           v[h + jj + 1]);
+          ptx::tmem_st8(tmem + lane_base + col + (uint32_t)(Sp + u * kUnit + h),
+                        *reinterpret_cast<const uint32_t (*)[8]>(v + h));
+        }
+      }
+      ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      ptx::mbar_arrive(bar_s_full + 8 * s);
+      if (t == 0) {
+        // planes near a column's ends have fewer than KR reader tiles:
+        // complete the slot's empty phase for the missing ones
+        const int first = pl - KR + 1 > 0 ? pl - KR + 1 : 0, last = pl < p.R - 1 ? pl : p.R - 1;
+        for (int m = last - first + 1; m < KR; ++m) ptx::mbar_arrive(bar_s_empty + 8 * s);
+      }
+    }
+  } else if (warp >= kMmaWarp && warp - kMmaWarp < nslots) {
+    // ------------------------------------------------------------ MMA issuers
+    // warp b issues tiles it = b, b + nslots, ...: tile (j, d) = (it / R, it % R)
+    // sums the 3xTF32 products of slabs j * P + d + kr with weight blocks kr
+    const int slot = __shfl_sync(0xffffffffu, warp - kMmaWarp, 0);
+    const uint32_t idesc = ptx::idesc_tf32(kTileM, (uint32_t)p.Npad);
+    const uint32_t bhi = ptx::smem_addr(b_hi), blo = ptx::smem_addr(b_lo);
+    const uint32_t d_tmem = tmem + (uint32_t)(slot * p.Npad);
+    const int64_t my_tiles = ncols * p.R;
+    bool aborted = false;
+    for (int64_t it = slot; it < my_tiles && !aborted; it += nslots) {
+      const int64_t li = it / nslots;
+      if (!__all_sync(0xffffffffu, wait_phase(bar_d_empty + 8 * slot, ((uint32_t)li & 1) ^ 1, abort_flag,
+                                                  p.wait_limit, kWaitSiteDEmpty))) break;
+      ptx::tc_fence_after();
+      const int64_t j = it / p.R, d = it - j * p.R;
+      for (int kr = 0; kr < KR; ++kr) {
+        const int64_t sidx = j * P + d + kr;
+        const uint32_t s = (uint32_t)(sidx % NS), q = (uint32_t)(sidx / NS);
+        if (!__all_sync(0xffffffffu, wait_phase(bar_s_full + 8 * s, q & 1, abort_flag, p.wait_limit, kWaitSiteAFull))) {
+          aborted = true;
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t a_hi = tmem + slab_col0 + 2u * (uint32_t)Sp * s;
+        const uint32_t a_lo = a_hi + (uint32_t)Sp;
+        if (ptx::elect_one()) {
+          for (int ks = 0; ks < Sp / 8; ++ks) {
+            const uint64_t dh = ptx::smem_desc_noswizzle(bhi + kr * blk_bytes + 256u * ks, 128, (uint32_t)Sp * 32);
+            const uint64_t dl = ptx::smem_desc_noswizzle(blo + kr * blk_bytes + 256u * ks, 128, (uint32_t)Sp * 32);
+            ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dh, idesc, (kr | ks) != 0);
+            ptx::mma_tf32_ts(d_tmem, a_hi + 8 * ks, dl, idesc, 1);
+            ptx::mma_tf32_ts(d_tmem, a_lo + 8 * ks, dh, idesc, 1);
+          }
+          ptx::mma_commit(bar_s_empty + 8 * s);
+        }
+        __syncwarp();
+      }
+      if (aborted) break;
+      if (ptx::elect_one()) ptx::mma_commit(bar_d_full + 8 * slot);
+      __syncwarp();
+    }
+    if (*abort_flag) {
+      // drain: every MMA this warp issued completes before TMEM is released
+      if (ptx::elect_one()) {
+        ptx::mma_commit(bar_drain + 8 * slot);
+        const long long t0 = clock64();
+        while (!ptx::mbar_try_wait(bar_drain + 8 * slot, 0) && clock64() - t0 < kWaitLimitCycles) {
+        }
+      }
+      __syncwarp();
+    }
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 #include "igemm_bf16.cuh"
 
 int g_num_sms[64] = {0};
@@ -1267,6 +1503,8 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
     e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false, false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kMaxSmem);
     if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(fused_slab_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    if (e == cudaSuccess)
       e = cudaFuncSetAttribute(igemm_3xtf32_kernel<16, false, true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kMaxSmem);
     if (e != cudaSuccess) return e;
@@ -1339,6 +1577,33 @@ cudaError_t launch_igemm_fused_min_softmax(const float *x, const float *w, const
   p.Kred = pl.Kred;
   p.Kpad = pl.Kpad;
   p.nchunks = pl.nchunks;
+  // slabs: each input plane along the reduced axis gathered once (a slab of
+  // C_in x KA x KB columns, padded to 16) and read by the KR tiles that need
+  // it, when a ring of KR + 3 slabs (four tiles in flight) fits in TMEM
+  // beside the four accumulators
+  {
+    const int kr = min_dim == 2 ? g.KD : min_dim == 3 ? g.KH : g.KW;
+    const int ka = min_dim == 2 ? g.KH : g.KD, kb = min_dim == 4 ? g.KH : g.KW;
+    const int64_t sc = g.C * (int64_t)ka * kb;
+    const int sp = (int)((sc + 15) / 16 * 16);
+    int ns = sp > 0 ? (int)((kTmemCols - kMaxSlots * pl.Npad) / (2 * sp)) : 0;
+    if (ns > kMaxStages) ns = kMaxStages;
+    // (the min over width reaches here as a min over height of transposed
+    // copies; read directly, along W, it keeps the chunked kernel)
+    if (min_dim != 4 && sc <= 32 && pl.nslots == kMaxSlots && ns >= kr + kMaxSlots - 1) {
+      p.slab_cols = sp;
+      p.slab_real = (int)sc;
+      p.slab_kr = kr;
+      p.nslabs = ns;
+      p.b_bytes = (uint32_t)((size_t)kr * pl.Npad * sp * 4);
+      const size_t need = 2 * (size_t)p.b_bytes + (size_t)sp * 4 + (size_t)pl.Npad * 4 + 16 + kNumBars * 8 + 16;
+      const size_t smem = need < (size_t)kMinSmem ? (size_t)kMinSmem : need;
+      CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && kMaxSlots * pl.Npad + 2 * sp * ns <= (int)kTmemCols);
+      CONV_PLAN_CHECK(p.R + kr - 1 == (min_dim == 2 ? g.D : min_dim == 3 ? g.H : g.W));
+      fused_slab_kernel<<<(unsigned)grid, kThreads, smem, stream>>>(p);
+      return cudaGetLastError();
+    }
+  }
   p.b_bytes = (uint32_t)((size_t)pl.Npad * pl.Kpad * 4);
   CONV_PLAN_CHECK(pl.smem <= (size_t)kMaxSmem && pl.npasses == 1);
   igemm_3xtf32_kernel<16, false, false, true><<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);

@@ -327,18 +327,18 @@ CONVFWD_API int conv_algo_supported(int ndim, int64_t N, int64_t C_in, int64_t C
  * min_dim outside {2, 3, 4}: CONV_ERR_ARG.  Two kernel families: the FFMA
  * kernels (C_out up to 96, a kernel extent along y's last axis up to 7) and a
  * tensor-core kernel (any C_out, kernel extents up to 32; a 3xTF32 implicit
- * GEMM whose epilogue keeps each
- * position's running minimum over the reduced dim in registers, 32 channels
- * per launch: wider layers run block by block, then one channel-softmax pass
- * over y; weights that exceed shared memory stream through a stream-ordered
- * block of the call, as for conv_fwd_nd).  The min over width runs, in both
+ * GEMM whose epilogue keeps each position's running minimum over the reduced
+ * dim in registers, 32 channels per launch: wider layers run block by block,
+ * then one channel-softmax pass over y; when one input plane's receptive-field
+ * columns along the other two axes number at most 32, each plane is gathered
+ * once and shared by the tiles that read it; weights that exceed shared
+ * memory stream through a stream-ordered block of the call, as for
+ * conv_fwd_nd).  The min over width runs, in both
  * families where they can, as the min over height of x and w transposed in
  * their last two dims (a stream-ordered block).  Where both families run, the
- * planner takes the one measured faster for the shape class: the tensor-core
- * kernel, except for the shortest reductions (K = C_in * |kernel| <= 32) on up
- * to 24 channels over depth, or on 25..48 channels over depth or height, which
- * keep the FFMA kernels (conv3d_min_softmax_select_algo reports the choice).
- * Shapes neither family runs are CONV_ERR_UNSUPPORTED.
+ * planner takes the tensor-core kernel, measured faster on every shape class
+ * tried (conv3d_min_softmax_select_algo reports the choice).  Shapes neither
+ * family runs are CONV_ERR_UNSUPPORTED.
  */
 CONVFWD_API int conv3d_min_softmax(const conv_tensor5_t *x, const conv_tensor5_t *w, const float *bias, conv_tensor4_t *y,
                        int min_dim, conv_stream_t stream);

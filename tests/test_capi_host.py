@@ -208,18 +208,11 @@ def test_fused_validation_statuses(lib):
 
 def test_fused_select_algo_host_only(lib):
     sel = cf.fused_select_algo
-    # the page's shape takes the tensor cores; a 27-column reduction on 24 channels keeps the
-    # FFMA kernels over depth
+    # the tensor cores wherever they run, from the shortest reductions to the widest layers
     for md in (2, 3, 4):
-        assert sel((128, 3, 24, 32, 32), (24, 3, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
-        want = cf.CONV_ALGO_DIRECT_FFMA if md == 2 else cf.CONV_ALGO_IGEMM_3XTF32
-        assert sel((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), md) == want
-        assert sel((2, 1, 10, 20, 20), (32, 1, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
-        assert sel((2, 1, 10, 20, 20), (64, 1, 3, 3, 3), md) == cf.CONV_ALGO_IGEMM_3XTF32
-    # 25..48 channels: FFMA over depth and height, tensor cores over width
-    assert sel((2, 1, 10, 20, 20), (40, 1, 3, 3, 3), 2) == cf.CONV_ALGO_DIRECT_FFMA
-    assert sel((2, 1, 10, 20, 20), (40, 1, 3, 3, 3), 3) == cf.CONV_ALGO_DIRECT_FFMA
-    assert sel((2, 1, 10, 20, 20), (40, 1, 3, 3, 3), 4) == cf.CONV_ALGO_IGEMM_3XTF32
+        for xs, ws in [((128, 3, 24, 32, 32), (24, 3, 3, 3, 3)), ((2, 1, 10, 20, 20), (24, 1, 3, 3, 3)),
+                       ((2, 1, 10, 20, 20), (40, 1, 3, 3, 3)), ((2, 8, 10, 20, 20), (64, 8, 3, 3, 3))]:
+            assert sel(xs, ws, md) == cf.CONV_ALGO_IGEMM_3XTF32, (xs, ws, md)
     # only one family runs: 100 channels (beyond the FFMA kernels), a kernel extent of 9 along W
     assert sel((1, 4, 5, 9, 20), (100, 4, 2, 3, 9), 2) == cf.CONV_ALGO_IGEMM_3XTF32
     # neither family, and invalid requests
@@ -387,8 +380,8 @@ import implicit_gemm_convolution_fwd_gb300 as cf
 head = cf.select_algo(16, 3, 64, (64, 64, 64), (3, 5, 7))       # the planner: tensor cores
 small = cf.select_algo(2, 4, 8, (1024,), (3,), 3, 0, 4)         # the planner: FFMA direct
 fused_tc = cf.fused_select_algo((128, 3, 24, 32, 32), (24, 3, 3, 3, 3), 2)   # the planner: tensor cores
-fused_ffma = cf.fused_select_algo((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), 2)   # the planner: FFMA
-print(head, small, fused_tc, fused_ffma)
+fused_short = cf.fused_select_algo((2, 1, 10, 20, 20), (24, 1, 3, 3, 3), 2)  # the planner: tensor cores
+print(head, small, fused_tc, fused_short)
 """
 
 
@@ -396,10 +389,10 @@ TC_, FF_ = cf.CONV_ALGO_IGEMM_3XTF32, cf.CONV_ALGO_DIRECT_FFMA
 
 
 @pytest.mark.parametrize("value,expect", [
-    ("", (TC_, FF_, TC_, FF_)),
+    ("", (TC_, FF_, TC_, TC_)),
     ("direct_ffma", (FF_, FF_, FF_, FF_)),
     ("igemm_3xtf32", (TC_, TC_, TC_, TC_)),
-    ("bogus", (TC_, FF_, TC_, FF_)),
+    ("bogus", (TC_, FF_, TC_, TC_)),
 ])
 def test_force_algo_environment_variable(lib, value, expect):
     # read once per process, so each setting gets a process of its own

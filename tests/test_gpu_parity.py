@@ -305,39 +305,55 @@ def test_fused_tensor_core_streamed_weights(shape, C_out, k):
     assert torch.equal(cf.conv3d_min_softmax(xt, wt, bt, 2), torch.from_numpy(y).cuda())
 
 
-def test_fused_planner_takes_the_measured_family():
-    """AUTO must equal the family the planner query names, bit for bit: the tensor cores on the
-    page's C_in = 3, C_out = 24 shape (reduced batch), the FFMA kernels for a 27-column reduction
-    on 24 channels (the two families differ in rounding)."""
+# The tensor-core fused kernel gathers each input plane along the reduced axis
+# once when its receptive-field columns (C_in x the other two kernel extents)
+# number at most 32, sharing it among the KR tiles that read it: a single tile
+# per column (R = 1), a kernel extent of 1 and of 5 along the reduced axis
+# (16-column slabs, up to 8 in the ring), exactly 32 and 17 columns, a ragged
+# last column, two channel blocks, and both reduced axes it serves.
+SLAB_CASES = [
+    ((2, 3, 3, 12, 17), 24, (3, 3, 3)),      # R = 1 over depth
+    ((3, 2, 5, 11, 13), 16, (1, 3, 3)),      # KR = 1
+    ((2, 1, 9, 10, 14), 24, (5, 3, 3)),      # KR = 5, 9 columns (16-column slabs)
+    ((2, 2, 6, 9, 12), 32, (2, 4, 4)),       # 32 columns
+    ((2, 17, 6, 8, 9), 8, (3, 1, 1)),        # 17 columns (padded to 32)
+    ((3, 3, 7, 13, 11), 40, (3, 3, 3)),      # two channel blocks, ragged last column
+]
+
+
+@pytest.mark.parametrize("min_dim", [2, 3, 4])
+@pytest.mark.parametrize("shape,C_out,k", SLAB_CASES)
+def test_fused_tensor_core_shared_planes(shape, C_out, k, min_dim):
+    rng = np.random.default_rng(shape[1] * 100 + C_out + k[0])
+    x = rng.standard_normal(shape).astype(np.float32)
+    w = ((rng.random((C_out, shape[1]) + k) - 0.5) * 0.4).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    y = cf.conv3d_min_softmax(torch.from_numpy(x).cuda(), torch.from_numpy(w).cuda(), torch.from_numpy(b).cuda(),
+                              min_dim, algo=TC)
+    assert_close(y.cpu().numpy(), oracle.conv3d_min_softmax(x, w, b, min_dim),
+                 f"shared planes {shape} {C_out} {k} min_dim={min_dim}")
+
+
+@pytest.mark.parametrize("min_dim", [2, 3, 4])
+def test_fused_planner_takes_the_tensor_cores(min_dim):
+    """AUTO equals the tensor-core result bit for bit (the two families differ in rounding):
+    on the page's C_in = 3, C_out = 24 shape (reduced batch, planes gathered once), on a 27-column
+    reduction and on 40 channels over C_in = 8 (two channel blocks, no shared planes)."""
     wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
-    assert cf.fused_select_algo(x.shape, w.shape, 2) == TC
-    auto, ffma, tc = (run_fused(x, w, b, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
-    assert (auto == tc).all() and not (auto == ffma).all()
     rng = np.random.default_rng(11)
-    x = rng.random((2, 1, 10, 20, 20)).astype(np.float32)
-    w = ((rng.random((24, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
-    assert cf.fused_select_algo(x.shape, w.shape, 2) == FFMA
-    auto, ffma, tc = (run_fused(x, w, None, a).cpu().numpy() for a in (cf.CONV_ALGO_AUTO, FFMA, TC))
-    assert (auto == ffma).all() and not (auto == tc).all()
-
-
-@pytest.mark.parametrize("min_dim", [3, 4])
-def test_fused_planner_over_height_and_width(min_dim):
-    # the page's shape takes the tensor cores over height and width too; a 27-column reduction on
-    # 40 channels keeps the FFMA kernels over height, not over width
-    wl, x, w, b = workload_inputs("conv3d_min_softmax", 2)
-    xt, wt, bt = (torch.from_numpy(a).cuda() for a in (x, w, b))
-    assert cf.fused_select_algo(x.shape, w.shape, min_dim) == TC
-    auto, tc = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, TC))
-    assert torch.equal(auto, tc)
-    rng = np.random.default_rng(12)
-    x1 = rng.random((2, 1, 10, 20, 20)).astype(np.float32)
-    w1 = ((rng.random((40, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32)
-    want = FFMA if min_dim == 3 else TC
-    assert cf.fused_select_algo(x1.shape, w1.shape, min_dim) == want
-    xt, wt = torch.from_numpy(x1).cuda(), torch.from_numpy(w1).cuda()
-    auto, fam = (cf.conv3d_min_softmax(xt, wt, None, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, want))
-    assert torch.equal(auto, fam)
+    cases = [(x, w, b),
+             (rng.random((2, 1, 10, 20, 20)).astype(np.float32),
+              ((rng.random((24, 1, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32), None),
+             (rng.random((2, 8, 8, 12, 14)).astype(np.float32),
+              ((rng.random((40, 8, 3, 3, 3)) - 0.5) * 0.2).astype(np.float32), None)]
+    for xc, wc, bc in cases:
+        assert cf.fused_select_algo(xc.shape, wc.shape, min_dim) == TC
+        xt, wt = torch.from_numpy(xc).cuda(), torch.from_numpy(wc).cuda()
+        bt = None if bc is None else torch.from_numpy(bc).cuda()
+        auto, tc, ffma = (cf.conv3d_min_softmax(xt, wt, bt, min_dim, algo=a) for a in (cf.CONV_ALGO_AUTO, TC, FFMA))
+        assert torch.equal(auto, tc) and not torch.equal(auto, ffma)
+        ref = oracle.conv3d_min_softmax(xc, wc, bc, min_dim)
+        assert_close(auto.cpu().numpy(), ref, f"fused AUTO {xc.shape} {wc.shape} min_dim={min_dim}")
 
 
 @pytest.mark.parametrize("min_dim", [2, 3, 4])
