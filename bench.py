@@ -395,22 +395,22 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.817024e6 + 823.936512e6, "batch": 16,
-        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
-    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.320960e6 + 307.175680e6, "batch": 4,
-        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
-    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.493056e6 + 0.068864e6, "batch": 8,
-        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
-    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.499648e6 + 67.123200e6, "batch": 8,
-        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.418624e6 + 8.438784e6, "batch": 4,
-        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
-    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.840896e6 + 0.003584e6, "batch": 128,
-        "sha256": "99e32ef2a38c011af747df6eff64389ee3c70e4a178d902c7f51cbc5678845e2"},
-    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.323520e6 + 385.913088e6, "batch": 16,
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.521344e6 + 824.131840e6, "batch": 16,
+        "sha256": "5c36e0881cfaeecd171eb8f2a764b64eebb8e664a89b6d28741c46b17344fa87"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.366272e6 + 307.061760e6, "batch": 4,
+        "sha256": "5c36e0881cfaeecd171eb8f2a764b64eebb8e664a89b6d28741c46b17344fa87"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.493056e6 + 0.056064e6, "batch": 8,
+        "sha256": "5c36e0881cfaeecd171eb8f2a764b64eebb8e664a89b6d28741c46b17344fa87"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.432832e6 + 66.668288e6, "batch": 8,
+        "sha256": "5c36e0881cfaeecd171eb8f2a764b64eebb8e664a89b6d28741c46b17344fa87"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.436544e6 + 7.951616e6, "batch": 4,
+        "sha256": "5c36e0881cfaeecd171eb8f2a764b64eebb8e664a89b6d28741c46b17344fa87"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.824512e6 + 0.003072e6, "batch": 128,
+        "sha256": "5c36e0881cfaeecd171eb8f2a764b64eebb8e664a89b6d28741c46b17344fa87"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.297920e6 + 385.989632e6, "batch": 16,
         "sha256": "2986faafe4ddbf1021cc4da72daec446b859c65765d5d7c9d147e092a6162ae3"},
-    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.822464e6 + 0.000256e6, "batch": 128,
-        "sha256": "e420278244e71807996932fd3600d956d407ef4d2540cfbed9e6e6f302e5c283"},
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.817600e6 + 0.001536e6, "batch": 128,
+        "sha256": "d7b3eb929d7b9c18018afbc7d515d7c578250c6c7bcdeecece2e78aeb73812eb"},
     ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051712e6, "batch": 2,
         "sha256": "c89212c4b2a3b47cebf81b80fa94530bb29ddb0f5ed58ae23df0585b90d2ac41"},
 }
