@@ -1128,17 +1128,22 @@ __global__ void __launch_bounds__(kThreads, 1) fused_slab_kernel(const IgemmPara
       if (!__all_sync(0xffffffffu, ok)) break;
       ptx::tc_fence_after();
       const uint32_t col = slab_col0 + 2u * (uint32_t)Sp * s;
+      const float *xo = p.x + (valid ? xoff : 0);
       for (int u = 0; u < Sp / kUnit; ++u) {
         float v[kUnit];
+        const int4 *o4 = reinterpret_cast<const int4 *>(toff + u * kUnit);
 #pragma unroll
-        for (int jj = 0; jj < kUnit; ++jj) {
-          const int k = u * kUnit + jj;
-          float x = 0.f;
-          if (valid && k < Sc) {
-            const int64_t xi = xoff + toff[k];
-            if (CONV_DBG_OK(xi, p.x_elems, kStatusBoundsX)) x = __ldg(p.x + xi);
+        for (int q = 0; q < kUnit / 4; ++q) {
+          // four offsets per shared load; columns past the slab (and invalid rows) read nothing
+          const int k = u * kUnit + 4 * q;
+          const int4 o = o4[q];
+          const int oo[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            float x = 0.f;
+            if (valid && k + e < Sc && CONV_DBG_OK(xoff + oo[e], p.x_elems, kStatusBoundsX)) x = __ldg(xo + oo[e]);
+            v[4 * q + e] = x;
           }
-          v[jj] = x;
         }
 #pragma unroll
         for (int h = 0; h < kUnit; h += 8) {
