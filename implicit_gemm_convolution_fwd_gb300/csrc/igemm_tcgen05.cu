@@ -387,12 +387,15 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
                                             int Kred, int tg, bool vec4, float (&v)[kUnit]) {
   if (vec4) {
     // channels last, C % 4 == 0: columns 4q .. 4q+3 are 4 consecutive channels
-    // of one tap, 16-byte aligned; one test per group, one 16-byte load
+    // of one tap, 16-byte aligned; one 16-byte load per group, and one test
+    // per tg-column block of one tap
+    bool in = false;
 #pragma unroll
     for (int q = 0; q < kUnit / 4; ++q) {
       const int k = k0 + 4 * q;
-      bool in = k < Kred;
-      if (!ps.warp_full) {
+      if (ps.warp_full) {
+        in = k < Kred;
+      } else if (q == 0 || tg == 4 || (q == 2 && tg == 8)) {
         const uint32_t e = ttap[k];
         const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
         in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
