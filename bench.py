@@ -102,29 +102,47 @@ def problem_counts(wl, out_dims, esize=4):
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle sampling in the background during the timed region."""
+    """nvidia-smi clocks/throttle sampling in the background during the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    The sampler is started, and its first sample awaited (at most a few seconds),
+    before the timed region begins; mark(start, end) records the region's host
+    times, and summary() takes the median SM clock over the samples stamped
+    inside it (the nearest sample after the region when it was too short to
+    hold one) and every throttle reason seen in or next to it."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    PERIOD_MS = 10
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
+        self.region = None
         self.path = os.path.join("/tmp", f"convfwd_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                          "--format=csv,noheader,nounits", "-lms", str(self.PERIOD_MS)],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return self
+        deadline = time.time() + 5.0
+        while time.time() < deadline and self.proc.poll() is None:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.01)
         return self
+
+    def mark(self, t_start, t_end):
+        self.region = (t_start, t_end)
 
     def __exit__(self, *a):
         if self.proc is not None:
+            time.sleep(3 * self.PERIOD_MS / 1000.0)  # one more sample after the region
             self.proc.terminate()
             try:
                 self.proc.wait(timeout=5)
@@ -132,30 +150,60 @@ class ClockSampler:
                 self.proc.kill()
             self.f.close()
 
-    def summary(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+    @staticmethod
+    def parse(lines):
+        """Rows (host time or None, SM MHz, max SM MHz, [reason fields]) of nvidia-smi's CSV."""
+        import datetime
         rows = []
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            try:
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[5:]))
             except ValueError:
                 continue
+        return rows
+
+    @staticmethod
+    def summarize(rows, region=None):
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        use = rows
+        in_region = None
+        if region is not None and all(r[0] is not None for r in rows):
+            t0, t1 = region
+            inside = [r for r in rows if t0 <= r[0] <= t1]
+            in_region = len(inside)
+            if inside:
+                use = inside
+            else:
+                after = [r for r in rows if r[0] > t1]
+                use = after[:1] or rows[-1:]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = set()
-        for _, _, r in rows:
+        for _, _, _, r in use:
             for nm, v in zip(names, r[1:5]):
                 if v.lower().startswith("active"):
                     reasons.add(nm)
-        mhz = [r[0] for r in rows]
+        mhz = [r[1] for r in use]
         loaded = [m for m in mhz if m > 0.5 * max(mhz)] or mhz
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[1] for r in rows),
-                "reasons": sorted(reasons), "samples": len(rows)}
+        out = {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(r[2] for r in use),
+               "reasons": sorted(reasons), "samples": len(use)}
+        if in_region is not None:
+            out["samples_in_timed_region"] = in_region
+            out["period_ms"] = ClockSampler.PERIOD_MS
+        return out
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        with open(self.path) as f:
+            return self.summarize(self.parse(f), self.region)
 
 
 # --------------------------------------------------------------- our arm
@@ -590,14 +638,16 @@ def main():
         runner = OurRunner(wl, dev, args.fused_algo)
     flops, bytes_alg, in_b, out_b = problem_counts(wl, runner.out_dims, runner.y.element_size())
     # warm-up, then EXACTLY K timed steps bracketed by barrier + synchronize
-    runner.timed(0, args.warmup)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    with ClockSampler(local) as clk:  # live before the warm-up starts
+        runner.timed(0, args.warmup)
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
         t0 = time.perf_counter()
+        h0 = time.time()
         per_step = runner.timed(args.steps, 0)
         torch.cuda.synchronize()
+        clk.mark(h0, time.time())
         wall = time.perf_counter() - t0
     if world > 1:
         dist.barrier()
