@@ -526,9 +526,12 @@ __device__ __forceinline__ void fused_epilogue(const IgemmParams &p, uint32_t tm
         if (p.fused_min_only) {
           // one block of a layer wider than 32 channels: the softmax over all
           // of them runs afterwards as a pass of its own
+          float *q = yp;  // stepped: 32 hoisted 64-bit addresses would spill
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < K) yp[(int64_t)j * plane] = mn[j] + bias_s[j];
+          for (int j = 0; j < 32; ++j) {
+            if (j < K) *q = mn[j] + bias_s[j];
+            q += plane;
+          }
         } else {
           float mx = -INFINITY;
 #pragma unroll
@@ -543,9 +546,12 @@ __device__ __forceinline__ void fused_epilogue(const IgemmParams &p, uint32_t tm
             sum += mn[j];
           }
           const float inv = 1.f / sum;
+          float *q = yp;
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < K) __stcs(yp + (int64_t)j * plane, mn[j] * inv);
+          for (int j = 0; j < 32; ++j) {
+            if (j < K) __stcs(q, mn[j] * inv);
+            q += plane;
+          }
         }
       }
     }
