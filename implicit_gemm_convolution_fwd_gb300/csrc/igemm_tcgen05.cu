@@ -94,6 +94,7 @@ struct IgemmParams {
   int tap_major;    // reduction ordered (tap, c) instead of (c, tap); padded convs with C_in % 4 == 0,
                     // and always for channels-last tensors
   int vec4;         // channels last with 16-byte aligned groups of 4 channels: float4 gathers
+  int vec8;         // ... and 32-byte aligned groups of 8 channels: one 32-byte load per 8 columns
   int vec_store;    // channels last with 16-byte aligned output rows: float4 stores
   uint32_t b_bytes; // Npad * Kpad * 4; with streamed weights the whole B stage region
   // streamed weights: B chunks prepared once (hi then lo, each in the core-matrix
@@ -384,8 +385,32 @@ __device__ __forceinline__ PosInfo position_info(const IgemmParams &p, bool vali
 // 16-byte shared load and skip every bounds test; only a unit that reaches the
 // padding columns checks them.
 __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
-                                            int Kred, int tg, bool vec4, float (&v)[kUnit]) {
-  if (vec4) {
+                                            int Kred, int tg, bool vec4, bool vec8, float (&v)[kUnit]) {
+  if (vec8) {
+    // channels last, C % 8 == 0: columns 8q .. 8q+7 are 8 consecutive channels
+    // of one tap, 32-byte aligned: one 32-byte load per group (half the load
+    // instructions, and L1 tag lookups, of the 16-byte form)
+    bool in = false;
+#pragma unroll
+    for (int q = 0; q < kUnit / 8; ++q) {
+      const int k = k0 + 8 * q;
+      if (ps.warp_full) {
+        in = k < Kred;
+      } else if (q == 0 || tg == 8) {
+        const uint32_t e = ttap[k];
+        const uint32_t kd = e & 0xffu, kh = (e >> 8) & 0xffu, kw = (e >> 16) & 0xffu;
+        in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
+      }
+      float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#ifdef CONVFWD_DEBUG
+      if (in) in = CONV_DBG_OK(ps.xoff + toff[k], ps.xn, kStatusBoundsX) &&
+                   CONV_DBG_OK(ps.xoff + toff[k] + 7, ps.xn, kStatusBoundsX);
+#endif
+      if (in) ptx::ldg_nc_v8(ps.xo + toff[k], a);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[8 * q + j] = a[j];
+    }
+  } else if (vec4) {
     // channels last, C % 4 == 0: columns 4q .. 4q+3 are 4 consecutive channels
     // of one tap, 16-byte aligned; one 16-byte load per group, and one test
     // per tg-column block of one tap
@@ -796,7 +821,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, tg, p.vec4 != 0, vu);
+          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, tg, p.vec4 != 0, p.vec8 != 0, vu);
         }
       }
     };
@@ -1366,6 +1391,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     p.nslots = pl.nslots;
     p.tap_major = pl.tap_major;
     p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
+    p.vec8 = (p.vec4 && g.C % 8 == 0 && (g.G * g.C) % 8 == 0 && ((uintptr_t)x & 31u) == 0) ? 1 : 0;
     p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)y & 15u) == 0) ? 1 : 0;
     p.wsp = ws;
     p.sb_stage_bytes = (uint32_t)(2 * pl.Npad * pl.KC * 4);
@@ -1378,6 +1404,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     const size_t smem = smem_need < (size_t)kMinSmem ? (size_t)kMinSmem : smem_need;
     const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
     CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && p.sb_stage_bytes % 16 == 0 && grid >= 1);
+    CONV_PLAN_CHECK(!p.vec8 || (((uintptr_t)x & 31u) == 0 && p.tap_major && kfull % 8 == 0));
     auto kern = pl.KC <= 16 ? igemm_3xtf32_kernel<16, false, true> : igemm_3xtf32_kernel<32, false, true>;
     kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
@@ -1416,6 +1443,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       p.nslots = pl.nslots;
       p.tap_major = pl.tap_major;
       p.vec4 = (g.cl && g.C % 4 == 0 && (g.G * g.C) % 4 == 0 && ((uintptr_t)x & 15u) == 0) ? 1 : 0;
+      p.vec8 = (p.vec4 && g.C % 8 == 0 && (g.G * g.C) % 8 == 0 && ((uintptr_t)x & 31u) == 0) ? 1 : 0;
       p.vec_store = (g.cl && (g.G * g.K) % 4 == 0 && ((uintptr_t)p.y & 15u) == 0) ? 1 : 0;
       p.b_bytes = (uint32_t)((size_t)pl.Npad * p.Kpad * 4);
       p.x_elems = x_extent(g);
@@ -1430,6 +1458,7 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       CONV_PLAN_CHECK(tmem_cols_used(pl.nslots, pl.Npad, pl.KC) <= (int)kTmemCols);
       CONV_PLAN_CHECK(k_begin + kred <= kfull && (o0 + gb.K) <= g.K);
       CONV_PLAN_CHECK(!p.vec4 || ((uintptr_t)x & 15u) == 0);
+      CONV_PLAN_CHECK(!p.vec8 || (((uintptr_t)x & 31u) == 0 && p.tap_major && k_begin % 8 == 0 && kred % 8 == 0));
       auto kern = pl.KC <= 16 ? (pass ? igemm_3xtf32_kernel<16, true, false> : igemm_3xtf32_kernel<16, false, false>)
                               : (pass ? igemm_3xtf32_kernel<32, true, false> : igemm_3xtf32_kernel<32, false, false>);
       kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);

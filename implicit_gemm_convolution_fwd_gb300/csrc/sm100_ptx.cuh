@@ -244,6 +244,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "memory");
 }
 
+// 32 bytes (8 floats) from read-only global memory in one load; p 32-byte aligned.
+__device__ __forceinline__ void ldg_nc_v8(const float *p, float (&a)[8]) {
+  asm("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=f"(a[0]), "=f"(a[1]), "=f"(a[2]), "=f"(a[3]), "=f"(a[4]), "=f"(a[5]), "=f"(a[6]), "=f"(a[7])
+      : "l"(p));
+}
+
 // (a0 - b0, a1 - b1) with one packed f32x2 instruction, round to nearest.
 __device__ __forceinline__ void sub_f32x2(float a0, float a1, float b0, float b1, float &d0, float &d1) {
   asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"

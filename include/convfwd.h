@@ -168,9 +168,10 @@ CONVFWD_API int conv_fwd_nd_grouped(const float *x, const float *w, const float 
  *   x [N, in_dims..., C_in]   w [C_out, k_dims..., C_in/groups]   y [N, out_dims..., C_out]
  *   bias [C_out] or NULL.  Everything else as conv_fwd_nd_grouped.
  * The reduction runs tap by tap with the channels innermost, so with
- * C_in/groups % 4 == 0 and 16-byte aligned x each gather is one 16-byte load
- * of 4 channels, and each output position's channels are written as one
- * contiguous run.  Only the tensor-core family runs this layout: algo must be
+ * C_in/groups % 8 == 0 and 32-byte aligned x each gather is one 32-byte load
+ * of 8 channels (with % 4 and 16-byte alignment, one 16-byte load of 4;
+ * otherwise one load per value), and each output position's channels are
+ * written as one contiguous run.  Only the tensor-core family runs this layout: algo must be
  * CONV_ALGO_AUTO or CONV_ALGO_IGEMM_3XTF32; CONV_ALGO_DIRECT_FFMA and shapes
  * the tensor-core path does not take return CONV_ERR_UNSUPPORTED.
  */

@@ -671,6 +671,29 @@ def test_channels_last_conv(nd, groups, C_in, C_out, k, s, p, d, N):
     assert_close(y.cpu().numpy(), ref, f"channels last nd={nd} C_in={C_in} C_out={C_out} G={groups}")
 
 
+@pytest.mark.parametrize("offset", [0, 4, 2, 1])
+def test_channels_last_input_alignment(offset):
+    """x starting 0, 16, 8 or 4 bytes past a 32-byte boundary: 32-byte channel
+    groups, 16-byte groups, or scalar gathers; the same values either way."""
+    rng = np.random.default_rng(71 + offset)
+    N, C_in, C_out, ins, k = 2, 16, 32, (6, 9, 11), (3, 3, 3)
+    x = rng.standard_normal((N, C_in) + ins).astype(np.float32)
+    w = ((rng.random((C_out, C_in) + k) - 0.5) * 0.3).astype(np.float32)
+    b = rng.standard_normal(C_out).astype(np.float32)
+    ref = oracle.conv_nd(x, w, b, 1, 1, 1)
+    xcl = np.ascontiguousarray(np.moveaxis(x, 1, -1)).ravel()
+    buf = torch.zeros(xcl.size + 8, dtype=torch.float32, device="cuda")
+    assert buf.data_ptr() % 32 == 0
+    buf[offset:offset + xcl.size] = torch.from_numpy(xcl).cuda()
+    sp = ins[0] * ins[1] * ins[2]
+    xt = torch.as_strided(buf, (N, C_in) + ins, (sp * C_in, 1, ins[1] * ins[2] * C_in, ins[2] * C_in, C_in),
+                          storage_offset=offset)
+    assert xt.data_ptr() % 32 == offset * 4
+    y = cf.conv_fwd_nd(xt, to_channels_last(w), torch.from_numpy(b).cuda(), 1, 1, 1, channels_last=True)
+    torch.cuda.synchronize()
+    assert_close(y.cpu().numpy(), ref, f"channels last, x offset {offset * 4} bytes")
+
+
 def test_channels_last_rejects_direct_family():
     x = to_channels_last(np.zeros((1, 4, 9), np.float32))
     w = to_channels_last(np.zeros((8, 4, 3), np.float32))
