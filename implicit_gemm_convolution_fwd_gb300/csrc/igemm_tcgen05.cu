@@ -95,6 +95,7 @@ struct IgemmParams {
                     // and always for channels-last tensors
   int vec4;         // channels last with 16-byte aligned groups of 4 channels: float4 gathers
   int vec8;         // ... and 32-byte aligned groups of 8 channels: one 32-byte load per 8 columns
+                    // (the host picks the kernel instance with that gather form: VEC 1 / 2)
   int vec_store;    // channels last with 16-byte aligned output rows: float4 stores
   uint32_t b_bytes; // Npad * Kpad * 4; with streamed weights the whole B stage region
   // streamed weights: B chunks prepared once (hi then lo, each in the core-matrix
@@ -384,9 +385,14 @@ __device__ __forceinline__ PosInfo position_info(const IgemmParams &p, bool vali
 // Warps whose receptive fields are all inside the input read four offsets per
 // 16-byte shared load and skip every bounds test; only a unit that reaches the
 // padding columns checks them.
+// VEC (compile time: each form is its own kernel instance, so that the
+// N C D H W gather is compiled without the channels-last forms): 2 = 32-byte
+// loads of 8 channels, 1 = 16-byte loads of 4 (channels last), 0 = one load
+// per value (any layout).
+template <int VEC>
 __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *toff, const uint32_t *ttap, int k0,
-                                            int Kred, int tg, bool vec4, bool vec8, float (&v)[kUnit]) {
-  if (vec8) {
+                                            int Kred, int tg, float (&v)[kUnit]) {
+  if constexpr (VEC == 2) {
     // channels last, C % 8 == 0: columns 8q .. 8q+7 are 8 consecutive channels
     // of one tap, 32-byte aligned: one 32-byte load per group (half the load
     // instructions, and L1 tag lookups, of the 16-byte form)
@@ -410,7 +416,7 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[8 * q + j] = a[j];
     }
-  } else if (vec4) {
+  } else if constexpr (VEC == 1) {
     // channels last, C % 4 == 0: columns 4q .. 4q+3 are 4 consecutive channels
     // of one tap, 16-byte aligned; one 16-byte load per group, and one test
     // per tg-column block of one tap
@@ -436,7 +442,8 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
       v[4 * q + 2] = a.z;
       v[4 * q + 3] = a.w;
     }
-  } else if (ps.warp_full) {
+  } else {
+  if (ps.warp_full) {
     const int4 *o4 = reinterpret_cast<const int4 *>(toff + k0);
     if (k0 + kUnit <= Kred) {
 #pragma unroll
@@ -491,6 +498,7 @@ __device__ __forceinline__ void gather_cols(const PosInfo &ps, const int32_t *to
       const bool in = ps.valid && !(e >> 31) && (((ps.dm >> kd) & (ps.hm >> kh) & (ps.wm >> kw)) & 1u);
       v[j] = in ? ldx(ps, toff[k0 + j]) : 0.f;
     }
+  }
   }
 }
 
@@ -592,7 +600,7 @@ __device__ __forceinline__ void fused_epilogue(const IgemmParams &p, uint32_t tm
 // depth tiles of a column consecutive, and an epilogue that keeps each
 // position's running minimum over depth in registers and writes only the
 // softmax of the last one.
-template <int CH, bool ACC, bool SB, bool FUSED = false>
+template <int CH, bool ACC, bool SB, bool FUSED = false, int VEC = 0>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
@@ -821,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
       for (int u = 0; u < CH / kUnit; ++u) {
         if (u * kUnit < ncols) {
           float (&vu)[kUnit] = *reinterpret_cast<float (*)[kUnit]>(v + u * kUnit);
-          gather_cols(ps, toff, ttap, k0 + u * kUnit, p.Kred, tg, p.vec4 != 0, p.vec8 != 0, vu);
+          gather_cols<VEC>(ps, toff, ttap, k0 + u * kUnit, p.Kred, tg, vu);
         }
       }
     };
@@ -892,7 +900,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
         v[4 * i + 3] = ldx(ps, o.w);
       }
     };
-    const int nfull = (p.KC == CH && !p.vec4) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
+    const int nfull = (p.KC == CH && VEC == 0) ? p.Kred / CH : 0;  // chunks entirely inside the reduction
     bool aborted = false;
     for (int64_t li = 0; li < slot_tiles && !aborted; ++li) {
       const PosInfo ps = decode_position<FUSED>(p, tile_of<FUSED>(p, li * nslots + slot), t);
@@ -1341,7 +1349,15 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
                            (const void *)igemm_3xtf32_kernel<16, true, false>,
                            (const void *)igemm_3xtf32_kernel<32, true, false>,
                            (const void *)igemm_3xtf32_kernel<16, false, true>,
-                           (const void *)igemm_3xtf32_kernel<32, false, true>};
+                           (const void *)igemm_3xtf32_kernel<32, false, true>,
+                           (const void *)igemm_3xtf32_kernel<16, false, false, false, 1>,
+                           (const void *)igemm_3xtf32_kernel<32, false, false, false, 1>,
+                           (const void *)igemm_3xtf32_kernel<16, false, true, false, 1>,
+                           (const void *)igemm_3xtf32_kernel<32, false, true, false, 1>,
+                           (const void *)igemm_3xtf32_kernel<16, false, false, false, 2>,
+                           (const void *)igemm_3xtf32_kernel<32, false, false, false, 2>,
+                           (const void *)igemm_3xtf32_kernel<16, false, true, false, 2>,
+                           (const void *)igemm_3xtf32_kernel<32, false, true, false, 2>};
     for (const void *k : kerns) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
       if (e != cudaSuccess) return e;
@@ -1405,7 +1421,13 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
     CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && p.sb_stage_bytes % 16 == 0 && grid >= 1);
     CONV_PLAN_CHECK(!p.vec8 || (((uintptr_t)x & 31u) == 0 && p.tap_major && kfull % 8 == 0));
-    auto kern = pl.KC <= 16 ? igemm_3xtf32_kernel<16, false, true> : igemm_3xtf32_kernel<32, false, true>;
+    const int vec = p.vec8 ? 2 : p.vec4 ? 1 : 0;
+    auto kern = pl.KC <= 16 ? (vec == 2   ? igemm_3xtf32_kernel<16, false, true, false, 2>
+                               : vec == 1 ? igemm_3xtf32_kernel<16, false, true, false, 1>
+                                          : igemm_3xtf32_kernel<16, false, true>)
+                            : (vec == 2   ? igemm_3xtf32_kernel<32, false, true, false, 2>
+                               : vec == 1 ? igemm_3xtf32_kernel<32, false, true, false, 1>
+                                          : igemm_3xtf32_kernel<32, false, true>);
     kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
   }
@@ -1459,8 +1481,18 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       CONV_PLAN_CHECK(k_begin + kred <= kfull && (o0 + gb.K) <= g.K);
       CONV_PLAN_CHECK(!p.vec4 || ((uintptr_t)x & 15u) == 0);
       CONV_PLAN_CHECK(!p.vec8 || (((uintptr_t)x & 31u) == 0 && p.tap_major && k_begin % 8 == 0 && kred % 8 == 0));
-      auto kern = pl.KC <= 16 ? (pass ? igemm_3xtf32_kernel<16, true, false> : igemm_3xtf32_kernel<16, false, false>)
-                              : (pass ? igemm_3xtf32_kernel<32, true, false> : igemm_3xtf32_kernel<32, false, false>);
+      // the vector gathers serve single-pass launches; reduction passes
+      // (rare: weights beyond shared memory without a streaming block) take
+      // the per-value gather, which serves any layout
+      const int vec = pl.npasses != 1 ? 0 : p.vec8 ? 2 : p.vec4 ? 1 : 0;
+      auto kern = pl.KC <= 16 ? (pass         ? igemm_3xtf32_kernel<16, true, false>
+                                 : vec == 2 ? igemm_3xtf32_kernel<16, false, false, false, 2>
+                                 : vec == 1 ? igemm_3xtf32_kernel<16, false, false, false, 1>
+                                            : igemm_3xtf32_kernel<16, false, false>)
+                              : (pass         ? igemm_3xtf32_kernel<32, true, false>
+                                 : vec == 2 ? igemm_3xtf32_kernel<32, false, false, false, 2>
+                                 : vec == 1 ? igemm_3xtf32_kernel<32, false, false, false, 1>
+                                            : igemm_3xtf32_kernel<32, false, false>);
       kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
