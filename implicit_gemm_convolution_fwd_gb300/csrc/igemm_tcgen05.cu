@@ -246,6 +246,14 @@ __device__ __forceinline__ uint32_t tf32_hi_bits(float v) { return __float_as_ui
 // The n lowest bits set, 0 <= n <= 32 (a kernel extent of 32 taps fills the word).
 __device__ __forceinline__ uint32_t low_bits(int n) { return n >= 32 ? 0xffffffffu : (1u << n) - 1u; }
 
+// Columns per in-bounds test of the tested gather: with a tap-major
+// reduction over a channel count that is a multiple of 4, the largest of 16,
+// 8, 4 dividing C_in (every aligned block of that many columns shares a tap);
+// else 1.  The host picks the kernel instance with the same value.
+__host__ __device__ __forceinline__ int test_group_cols(int tap_major, int C) {
+  return (tap_major && C % 4 == 0) ? (C % 16 == 0 ? 16 : C % 8 == 0 ? 8 : 4) : 1;
+}
+
 // One producer thread's output position within a tile.
 struct PosInfo {
   const float *xo;      // x at the receptive field's origin (may lie in the padding)
@@ -599,11 +607,20 @@ __device__ __forceinline__ void fused_epilogue(const IgemmParams &p, uint32_t tm
 // (turns 1-2): a tile is 128 (image, plane position) pairs at one depth, the
 // depth tiles of a column consecutive, and an epilogue that keeps each
 // position's running minimum over depth in registers and writes only the
-// softmax of the last one.
-template <int CH, bool ACC, bool SB, bool FUSED = false, int VEC = 0>
+// softmax of the last one.  VEC: the gather form (see gather_cols).  TG: the
+// columns per in-bounds test fixed at compile time (0: read at run time).
+template <int CH, bool ACC, bool SB, bool FUSED = false, int VEC = 0, int TG = 0>
 __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
+  if constexpr (TG != 0) {
+    // an instance compiled for another test group does no work and reports
+    // like a kernel that gave up (the host never launches one)
+    if (TG != test_group_cols(p.tap_major, g.C)) {
+      if (threadIdx.x == 0) atomicOr(&g_device_status, kStatusIgemmWatchdog);
+      return;
+    }
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   uint8_t *b_hi = smem;              // resident weights: hi [Npad x Kpad]; streamed: the B stages
@@ -820,7 +837,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_3xtf32_kernel(const IgemmPa
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;  // it = slot, slot + nslots, ...
     // columns per in-bounds test of the tested gather: the largest of 16, 8, 4
     // dividing C_in when the reduction is tap-major (warp-uniform)
-    const int tg = (p.tap_major && g.C % 4 == 0) ? (g.C % 16 == 0 ? 16 : g.C % 8 == 0 ? 8 : 4) : 1;
+    const int tg = TG != 0 ? TG : test_group_cols(p.tap_major, g.C);  // compile time where TG is given
     // Chunk q of a tile: gather its K columns into registers (loads only).
     auto gather_chunk = [&](const PosInfo &ps, int q, float (&v)[CH]) {
       const int k0 = q * p.KC;
@@ -1275,6 +1292,26 @@ __global__ void __launch_bounds__(kThreads, 1) fused_slab_kernel(const IgemmPara
 
 #include "igemm_bf16.cuh"
 
+// The plain-convolution kernel instance for a launch: a later reduction pass
+// (per-value gather, run-time test group), else by gather form (vec 2 / 1)
+// and, for the per-value form, by test group (16 / 8 / 4 compiled in; 1 and
+// the streamed weights' 8 and 4 read at run time).
+using IgemmKern = void (*)(const IgemmParams);
+template <int CH, bool SB>
+IgemmKern pick_plain(bool acc, int vec, int tg) {
+  if constexpr (!SB) {
+    if (acc) return igemm_3xtf32_kernel<CH, true, false>;
+  }
+  if (vec == 2) return igemm_3xtf32_kernel<CH, false, SB, false, 2>;
+  if (vec == 1) return igemm_3xtf32_kernel<CH, false, SB, false, 1>;
+  if (tg == 16) return igemm_3xtf32_kernel<CH, false, SB, false, 0, 16>;
+  if constexpr (!SB) {
+    if (tg == 8) return igemm_3xtf32_kernel<CH, false, false, false, 0, 8>;
+    if (tg == 4) return igemm_3xtf32_kernel<CH, false, false, false, 0, 4>;
+  }
+  return igemm_3xtf32_kernel<CH, false, SB>;
+}
+
 int g_num_sms[64] = {0};
 // the pipeline waits' limit for the next launches (set_wait_limit)
 std::atomic<long long> g_wait_limit{kWaitLimitCycles};
@@ -1344,20 +1381,26 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     if (e != cudaSuccess) return e;
   }
   if (!g_attr_set[dev]) {
-    const void *kerns[] = {(const void *)igemm_3xtf32_kernel<16, false, false>,
-                           (const void *)igemm_3xtf32_kernel<32, false, false>,
-                           (const void *)igemm_3xtf32_kernel<16, true, false>,
-                           (const void *)igemm_3xtf32_kernel<32, true, false>,
-                           (const void *)igemm_3xtf32_kernel<16, false, true>,
-                           (const void *)igemm_3xtf32_kernel<32, false, true>,
-                           (const void *)igemm_3xtf32_kernel<16, false, false, false, 1>,
-                           (const void *)igemm_3xtf32_kernel<32, false, false, false, 1>,
-                           (const void *)igemm_3xtf32_kernel<16, false, true, false, 1>,
-                           (const void *)igemm_3xtf32_kernel<32, false, true, false, 1>,
-                           (const void *)igemm_3xtf32_kernel<16, false, false, false, 2>,
-                           (const void *)igemm_3xtf32_kernel<32, false, false, false, 2>,
-                           (const void *)igemm_3xtf32_kernel<16, false, true, false, 2>,
-                           (const void *)igemm_3xtf32_kernel<32, false, true, false, 2>};
+    const void *kerns[] = {
+        (const void *)igemm_3xtf32_kernel<16, false, false>, (const void *)igemm_3xtf32_kernel<32, false, false>,
+        (const void *)igemm_3xtf32_kernel<16, true, false>, (const void *)igemm_3xtf32_kernel<32, true, false>,
+        (const void *)igemm_3xtf32_kernel<16, false, true>, (const void *)igemm_3xtf32_kernel<32, false, true>,
+        (const void *)igemm_3xtf32_kernel<16, false, false, false, 1>,
+        (const void *)igemm_3xtf32_kernel<32, false, false, false, 1>,
+        (const void *)igemm_3xtf32_kernel<16, false, true, false, 1>,
+        (const void *)igemm_3xtf32_kernel<32, false, true, false, 1>,
+        (const void *)igemm_3xtf32_kernel<16, false, false, false, 2>,
+        (const void *)igemm_3xtf32_kernel<32, false, false, false, 2>,
+        (const void *)igemm_3xtf32_kernel<16, false, true, false, 2>,
+        (const void *)igemm_3xtf32_kernel<32, false, true, false, 2>,
+        (const void *)igemm_3xtf32_kernel<16, false, false, false, 0, 16>,
+        (const void *)igemm_3xtf32_kernel<32, false, false, false, 0, 16>,
+        (const void *)igemm_3xtf32_kernel<16, false, true, false, 0, 16>,
+        (const void *)igemm_3xtf32_kernel<32, false, true, false, 0, 16>,
+        (const void *)igemm_3xtf32_kernel<16, false, false, false, 0, 8>,
+        (const void *)igemm_3xtf32_kernel<32, false, false, false, 0, 8>,
+        (const void *)igemm_3xtf32_kernel<16, false, false, false, 0, 4>,
+        (const void *)igemm_3xtf32_kernel<32, false, false, false, 0, 4>};
     for (const void *k : kerns) {
       e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
       if (e != cudaSuccess) return e;
@@ -1422,12 +1465,8 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
     CONV_PLAN_CHECK(smem <= (size_t)kMaxSmem && p.sb_stage_bytes % 16 == 0 && grid >= 1);
     CONV_PLAN_CHECK(!p.vec8 || (((uintptr_t)x & 31u) == 0 && p.tap_major && kfull % 8 == 0));
     const int vec = p.vec8 ? 2 : p.vec4 ? 1 : 0;
-    auto kern = pl.KC <= 16 ? (vec == 2   ? igemm_3xtf32_kernel<16, false, true, false, 2>
-                               : vec == 1 ? igemm_3xtf32_kernel<16, false, true, false, 1>
-                                          : igemm_3xtf32_kernel<16, false, true>)
-                            : (vec == 2   ? igemm_3xtf32_kernel<32, false, true, false, 2>
-                               : vec == 1 ? igemm_3xtf32_kernel<32, false, true, false, 1>
-                                          : igemm_3xtf32_kernel<32, false, true>);
+    const int tg = test_group_cols(p.tap_major, g.C);
+    const IgemmKern kern = pl.KC <= 16 ? pick_plain<16, true>(false, vec, tg) : pick_plain<32, true>(false, vec, tg);
     kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
     return cudaGetLastError();
   }
@@ -1485,14 +1524,9 @@ cudaError_t launch_igemm_3xtf32(const float *x, const float *w, const float *bia
       // (rare: weights beyond shared memory without a streaming block) take
       // the per-value gather, which serves any layout
       const int vec = pl.npasses != 1 ? 0 : p.vec8 ? 2 : p.vec4 ? 1 : 0;
-      auto kern = pl.KC <= 16 ? (pass         ? igemm_3xtf32_kernel<16, true, false>
-                                 : vec == 2 ? igemm_3xtf32_kernel<16, false, false, false, 2>
-                                 : vec == 1 ? igemm_3xtf32_kernel<16, false, false, false, 1>
-                                            : igemm_3xtf32_kernel<16, false, false>)
-                              : (pass         ? igemm_3xtf32_kernel<32, true, false>
-                                 : vec == 2 ? igemm_3xtf32_kernel<32, false, false, false, 2>
-                                 : vec == 1 ? igemm_3xtf32_kernel<32, false, false, false, 1>
-                                            : igemm_3xtf32_kernel<32, false, false>);
+      const int tg = pl.npasses != 1 ? 0 : test_group_cols(p.tap_major, g.C);
+      const IgemmKern kern =
+          pl.KC <= 16 ? pick_plain<16, false>(pass > 0, vec, tg) : pick_plain<32, false>(pass > 0, vec, tg);
       kern<<<(unsigned)grid, kThreads, smem, stream>>>(p);
       e = cudaGetLastError();
       if (e != cudaSuccess) return e;
