@@ -160,10 +160,20 @@ __global__ void split_weights_bf16_kernel(const uint16_t *__restrict__ w, uint16
 
 // HALF = false: bfloat16 tensors; true: float16 tensors (A and B always of one type).
 // SB: streamed weights (p.wsp: the prepared chunks, p.sb_stage_bytes each).
-template <bool HALF, bool SB>
+// TG: the tested gather's columns per in-bounds test fixed at compile time
+// (0: read at run time), as in the 32-bit kernel.
+template <bool HALF, bool SB, int TG = 0>
 __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmParams p) {
   extern __shared__ __align__(1024) uint8_t smem[];
   const Geom &g = p.g;
+  if constexpr (TG != 0) {
+    // an instance compiled for another test group does no work and reports
+    // like a kernel that gave up (the host never launches one)
+    if (TG != test_group_cols(p.tap_major, g.C)) {
+      if (threadIdx.x == 0) atomicOr(&g_device_status, kStatusIgemmWatchdog);
+      return;
+    }
+  }
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   uint8_t *b_s = smem;  // resident weights, or (SB) one B stage per A stage
@@ -316,7 +326,7 @@ __global__ void __launch_bounds__(kThreads, 1) igemm_bf16_kernel(const IgemmPara
     const int64_t slot_tiles = (my_tiles - slot + nslots - 1) / nslots;
     // columns per in-bounds test of the tested gather (tap-major: the largest
     // of 16, 8, 4 dividing C_in; else each column)
-    const int tg = p.tap_major ? (g.C % 16 == 0 ? 16 : g.C % 8 == 0 ? 8 : 4) : 1;
+    const int tg = TG != 0 ? TG : test_group_cols(p.tap_major, g.C);  // compile time where TG is given
     // streamed weights: the group's thread 0 brings chunk q's B into the stage
     // and remembers its last copy, to wait for it before leaving
     int sb_last_stage = -1;

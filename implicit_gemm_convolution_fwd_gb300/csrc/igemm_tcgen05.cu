@@ -1747,12 +1747,17 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
   }
   bool &attr_set = fp16 ? g_attr_f16_set[dev] : g_attr_bf16_set[dev];
   if (!attr_set) {
-    e = cudaFuncSetAttribute(fp16 ? igemm_bf16_kernel<true, false> : igemm_bf16_kernel<false, false>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(fp16 ? igemm_bf16_kernel<true, true> : igemm_bf16_kernel<false, true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-    if (e != cudaSuccess) return e;
+    const void *kerns[2][5] = {
+        {(const void *)igemm_bf16_kernel<false, false>, (const void *)igemm_bf16_kernel<false, true>,
+         (const void *)igemm_bf16_kernel<false, false, 16>, (const void *)igemm_bf16_kernel<false, false, 8>,
+         (const void *)igemm_bf16_kernel<false, false, 4>},
+        {(const void *)igemm_bf16_kernel<true, false>, (const void *)igemm_bf16_kernel<true, true>,
+         (const void *)igemm_bf16_kernel<true, false, 16>, (const void *)igemm_bf16_kernel<true, false, 8>,
+         (const void *)igemm_bf16_kernel<true, false, 4>}};
+    for (const void *k : kerns[fp16 ? 1 : 0]) {
+      e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+      if (e != cudaSuccess) return e;
+    }
     attr_set = true;
   }
   const int64_t osp = (int64_t)g.OD * g.OH * g.OW;
@@ -1809,8 +1814,17 @@ cudaError_t launch_igemm_bf16(const uint16_t *x, const uint16_t *w, const uint16
     const int64_t grid = p.tiles < g_num_sms[dev] ? p.tiles : g_num_sms[dev];
     CONV_PLAN_CHECK(pl.smem <= (size_t)kMaxSmem && grid >= 1 && pl.Kred == kfull && !g.cl);
     CONV_PLAN_CHECK(pl.nchunks * kBfChunk >= pl.Kpad && pl.nslots * pl.Npad + pl.nslots * 2 * 16 <= (int)kTmemCols);
-    auto kern = fp16 ? (pl.streamed ? igemm_bf16_kernel<true, true> : igemm_bf16_kernel<true, false>)
-                     : (pl.streamed ? igemm_bf16_kernel<false, true> : igemm_bf16_kernel<false, false>);
+    // resident weights: the instance with the test group compiled in (16 / 8 / 4)
+    const int tg = pl.streamed ? 0 : test_group_cols(p.tap_major, g.C);
+    auto pick = [&](auto half) -> IgemmKern {
+      constexpr bool H = decltype(half)::value;
+      if (pl.streamed) return igemm_bf16_kernel<H, true>;
+      if (tg == 16) return igemm_bf16_kernel<H, false, 16>;
+      if (tg == 8) return igemm_bf16_kernel<H, false, 8>;
+      if (tg == 4) return igemm_bf16_kernel<H, false, 4>;
+      return igemm_bf16_kernel<H, false>;
+    };
+    const IgemmKern kern = fp16 ? pick(std::true_type{}) : pick(std::false_type{});
     kern<<<(unsigned)grid, kThreads, pl.smem, stream>>>(p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
