@@ -443,21 +443,21 @@ KERNEL_SOURCE = {"igemm_3xtf32": "igemm_tcgen05.cu", "igemm_3xtf32_streamed": "i
                  "igemm_bf16": "igemm_bf16.cuh", "igemm_fp16": "igemm_bf16.cuh", "direct_ffma": "direct.cu",
                  "fused_ffma": "fused.cu"}
 NCU_TRAFFIC = {
-    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.519296e6 + 824.144640e6, "batch": 16,
-        "sha256": "3de519b8324967288321aa9c27f663cbe23b7c1ed6a3056623936cfa1cb3bb27"},
-    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.348096e6 + 307.693056e6, "batch": 4,
-        "sha256": "3de519b8324967288321aa9c27f663cbe23b7c1ed6a3056623936cfa1cb3bb27"},
-    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.494336e6 + 0.073472e6, "batch": 8,
-        "sha256": "3de519b8324967288321aa9c27f663cbe23b7c1ed6a3056623936cfa1cb3bb27"},
-    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.572608e6 + 67.233792e6, "batch": 8,
-        "sha256": "3de519b8324967288321aa9c27f663cbe23b7c1ed6a3056623936cfa1cb3bb27"},
-    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.418880e6 + 8.559872e6, "batch": 4,
-        "sha256": "3de519b8324967288321aa9c27f663cbe23b7c1ed6a3056623936cfa1cb3bb27"},
-    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.828352e6 + 0.001792e6, "batch": 128,
-        "sha256": "3de519b8324967288321aa9c27f663cbe23b7c1ed6a3056623936cfa1cb3bb27"},
-    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.303552e6 + 386.575360e6, "batch": 16,
-        "sha256": "2986faafe4ddbf1021cc4da72daec446b859c65765d5d7c9d147e092a6162ae3"},
-    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.822208e6 + 0.001280e6, "batch": 128,
+    ("igemm_3xtf32", "conv3d_asym"): {"bytes": 50.554624e6 + 824.594176e6, "batch": 16,
+        "sha256": "25bb5b03715d2abeff46c02a42be790bb2d90d37c91bec4844a831ee1180ead4"},
+    ("igemm_3xtf32", "conv1d_long"): {"bytes": 537.302272e6 + 307.885056e6, "batch": 4,
+        "sha256": "25bb5b03715d2abeff46c02a42be790bb2d90d37c91bec4844a831ee1180ead4"},
+    ("igemm_3xtf32", "conv3d_sweep_a"): {"bytes": 28.485888e6 + 0.098816e6, "batch": 8,
+        "sha256": "25bb5b03715d2abeff46c02a42be790bb2d90d37c91bec4844a831ee1180ead4"},
+    ("igemm_3xtf32", "conv3d_sweep_b"): {"bytes": 113.475328e6 + 69.095936e6, "batch": 8,
+        "sha256": "25bb5b03715d2abeff46c02a42be790bb2d90d37c91bec4844a831ee1180ead4"},
+    ("igemm_3xtf32_streamed", "conv3d_wide_k"): {"bytes": 35.432704e6 + 8.658944e6, "batch": 4,
+        "sha256": "25bb5b03715d2abeff46c02a42be790bb2d90d37c91bec4844a831ee1180ead4"},
+    ("fused_igemm_3xtf32", "conv3d_min_softmax"): {"bytes": 37.823488e6 + 0.006656e6, "batch": 128,
+        "sha256": "25bb5b03715d2abeff46c02a42be790bb2d90d37c91bec4844a831ee1180ead4"},
+    ("igemm_bf16", "conv3d_asym"): {"bytes": 25.515776e6 + 386.445568e6, "batch": 16,
+        "sha256": "f3b938ade490fd2bf7935b687e4595f796a923254b86fe6c215db4fb9b533691"},
+    ("fused_ffma", "conv3d_min_softmax"): {"bytes": 37.817344e6 + 0.003328e6, "batch": 128,
         "sha256": "d7b3eb929d7b9c18018afbc7d515d7c578250c6c7bcdeecece2e78aeb73812eb"},
     ("direct_ffma", "conv1d_tiny"): {"bytes": 0.051712e6, "batch": 2,
         "sha256": "c89212c4b2a3b47cebf81b80fa94530bb29ddb0f5ed58ae23df0585b90d2ac41"},
