@@ -504,7 +504,9 @@ def roofline_for(runner, peaks, pipes, ms):
     best = max(pipes["ffma"]["tflops"], pipes["tf32x3"]["tflops"])
     t_best = max(flops / (best * 1e12), t_mem)
     frac_best = t_best / t
-    common = {"traffic": traffic_for(runner.algo, wl), "algorithmic_bytes": bytes_alg, "frac_best_path": frac_best,
+    # the table's captures are of N C D H W launches; a channels-last run has none
+    traffic = None if getattr(runner, "channels_last", False) else traffic_for(runner.algo, wl)
+    common = {"traffic": traffic, "algorithmic_bytes": bytes_alg, "frac_best_path": frac_best,
               "peak_source": pipes["source"], "peak_mhz": pipes["tf32"]["scaled_to_mhz"]}
     if t_mem > t_compute:
         return dict(common, bound="hbm", achieved=bytes_alg / t / 1e9, peak=hbm_peak, unit="GB/s",
@@ -602,6 +604,8 @@ def main():
                     help="run the workload on 16-bit tensors (the 16-bit tensor-core entry points)")
     ap.add_argument("--fused-algo", choices=["auto", "ffma", "tc"], default="auto",
                     help="kernel family of a fused workload (auto: the library's planner)")
+    ap.add_argument("--channels-last", action="store_true",
+                    help="x, w and y stored channels last (conv_fwd_nd_channels_last); a profiling aid")
     ap.add_argument("--workspace", action="store_true",
                     help="run the workload through conv_fwd_nd_ws (streamed weights when they exceed shared memory)")
     args = ap.parse_args()
@@ -627,9 +631,9 @@ def main():
     sm_max_mhz = float(peaks.get("sm_max_mhz") or SM_MAX_MHZ_NOMINAL)
     pipes = measure_pipe_peaks(cf, sm_max_mhz)  # before the timed region
 
-    if args.dtype != "f32" or args.workspace:
+    if args.dtype != "f32" or args.workspace or args.channels_last:
         dt = {"f32": None, "bf16": torch.bfloat16, "fp16": torch.float16}[args.dtype]
-        runner = VariantRunner(wl, dev, dtype=dt, workspace=args.workspace)
+        runner = VariantRunner(wl, dev, dtype=dt, workspace=args.workspace, channels_last=args.channels_last)
         if dt is not None:
             runner.algo = "igemm_" + args.dtype
         elif runner.ws is not None and runner.ws_stream > 0:
@@ -712,6 +716,7 @@ def main():
                        "in_dims": list(wl.in_dims), "k_dims": list(wl.k_dims), "C_in": wl.C_in, "C_out": wl.C_out,
                        "stride": list(wl.stride), "pad": list(wl.pad), "dilation": list(wl.dilation),
                        "bias": wl.bias, "parallelism": f"replicas{world}",
+                       "layout": "channels last" if args.channels_last else "N C (D) (H) W",
                        "l2": "flushed before every step (2x L2 write, outside the per-step events)",
                        "kernel": runner.algo, "gflop_per_step": flops / 1e9, "bytes_per_step": bytes_alg,
                        "gbs": bytes_alg / (ms * 1e-3) / 1e9, "ms_min": min(per_step),
