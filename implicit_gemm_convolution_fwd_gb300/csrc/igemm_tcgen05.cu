@@ -1361,7 +1361,10 @@ size_t igemm_stream_bytes_one_group(const Geom &g) {
   if (g.K > kMaxNpad) return 0;
   Plan pl;
   const char *why = "";
-  if (!make_plan(g, &pl, &why) || pl.npasses <= 1) return 0;
+  // channels-last layers stream their weights even when they would fit:
+  // the freed shared memory becomes L1 for the gather, which re-reads each
+  // tap's channel line (sweep b 0.564 -> 0.527 ms)
+  if (!make_plan(g, &pl, &why) || (pl.npasses <= 1 && !g.cl)) return 0;
   const int64_t kfull = g.C * (int64_t)g.taps();
   const int64_t kpad = (kfull + 31) / 32 * 32;
   const size_t smem = (size_t)pl.nslots * 2 * 2 * pl.Npad * pl.KC * 4 + (size_t)kpad * 8 + (size_t)pl.Npad * 4 +

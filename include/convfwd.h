@@ -173,7 +173,11 @@ CONVFWD_API int conv_fwd_nd_grouped(const float *x, const float *w, const float 
  * otherwise one load per value), and each output position's channels are
  * written as one contiguous run.  Only the tensor-core family runs this layout: algo must be
  * CONV_ALGO_AUTO or CONV_ALGO_IGEMM_3XTF32; CONV_ALGO_DIRECT_FFMA and shapes
- * the tensor-core path does not take return CONV_ERR_UNSUPPORTED.
+ * the tensor-core path does not take return CONV_ERR_UNSUPPORTED.  The weights
+ * always stream through the kernel from a stream-ordered block of the call
+ * (released on `stream`), which leaves the shared memory they would occupy to
+ * the L1 that the gather re-reads; if that block cannot be had, they are held
+ * in shared memory as in the other calls.
  */
 CONVFWD_API int conv_fwd_nd_channels_last(const float *x, const float *w, const float *bias, float *y, int ndim,
                                           int64_t N, int64_t C_in, int64_t C_out, int64_t groups,
